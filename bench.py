@@ -1,0 +1,498 @@
+"""Benchmark of the replay hot path on the 2,097,152-position workload.
+
+One step = capture of the prompt K/V into pages (P = 2,097,152, Hkv = 4, 256-token
+pages) + serial replay of G = 8 members (R = 4096, Hq = 24): per member the replay
+attention forward, the GRPO loss / logits gradient (V = 151,936 bf16) and the replay
+attention backward with dQ/dK/dV accumulated across members.  Inputs are synthetic,
+seeded, resident in HBM before the timed region (except for the e2e figure, which
+copies them in from pinned host memory every step).
+
+Prints one JSON line.  value = algorithmic replay-attention fwd+bwd FLOPs of the step
+/ step time (TFLOP/s); components add prompt-KV GB/s and GRPO tokens/s.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "replay attn fwd+bwd TFLOP/s & prompt-KV GB/s at P=2.1M; GRPO loss tokens/s"
+WORKLOAD = "p2m"
+D = 128
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ------------------------------------------------------------------ work accounting
+
+def attn_flops(P: int, R: int, hq: int) -> tuple[float, float]:
+    """Algorithmic FLOPs of one member's forward and backward (exact counts: the
+    prompt part is dense R x P, the response part is the causal triangle)."""
+    tri = R * (R + 1) / 2
+    fwd = 4.0 * hq * D * (R * P + tri)
+    bwd = hq * D * (6.0 * R * P + 10.0 * tri)
+    return fwd, bwd
+
+
+def prompt_kv_bytes(P: int, hkv: int) -> float:
+    return float(P) * hkv * D * 2 * 2          # K and V, bf16
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def traffic_from_profile(kernel_file: str, kernel: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, or None when
+    the summary is missing or was taken on a different version of the kernel source."""
+    prof = os.path.join(ROOT, "profiles", f"{kernel}_{WORKLOAD}.md")
+    try:
+        with open(prof) as f:
+            txt = f.read()
+        with open(os.path.join(ROOT, "response_replay_gb300", "csrc", kernel_file), "rb") as f:
+            h = hashlib.sha256(f.read()).hexdigest()[:16]
+    except OSError:
+        return None
+    m = re.search(r"source_sha256_16:\s*([0-9a-f]{16})", txt)
+    t = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", txt)
+    if not m or not t or m.group(1) != h:
+        return None
+    return float(t.group(1))
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines: list[str] = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.t.join(timeout=2)
+
+    def summary(self) -> dict:
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        sm.sort()
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ our arm
+
+def run_ours(args, rank: int, world: int, local_rank: int):
+    import numpy as np
+    import torch
+
+    from response_replay_gb300 import synthetic as syn
+    from response_replay_gb300 import torch_api as api
+    from response_replay_gb300 import binding as B
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    w = syn.WORKLOADS[WORKLOAD]
+    G = w.G if args.members is None else args.members
+    R = w.R[0]
+    seed = syn.seed_of(WORKLOAD) + 1000 * rank
+    scale = D ** -0.5
+    stream = torch.cuda.current_stream()
+
+    # ---- resident inputs
+    pr = syn.make_prompt(w.P, w.hkv, D, w.page_size, seed, dev)
+    cache = api.PagedKVCache(pr.num_pages, pr.page_table, w.page_size, w.hkv, w.P, device=dev)
+    branches = [syn.make_branch(R, w.hq, w.hkv, D, seed + 1 + i, dev) for i in range(G)]
+    lens = list(w.R[:G])
+    gin = syn.make_grpo(lens, w.vocab, w.logits_dtype, w.rewards, seed, dev, shift_frac=w.shift_frac)
+    T = sum(lens)
+    off = [0]
+    for n in lens:
+        off.append(off[-1] + n)
+    # logp_old = logp + noise: logp from one untimed call of the library itself
+    logp = torch.empty(T, dtype=torch.float32, device=dev)
+    zero = torch.zeros(T, dtype=torch.float32, device=dev)
+    for i in range(G):
+        api.grpo_loss_fwd_bwd(gin.logits[off[i]:off[i + 1]], gin.targets[off[i]:off[i + 1]],
+                              zero[off[i]:off[i + 1]], gin.rewards, gin.resp_lens, i, i + 1, 0.2,
+                              logp_out=logp[off[i]:off[i + 1]],
+                              dlogits=torch.empty_like(gin.logits[off[i]:off[i + 1]]))
+    logp_old = (logp + gin.noise).contiguous()
+    del zero
+    o = torch.empty((R, w.hq, D), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((R, w.hq), dtype=torch.float32, device=dev)
+    dq = torch.zeros((R, w.hq, D), dtype=torch.float32, device=dev)
+    dk = torch.zeros((R, w.hkv, D), dtype=torch.float32, device=dev)
+    dv = torch.zeros((R, w.hkv, D), dtype=torch.float32, device=dev)
+    dlog = torch.empty((R, w.vocab), dtype=gin.logits.dtype, device=dev)
+    loss = torch.zeros(1, dtype=torch.float32, device=dev)
+    stats = torch.empty(4, dtype=torch.float32, device=dev)
+    lp_out = torch.empty(T, dtype=torch.float32, device=dev)
+
+    def ev():
+        e = torch.cuda.Event(enable_timing=True)
+        e.record(stream)
+        return e
+
+    def step(marks=None):
+        m = [ev()] if marks is not None else None
+        cache.capture(pr.k, pr.v, 0, stream)
+        if m is not None:
+            m.append(ev())
+        for i in range(G):
+            br = branches[i]
+            api.replay_fwd(cache, br.q, br.k, br.v, scale, w.num_splits, o=o, lse=lse, stream=stream)
+            if m is not None:
+                m.append(ev())
+            s, e = off[i], off[i + 1]
+            api.grpo_loss_fwd_bwd(gin.logits[s:e], gin.targets[s:e], logp_old[s:e], gin.rewards,
+                                  gin.resp_lens, i, i + 1, 0.2, loss=loss, accumulate=i > 0,
+                                  dlogits=dlog[: e - s], logp_out=lp_out[s:e], stats=stats,
+                                  stream=stream)
+            if m is not None:
+                m.append(ev())
+            api.replay_bwd(cache, br.q, br.k, br.v, o, lse, br.d_o, scale, w.num_splits, dq=dq,
+                           dk=dk, dv=dv, accumulate=i > 0, stream=stream)
+            if m is not None:
+                m.append(ev())
+        return m
+
+    # kernel launches of one step (CUPTI via the torch profiler; 0 if unavailable)
+    launches = None
+    try:
+        from torch.profiler import ProfilerActivity, profile
+        with profile(activities=[ProfilerActivity.CUDA]) as prof:
+            step()
+            torch.cuda.synchronize()
+        names = [e.name for e in prof.events() if getattr(e, "device_type", None) is not None
+                 and str(e.device_type).endswith("CUDA")]
+        ours = [n for n in names if any(k in n for k in ("replay", "capture_kv", "grpo", "bwd_"))]
+        launches = len(ours) if ours else None
+    except Exception:
+        launches = None
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+
+    # ---- timed region (device-resident inputs)
+    marks_all = []
+    with ClockSampler(local_rank) as clk:
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        t0 = ev()
+        for _ in range(args.steps):
+            marks_all.append(step(marks=True))
+        t1 = ev()
+        torch.cuda.synchronize()
+    total_ms = t0.elapsed_time(t1)
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    assert B.ls_last_device_error(0) == B.LS_OK
+    assert torch.isfinite(loss).all() and torch.isfinite(dq).all()
+
+    cap_ms = fwd_ms = grpo_ms = bwd_ms = 0.0
+    for m in marks_all:
+        cap_ms += m[0].elapsed_time(m[1])
+        for i in range(G):
+            a = 1 + 3 * i
+            fwd_ms += m[a].elapsed_time(m[a + 1])
+            grpo_ms += m[a + 1].elapsed_time(m[a + 2])
+            bwd_ms += m[a + 2].elapsed_time(m[a + 3])
+    K = args.steps
+    f_fwd, f_bwd = attn_flops(w.P, R, w.hq)
+    step_flops = G * (f_fwd + f_bwd)
+    ms_per_step = total_ms / K
+    value = step_flops * world / (ms_per_step * 1e-3) / 1e12
+    kv_bytes = prompt_kv_bytes(w.P, w.hkv)
+    comps = {
+        "attn_fwd_tflops": G * K * f_fwd / (fwd_ms * 1e-3) / 1e12,
+        "attn_bwd_tflops": G * K * f_bwd / (bwd_ms * 1e-3) / 1e12,
+        "prompt_kv_gbs": 2 * G * K * kv_bytes / ((fwd_ms + bwd_ms) * 1e-3) / 1e9,
+        "grpo_tokens_per_s": T * K / (grpo_ms * 1e-3),
+        "capture_gbs": 2 * kv_bytes * K / (cap_ms * 1e-3) / 1e9,
+        "ms_capture": cap_ms / K, "ms_fwd_per_member": fwd_ms / (K * G),
+        "ms_grpo_per_member": grpo_ms / (K * G), "ms_bwd_per_member": bwd_ms / (K * G),
+    }
+    pk, pk_src = peaks()
+    peak = pk.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
+    # dominant launch: the larger of the per-member backward and forward calls
+    if bwd_ms >= fwd_ms:
+        dom, dom_flops, dom_ms, kfile, kname = "replay_attn_bwd", f_bwd, bwd_ms / (K * G), \
+            "replay_bwd.cu", "bwd_dq_kernel"
+    else:
+        dom, dom_flops, dom_ms, kfile, kname = "replay_attn_fwd", f_fwd, fwd_ms / (K * G), \
+            "replay_fwd.cu", "replay_fwd_kernel"
+    achieved = dom_flops / (dom_ms * 1e-3) / 1e12
+    roofline = {"bound": "tensor", "kernel": kname, "timed": f"{dom} call (CUDA events)",
+                "achieved": achieved, "peak": peak, "peak_source": f"{pk_src} bf16 sustained",
+                "unit": "TFLOP/s", "frac": achieved / peak,
+                "traffic": traffic_from_profile(kfile, kname)}
+
+    # ---- e2e: the same step through the public API with inputs copied in from pinned
+    # host memory every step and the loss read back
+    e2e = None
+    if not args.no_e2e:
+        host = {}
+
+        def pin(t):
+            h = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+            h.copy_(t)
+            return h
+
+        host["k"], host["v"] = pin(pr.k), pin(pr.v)
+        host["br"] = [(pin(b.q), pin(b.k), pin(b.v), pin(b.d_o)) for b in branches]
+        host["logits"] = pin(gin.logits)
+        host["targets"], host["logp_old"] = pin(gin.targets), pin(logp_old)
+        host["rewards"], host["lens"] = pin(gin.rewards), pin(gin.resp_lens)
+        loss_h = torch.empty(1, dtype=torch.float32, pin_memory=True)
+        h2d = sum(t.numel() * t.element_size() for t in
+                  [host["k"], host["v"], host["logits"], host["targets"], host["logp_old"],
+                   host["rewards"], host["lens"]] + [x for b in host["br"] for x in b])
+        d2h = 4
+
+        def e2e_step():
+            pr.k.copy_(host["k"], non_blocking=True)
+            pr.v.copy_(host["v"], non_blocking=True)
+            for b, hb in zip(branches, host["br"]):
+                for dst, src in zip((b.q, b.k, b.v, b.d_o), hb):
+                    dst.copy_(src, non_blocking=True)
+            gin.logits.copy_(host["logits"], non_blocking=True)
+            gin.targets.copy_(host["targets"], non_blocking=True)
+            logp_old.copy_(host["logp_old"], non_blocking=True)
+            gin.rewards.copy_(host["rewards"], non_blocking=True)
+            gin.resp_lens.copy_(host["lens"], non_blocking=True)
+            step()
+            loss_h.copy_(loss, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        a = ev()
+        for _ in range(args.steps):
+            e2e_step()
+        b = ev()
+        torch.cuda.synchronize()
+        e_ms = a.elapsed_time(b)
+        if world > 1:
+            t = torch.tensor([e_ms], device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            e_ms = float(t.item())
+        e2e = {"value": step_flops * world / (e_ms / K * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": d2h,
+               "ms_per_step": e_ms / K}
+
+    # ---- CPU baseline: the oracle on a bounded sample of the same workload
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline_attention(cache, branches[0], w, scale, budget_s=args.cpu_budget)
+
+    out = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded; shapes of the pages' 2,097,152-position runs)",
+        "config": {"workload": "P=2,097,152 prompt positions, Hq=24, Hkv=4, d=128, 256-token "
+                               "pages shuffled, 256 KV splits; G=8 serial replays R=4096; GRPO "
+                               "V=151,936 bf16 logits",
+                   "members": G, "l2": "inputs larger than L2 (prompt KV 4.29 GB per pass)"},
+        "components": comps, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": launches * K if launches is not None else None,
+        "clocks": clk.summary(),
+    }
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+
+
+def cpu_baseline_attention(cache, br, w, scale, budget_s: float):
+    """Time the fp64 oracle on sampled rows of the same workload (forward + dQ of each
+    sampled row over the full prompt) and express it in the metric's unit."""
+    import numpy as np
+
+    import oracle
+    from response_replay_gb300 import synthetic as syn
+
+    pb = oracle.AttnProblem(syn.bf16_bits(cache.k_pool), syn.bf16_bits(cache.v_pool),
+                            cache.page_table.cpu().numpy(), w.P, syn.bf16_bits(br.q),
+                            syn.bf16_bits(br.k), syn.bf16_bits(br.v), scale, w.num_splits)
+    d_o = syn.bf16_bits(br.d_o)
+    rng = np.random.default_rng(0)
+    R = br.q.shape[0]
+    threads = oracle.num_threads()
+
+    def run(n):
+        ts = rng.integers(0, R, n).astype(np.int32)
+        hs = rng.integers(0, w.hq, n).astype(np.int32)
+        t0 = time.perf_counter()
+        oracle.attn_fwd_rows(pb, ts, hs)
+        oracle.attn_bwd_dq_rows(pb, d_o, ts, hs)
+        dt = time.perf_counter() - t0
+        fl = sum(4.0 * D * (w.P + t + 1) + 6.0 * D * (w.P + t + 1) for t in ts)
+        return fl, dt
+
+    n = max(threads, 1)
+    fl, dt = run(n)
+    if dt < budget_s / 4:
+        n2 = int(n * min(64, max(1.0, (budget_s * 0.75) / max(dt, 1e-3))))
+        n2 = max(n, (n2 // max(threads, 1)) * max(threads, 1))
+        fl, dt = run(n2)
+        n = n2
+    return {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": f"{n} random (t, h) rows of one member: fp64 forward + dQ over all "
+                      f"{w.P} prompt keys and the causal response keys; {dt:.1f} s"}
+
+
+# ------------------------------------------------------------------ reference arm
+
+def run_reference(args, rank: int, world: int):
+    """The oracle as the reference arm: each step is a bounded sample of the same
+    workload on the host cores (rank 0 only)."""
+    if rank != 0:
+        return
+    import numpy as np
+
+    import oracle
+    from response_replay_gb300 import synthetic as syn
+
+    w = syn.WORKLOADS[WORKLOAD]
+    R = w.R[0]
+    seed = syn.seed_of(WORKLOAD)
+    rng = np.random.default_rng(seed)
+    # host-side inputs of the same shapes (bf16 bit patterns of N(0,1)/sqrt(d) values)
+    import torch
+    pr = syn.make_prompt(w.P, w.hkv, D, w.page_size, seed, "cpu")
+    pool_k = np.zeros((pr.num_pages, w.hkv, w.page_size, D), np.uint16)
+    pool_v = np.zeros_like(pool_k)
+    oracle.capture_kv(pool_k, pool_v, pr.page_table.numpy(), w.page_size, syn.bf16_bits(pr.k),
+                      syn.bf16_bits(pr.v), 0)
+    br = syn.make_branch(R, w.hq, w.hkv, D, seed + 1, "cpu")
+    pb = oracle.AttnProblem(pool_k, pool_v, pr.page_table.numpy(), w.P, syn.bf16_bits(br.q),
+                            syn.bf16_bits(br.k), syn.bf16_bits(br.v), D ** -0.5, w.num_splits)
+    d_o = syn.bf16_bits(br.d_o)
+    threads = oracle.num_threads()
+    n = max(threads, 1) * args.ref_rows_per_core
+
+    def sample_step():
+        ts = rng.integers(0, R, n).astype(np.int32)
+        hs = rng.integers(0, w.hq, n).astype(np.int32)
+        oracle.attn_fwd_rows(pb, ts, hs)
+        oracle.attn_bwd_dq_rows(pb, d_o, ts, hs)
+        return sum(10.0 * D * (w.P + t + 1) for t in ts)
+
+    for _ in range(args.warmup):
+        sample_step()
+    t0 = time.perf_counter()
+    fl = 0.0
+    for _ in range(args.steps):
+        fl += sample_step()
+    dt = time.perf_counter() - t0
+    v = fl / dt / 1e12
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": "P=2,097,152, Hq=24, Hkv=4, d=128, R=4096 "
+                                                    "(sampled rows)"},
+        "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": f"{n} random (t, h) rows per step: fp64 forward + dQ over "
+                                   f"the full prompt"},
+        "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--members", type=int, default=None, help="replay fewer members (debug)")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--ref-rows-per-core", type=int, default=2)
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        print("note: fewer than 3 warm-up steps", file=sys.stderr)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        import torch
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl")
+    try:
+        run_ours(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,195 @@
+/*
+ * longstraw.h -- C ABI of the GB300 response-replay hot path.
+ *
+ * LongStraw trains GRPO at million-token contexts by evaluating the shared prompt once
+ * without autograd, keeping only the state later tokens need (for full attention: K/V
+ * pages), and replaying one response branch at a time under autograd (LongStraw paper
+ * digest, "TL;DR" and "Method" steps 1-4; explainer "LongStraw: fitting million-token
+ * RL onto a fixed GPU budget", "The move: change the graph boundary" and "Serial replay
+ * makes G a schedule").  This library is that replay for one full-attention layer plus
+ * the GRPO loss, on one GPU:
+ *
+ *   ls_capture_kv          write the prompt's K/V into pages behind a page table
+ *   ls_replay_attn_fwd     exact attention of one response branch over the captured
+ *                          pages plus causal self-attention, split-KV partials merged
+ *                          by log-sum-exp
+ *   ls_replay_attn_bwd     dQ through prompt and response keys; dK/dV for the
+ *                          response's own keys only (the prompt state is stopgrad)
+ *   ls_grpo_loss_fwd_bwd   token-level clipped surrogate with group-relative
+ *                          advantages and its logits gradient
+ *
+ * Conventions shared by every call
+ *   - Memory: every pointer argument is DEVICE memory on the current CUDA device unless
+ *     stated otherwise, allocated and owned by the caller.  The library allocates no
+ *     device memory; temporary space is the caller's `workspace` (size from the
+ *     matching *_workspace query, which depends on the current device's SM count).
+ *   - Streams: work is enqueued on `stream` (NULL = legacy default stream) and the
+ *     calls return without synchronising, except ls_last_device_error.
+ *   - Layouts: dense row-major, innermost dimension last, no padding.  bf16 is the
+ *     upper half of an IEEE-754 binary32 (1 sign, 8 exponent, 7 fraction bits);
+ *     fp32 is binary32.
+ *   - Alignment: every device pointer must be 16-byte aligned.
+ *   - Errors: arguments are checked on the host first; on failure the call returns
+ *     LS_ERR_INVALID_ARG / LS_ERR_UNSUPPORTED / LS_ERR_WORKSPACE and launches
+ *     nothing.  A failed launch returns LS_ERR_CUDA.  Conditions only the device can
+ *     see (a page id outside the pool, response lengths that do not add up, a
+ *     pipeline wait that exceeded its time limit) never trap: the kernel skips the
+ *     offending access, records a code in a per-device error word and carries on;
+ *     ls_last_device_error() reports and clears it.
+ *   - Determinism: no floating-point atomics; the same inputs and launch
+ *     configuration give bit-identical outputs.
+ */
+#ifndef LONGSTRAW_H
+#define LONGSTRAW_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st* ls_stream_t;
+
+typedef enum {
+  LS_OK = 0,
+  LS_ERR_INVALID_ARG = 1,   /* a size, pointer, alignment or dtype is not accepted   */
+  LS_ERR_UNSUPPORTED = 2,   /* valid in principle, not built (e.g. head_dim != 128)  */
+  LS_ERR_WORKSPACE = 3,     /* workspace NULL or smaller than the query says          */
+  LS_ERR_CUDA = 4,          /* a CUDA runtime/driver call failed                      */
+  LS_ERR_TIMEOUT = 5,       /* a device pipeline wait hit its time limit              */
+  LS_ERR_DEVICE_CHECK = 6   /* a device-side argument check failed (bad page id ...)  */
+} ls_status;
+
+typedef enum { LS_BF16 = 0, LS_FP32 = 1 } ls_dtype;
+
+/* The captured prompt state of one attention layer: K and V pages plus the page table
+ * (the digest's "CP-sharded KV pages" of the Qwen implementation, held whole on one
+ * GPU).  Caller-owned; read-only after capture.
+ *   k_pool, v_pool  bf16 [num_pages][num_kv_heads][page_size][head_dim]
+ *   page_table      int32 [num_logical_pages]: logical page -> physical page in
+ *                   [0, num_pages).  Logical page p holds prompt positions
+ *                   [p * page_size, (p + 1) * page_size).
+ *   num_tokens      P, the valid prompt positions; P <= num_logical_pages * page_size.
+ *                   Positions >= P on the last page are never read by attention.
+ * Supported: head_dim == 128; page_size a power of two in [16, 4096]; num_pages *
+ * num_kv_heads * page_size < 2^31. */
+typedef struct {
+  void* k_pool;
+  void* v_pool;
+  const int32_t* page_table;
+  int32_t num_pages;
+  int32_t num_logical_pages;
+  int32_t page_size;
+  int32_t num_kv_heads;
+  int32_t head_dim;
+  int64_t num_tokens;
+} ls_kv_cache;
+
+/* ---------------------------------------------------------------- capture
+ * Prompt capture keeps the prompt's K/V as resident pages (digest, Method step 1;
+ * explainer, "The move: change the graph boundary").  Copies positions
+ * [start_pos, start_pos + n) of the prompt:
+ *   k_pool[pt[p / ps]][h][p % ps][:] = k[p - start_pos][h][:]   (same for v)
+ * k, v: bf16 [n][num_kv_heads][head_dim].  Bit copy.  Can be called in chunks.  A page
+ * id outside [0, num_pages) skips that position and sets LS_ERR_DEVICE_CHECK.
+ * start_pos + n must not exceed num_logical_pages * page_size. */
+ls_status ls_capture_kv(const ls_kv_cache* cache, const void* k, const void* v,
+                        int64_t start_pos, int64_t n, ls_stream_t stream);
+
+/* ---------------------------------------------------------------- replay forward
+ * Exact attention of one response branch (explainer, "Serial replay makes G a
+ * schedule"; digest, Method step 3) over the captured prompt and causally over its own
+ * keys; the prompt's split-KV partials are composed by log-sum-exp into the exact
+ * output, which the pages do across eight GPUs (explainer, "Two incompatible
+ * architectures", Qwen bullet) and this call does on one:
+ *   s_{t,j} = softmax_scale * <q_{t,h}, k_{j,h/g}>,  j over all P prompt positions and
+ *             response positions j <= t (g = Hq / num_kv_heads)
+ *   lse_{t,h} = log sum_j exp(s_{t,j})           (natural log)
+ *   o_{t,h}   = sum_j exp(s_{t,j} - lse_{t,h}) v_j
+ * q: bf16 [R][Hq][128]; k_resp, v_resp: bf16 [R][num_kv_heads][128] (the response's
+ * own keys/values); o: bf16 [R][Hq][128] (round-to-nearest-even); lse: fp32 [R][Hq].
+ * num_splits (>= 1) cuts the prompt into that many contiguous ranges of 128-token
+ * tiles; the result does not depend on it beyond rounding.  Hq % num_kv_heads == 0.
+ * R == 0 is a no-op.  P == 0 is plain causal attention of the response. */
+ls_status ls_replay_attn_fwd_workspace(const ls_kv_cache* cache, int R, int Hq,
+                                       int num_splits, size_t* bytes);
+ls_status ls_replay_attn_fwd(const ls_kv_cache* cache, const void* q, const void* k_resp,
+                             const void* v_resp, int R, int Hq, float softmax_scale,
+                             int num_splits, void* o, float* lse, void* workspace,
+                             size_t workspace_bytes, ls_stream_t stream);
+
+/* ---------------------------------------------------------------- replay backward
+ * Gradient of the replayed branch with the prompt state stopgrad: only
+ * d(loss)/d(theta) at the captured state is formed and the path through the prompt
+ * state is dropped (digest, Method, last paragraph; explainer, Figure 2 caption), so
+ * prompt keys and values receive no gradient and only the response's own keys do
+ * (explainer, "Two incompatible architectures": K/V gradient pages exist only where a
+ * response backward touches them).  With P_{t,j} = exp(s_{t,j} - lse_t),
+ * D_t = <dO_t, O_t>, dS_{t,j} = P_{t,j} (<dO_t, v_j> - D_t):
+ *   dq_t   = softmax_scale * sum_j dS_{t,j} k_j          (prompt and response keys)
+ *   dk_j   = softmax_scale * sum_{h in group, t >= j} dS_{t,j} q_t    (response j)
+ *   dv_j   = sum_{h in group, t >= j} P_{t,j} dO_t                    (response j)
+ * o, lse: the forward's outputs for the same inputs; d_o: bf16 [R][Hq][128].
+ * dq: fp32 [R][Hq][128]; dk_resp, dv_resp: fp32 [R][num_kv_heads][128].
+ * accumulate != 0 adds into dq/dk_resp/dv_resp instead of overwriting them (serial
+ * replay accumulates gradients member by member: digest, Method step 3). */
+ls_status ls_replay_attn_bwd_workspace(const ls_kv_cache* cache, int R, int Hq,
+                                       int num_splits, size_t* bytes);
+ls_status ls_replay_attn_bwd(const ls_kv_cache* cache, const void* q, const void* k_resp,
+                             const void* v_resp, const void* o, const float* lse,
+                             const void* d_o, int R, int Hq, float softmax_scale,
+                             int num_splits, int accumulate, float* dq, float* dk_resp,
+                             float* dv_resp, void* workspace, size_t workspace_bytes,
+                             ls_stream_t stream);
+
+/* ---------------------------------------------------------------- GRPO loss
+ * The clipped surrogate of the digest's Method section,
+ *   L = -(1/G) sum_i (1/R_i) sum_t min(rho_{i,t} A_i, clip(rho_{i,t}, 1-eps, 1+eps) A_i),
+ *   rho = exp(logp - logp_old),  logp = logits[target] - logsumexp(logits),
+ *   A_i = (r_i - mean r) / (std r + adv_eps)   (group-relative; std with std_ddof;
+ *                                             mean/std in fp64),
+ * and its gradient dL/dlogits_v = c_t (1[v == target] - softmax_v), where
+ * c_t = -A_i rho_t / (G R_i) when the unclipped term is the active minimum (ties
+ * included) and 0 when the clip holds the term constant.
+ * Serial replay calls this once per member (digest, Method step 3): logits hold the
+ * tokens of members [member_begin, member_end) back to back (member-major), while
+ * rewards and resp_lens describe all G members so every call sees the whole group.
+ *   logits   [T][V] of type dtype; T = sum of resp_lens over the range (checked on the
+ *            device: a mismatch sets LS_ERR_DEVICE_CHECK and writes nothing)
+ *   targets  int32 [T] in [0, V);  logp_old fp32 [T]
+ *   rewards  fp32 [G];  resp_lens int32 [G]
+ *   loss     fp32 device scalar: this call's contribution (accumulate_loss != 0 adds
+ *            it to the current value)
+ *   dlogits  [T][V] of type dtype (may alias nothing else)
+ *   logp_out fp32 [T] or NULL
+ *   stats    fp32 [4] or NULL: {tokens whose gradient the clip zeroed, sum of rho,
+ *            min rho, max rho} over this call's tokens
+ * G - std_ddof must be >= 1; 0 <= member_begin <= member_end <= G; V <= 2^30. */
+ls_status ls_grpo_workspace(int64_t T, int G, size_t* bytes);
+ls_status ls_grpo_loss_fwd_bwd(const void* logits, ls_dtype dtype, int64_t T, int V,
+                               const int32_t* targets, const float* logp_old,
+                               const float* rewards, const int32_t* resp_lens, int G,
+                               int member_begin, int member_end, float eps, float adv_eps,
+                               int std_ddof, int accumulate_loss, float* loss, void* dlogits,
+                               float* logp_out, float* stats, void* workspace,
+                               size_t workspace_bytes, ls_stream_t stream);
+
+/* ---------------------------------------------------------------- checks
+ * ls_validate_page_table: enqueue a check that every entry of the page table covering
+ * the cache's num_tokens lies in [0, num_pages) and that no physical page is used
+ * twice; a failure sets LS_ERR_DEVICE_CHECK in the device error word.
+ * ls_last_device_error: synchronise `stream`, return the first device-side error
+ * recorded on the current device since the last call (LS_OK if none) and clear it. */
+ls_status ls_validate_page_table(const ls_kv_cache* cache, void* workspace,
+                                 size_t workspace_bytes, ls_stream_t stream);
+ls_status ls_validate_page_table_workspace(const ls_kv_cache* cache, size_t* bytes);
+ls_status ls_last_device_error(ls_stream_t stream);
+
+const char* ls_status_string(ls_status status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* LONGSTRAW_H */

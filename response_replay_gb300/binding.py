@@ -1,0 +1,157 @@
+"""ctypes binding of include/longstraw.h.
+
+Argument marshalling only: every function below forwards to the C entry point of the
+same name in liblongstraw.so, which validates the arguments and launches the CUDA
+kernels.  Pointers are passed as integers (device addresses, e.g. tensor.data_ptr()),
+streams as integers (torch.cuda.Stream.cuda_stream; 0 = legacy default stream).
+
+There is no fallback: if the CUDA library has not been built, the first call raises.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "liblongstraw.so")
+
+LS_OK, LS_ERR_INVALID_ARG, LS_ERR_UNSUPPORTED, LS_ERR_WORKSPACE, LS_ERR_CUDA, \
+    LS_ERR_TIMEOUT, LS_ERR_DEVICE_CHECK = range(7)
+LS_BF16, LS_FP32 = 0, 1
+
+EXPORTED = (
+    "ls_capture_kv", "ls_replay_attn_fwd_workspace", "ls_replay_attn_fwd",
+    "ls_replay_attn_bwd_workspace", "ls_replay_attn_bwd", "ls_grpo_workspace",
+    "ls_grpo_loss_fwd_bwd", "ls_validate_page_table", "ls_validate_page_table_workspace",
+    "ls_last_device_error", "ls_status_string",
+)
+
+
+class ls_kv_cache(C.Structure):
+    _fields_ = [
+        ("k_pool", C.c_void_p), ("v_pool", C.c_void_p), ("page_table", C.c_void_p),
+        ("num_pages", C.c_int32), ("num_logical_pages", C.c_int32), ("page_size", C.c_int32),
+        ("num_kv_heads", C.c_int32), ("head_dim", C.c_int32), ("num_tokens", C.c_int64),
+    ]
+
+
+class LongstrawError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn}: {status_string(status)} (status {status})")
+
+
+_lib = None
+
+
+def lib() -> C.CDLL:
+    """The loaded CUDA library; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is missing: build the CUDA library first "
+                "(python -c 'import __graft_entry__ as g; g.build()')")
+        l = C.CDLL(LIB_PATH)
+        P, i32, i64, sz, f32 = C.c_void_p, C.c_int, C.c_int64, C.c_size_t, C.c_float
+        cache = C.POINTER(ls_kv_cache)
+        szp = C.POINTER(C.c_size_t)
+        sig = {
+            "ls_capture_kv": [cache, P, P, i64, i64, P],
+            "ls_replay_attn_fwd_workspace": [cache, i32, i32, i32, szp],
+            "ls_replay_attn_fwd": [cache, P, P, P, i32, i32, f32, i32, P, P, P, sz, P],
+            "ls_replay_attn_bwd_workspace": [cache, i32, i32, i32, szp],
+            "ls_replay_attn_bwd": [cache, P, P, P, P, P, P, i32, i32, f32, i32, i32, P, P, P, P,
+                                   sz, P],
+            "ls_grpo_workspace": [i64, i32, szp],
+            "ls_grpo_loss_fwd_bwd": [P, i32, i64, i32, P, P, P, P, i32, i32, i32, f32, f32, i32,
+                                     i32, P, P, P, P, P, sz, P],
+            "ls_validate_page_table": [cache, P, sz, P],
+            "ls_validate_page_table_workspace": [cache, szp],
+            "ls_last_device_error": [P],
+            "ls_status_string": [i32],
+        }
+        for name, args in sig.items():
+            f = getattr(l, name)
+            f.argtypes = args
+            f.restype = C.c_int
+        l.ls_status_string.restype = C.c_char_p
+        _lib = l
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().ls_status_string(status).decode()
+
+
+def _ok(fn: str, status: int) -> None:
+    if status != LS_OK:
+        raise LongstrawError(fn, status)
+
+
+def _size(fn: str, *args) -> int:
+    out = C.c_size_t(0)
+    _ok(fn, getattr(lib(), fn)(*args, C.byref(out)))
+    return out.value
+
+
+def ls_capture_kv(cache: ls_kv_cache, k: int, v: int, start_pos: int, n: int,
+                  stream: int = 0) -> None:
+    _ok("ls_capture_kv", lib().ls_capture_kv(C.byref(cache), k, v, start_pos, n, stream))
+
+
+def ls_replay_attn_fwd_workspace(cache: ls_kv_cache, R: int, Hq: int, num_splits: int) -> int:
+    return _size("ls_replay_attn_fwd_workspace", C.byref(cache), R, Hq, num_splits)
+
+
+def ls_replay_attn_fwd(cache: ls_kv_cache, q: int, k_resp: int, v_resp: int, R: int, Hq: int,
+                       softmax_scale: float, num_splits: int, o: int, lse: int, workspace: int,
+                       workspace_bytes: int, stream: int = 0) -> None:
+    _ok("ls_replay_attn_fwd",
+        lib().ls_replay_attn_fwd(C.byref(cache), q, k_resp, v_resp, R, Hq, softmax_scale,
+                                 num_splits, o, lse, workspace, workspace_bytes, stream))
+
+
+def ls_replay_attn_bwd_workspace(cache: ls_kv_cache, R: int, Hq: int, num_splits: int) -> int:
+    return _size("ls_replay_attn_bwd_workspace", C.byref(cache), R, Hq, num_splits)
+
+
+def ls_replay_attn_bwd(cache: ls_kv_cache, q: int, k_resp: int, v_resp: int, o: int, lse: int,
+                       d_o: int, R: int, Hq: int, softmax_scale: float, num_splits: int,
+                       accumulate: int, dq: int, dk_resp: int, dv_resp: int, workspace: int,
+                       workspace_bytes: int, stream: int = 0) -> None:
+    _ok("ls_replay_attn_bwd",
+        lib().ls_replay_attn_bwd(C.byref(cache), q, k_resp, v_resp, o, lse, d_o, R, Hq,
+                                 softmax_scale, num_splits, accumulate, dq, dk_resp, dv_resp,
+                                 workspace, workspace_bytes, stream))
+
+
+def ls_grpo_workspace(T: int, G: int) -> int:
+    return _size("ls_grpo_workspace", T, G)
+
+
+def ls_grpo_loss_fwd_bwd(logits: int, dtype: int, T: int, V: int, targets: int, logp_old: int,
+                         rewards: int, resp_lens: int, G: int, member_begin: int, member_end: int,
+                         eps: float, adv_eps: float, std_ddof: int, accumulate_loss: int,
+                         loss: int, dlogits: int, logp_out: int | None, stats: int | None,
+                         workspace: int, workspace_bytes: int, stream: int = 0) -> None:
+    _ok("ls_grpo_loss_fwd_bwd",
+        lib().ls_grpo_loss_fwd_bwd(logits, dtype, T, V, targets, logp_old, rewards, resp_lens, G,
+                                   member_begin, member_end, eps, adv_eps, std_ddof,
+                                   accumulate_loss, loss, dlogits, logp_out, stats, workspace,
+                                   workspace_bytes, stream))
+
+
+def ls_validate_page_table_workspace(cache: ls_kv_cache) -> int:
+    return _size("ls_validate_page_table_workspace", C.byref(cache))
+
+
+def ls_validate_page_table(cache: ls_kv_cache, workspace: int, workspace_bytes: int,
+                           stream: int = 0) -> None:
+    _ok("ls_validate_page_table",
+        lib().ls_validate_page_table(C.byref(cache), workspace, workspace_bytes, stream))
+
+
+def ls_last_device_error(stream: int = 0) -> int:
+    """Synchronise `stream`; return the recorded device-side status (LS_OK if none)."""
+    return lib().ls_last_device_error(stream)

@@ -1,0 +1,375 @@
+// grpo_loss.cu -- fused token-level clipped GRPO surrogate and its logits gradient.
+//
+// Loss (LongStraw paper digest, "Method", the L_policy equation):
+//   L = -(1/G) sum_i (1/R_i) sum_t min(rho A_i, clip(rho, 1-eps, 1+eps) A_i),
+//   rho = exp(logp - logp_old), logp = z_target - logsumexp(z),
+//   A_i = (r_i - mean r) / (std r + adv_eps)  (group-relative advantages).
+// Gradient: dL/dz_v = c_t (1[v == target] - softmax_v), c_t = -A_i rho / (G R_i) when
+// the unclipped term is the active minimum, 0 when the clip holds the term constant.
+//
+// Three launches:
+//   grpo_prep   1 block : advantages in fp64 (mean/std about the first reward), member
+//                         token offsets, 1/(G R_i); checks that lengths cover T.
+//   grpo_rows   grid    : one CTA per token row at a time.  Pass 1 streams the row once
+//                         (online max / sum-exp, 16-byte loads) and gathers z_target;
+//                         pass 2 re-reads the row (from L2: the row was just read) and
+//                         writes dlogits, or writes zeros without reading when c_t = 0.
+//                         HBM: V*b read + V*b written per token, the algorithmic floor.
+//   grpo_final  1 block : fixed-order fp64 reduction of the per-token terms -> loss,
+//                         stats.  No floating-point atomics: results are deterministic.
+#include <float.h>
+
+#include "ls_device.cuh"
+#include "ls_internal.h"
+
+namespace {
+
+constexpr int kRowThreads = 512;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+struct WsLayout {
+  size_t flag, adv, inv_norm, off, term, rho, zeroed, total;
+};
+
+__host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+__host__ __device__ inline WsLayout ws_layout(int64_t T, int G) {
+  WsLayout w;
+  size_t p = 0;
+  w.flag = p;      p = align256(p + 16);
+  w.adv = p;       p = align256(p + sizeof(double) * G);
+  w.inv_norm = p;  p = align256(p + sizeof(double) * G);
+  w.off = p;       p = align256(p + sizeof(int64_t) * (G + 1));
+  w.term = p;      p = align256(p + sizeof(double) * (T > 0 ? T : 1));
+  w.rho = p;       p = align256(p + sizeof(float) * (T > 0 ? T : 1));
+  w.zeroed = p;    p = align256(p + sizeof(float) * (T > 0 ? T : 1));
+  w.total = p;
+  return w;
+}
+
+template <typename P>
+__device__ __forceinline__ P* at(void* base, size_t off) {
+  return reinterpret_cast<P*>(static_cast<char*>(base) + off);
+}
+
+__global__ void grpo_prep(const float* __restrict__ rewards, const int32_t* __restrict__ lens,
+                          int G, int mb, int me, int std_ddof, double adv_eps, int64_t T,
+                          void* ws, uint32_t* err) {
+  if (threadIdx.x != 0) return;
+  const WsLayout w = ws_layout(T, G);
+  int32_t* flag = at<int32_t>(ws, w.flag);
+  double* adv = at<double>(ws, w.adv);
+  double* inv = at<double>(ws, w.inv_norm);
+  int64_t* off = at<int64_t>(ws, w.off);
+  const double r0 = rewards[0];
+  double mean = 0.0, var = 0.0;
+  for (int i = 0; i < G; ++i) mean += (double)rewards[i] - r0;
+  mean /= G;
+  for (int i = 0; i < G; ++i) {
+    const double dev = ((double)rewards[i] - r0) - mean;
+    var += dev * dev;
+  }
+  var /= (double)(G - std_ddof);
+  const double sd = sqrt(var);
+  for (int i = 0; i < G; ++i) adv[i] = (((double)rewards[i] - r0) - mean) / (sd + adv_eps);
+  int ok = 1;
+  off[0] = 0;
+  for (int i = mb; i < me; ++i) {
+    const int32_t n = lens[i];
+    if (n < 0) ok = 0;
+    off[i - mb + 1] = off[i - mb] + (n > 0 ? n : 0);
+    inv[i] = n > 0 ? 1.0 / ((double)G * (double)n) : 0.0;
+  }
+  if (off[me - mb] != T) ok = 0;
+  if (!ok) ls_report(err, LS_DEVERR_CHECK);
+  *flag = ok;
+}
+
+template <typename E>
+struct Vec;
+template <>
+struct Vec<float> {
+  static constexpr int N = 4;
+  __device__ static void unpack(const uint4& u, float* x) {
+    x[0] = __uint_as_float(u.x); x[1] = __uint_as_float(u.y);
+    x[2] = __uint_as_float(u.z); x[3] = __uint_as_float(u.w);
+  }
+  __device__ static uint4 pack(const float* x) {
+    return make_uint4(__float_as_uint(x[0]), __float_as_uint(x[1]), __float_as_uint(x[2]),
+                      __float_as_uint(x[3]));
+  }
+  __device__ static float load1(const float* p) { return *p; }
+  __device__ static void store1(float* p, float x) { *p = x; }
+};
+template <>
+struct Vec<__nv_bfloat16> {
+  static constexpr int N = 8;
+  __device__ static void unpack(const uint4& u, float* x) {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      x[2 * i] = __uint_as_float(w[i] << 16);
+      x[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+  }
+  __device__ static uint4 pack(const float* x) {
+    return make_uint4(pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]), pack_bf16(x[4], x[5]),
+                      pack_bf16(x[6], x[7]));
+  }
+  __device__ static float load1(const __nv_bfloat16* p) { return __bfloat162float(*p); }
+  __device__ static void store1(__nv_bfloat16* p, float x) { *p = __float2bfloat16_rn(x); }
+};
+
+// Online (max, sum of exp2) pair in the log2 domain.
+struct MS {
+  float m, s;
+};
+__device__ __forceinline__ MS ms_merge(MS a, MS b) {
+  const float m = fmaxf(a.m, b.m);
+  if (m == -INFINITY) return {m, 0.f};
+  return {m, a.s * fast_exp2(a.m - m) + b.s * fast_exp2(b.m - m)};
+}
+__device__ __forceinline__ void ms_add(MS& a, const float* x2, int n) {
+  float mx = x2[0];
+  for (int i = 1; i < n; ++i) mx = fmaxf(mx, x2[i]);
+  if (mx > a.m) {
+    a.s *= fast_exp2(a.m - mx);
+    a.m = mx;
+  }
+  for (int i = 0; i < n; ++i) a.s += fast_exp2(x2[i] - a.m);
+}
+
+template <typename E>
+__global__ void __launch_bounds__(kRowThreads) grpo_rows(
+    const E* __restrict__ logits, int64_t T, int V, const int32_t* __restrict__ targets,
+    const float* __restrict__ logp_old, int G, int mb, int me, float eps, E* __restrict__ dlogits,
+    float* __restrict__ logp_out, void* ws, uint32_t* err) {
+  using VT = Vec<E>;
+  constexpr int NV = VT::N;
+  const WsLayout w = ws_layout(T, G);
+  if (*at<int32_t>(ws, w.flag) == 0) return;
+  const double* adv = at<double>(ws, w.adv);
+  const double* inv = at<double>(ws, w.inv_norm);
+  const int64_t* off = at<int64_t>(ws, w.off);
+  double* term_out = at<double>(ws, w.term);
+  float* rho_out = at<float>(ws, w.rho);
+  float* zeroed_out = at<float>(ws, w.zeroed);
+
+  __shared__ MS red[kRowThreads / 32];
+  __shared__ float s_bcast[2];
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const int nm = me - mb;
+
+  for (int64_t row = blockIdx.x; row < T; row += gridDim.x) {
+    const E* zr = logits + row * (int64_t)V;
+    E* gr = dlogits + row * (int64_t)V;
+    // 16-byte aligned body [h, h + nvec*NV), scalar head [0, h) and tail.
+    const int h = (int)(((16 - (reinterpret_cast<uintptr_t>(zr) & 15)) & 15) / sizeof(E));
+    const int head = h < V ? h : V;
+    const int nvec = (V - head) / NV;
+    const int tail0 = head + nvec * NV;
+    const uint4* zv = reinterpret_cast<const uint4*>(zr + head);
+
+    // ---- pass 1: online max / sum-exp (log2 domain)
+    MS ms = {-INFINITY, 0.f};
+    for (int i = tid; i < head; i += kRowThreads) {
+      float x = VT::load1(zr + i) * kLog2e;
+      ms_add(ms, &x, 1);
+    }
+    for (int i = tail0 + tid; i < V; i += kRowThreads) {
+      float x = VT::load1(zr + i) * kLog2e;
+      ms_add(ms, &x, 1);
+    }
+    for (int i = tid; i < nvec; i += 4 * kRowThreads) {
+      uint4 u[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        if (i + k * kRowThreads < nvec) u[k] = zv[i + k * kRowThreads];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        if (i + k * kRowThreads < nvec) {
+          float x[NV];
+          VT::unpack(u[k], x);
+#pragma unroll
+          for (int e = 0; e < NV; ++e) x[e] *= kLog2e;
+          ms_add(ms, x, NV);
+        }
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      MS other = {__shfl_xor_sync(0xffffffffu, ms.m, o), __shfl_xor_sync(0xffffffffu, ms.s, o)};
+      ms = ms_merge(ms, other);
+    }
+    if (lane == 0) red[wid] = ms;
+    __syncthreads();
+    if (wid == 0) {
+      MS a = lane < kRowThreads / 32 ? red[lane] : MS{-INFINITY, 0.f};
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        MS other = {__shfl_xor_sync(0xffffffffu, a.m, o), __shfl_xor_sync(0xffffffffu, a.s, o)};
+        a = ms_merge(a, other);
+      }
+      if (lane == 0) {
+        // member of this token (binary search over the range's offsets)
+        int lo = 0, hi = nm - 1;
+        while (lo < hi) {
+          const int mid = (lo + hi + 1) >> 1;
+          if (off[mid] <= row) lo = mid; else hi = mid - 1;
+        }
+        const int mi = mb + lo;
+        const float lse2 = a.m + log2f(a.s);
+        const int32_t y = targets[row];
+        float c = 0.f;
+        double term = 0.0;
+        float rho = 0.f, zeroed = 0.f;
+        if ((uint32_t)y < (uint32_t)V) {
+          const float logp = VT::load1(zr + y) - lse2 * kLn2;
+          rho = expf(logp - logp_old[row]);
+          const float A = (float)adv[mi];
+          const float clipped = fminf(fmaxf(rho, 1.f - eps), 1.f + eps);
+          const bool active = rho * A <= clipped * A;  // ties: the unclipped branch
+          term = (double)(active ? rho : clipped) * adv[mi];
+          c = active ? (float)(-adv[mi] * (double)rho * inv[mi]) : 0.f;
+          zeroed = (!active && A != 0.f) ? 1.f : 0.f;
+          if (logp_out) logp_out[row] = logp;
+        } else {
+          ls_report(err, LS_DEVERR_CHECK);
+          if (logp_out) logp_out[row] = NAN;
+        }
+        term_out[row] = term;
+        rho_out[row] = rho;
+        zeroed_out[row] = zeroed;
+        s_bcast[0] = c;
+        s_bcast[1] = lse2;
+      }
+    }
+    __syncthreads();
+    const float c = s_bcast[0], lse2 = s_bcast[1];
+    const int32_t y = targets[row];
+
+    // ---- pass 2: dlogits = c (1[v == y] - exp2(z log2e - lse2))
+    if (c == 0.f) {
+      const uint4 zero = make_uint4(0, 0, 0, 0);
+      uint4* gv = reinterpret_cast<uint4*>(gr + head);
+      for (int i = tid; i < nvec; i += kRowThreads) __stcs(gv + i, zero);
+      for (int i = tid; i < head; i += kRowThreads) VT::store1(gr + i, 0.f);
+      for (int i = tail0 + tid; i < V; i += kRowThreads) VT::store1(gr + i, 0.f);
+    } else {
+      uint4* gv = reinterpret_cast<uint4*>(gr + head);
+      for (int i = tid; i < nvec; i += 4 * kRowThreads) {
+        uint4 u[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          if (i + k * kRowThreads < nvec) u[k] = __ldcs(zv + i + k * kRowThreads);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int vi = i + k * kRowThreads;
+          if (vi < nvec) {
+            float x[NV];
+            VT::unpack(u[k], x);
+            const int v0 = head + vi * NV;
+#pragma unroll
+            for (int e = 0; e < NV; ++e) {
+              x[e] = -c * fast_exp2(fmaf(x[e], kLog2e, -lse2));
+              if (v0 + e == y) x[e] += c;
+            }
+            __stcs(gv + vi, VT::pack(x));
+          }
+        }
+      }
+      for (int i = tid; i < head; i += kRowThreads) {
+        float g = -c * fast_exp2(fmaf(VT::load1(zr + i), kLog2e, -lse2));
+        VT::store1(gr + i, i == y ? g + c : g);
+      }
+      for (int i = tail0 + tid; i < V; i += kRowThreads) {
+        float g = -c * fast_exp2(fmaf(VT::load1(zr + i), kLog2e, -lse2));
+        VT::store1(gr + i, i == y ? g + c : g);
+      }
+    }
+    __syncthreads();  // red / s_bcast reuse in the next row
+  }
+}
+
+__global__ void __launch_bounds__(1024) grpo_final(int64_t T, int G, int mb, int me,
+                                                   int accumulate, float* loss, float* stats,
+                                                   void* ws) {
+  const WsLayout w = ws_layout(T, G);
+  if (*at<int32_t>(ws, w.flag) == 0) return;
+  const double* inv = at<double>(ws, w.inv_norm);
+  const int64_t* off = at<int64_t>(ws, w.off);
+  const double* term = at<double>(ws, w.term);
+  const float* rho = at<float>(ws, w.rho);
+  const float* zeroed = at<float>(ws, w.zeroed);
+  __shared__ double s_sum[1024];
+  __shared__ double s_z[1024], s_r[1024];
+  __shared__ float s_mn[1024], s_mx[1024];
+  const int tid = threadIdx.x;
+  double acc = 0.0, zc = 0.0, rs = 0.0;
+  float mn = FLT_MAX, mx = -FLT_MAX;
+  const int nm = me - mb;
+  for (int m = 0; m < nm; ++m) {
+    const double wgt = inv[mb + m] * (double)G;  // 1 / R_i
+    for (int64_t t = off[m] + tid; t < off[m + 1]; t += blockDim.x) acc += term[t] * wgt;
+  }
+  for (int64_t t = tid; t < T; t += blockDim.x) {
+    zc += zeroed[t];
+    rs += rho[t];
+    mn = fminf(mn, rho[t]);
+    mx = fmaxf(mx, rho[t]);
+  }
+  s_sum[tid] = acc; s_z[tid] = zc; s_r[tid] = rs; s_mn[tid] = mn; s_mx[tid] = mx;
+  __syncthreads();
+  for (int s = blockDim.x / 2; s > 0; s >>= 1) {
+    if (tid < s) {
+      s_sum[tid] += s_sum[tid + s];
+      s_z[tid] += s_z[tid + s];
+      s_r[tid] += s_r[tid + s];
+      s_mn[tid] = fminf(s_mn[tid], s_mn[tid + s]);
+      s_mx[tid] = fmaxf(s_mx[tid], s_mx[tid + s]);
+    }
+    __syncthreads();
+  }
+  if (tid == 0) {
+    const float contrib = (float)(-s_sum[0] / (double)G);
+    loss[0] = accumulate ? loss[0] + contrib : contrib;
+    if (stats) {
+      stats[0] = (float)s_z[0];
+      stats[1] = (float)s_r[0];
+      stats[2] = T > 0 ? s_mn[0] : 0.f;
+      stats[3] = T > 0 ? s_mx[0] : 0.f;
+    }
+  }
+}
+
+}  // namespace
+
+size_t ls_grpo_ws_bytes(int64_t T, int G) { return ws_layout(T, G).total; }
+
+cudaError_t ls_launch_grpo(const LsGrpoArgs& a, int num_sms, cudaStream_t st) {
+  grpo_prep<<<1, 32, 0, st>>>(a.rewards, a.resp_lens, a.G, a.member_begin, a.member_end,
+                              a.std_ddof, a.adv_eps, a.T, a.workspace, a.err);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  if (a.T > 0) {
+    int64_t grid = (int64_t)num_sms * 2;
+    if (grid > a.T) grid = a.T;
+    if (a.is_bf16) {
+      grpo_rows<__nv_bfloat16><<<(unsigned)grid, kRowThreads, 0, st>>>(
+          static_cast<const __nv_bfloat16*>(a.logits), a.T, a.V, a.targets, a.logp_old, a.G,
+          a.member_begin, a.member_end, a.eps, static_cast<__nv_bfloat16*>(a.dlogits),
+          a.logp_out, a.workspace, a.err);
+    } else {
+      grpo_rows<float><<<(unsigned)grid, kRowThreads, 0, st>>>(
+          static_cast<const float*>(a.logits), a.T, a.V, a.targets, a.logp_old, a.G,
+          a.member_begin, a.member_end, a.eps, static_cast<float*>(a.dlogits), a.logp_out,
+          a.workspace, a.err);
+    }
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  grpo_final<<<1, 1024, 0, st>>>(a.T, a.G, a.member_begin, a.member_end, a.accumulate_loss,
+                                 a.loss, a.stats, a.workspace);
+  return cudaGetLastError();
+}

@@ -1,0 +1,355 @@
+// ls_api.cu -- the extern "C" entry points of include/longstraw.h: argument checks,
+// workspace layout, the per-device error word and the kernel launches.
+#include <math.h>
+#include <mutex>
+
+#include "../../include/longstraw.h"
+#include "ls_internal.h"
+
+// One error word per device (module globals are instantiated per device).  Kernels
+// OR LS_DEVERR_* bits into it; ls_last_device_error reads and clears it.
+__device__ uint32_t g_ls_device_error;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int kHeadDim = 128;
+
+struct DevInfo {
+  int sms = 0;
+  uint32_t* err = nullptr;
+};
+DevInfo g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+// SM count and error-word address of the current device (looked up once per device,
+// with that device current).
+ls_status dev_info(DevInfo* out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return LS_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_dev_mu);
+  DevInfo& d = g_dev[dev];
+  if (d.sms == 0) {
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return LS_ERR_CUDA;
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_ls_device_error) != cudaSuccess) return LS_ERR_CUDA;
+    d.err = static_cast<uint32_t*>(p);
+    d.sms = sms;
+  }
+  *out = d;
+  return LS_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+int ilog2_exact(int x) {
+  if (x <= 0 || (x & (x - 1))) return -1;
+  int l = 0;
+  while ((1 << l) < x) ++l;
+  return l;
+}
+
+// Checks shared by every call that reads the cache.
+ls_status check_cache(const ls_kv_cache* c) {
+  if (!c) return LS_ERR_INVALID_ARG;
+  if (c->head_dim != kHeadDim) return LS_ERR_UNSUPPORTED;
+  const int l = ilog2_exact(c->page_size);
+  if (l < 4 || l > 12) return LS_ERR_UNSUPPORTED;
+  if (c->num_kv_heads <= 0 || c->num_pages <= 0 || c->num_logical_pages < 0 || c->num_tokens < 0)
+    return LS_ERR_INVALID_ARG;
+  if ((int64_t)c->num_pages * c->num_kv_heads * c->page_size >= (1ll << 31)) return LS_ERR_UNSUPPORTED;
+  if (c->num_tokens > (int64_t)c->num_logical_pages * c->page_size) return LS_ERR_INVALID_ARG;
+  if (!c->k_pool || !c->v_pool || !aligned16(c->k_pool) || !aligned16(c->v_pool))
+    return LS_ERR_INVALID_ARG;
+  if (c->num_logical_pages > 0 && !c->page_table) return LS_ERR_INVALID_ARG;
+  return LS_OK;
+}
+
+ls_status from_cuda(cudaError_t e) { return e == cudaSuccess ? LS_OK : LS_ERR_CUDA; }
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+// ---- replay attention: argument block, schedule and workspace layout
+
+ls_status check_replay(const ls_kv_cache* c, int R, int Hq, int num_splits) {
+  ls_status s = check_cache(c);
+  if (s != LS_OK) return s;
+  if (R < 0 || Hq <= 0 || num_splits < 1) return LS_ERR_INVALID_ARG;
+  if (Hq % c->num_kv_heads != 0) return LS_ERR_INVALID_ARG;
+  return LS_OK;
+}
+
+LsSched make_sched(const ls_kv_cache* c, int R, int Hq, int num_splits, int unit_rows, int tile,
+                   int ctas) {
+  const int units = ls_num_units(R, Hq, c->num_kv_heads, unit_rows);
+  const int ntiles = (int)((c->num_tokens + tile - 1) / tile);
+  return ls_make_sched(units, ntiles, num_splits, ctas);
+}
+
+struct FwdWs {
+  size_t part_o, part_lse, total;
+};
+FwdWs fwd_ws(const LsSched& sc, int unit_rows) {
+  FwdWs w;
+  size_t p = 0;
+  const bool tail = sc.tail_items > 0;
+  w.part_o = p;
+  p = align256(p + (tail ? (size_t)2 * sc.ctas * unit_rows * kHeadDim * 4 : 0));
+  w.part_lse = p;
+  p = align256(p + (tail ? (size_t)2 * sc.ctas * unit_rows * 4 : 0));
+  w.total = p;
+  return w;
+}
+
+struct BwdWs {
+  size_t delta, part_dq, total;
+};
+BwdWs bwd_ws(const LsSched& sc, int unit_rows, int R, int Hq) {
+  BwdWs w;
+  size_t p = 0;
+  w.delta = p;
+  p = align256(p + (size_t)R * Hq * 4);
+  w.part_dq = p;
+  p = align256(p + (sc.tail_items > 0 ? (size_t)2 * sc.ctas * unit_rows * kHeadDim * 4 : 0));
+  w.total = p;
+  return w;
+}
+
+LsAttnArgs attn_args(const ls_kv_cache* c, const void* q, const void* kr, const void* vr, int R,
+                     int Hq, float scale, uint32_t* err) {
+  LsAttnArgs a;
+  a.k_pool = c->k_pool;
+  a.v_pool = c->v_pool;
+  a.page_table = c->page_table;
+  a.num_pages = c->num_pages;
+  a.ps_log2 = ilog2_exact(c->page_size);
+  a.P = c->num_tokens;
+  a.hkv = c->num_kv_heads;
+  a.hq = Hq;
+  a.g = Hq / c->num_kv_heads;
+  a.R = R;
+  a.q = q;
+  a.k_resp = kr;
+  a.v_resp = vr;
+  a.scale = scale;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.err = err;
+  return a;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* ls_status_string(ls_status s) {
+  switch (s) {
+    case LS_OK: return "ok";
+    case LS_ERR_INVALID_ARG: return "invalid argument";
+    case LS_ERR_UNSUPPORTED: return "unsupported configuration";
+    case LS_ERR_WORKSPACE: return "workspace missing or too small";
+    case LS_ERR_CUDA: return "CUDA error";
+    case LS_ERR_TIMEOUT: return "device pipeline wait timed out";
+    case LS_ERR_DEVICE_CHECK: return "device-side argument check failed";
+  }
+  return "unknown status";
+}
+
+ls_status ls_capture_kv(const ls_kv_cache* cache, const void* k, const void* v, int64_t start_pos,
+                        int64_t n, ls_stream_t stream) {
+  ls_status s = check_cache(cache);
+  if (s != LS_OK) return s;
+  if (start_pos < 0 || n < 0) return LS_ERR_INVALID_ARG;
+  if (start_pos + n > (int64_t)cache->num_logical_pages * cache->page_size) return LS_ERR_INVALID_ARG;
+  if (n == 0) return LS_OK;
+  if (!k || !v || !aligned16(k) || !aligned16(v)) return LS_ERR_INVALID_ARG;
+  DevInfo d;
+  if ((s = dev_info(&d)) != LS_OK) return s;
+  return from_cuda(ls_launch_capture(k, v, cache->k_pool, cache->v_pool, cache->page_table,
+                                     cache->num_pages, ilog2_exact(cache->page_size),
+                                     cache->num_kv_heads, start_pos, n, d.sms, d.err,
+                                     (cudaStream_t)stream));
+}
+
+ls_status ls_replay_attn_fwd_workspace(const ls_kv_cache* cache, int R, int Hq, int num_splits,
+                                       size_t* bytes) {
+  ls_status s = check_replay(cache, R, Hq, num_splits);
+  if (s != LS_OK) return s;
+  if (!bytes) return LS_ERR_INVALID_ARG;
+  DevInfo d;
+  if ((s = dev_info(&d)) != LS_OK) return s;
+  const LsSched sc = make_sched(cache, R, Hq, num_splits, ls_fwd_unit_rows(), ls_fwd_tile(),
+                                d.sms * ls_fwd_ctas_per_sm());
+  *bytes = fwd_ws(sc, ls_fwd_unit_rows()).total;
+  return LS_OK;
+}
+
+ls_status ls_replay_attn_fwd(const ls_kv_cache* cache, const void* q, const void* k_resp,
+                             const void* v_resp, int R, int Hq, float softmax_scale, int num_splits,
+                             void* o, float* lse, void* workspace, size_t workspace_bytes,
+                             ls_stream_t stream) {
+  ls_status s = check_replay(cache, R, Hq, num_splits);
+  if (s != LS_OK) return s;
+  if (!isfinite(softmax_scale)) return LS_ERR_INVALID_ARG;
+  if (R == 0) return LS_OK;
+  const void* ptrs[] = {q, k_resp, v_resp, o, lse};
+  for (const void* p : ptrs)
+    if (!p || !aligned16(p)) return LS_ERR_INVALID_ARG;
+  DevInfo d;
+  if ((s = dev_info(&d)) != LS_OK) return s;
+  const LsSched sc = make_sched(cache, R, Hq, num_splits, ls_fwd_unit_rows(), ls_fwd_tile(),
+                                d.sms * ls_fwd_ctas_per_sm());
+  const FwdWs w = fwd_ws(sc, ls_fwd_unit_rows());
+  if (w.total > 0 && (!workspace || workspace_bytes < w.total || !aligned16(workspace)))
+    return LS_ERR_WORKSPACE;
+  const LsAttnArgs a = attn_args(cache, q, k_resp, v_resp, R, Hq, softmax_scale, d.err);
+  LsFwdOut out;
+  out.o = o;
+  out.lse = lse;
+  out.part_o = reinterpret_cast<float*>(static_cast<char*>(workspace) + w.part_o);
+  out.part_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) + w.part_lse);
+  return from_cuda(ls_launch_replay_fwd(a, sc, out, (cudaStream_t)stream));
+}
+
+ls_status ls_replay_attn_bwd_workspace(const ls_kv_cache* cache, int R, int Hq, int num_splits,
+                                       size_t* bytes) {
+  ls_status s = check_replay(cache, R, Hq, num_splits);
+  if (s != LS_OK) return s;
+  if (!bytes) return LS_ERR_INVALID_ARG;
+  DevInfo d;
+  if ((s = dev_info(&d)) != LS_OK) return s;
+  const LsSched sc = make_sched(cache, R, Hq, num_splits, ls_bwd_unit_rows(), ls_bwd_tile(),
+                                d.sms * ls_bwd_ctas_per_sm());
+  *bytes = bwd_ws(sc, ls_bwd_unit_rows(), R, Hq).total;
+  return LS_OK;
+}
+
+ls_status ls_replay_attn_bwd(const ls_kv_cache* cache, const void* q, const void* k_resp,
+                             const void* v_resp, const void* o, const float* lse, const void* d_o,
+                             int R, int Hq, float softmax_scale, int num_splits, int accumulate,
+                             float* dq, float* dk_resp, float* dv_resp, void* workspace,
+                             size_t workspace_bytes, ls_stream_t stream) {
+  ls_status s = check_replay(cache, R, Hq, num_splits);
+  if (s != LS_OK) return s;
+  if (!isfinite(softmax_scale)) return LS_ERR_INVALID_ARG;
+  if (R == 0) return LS_OK;
+  const void* ptrs[] = {q, k_resp, v_resp, o, lse, d_o, dq, dk_resp, dv_resp};
+  for (const void* p : ptrs)
+    if (!p || !aligned16(p)) return LS_ERR_INVALID_ARG;
+  DevInfo d;
+  if ((s = dev_info(&d)) != LS_OK) return s;
+  const LsSched sc = make_sched(cache, R, Hq, num_splits, ls_bwd_unit_rows(), ls_bwd_tile(),
+                                d.sms * ls_bwd_ctas_per_sm());
+  const BwdWs w = bwd_ws(sc, ls_bwd_unit_rows(), R, Hq);
+  if (!workspace || workspace_bytes < w.total || !aligned16(workspace)) return LS_ERR_WORKSPACE;
+  const LsAttnArgs a = attn_args(cache, q, k_resp, v_resp, R, Hq, softmax_scale, d.err);
+  LsBwdIn b;
+  b.o = o;
+  b.lse = lse;
+  b.d_o = d_o;
+  b.delta = reinterpret_cast<float*>(static_cast<char*>(workspace) + w.delta);
+  b.part_dq = reinterpret_cast<float*>(static_cast<char*>(workspace) + w.part_dq);
+  b.dq = dq;
+  b.dk = dk_resp;
+  b.dv = dv_resp;
+  b.accumulate = accumulate != 0;
+  return from_cuda(ls_launch_replay_bwd(a, sc, b, d.sms, (cudaStream_t)stream));
+}
+
+ls_status ls_grpo_workspace(int64_t T, int G, size_t* bytes) {
+  if (T < 0 || G <= 0 || !bytes) return LS_ERR_INVALID_ARG;
+  *bytes = ls_grpo_ws_bytes(T, G);
+  return LS_OK;
+}
+
+ls_status ls_grpo_loss_fwd_bwd(const void* logits, ls_dtype dtype, int64_t T, int V,
+                               const int32_t* targets, const float* logp_old, const float* rewards,
+                               const int32_t* resp_lens, int G, int member_begin, int member_end,
+                               float eps, float adv_eps, int std_ddof, int accumulate_loss,
+                               float* loss, void* dlogits, float* logp_out, float* stats,
+                               void* workspace, size_t workspace_bytes, ls_stream_t stream) {
+  if (dtype != LS_BF16 && dtype != LS_FP32) return LS_ERR_INVALID_ARG;
+  if (T < 0 || V <= 0 || V > (1 << 30) || G <= 0 || std_ddof < 0 || G - std_ddof < 1)
+    return LS_ERR_INVALID_ARG;
+  if (member_begin < 0 || member_end > G || member_begin > member_end) return LS_ERR_INVALID_ARG;
+  if (!(eps >= 0.f) || !isfinite(adv_eps) || adv_eps < 0.f) return LS_ERR_INVALID_ARG;
+  if (!rewards || !resp_lens || !loss || !aligned16(rewards) || !aligned16(resp_lens) ||
+      !aligned16(loss))
+    return LS_ERR_INVALID_ARG;
+  if (T > 0) {
+    const void* ptrs[] = {logits, targets, logp_old, dlogits};
+    for (const void* p : ptrs)
+      if (!p || !aligned16(p)) return LS_ERR_INVALID_ARG;
+    if (logp_out && !aligned16(logp_out)) return LS_ERR_INVALID_ARG;
+  }
+  if (stats && !aligned16(stats)) return LS_ERR_INVALID_ARG;
+  const size_t need = ls_grpo_ws_bytes(T, G);
+  if (!workspace || workspace_bytes < need || !aligned16(workspace)) return LS_ERR_WORKSPACE;
+  DevInfo d;
+  ls_status s = dev_info(&d);
+  if (s != LS_OK) return s;
+  LsGrpoArgs a;
+  a.logits = logits;
+  a.is_bf16 = dtype == LS_BF16;
+  a.T = T;
+  a.V = V;
+  a.targets = targets;
+  a.logp_old = logp_old;
+  a.rewards = rewards;
+  a.resp_lens = resp_lens;
+  a.G = G;
+  a.member_begin = member_begin;
+  a.member_end = member_end;
+  a.eps = eps;
+  a.adv_eps = adv_eps;
+  a.std_ddof = std_ddof;
+  a.accumulate_loss = accumulate_loss != 0;
+  a.loss = loss;
+  a.dlogits = dlogits;
+  a.logp_out = logp_out;
+  a.stats = stats;
+  a.workspace = workspace;
+  a.err = d.err;
+  return from_cuda(ls_launch_grpo(a, d.sms, (cudaStream_t)stream));
+}
+
+ls_status ls_validate_page_table_workspace(const ls_kv_cache* cache, size_t* bytes) {
+  ls_status s = check_cache(cache);
+  if (s != LS_OK) return s;
+  if (!bytes) return LS_ERR_INVALID_ARG;
+  *bytes = align256(((size_t)cache->num_pages + 31) / 32 * 4);
+  return LS_OK;
+}
+
+ls_status ls_validate_page_table(const ls_kv_cache* cache, void* workspace, size_t workspace_bytes,
+                                 ls_stream_t stream) {
+  size_t need = 0;
+  ls_status s = ls_validate_page_table_workspace(cache, &need);
+  if (s != LS_OK) return s;
+  if (!workspace || workspace_bytes < need || !aligned16(workspace)) return LS_ERR_WORKSPACE;
+  DevInfo d;
+  if ((s = dev_info(&d)) != LS_OK) return s;
+  const int32_t logical =
+      (int32_t)((cache->num_tokens + cache->page_size - 1) / cache->page_size);
+  if (logical == 0) return LS_OK;
+  return from_cuda(ls_launch_validate_pages(cache->page_table, logical, cache->num_pages,
+                                            static_cast<uint32_t*>(workspace), d.err,
+                                            (cudaStream_t)stream));
+}
+
+ls_status ls_last_device_error(ls_stream_t stream) {
+  DevInfo d;
+  ls_status s = dev_info(&d);
+  if (s != LS_OK) return s;
+  if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return LS_ERR_CUDA;
+  uint32_t v = 0;
+  if (cudaMemcpy(&v, d.err, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess) return LS_ERR_CUDA;
+  if (v == 0) return LS_OK;
+  const uint32_t zero = 0;
+  if (cudaMemcpy(d.err, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess)
+    return LS_ERR_CUDA;
+  return (v & LS_DEVERR_TIMEOUT) ? LS_ERR_TIMEOUT : LS_ERR_DEVICE_CHECK;
+}
+
+}  // extern "C"

@@ -1,0 +1,97 @@
+// ls_internal.h -- host-side interface between the C ABI (ls_api.cu) and the kernel
+// translation units.  Not installed; the public interface is include/longstraw.h.
+#pragma once
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "ls_sched.h"
+
+// Bits of the per-device error word (see ls_last_device_error).
+#define LS_DEVERR_CHECK 1u    // a device-side argument check failed
+#define LS_DEVERR_TIMEOUT 2u  // a pipeline wait exceeded its time limit
+
+// Problem description shared by the replay-attention kernels (device pointers).
+struct LsAttnArgs {
+  const void* k_pool;        // bf16 [num_pages][hkv][ps][128]
+  const void* v_pool;
+  const int32_t* page_table; // [num_logical_pages]
+  int32_t num_pages;
+  int32_t ps_log2;           // page size = 1 << ps_log2
+  int64_t P;                 // valid prompt tokens
+  int32_t hkv, hq, g;        // g = hq / hkv
+  int32_t R;                 // response tokens
+  const void* q;             // bf16 [R][hq][128]
+  const void* k_resp;        // bf16 [R][hkv][128]
+  const void* v_resp;
+  float scale_log2;          // softmax_scale * log2(e)
+  float scale;               // softmax_scale
+  uint32_t* err;             // device error word
+};
+
+struct LsFwdOut {
+  void* o;                   // bf16 [R][hq][128]
+  float* lse;                // [R][hq]
+  float* part_o;             // workspace: [2*ctas][unit_rows][128]
+  float* part_lse;           // workspace: [2*ctas][unit_rows]
+};
+
+struct LsBwdIn {
+  const void* o;             // bf16 [R][hq][128]
+  const float* lse;          // [R][hq]
+  const void* d_o;           // bf16 [R][hq][128]
+  float* delta;              // workspace [R][hq]: D = <dO, O>
+  float* dq;                 // [R][hq][128]
+  float* dk;                 // [R][hkv][128]
+  float* dv;
+  float* part_dq;            // workspace: [2*ctas][unit_rows][128]
+  int32_t accumulate;
+};
+
+// Geometry of the replay kernels (fixed at build time).
+int ls_fwd_unit_rows();
+int ls_fwd_tile();
+int ls_fwd_ctas_per_sm();
+int ls_bwd_unit_rows();
+int ls_bwd_tile();
+int ls_bwd_ctas_per_sm();
+int ls_num_units(int R, int hq, int hkv, int unit_rows);
+
+cudaError_t ls_launch_capture(const void* k, const void* v, void* k_pool, void* v_pool,
+                              const int32_t* page_table, int32_t num_pages, int32_t ps_log2,
+                              int32_t hkv, int64_t start_pos, int64_t n, int num_sms,
+                              uint32_t* err, cudaStream_t st);
+
+cudaError_t ls_launch_validate_pages(const int32_t* page_table, int32_t num_logical,
+                                     int32_t num_pages, uint32_t* seen, uint32_t* err,
+                                     cudaStream_t st);
+
+cudaError_t ls_launch_replay_fwd(const LsAttnArgs& a, const LsSched& sc, const LsFwdOut& out,
+                                 cudaStream_t st);
+
+cudaError_t ls_launch_replay_bwd(const LsAttnArgs& a, const LsSched& sc, const LsBwdIn& b,
+                                 int num_sms, cudaStream_t st);
+
+struct LsGrpoArgs {
+  const void* logits;
+  int32_t is_bf16;
+  int64_t T;
+  int32_t V;
+  const int32_t* targets;
+  const float* logp_old;
+  const float* rewards;
+  const int32_t* resp_lens;
+  int32_t G, member_begin, member_end;
+  float eps;
+  double adv_eps;
+  int32_t std_ddof;
+  int32_t accumulate_loss;
+  float* loss;
+  void* dlogits;
+  float* logp_out;
+  float* stats;
+  void* workspace;
+  uint32_t* err;
+};
+size_t ls_grpo_ws_bytes(int64_t T, int G);
+cudaError_t ls_launch_grpo(const LsGrpoArgs& a, int num_sms, cudaStream_t st);

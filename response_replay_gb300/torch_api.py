@@ -1,0 +1,175 @@
+"""PyTorch-facing helpers over the C ABI.
+
+PyTorch supplies device memory and streams; every step of the computation runs in the
+CUDA kernels behind include/longstraw.h.  These helpers allocate outputs and workspace
+with torch, check shapes and dtypes, and pass raw pointers to the binding.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import binding as B
+
+HEAD_DIM = 128
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _check(t: torch.Tensor, name: str, dtype, shape=None):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name}: expected {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: expected shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+_workspaces: dict = {}
+
+
+def workspace(nbytes: int, device: torch.device, key: str = "default") -> torch.Tensor:
+    """A reusable uint8 workspace of at least nbytes on `device` (grown on demand).
+    Calls that share a key must not overlap on the GPU."""
+    k = (device.index if device.index is not None else torch.cuda.current_device(), key)
+    ws = _workspaces.get(k)
+    if ws is None or ws.numel() < max(nbytes, 1):
+        ws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+        _workspaces[k] = ws
+    return ws
+
+
+class PagedKVCache:
+    """K/V page pools plus page table of one attention layer (ls_kv_cache)."""
+
+    def __init__(self, num_pages: int, page_table: torch.Tensor, page_size: int, num_kv_heads: int,
+                 num_tokens: int, device=None, fill: float | None = None,
+                 k_pool: torch.Tensor | None = None, v_pool: torch.Tensor | None = None):
+        device = torch.device(device) if device is not None else page_table.device
+        shape = (num_pages, num_kv_heads, page_size, HEAD_DIM)
+        if k_pool is None:
+            k_pool = torch.empty(shape, dtype=torch.bfloat16, device=device)
+            v_pool = torch.empty(shape, dtype=torch.bfloat16, device=device)
+            if fill is not None:
+                k_pool.fill_(fill)
+                v_pool.fill_(fill)
+        _check(k_pool, "k_pool", torch.bfloat16, shape)
+        _check(v_pool, "v_pool", torch.bfloat16, shape)
+        _check(page_table, "page_table", torch.int32)
+        self.k_pool, self.v_pool, self.page_table = k_pool, v_pool, page_table
+        self.page_size, self.num_kv_heads, self.num_tokens = page_size, num_kv_heads, num_tokens
+        self.struct = B.ls_kv_cache(k_pool.data_ptr(), v_pool.data_ptr(), page_table.data_ptr(),
+                                    num_pages, page_table.numel(), page_size, num_kv_heads,
+                                    HEAD_DIM, num_tokens)
+
+    @property
+    def device(self):
+        return self.k_pool.device
+
+    def capture(self, k: torch.Tensor, v: torch.Tensor, start_pos: int = 0, stream=None) -> None:
+        n = k.shape[0]
+        _check(k, "k", torch.bfloat16, (n, self.num_kv_heads, HEAD_DIM))
+        _check(v, "v", torch.bfloat16, (n, self.num_kv_heads, HEAD_DIM))
+        B.ls_capture_kv(self.struct, k.data_ptr(), v.data_ptr(), start_pos, n, _stream(stream))
+
+    def validate(self, stream=None) -> None:
+        nbytes = B.ls_validate_page_table_workspace(self.struct)
+        ws = torch.empty(nbytes, dtype=torch.uint8, device=self.device)
+        B.ls_validate_page_table(self.struct, ws.data_ptr(), nbytes, _stream(stream))
+
+
+def replay_fwd(cache: PagedKVCache, q: torch.Tensor, k_resp: torch.Tensor, v_resp: torch.Tensor,
+               softmax_scale: float, num_splits: int, o: torch.Tensor | None = None,
+               lse: torch.Tensor | None = None, stream=None):
+    R, hq, _ = q.shape
+    _check(q, "q", torch.bfloat16, (R, hq, HEAD_DIM))
+    _check(k_resp, "k_resp", torch.bfloat16, (R, cache.num_kv_heads, HEAD_DIM))
+    _check(v_resp, "v_resp", torch.bfloat16, (R, cache.num_kv_heads, HEAD_DIM))
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((R, hq), dtype=torch.float32, device=q.device)
+    _check(o, "o", torch.bfloat16, q.shape)
+    _check(lse, "lse", torch.float32, (R, hq))
+    nbytes = B.ls_replay_attn_fwd_workspace(cache.struct, R, hq, num_splits)
+    ws = workspace(nbytes, q.device, "fwd")
+    B.ls_replay_attn_fwd(cache.struct, q.data_ptr(), k_resp.data_ptr(), v_resp.data_ptr(), R, hq,
+                         softmax_scale, num_splits, o.data_ptr(), lse.data_ptr(), ws.data_ptr(),
+                         ws.numel(), _stream(stream))
+    return o, lse
+
+
+def replay_bwd(cache: PagedKVCache, q, k_resp, v_resp, o, lse, d_o, softmax_scale: float,
+               num_splits: int, dq=None, dk=None, dv=None, accumulate: bool = False, stream=None):
+    R, hq, _ = q.shape
+    hkv = cache.num_kv_heads
+    for t, n in ((q, "q"), (o, "o"), (d_o, "d_o")):
+        _check(t, n, torch.bfloat16, (R, hq, HEAD_DIM))
+    _check(k_resp, "k_resp", torch.bfloat16, (R, hkv, HEAD_DIM))
+    _check(v_resp, "v_resp", torch.bfloat16, (R, hkv, HEAD_DIM))
+    _check(lse, "lse", torch.float32, (R, hq))
+    if dq is None:
+        dq = torch.empty((R, hq, HEAD_DIM), dtype=torch.float32, device=q.device)
+    if dk is None:
+        dk = torch.empty((R, hkv, HEAD_DIM), dtype=torch.float32, device=q.device)
+    if dv is None:
+        dv = torch.empty((R, hkv, HEAD_DIM), dtype=torch.float32, device=q.device)
+    _check(dq, "dq", torch.float32, (R, hq, HEAD_DIM))
+    _check(dk, "dk", torch.float32, (R, hkv, HEAD_DIM))
+    _check(dv, "dv", torch.float32, (R, hkv, HEAD_DIM))
+    nbytes = B.ls_replay_attn_bwd_workspace(cache.struct, R, hq, num_splits)
+    ws = workspace(nbytes, q.device, "bwd")
+    B.ls_replay_attn_bwd(cache.struct, q.data_ptr(), k_resp.data_ptr(), v_resp.data_ptr(),
+                         o.data_ptr(), lse.data_ptr(), d_o.data_ptr(), R, hq, softmax_scale,
+                         num_splits, int(accumulate), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                         ws.data_ptr(), ws.numel(), _stream(stream))
+    return dq, dk, dv
+
+
+def grpo_loss_fwd_bwd(logits: torch.Tensor, targets: torch.Tensor, logp_old: torch.Tensor,
+                      rewards: torch.Tensor, resp_lens: torch.Tensor, member_begin: int,
+                      member_end: int, eps: float, adv_eps: float = 1e-6, std_ddof: int = 1,
+                      loss: torch.Tensor | None = None, accumulate: bool = False,
+                      dlogits: torch.Tensor | None = None, logp_out: torch.Tensor | None = None,
+                      stats: torch.Tensor | None = None, stream=None):
+    """Returns (loss[1], dlogits, logp[T], stats[4]); loss accumulates when asked."""
+    T, V = logits.shape
+    if logits.dtype == torch.bfloat16:
+        dt = B.LS_BF16
+    elif logits.dtype == torch.float32:
+        dt = B.LS_FP32
+    else:
+        raise ValueError("logits must be bf16 or fp32")
+    _check(logits, "logits", logits.dtype)
+    _check(targets, "targets", torch.int32, (T,))
+    _check(logp_old, "logp_old", torch.float32, (T,))
+    G = rewards.numel()
+    _check(rewards, "rewards", torch.float32, (G,))
+    _check(resp_lens, "resp_lens", torch.int32, (G,))
+    dev = logits.device
+    if loss is None:
+        loss = torch.zeros(1, dtype=torch.float32, device=dev)
+    if dlogits is None:
+        dlogits = torch.empty_like(logits)
+    if logp_out is None:
+        logp_out = torch.empty(T, dtype=torch.float32, device=dev)
+    if stats is None:
+        stats = torch.empty(4, dtype=torch.float32, device=dev)
+    _check(dlogits, "dlogits", logits.dtype, (T, V))
+    nbytes = B.ls_grpo_workspace(T, G)
+    ws = workspace(nbytes, dev, "grpo")
+    B.ls_grpo_loss_fwd_bwd(logits.data_ptr(), dt, T, V, targets.data_ptr(), logp_old.data_ptr(),
+                           rewards.data_ptr(), resp_lens.data_ptr(), G, member_begin, member_end,
+                           eps, adv_eps, std_ddof, int(accumulate), loss.data_ptr(),
+                           dlogits.data_ptr(), logp_out.data_ptr(), stats.data_ptr(),
+                           ws.data_ptr(), ws.numel(), _stream(stream))
+    return loss, dlogits, logp_out, stats
+
+
+def last_device_error(stream=None) -> int:
+    return B.ls_last_device_error(_stream(stream))
