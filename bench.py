@@ -28,7 +28,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "replay attn fwd+bwd TFLOP/s & prompt-KV GB/s at P=2.1M; GRPO loss tokens/s"
-WORKLOAD = "p2m"
+WORKLOAD = "p2m"          # the configuration the metric is quoted on (P = 2,097,152)
 D = 128
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
@@ -148,10 +148,10 @@ def run_ours(args, rank: int, world: int, local_rank: int):
 
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
-    w = syn.WORKLOADS[WORKLOAD]
+    w = syn.WORKLOADS[args.workload]
     G = w.G if args.members is None else args.members
     R = w.R[0]
-    seed = syn.seed_of(WORKLOAD) + 1000 * rank
+    seed = syn.seed_of(args.workload) + 1000 * rank
     scale = D ** -0.5
     stream = torch.cuda.current_stream()
 
@@ -213,19 +213,11 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                 m.append(ev())
         return m
 
-    # kernel launches of one step (CUPTI via the torch profiler; 0 if unavailable)
-    launches = None
-    try:
-        from torch.profiler import ProfilerActivity, profile
-        with profile(activities=[ProfilerActivity.CUDA]) as prof:
-            step()
-            torch.cuda.synchronize()
-        names = [e.name for e in prof.events() if getattr(e, "device_type", None) is not None
-                 and str(e.device_type).endswith("CUDA")]
-        ours = [n for n in names if any(k in n for k in ("replay", "capture_kv", "grpo", "bwd_"))]
-        launches = len(ours) if ours else None
-    except Exception:
-        launches = None
+    # kernel launches of one step, as counted by the library itself
+    n0 = B.ls_kernel_launches()
+    step()
+    torch.cuda.synchronize()
+    launches = B.ls_kernel_launches() - n0
 
     for _ in range(args.warmup):
         step()
@@ -354,12 +346,15 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded; shapes of the pages' 2,097,152-position runs)",
-        "config": {"workload": "P=2,097,152 prompt positions, Hq=24, Hkv=4, d=128, 256-token "
-                               "pages shuffled, 256 KV splits; G=8 serial replays R=4096; GRPO "
-                               "V=151,936 bf16 logits",
-                   "members": G, "l2": "inputs larger than L2 (prompt KV 4.29 GB per pass)"},
+        "config": {"workload": f"{args.workload}: P={w.P:,} prompt positions, Hq={w.hq}, "
+                               f"Hkv={w.hkv}, d=128, {w.page_size}-token pages shuffled, "
+                               f"{w.num_splits} KV splits; G={G} serial replays R={R}; GRPO "
+                               f"V={w.vocab:,} {w.logits_dtype} logits",
+                   "members": G,
+                   "l2": f"inputs larger than L2 (prompt KV {prompt_kv_bytes(w.P, w.hkv)/1e9:.2f} "
+                         f"GB per pass)"},
         "components": comps, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-        "gpu_launches": launches * K if launches is not None else None,
+        "gpu_launches": launches * K,
         "clocks": clk.summary(),
     }
     if rank == 0:
@@ -469,6 +464,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--members", type=int, default=None, help="replay fewer members (debug)")
+    ap.add_argument("--workload", default=WORKLOAD,
+                    help="p2m (default, the metric's configuration); smaller ones for profiling")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)

@@ -112,6 +112,7 @@ ls_status ls_capture_kv(const ls_kv_cache* cache, const void* k, const void* v,
  * own keys/values); o: bf16 [R][Hq][128] (round-to-nearest-even); lse: fp32 [R][Hq].
  * num_splits (>= 1) cuts the prompt into that many contiguous ranges of 128-token
  * tiles; the result does not depend on it beyond rounding.  Hq % num_kv_heads == 0.
+ * softmax_scale must be finite and > 0 (typically 1/sqrt(128)).
  * R == 0 is a no-op.  P == 0 is plain causal attention of the response. */
 ls_status ls_replay_attn_fwd_workspace(const ls_kv_cache* cache, int R, int Hq,
                                        int num_splits, size_t* bytes);
@@ -188,6 +189,10 @@ ls_status ls_validate_page_table_workspace(const ls_kv_cache* cache, size_t* byt
 ls_status ls_last_device_error(ls_stream_t stream);
 
 const char* ls_status_string(ls_status status);
+
+/* Diagnostic: number of kernel launches this library has issued in the process (all
+ * devices), e.g. to count the launches of one step. */
+uint64_t ls_kernel_launches(void);
 
 #ifdef __cplusplus
 }

@@ -23,7 +23,7 @@ EXPORTED = (
     "ls_capture_kv", "ls_replay_attn_fwd_workspace", "ls_replay_attn_fwd",
     "ls_replay_attn_bwd_workspace", "ls_replay_attn_bwd", "ls_grpo_workspace",
     "ls_grpo_loss_fwd_bwd", "ls_validate_page_table", "ls_validate_page_table_workspace",
-    "ls_last_device_error", "ls_status_string",
+    "ls_last_device_error", "ls_status_string", "ls_kernel_launches",
 )
 
 
@@ -76,6 +76,8 @@ def lib() -> C.CDLL:
             f.argtypes = args
             f.restype = C.c_int
         l.ls_status_string.restype = C.c_char_p
+        l.ls_kernel_launches.argtypes = []
+        l.ls_kernel_launches.restype = C.c_uint64
         _lib = l
     return _lib
 
@@ -150,6 +152,11 @@ def ls_validate_page_table(cache: ls_kv_cache, workspace: int, workspace_bytes: 
                            stream: int = 0) -> None:
     _ok("ls_validate_page_table",
         lib().ls_validate_page_table(C.byref(cache), workspace, workspace_bytes, stream))
+
+
+def ls_kernel_launches() -> int:
+    """Kernel launches issued by the library so far in this process."""
+    return lib().ls_kernel_launches()
 
 
 def ls_last_device_error(stream: int = 0) -> int:

@@ -84,6 +84,7 @@ cudaError_t ls_launch_capture(const void* k, const void* v, void* k_pool, void* 
   capture_kv_kernel<<<(unsigned)blocks, 256, 0, st>>>(
       static_cast<const uint4*>(k), static_cast<const uint4*>(v), static_cast<uint4*>(k_pool),
       static_cast<uint4*>(v_pool), page_table, num_pages, ps_log2, hkv, start_pos, n, err);
+  ls_note_launch();
   return cudaGetLastError();
 }
 
@@ -96,5 +97,6 @@ cudaError_t ls_launch_validate_pages(const int32_t* page_table, int32_t num_logi
   if (blocks > 1024) blocks = 1024;
   if (blocks < 1) blocks = 1;
   validate_pages_kernel<<<blocks, 256, 0, st>>>(page_table, num_logical, num_pages, seen, err);
+  ls_note_launch();
   return cudaGetLastError();
 }

@@ -137,6 +137,7 @@ __device__ __forceinline__ void ms_add(MS& a, const float* x2, int n) {
     a.s *= fast_exp2(a.m - mx);
     a.m = mx;
   }
+  if (a.m == -INFINITY) return;  // only -inf logits so far: they add nothing
   for (int i = 0; i < n; ++i) a.s += fast_exp2(x2[i] - a.m);
 }
 
@@ -350,6 +351,7 @@ size_t ls_grpo_ws_bytes(int64_t T, int G) { return ws_layout(T, G).total; }
 cudaError_t ls_launch_grpo(const LsGrpoArgs& a, int num_sms, cudaStream_t st) {
   grpo_prep<<<1, 32, 0, st>>>(a.rewards, a.resp_lens, a.G, a.member_begin, a.member_end,
                               a.std_ddof, a.adv_eps, a.T, a.workspace, a.err);
+  ls_note_launch();
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (a.T > 0) {
@@ -360,16 +362,19 @@ cudaError_t ls_launch_grpo(const LsGrpoArgs& a, int num_sms, cudaStream_t st) {
           static_cast<const __nv_bfloat16*>(a.logits), a.T, a.V, a.targets, a.logp_old, a.G,
           a.member_begin, a.member_end, a.eps, static_cast<__nv_bfloat16*>(a.dlogits),
           a.logp_out, a.workspace, a.err);
+  ls_note_launch();
     } else {
       grpo_rows<float><<<(unsigned)grid, kRowThreads, 0, st>>>(
           static_cast<const float*>(a.logits), a.T, a.V, a.targets, a.logp_old, a.G,
           a.member_begin, a.member_end, a.eps, static_cast<float*>(a.dlogits), a.logp_out,
           a.workspace, a.err);
+  ls_note_launch();
     }
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
   grpo_final<<<1, 1024, 0, st>>>(a.T, a.G, a.member_begin, a.member_end, a.accumulate_loss,
                                  a.loss, a.stats, a.workspace);
+  ls_note_launch();
   return cudaGetLastError();
 }

@@ -1,6 +1,7 @@
 // ls_api.cu -- the extern "C" entry points of include/longstraw.h: argument checks,
 // workspace layout, the per-device error word and the kernel launches.
 #include <math.h>
+#include <atomic>
 #include <mutex>
 
 #include "../../include/longstraw.h"
@@ -9,6 +10,12 @@
 // One error word per device (module globals are instantiated per device).  Kernels
 // OR LS_DEVERR_* bits into it; ls_last_device_error reads and clears it.
 __device__ uint32_t g_ls_device_error;
+
+namespace {
+std::atomic<uint64_t> g_launches{0};
+}  // namespace
+
+void ls_note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
 namespace {
 
@@ -143,6 +150,8 @@ LsAttnArgs attn_args(const ls_kv_cache* c, const void* q, const void* kr, const 
 
 extern "C" {
 
+uint64_t ls_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
+
 const char* ls_status_string(ls_status s) {
   switch (s) {
     case LS_OK: return "ok";
@@ -191,7 +200,7 @@ ls_status ls_replay_attn_fwd(const ls_kv_cache* cache, const void* q, const void
                              ls_stream_t stream) {
   ls_status s = check_replay(cache, R, Hq, num_splits);
   if (s != LS_OK) return s;
-  if (!isfinite(softmax_scale)) return LS_ERR_INVALID_ARG;
+  if (!isfinite(softmax_scale) || !(softmax_scale > 0.f)) return LS_ERR_INVALID_ARG;
   if (R == 0) return LS_OK;
   const void* ptrs[] = {q, k_resp, v_resp, o, lse};
   for (const void* p : ptrs)
@@ -232,7 +241,7 @@ ls_status ls_replay_attn_bwd(const ls_kv_cache* cache, const void* q, const void
                              size_t workspace_bytes, ls_stream_t stream) {
   ls_status s = check_replay(cache, R, Hq, num_splits);
   if (s != LS_OK) return s;
-  if (!isfinite(softmax_scale)) return LS_ERR_INVALID_ARG;
+  if (!isfinite(softmax_scale) || !(softmax_scale > 0.f)) return LS_ERR_INVALID_ARG;
   if (R == 0) return LS_OK;
   const void* ptrs[] = {q, k_resp, v_resp, o, lse, d_o, dq, dk_resp, dv_resp};
   for (const void* p : ptrs)

@@ -11,6 +11,9 @@
 #define LS_DEVERR_CHECK 1u    // a device-side argument check failed
 #define LS_DEVERR_TIMEOUT 2u  // a pipeline wait exceeded its time limit
 
+// Counts every kernel launch the library makes (reported by ls_kernel_launches).
+void ls_note_launch();
+
 // Problem description shared by the replay-attention kernels (device pointers).
 struct LsAttnArgs {
   const void* k_pool;        // bf16 [num_pages][hkv][ps][128]

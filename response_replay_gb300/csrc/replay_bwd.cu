@@ -452,16 +452,19 @@ cudaError_t ls_launch_replay_bwd(const LsAttnArgs& a, const LsSched& sc, const L
   if (blocks > num_sms * 16) blocks = num_sms * 16;
   bwd_delta<<<blocks, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(b.o),
                                     static_cast<const __nv_bfloat16*>(b.d_o), rows, b.delta);
+  ls_note_launch();
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDqSmem);
   if (e != cudaSuccess) return e;
   bwd_dq_kernel<<<sc.ctas, kThreads, kDqSmem, st>>>(a, sc, b);
+  ls_note_launch();
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int64_t tail_units = sc.units - (int64_t)sc.waves * sc.ctas;
   if (tail_units > 0) {
     bwd_dq_combine<<<(unsigned)tail_units, kD, 0, st>>>(a, sc, b);
+  ls_note_launch();
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
@@ -469,5 +472,6 @@ cudaError_t ls_launch_replay_bwd(const LsAttnArgs& a, const LsSched& sc, const L
   if (e != cudaSuccess) return e;
   const int nKB = (a.R + kBN - 1) / kBN;
   bwd_dkdv_kernel<<<a.hkv * nKB, kThreads, kKvSmem, st>>>(a, b);
+  ls_note_launch();
   return cudaGetLastError();
 }

@@ -107,7 +107,10 @@ replay_fwd_kernel(const LsAttnArgs a, const LsSched sc, const LsFwdOut out) {
   bool first, last, complete;
   uint32_t qa[8][4];                  // Q fragments of this warp's 16 rows
   float o[16][4];
-  float m[2], l[2];
+  // Row max (log2 domain) and row sum.  The sum runs over up to millions of keys per
+  // thread, so it is kept as an unevaluated pair l + lcomp (Fast2Sum per tile): a plain
+  // fp32 accumulator loses ~1e-3 relative at P = 2M.
+  float m[2], l[2], lcomp[2];
   Unit un{0, 0, 0};
   while (walk.next(&u, &s, &first, &last, &complete)) {
     if (first) {
@@ -118,7 +121,7 @@ replay_fwd_kernel(const LsAttnArgs a, const LsSched sc, const LsFwdOut out) {
 #pragma unroll
       for (int j = 0; j < 16; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
       m[0] = m[1] = -INFINITY;
-      l[0] = l[1] = 0.f;
+      l[0] = l[1] = lcomp[0] = lcomp[1] = 0.f;
     }
     // KV tile range of this item
     const bool response = (s == sc.nsplit);
@@ -191,20 +194,28 @@ replay_fwd_kernel(const LsAttnArgs a, const LsSched sc, const LsFwdOut out) {
         alpha[r] = fast_exp2(m[r] - mn);
         m[r] = mn;
         l[r] *= alpha[r];
+        lcomp[r] *= alpha[r];
       }
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
         o[j][0] *= alpha[0]; o[j][1] *= alpha[0];
         o[j][2] *= alpha[1]; o[j][3] *= alpha[1];
       }
+      float ls[2] = {0.f, 0.f};
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const float p = fast_exp2(sacc[j][e] - m[e >> 1]);
           sacc[j][e] = p;
-          l[e >> 1] += p;
+          ls[e >> 1] += p;
         }
+      }
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {   // Fast2Sum: l + lcomp += ls
+        const float t = l[r] + ls[r];
+        lcomp[r] += (l[r] - t) + ls[r];
+        l[r] = t;
       }
       // O += P V
 #pragma unroll
@@ -231,7 +242,8 @@ replay_fwd_kernel(const LsAttnArgs a, const LsSched sc, const LsFwdOut out) {
       float lt[2], lse[2];
 #pragma unroll
       for (int r = 0; r < 2; ++r) {
-        lt[r] = l[r] + __shfl_xor_sync(0xffffffffu, l[r], 1);
+        lt[r] = l[r] + lcomp[r];
+        lt[r] += __shfl_xor_sync(0xffffffffu, lt[r], 1);
         lt[r] += __shfl_xor_sync(0xffffffffu, lt[r], 2);
         lse[r] = (m[r] + log2f(lt[r])) * kLn2;
       }
@@ -319,11 +331,13 @@ cudaError_t ls_launch_replay_fwd(const LsAttnArgs& a, const LsSched& sc, const L
                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e0 != cudaSuccess) return e0;
   replay_fwd_kernel<<<sc.ctas, kThreads, kSmem, st>>>(a, sc, out);
+  ls_note_launch();
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int64_t tail_units = sc.units - (int64_t)sc.waves * sc.ctas;
   if (tail_units > 0) {
     replay_fwd_combine<<<(unsigned)tail_units, kD, 0, st>>>(a, sc, out);
+  ls_note_launch();
     e = cudaGetLastError();
   }
   return e;
