@@ -177,6 +177,27 @@ ls_status ls_grpo_loss_fwd_bwd(const void* logits, ls_dtype dtype, int64_t T, in
                                float* logp_out, float* stats, void* workspace,
                                size_t workspace_bytes, ls_stream_t stream);
 
+/* ls_grpo_loss_fwd_bwd_noalloc: the same computation as ls_grpo_loss_fwd_bwd, for
+ * callers that cannot provide or allocate device memory at the point of the call (for
+ * example a training loop whose host framework plans all device memory up front and
+ * forbids new allocations mid-step).  The paper has no counterpart: this is an
+ * interface convenience of this library.  Instead of a caller workspace it uses one
+ * fixed scratch array inside the library's device image (4.125 MiB per device, held
+ * until process exit); it calls no allocator.  Limits: T <= 262,144 tokens and
+ * G <= 1,024 members, otherwise LS_ERR_WORKSPACE is returned and nothing is launched.
+ * The first call on a device looks up the array's device address (a runtime query,
+ * no allocation); make that first call before any stream capture.  All calls share
+ * the array: calls whose kernels could overlap on the GPU race, so order them (one
+ * stream, or events).  Nothing in the array needs to start at zero.  Arguments and
+ * outputs otherwise as ls_grpo_loss_fwd_bwd. */
+ls_status ls_grpo_loss_fwd_bwd_noalloc(const void* logits, ls_dtype dtype, int64_t T, int V,
+                                       const int32_t* targets, const float* logp_old,
+                                       const float* rewards, const int32_t* resp_lens, int G,
+                                       int member_begin, int member_end, float eps,
+                                       float adv_eps, int std_ddof, int accumulate_loss,
+                                       float* loss, void* dlogits, float* logp_out,
+                                       float* stats, ls_stream_t stream);
+
 /* ---------------------------------------------------------------- checks
  * ls_validate_page_table: enqueue a check that every entry of the page table covering
  * the cache's num_tokens lies in [0, num_pages) and that no physical page is used

@@ -24,6 +24,7 @@ EXPORTED = (
     "ls_replay_attn_bwd_workspace", "ls_replay_attn_bwd", "ls_grpo_workspace",
     "ls_grpo_loss_fwd_bwd", "ls_validate_page_table", "ls_validate_page_table_workspace",
     "ls_last_device_error", "ls_status_string", "ls_kernel_launches",
+    "ls_grpo_loss_fwd_bwd_noalloc",
 )
 
 
@@ -66,6 +67,8 @@ def lib() -> C.CDLL:
             "ls_grpo_workspace": [i64, i32, szp],
             "ls_grpo_loss_fwd_bwd": [P, i32, i64, i32, P, P, P, P, i32, i32, i32, f32, f32, i32,
                                      i32, P, P, P, P, P, sz, P],
+            "ls_grpo_loss_fwd_bwd_noalloc": [P, i32, i64, i32, P, P, P, P, i32, i32, i32, f32,
+                                             f32, i32, i32, P, P, P, P, P],
             "ls_validate_page_table": [cache, P, sz, P],
             "ls_validate_page_table_workspace": [cache, szp],
             "ls_last_device_error": [P],
@@ -142,6 +145,21 @@ def ls_grpo_loss_fwd_bwd(logits: int, dtype: int, T: int, V: int, targets: int, 
                                    member_begin, member_end, eps, adv_eps, std_ddof,
                                    accumulate_loss, loss, dlogits, logp_out, stats, workspace,
                                    workspace_bytes, stream))
+
+
+def ls_grpo_loss_fwd_bwd_noalloc(logits: int, dtype: int, T: int, V: int, targets: int,
+                                 logp_old: int, rewards: int, resp_lens: int, G: int,
+                                 member_begin: int, member_end: int, eps: float, adv_eps: float,
+                                 std_ddof: int, accumulate_loss: int, loss: int, dlogits: int,
+                                 logp_out: int | None, stats: int | None,
+                                 stream: int = 0) -> None:
+    """The GRPO loss without a caller workspace (library-owned fixed scratch; limits
+    T <= 262,144 and G <= 1,024; calls must not overlap on the GPU)."""
+    _ok("ls_grpo_loss_fwd_bwd_noalloc",
+        lib().ls_grpo_loss_fwd_bwd_noalloc(logits, dtype, T, V, targets, logp_old, rewards,
+                                           resp_lens, G, member_begin, member_end, eps, adv_eps,
+                                           std_ddof, accumulate_loss, loss, dlogits, logp_out,
+                                           stats, stream))
 
 
 def ls_validate_page_table_workspace(cache: ls_kv_cache) -> int:
