@@ -72,6 +72,9 @@ cudaError_t ls_launch_validate_pages(const int32_t* page_table, int32_t num_logi
 cudaError_t ls_launch_replay_fwd(const LsAttnArgs& a, const LsSched& sc, const LsFwdOut& out,
                                  cudaStream_t st);
 
+cudaError_t ls_launch_bwd_dq(const LsAttnArgs& a, const LsSched& sc, const LsBwdIn& b,
+                             cudaStream_t st);
+
 cudaError_t ls_launch_replay_bwd(const LsAttnArgs& a, const LsSched& sc, const LsBwdIn& b,
                                  int num_sms, cudaStream_t st);
 

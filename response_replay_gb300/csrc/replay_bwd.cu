@@ -10,14 +10,14 @@
 //
 // Launches:
 //   bwd_delta     D = rowsum(dO * O) per (t, h), one warp per row.
-//   bwd_dq        q-stationary, same units / schedule as the forward: the Q and dO
-//                 tiles of a unit stay in shared memory while 64-key K/V tiles stream
-//                 past; S and dP are recomputed, dS = P (dP - D), dQ += dS K.
-//   bwd_dq_combine  fixed-order sum of split partials for tail units.
+//   dQ            replay_bwd_dq_tc.cu: q-stationary tcgen05 kernel over prompt and
+//                 response keys, same schedule as the forward, plus its split combine.
 //   bwd_dkdv      key-stationary over response keys only: a CTA owns 64 response keys
 //                 of one kv head and walks the query blocks t >= j of every query
-//                 head in the group; dV += P^T dO, dK += dS^T Q.
-// All MMAs are mma.sync m16n8k16 (bf16 in, fp32 accumulate).  Deterministic: no atomics.
+//                 head in the group; dV += P^T dO, dK += dS^T Q.  This part is the
+//                 causal R x R triangle (under 0.2% of the work at P = 2M, R = 4096)
+//                 and uses warp-level mma.sync m16n8k16 (bf16 in, fp32 accumulate).
+// Deterministic: no atomics.
 #include <math.h>
 
 #include "ls_device.cuh"
@@ -32,18 +32,6 @@ constexpr int kThreads = 128;
 constexpr int kTileBytes = 64 * kD * 2;
 constexpr float kLog2e = 1.4426950408889634f;
 
-struct Unit {
-  int h, kvh, t0;
-};
-__device__ __forceinline__ Unit decode_unit(const LsAttnArgs& a, int u) {
-  const int nTB = (a.R + kBM - 1) / kBM;
-  Unit x;
-  x.h = u / nTB;
-  x.t0 = (u % nTB) * kBM;
-  x.kvh = x.h / a.g;
-  return x;
-}
-
 // 64 rows of bf16 [row][128] (row stride `pitch` elements) into a swizzled tile;
 // rows >= nvalid are zero-filled.
 __device__ __forceinline__ void load_rows(const __nv_bfloat16* base, int64_t pitch, int nvalid,
@@ -54,39 +42,6 @@ __device__ __forceinline__ void load_rows(const __nv_bfloat16* base, int64_t pit
     const int r = i >> 4, c = i & 15;
     const bool ok = r < nvalid;
     cp_async16(dst + swz(r, c), base + (ok ? r * pitch + c * 8 : 0), ok ? 16 : 0);
-  }
-}
-
-__device__ __forceinline__ void load_kv_tile(const LsAttnArgs& a, int kvh, bool response,
-                                             int64_t p0, uint32_t ks, uint32_t vs) {
-  const int64_t ps_mask = (1ll << a.ps_log2) - 1;
-#pragma unroll
-  for (int it = 0; it < (kBN * 16) / kThreads; ++it) {
-    const int i = threadIdx.x + it * kThreads;
-    const int r = i >> 4, c = i & 15;
-    const int64_t p = p0 + r;
-    const __nv_bfloat16* ksrc = static_cast<const __nv_bfloat16*>(a.k_resp);
-    const __nv_bfloat16* vsrc = static_cast<const __nv_bfloat16*>(a.v_resp);
-    int64_t off = 0;
-    uint32_t bytes = 0;
-    if (response) {
-      if (p < a.R) {
-        off = (p * a.hkv + kvh) * kD + c * 8;
-        bytes = 16;
-      }
-    } else if (p < a.P) {
-      const int32_t phys = __ldg(a.page_table + (p >> a.ps_log2));
-      if ((uint32_t)phys < (uint32_t)a.num_pages) {
-        off = ((((int64_t)phys * a.hkv + kvh) << a.ps_log2) + (p & ps_mask)) * kD + c * 8;
-        bytes = 16;
-        ksrc = static_cast<const __nv_bfloat16*>(a.k_pool);
-        vsrc = static_cast<const __nv_bfloat16*>(a.v_pool);
-      } else {
-        ls_report(a.err, LS_DEVERR_CHECK);
-      }
-    }
-    cp_async16(ks + swz(r, c), ksrc + off, bytes);
-    cp_async16(vs + swz(r, c), vsrc + off, bytes);
   }
 }
 
@@ -108,184 +63,6 @@ __global__ void bwd_delta(const __nv_bfloat16* __restrict__ o, const __nv_bfloat
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
     if (lane == 0) delta[r] = s;
-  }
-}
-
-// ------------------------------------------------------------------ dQ
-constexpr int kDqSmem = 6 * kTileBytes;  // Q, dO, 2 x (K, V)
-
-__global__ void __launch_bounds__(kThreads, 2)
-bwd_dq_kernel(const LsAttnArgs a, const LsSched sc, const LsBwdIn b) {
-  extern __shared__ __align__(1024) uint8_t smem[];
-  const uint32_t qs = smem_u32(smem), dos = qs + kTileBytes;
-  const uint32_t ks[2] = {qs + 2 * kTileBytes, qs + 4 * kTileBytes};
-  const uint32_t vs[2] = {qs + 3 * kTileBytes, qs + 5 * kTileBytes};
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int lr = lane >> 2, lc = (lane & 3) * 2;
-
-  LsWalk walk(sc, blockIdx.x);
-  int u, s;
-  bool first, last, complete;
-  float dq[16][4];
-  float lse2[2], dd[2];
-  Unit un{0, 0, 0};
-  while (walk.next(&u, &s, &first, &last, &complete)) {
-    if (first) {
-      un = decode_unit(a, u);
-      __syncthreads();
-      const int nv = a.R - un.t0 < kBM ? a.R - un.t0 : kBM;
-      load_rows(static_cast<const __nv_bfloat16*>(a.q) + ((int64_t)un.t0 * a.hq + un.h) * kD,
-                (int64_t)a.hq * kD, nv, qs);
-      load_rows(static_cast<const __nv_bfloat16*>(b.d_o) + ((int64_t)un.t0 * a.hq + un.h) * kD,
-                (int64_t)a.hq * kD, nv, dos);
-      cp_async_commit();
-#pragma unroll
-      for (int j = 0; j < 16; ++j) dq[j][0] = dq[j][1] = dq[j][2] = dq[j][3] = 0.f;
-#pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        const int t = un.t0 + warp * 16 + lr + r * 8;
-        const int64_t row = (int64_t)(t < a.R ? t : a.R - 1) * a.hq + un.h;
-        lse2[r] = b.lse[row] * kLog2e;
-        dd[r] = b.delta[row];
-      }
-    }
-    const bool response = (s == sc.nsplit);
-    int64_t k0, k1;
-    if (response) {
-      k0 = 0;
-      const int64_t qe = (int64_t)un.t0 + kBM;
-      k1 = qe < a.R ? qe : a.R;
-    } else {
-      int t0, t1;
-      sc.split_tiles(s, &t0, &t1);
-      k0 = (int64_t)t0 * kBN;
-      k1 = (int64_t)t1 * kBN;
-      if (k1 > a.P) k1 = a.P;
-    }
-    const int ntile = (int)((k1 - k0 + kBN - 1) / kBN);
-    __syncthreads();
-    if (ntile > 0) load_kv_tile(a, un.kvh, response, k0, ks[0], vs[0]);
-    cp_async_commit();
-    for (int it = 0; it < ntile; ++it) {
-      const int buf = it & 1;
-      if (it + 1 < ntile)
-        load_kv_tile(a, un.kvh, response, k0 + (int64_t)(it + 1) * kBN, ks[buf ^ 1], vs[buf ^ 1]);
-      cp_async_commit();
-      cp_async_wait<1>();
-      __syncthreads();
-      float sacc[8][4], pacc[8][4];
-#pragma unroll
-      for (int j = 0; j < 8; ++j)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) sacc[j][e] = pacc[j][e] = 0.f;
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        uint32_t qa[4], da[4];
-        const uint32_t arow = warp * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
-        ldsm_x4(qs + swz(arow, 2 * kk + (lane >> 4)), qa[0], qa[1], qa[2], qa[3]);
-        ldsm_x4(dos + swz(arow, 2 * kk + (lane >> 4)), da[0], da[1], da[2], da[3]);
-#pragma unroll
-        for (int nn = 0; nn < 4; ++nn) {
-          uint32_t b0, b1, b2, b3;
-          const int brow = nn * 16 + (lane & 7) + (lane >> 4) * 8;
-          const int bch = 2 * kk + ((lane >> 3) & 1);
-          ldsm_x4(ks[buf] + swz(brow, bch), b0, b1, b2, b3);
-          mma16816(sacc[2 * nn], qa, b0, b1);
-          mma16816(sacc[2 * nn + 1], qa, b2, b3);
-          ldsm_x4(vs[buf] + swz(brow, bch), b0, b1, b2, b3);
-          mma16816(pacc[2 * nn], da, b0, b1);
-          mma16816(pacc[2 * nn + 1], da, b2, b3);
-        }
-      }
-      // dS = P (dP - D), P = exp2(s scale log2e - lse log2e), masked keys -> 0
-      const int64_t kt = k0 + (int64_t)it * kBN;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int64_t key = kt + j * 8 + lc + (e & 1);
-          const int row = warp * 16 + lr + (e >> 1) * 8;
-          bool ok;
-          if (response) ok = key <= (int64_t)un.t0 + row && key < a.R;
-          else ok = key < a.P;
-          const float p = ok ? fast_exp2(sacc[j][e] * a.scale_log2 - lse2[e >> 1]) : 0.f;
-          sacc[j][e] = p * (pacc[j][e] - dd[e >> 1]);
-        }
-      }
-      // dQ += dS K
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        uint32_t pa[4];
-        pa[0] = pack_bf16(sacc[2 * kk][0], sacc[2 * kk][1]);
-        pa[1] = pack_bf16(sacc[2 * kk][2], sacc[2 * kk][3]);
-        pa[2] = pack_bf16(sacc[2 * kk + 1][0], sacc[2 * kk + 1][1]);
-        pa[3] = pack_bf16(sacc[2 * kk + 1][2], sacc[2 * kk + 1][3]);
-#pragma unroll
-        for (int dn = 0; dn < 8; ++dn) {
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4_t(ks[buf] + swz(kk * 16 + (lane & 7) + ((lane >> 3) & 1) * 8, 2 * dn + (lane >> 4)),
-                    b0, b1, b2, b3);
-          mma16816(dq[2 * dn], pa, b0, b1);
-          mma16816(dq[2 * dn + 1], pa, b2, b3);
-        }
-      }
-      __syncthreads();
-    }
-    cp_async_wait<0>();
-
-    if (last) {
-      if (complete) {
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-          const int t = un.t0 + warp * 16 + lr + r * 8;
-          if (t < a.R) {
-            float* dst = b.dq + ((int64_t)t * a.hq + un.h) * kD;
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              float2 v = make_float2(dq[j][2 * r] * a.scale, dq[j][2 * r + 1] * a.scale);
-              float2* p = reinterpret_cast<float2*>(dst + j * 8 + lc);
-              if (b.accumulate) {
-                const float2 old = *p;
-                v.x += old.x;
-                v.y += old.y;
-              }
-              *p = v;
-            }
-          }
-        }
-      } else {
-        float* pd = b.part_dq + (int64_t)sc.slot_of(blockIdx.x, u) * kBM * kD;
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-          const int row = warp * 16 + lr + r * 8;
-#pragma unroll
-          for (int j = 0; j < 16; ++j)
-            *reinterpret_cast<float2*>(pd + row * kD + j * 8 + lc) =
-                make_float2(dq[j][2 * r] * a.scale, dq[j][2 * r + 1] * a.scale);
-        }
-      }
-    }
-  }
-}
-
-// Sum the split partials of each tail unit in CTA order; one block per unit.
-__global__ void __launch_bounds__(kD) bwd_dq_combine(const LsAttnArgs a, const LsSched sc,
-                                                     const LsBwdIn b) {
-  const int u = sc.tail_unit0() + blockIdx.x;
-  const int64_t ipu = sc.items_per_unit();
-  const int64_t i0 = (int64_t)(u - sc.tail_unit0()) * ipu;
-  const int c_lo = sc.tail_cta_of(i0), c_hi = sc.tail_cta_of(i0 + ipu - 1);
-  if (c_lo == c_hi) return;
-  const Unit un = decode_unit(a, u);
-  const int col = threadIdx.x;
-  for (int r = 0; r < kBM; ++r) {
-    const int t = un.t0 + r;
-    if (t >= a.R) break;
-    float acc = 0.f;
-    for (int c = c_lo; c <= c_hi; ++c)
-      if (sc.tail_nonempty(c)) acc += b.part_dq[((int64_t)sc.slot_of(c, u) * kBM + r) * kD + col];
-    float* dst = b.dq + ((int64_t)t * a.hq + un.h) * kD + col;
-    *dst = b.accumulate ? *dst + acc : acc;
   }
 }
 
@@ -441,9 +218,6 @@ bwd_dkdv_kernel(const LsAttnArgs a, const LsBwdIn b) {
 
 }  // namespace
 
-int ls_bwd_unit_rows() { return kBM; }
-int ls_bwd_tile() { return kBN; }
-int ls_bwd_ctas_per_sm() { return 2; }
 
 cudaError_t ls_launch_replay_bwd(const LsAttnArgs& a, const LsSched& sc, const LsBwdIn& b,
                                  int num_sms, cudaStream_t st) {
@@ -455,19 +229,8 @@ cudaError_t ls_launch_replay_bwd(const LsAttnArgs& a, const LsSched& sc, const L
   ls_note_launch();
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDqSmem);
+  e = ls_launch_bwd_dq(a, sc, b, st);
   if (e != cudaSuccess) return e;
-  bwd_dq_kernel<<<sc.ctas, kThreads, kDqSmem, st>>>(a, sc, b);
-  ls_note_launch();
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  const int64_t tail_units = sc.units - (int64_t)sc.waves * sc.ctas;
-  if (tail_units > 0) {
-    bwd_dq_combine<<<(unsigned)tail_units, kD, 0, st>>>(a, sc, b);
-  ls_note_launch();
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-  }
   e = cudaFuncSetAttribute(bwd_dkdv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kKvSmem);
   if (e != cudaSuccess) return e;
   const int nKB = (a.R + kBN - 1) / kBN;

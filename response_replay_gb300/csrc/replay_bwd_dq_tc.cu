@@ -1,0 +1,469 @@
+// replay_bwd_dq_tc.cu -- dQ of the replay backward on the 5th-generation tensor cores.
+//
+// With the prompt state stopgrad (LongStraw paper digest, Method, last paragraph),
+// the prompt keys feed only dQ:
+//   P_{t,j} = exp(s_{t,j} - lse_t),  dP_{t,j} = <dO_t, v_j>,  dS = P (dP - D_t),
+//   dq_t = scale * sum_j dS_{t,j} k_j    over every prompt key and response keys j <= t.
+// S and P are recomputed from the forward's LSE (storing P would need ~400 GB at
+// 2M positions); D = <dO, O> comes from bwd_delta.
+//
+// CTA (one per SM, persistent, 12 warps) owns a unit = 128 consecutive response tokens
+// of one query head; Q and dO stay in shared memory while K/V tiles stream past:
+//   warp 0      TMA producer: Q and dO tiles, then K (3-stage ring) and V (2-stage ring)
+//               tiles of 128 keys, prompt tiles gathered page by page.
+//   warp 1      MMA issuer: S = Q K^T (SS, into one of two S buffers), dP = dO V^T (SS),
+//               dQ += dS K (TS: dS from tensor memory, K as an MN-major operand).
+//               Order per tile j: dP(j+1), dQ(j), S(j+2), so the tensor core works on
+//               the next tiles while the softmax warps turn S(j), dP(j) into dS(j).
+//   warps 2-3   idle (complete warpgroup 0)
+//   warps 4-7 / 8-11  two warpgroups split the 128 key columns of each query row (64
+//               each): p = exp2(s scale log2e - lse log2e), ds = p (dp - D), packed as
+//               bf16 pairs over their own S columns; at the end of a unit they read dQ,
+//               scale it and write dq (or a split partial).
+// Tensor memory (512 columns): S0 [0,128) S1 [128,256) dP [256,384) dQ [384,512).
+// dS of warpgroup c lives in S columns [64c, 64c+32) of the current S buffer.
+#include <math.h>
+
+#include "ls_device.cuh"
+#include "ls_internal.h"
+#include "ls_tiles.cuh"
+#include "ls_tmap.h"
+#include "ls_umma.cuh"
+
+namespace {
+
+using namespace umma;
+
+constexpr int kD = 128;
+constexpr int kTile = 128;
+constexpr int kUnitRows = 128;
+constexpr int kKStages = 3, kVStages = 2;
+constexpr int kThreads = 384;
+constexpr uint32_t kTileBytes = kTile * kD * 2;
+constexpr uint32_t kHalfBytes = kTileBytes / 2;
+constexpr uint32_t kOffQ = 0, kOffDO = kTileBytes;
+constexpr uint32_t kOffK = 2 * kTileBytes;
+constexpr uint32_t kOffV = kOffK + kKStages * kTileBytes;
+constexpr uint32_t kOffBar = kOffV + kVStages * kTileBytes;
+constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;
+constexpr float kLog2e = 1.4426950408889634f;
+
+enum {
+  B_K_FULL = 0,
+  B_K_EMPTY = B_K_FULL + kKStages,
+  B_V_FULL = B_K_EMPTY + kKStages,
+  B_V_EMPTY = B_V_FULL + kVStages,
+  B_Q_FULL = B_V_EMPTY + kVStages,
+  B_Q_EMPTY,
+  B_S_FULL,  // 2
+  B_DP_FULL = B_S_FULL + 2,
+  B_DS_FULL,
+  B_DQ_DONE,
+  B_DONE,
+  B_COUNT
+};
+static_assert(B_COUNT * 8 + 16 <= 256, "barrier area");
+
+struct TmapSet {
+  CUtensorMap q, d_o, kp, vp, kr, vr;
+};
+
+using DqCursor = TileCursor<kUnitRows, kTile>;
+
+__device__ __forceinline__ uint32_t bar_addr(uint32_t base, int i) { return base + kOffBar + 8 * i; }
+
+__global__ void __launch_bounds__(kThreads, 1)
+bwd_dq_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a, const LsSched sc,
+                 const LsBwdIn b) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + kOffBar + B_COUNT * 8);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffBar + B_COUNT * 8 + 4);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  if (tid == 0) {
+    for (int i = 0; i < kKStages; ++i) {
+      mbar_init(bar_addr(sbase, B_K_FULL + i), 1);
+      mbar_init(bar_addr(sbase, B_K_EMPTY + i), 1);
+    }
+    for (int i = 0; i < kVStages; ++i) {
+      mbar_init(bar_addr(sbase, B_V_FULL + i), 1);
+      mbar_init(bar_addr(sbase, B_V_EMPTY + i), 1);
+    }
+    mbar_init(bar_addr(sbase, B_Q_FULL), 1);
+    mbar_init(bar_addr(sbase, B_Q_EMPTY), 1);
+    mbar_init(bar_addr(sbase, B_S_FULL + 0), 1);
+    mbar_init(bar_addr(sbase, B_S_FULL + 1), 1);
+    mbar_init(bar_addr(sbase, B_DP_FULL), 1);
+    mbar_init(bar_addr(sbase, B_DS_FULL), 256);
+    mbar_init(bar_addr(sbase, B_DQ_DONE), 1);
+    mbar_init(bar_addr(sbase, B_DONE), 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(const_cast<uint32_t*>(tmem_slot)), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  auto fail = [&](void) {
+    ls_report(a.err, LS_DEVERR_TIMEOUT);
+    *abort_flag = 1;
+  };
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tm.q);
+      tma_prefetch_desc(&tm.d_o);
+      tma_prefetch_desc(&tm.kp);
+      tma_prefetch_desc(&tm.vp);
+      tma_prefetch_desc(&tm.kr);
+      tma_prefetch_desc(&tm.vr);
+      DqCursor cur(sc, blockIdx.x, a.R, a.g);
+      TileRec r;
+      uint32_t kc = 0, vc = 0, units = 0;
+      const int32_t ps = 1 << a.ps_log2;
+      const int32_t box_rows = ps < kTile ? ps : kTile;
+      const int32_t pool_rows = a.num_pages * a.hkv * ps;
+      bool ok = true;
+      while (ok && cur.next(&r)) {
+        if (r.first_of_unit) {
+          if (units > 0 && !mbar_wait(bar_addr(sbase, B_Q_EMPTY), (units - 1) & 1)) { fail(); break; }
+          const uint32_t qb = bar_addr(sbase, B_Q_FULL);
+          mbar_expect_tx(qb, 2 * kTileBytes);
+          for (int hf = 0; hf < 2; ++hf) {
+            tma_load_3d(sbase + kOffQ + hf * kHalfBytes, &tm.q, hf * 64, r.h, r.t0, qb);
+            tma_load_3d(sbase + kOffDO + hf * kHalfBytes, &tm.d_o, hf * 64, r.h, r.t0, qb);
+          }
+          ++units;
+        }
+        for (int kv = 0; kv < 2; ++kv) {
+          const uint32_t cnt = kv == 0 ? kc : vc;
+          const int nst = kv == 0 ? kKStages : kVStages;
+          const uint32_t st = cnt % nst;
+          const int be = (kv == 0 ? B_K_EMPTY : B_V_EMPTY) + st;
+          const int bf = (kv == 0 ? B_K_FULL : B_V_FULL) + st;
+          if (!mbar_wait(bar_addr(sbase, be), ((cnt / nst) & 1) ^ 1)) { fail(); ok = false; break; }
+          if (*abort_flag) { ok = false; break; }
+          const uint32_t fb = bar_addr(sbase, bf);
+          const uint32_t dst = sbase + (kv == 0 ? kOffK : kOffV) + st * kTileBytes;
+          mbar_expect_tx(fb, kTileBytes);
+          if (r.resp) {
+            const void* map = kv == 0 ? (const void*)&tm.kr : (const void*)&tm.vr;
+            for (int hf = 0; hf < 2; ++hf) tma_load_3d(dst + hf * kHalfBytes, map, hf * 64, r.kvh, r.key0, fb);
+          } else {
+            const void* map = kv == 0 ? (const void*)&tm.kp : (const void*)&tm.vp;
+            for (int bb = 0; bb < kTile / box_rows; ++bb) {
+              const int32_t pos = r.key0 + bb * box_rows;
+              int32_t y = pool_rows;
+              if (pos < a.P) {
+                const int32_t phys = __ldg(a.page_table + (pos >> a.ps_log2));
+                if ((uint32_t)phys < (uint32_t)a.num_pages)
+                  y = (phys * a.hkv + r.kvh) * ps + (pos & (ps - 1));
+                else
+                  ls_report(a.err, LS_DEVERR_CHECK);
+              }
+              for (int hf = 0; hf < 2; ++hf)
+                tma_load_2d(dst + hf * kHalfBytes + bb * box_rows * 128, map, hf * 64, y, fb);
+            }
+          }
+          if (kv == 0) ++kc; else ++vc;
+        }
+      }
+      for (uint32_t i = kc > kKStages ? kc - kKStages : 0; i < kc; ++i)
+        mbar_wait(bar_addr(sbase, B_K_FULL + i % kKStages), (i / kKStages) & 1);
+      for (uint32_t i = vc > kVStages ? vc - kVStages : 0; i < vc; ++i)
+        mbar_wait(bar_addr(sbase, B_V_FULL + i % kVStages), (i / kVStages) & 1);
+      if (units > 0) mbar_wait(bar_addr(sbase, B_Q_FULL), (units - 1) & 1);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    // All 32 lanes walk the same tiles and keep identical counters; lane 0 issues.
+    // Tiles are looked at three at a time: j (dQ), j+1 (dP), j+2 (S).
+    const uint32_t idQK = idesc_bf16_f32(kTile, kTile, false);
+    const uint32_t idDQ = idesc_bf16_f32(kTile, kD, true);
+    DqCursor cursor(sc, blockIdx.x, a.R, a.g);
+    TileRec rec[3];
+    bool have[3];
+    have[0] = cursor.next(&rec[0]);
+    have[1] = have[0] && cursor.next(&rec[1]);
+    have[2] = have[1] && cursor.next(&rec[2]);
+    uint32_t kc_s = 0, kc_q = 0, vc = 0, qunits = 0, j = 0;
+    bool ok = true;
+    // K tiles must be finite where dQ reads them: rows past the prompt end of a ragged
+    // last tile are zeroed (their dS is exactly 0, but 0 * NaN would still be NaN).
+    auto zero_tail_rows = [&](uint32_t kstage, uint32_t kpar, const TileRec& r) {
+      if (r.resp || r.key0 + kTile <= a.P) return;
+      mbar_wait(bar_addr(sbase, B_K_FULL + kstage), kpar);
+      const int valid = (int)(a.P - r.key0);
+      uint8_t* kb = smem + kOffK + kstage * kTileBytes;
+      for (int i = valid * 8 + lane; i < kTile * 8; i += 32) {
+        const int row = i >> 3, c = i & 7;
+        *reinterpret_cast<uint4*>(kb + row * 128 + c * 16) = make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4*>(kb + kHalfBytes + row * 128 + c * 16) = make_uint4(0, 0, 0, 0);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+    };
+    // S(r) = Q K^T into S buffer sb; K tile kc_s
+    auto issue_s = [&](const TileRec& r, int sb) -> bool {
+      if (r.first_of_unit) {
+        bool w = true;
+        if (lane == 0) w = mbar_wait(bar_addr(sbase, B_Q_FULL), qunits & 1);
+        w = __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
+        ++qunits;
+        if (!w) return false;
+      }
+      const uint32_t st = kc_s % kKStages, par = (kc_s / kKStages) & 1;
+      ++kc_s;
+      bool w = true;
+      if (lane == 0) w = mbar_wait(bar_addr(sbase, B_K_FULL + st), par);
+      w = __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
+      if (!w) return false;
+      zero_tail_rows(st, par, r);
+      if (lane == 0) {
+        tc_fence_after();
+        const uint32_t kb = sbase + kOffK + st * kTileBytes;
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
+          mma_ss(tmem + sb * kTile, sdesc_kmajor(sbase + kOffQ + off), sdesc_kmajor(kb + off), idQK,
+                 kk > 0);
+        }
+        mma_commit(bar_addr(sbase, B_S_FULL + sb));
+      }
+      return true;
+    };
+    // dP(r) = dO V^T; V tile vc
+    auto issue_dp = [&](const TileRec& r) -> bool {
+      const uint32_t st = vc % kVStages, par = (vc / kVStages) & 1;
+      ++vc;
+      bool w = true;
+      if (lane == 0) w = mbar_wait(bar_addr(sbase, B_V_FULL + st), par);
+      w = __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
+      if (!w) return false;
+      if (lane == 0) {
+        tc_fence_after();
+        const uint32_t vb = sbase + kOffV + st * kTileBytes;
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
+          mma_ss(tmem + 256, sdesc_kmajor(sbase + kOffDO + off), sdesc_kmajor(vb + off), idQK, kk > 0);
+        }
+        mma_commit(bar_addr(sbase, B_DP_FULL));
+        mma_commit(bar_addr(sbase, B_V_EMPTY + st));
+        if (r.last_of_unit) mma_commit(bar_addr(sbase, B_Q_EMPTY));
+      }
+      return true;
+    };
+    if (have[0]) {
+      ok = issue_s(rec[0], 0) && issue_dp(rec[0]);
+      if (ok && have[1]) ok = issue_s(rec[1], 1);
+      if (!ok && lane == 0) fail();
+    }
+    while (ok && have[0]) {
+      const int sb = j & 1;
+      bool w = true;
+      if (lane == 0) w = mbar_wait(bar_addr(sbase, B_DS_FULL), j & 1);
+      w = __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
+      if (!w) { if (lane == 0) fail(); break; }
+      if (have[1] && !issue_dp(rec[1])) { if (lane == 0) fail(); break; }
+      if (lane == 0) {
+        tc_fence_after();
+        const uint32_t kb = sbase + kOffK + (kc_q % kKStages) * kTileBytes;
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t acol = sb * kTile + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8);
+          mma_ts(tmem + 384, tmem + acol, sdesc_mnmajor(kb + kk * 2048, kHalfBytes), idDQ,
+                 (!rec[0].first_of_unit || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(bar_addr(sbase, B_K_EMPTY + kc_q % kKStages));
+        if (rec[0].last_of_unit) mma_commit(bar_addr(sbase, B_DQ_DONE));
+      }
+      ++kc_q;
+      if (have[2] && !issue_s(rec[2], sb)) { if (lane == 0) fail(); break; }
+      rec[0] = rec[1];
+      rec[1] = rec[2];
+      have[0] = have[1];
+      have[1] = have[2];
+      have[2] = have[2] && cursor.next(&rec[2]);
+      ++j;
+      if (*abort_flag) break;
+    }
+    if (lane == 0) {
+      mma_commit(bar_addr(sbase, B_DONE));
+      mbar_wait(bar_addr(sbase, B_DONE), 0);
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ dS warpgroups
+    const int cgrp = (warp - 4) >> 2;       // key columns [64 cgrp, 64 cgrp + 64)
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+    const float c = a.scale_log2;
+    DqCursor cursor(sc, blockIdx.x, a.R, a.g);
+    TileRec r;
+    uint32_t j = 0, uc = 0;
+    float lse2 = 0.f, dd = 0.f;
+    while (cursor.next(&r)) {
+      const int32_t tq = r.t0 + row;
+      if (r.first_of_unit) {
+        const int64_t idx = (int64_t)(tq < a.R ? tq : a.R - 1) * a.hq + r.h;
+        lse2 = b.lse[idx] * kLog2e;
+        dd = b.delta[idx];
+      }
+      const int sb = j & 1;
+      if (!mbar_wait(bar_addr(sbase, B_S_FULL + sb), (j >> 1) & 1)) { fail(); break; }
+      if (!mbar_wait(bar_addr(sbase, B_DP_FULL), j & 1)) { fail(); break; }
+      tc_fence_after();
+      int32_t lim = kTile;
+      if (r.resp) {
+        const int32_t lr = (tq + 1 < a.R ? tq + 1 : a.R) - r.key0;
+        lim = lr < kTile ? lr : kTile;
+      } else if (r.key0 + kTile > a.P) {
+        lim = (int32_t)(a.P - r.key0);
+      }
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        const int col0 = 64 * cgrp + 32 * q;
+        uint32_t sv[32], pv[32], ds[16];
+        tmem_ld32(tmem + lane_off + sb * kTile + col0, sv);
+        tmem_ld32(tmem + lane_off + 256 + col0, pv);
+        tmem_wait_ld();
+        reg_fence32(sv);
+        reg_fence32(pv);
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+          float d2[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const bool okk = col0 + i + e < lim;
+            const float p = fast_exp2(fmaf(__uint_as_float(sv[i + e]), c, -lse2));
+            d2[e] = okk ? p * (__uint_as_float(pv[i + e]) - dd) : 0.f;
+          }
+          ds[i >> 1] = pack_bf16(d2[0], d2[1]);
+        }
+        tmem_st16(tmem + lane_off + sb * kTile + 64 * cgrp + 16 * q, ds);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar_addr(sbase, B_DS_FULL));
+      ++j;
+      if (r.last_of_unit) {
+        if (!mbar_wait(bar_addr(sbase, B_DQ_DONE), uc & 1)) { fail(); break; }
+        ++uc;
+        tc_fence_after();
+        const bool valid = tq < a.R;
+        float* dst;
+        bool acc = false;
+        if (r.complete) {
+          dst = b.dq + ((int64_t)(valid ? tq : 0) * a.hq + r.h) * kD;
+          acc = b.accumulate != 0;
+        } else {
+          dst = b.part_dq + ((int64_t)sc.slot_of(blockIdx.x, r.u) * kUnitRows + row) * kD;
+        }
+#pragma unroll 1
+        for (int q = 0; q < 2; ++q) {
+          const int col0 = 64 * cgrp + 32 * q;
+          uint32_t v[32];
+          tmem_ld32(tmem + lane_off + 384 + col0, v);
+          tmem_wait_ld();
+          reg_fence32(v);
+          if (valid || !r.complete) {
+#pragma unroll
+            for (int i = 0; i < 32; i += 4) {
+              float4 x = make_float4(__uint_as_float(v[i]) * a.scale, __uint_as_float(v[i + 1]) * a.scale,
+                                     __uint_as_float(v[i + 2]) * a.scale, __uint_as_float(v[i + 3]) * a.scale);
+              float4* p4 = reinterpret_cast<float4*>(dst + col0 + i);
+              if (acc) {
+                const float4 o = *p4;
+                x.x += o.x; x.y += o.y; x.z += o.z; x.w += o.w;
+              }
+              *p4 = x;
+            }
+          }
+        }
+        tc_fence_before();
+      }
+      if (*abort_flag) break;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// Sum the split partials of each tail unit in CTA order; one block per unit.
+__global__ void __launch_bounds__(kD) bwd_dq_tc_combine(const LsAttnArgs a, const LsSched sc,
+                                                        const LsBwdIn b) {
+  const int u = sc.tail_unit0() + blockIdx.x;
+  const int64_t ipu = sc.items_per_unit();
+  const int64_t i0 = (int64_t)(u - sc.tail_unit0()) * ipu;
+  const int c_lo = sc.tail_cta_of(i0), c_hi = sc.tail_cta_of(i0 + ipu - 1);
+  if (c_lo == c_hi) return;
+  const int nTB = (a.R + kUnitRows - 1) / kUnitRows;
+  const int h = u / nTB, t0 = (u % nTB) * kUnitRows;
+  const int col = threadIdx.x;
+  for (int r = 0; r < kUnitRows; ++r) {
+    const int t = t0 + r;
+    if (t >= a.R) break;
+    float acc = 0.f;
+    for (int cc = c_lo; cc <= c_hi; ++cc)
+      if (sc.tail_nonempty(cc)) acc += b.part_dq[((int64_t)sc.slot_of(cc, u) * kUnitRows + r) * kD + col];
+    float* dst = b.dq + ((int64_t)t * a.hq + h) * kD + col;
+    *dst = b.accumulate ? *dst + acc : acc;
+  }
+}
+
+}  // namespace
+
+int ls_bwd_unit_rows() { return kUnitRows; }
+int ls_bwd_tile() { return kTile; }
+int ls_bwd_ctas_per_sm() { return 1; }
+
+cudaError_t ls_launch_bwd_dq(const LsAttnArgs& a, const LsSched& sc, const LsBwdIn& b,
+                             cudaStream_t st) {
+  TmapSet tm;
+  const uint32_t box_q[3] = {64, 1, kTile};
+  {
+    const uint64_t dims[3] = {(uint64_t)kD, (uint64_t)a.hq, (uint64_t)a.R};
+    const uint64_t strides[2] = {(uint64_t)kD * 2, (uint64_t)a.hq * kD * 2};
+    if (!ls_make_tmap_bf16(&tm.q, a.q, 3, dims, strides, box_q)) return cudaErrorInvalidValue;
+    if (!ls_make_tmap_bf16(&tm.d_o, b.d_o, 3, dims, strides, box_q)) return cudaErrorInvalidValue;
+  }
+  {
+    const uint64_t dims[3] = {(uint64_t)kD, (uint64_t)a.hkv, (uint64_t)a.R};
+    const uint64_t strides[2] = {(uint64_t)kD * 2, (uint64_t)a.hkv * kD * 2};
+    if (!ls_make_tmap_bf16(&tm.kr, a.k_resp, 3, dims, strides, box_q)) return cudaErrorInvalidValue;
+    if (!ls_make_tmap_bf16(&tm.vr, a.v_resp, 3, dims, strides, box_q)) return cudaErrorInvalidValue;
+  }
+  {
+    const int ps = 1 << a.ps_log2;
+    const uint64_t dims[2] = {(uint64_t)kD, (uint64_t)a.num_pages * a.hkv * ps};
+    const uint64_t strides[1] = {(uint64_t)kD * 2};
+    const uint32_t box[2] = {64, (uint32_t)(ps < kTile ? ps : kTile)};
+    if (!ls_make_tmap_bf16(&tm.kp, a.k_pool, 2, dims, strides, box)) return cudaErrorInvalidValue;
+    if (!ls_make_tmap_bf16(&tm.vp, a.v_pool, 2, dims, strides, box)) return cudaErrorInvalidValue;
+  }
+  cudaError_t e =
+      cudaFuncSetAttribute(bwd_dq_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e != cudaSuccess) return e;
+  bwd_dq_tc_kernel<<<sc.ctas, kThreads, kSmemBytes, st>>>(tm, a, sc, b);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  ls_note_launch();
+  const int64_t tail_units = sc.units - (int64_t)sc.waves * sc.ctas;
+  if (tail_units > 0) {
+    bwd_dq_tc_combine<<<(unsigned)tail_units, kD, 0, st>>>(a, sc, b);
+    e = cudaGetLastError();
+    if (e == cudaSuccess) ls_note_launch();
+  }
+  return e;
+}

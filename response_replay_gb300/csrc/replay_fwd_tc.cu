@@ -1,0 +1,535 @@
+// replay_fwd_tc.cu -- replay attention forward on the 5th-generation tensor cores.
+//
+// Definition (LongStraw explainer, "Serial replay makes G a schedule" and "Two
+// incompatible architectures", Qwen bullet; paper digest, Method step 3):
+//   s_{t,j} = scale <q_{t,h}, k_{j,h/g}>,  j over every prompt position and response j <= t
+//   lse_t = log sum_j exp(s_{t,j}),  o_t = sum_j exp(s_{t,j} - lse_t) v_j
+// Prompt splits are merged on chip by the online-softmax rescaling when one CTA runs
+// them back to back, and by log-sum-exp in replay_fwd_tc_combine otherwise.
+//
+// CTA (one per SM, persistent, 12 warps) owns a unit = 256 consecutive response tokens
+// of one query head, as two 128-row tiles A and B that share every K/V tile:
+//   warp 0      TMA producer: Q tiles, then K and V tiles (128 keys x 128 dims, two
+//               128-byte-swizzled halves each) into a 4-stage ring; prompt tiles are
+//               gathered page by page through the page table.
+//   warp 1      MMA issuer (one thread): S_t = Q_t K^T into tensor memory (SS MMA,
+//               M=128 N=128 K=128), O_t += P_t V with P_t read from tensor memory (TS
+//               MMA); ping-pong between tiles A and B so the tensor core always has
+//               the other tile's work while one tile's softmax runs.
+//   warps 2-3   idle (they complete warpgroup 0, whose registers go to the softmax)
+//   warps 4-7   softmax of tile A, warps 8-11 softmax of tile B: each thread owns one
+//               query row; reads its S row from tensor memory, masks, updates the
+//               running max (log2 domain; O is rescaled only when the max grows by more
+//               than 2^8) and the compensated row sum, writes P as bf16 pairs back over
+//               its S columns, and at the end of a unit normalises O and writes O / LSE.
+// Tensor memory (512 columns): S_A [0,128) S_B [128,256) O_A [256,384) O_B [384,512);
+// P_t overlays the first 64 columns of S_t.
+#include <math.h>
+
+#include "ls_device.cuh"
+#include "ls_internal.h"
+#include "ls_tiles.cuh"
+#include "ls_tmap.h"
+#include "ls_umma.cuh"
+
+namespace {
+
+using namespace umma;
+
+constexpr int kD = 128;
+constexpr int kTile = 128;                 // query rows per tile, keys per KV tile
+constexpr int kUnitRows = 2 * kTile;       // tokens per unit
+constexpr int kStages = 4;
+constexpr int kThreads = 384;
+// Register split (setmaxnreg): the launch gives 168 per thread (384 x 168 = 64512);
+// warpgroup 0 (TMA + MMA control, ~100 live registers) drops to 112 and the two softmax
+// warpgroups (a full 128-column S row per thread) rise to 192:
+// 128 x 112 + 256 x 192 = 63488 <= 64512.
+constexpr int kRegsLaunch = 168, kRegsControl = 112, kRegsSoftmax = 192;
+static_assert(128 * kRegsControl + 256 * kRegsSoftmax <= kThreads * kRegsLaunch, "register split");
+constexpr uint32_t kTileBytes = kTile * kD * 2;  // 32 KB
+constexpr uint32_t kHalfBytes = kTileBytes / 2;  // 16 KB: 128 rows x 64 dims
+constexpr uint32_t kOffQ = 0;                    // Q_A, Q_B
+constexpr uint32_t kOffRing = 2 * kTileBytes;
+constexpr uint32_t kOffBar = kOffRing + kStages * kTileBytes;
+constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;  // + barriers + alignment slack
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleLog2 = 8.0f;
+
+// barrier indices (8 bytes each from kOffBar)
+enum {
+  B_KV_FULL = 0,
+  B_KV_EMPTY = B_KV_FULL + kStages,
+  B_Q_FULL = B_KV_EMPTY + kStages,
+  B_Q_EMPTY,
+  B_S_FULL,          // 2
+  B_P_FULL = B_S_FULL + 2,
+  B_O_DONE = B_P_FULL + 2,
+  B_DONE = B_O_DONE + 2,
+  B_COUNT
+};
+static_assert(B_COUNT * 8 + 16 <= 256, "barrier area");
+
+struct TmapSet {
+  CUtensorMap q, kp, vp, kr, vr;
+};
+
+using FwdCursor = TileCursor<kUnitRows, kTile>;
+
+__device__ __forceinline__ uint32_t bar_addr(uint32_t base, int i) { return base + kOffBar + 8 * i; }
+
+__global__ void __launch_bounds__(kThreads, 1)
+replay_fwd_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a, const LsSched sc,
+                     const LsFwdOut out) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + kOffBar + B_COUNT * 8);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffBar + B_COUNT * 8 + 4);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  if (tid == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(bar_addr(sbase, B_KV_FULL + i), 1);
+      mbar_init(bar_addr(sbase, B_KV_EMPTY + i), 1);
+    }
+    mbar_init(bar_addr(sbase, B_Q_FULL), 1);
+    mbar_init(bar_addr(sbase, B_Q_EMPTY), 1);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(bar_addr(sbase, B_S_FULL + t), 1);
+      mbar_init(bar_addr(sbase, B_P_FULL + t), kTile);
+      mbar_init(bar_addr(sbase, B_O_DONE + t), 1);
+    }
+    mbar_init(bar_addr(sbase, B_DONE), 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(const_cast<uint32_t*>(tmem_slot)), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  auto fail = [&](void) {
+    ls_report(a.err, LS_DEVERR_TIMEOUT);
+    *abort_flag = 1;
+  };
+
+  if (warp < 4) {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsControl));
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tm.q);
+      tma_prefetch_desc(&tm.kp);
+      tma_prefetch_desc(&tm.vp);
+      tma_prefetch_desc(&tm.kr);
+      tma_prefetch_desc(&tm.vr);
+      FwdCursor cur(sc, blockIdx.x, a.R, a.g);
+      TileRec r;
+      uint32_t ring = 0, units = 0;
+      const int32_t ps = 1 << a.ps_log2;
+      const int32_t box_rows = ps < kTile ? ps : kTile;
+      const int32_t pool_rows = a.num_pages * a.hkv * ps;
+      bool ok = true;
+      while (ok && cur.next(&r)) {
+        if (r.first_of_unit) {
+          if (units > 0 && !mbar_wait(bar_addr(sbase, B_Q_EMPTY), (units - 1) & 1)) { fail(); break; }
+          const uint32_t qb = bar_addr(sbase, B_Q_FULL);
+          mbar_expect_tx(qb, 2 * kTileBytes);
+          for (int tt = 0; tt < 2; ++tt)
+            for (int hf = 0; hf < 2; ++hf)
+              tma_load_3d(sbase + kOffQ + tt * kTileBytes + hf * kHalfBytes, &tm.q, hf * 64, r.h,
+                          r.t0 + tt * kTile, qb);
+          ++units;
+        }
+        for (int kv = 0; kv < 2 && ok; ++kv) {
+          const uint32_t st = ring % kStages;
+          if (!mbar_wait(bar_addr(sbase, B_KV_EMPTY + st), ((ring / kStages) & 1) ^ 1)) {
+            fail();
+            ok = false;
+            break;
+          }
+          if (*abort_flag) { ok = false; break; }
+          const uint32_t fb = bar_addr(sbase, B_KV_FULL + st);
+          const uint32_t dst = sbase + kOffRing + st * kTileBytes;
+          mbar_expect_tx(fb, kTileBytes);
+          if (r.resp) {
+            const void* map = kv == 0 ? (const void*)&tm.kr : (const void*)&tm.vr;
+            for (int hf = 0; hf < 2; ++hf)
+              tma_load_3d(dst + hf * kHalfBytes, map, hf * 64, r.kvh, r.key0, fb);
+          } else {
+            const void* map = kv == 0 ? (const void*)&tm.kp : (const void*)&tm.vp;
+            for (int b = 0; b < kTile / box_rows; ++b) {
+              const int32_t pos = r.key0 + b * box_rows;
+              int32_t y = pool_rows;  // out of bounds: zero fill
+              if (pos < a.P) {
+                const int32_t phys = __ldg(a.page_table + (pos >> a.ps_log2));
+                if ((uint32_t)phys < (uint32_t)a.num_pages)
+                  y = (phys * a.hkv + r.kvh) * ps + (pos & (ps - 1));
+                else
+                  ls_report(a.err, LS_DEVERR_CHECK);
+              }
+              for (int hf = 0; hf < 2; ++hf)
+                tma_load_2d(dst + hf * kHalfBytes + b * box_rows * 128, map, hf * 64, y, fb);
+            }
+          }
+          ++ring;
+        }
+      }
+      // Do not leave while loads into this CTA's shared memory may still be in flight.
+      for (uint32_t i = ring > kStages ? ring - kStages : 0; i < ring; ++i)
+        mbar_wait(bar_addr(sbase, B_KV_FULL + i % kStages), (i / kStages) & 1);
+      if (units > 0) mbar_wait(bar_addr(sbase, B_Q_FULL), (units - 1) & 1);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    const uint32_t idS = idesc_bf16_f32(kTile, kTile, false);
+    const uint32_t idPV = idesc_bf16_f32(kTile, kD, true);
+    FwdCursor cursor(sc, blockIdx.x, a.R, a.g);
+    TileRec cur, nxt;
+    uint32_t ring = 0, units = 0, kc = 0;
+    bool ok = cursor.next(&cur);
+    auto issue_s = [&](int t, uint32_t kstage) {
+      const uint32_t qa = sbase + kOffQ + t * kTileBytes;
+      const uint32_t kb = sbase + kOffRing + kstage * kTileBytes;
+      for (int kk = 0; kk < 8; ++kk) {
+        const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
+        mma_ss(tmem + t * kTile, sdesc_kmajor(qa + off), sdesc_kmajor(kb + off), idS, kk > 0);
+      }
+    };
+    auto issue_pv = [&](int t, uint32_t vstage, bool accumulate) {
+      const uint32_t vb = sbase + kOffRing + vstage * kTileBytes;
+      for (int kk = 0; kk < 8; ++kk)
+        mma_ts(tmem + 256 + t * kTile, tmem + t * kTile + kk * 8,
+               sdesc_mnmajor(vb + kk * 2048, kHalfBytes), idPV, (accumulate || kk > 0) ? 1u : 0u);
+    };
+    uint32_t kstage = 0;
+    if (ok) {
+      // prologue: S_A(0), S_B(0)
+      if (lane == 0) {
+        if (!mbar_wait(bar_addr(sbase, B_Q_FULL), units & 1)) { fail(); ok = false; }
+        kstage = ring % kStages;
+        if (ok && !mbar_wait(bar_addr(sbase, B_KV_FULL + kstage), (ring / kStages) & 1)) { fail(); ok = false; }
+        if (ok) {
+          tc_fence_after();
+          issue_s(0, kstage);
+          mma_commit(bar_addr(sbase, B_S_FULL + 0));
+          issue_s(1, kstage);
+          mma_commit(bar_addr(sbase, B_S_FULL + 1));
+          mma_commit(bar_addr(sbase, B_KV_EMPTY + kstage));
+          if (cur.last_of_unit) mma_commit(bar_addr(sbase, B_Q_EMPTY));
+        }
+      }
+      ++units;
+      ++ring;
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    }
+    while (ok) {
+      const bool has_nxt = cursor.next(&nxt);
+      // V of the current tile
+      const uint32_t vstage = ring % kStages;
+      const uint32_t vpar = (ring / kStages) & 1;
+      ++ring;
+      if (lane == 0 && !mbar_wait(bar_addr(sbase, B_KV_FULL + vstage), vpar)) { fail(); ok = false; }
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      if (!ok) break;
+      if (!cur.resp && cur.key0 + kTile > a.P) {
+        // ragged last prompt tile: rows past the prompt end may hold stale page data;
+        // zero them so that 0-probability rows cannot inject NaN/Inf into P V.
+        const int valid = (int)(a.P - cur.key0);
+        mbar_wait(bar_addr(sbase, B_KV_FULL + vstage), vpar);
+        uint8_t* vb = smem + kOffRing + vstage * kTileBytes;
+        for (int i = valid * 8 + lane; i < kTile * 8; i += 32) {
+          const int row = i >> 3, c = i & 7;
+          *reinterpret_cast<uint4*>(vb + row * 128 + c * 16) = make_uint4(0, 0, 0, 0);
+          *reinterpret_cast<uint4*>(vb + kHalfBytes + row * 128 + c * 16) = make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+      }
+      const bool nxt_new_unit = has_nxt && nxt.first_of_unit;
+      if (lane == 0) {
+        // tile A: PV_A(cur), then S_A(nxt)
+        if (!mbar_wait(bar_addr(sbase, B_P_FULL + 0), kc & 1)) { fail(); ok = false; }
+        if (ok) {
+          tc_fence_after();
+          issue_pv(0, vstage, !cur.first_of_unit);
+          if (cur.last_of_unit) mma_commit(bar_addr(sbase, B_O_DONE + 0));
+        }
+        if (ok && has_nxt) {
+          if (nxt_new_unit && !mbar_wait(bar_addr(sbase, B_Q_FULL), units & 1)) { fail(); ok = false; }
+          kstage = ring % kStages;
+          if (ok && !mbar_wait(bar_addr(sbase, B_KV_FULL + kstage), (ring / kStages) & 1)) { fail(); ok = false; }
+          if (ok) {
+            tc_fence_after();
+            issue_s(0, kstage);
+            mma_commit(bar_addr(sbase, B_S_FULL + 0));
+          }
+        }
+        // tile B: PV_B(cur), then S_B(nxt)
+        if (ok && !mbar_wait(bar_addr(sbase, B_P_FULL + 1), kc & 1)) { fail(); ok = false; }
+        if (ok) {
+          tc_fence_after();
+          issue_pv(1, vstage, !cur.first_of_unit);
+          if (cur.last_of_unit) mma_commit(bar_addr(sbase, B_O_DONE + 1));
+          mma_commit(bar_addr(sbase, B_KV_EMPTY + vstage));
+          if (has_nxt) {
+            issue_s(1, kstage);
+            mma_commit(bar_addr(sbase, B_S_FULL + 1));
+            mma_commit(bar_addr(sbase, B_KV_EMPTY + kstage));
+            if (nxt.last_of_unit) mma_commit(bar_addr(sbase, B_Q_EMPTY));
+          }
+        }
+      }
+      if (nxt_new_unit) ++units;
+      if (has_nxt) ++ring;
+      ++kc;
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      if (!has_nxt) break;
+      cur = nxt;
+    }
+    // make sure every issued MMA has finished before tensor memory is released
+    if (lane == 0) {
+      mma_commit(bar_addr(sbase, B_DONE));
+      mbar_wait(bar_addr(sbase, B_DONE), 0);
+    }
+    __syncwarp();
+  }
+  } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
+    // ------------------------------------------------------------ softmax warpgroups
+    const int t = (warp - 4) >> 2;         // tile A (0) or B (1)
+    const int quad = warp & 3;             // tensor-memory lane quadrant of this warp
+    const int row = quad * 32 + lane;      // query row within the tile
+    const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+    const uint32_t s_col = tmem + lane_off + t * kTile;
+    const uint32_t o_col = tmem + lane_off + 256 + t * kTile;
+    const float c = a.scale_log2;
+    FwdCursor cursor(sc, blockIdx.x, a.R, a.g);
+    TileRec r;
+    uint32_t kc = 0, oc = 0;
+    float m = -INFINITY, l = 0.f, lcomp = 0.f;
+    while (cursor.next(&r)) {
+      if (!mbar_wait(bar_addr(sbase, B_S_FULL + t), kc & 1)) { fail(); break; }
+      tc_fence_after();
+      uint32_t sr[128];
+      tmem_ld32(s_col + 0, sr);
+      tmem_ld32(s_col + 32, sr + 32);
+      tmem_ld32(s_col + 64, sr + 64);
+      tmem_ld32(s_col + 96, sr + 96);
+      tmem_wait_ld();
+      reg_fence32(sr);
+      reg_fence32(sr + 32);
+      reg_fence32(sr + 64);
+      reg_fence32(sr + 96);
+      const int32_t tq = r.t0 + t * kTile + row;  // this row's response token
+      int32_t lim = kTile;                          // keys [key0, key0 + lim) visible
+      if (r.resp) {
+        const int32_t lr = (tq + 1 < a.R ? tq + 1 : a.R) - r.key0;
+        lim = lr < kTile ? lr : kTile;
+      } else if (r.key0 + kTile > a.P) {
+        lim = (int32_t)(a.P - r.key0);
+      }
+      float mx = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < 128; ++j) {
+        float x = __uint_as_float(sr[j]);
+        x = j < lim ? x : -INFINITY;
+        sr[j] = __float_as_uint(x);
+        mx = fmaxf(mx, x);
+      }
+      const float mt = mx * c;
+      bool rescale = false;
+      float alpha = 1.f;
+      if (r.first_of_unit) {
+        m = mt;
+        l = lcomp = 0.f;
+      } else if (mt > m + kRescaleLog2) {
+        alpha = fast_exp2(m - mt);
+        m = mt;
+        l *= alpha;
+        lcomp *= alpha;
+        rescale = true;
+      }
+      const float msub = (m == -INFINITY) ? 0.f : m;
+      float ls = 0.f;
+      uint32_t pk[64];
+#pragma unroll
+      for (int j = 0; j < 64; ++j) {
+        const float p0 = fast_exp2(fmaf(__uint_as_float(sr[2 * j]), c, -msub));
+        const float p1 = fast_exp2(fmaf(__uint_as_float(sr[2 * j + 1]), c, -msub));
+        ls += p0 + p1;
+        pk[j] = pack_bf16(p0, p1);
+      }
+      {
+        const float tsum = l + ls;
+        lcomp += (l - tsum) + ls;
+        l = tsum;
+      }
+      if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll 1
+        for (int c0 = 0; c0 < 128; c0 += 32) {
+          uint32_t ov[32];
+          tmem_ld32(o_col + c0, ov);
+          tmem_wait_ld();
+          reg_fence32(ov);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+          tmem_st32(o_col + c0, ov);
+        }
+      }
+      tmem_st32(s_col + 0, pk);
+      tmem_st32(s_col + 32, pk + 32);
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar_addr(sbase, B_P_FULL + t));
+      ++kc;
+      if (r.last_of_unit) {
+        if (!mbar_wait(bar_addr(sbase, B_O_DONE + t), oc & 1)) { fail(); break; }
+        ++oc;
+        tc_fence_after();
+        const float lt = l + lcomp;
+        const float inv = 1.f / lt;
+        const float lse = (m + log2f(lt)) * kLn2;
+        if (r.complete) {
+          const bool valid = tq < a.R;
+          __nv_bfloat16* orow =
+              static_cast<__nv_bfloat16*>(out.o) + ((int64_t)(valid ? tq : 0) * a.hq + r.h) * kD;
+#pragma unroll 1
+          for (int c0 = 0; c0 < 128; c0 += 32) {
+            uint32_t ov[32];
+            tmem_ld32(o_col + c0, ov);
+            tmem_wait_ld();
+            reg_fence32(ov);
+            if (valid) {
+#pragma unroll
+              for (int i = 0; i < 32; i += 8) {
+                uint4 w;
+                w.x = pack_bf16(__uint_as_float(ov[i]) * inv, __uint_as_float(ov[i + 1]) * inv);
+                w.y = pack_bf16(__uint_as_float(ov[i + 2]) * inv, __uint_as_float(ov[i + 3]) * inv);
+                w.z = pack_bf16(__uint_as_float(ov[i + 4]) * inv, __uint_as_float(ov[i + 5]) * inv);
+                w.w = pack_bf16(__uint_as_float(ov[i + 6]) * inv, __uint_as_float(ov[i + 7]) * inv);
+                *reinterpret_cast<uint4*>(orow + c0 + i) = w;
+              }
+            }
+          }
+          if (valid) out.lse[(int64_t)tq * a.hq + r.h] = lse;
+        } else {
+          const int slot = sc.slot_of(blockIdx.x, r.u);
+          float* prow = out.part_o + ((int64_t)slot * kUnitRows + t * kTile + row) * kD;
+#pragma unroll 1
+          for (int c0 = 0; c0 < 128; c0 += 32) {
+            uint32_t ov[32];
+            tmem_ld32(o_col + c0, ov);
+            tmem_wait_ld();
+            reg_fence32(ov);
+#pragma unroll
+            for (int i = 0; i < 32; i += 4)
+              *reinterpret_cast<float4*>(prow + c0 + i) =
+                  make_float4(__uint_as_float(ov[i]) * inv, __uint_as_float(ov[i + 1]) * inv,
+                              __uint_as_float(ov[i + 2]) * inv, __uint_as_float(ov[i + 3]) * inv);
+          }
+          out.part_lse[(int64_t)slot * kUnitRows + t * kTile + row] = lse;
+        }
+        tc_fence_before();
+        m = -INFINITY;
+        l = lcomp = 0.f;
+      }
+      if (*abort_flag) break;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// Merge the partial (o, lse) of every tail unit split across CTAs (fixed order):
+//   lse = log sum_c exp(lse_c),  o = sum_c exp(lse_c - lse) o_c.
+__global__ void __launch_bounds__(kD) replay_fwd_tc_combine(const LsAttnArgs a, const LsSched sc,
+                                                            const LsFwdOut out) {
+  const int u = sc.tail_unit0() + blockIdx.x;
+  const int64_t ipu = sc.items_per_unit();
+  const int64_t i0 = (int64_t)(u - sc.tail_unit0()) * ipu;
+  const int c_lo = sc.tail_cta_of(i0), c_hi = sc.tail_cta_of(i0 + ipu - 1);
+  if (c_lo == c_hi) return;
+  const int nTB = (a.R + kUnitRows - 1) / kUnitRows;
+  const int h = u / nTB, t0 = (u % nTB) * kUnitRows;
+  const int col = threadIdx.x;
+  for (int r = 0; r < kUnitRows; ++r) {
+    const int t = t0 + r;
+    if (t >= a.R) break;
+    float mx = -INFINITY;
+    for (int cc = c_lo; cc <= c_hi; ++cc)
+      if (sc.tail_nonempty(cc)) mx = fmaxf(mx, out.part_lse[(int64_t)sc.slot_of(cc, u) * kUnitRows + r]);
+    float sum = 0.f;
+    for (int cc = c_lo; cc <= c_hi; ++cc)
+      if (sc.tail_nonempty(cc)) sum += expf(out.part_lse[(int64_t)sc.slot_of(cc, u) * kUnitRows + r] - mx);
+    const float lse = mx + logf(sum);
+    float acc = 0.f;
+    for (int cc = c_lo; cc <= c_hi; ++cc) {
+      if (!sc.tail_nonempty(cc)) continue;
+      const int64_t slot = sc.slot_of(cc, u);
+      acc += expf(out.part_lse[slot * kUnitRows + r] - lse) * out.part_o[(slot * kUnitRows + r) * kD + col];
+    }
+    const int64_t row = (int64_t)t * a.hq + h;
+    static_cast<__nv_bfloat16*>(out.o)[row * kD + col] = __float2bfloat16_rn(acc);
+    if (col == 0) out.lse[row] = lse;
+  }
+}
+
+}  // namespace
+
+int ls_fwd_unit_rows() { return kUnitRows; }
+int ls_fwd_tile() { return kTile; }
+int ls_fwd_ctas_per_sm() { return 1; }
+int ls_num_units(int R, int hq, int hkv, int unit_rows) {
+  (void)hkv;
+  return hq * ((R + unit_rows - 1) / unit_rows);
+}
+
+cudaError_t ls_launch_replay_fwd(const LsAttnArgs& a, const LsSched& sc, const LsFwdOut& out,
+                                 cudaStream_t st) {
+  TmapSet tm;
+  const uint32_t box_q[3] = {64, 1, kTile};
+  {
+    const uint64_t dims[3] = {(uint64_t)kD, (uint64_t)a.hq, (uint64_t)a.R};
+    const uint64_t strides[2] = {(uint64_t)kD * 2, (uint64_t)a.hq * kD * 2};
+    if (!ls_make_tmap_bf16(&tm.q, a.q, 3, dims, strides, box_q)) return cudaErrorInvalidValue;
+  }
+  {
+    const uint64_t dims[3] = {(uint64_t)kD, (uint64_t)a.hkv, (uint64_t)a.R};
+    const uint64_t strides[2] = {(uint64_t)kD * 2, (uint64_t)a.hkv * kD * 2};
+    if (!ls_make_tmap_bf16(&tm.kr, a.k_resp, 3, dims, strides, box_q)) return cudaErrorInvalidValue;
+    if (!ls_make_tmap_bf16(&tm.vr, a.v_resp, 3, dims, strides, box_q)) return cudaErrorInvalidValue;
+  }
+  {
+    const int ps = 1 << a.ps_log2;
+    const uint64_t dims[2] = {(uint64_t)kD, (uint64_t)a.num_pages * a.hkv * ps};
+    const uint64_t strides[1] = {(uint64_t)kD * 2};
+    const uint32_t box[2] = {64, (uint32_t)(ps < kTile ? ps : kTile)};
+    if (!ls_make_tmap_bf16(&tm.kp, a.k_pool, 2, dims, strides, box)) return cudaErrorInvalidValue;
+    if (!ls_make_tmap_bf16(&tm.vp, a.v_pool, 2, dims, strides, box)) return cudaErrorInvalidValue;
+  }
+  cudaError_t e = cudaFuncSetAttribute(replay_fwd_tc_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e != cudaSuccess) return e;
+  replay_fwd_tc_kernel<<<sc.ctas, kThreads, kSmemBytes, st>>>(tm, a, sc, out);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  ls_note_launch();
+  const int64_t tail_units = sc.units - (int64_t)sc.waves * sc.ctas;
+  if (tail_units > 0) {
+    replay_fwd_tc_combine<<<(unsigned)tail_units, kD, 0, st>>>(a, sc, out);
+    e = cudaGetLastError();
+    if (e == cudaSuccess) ls_note_launch();
+  }
+  return e;
+}
