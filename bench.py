@@ -161,6 +161,11 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     branches = [syn.make_branch(R, w.hq, w.hkv, D, seed + 1 + i, dev) for i in range(G)]
     lens = list(w.R[:G])
     gin = syn.make_grpo(lens, w.vocab, w.logits_dtype, w.rewards, seed, dev, shift_frac=w.shift_frac)
+    if G < w.G:
+        # fewer members replayed (profiling): the loss still sees the whole group
+        gin.rewards = torch.from_numpy(
+            syn.draw_rewards(w.rewards, w.G, np.random.default_rng(seed))).to(dev)
+        gin.resp_lens = torch.tensor(list(w.R), dtype=torch.int32, device=dev)
     T = sum(lens)
     off = [0]
     for n in lens:

@@ -336,17 +336,19 @@ bwd_dq_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a, const L
         tmem_wait_ld();
         reg_fence32(sv);
         reg_fence32(pv);
+        float d2[32];
 #pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-          float d2[2];
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const bool okk = col0 + i + e < lim;
-            const float p = fast_exp2(fmaf(__uint_as_float(sv[i + e]), c, -lse2));
-            d2[e] = okk ? p * (__uint_as_float(pv[i + e]) - dd) : 0.f;
-          }
-          ds[i >> 1] = pack_bf16(d2[0], d2[1]);
+        for (int i = 0; i < 32; ++i) {
+          const float p = fast_exp2(fmaf(__uint_as_float(sv[i]), c, -lse2));
+          d2[i] = p * (__uint_as_float(pv[i]) - dd);
         }
+        if (col0 + 32 > lim) {  // only the ragged prompt tail and the diagonal need a mask
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (col0 + i >= lim) d2[i] = 0.f;
+        }
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) ds[i >> 1] = pack_bf16(d2[i], d2[i + 1]);
         tmem_st16(tmem + lane_off + sb * kTile + 64 * cgrp + 16 * q, ds);
       }
       tmem_wait_st();

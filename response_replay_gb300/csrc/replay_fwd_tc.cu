@@ -335,14 +335,19 @@ replay_fwd_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a, con
       } else if (r.key0 + kTile > a.P) {
         lim = (int32_t)(a.P - r.key0);
       }
-      float mx = -INFINITY;
+      if (lim < kTile) {  // only the ragged prompt tail and the diagonal need a mask
 #pragma unroll
-      for (int j = 0; j < 128; ++j) {
-        float x = __uint_as_float(sr[j]);
-        x = j < lim ? x : -INFINITY;
-        sr[j] = __float_as_uint(x);
-        mx = fmaxf(mx, x);
+        for (int j = 0; j < 128; ++j)
+          if (j >= lim) sr[j] = __float_as_uint(-INFINITY);
       }
+      // row max with 8 independent chains (latency, not throughput, bounds one row)
+      float mx8[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) mx8[k] = __uint_as_float(sr[k]);
+#pragma unroll
+      for (int j = 8; j < 128; ++j) mx8[j & 7] = fmaxf(mx8[j & 7], __uint_as_float(sr[j]));
+      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
       const float mt = mx * c;
       bool rescale = false;
       float alpha = 1.f;
@@ -357,15 +362,16 @@ replay_fwd_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a, con
         rescale = true;
       }
       const float msub = (m == -INFINITY) ? 0.f : m;
-      float ls = 0.f;
+      float ls8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
       uint32_t pk[64];
 #pragma unroll
       for (int j = 0; j < 64; ++j) {
         const float p0 = fast_exp2(fmaf(__uint_as_float(sr[2 * j]), c, -msub));
         const float p1 = fast_exp2(fmaf(__uint_as_float(sr[2 * j + 1]), c, -msub));
-        ls += p0 + p1;
+        ls8[j & 7] += p0 + p1;
         pk[j] = pack_bf16(p0, p1);
       }
+      const float ls = ((ls8[0] + ls8[1]) + (ls8[2] + ls8[3])) + ((ls8[4] + ls8[5]) + (ls8[6] + ls8[7]));
       {
         const float tsum = l + ls;
         lcomp += (l - tsum) + ls;
