@@ -196,6 +196,13 @@ bwd_dq_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a, const L
     have[2] = have[1] && cursor.next(&rec[2]);
     uint32_t kc_s = 0, kc_q = 0, vc = 0, qunits = 0, j = 0;
     bool ok = true;
+    // Descriptor bases built once; each MMA only adds a compile-time offset, so the
+    // issuing thread is not slowed by per-instruction 64-bit descriptor arithmetic.
+    const uint32_t dq_base = sdesc_lo(sbase + kOffQ, 16);
+    const uint32_t ddo_base = sdesc_lo(sbase + kOffDO, 16);
+    const uint32_t dk_base = sdesc_lo(sbase + kOffK, 16);
+    const uint32_t dv_base = sdesc_lo(sbase + kOffV, 16);
+    const uint32_t dkm_base = sdesc_lo(sbase + kOffK, kHalfBytes);
     // K tiles must be finite where dQ reads them: rows past the prompt end of a ragged
     // last tile are zeroed (their dS is exactly 0, but 0 * NaN would still be NaN).
     auto zero_tail_rows = [&](uint32_t kstage, uint32_t kpar, const TileRec& r) {
@@ -229,11 +236,12 @@ bwd_dq_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a, const L
       zero_tail_rows(st, par, r);
       if (lane == 0) {
         tc_fence_after();
-        const uint32_t kb = sbase + kOffK + st * kTileBytes;
+        const uint32_t b0 = dk_base + ((st * kTileBytes) >> 4);
+        const uint32_t d = tmem + sb * kTile;
+#pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-          mma_ss(tmem + sb * kTile, sdesc_kmajor(sbase + kOffQ + off), sdesc_kmajor(kb + off), idQK,
-                 kk > 0);
+          const uint32_t off = ((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4;
+          mma_ss_lo(d, dq_base + off, b0 + off, idQK, kk > 0);
         }
         mma_commit(bar_addr(sbase, B_S_FULL + sb));
       }
@@ -249,10 +257,11 @@ bwd_dq_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a, const L
       if (!w) return false;
       if (lane == 0) {
         tc_fence_after();
-        const uint32_t vb = sbase + kOffV + st * kTileBytes;
+        const uint32_t b0 = dv_base + ((st * kTileBytes) >> 4);
+#pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-          mma_ss(tmem + 256, sdesc_kmajor(sbase + kOffDO + off), sdesc_kmajor(vb + off), idQK, kk > 0);
+          const uint32_t off = ((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4;
+          mma_ss_lo(tmem + 256, ddo_base + off, b0 + off, idQK, kk > 0);
         }
         mma_commit(bar_addr(sbase, B_DP_FULL));
         mma_commit(bar_addr(sbase, B_V_EMPTY + st));
@@ -274,11 +283,13 @@ bwd_dq_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a, const L
       if (have[1] && !issue_dp(rec[1])) { if (lane == 0) fail(); break; }
       if (lane == 0) {
         tc_fence_after();
-        const uint32_t kb = sbase + kOffK + (kc_q % kKStages) * kTileBytes;
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t acol = sb * kTile + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8);
-          mma_ts(tmem + 384, tmem + acol, sdesc_mnmajor(kb + kk * 2048, kHalfBytes), idDQ,
-                 (!rec[0].first_of_unit || kk > 0) ? 1u : 0u);
+        const uint32_t b0 = dkm_base + (((kc_q % kKStages) * kTileBytes) >> 4);
+        const uint32_t a = tmem + sb * kTile;
+        mma_ts_lo(tmem + 384, a, b0, idDQ, rec[0].first_of_unit ? 0u : 1u);
+#pragma unroll
+        for (int kk = 1; kk < 8; ++kk) {
+          const uint32_t acol = kk < 4 ? kk * 8 : 64 + (kk - 4) * 8;
+          mma_ts_lo(tmem + 384, a + acol, b0 + ((kk * 2048) >> 4), idDQ, 1u);
         }
         mma_commit(bar_addr(sbase, B_K_EMPTY + kc_q % kKStages));
         if (rec[0].last_of_unit) mma_commit(bar_addr(sbase, B_DQ_DONE));

@@ -194,19 +194,29 @@ replay_fwd_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a, con
     TileRec cur, nxt;
     uint32_t ring = 0, units = 0, kc = 0;
     bool ok = cursor.next(&cur);
+    // Descriptor bases built once; every MMA below only adds a compile-time offset
+    // (descriptor start addresses are in 16-byte units in the low bits), so the single
+    // issuing thread keeps the tensor core fed instead of rebuilding 64-bit
+    // descriptors through a dependent chain of integer ops per instruction.
+    const uint32_t dq_base = sdesc_lo(sbase + kOffQ, 16);
+    const uint32_t dk_base = sdesc_lo(sbase + kOffRing, 16);
+    const uint32_t dv_base = sdesc_lo(sbase + kOffRing, kHalfBytes);
     auto issue_s = [&](int t, uint32_t kstage) {
-      const uint32_t qa = sbase + kOffQ + t * kTileBytes;
-      const uint32_t kb = sbase + kOffRing + kstage * kTileBytes;
+      const uint32_t a0 = dq_base + ((t * kTileBytes) >> 4);
+      const uint32_t b0 = dk_base + ((kstage * kTileBytes) >> 4);
+      const uint32_t d = tmem + t * kTile;
+#pragma unroll
       for (int kk = 0; kk < 8; ++kk) {
-        const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-        mma_ss(tmem + t * kTile, sdesc_kmajor(qa + off), sdesc_kmajor(kb + off), idS, kk > 0);
+        const uint32_t off = ((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4;
+        mma_ss_lo(d, a0 + off, b0 + off, idS, kk > 0);
       }
     };
     auto issue_pv = [&](int t, uint32_t vstage, bool accumulate) {
-      const uint32_t vb = sbase + kOffRing + vstage * kTileBytes;
-      for (int kk = 0; kk < 8; ++kk)
-        mma_ts(tmem + 256 + t * kTile, tmem + t * kTile + kk * 8,
-               sdesc_mnmajor(vb + kk * 2048, kHalfBytes), idPV, (accumulate || kk > 0) ? 1u : 0u);
+      const uint32_t b0 = dv_base + ((vstage * kTileBytes) >> 4);
+      const uint32_t d = tmem + 256 + t * kTile, a = tmem + t * kTile;
+      mma_ts_lo(d, a, b0, idPV, accumulate ? 1u : 0u);
+#pragma unroll
+      for (int kk = 1; kk < 8; ++kk) mma_ts_lo(d, a + kk * 8, b0 + ((kk * 2048) >> 4), idPV, 1u);
     };
     uint32_t kstage = 0;
     if (ok) {
