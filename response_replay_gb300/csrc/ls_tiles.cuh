@@ -21,17 +21,22 @@ struct TileCursor {
   int32_t u, s, t, t_end;
   bool item_first, item_last, item_complete, valid;
   int32_t R, g, nTB;
+  int32_t h, kvh, t0;  // derived from u once per item, not per tile
+  bool resp;
 
   __device__ TileCursor(const LsSched& sc, int cta, int32_t R_, int32_t g_)
       : walk(sc, cta), u(0), s(0), t(0), t_end(0), item_first(false), item_last(false),
-        item_complete(false), valid(false), R(R_), g(g_) {
+        item_complete(false), valid(false), R(R_), g(g_), h(0), kvh(0), t0(0), resp(false) {
     nTB = (R + UnitRows - 1) / UnitRows;
   }
 
   __device__ bool open_item() {
     while (walk.next(&u, &s, &item_first, &item_last, &item_complete)) {
-      if (s == walk.sc.nsplit) {
-        const int32_t t0 = (u % nTB) * UnitRows;
+      h = u / nTB;
+      t0 = (u - h * nTB) * UnitRows;
+      kvh = h / g;
+      resp = (s == walk.sc.nsplit);
+      if (resp) {
         const int32_t qe = t0 + UnitRows < R ? t0 + UnitRows : R;
         t = 0;
         t_end = (qe + Tile - 1) / Tile;
@@ -52,10 +57,10 @@ struct TileCursor {
       r->first_of_unit = false;
     }
     r->u = u;
-    r->h = u / nTB;
-    r->t0 = (u % nTB) * UnitRows;
-    r->kvh = r->h / g;
-    r->resp = (s == walk.sc.nsplit);
+    r->h = h;
+    r->t0 = t0;
+    r->kvh = kvh;
+    r->resp = resp;
     r->key0 = t * Tile;
     ++t;
     r->last_of_unit = item_last && t >= t_end;

@@ -348,10 +348,17 @@ bwd_dq_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a, const L
         reg_fence32(sv);
         reg_fence32(pv);
         float d2[32];
+        const float2 c2 = make_float2(c, c), nl2 = make_float2(-lse2, -lse2);
+        const float2 nd2 = make_float2(-dd, -dd);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const float p = fast_exp2(fmaf(__uint_as_float(sv[i]), c, -lse2));
-          d2[i] = p * (__uint_as_float(pv[i]) - dd);
+        for (int i = 0; i < 32; i += 2) {  // packed fp32x2 arithmetic
+          float2 x = __ffma2_rn(make_float2(__uint_as_float(sv[i]), __uint_as_float(sv[i + 1])), c2, nl2);
+          x.x = fast_exp2(x.x);
+          x.y = fast_exp2(x.y);
+          const float2 dpm = __fadd2_rn(make_float2(__uint_as_float(pv[i]), __uint_as_float(pv[i + 1])), nd2);
+          const float2 ds2 = __fmul2_rn(x, dpm);
+          d2[i] = ds2.x;
+          d2[i + 1] = ds2.y;
         }
         if (col0 + 32 > lim) {  // only the ragged prompt tail and the diagonal need a mask
 #pragma unroll

@@ -10,7 +10,7 @@
 // CTA (one per SM, persistent, 12 warps) owns a unit = 256 consecutive response tokens
 // of one query head, as two 128-row tiles A and B that share every K/V tile:
 //   warp 0      TMA producer: Q tiles, then K and V tiles (128 keys x 128 dims, two
-//               128-byte-swizzled halves each) into a 4-stage ring; prompt tiles are
+//               128-byte-swizzled halves each) into a 5-stage ring; prompt tiles are
 //               gathered page by page through the page table.
 //   warp 1      MMA issuer (one thread): S_t = Q_t K^T into tensor memory (SS MMA,
 //               M=128 N=128 K=128), O_t += P_t V with P_t read from tensor memory (TS
@@ -39,13 +39,12 @@ using namespace umma;
 constexpr int kD = 128;
 constexpr int kTile = 128;                 // query rows per tile, keys per KV tile
 constexpr int kUnitRows = 2 * kTile;       // tokens per unit
-constexpr int kStages = 4;
+constexpr int kStages = 5;
 constexpr int kThreads = 384;
 // Register split (setmaxnreg): the launch gives 168 per thread (384 x 168 = 64512);
-// warpgroup 0 (TMA + MMA control, ~100 live registers) drops to 112 and the two softmax
-// warpgroups (a full 128-column S row per thread) rise to 192:
-// 128 x 112 + 256 x 192 = 63488 <= 64512.
-constexpr int kRegsLaunch = 168, kRegsControl = 112, kRegsSoftmax = 192;
+// warpgroup 0 (TMA + MMA control) drops to 120 and the two softmax warpgroups (a full
+// 128-column S row per thread) rise to 184: 128 x 120 + 256 x 184 = 62464 <= 64512.
+constexpr int kRegsLaunch = 168, kRegsControl = 120, kRegsSoftmax = 184;
 static_assert(128 * kRegsControl + 256 * kRegsSoftmax <= kThreads * kRegsLaunch, "register split");
 constexpr uint32_t kTileBytes = kTile * kD * 2;  // 32 KB
 constexpr uint32_t kHalfBytes = kTileBytes / 2;  // 16 KB: 128 rows x 64 dims
@@ -372,16 +371,27 @@ replay_fwd_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a, con
         rescale = true;
       }
       const float msub = (m == -INFINITY) ? 0.f : m;
-      float ls8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-      uint32_t pk[64];
+      // packed fp32x2 arithmetic: one instruction per pair of columns
+      const float2 c2 = make_float2(c, c), nm2 = make_float2(-msub, -msub);
+      float2 ls4[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                       make_float2(0.f, 0.f)};
 #pragma unroll
-      for (int j = 0; j < 64; ++j) {
-        const float p0 = fast_exp2(fmaf(__uint_as_float(sr[2 * j]), c, -msub));
-        const float p1 = fast_exp2(fmaf(__uint_as_float(sr[2 * j + 1]), c, -msub));
-        ls8[j & 7] += p0 + p1;
-        pk[j] = pack_bf16(p0, p1);
+      for (int half = 0; half < 2; ++half) {  // P in two 64-column halves
+        uint32_t pk[32];
+#pragma unroll
+        for (int jj = 0; jj < 32; ++jj) {
+          const int j = half * 32 + jj;
+          float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[2 * j]), __uint_as_float(sr[2 * j + 1])),
+                                c2, nm2);
+          x.x = fast_exp2(x.x);
+          x.y = fast_exp2(x.y);
+          ls4[jj & 3] = __fadd2_rn(ls4[jj & 3], x);
+          pk[jj] = pack_bf16(x.x, x.y);
+        }
+        tmem_st32(s_col + half * 32, pk);
       }
-      const float ls = ((ls8[0] + ls8[1]) + (ls8[2] + ls8[3])) + ((ls8[4] + ls8[5]) + (ls8[6] + ls8[7]));
+      const float2 lsa = __fadd2_rn(__fadd2_rn(ls4[0], ls4[1]), __fadd2_rn(ls4[2], ls4[3]));
+      const float ls = lsa.x + lsa.y;
       {
         const float tsum = l + ls;
         lcomp += (l - tsum) + ls;
@@ -399,8 +409,6 @@ replay_fwd_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a, con
           tmem_st32(o_col + c0, ov);
         }
       }
-      tmem_st32(s_col + 0, pk);
-      tmem_st32(s_col + 32, pk + 32);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar_addr(sbase, B_P_FULL + t));
