@@ -420,7 +420,10 @@ bwd_dq_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a, const L
   }
 }
 
-// Sum the split partials of each tail unit in CTA order; one block per unit.
+// Sum the split partials of each tail unit in CTA order.
+// Grid: (tail units, row groups of kCombineRows); one thread per head_dim column.
+constexpr int kCombineRows = 8;
+constexpr int kMaxSlots = 1024;
 __global__ void __launch_bounds__(kD) bwd_dq_tc_combine(const LsAttnArgs a, const LsSched sc,
                                                         const LsBwdIn b) {
   const int u = sc.tail_unit0() + blockIdx.x;
@@ -428,15 +431,24 @@ __global__ void __launch_bounds__(kD) bwd_dq_tc_combine(const LsAttnArgs a, cons
   const int64_t i0 = (int64_t)(u - sc.tail_unit0()) * ipu;
   const int c_lo = sc.tail_cta_of(i0), c_hi = sc.tail_cta_of(i0 + ipu - 1);
   if (c_lo == c_hi) return;
+  __shared__ int s_slot[kMaxSlots];
+  __shared__ int s_n;
+  if (threadIdx.x == 0) {
+    int n = 0;
+    for (int cc = c_lo; cc <= c_hi && n < kMaxSlots; ++cc)
+      if (sc.tail_nonempty(cc)) s_slot[n++] = sc.slot_of(cc, u);
+    s_n = n;
+  }
+  __syncthreads();
+  const int n = s_n;
   const int nTB = (a.R + kUnitRows - 1) / kUnitRows;
   const int h = u / nTB, t0 = (u % nTB) * kUnitRows;
   const int col = threadIdx.x;
-  for (int r = 0; r < kUnitRows; ++r) {
+  for (int r = blockIdx.y * kCombineRows; r < (blockIdx.y + 1) * kCombineRows; ++r) {
     const int t = t0 + r;
     if (t >= a.R) break;
     float acc = 0.f;
-    for (int cc = c_lo; cc <= c_hi; ++cc)
-      if (sc.tail_nonempty(cc)) acc += b.part_dq[((int64_t)sc.slot_of(cc, u) * kUnitRows + r) * kD + col];
+    for (int i = 0; i < n; ++i) acc += b.part_dq[((int64_t)s_slot[i] * kUnitRows + r) * kD + col];
     float* dst = b.dq + ((int64_t)t * a.hq + h) * kD + col;
     *dst = b.accumulate ? *dst + acc : acc;
   }
@@ -481,7 +493,7 @@ cudaError_t ls_launch_bwd_dq(const LsAttnArgs& a, const LsSched& sc, const LsBwd
   ls_note_launch();
   const int64_t tail_units = sc.units - (int64_t)sc.waves * sc.ctas;
   if (tail_units > 0) {
-    bwd_dq_tc_combine<<<(unsigned)tail_units, kD, 0, st>>>(a, sc, b);
+    bwd_dq_tc_combine<<<dim3((unsigned)tail_units, kUnitRows / kCombineRows), kD, 0, st>>>(a, sc, b);
     e = cudaGetLastError();
     if (e == cudaSuccess) ls_note_launch();
   }
