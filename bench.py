@@ -76,6 +76,31 @@ def traffic_from_profile(kernel_file: str, kernel: str):
     return float(t.group(1))
 
 
+# ------------------------------------------------------------------ ranks
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """The largest value of x over all ranks (every rank receives it): the whole job
+    takes as long as its slowest rank."""
+    if world <= 1:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank_step: float, world: int, ms_per_step: float) -> float:
+    """Units per second of the whole job: every rank processes the same number of
+    independent units per step (weak scaling), and the step lasts the slowest rank's
+    time."""
+    return units_per_rank_step * world / (ms_per_step * 1e-3)
+
+
+def rank_seed(base: int, rank: int) -> int:
+    """Each rank replays its own independent problem, drawn from its own seed."""
+    return base + 1000 * rank
+
+
 # ------------------------------------------------------------------ clocks
 
 class ClockSampler:
@@ -151,7 +176,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     w = syn.WORKLOADS[args.workload]
     G = w.G if args.members is None else args.members
     R = w.R[0]
-    seed = syn.seed_of(args.workload) + 1000 * rank
+    seed = rank_seed(syn.seed_of(args.workload), rank)
     scale = D ** -0.5
     stream = torch.cuda.current_stream()
 
@@ -241,11 +266,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
             marks_all.append(step(marks=True))
         t1 = ev()
         torch.cuda.synchronize()
-    total_ms = t0.elapsed_time(t1)
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(t0.elapsed_time(t1), world, dev)
     assert B.ls_last_device_error(0) == B.LS_OK
     assert torch.isfinite(loss).all() and torch.isfinite(dq).all()
 
@@ -261,7 +282,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     f_fwd, f_bwd = attn_flops(w.P, R, w.hq)
     step_flops = G * (f_fwd + f_bwd)
     ms_per_step = total_ms / K
-    value = step_flops * world / (ms_per_step * 1e-3) / 1e12
+    value = whole_job_rate(step_flops, world, ms_per_step) / 1e12
     kv_bytes = prompt_kv_bytes(w.P, w.hkv)
     comps = {
         "attn_fwd_tflops": G * K * f_fwd / (fwd_ms * 1e-3) / 1e12,
@@ -277,10 +298,10 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     # dominant launch: the larger of the per-member backward and forward calls
     if bwd_ms >= fwd_ms:
         dom, dom_flops, dom_ms, kfile, kname = "replay_attn_bwd", f_bwd, bwd_ms / (K * G), \
-            "replay_bwd.cu", "bwd_dq_kernel"
+            "replay_bwd_dq_tc.cu", "bwd_dq_tc_kernel"
     else:
         dom, dom_flops, dom_ms, kfile, kname = "replay_attn_fwd", f_fwd, fwd_ms / (K * G), \
-            "replay_fwd.cu", "replay_fwd_kernel"
+            "replay_fwd_tc.cu", "replay_fwd_tc_kernel"
     achieved = dom_flops / (dom_ms * 1e-3) / 1e12
     roofline = {"bound": "tensor", "kernel": kname, "timed": f"{dom} call (CUDA events)",
                 "achieved": achieved, "peak": peak, "peak_source": f"{pk_src} bf16 sustained",
@@ -332,12 +353,8 @@ def run_ours(args, rank: int, world: int, local_rank: int):
             e2e_step()
         b = ev()
         torch.cuda.synchronize()
-        e_ms = a.elapsed_time(b)
-        if world > 1:
-            t = torch.tensor([e_ms], device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            e_ms = float(t.item())
-        e2e = {"value": step_flops * world / (e_ms / K * 1e-3) / 1e12, "unit": "TFLOP/s",
+        e_ms = max_over_ranks(a.elapsed_time(b), world, dev)
+        e2e = {"value": whole_job_rate(step_flops, world, e_ms / K) / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": d2h,
                "ms_per_step": e_ms / K}
 
