@@ -12,11 +12,11 @@
 //   warp 0      TMA producer: Q tiles, then K and V tiles (128 keys x 128 dims, two
 //               128-byte-swizzled halves each) into a 5-stage ring; prompt tiles are
 //               gathered page by page through the page table.
-//   warp 1      MMA issuer (one thread): S_t = Q_t K^T into tensor memory (SS MMA,
-//               M=128 N=128 K=128), O_t += P_t V with P_t read from tensor memory (TS
-//               MMA); ping-pong between tiles A and B so the tensor core always has
-//               the other tile's work while one tile's softmax runs.
-//   warps 2-3   idle (they complete warpgroup 0, whose registers go to the softmax)
+//   warps 1, 2  MMA issuers, one thread each, for tile A and tile B: S_t = Q_t K^T into
+//               tensor memory (SS MMA, M=128 N=128 K=128), O_t += P_t V with P_t read
+//               from tensor memory (TS MMA); the two tiles' MMAs interleave on the tensor
+//               core, so it has one tile's work while the other tile's softmax runs.
+//   warp 3      idle (it completes warpgroup 0, whose registers go to the softmax)
 //   warps 4-7   softmax of tile A, warps 8-11 softmax of tile B: each thread owns one
 //               query row; reads its S row from tensor memory, masks, updates the
 //               running max (log2 domain; O is rescaled only when the max grows by more
@@ -42,9 +42,9 @@ constexpr int kUnitRows = 2 * kTile;       // tokens per unit
 constexpr int kStages = 5;
 constexpr int kThreads = 384;
 // Register split (setmaxnreg): the launch gives 168 per thread (384 x 168 = 64512);
-// warpgroup 0 (TMA + MMA control) drops to 120 and the two softmax warpgroups (a full
-// 128-column S row per thread) rise to 184: 128 x 120 + 256 x 184 = 62464 <= 64512.
-constexpr int kRegsLaunch = 168, kRegsControl = 120, kRegsSoftmax = 184;
+// warpgroup 0 (TMA + MMA control) drops to 112 and the two softmax warpgroups (a full
+// 128-column S row per thread) rise to 192: 128 x 112 + 256 x 192 = 63488 <= 64512.
+constexpr int kRegsLaunch = 168, kRegsControl = 112, kRegsSoftmax = 192;
 static_assert(128 * kRegsControl + 256 * kRegsSoftmax <= kThreads * kRegsLaunch, "register split");
 constexpr uint32_t kTileBytes = kTile * kD * 2;  // 32 KB
 constexpr uint32_t kHalfBytes = kTileBytes / 2;  // 16 KB: 128 rows x 64 dims
@@ -64,8 +64,10 @@ enum {
   B_S_FULL,          // 2
   B_P_FULL = B_S_FULL + 2,
   B_O_DONE = B_P_FULL + 2,
-  B_DONE = B_O_DONE + 2,
-  B_COUNT
+  B_DONE = B_O_DONE + 2,   // 2
+  B_AUX = B_DONE + 2,      // producer: ragged V tile landed
+  B_PV_DONE,               // 2: P_t V of a tile finished (orders the issuers)
+  B_COUNT = B_PV_DONE + 2
 };
 static_assert(B_COUNT * 8 + 16 <= 256, "barrier area");
 
@@ -91,16 +93,18 @@ replay_fwd_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a, con
   if (tid == 0) {
     for (int i = 0; i < kStages; ++i) {
       mbar_init(bar_addr(sbase, B_KV_FULL + i), 1);
-      mbar_init(bar_addr(sbase, B_KV_EMPTY + i), 1);
+      mbar_init(bar_addr(sbase, B_KV_EMPTY + i), 2);  // one commit per issuer
     }
     mbar_init(bar_addr(sbase, B_Q_FULL), 1);
-    mbar_init(bar_addr(sbase, B_Q_EMPTY), 1);
+    mbar_init(bar_addr(sbase, B_Q_EMPTY), 2);
+    mbar_init(bar_addr(sbase, B_AUX), 1);
     for (int t = 0; t < 2; ++t) {
       mbar_init(bar_addr(sbase, B_S_FULL + t), 1);
       mbar_init(bar_addr(sbase, B_P_FULL + t), kTile);
       mbar_init(bar_addr(sbase, B_O_DONE + t), 1);
+      mbar_init(bar_addr(sbase, B_DONE + t), 1);
+      mbar_init(bar_addr(sbase, B_PV_DONE + t), 1);
     }
-    mbar_init(bar_addr(sbase, B_DONE), 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -130,7 +134,7 @@ replay_fwd_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a, con
       tma_prefetch_desc(&tm.vr);
       FwdCursor cur(sc, blockIdx.x, a.R, a.g);
       TileRec r;
-      uint32_t ring = 0, units = 0;
+      uint32_t ring = 0, units = 0, aux = 0;
       const int32_t ps = 1 << a.ps_log2;
       const int32_t box_rows = ps < kTile ? ps : kTile;
       const int32_t pool_rows = a.num_pages * a.hkv * ps;
@@ -154,7 +158,11 @@ replay_fwd_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a, con
             break;
           }
           if (*abort_flag) { ok = false; break; }
-          const uint32_t fb = bar_addr(sbase, B_KV_FULL + st);
+          // The last prompt tile may end inside a page whose later slots hold stale data
+          // (even NaN); P is 0 there but 0 x NaN is not, so those V rows are zeroed
+          // before the tile is handed to the MMA issuers.
+          const bool ragged_v = kv == 1 && !r.resp && r.key0 + kTile > a.P;
+          const uint32_t fb = bar_addr(sbase, ragged_v ? B_AUX : B_KV_FULL + st);
           const uint32_t dst = sbase + kOffRing + st * kTileBytes;
           mbar_expect_tx(fb, kTileBytes);
           if (r.resp) {
@@ -177,6 +185,18 @@ replay_fwd_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a, con
                 tma_load_2d(dst + hf * kHalfBytes + b * box_rows * 128, map, hf * 64, y, fb);
             }
           }
+          if (ragged_v) {
+            if (!mbar_wait(fb, aux & 1)) { fail(); ok = false; break; }
+            ++aux;
+            uint8_t* vb = smem + kOffRing + st * kTileBytes;
+            for (int i = (int)(a.P - r.key0) * 8; i < kTile * 8; ++i) {
+              const int row = i >> 3, c = i & 7;
+              *reinterpret_cast<uint4*>(vb + row * 128 + c * 16) = make_uint4(0, 0, 0, 0);
+              *reinterpret_cast<uint4*>(vb + kHalfBytes + row * 128 + c * 16) = make_uint4(0, 0, 0, 0);
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(bar_addr(sbase, B_KV_FULL + st));
+          }
           ++ring;
         }
       }
@@ -185,129 +205,96 @@ replay_fwd_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a, con
         mbar_wait(bar_addr(sbase, B_KV_FULL + i % kStages), (i / kStages) & 1);
       if (units > 0) mbar_wait(bar_addr(sbase, B_Q_FULL), (units - 1) & 1);
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    const uint32_t idS = idesc_bf16_f32(kTile, kTile, false);
-    const uint32_t idPV = idesc_bf16_f32(kTile, kD, true);
-    FwdCursor cursor(sc, blockIdx.x, a.R, a.g);
-    TileRec cur, nxt;
-    uint32_t ring = 0, units = 0, kc = 0;
-    bool ok = cursor.next(&cur);
-    // Descriptor bases built once; every MMA below only adds a compile-time offset
-    // (descriptor start addresses are in 16-byte units in the low bits), so the single
-    // issuing thread keeps the tensor core fed instead of rebuilding 64-bit
-    // descriptors through a dependent chain of integer ops per instruction.
-    const uint32_t dq_base = sdesc_lo(sbase + kOffQ, 16);
-    const uint32_t dk_base = sdesc_lo(sbase + kOffRing, 16);
-    const uint32_t dv_base = sdesc_lo(sbase + kOffRing, kHalfBytes);
-    auto issue_s = [&](int t, uint32_t kstage) {
-      const uint32_t a0 = dq_base + ((t * kTileBytes) >> 4);
-      const uint32_t b0 = dk_base + ((kstage * kTileBytes) >> 4);
-      const uint32_t d = tmem + t * kTile;
+  } else if (warp == 1 || warp == 2) {
+    // ------------------------------------------------------------ MMA issuers
+    // One thread per tile: warp 1 drives tile A, warp 2 tile B.  A tcgen05.mma issue
+    // stalls the issuing thread while the tensor core's queue is full, so a single
+    // thread driving both tiles could not take up one tile's finished P while it sat in
+    // the other tile's issue; with one thread per tile each tile's S -> softmax -> P V
+    // loop runs on its own and the two interleave on the tensor core.
+    if (lane == 0) {
+      const int t = warp - 1;
+      const uint32_t idS = idesc_bf16_f32(kTile, kTile, false);
+      const uint32_t idPV = idesc_bf16_f32(kTile, kD, true);
+      // Descriptor bases built once; every MMA below only adds a compile-time offset
+      // (descriptor start addresses are in 16-byte units in the low bits).
+      const uint32_t dq = sdesc_lo(sbase + kOffQ + t * kTileBytes, 16);
+      const uint32_t dk_base = sdesc_lo(sbase + kOffRing, 16);
+      const uint32_t dv_base = sdesc_lo(sbase + kOffRing, kHalfBytes);
+      const uint32_t d_s = tmem + t * kTile, d_o = tmem + 256 + t * kTile;
+      auto issue_s = [&](uint32_t kstage) {
+        const uint32_t b0 = dk_base + ((kstage * kTileBytes) >> 4);
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        const uint32_t off = ((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4;
-        mma_ss_lo(d, a0 + off, b0 + off, idS, kk > 0);
-      }
-    };
-    auto issue_pv = [&](int t, uint32_t vstage, bool accumulate) {
-      const uint32_t b0 = dv_base + ((vstage * kTileBytes) >> 4);
-      const uint32_t d = tmem + 256 + t * kTile, a = tmem + t * kTile;
-      mma_ts_lo(d, a, b0, idPV, accumulate ? 1u : 0u);
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t off = ((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4;
+          mma_ss_lo(d_s, dq + off, b0 + off, idS, kk > 0);
+        }
+      };
+      auto issue_pv = [&](uint32_t vstage, bool accumulate) {
+        const uint32_t b0 = dv_base + ((vstage * kTileBytes) >> 4);
+        mma_ts_lo(d_o, d_s, b0, idPV, accumulate ? 1u : 0u);
 #pragma unroll
-      for (int kk = 1; kk < 8; ++kk) mma_ts_lo(d, a + kk * 8, b0 + ((kk * 2048) >> 4), idPV, 1u);
-    };
-    uint32_t kstage = 0;
-    if (ok) {
-      // prologue: S_A(0), S_B(0)
-      if (lane == 0) {
+        for (int kk = 1; kk < 8; ++kk) mma_ts_lo(d_o, d_s + kk * 8, b0 + ((kk * 2048) >> 4), idPV, 1u);
+      };
+      FwdCursor cursor(sc, blockIdx.x, a.R, a.g);
+      TileRec cur, nxt;
+      uint32_t ring = 0, units = 0, kc = 0;
+      bool ok = cursor.next(&cur);
+      // S_t of the first tile
+      if (ok) {
         if (!mbar_wait(bar_addr(sbase, B_Q_FULL), units & 1)) { fail(); ok = false; }
-        kstage = ring % kStages;
+        ++units;
+        const uint32_t kstage = ring % kStages;
         if (ok && !mbar_wait(bar_addr(sbase, B_KV_FULL + kstage), (ring / kStages) & 1)) { fail(); ok = false; }
+        ++ring;
         if (ok) {
           tc_fence_after();
-          issue_s(0, kstage);
-          mma_commit(bar_addr(sbase, B_S_FULL + 0));
-          issue_s(1, kstage);
-          mma_commit(bar_addr(sbase, B_S_FULL + 1));
+          issue_s(kstage);
+          mma_commit(bar_addr(sbase, B_S_FULL + t));
           mma_commit(bar_addr(sbase, B_KV_EMPTY + kstage));
           if (cur.last_of_unit) mma_commit(bar_addr(sbase, B_Q_EMPTY));
         }
       }
-      ++units;
-      ++ring;
-      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-    }
-    while (ok) {
-      const bool has_nxt = cursor.next(&nxt);
-      // V of the current tile
-      const uint32_t vstage = ring % kStages;
-      const uint32_t vpar = (ring / kStages) & 1;
-      ++ring;
-      if (lane == 0 && !mbar_wait(bar_addr(sbase, B_KV_FULL + vstage), vpar)) { fail(); ok = false; }
-      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-      if (!ok) break;
-      if (!cur.resp && cur.key0 + kTile > a.P) {
-        // ragged last prompt tile: rows past the prompt end may hold stale page data;
-        // zero them so that 0-probability rows cannot inject NaN/Inf into P V.
-        const int valid = (int)(a.P - cur.key0);
-        mbar_wait(bar_addr(sbase, B_KV_FULL + vstage), vpar);
-        uint8_t* vb = smem + kOffRing + vstage * kTileBytes;
-        for (int i = valid * 8 + lane; i < kTile * 8; i += 32) {
-          const int row = i >> 3, c = i & 7;
-          *reinterpret_cast<uint4*>(vb + row * 128 + c * 16) = make_uint4(0, 0, 0, 0);
-          *reinterpret_cast<uint4*>(vb + kHalfBytes + row * 128 + c * 16) = make_uint4(0, 0, 0, 0);
+      while (ok) {
+        const bool has_nxt = cursor.next(&nxt);
+        // P_t V of the current tile
+        const uint32_t vstage = ring % kStages;
+        if (!mbar_wait(bar_addr(sbase, B_KV_FULL + vstage), (ring / kStages) & 1)) { fail(); break; }
+        ++ring;
+        if (!mbar_wait(bar_addr(sbase, B_P_FULL + t), kc & 1)) { fail(); break; }
+        // Keep the tiles half a period apart: tile B's group for tile k follows tile A's
+        // P V of tile k, tile A's group for tile k follows tile B's P V of tile k - 1.
+        // Each group then lands in the tensor core's queue while the other tile's S is
+        // still running, and each tile's softmax overlaps the other tile's MMAs instead
+        // of both softmax warpgroups contending for the exp2 units at the same time.
+        if (t == 1 && !mbar_wait(bar_addr(sbase, B_PV_DONE + 0), kc & 1)) { fail(); break; }
+        if (t == 0 && kc > 0 && !mbar_wait(bar_addr(sbase, B_PV_DONE + 1), (kc - 1) & 1)) { fail(); break; }
+        ++kc;
+        tc_fence_after();
+        issue_pv(vstage, !cur.first_of_unit);
+        mma_commit(bar_addr(sbase, B_PV_DONE + t));
+        if (cur.last_of_unit) mma_commit(bar_addr(sbase, B_O_DONE + t));
+        mma_commit(bar_addr(sbase, B_KV_EMPTY + vstage));
+        if (!has_nxt) break;
+        // S_t of the next tile (after P_t V in issue order: it overwrites P_t)
+        if (nxt.first_of_unit) {
+          if (!mbar_wait(bar_addr(sbase, B_Q_FULL), units & 1)) { fail(); break; }
+          ++units;
         }
-        fence_proxy_async_smem();
-        __syncwarp();
+        const uint32_t kstage = ring % kStages;
+        if (!mbar_wait(bar_addr(sbase, B_KV_FULL + kstage), (ring / kStages) & 1)) { fail(); break; }
+        ++ring;
+        tc_fence_after();
+        issue_s(kstage);
+        mma_commit(bar_addr(sbase, B_S_FULL + t));
+        mma_commit(bar_addr(sbase, B_KV_EMPTY + kstage));
+        if (nxt.last_of_unit) mma_commit(bar_addr(sbase, B_Q_EMPTY));
+        cur = nxt;
       }
-      const bool nxt_new_unit = has_nxt && nxt.first_of_unit;
-      if (lane == 0) {
-        // tile A: PV_A(cur), then S_A(nxt)
-        if (!mbar_wait(bar_addr(sbase, B_P_FULL + 0), kc & 1)) { fail(); ok = false; }
-        if (ok) {
-          tc_fence_after();
-          issue_pv(0, vstage, !cur.first_of_unit);
-          if (cur.last_of_unit) mma_commit(bar_addr(sbase, B_O_DONE + 0));
-        }
-        if (ok && has_nxt) {
-          if (nxt_new_unit && !mbar_wait(bar_addr(sbase, B_Q_FULL), units & 1)) { fail(); ok = false; }
-          kstage = ring % kStages;
-          if (ok && !mbar_wait(bar_addr(sbase, B_KV_FULL + kstage), (ring / kStages) & 1)) { fail(); ok = false; }
-          if (ok) {
-            tc_fence_after();
-            issue_s(0, kstage);
-            mma_commit(bar_addr(sbase, B_S_FULL + 0));
-          }
-        }
-        // tile B: PV_B(cur), then S_B(nxt)
-        if (ok && !mbar_wait(bar_addr(sbase, B_P_FULL + 1), kc & 1)) { fail(); ok = false; }
-        if (ok) {
-          tc_fence_after();
-          issue_pv(1, vstage, !cur.first_of_unit);
-          if (cur.last_of_unit) mma_commit(bar_addr(sbase, B_O_DONE + 1));
-          mma_commit(bar_addr(sbase, B_KV_EMPTY + vstage));
-          if (has_nxt) {
-            issue_s(1, kstage);
-            mma_commit(bar_addr(sbase, B_S_FULL + 1));
-            mma_commit(bar_addr(sbase, B_KV_EMPTY + kstage));
-            if (nxt.last_of_unit) mma_commit(bar_addr(sbase, B_Q_EMPTY));
-          }
-        }
-      }
-      if (nxt_new_unit) ++units;
-      if (has_nxt) ++ring;
-      ++kc;
-      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-      if (!has_nxt) break;
-      cur = nxt;
+      // every MMA this thread issued has finished before tensor memory is released
+      mma_commit(bar_addr(sbase, B_DONE + t));
+      mbar_wait(bar_addr(sbase, B_DONE + t), 0);
     }
-    // make sure every issued MMA has finished before tensor memory is released
-    if (lane == 0) {
-      mma_commit(bar_addr(sbase, B_DONE));
-      mbar_wait(bar_addr(sbase, B_DONE), 0);
-    }
-    __syncwarp();
   }
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
