@@ -336,14 +336,17 @@ replay_fwd_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a, con
         for (int j = 0; j < 128; ++j)
           if (j >= lim) sr[j] = __float_as_uint(-INFINITY);
       }
-      // row max with 8 independent chains (latency, not throughput, bounds one row)
+      // row max: 8 independent chains of three-operand max
       float mx8[8];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) mx8[k] = __uint_as_float(sr[k]);
+      for (int k = 0; k < 8; ++k) mx8[k] = fmaxf(__uint_as_float(sr[k]), __uint_as_float(sr[k + 8]));
 #pragma unroll
-      for (int j = 8; j < 128; ++j) mx8[j & 7] = fmaxf(mx8[j & 7], __uint_as_float(sr[j]));
-      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+      for (int j = 16; j < 128; j += 16)
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          mx8[k] = fmax3(mx8[k], __uint_as_float(sr[j + k]), __uint_as_float(sr[j + 8 + k]));
+      const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
+                             fmaxf(mx8[6], mx8[7]));
       const float mt = mx * c;
       bool rescale = false;
       float alpha = 1.f;
