@@ -10,11 +10,14 @@
 // CTA (one per SM, persistent, 12 warps) owns a unit = 128 consecutive response tokens
 // of one query head; Q and dO stay in shared memory while K/V tiles stream past:
 //   warp 0      TMA producer: Q and dO tiles, then K (3-stage ring) and V (2-stage ring)
-//               tiles of 128 keys, prompt tiles gathered page by page.
-//   warp 1      MMA issuer: S = Q K^T (SS, into one of two S buffers), dP = dO V^T (SS),
-//               dQ += dS K (TS: dS from tensor memory, K as an MN-major operand).
-//               Order per tile j: dP(j+1), dQ(j), S(j+2), so the tensor core works on
-//               the next tiles while the softmax warps turn S(j), dP(j) into dS(j).
+//               tiles of 128 keys, prompt tiles gathered page by page; rows of a ragged
+//               last prompt K tile are zeroed before the tile is handed over.
+//   warp 1      MMA issuer (one thread): S = Q K^T (SS, into one of two S buffers),
+//               dP = dO V^T (SS), dQ += dS K (TS: dS from tensor memory, K as an
+//               MN-major operand).  Per tile j, after dS(j) is in tensor memory:
+//               S(j+1), dP(j+1), dQ(j) back to back; the dS warps turn S(j+1), dP(j+1)
+//               into dS(j+1) while dQ(j) runs.  A K tile lives from S(j) to dQ(j), so
+//               the 3-stage ring gives each K load about two tiles of lead time.
 //   warps 2-3   idle (complete warpgroup 0)
 //   warps 4-7 / 8-11  two warpgroups split the 128 key columns of each query row (64
 //               each): p = exp2(s scale log2e - lse log2e), ds = p (dp - D), packed as
@@ -60,6 +63,7 @@ enum {
   B_DS_FULL,
   B_DQ_DONE,
   B_DONE,
+  B_AUX,  // producer: ragged K tile landed
   B_COUNT
 };
 static_assert(B_COUNT * 8 + 16 <= 256, "barrier area");
@@ -100,6 +104,7 @@ bwd_dq_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a, const L
     mbar_init(bar_addr(sbase, B_DS_FULL), 256);
     mbar_init(bar_addr(sbase, B_DQ_DONE), 1);
     mbar_init(bar_addr(sbase, B_DONE), 1);
+    mbar_init(bar_addr(sbase, B_AUX), 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -127,7 +132,7 @@ bwd_dq_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a, const L
       tma_prefetch_desc(&tm.vr);
       DqCursor cur(sc, blockIdx.x, a.R, a.g);
       TileRec r;
-      uint32_t kc = 0, vc = 0, units = 0;
+      uint32_t kc = 0, vc = 0, units = 0, aux = 0;
       const int32_t ps = 1 << a.ps_log2;
       const int32_t box_rows = ps < kTile ? ps : kTile;
       const int32_t pool_rows = a.num_pages * a.hkv * ps;
@@ -151,7 +156,11 @@ bwd_dq_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a, const L
           const int bf = (kv == 0 ? B_K_FULL : B_V_FULL) + st;
           if (!mbar_wait(bar_addr(sbase, be), ((cnt / nst) & 1) ^ 1)) { fail(); ok = false; break; }
           if (*abort_flag) { ok = false; break; }
-          const uint32_t fb = bar_addr(sbase, bf);
+          // K rows past the end of a ragged last prompt tile may hold stale page data
+          // (even NaN); their dS is 0 but 0 x NaN is not, so they are zeroed before
+          // the tile is handed to the MMA issuer.
+          const bool ragged_k = kv == 0 && !r.resp && r.key0 + kTile > a.P;
+          const uint32_t fb = bar_addr(sbase, ragged_k ? (int)B_AUX : bf);
           const uint32_t dst = sbase + (kv == 0 ? kOffK : kOffV) + st * kTileBytes;
           mbar_expect_tx(fb, kTileBytes);
           if (r.resp) {
@@ -173,6 +182,18 @@ bwd_dq_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a, const L
                 tma_load_2d(dst + hf * kHalfBytes + bb * box_rows * 128, map, hf * 64, y, fb);
             }
           }
+          if (ragged_k) {
+            if (!mbar_wait(fb, aux & 1)) { fail(); ok = false; break; }
+            ++aux;
+            uint8_t* kb = smem + kOffK + st * kTileBytes;
+            for (int i = (int)(a.P - r.key0) * 8; i < kTile * 8; ++i) {
+              const int row = i >> 3, c = i & 7;
+              *reinterpret_cast<uint4*>(kb + row * 128 + c * 16) = make_uint4(0, 0, 0, 0);
+              *reinterpret_cast<uint4*>(kb + kHalfBytes + row * 128 + c * 16) = make_uint4(0, 0, 0, 0);
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(bar_addr(sbase, bf));
+          }
           if (kv == 0) ++kc; else ++vc;
         }
       }
@@ -184,58 +205,33 @@ bwd_dq_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a, const L
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    // All 32 lanes walk the same tiles and keep identical counters; lane 0 issues.
-    // Tiles are looked at three at a time: j (dQ), j+1 (dP), j+2 (S).
-    const uint32_t idQK = idesc_bf16_f32(kTile, kTile, false);
-    const uint32_t idDQ = idesc_bf16_f32(kTile, kD, true);
-    DqCursor cursor(sc, blockIdx.x, a.R, a.g);
-    TileRec rec[3];
-    bool have[3];
-    have[0] = cursor.next(&rec[0]);
-    have[1] = have[0] && cursor.next(&rec[1]);
-    have[2] = have[1] && cursor.next(&rec[2]);
-    uint32_t kc_s = 0, kc_q = 0, vc = 0, qunits = 0, j = 0;
-    bool ok = true;
-    // Descriptor bases built once; each MMA only adds a compile-time offset, so the
-    // issuing thread is not slowed by per-instruction 64-bit descriptor arithmetic.
-    const uint32_t dq_base = sdesc_lo(sbase + kOffQ, 16);
-    const uint32_t ddo_base = sdesc_lo(sbase + kOffDO, 16);
-    const uint32_t dk_base = sdesc_lo(sbase + kOffK, 16);
-    const uint32_t dv_base = sdesc_lo(sbase + kOffV, 16);
-    const uint32_t dkm_base = sdesc_lo(sbase + kOffK, kHalfBytes);
-    // K tiles must be finite where dQ reads them: rows past the prompt end of a ragged
-    // last tile are zeroed (their dS is exactly 0, but 0 * NaN would still be NaN).
-    auto zero_tail_rows = [&](uint32_t kstage, uint32_t kpar, const TileRec& r) {
-      if (r.resp || r.key0 + kTile <= a.P) return;
-      mbar_wait(bar_addr(sbase, B_K_FULL + kstage), kpar);
-      const int valid = (int)(a.P - r.key0);
-      uint8_t* kb = smem + kOffK + kstage * kTileBytes;
-      for (int i = valid * 8 + lane; i < kTile * 8; i += 32) {
-        const int row = i >> 3, c = i & 7;
-        *reinterpret_cast<uint4*>(kb + row * 128 + c * 16) = make_uint4(0, 0, 0, 0);
-        *reinterpret_cast<uint4*>(kb + kHalfBytes + row * 128 + c * 16) = make_uint4(0, 0, 0, 0);
-      }
-      fence_proxy_async_smem();
-      __syncwarp();
-    };
-    // S(r) = Q K^T into S buffer sb; K tile kc_s
-    auto issue_s = [&](const TileRec& r, int sb) -> bool {
-      if (r.first_of_unit) {
-        bool w = true;
-        if (lane == 0) w = mbar_wait(bar_addr(sbase, B_Q_FULL), qunits & 1);
-        w = __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
+    // One thread.  Issuing a tcgen05.mma holds the thread until the tensor core has
+    // nearly taken the instruction, so the tensor core only stays busy if nothing but
+    // MMAs sits between groups: for each tile j every index, descriptor and wait on
+    // loaded data is settled first, then the one real dependency (dS(j) in tensor
+    // memory) is awaited, then S(j+1), dP(j+1), dQ(j) go out back to back.
+    if (lane == 0) {
+      const uint32_t idQK = idesc_bf16_f32(kTile, kTile, false);
+      const uint32_t idDQ = idesc_bf16_f32(kTile, kD, true);
+      const uint32_t dq_base = sdesc_lo(sbase + kOffQ, 16);
+      const uint32_t ddo_base = sdesc_lo(sbase + kOffDO, 16);
+      const uint32_t dk_base = sdesc_lo(sbase + kOffK, 16);
+      const uint32_t dv_base = sdesc_lo(sbase + kOffV, 16);
+      const uint32_t dkm_base = sdesc_lo(sbase + kOffK, kHalfBytes);
+      DqCursor cursor(sc, blockIdx.x, a.R, a.g);
+      TileRec rec[2];
+      bool have[2];
+      have[0] = cursor.next(&rec[0]);
+      have[1] = have[0] && cursor.next(&rec[1]);
+      uint32_t kc_s = 0, kc_q = 0, vc = 0, qunits = 0, j = 0;
+      bool ok = true;
+      auto wait_q = [&]() -> bool {
+        const bool w = mbar_wait(bar_addr(sbase, B_Q_FULL), qunits & 1);
         ++qunits;
-        if (!w) return false;
-      }
-      const uint32_t st = kc_s % kKStages, par = (kc_s / kKStages) & 1;
-      ++kc_s;
-      bool w = true;
-      if (lane == 0) w = mbar_wait(bar_addr(sbase, B_K_FULL + st), par);
-      w = __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
-      if (!w) return false;
-      zero_tail_rows(st, par, r);
-      if (lane == 0) {
-        tc_fence_after();
+        return w;
+      };
+      // S = Q K^T into S buffer sb from K stage st
+      auto mma_s = [&](uint32_t st, int sb) {
         const uint32_t b0 = dk_base + ((st * kTileBytes) >> 4);
         const uint32_t d = tmem + sb * kTile;
 #pragma unroll
@@ -244,19 +240,9 @@ bwd_dq_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a, const L
           mma_ss_lo(d, dq_base + off, b0 + off, idQK, kk > 0);
         }
         mma_commit(bar_addr(sbase, B_S_FULL + sb));
-      }
-      return true;
-    };
-    // dP(r) = dO V^T; V tile vc
-    auto issue_dp = [&](const TileRec& r) -> bool {
-      const uint32_t st = vc % kVStages, par = (vc / kVStages) & 1;
-      ++vc;
-      bool w = true;
-      if (lane == 0) w = mbar_wait(bar_addr(sbase, B_V_FULL + st), par);
-      w = __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
-      if (!w) return false;
-      if (lane == 0) {
-        tc_fence_after();
+      };
+      // dP = dO V^T from V stage st
+      auto mma_dp = [&](uint32_t st, bool last_of_unit) {
         const uint32_t b0 = dv_base + ((st * kTileBytes) >> 4);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
@@ -265,50 +251,66 @@ bwd_dq_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a, const L
         }
         mma_commit(bar_addr(sbase, B_DP_FULL));
         mma_commit(bar_addr(sbase, B_V_EMPTY + st));
-        if (r.last_of_unit) mma_commit(bar_addr(sbase, B_Q_EMPTY));
+        if (last_of_unit) mma_commit(bar_addr(sbase, B_Q_EMPTY));
+      };
+      // prologue: S(0), dP(0)
+      if (have[0]) {
+        const uint32_t st0 = kc_s % kKStages, p0 = (kc_s / kKStages) & 1;
+        const uint32_t sv0 = vc % kVStages, pv0 = (vc / kVStages) & 1;
+        ++kc_s;
+        ++vc;
+        ok = wait_q() && mbar_wait(bar_addr(sbase, B_K_FULL + st0), p0) &&
+             mbar_wait(bar_addr(sbase, B_V_FULL + sv0), pv0);
+        if (ok) {
+          tc_fence_after();
+          mma_s(st0, 0);
+          mma_dp(sv0, rec[0].last_of_unit);
+        } else {
+          fail();
+        }
       }
-      return true;
-    };
-    if (have[0]) {
-      ok = issue_s(rec[0], 0) && issue_dp(rec[0]);
-      if (ok && have[1]) ok = issue_s(rec[1], 1);
-      if (!ok && lane == 0) fail();
-    }
-    while (ok && have[0]) {
-      const int sb = j & 1;
-      bool w = true;
-      if (lane == 0) w = mbar_wait(bar_addr(sbase, B_DS_FULL), j & 1);
-      w = __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
-      if (!w) { if (lane == 0) fail(); break; }
-      if (have[1] && !issue_dp(rec[1])) { if (lane == 0) fail(); break; }
-      if (lane == 0) {
+      while (ok && have[0]) {
+        // Everything that does not depend on dS(j): stage indices and descriptors, and
+        // the loads of tile j+1 (K(j+1) was freed by dQ(j-2), V(j+1) by dP(j-1), so
+        // they normally landed long ago).
+        const uint32_t sk = kc_s % kKStages, pk = (kc_s / kKStages) & 1;
+        const uint32_t sv = vc % kVStages, pv = (vc / kVStages) & 1;
+        const uint32_t sq = kc_q % kKStages;
+        if (have[1]) {
+          if (rec[1].first_of_unit && !wait_q()) { fail(); break; }
+          if (!mbar_wait(bar_addr(sbase, B_K_FULL + sk), pk)) { fail(); break; }
+          if (!mbar_wait(bar_addr(sbase, B_V_FULL + sv), pv)) { fail(); break; }
+        }
+        const uint32_t bq = dkm_base + ((sq * kTileBytes) >> 4);
+        const uint32_t aq = tmem + (j & 1) * kTile;
+        const bool acc_q = !rec[0].first_of_unit, last0 = rec[0].last_of_unit;
+        if (!mbar_wait(bar_addr(sbase, B_DS_FULL), j & 1)) { fail(); break; }
         tc_fence_after();
-        const uint32_t b0 = dkm_base + (((kc_q % kKStages) * kTileBytes) >> 4);
-        const uint32_t a = tmem + sb * kTile;
-        mma_ts_lo(tmem + 384, a, b0, idDQ, rec[0].first_of_unit ? 0u : 1u);
+        // S(j+1) and dP(j+1) first: the dS warps need both for dS(j+1)
+        if (have[1]) {
+          mma_s(sk, (j + 1) & 1);
+          mma_dp(sv, rec[1].last_of_unit);
+          ++kc_s;
+          ++vc;
+        }
+        mma_ts_lo(tmem + 384, aq, bq, idDQ, acc_q ? 1u : 0u);
 #pragma unroll
         for (int kk = 1; kk < 8; ++kk) {
           const uint32_t acol = kk < 4 ? kk * 8 : 64 + (kk - 4) * 8;
-          mma_ts_lo(tmem + 384, a + acol, b0 + ((kk * 2048) >> 4), idDQ, 1u);
+          mma_ts_lo(tmem + 384, aq + acol, bq + ((kk * 2048) >> 4), idDQ, 1u);
         }
-        mma_commit(bar_addr(sbase, B_K_EMPTY + kc_q % kKStages));
-        if (rec[0].last_of_unit) mma_commit(bar_addr(sbase, B_DQ_DONE));
+        mma_commit(bar_addr(sbase, B_K_EMPTY + sq));
+        if (last0) mma_commit(bar_addr(sbase, B_DQ_DONE));
+        ++kc_q;
+        rec[0] = rec[1];
+        have[0] = have[1];
+        have[1] = have[1] && cursor.next(&rec[1]);
+        ++j;
+        if (*abort_flag) break;
       }
-      ++kc_q;
-      if (have[2] && !issue_s(rec[2], sb)) { if (lane == 0) fail(); break; }
-      rec[0] = rec[1];
-      rec[1] = rec[2];
-      have[0] = have[1];
-      have[1] = have[2];
-      have[2] = have[2] && cursor.next(&rec[2]);
-      ++j;
-      if (*abort_flag) break;
-    }
-    if (lane == 0) {
       mma_commit(bar_addr(sbase, B_DONE));
       mbar_wait(bar_addr(sbase, B_DONE), 0);
     }
-    __syncwarp();
   } else if (warp >= 4) {
     // ------------------------------------------------------------ dS warpgroups
     const int cgrp = (warp - 4) >> 2;       // key columns [64 cgrp, 64 cgrp + 64)
