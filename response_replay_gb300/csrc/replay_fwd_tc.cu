@@ -257,10 +257,15 @@ replay_fwd_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a, con
       }
       while (ok) {
         const bool has_nxt = cursor.next(&nxt);
-        // P_t V of the current tile
-        const uint32_t vstage = ring % kStages;
-        if (!mbar_wait(bar_addr(sbase, B_KV_FULL + vstage), (ring / kStages) & 1)) { fail(); break; }
-        ++ring;
+        // Loads first, then the one real dependency (P_t), then the MMAs back to back:
+        // V of this tile, and K of the next one unless that tile opens a new unit (its
+        // K is loaded only after the new unit's Q, which waits for this unit's last S).
+        const uint32_t vstage = ring % kStages, vpar = (ring / kStages) & 1;
+        const uint32_t kstage = (ring + 1) % kStages, kpar = ((ring + 1) / kStages) & 1;
+        ring += has_nxt ? 2 : 1;
+        const bool early_k = has_nxt && !nxt.first_of_unit;
+        if (!mbar_wait(bar_addr(sbase, B_KV_FULL + vstage), vpar)) { fail(); break; }
+        if (early_k && !mbar_wait(bar_addr(sbase, B_KV_FULL + kstage), kpar)) { fail(); break; }
         if (!mbar_wait(bar_addr(sbase, B_P_FULL + t), kc & 1)) { fail(); break; }
         // Keep the tiles half a period apart: tile B's group for tile k follows tile A's
         // P V of tile k, tile A's group for tile k follows tile B's P V of tile k - 1.
@@ -277,14 +282,12 @@ replay_fwd_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a, con
         mma_commit(bar_addr(sbase, B_KV_EMPTY + vstage));
         if (!has_nxt) break;
         // S_t of the next tile (after P_t V in issue order: it overwrites P_t)
-        if (nxt.first_of_unit) {
+        if (!early_k) {
           if (!mbar_wait(bar_addr(sbase, B_Q_FULL), units & 1)) { fail(); break; }
           ++units;
+          if (!mbar_wait(bar_addr(sbase, B_KV_FULL + kstage), kpar)) { fail(); break; }
+          tc_fence_after();
         }
-        const uint32_t kstage = ring % kStages;
-        if (!mbar_wait(bar_addr(sbase, B_KV_FULL + kstage), (ring / kStages) & 1)) { fail(); break; }
-        ++ring;
-        tc_fence_after();
         issue_s(kstage);
         mma_commit(bar_addr(sbase, B_S_FULL + t));
         mma_commit(bar_addr(sbase, B_KV_EMPTY + kstage));
