@@ -58,6 +58,17 @@ def peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
+def kernel_source_hash(kernel_file: str) -> str:
+    """First 16 hex digits of the sha256 of a kernel's .cu file followed by every shared
+    header of the library (so a change to a header the kernel uses also counts)."""
+    csrc = os.path.join(ROOT, "response_replay_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in [kernel_file] + sorted(f for f in os.listdir(csrc) if f.endswith((".h", ".cuh"))):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
 def traffic_from_profile(kernel_file: str, kernel: str):
     """DRAM bytes per launch of `kernel` from the committed ncu summary, or None when
     the summary is missing or was taken on a different version of the kernel source."""
@@ -65,8 +76,7 @@ def traffic_from_profile(kernel_file: str, kernel: str):
     try:
         with open(prof) as f:
             txt = f.read()
-        with open(os.path.join(ROOT, "response_replay_gb300", "csrc", kernel_file), "rb") as f:
-            h = hashlib.sha256(f.read()).hexdigest()[:16]
+        h = kernel_source_hash(kernel_file)
     except OSError:
         return None
     m = re.search(r"source_sha256_16:\s*([0-9a-f]{16})", txt)
