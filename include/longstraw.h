@@ -215,6 +215,14 @@ const char* ls_status_string(ls_status status);
  * devices), e.g. to count the launches of one step. */
 uint64_t ls_kernel_launches(void);
 
+/* Diagnostic (the pages have no counterpart): enqueue one block that waits, through the
+ * pipelines' own bounded mbarrier wait, on a barrier nothing completes.  After the
+ * wait's time limit (about 2 s of SM clock) the block records LS_ERR_TIMEOUT in the
+ * device error word and exits, so a following ls_last_device_error() returns
+ * LS_ERR_TIMEOUT and the context stays usable.  Returns LS_OK once enqueued,
+ * LS_ERR_CUDA if the launch fails.  Used by the tests of the failure path. */
+ls_status ls_selftest_wait_timeout(ls_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

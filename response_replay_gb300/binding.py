@@ -24,7 +24,7 @@ EXPORTED = (
     "ls_replay_attn_bwd_workspace", "ls_replay_attn_bwd", "ls_grpo_workspace",
     "ls_grpo_loss_fwd_bwd", "ls_validate_page_table", "ls_validate_page_table_workspace",
     "ls_last_device_error", "ls_status_string", "ls_kernel_launches",
-    "ls_grpo_loss_fwd_bwd_noalloc",
+    "ls_grpo_loss_fwd_bwd_noalloc", "ls_selftest_wait_timeout",
 )
 
 
@@ -72,6 +72,7 @@ def lib() -> C.CDLL:
             "ls_validate_page_table": [cache, P, sz, P],
             "ls_validate_page_table_workspace": [cache, szp],
             "ls_last_device_error": [P],
+            "ls_selftest_wait_timeout": [P],
             "ls_status_string": [i32],
         }
         for name, args in sig.items():
@@ -175,6 +176,11 @@ def ls_validate_page_table(cache: ls_kv_cache, workspace: int, workspace_bytes: 
 def ls_kernel_launches() -> int:
     """Kernel launches issued by the library so far in this process."""
     return lib().ls_kernel_launches()
+
+
+def ls_selftest_wait_timeout(stream: int = 0) -> None:
+    """Enqueue a bounded wait that must run out (see include/longstraw.h)."""
+    _ok("ls_selftest_wait_timeout", lib().ls_selftest_wait_timeout(stream))
 
 
 def ls_last_device_error(stream: int = 0) -> int:

@@ -347,6 +347,13 @@ ls_status ls_validate_page_table(const ls_kv_cache* cache, void* workspace, size
                                             (cudaStream_t)stream));
 }
 
+ls_status ls_selftest_wait_timeout(ls_stream_t stream) {
+  DevInfo d;
+  ls_status s = dev_info(&d);
+  if (s != LS_OK) return s;
+  return from_cuda(ls_launch_wait_timeout(d.err, (cudaStream_t)stream));
+}
+
 ls_status ls_last_device_error(ls_stream_t stream) {
   DevInfo d;
   ls_status s = dev_info(&d);

@@ -65,6 +65,7 @@ cudaError_t ls_launch_capture(const void* k, const void* v, void* k_pool, void* 
                               int32_t hkv, int64_t start_pos, int64_t n, int num_sms,
                               uint32_t* err, cudaStream_t st);
 
+cudaError_t ls_launch_wait_timeout(uint32_t* err, cudaStream_t stream);
 cudaError_t ls_launch_validate_pages(const int32_t* page_table, int32_t num_logical,
                                      int32_t num_pages, uint32_t* seen, uint32_t* err,
                                      cudaStream_t st);

@@ -93,23 +93,24 @@ inline LsSched ls_make_sched(int32_t units, int32_t ntiles, int32_t num_splits, 
 // first/last: this item is the first/last of unit u that this CTA processes;
 // complete: this CTA processes every item of u (only meaningful when last is set).
 struct LsWalk {
-  LsSched sc;
+  const LsSched* sc;   // the schedule (the kernel's __grid_constant__ parameter on the
+                       // device, so the walk holds a pointer, not a register copy)
   int32_t cta;
   int32_t range;       // 0..waves-1 whole units, waves = tail
   int64_t item, end;   // current / end item (global item index u*(S+1)+s)
   int64_t range_begin;
 
-  LS_HD LsWalk(const LsSched& s, int32_t c) : sc(s), cta(c), range(-1), item(0), end(0), range_begin(0) {}
+  LS_HD LsWalk(const LsSched& s, int32_t c) : sc(&s), cta(c), range(-1), item(0), end(0), range_begin(0) {}
 
   LS_HD bool open_range(int32_t r) {
-    const int64_t ipu = sc.items_per_unit();
-    if (r < sc.waves) {
-      range_begin = (int64_t)(r * sc.ctas + cta) * ipu;
+    const int64_t ipu = sc->items_per_unit();
+    if (r < sc->waves) {
+      range_begin = (int64_t)(r * sc->ctas + cta) * ipu;
       end = range_begin + ipu;
-    } else if (r == sc.waves && sc.tail_items > 0) {
-      int64_t base = (int64_t)sc.tail_unit0() * ipu;
-      range_begin = base + sc.tail_begin(cta);
-      end = base + sc.tail_begin(cta + 1);
+    } else if (r == sc->waves && sc->tail_items > 0) {
+      int64_t base = (int64_t)sc->tail_unit0() * ipu;
+      range_begin = base + sc->tail_begin(cta);
+      end = base + sc->tail_begin(cta + 1);
     } else {
       return false;
     }
@@ -122,7 +123,7 @@ struct LsWalk {
     while (range < 0 || item >= end) {
       if (!open_range(range + 1)) return false;
     }
-    const int64_t ipu = sc.items_per_unit();
+    const int64_t ipu = sc->items_per_unit();
     *u = (int32_t)(item / ipu);
     *s = (int32_t)(item % ipu);
     *first = (item == range_begin) || (*s == 0);

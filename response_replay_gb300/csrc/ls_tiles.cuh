@@ -35,13 +35,13 @@ struct TileCursor {
       h = u / nTB;
       t0 = (u - h * nTB) * UnitRows;
       kvh = h / g;
-      resp = (s == walk.sc.nsplit);
+      resp = (s == walk.sc->nsplit);
       if (resp) {
         const int32_t qe = t0 + UnitRows < R ? t0 + UnitRows : R;
         t = 0;
         t_end = (qe + Tile - 1) / Tile;
       } else {
-        walk.sc.split_tiles(s, &t, &t_end);
+        walk.sc->split_tiles(s, &t, &t_end);
       }
       if (t < t_end) return true;
     }

@@ -80,7 +80,7 @@ using FwdCursor = TileCursor<kUnitRows, kTile>;
 __device__ __forceinline__ uint32_t bar_addr(uint32_t base, int i) { return base + kOffBar + 8 * i; }
 
 __global__ void __launch_bounds__(kThreads, 1)
-replay_fwd_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a, const LsSched sc,
+replay_fwd_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a, const __grid_constant__ LsSched sc,
                      const LsFwdOut out) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
