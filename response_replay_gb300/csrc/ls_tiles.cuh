@@ -48,6 +48,22 @@ struct TileCursor {
     return false;
   }
 
+  // The same walk as next(), reporting only whether the tile is the first / last of
+  // its unit in this CTA (what an MMA issuer needs), so the common step is a compare
+  // and an increment.
+  __device__ bool next_flags(bool* first, bool* last) {
+    if (!valid || t >= t_end) {
+      valid = open_item();
+      if (!valid) return false;
+      *first = item_first;
+    } else {
+      *first = false;
+    }
+    ++t;
+    *last = item_last && t >= t_end;
+    return true;
+  }
+
   __device__ bool next(TileRec* r) {
     if (!valid || t >= t_end) {
       valid = open_item();

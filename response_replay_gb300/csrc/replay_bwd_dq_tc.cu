@@ -12,19 +12,20 @@
 //   warp 0      TMA producer: Q and dO tiles, then K (3-stage ring) and V (2-stage ring)
 //               tiles of 128 keys, prompt tiles gathered page by page; rows of a ragged
 //               last prompt K tile are zeroed before the tile is handed over.
-//   warp 1      MMA issuer (one thread): S = Q K^T (SS, into one of two S buffers),
-//               dP = dO V^T (SS), dQ += dS K (TS: dS from tensor memory, K as an
-//               MN-major operand).  Per tile j, after dS(j) is in tensor memory:
-//               S(j+1), dP(j+1), dQ(j) back to back; the dS warps turn S(j+1), dP(j+1)
-//               into dS(j+1) while dQ(j) runs.  A K tile lives from S(j) to dQ(j), so
-//               the 3-stage ring gives each K load about two tiles of lead time.
+//   warp 1      MMA issuer (one thread): S = Q K^T (SS), dP = dO V^T (SS, into one of two
+//               dP buffers), dQ += dS K (TS: dS from tensor memory, K as an MN-major
+//               operand).  Per tile j: dP(j+1) once V(j+1) has landed; S(j+1) once the
+//               dS warps hold S(j) and dP(j) in registers (both run while dS(j) is
+//               computed); dQ(j) once dS(j) is in tensor memory.  Every wait sits behind
+//               a group that is still running.  A K tile lives from S(j) to dQ(j), so the
+//               3-stage ring gives each K load about two tiles of lead.
 //   warps 2-3   idle (complete warpgroup 0)
 //   warps 4-7 / 8-11  two warpgroups split the 128 key columns of each query row (64
 //               each): p = exp2(s scale log2e - lse log2e), ds = p (dp - D), packed as
-//               bf16 pairs over their own S columns; at the end of a unit they read dQ,
+//               bf16 pairs over their own dP columns; at the end of a unit they read dQ,
 //               scale it and write dq (or a split partial).
-// Tensor memory (512 columns): S0 [0,128) S1 [128,256) dP [256,384) dQ [384,512).
-// dS of warpgroup c lives in S columns [64c, 64c+32) of the current S buffer.
+// Tensor memory (512 columns): S [0,128), dP0 [128,256), dP1 [256,384), dQ [384,512).
+// dS(j) of warpgroup c lives in columns [64c, 64c+32) of dP buffer j & 1.
 #include <math.h>
 
 #include "ls_device.cuh"
@@ -42,6 +43,13 @@ constexpr int kTile = 128;
 constexpr int kUnitRows = 128;
 constexpr int kKStages = 3, kVStages = 2;
 constexpr int kThreads = 384;
+// Register split (setmaxnreg): the launch gives 168 per thread (384 x 168 = 64512);
+// warpgroup 0 (TMA + MMA control) drops to 112 and the dS warpgroups (64 S and 64 dP
+// values per thread held at once) rise to 192: 128 x 112 + 256 x 192 = 63488 <= 64512.
+constexpr int kRegsLaunch = 168, kRegsControl = 112, kRegsDs = 192;
+static_assert(128 * kRegsControl + 256 * kRegsDs <= kThreads * kRegsLaunch, "register split");
+// Tensor memory columns: S, two dP buffers (dS(j) is written over dP(j)), dQ.
+constexpr uint32_t kColS = 0, kColDp = 128, kColDq = 384;
 constexpr uint32_t kTileBytes = kTile * kD * 2;
 constexpr uint32_t kHalfBytes = kTileBytes / 2;
 constexpr uint32_t kOffQ = 0, kOffDO = kTileBytes;
@@ -58,10 +66,11 @@ enum {
   B_V_EMPTY = B_V_FULL + kVStages,
   B_Q_FULL = B_V_EMPTY + kVStages,
   B_Q_EMPTY,
-  B_S_FULL,  // 2
-  B_DP_FULL = B_S_FULL + 2,
-  B_DS_FULL,
-  B_DQ_DONE,
+  B_S_FULL,
+  B_DP_FULL,   // 2: dP(j) in dP buffer j & 1
+  B_SDP_FREE = B_DP_FULL + 2,  // the dS warps hold S(j) and dP(j) in registers
+  B_DS_FULL,   // 2: dS(j) in dP buffer j & 1
+  B_DQ_DONE = B_DS_FULL + 2,
   B_DONE,
   B_AUX,  // producer: ragged K tile landed
   B_COUNT
@@ -98,10 +107,12 @@ bwd_dq_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a, const _
     }
     mbar_init(bar_addr(sbase, B_Q_FULL), 1);
     mbar_init(bar_addr(sbase, B_Q_EMPTY), 1);
-    mbar_init(bar_addr(sbase, B_S_FULL + 0), 1);
-    mbar_init(bar_addr(sbase, B_S_FULL + 1), 1);
-    mbar_init(bar_addr(sbase, B_DP_FULL), 1);
-    mbar_init(bar_addr(sbase, B_DS_FULL), 256);
+    mbar_init(bar_addr(sbase, B_S_FULL), 1);
+    mbar_init(bar_addr(sbase, B_DP_FULL + 0), 1);
+    mbar_init(bar_addr(sbase, B_DP_FULL + 1), 1);
+    mbar_init(bar_addr(sbase, B_SDP_FREE), 256);
+    mbar_init(bar_addr(sbase, B_DS_FULL + 0), 256);
+    mbar_init(bar_addr(sbase, B_DS_FULL + 1), 256);
     mbar_init(bar_addr(sbase, B_DQ_DONE), 1);
     mbar_init(bar_addr(sbase, B_DONE), 1);
     mbar_init(bar_addr(sbase, B_AUX), 1);
@@ -121,6 +132,8 @@ bwd_dq_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a, const _
     *abort_flag = 1;
   };
 
+  if (warp < 4) {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsControl));
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
@@ -206,10 +219,10 @@ bwd_dq_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a, const _
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     // One thread.  Issuing a tcgen05.mma holds the thread until the tensor core has
-    // nearly taken the instruction, so the tensor core only stays busy if nothing but
-    // MMAs sits between groups: for each tile j every index, descriptor and wait on
-    // loaded data is settled first, then the one real dependency (dS(j) in tensor
-    // memory) is awaited, then S(j+1), dP(j+1), dQ(j) go out back to back.
+    // nearly taken the instruction, so nothing but MMAs may sit between groups.  Per
+    // tile j: settle the loads of tile j+1, then as soon as the dS warps hold S(j) and
+    // dP(j) in registers issue S(j+1) and dP(j+1) (they run while dS(j) is computed),
+    // then once dS(j) is in tensor memory issue dQ(j).
     if (lane == 0) {
       const uint32_t idQK = idesc_bf16_f32(kTile, kTile, false);
       const uint32_t idDQ = idesc_bf16_f32(kTile, kD, true);
@@ -219,99 +232,104 @@ bwd_dq_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a, const _
       const uint32_t dv_base = sdesc_lo(sbase + kOffV, 16);
       const uint32_t dkm_base = sdesc_lo(sbase + kOffK, kHalfBytes);
       DqCursor cursor(sc, blockIdx.x, a.R, a.g);
-      TileRec rec[2];
-      bool have[2];
-      have[0] = cursor.next(&rec[0]);
-      have[1] = have[0] && cursor.next(&rec[1]);
-      uint32_t kc_s = 0, kc_q = 0, vc = 0, qunits = 0, j = 0;
+      // first / last of unit of tiles j (f0, l0) and j+1 (f1, l1)
+      bool f0 = false, l0 = false, f1 = false, l1 = false;
+      bool have0 = cursor.next_flags(&f0, &l0);
+      bool have1 = have0 && cursor.next_flags(&f1, &l1);
+      RingPos<kKStages> ks, kq;  // K ring: next S, next dQ
+      RingPos<kVStages> vs;      // V ring: next dP
+      uint32_t qunits = 0, j = 0;
       bool ok = true;
       auto wait_q = [&]() -> bool {
         const bool w = mbar_wait(bar_addr(sbase, B_Q_FULL), qunits & 1);
         ++qunits;
         return w;
       };
-      // S = Q K^T into S buffer sb from K stage st
-      auto mma_s = [&](uint32_t st, int sb) {
+      // S = Q K^T from K stage st
+      auto mma_s = [&](uint32_t st, bool last_of_unit) {
         const uint32_t b0 = dk_base + ((st * kTileBytes) >> 4);
-        const uint32_t d = tmem + sb * kTile;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t off = ((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4;
-          mma_ss_lo(d, dq_base + off, b0 + off, idQK, kk > 0);
+          mma_ss_lo(tmem + kColS, dq_base + off, b0 + off, idQK, kk > 0);
         }
-        mma_commit(bar_addr(sbase, B_S_FULL + sb));
-      };
-      // dP = dO V^T from V stage st
-      auto mma_dp = [&](uint32_t st, bool last_of_unit) {
-        const uint32_t b0 = dv_base + ((st * kTileBytes) >> 4);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t off = ((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4;
-          mma_ss_lo(tmem + 256, ddo_base + off, b0 + off, idQK, kk > 0);
-        }
-        mma_commit(bar_addr(sbase, B_DP_FULL));
-        mma_commit(bar_addr(sbase, B_V_EMPTY + st));
+        mma_commit(bar_addr(sbase, B_S_FULL));
+        // the unit's Q and dO are free once its last S (issued after its last dP) is done
         if (last_of_unit) mma_commit(bar_addr(sbase, B_Q_EMPTY));
       };
+      // dP = dO V^T into dP buffer db from V stage st
+      auto mma_dp = [&](uint32_t st, uint32_t db) {
+        const uint32_t b0 = dv_base + ((st * kTileBytes) >> 4);
+        const uint32_t d = tmem + kColDp + db * kTile;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t off = ((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4;
+          mma_ss_lo(d, ddo_base + off, b0 + off, idQK, kk > 0);
+        }
+        mma_commit(bar_addr(sbase, B_DP_FULL + db));
+        mma_commit(bar_addr(sbase, B_V_EMPTY + st));
+      };
       // prologue: S(0), dP(0)
-      if (have[0]) {
-        const uint32_t st0 = kc_s % kKStages, p0 = (kc_s / kKStages) & 1;
-        const uint32_t sv0 = vc % kVStages, pv0 = (vc / kVStages) & 1;
-        ++kc_s;
-        ++vc;
-        ok = wait_q() && mbar_wait(bar_addr(sbase, B_K_FULL + st0), p0) &&
-             mbar_wait(bar_addr(sbase, B_V_FULL + sv0), pv0);
+      if (have0) {
+        ok = wait_q() && mbar_wait(bar_addr(sbase, B_K_FULL + ks.stage), ks.phase) &&
+             mbar_wait(bar_addr(sbase, B_V_FULL + vs.stage), vs.phase);
         if (ok) {
           tc_fence_after();
-          mma_s(st0, 0);
-          mma_dp(sv0, rec[0].last_of_unit);
+          mma_dp(vs.stage, 0);
+          mma_s(ks.stage, l0);
+          ks.advance();
+          vs.advance();
         } else {
           fail();
         }
       }
-      while (ok && have[0]) {
-        // Everything that does not depend on dS(j): stage indices and descriptors, and
-        // the loads of tile j+1 (K(j+1) was freed by dQ(j-2), V(j+1) by dP(j-1), so
-        // they normally landed long ago).
-        const uint32_t sk = kc_s % kKStages, pk = (kc_s / kKStages) & 1;
-        const uint32_t sv = vc % kVStages, pv = (vc / kVStages) & 1;
-        const uint32_t sq = kc_q % kKStages;
-        if (have[1]) {
-          if (rec[1].first_of_unit && !wait_q()) { fail(); break; }
-          if (!mbar_wait(bar_addr(sbase, B_K_FULL + sk), pk)) { fail(); break; }
-          if (!mbar_wait(bar_addr(sbase, B_V_FULL + sv), pv)) { fail(); break; }
+      while (ok && have0) {
+        // Groups of tile j+1 and j, each wait placed so that the group before it is
+        // still running on the tensor core:
+        //   dP(j+1) needs V(j+1) (its buffer's previous dS(j-1) went to dQ(j-1), issued
+        //     earlier by this thread); a new unit's dO also needs that unit's Q/dO load,
+        //     which follows the old unit's last S;
+        //   S(j+1) needs K(j+1) and the dS warps to hold S(j) in registers;
+        //   dQ(j) needs dS(j).
+        const uint32_t bq = dkm_base + ((kq.stage * kTileBytes) >> 4);
+        const uint32_t aq = tmem + kColDp + (j & 1) * kTile;  // dS(j)
+        if (have1) {
+          if (f1 && !wait_q()) { fail(); break; }
+          if (!mbar_wait(bar_addr(sbase, B_V_FULL + vs.stage), vs.phase)) { fail(); break; }
+          tc_fence_after();
+          mma_dp(vs.stage, (j + 1) & 1);
+          vs.advance();
+          if (!mbar_wait(bar_addr(sbase, B_K_FULL + ks.stage), ks.phase)) { fail(); break; }
         }
-        const uint32_t bq = dkm_base + ((sq * kTileBytes) >> 4);
-        const uint32_t aq = tmem + (j & 1) * kTile;
-        const bool acc_q = !rec[0].first_of_unit, last0 = rec[0].last_of_unit;
-        if (!mbar_wait(bar_addr(sbase, B_DS_FULL), j & 1)) { fail(); break; }
+        if (!mbar_wait(bar_addr(sbase, B_SDP_FREE), j & 1)) { fail(); break; }
         tc_fence_after();
-        // S(j+1) and dP(j+1) first: the dS warps need both for dS(j+1)
-        if (have[1]) {
-          mma_s(sk, (j + 1) & 1);
-          mma_dp(sv, rec[1].last_of_unit);
-          ++kc_s;
-          ++vc;
+        if (have1) {
+          mma_s(ks.stage, l1);
+          ks.advance();
         }
-        mma_ts_lo(tmem + 384, aq, bq, idDQ, acc_q ? 1u : 0u);
+        if (!mbar_wait(bar_addr(sbase, B_DS_FULL + (j & 1)), (j >> 1) & 1)) { fail(); break; }
+        tc_fence_after();
+        mma_ts_lo(tmem + kColDq, aq, bq, idDQ, f0 ? 0u : 1u);
 #pragma unroll
         for (int kk = 1; kk < 8; ++kk) {
           const uint32_t acol = kk < 4 ? kk * 8 : 64 + (kk - 4) * 8;
-          mma_ts_lo(tmem + 384, aq + acol, bq + ((kk * 2048) >> 4), idDQ, 1u);
+          mma_ts_lo(tmem + kColDq, aq + acol, bq + ((kk * 2048) >> 4), idDQ, 1u);
         }
-        mma_commit(bar_addr(sbase, B_K_EMPTY + sq));
-        if (last0) mma_commit(bar_addr(sbase, B_DQ_DONE));
-        ++kc_q;
-        rec[0] = rec[1];
-        have[0] = have[1];
-        have[1] = have[1] && cursor.next(&rec[1]);
+        mma_commit(bar_addr(sbase, B_K_EMPTY + kq.stage));
+        if (l0) mma_commit(bar_addr(sbase, B_DQ_DONE));
+        kq.advance();
+        f0 = f1;
+        l0 = l1;
+        have0 = have1;
+        have1 = have1 && cursor.next_flags(&f1, &l1);
         ++j;
-        if (*abort_flag) break;
       }
       mma_commit(bar_addr(sbase, B_DONE));
       mbar_wait(bar_addr(sbase, B_DONE), 0);
     }
-  } else if (warp >= 4) {
+  }
+  } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsDs));
     // ------------------------------------------------------------ dS warpgroups
     const int cgrp = (warp - 4) >> 2;       // key columns [64 cgrp, 64 cgrp + 64)
     const int quad = warp & 3;
@@ -329,9 +347,9 @@ bwd_dq_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a, const _
         lse2 = b.lse[idx] * kLog2e;
         dd = b.delta[idx];
       }
-      const int sb = j & 1;
-      if (!mbar_wait(bar_addr(sbase, B_S_FULL + sb), (j >> 1) & 1)) { fail(); break; }
-      if (!mbar_wait(bar_addr(sbase, B_DP_FULL), j & 1)) { fail(); break; }
+      const uint32_t db = j & 1;  // dP buffer of tile j; dS(j) is written over it
+      if (!mbar_wait(bar_addr(sbase, B_S_FULL), j & 1)) { fail(); break; }
+      if (!mbar_wait(bar_addr(sbase, B_DP_FULL + db), (j >> 1) & 1)) { fail(); break; }
       tc_fence_after();
       int32_t lim = kTile;
       if (r.resp) {
@@ -340,24 +358,34 @@ bwd_dq_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a, const _
       } else if (r.key0 + kTile > a.P) {
         lim = (int32_t)(a.P - r.key0);
       }
+      // take S(j) and this warpgroup's dP(j) columns into registers, then let the MMA
+      // issuer start S(j+1) and dP(j+1) while dS(j) is computed
+      const uint32_t dp_col = tmem + lane_off + kColDp + db * kTile + 64 * cgrp;
+      uint32_t sv[64], pv[64];
+      tmem_ld32(tmem + lane_off + kColS + 64 * cgrp, sv);
+      tmem_ld32(tmem + lane_off + kColS + 64 * cgrp + 32, sv + 32);
+      tmem_ld32(dp_col, pv);
+      tmem_ld32(dp_col + 32, pv + 32);
+      tmem_wait_ld();
+      reg_fence32(sv);
+      reg_fence32(sv + 32);
+      reg_fence32(pv);
+      reg_fence32(pv + 32);
+      tc_fence_before();
+      mbar_arrive(bar_addr(sbase, B_SDP_FREE));
+      const float2 c2 = make_float2(c, c), nl2 = make_float2(-lse2, -lse2);
+      const float2 nd2 = make_float2(-dd, -dd);
 #pragma unroll
       for (int q = 0; q < 2; ++q) {
         const int col0 = 64 * cgrp + 32 * q;
-        uint32_t sv[32], pv[32], ds[16];
-        tmem_ld32(tmem + lane_off + sb * kTile + col0, sv);
-        tmem_ld32(tmem + lane_off + 256 + col0, pv);
-        tmem_wait_ld();
-        reg_fence32(sv);
-        reg_fence32(pv);
         float d2[32];
-        const float2 c2 = make_float2(c, c), nl2 = make_float2(-lse2, -lse2);
-        const float2 nd2 = make_float2(-dd, -dd);
 #pragma unroll
         for (int i = 0; i < 32; i += 2) {  // packed fp32x2 arithmetic
-          float2 x = __ffma2_rn(make_float2(__uint_as_float(sv[i]), __uint_as_float(sv[i + 1])), c2, nl2);
+          const int e = 32 * q + i;
+          float2 x = __ffma2_rn(make_float2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), c2, nl2);
           x.x = fast_exp2(x.x);
           x.y = fast_exp2(x.y);
-          const float2 dpm = __fadd2_rn(make_float2(__uint_as_float(pv[i]), __uint_as_float(pv[i + 1])), nd2);
+          const float2 dpm = __fadd2_rn(make_float2(__uint_as_float(pv[e]), __uint_as_float(pv[e + 1])), nd2);
           const float2 ds2 = __fmul2_rn(x, dpm);
           d2[i] = ds2.x;
           d2[i + 1] = ds2.y;
@@ -367,13 +395,16 @@ bwd_dq_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a, const _
           for (int i = 0; i < 32; ++i)
             if (col0 + i >= lim) d2[i] = 0.f;
         }
+        uint32_t ds[16];
 #pragma unroll
         for (int i = 0; i < 32; i += 2) ds[i >> 1] = pack_bf16(d2[i], d2[i + 1]);
-        tmem_st16(tmem + lane_off + sb * kTile + 64 * cgrp + 16 * q, ds);
+        // dS of keys [64 cgrp, 64 cgrp + 64) as bf16 pairs in this warpgroup's own
+        // (already read) dP columns [64 cgrp, 64 cgrp + 32)
+        tmem_st16(dp_col + 16 * q, ds);
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(bar_addr(sbase, B_DS_FULL));
+      mbar_arrive(bar_addr(sbase, B_DS_FULL + db));
       ++j;
       if (r.last_of_unit) {
         if (!mbar_wait(bar_addr(sbase, B_DQ_DONE), uc & 1)) { fail(); break; }
@@ -392,7 +423,7 @@ bwd_dq_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a, const _
         for (int q = 0; q < 2; ++q) {
           const int col0 = 64 * cgrp + 32 * q;
           uint32_t v[32];
-          tmem_ld32(tmem + lane_off + 384 + col0, v);
+          tmem_ld32(tmem + lane_off + kColDq + col0, v);
           tmem_wait_ld();
           reg_fence32(v);
           if (valid || !r.complete) {
