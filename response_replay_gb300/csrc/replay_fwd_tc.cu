@@ -62,8 +62,8 @@ enum {
   B_Q_FULL = B_KV_EMPTY + kStages,
   B_Q_EMPTY,
   B_S_FULL,          // 2
-  B_P_FULL = B_S_FULL + 2,
-  B_O_DONE = B_P_FULL + 2,
+  B_P_FULL = B_S_FULL + 2,   // 4: tile t, key half hf at 2 t + hf
+  B_O_DONE = B_P_FULL + 4,
   B_DONE = B_O_DONE + 2,   // 2
   B_AUX = B_DONE + 2,      // producer: ragged V tile landed
   B_PV_DONE,               // 2: P_t V of a tile finished (orders the issuers)
@@ -100,7 +100,8 @@ replay_fwd_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a, con
     mbar_init(bar_addr(sbase, B_AUX), 1);
     for (int t = 0; t < 2; ++t) {
       mbar_init(bar_addr(sbase, B_S_FULL + t), 1);
-      mbar_init(bar_addr(sbase, B_P_FULL + t), kTile);
+      mbar_init(bar_addr(sbase, B_P_FULL + 2 * t), kTile);
+      mbar_init(bar_addr(sbase, B_P_FULL + 2 * t + 1), kTile);
       mbar_init(bar_addr(sbase, B_O_DONE + t), 1);
       mbar_init(bar_addr(sbase, B_DONE + t), 1);
       mbar_init(bar_addr(sbase, B_PV_DONE + t), 1);
@@ -230,11 +231,15 @@ replay_fwd_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a, con
           mma_ss_lo(d_s, dq + off, b0 + off, idS, kk > 0);
         }
       };
-      auto issue_pv = [&](uint32_t vstage, bool accumulate) {
+      // P_t V over keys [64 hf, 64 hf + 64): K steps 4 hf .. 4 hf + 3
+      auto issue_pv_half = [&](uint32_t vstage, int hf, bool accumulate) {
         const uint32_t b0 = dv_base + ((vstage * kTileBytes) >> 4);
-        mma_ts_lo(d_o, d_s, b0, idPV, accumulate ? 1u : 0u);
 #pragma unroll
-        for (int kk = 1; kk < 8; ++kk) mma_ts_lo(d_o, d_s + kk * 8, b0 + ((kk * 2048) >> 4), idPV, 1u);
+        for (int k4 = 0; k4 < 4; ++k4) {
+          const int kk = 4 * hf + k4;
+          mma_ts_lo(d_o, d_s + kk * 8, b0 + ((kk * 2048) >> 4), idPV,
+                    (accumulate || kk > 0) ? 1u : 0u);
+        }
       };
       FwdCursor cursor(sc, blockIdx.x, a.R, a.g);
       TileRec cur, nxt;
@@ -266,7 +271,8 @@ replay_fwd_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a, con
         const bool early_k = has_nxt && !nxt.first_of_unit;
         if (!mbar_wait(bar_addr(sbase, B_KV_FULL + vstage), vpar)) { fail(); break; }
         if (early_k && !mbar_wait(bar_addr(sbase, B_KV_FULL + kstage), kpar)) { fail(); break; }
-        if (!mbar_wait(bar_addr(sbase, B_P_FULL + t), kc & 1)) { fail(); break; }
+        // first half of P_t (keys [0,64)); the softmax still works on the second
+        if (!mbar_wait(bar_addr(sbase, B_P_FULL + 2 * t), kc & 1)) { fail(); break; }
         // Keep the tiles half a period apart: tile B's group for tile k follows tile A's
         // P V of tile k, tile A's group for tile k follows tile B's P V of tile k - 1.
         // Each group then lands in the tensor core's queue while the other tile's S is
@@ -274,9 +280,12 @@ replay_fwd_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a, con
         // of both softmax warpgroups contending for the exp2 units at the same time.
         if (t == 1 && !mbar_wait(bar_addr(sbase, B_PV_DONE + 0), kc & 1)) { fail(); break; }
         if (t == 0 && kc > 0 && !mbar_wait(bar_addr(sbase, B_PV_DONE + 1), (kc - 1) & 1)) { fail(); break; }
+        tc_fence_after();
+        issue_pv_half(vstage, 0, !cur.first_of_unit);
+        if (!mbar_wait(bar_addr(sbase, B_P_FULL + 2 * t + 1), kc & 1)) { fail(); break; }
         ++kc;
         tc_fence_after();
-        issue_pv(vstage, !cur.first_of_unit);
+        issue_pv_half(vstage, 1, true);
         mma_commit(bar_addr(sbase, B_PV_DONE + t));
         if (cur.last_of_unit) mma_commit(bar_addr(sbase, B_O_DONE + t));
         mma_commit(bar_addr(sbase, B_KV_EMPTY + vstage));
@@ -364,32 +373,8 @@ replay_fwd_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a, con
         rescale = true;
       }
       const float msub = (m == -INFINITY) ? 0.f : m;
-      // packed fp32x2 arithmetic: one instruction per pair of columns
-      const float2 c2 = make_float2(c, c), nm2 = make_float2(-msub, -msub);
-      float2 ls4[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                       make_float2(0.f, 0.f)};
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {  // P in two 64-column halves
-        uint32_t pk[32];
-#pragma unroll
-        for (int jj = 0; jj < 32; ++jj) {
-          const int j = half * 32 + jj;
-          float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[2 * j]), __uint_as_float(sr[2 * j + 1])),
-                                c2, nm2);
-          x.x = fast_exp2(x.x);
-          x.y = fast_exp2(x.y);
-          ls4[jj & 3] = __fadd2_rn(ls4[jj & 3], x);
-          pk[jj] = pack_bf16(x.x, x.y);
-        }
-        tmem_st32(s_col + half * 32, pk);
-      }
-      const float2 lsa = __fadd2_rn(__fadd2_rn(ls4[0], ls4[1]), __fadd2_rn(ls4[2], ls4[3]));
-      const float ls = lsa.x + lsa.y;
-      {
-        const float tsum = l + ls;
-        lcomp += (l - tsum) + ls;
-        l = tsum;
-      }
+      // rescale O first (rare): P_t V of this tile adds to it as soon as the first half
+      // of P is in tensor memory
       if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll 1
         for (int c0 = 0; c0 < 128; c0 += 32) {
@@ -402,9 +387,35 @@ replay_fwd_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a, con
           tmem_st32(o_col + c0, ov);
         }
       }
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(bar_addr(sbase, B_P_FULL + t));
+      // packed fp32x2 arithmetic: one instruction per pair of columns
+      const float2 c2 = make_float2(c, c), nm2 = make_float2(-msub, -msub);
+      float2 ls4[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                       make_float2(0.f, 0.f)};
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {  // P in two 64-key halves, released one by one
+        uint32_t pk[32];
+#pragma unroll
+        for (int jj = 0; jj < 32; ++jj) {
+          const int j = half * 32 + jj;
+          float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[2 * j]), __uint_as_float(sr[2 * j + 1])),
+                                c2, nm2);
+          x.x = fast_exp2(x.x);
+          x.y = fast_exp2(x.y);
+          ls4[jj & 3] = __fadd2_rn(ls4[jj & 3], x);
+          pk[jj] = pack_bf16(x.x, x.y);
+        }
+        tmem_st32(s_col + half * 32, pk);
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(bar_addr(sbase, B_P_FULL + 2 * t + half));
+      }
+      const float2 lsa = __fadd2_rn(__fadd2_rn(ls4[0], ls4[1]), __fadd2_rn(ls4[2], ls4[3]));
+      const float ls = lsa.x + lsa.y;
+      {
+        const float tsum = l + ls;
+        lcomp += (l - tsum) + ls;
+        l = tsum;
+      }
       ++kc;
       if (r.last_of_unit) {
         if (!mbar_wait(bar_addr(sbase, B_O_DONE + t), oc & 1)) { fail(); break; }
