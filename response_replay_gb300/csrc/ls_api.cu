@@ -101,11 +101,12 @@ struct FwdWs {
 FwdWs fwd_ws(const LsSched& sc, int unit_rows) {
   FwdWs w;
   size_t p = 0;
-  const bool tail = sc.tail_items > 0;
+  // one partial (o, lse) per tail piece when the tail units are cut into pieces
+  const size_t slots = sc.has_partials() ? (size_t)sc.num_pieces() : 0;
   w.part_o = p;
-  p = align256(p + (tail ? (size_t)2 * sc.ctas * unit_rows * kHeadDim * 4 : 0));
+  p = align256(p + slots * unit_rows * kHeadDim * 4);
   w.part_lse = p;
-  p = align256(p + (tail ? (size_t)2 * sc.ctas * unit_rows * 4 : 0));
+  p = align256(p + slots * unit_rows * 4);
   w.total = p;
   return w;
 }
@@ -119,7 +120,7 @@ BwdWs bwd_ws(const LsSched& sc, int unit_rows, int R, int Hq) {
   w.delta = p;
   p = align256(p + (size_t)R * Hq * 4);
   w.part_dq = p;
-  p = align256(p + (sc.tail_items > 0 ? (size_t)2 * sc.ctas * unit_rows * kHeadDim * 4 : 0));
+  p = align256(p + (sc.has_partials() ? (size_t)sc.num_pieces() * unit_rows * kHeadDim * 4 : 0));
   w.total = p;
   return w;
 }

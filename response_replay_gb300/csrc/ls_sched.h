@@ -9,13 +9,17 @@
 // (the on-chip counterpart of the cross-rank LSE/output merge the LongStraw explainer
 // describes in "Two incompatible architectures", Qwen bullet).
 //
-// Schedule ("full waves + split tail"): with C persistent CTAs and U units, the first
-// W = floor(U / C) waves give each CTA whole units (unit w*C + c in wave w), so every
-// CTA of a wave starts at prompt position 0 at the same time and walks the prompt in
-// lockstep: CTAs that share a KV head read each KV tile from HBM once and from L2
-// after that.  The remaining U - W*C units are cut into their items and the items are
-// shared out evenly (a contiguous range per CTA), which balances the last wave; those
-// are the only units that need the combine.
+// Schedule ("full waves + aligned tail pieces"): with C persistent CTAs and U units,
+// the first W = floor(U / C) waves give each CTA whole units (unit w*C + c in wave w),
+// so every CTA of a wave starts at prompt position 0 at the same time and walks the
+// prompt in lockstep: CTAs that share a KV head read each KV tile from HBM once and
+// from L2 after that.  The T = U - W*C remaining units are each cut at the same Q item
+// boundaries into pieces, and piece k of tail unit t (number p = k*T + t) goes to CTA
+// p mod C in round p div C.  In a round, the CTAs holding piece k of different units
+// walk the same key range together, so the tail shares L2 the way the waves do; Q is
+// the smallest count whose rounds balance the tail to within 2% of T / C units of work
+// per CTA.  Each piece leaves a partial result (slot p) that the combine merges in
+// piece order (when Q = 1 the tail units are processed whole and need no combine).
 //
 // Included by host and device code.
 #pragma once
@@ -34,26 +38,19 @@ struct LsSched {
   int32_t ntiles;      // prompt KV tiles per unit: ceil(P / tile)
   int32_t tps;         // prompt tiles per split
   int32_t nsplit;      // non-empty prompt splits S (0 when P == 0)
-  int64_t tail_items;  // (U - W*C) * (S + 1)
+  int32_t tail_units;  // T = U - W*C
+  int32_t pieces;      // Q pieces per tail unit (1: tail units are processed whole)
 
   LS_HD int32_t items_per_unit() const { return nsplit + 1; }
   LS_HD int32_t tail_unit0() const { return waves * ctas; }
-  // Contiguous tail item range of CTA c, relative to the first tail item.
-  LS_HD int64_t tail_begin(int32_t c) const { return (int64_t)c * tail_items / ctas; }
-  // True when CTA c has tail items (with fewer tail items than CTAs, some ranges are
-  // empty; those CTAs write no partial results and the combine skips them).
-  LS_HD bool tail_nonempty(int32_t c) const { return tail_begin(c + 1) > tail_begin(c); }
-  // CTA whose tail range holds tail item i (the last CTA whose range starts at or
-  // before i, so CTAs with empty ranges are never returned).
-  LS_HD int32_t tail_cta_of(int64_t i) const {
-    return (int32_t)(((i + 1) * ctas + tail_items - 1) / tail_items - 1);
+  LS_HD int32_t num_pieces() const { return tail_units * pieces; }
+  LS_HD bool has_partials() const { return tail_units > 0 && pieces > 1; }
+  // First item of piece k of a tail unit (k = pieces gives items_per_unit()).
+  LS_HD int32_t piece_begin(int32_t k) const {
+    return (int32_t)((int64_t)k * items_per_unit() / pieces);
   }
-  // Partial-result slot of unit u in CTA c (tail units only): slot 2c for the first
-  // unit of c's tail range, 2c+1 for its last unit when that differs.
-  LS_HD int32_t slot_of(int32_t c, int32_t u) const {
-    int32_t first_u = tail_unit0() + (int32_t)(tail_begin(c) / items_per_unit());
-    return 2 * c + (u == first_u ? 0 : 1);
-  }
+  // True when CTA c has any work (some CTAs get no piece when T*Q < C and W = 0).
+  LS_HD bool cta_has_work(int32_t c) const { return waves > 0 || c < num_pieces(); }
   // Prompt tile range [t0, t1) of split s.
   LS_HD void split_tiles(int32_t s, int32_t* t0, int32_t* t1) const {
     int32_t a = s * tps, b = a + tps;
@@ -61,6 +58,12 @@ struct LsSched {
     *t1 = b < ntiles ? b : ntiles;
   }
 };
+
+// Tail time, in units of work per CTA, of T tail units cut into q pieces over C CTAs:
+// ceil(T*q / C) rounds of 1/q unit each.
+inline double ls_tail_cost(int32_t T, int32_t q, int32_t C) {
+  return (double)((T * (int64_t)q + C - 1) / C) / q;
+}
 
 // Host: build the schedule for U units, a prompt of `ntiles` tiles, the caller's split
 // request and a grid of at most `max_ctas` CTAs.
@@ -77,60 +80,82 @@ inline LsSched ls_make_sched(int32_t units, int32_t ntiles, int32_t num_splits, 
     s.tps = 1;
     s.nsplit = 0;
   }
-  int64_t total = (int64_t)units * (s.nsplit + 1);
+  const int32_t ipu = s.nsplit + 1;
+  int64_t total = (int64_t)units * ipu;
   int32_t c = max_ctas;
   if ((int64_t)c > total) c = (int32_t)total;
   if (c < 1) c = 1;
   s.ctas = c;
   s.waves = units / c;
-  s.tail_items = (int64_t)(units - s.waves * c) * (s.nsplit + 1);
+  s.tail_units = units - s.waves * c;
+  s.pieces = 1;
+  if (s.tail_units > 0) {
+    const int32_t qmax = ipu < 32 ? ipu : 32;  // a piece holds at least one item
+    double best = ls_tail_cost(s.tail_units, 1, c);
+    for (int32_t q = 2; q <= qmax; ++q) {
+      const double cq = ls_tail_cost(s.tail_units, q, c);
+      if (cq < best) best = cq;
+    }
+    for (int32_t q = 1; q <= qmax; ++q)
+      if (ls_tail_cost(s.tail_units, q, c) <= best * 1.02) {
+        s.pieces = q;
+        break;
+      }
+  }
   return s;
 }
 
-// Walks the item ranges of one CTA: W whole units, then its tail range.
-// Usage:  LsWalk w(sched, c); int32_t u, s; bool first, last, complete;
-//         while (w.next(&u, &s, &first, &last, &complete)) { ... }
-// first/last: this item is the first/last of unit u that this CTA processes;
-// complete: this CTA processes every item of u (only meaningful when last is set).
+// Walks the item ranges of one CTA: W whole units, then its tail pieces in round order.
+// Usage:  LsWalk w(sched, c); int32_t u, s, slot; bool first, last, complete;
+//         while (w.next(&u, &s, &first, &last, &complete, &slot)) { ... }
+// first/last: this item is the first/last of the current range (a whole unit or a
+// piece); complete: the range is the whole unit u; slot: the partial-result slot of a
+// range that is not complete (-1 otherwise).
 struct LsWalk {
   const LsSched* sc;   // the schedule (the kernel's __grid_constant__ parameter on the
                        // device, so the walk holds a pointer, not a register copy)
   int32_t cta;
-  int32_t range;       // 0..waves-1 whole units, waves = tail
-  int64_t item, end;   // current / end item (global item index u*(S+1)+s)
-  int64_t range_begin;
+  int32_t range;       // -1 before the first; < waves: whole units; then piece rounds
+  int32_t u, it0, it, it_end, slot;
+  bool complete;
 
-  LS_HD LsWalk(const LsSched& s, int32_t c) : sc(&s), cta(c), range(-1), item(0), end(0), range_begin(0) {}
+  LS_HD LsWalk(const LsSched& s, int32_t c)
+      : sc(&s), cta(c), range(-1), u(0), it0(0), it(0), it_end(0), slot(-1), complete(false) {}
 
   LS_HD bool open_range(int32_t r) {
-    const int64_t ipu = sc->items_per_unit();
     if (r < sc->waves) {
-      range_begin = (int64_t)(r * sc->ctas + cta) * ipu;
-      end = range_begin + ipu;
-    } else if (r == sc->waves && sc->tail_items > 0) {
-      int64_t base = (int64_t)sc->tail_unit0() * ipu;
-      range_begin = base + sc->tail_begin(cta);
-      end = base + sc->tail_begin(cta + 1);
+      u = r * sc->ctas + cta;
+      it0 = 0;
+      it_end = sc->items_per_unit();
+      slot = -1;
+      complete = true;
     } else {
-      return false;
+      const int64_t p = (int64_t)cta + (int64_t)(r - sc->waves) * sc->ctas;
+      if (p >= sc->num_pieces()) return false;
+      const int32_t T = sc->tail_units;
+      const int32_t k = (int32_t)(p / T);
+      u = sc->tail_unit0() + (int32_t)(p - (int64_t)k * T);
+      it0 = sc->piece_begin(k);
+      it_end = sc->piece_begin(k + 1);
+      complete = sc->pieces == 1;
+      slot = complete ? -1 : (int32_t)p;
     }
-    item = range_begin;
+    it = it0;
     range = r;
     return true;
   }
 
-  LS_HD bool next(int32_t* u, int32_t* s, bool* first, bool* last, bool* complete) {
-    while (range < 0 || item >= end) {
+  LS_HD bool next(int32_t* uo, int32_t* s, bool* first, bool* last, bool* cpl, int32_t* sl) {
+    while (range < 0 || it >= it_end) {
       if (!open_range(range + 1)) return false;
     }
-    const int64_t ipu = sc->items_per_unit();
-    *u = (int32_t)(item / ipu);
-    *s = (int32_t)(item % ipu);
-    *first = (item == range_begin) || (*s == 0);
-    *last = (item + 1 == end) || (*s == ipu - 1);
-    int64_t ub = (int64_t)(*u) * ipu;
-    *complete = (ub >= range_begin) && (ub + ipu <= end);
-    ++item;
+    *uo = u;
+    *s = it;
+    *first = it == it0;
+    *last = it + 1 == it_end;
+    *cpl = complete;
+    *sl = slot;
+    ++it;
     return true;
   }
 };

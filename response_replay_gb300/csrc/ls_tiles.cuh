@@ -11,6 +11,7 @@ struct TileRec {
   int32_t u;           // unit
   int32_t h, kvh, t0;  // query head, kv head, first token of the unit
   int32_t key0;        // first key of the tile (prompt position or response index)
+  int32_t slot;        // partial-result slot of the tile's range (-1: complete unit)
   bool resp;           // response keys (causal) vs prompt keys
   bool first_of_unit, last_of_unit, complete;
 };
@@ -18,20 +19,20 @@ struct TileRec {
 template <int UnitRows, int Tile>
 struct TileCursor {
   LsWalk walk;
-  int32_t u, s, t, t_end;
+  int32_t u, s, t, t_end, slot;
   bool item_first, item_last, item_complete, valid;
   int32_t R, g, nTB;
   int32_t h, kvh, t0;  // derived from u once per item, not per tile
   bool resp;
 
   __device__ TileCursor(const LsSched& sc, int cta, int32_t R_, int32_t g_)
-      : walk(sc, cta), u(0), s(0), t(0), t_end(0), item_first(false), item_last(false),
+      : walk(sc, cta), u(0), s(0), t(0), t_end(0), slot(-1), item_first(false), item_last(false),
         item_complete(false), valid(false), R(R_), g(g_), h(0), kvh(0), t0(0), resp(false) {
     nTB = (R + UnitRows - 1) / UnitRows;
   }
 
   __device__ bool open_item() {
-    while (walk.next(&u, &s, &item_first, &item_last, &item_complete)) {
+    while (walk.next(&u, &s, &item_first, &item_last, &item_complete, &slot)) {
       h = u / nTB;
       t0 = (u - h * nTB) * UnitRows;
       kvh = h / g;
@@ -78,6 +79,7 @@ struct TileCursor {
     r->kvh = kvh;
     r->resp = resp;
     r->key0 = t * Tile;
+    r->slot = slot;
     ++t;
     r->last_of_unit = item_last && t >= t_end;
     r->complete = item_complete;

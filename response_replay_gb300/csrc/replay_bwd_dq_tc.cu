@@ -417,7 +417,7 @@ bwd_dq_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a, const _
           dst = b.dq + ((int64_t)(valid ? tq : 0) * a.hq + r.h) * kD;
           acc = b.accumulate != 0;
         } else {
-          dst = b.part_dq + ((int64_t)sc.slot_of(blockIdx.x, r.u) * kUnitRows + row) * kD;
+          dst = b.part_dq + ((int64_t)r.slot * kUnitRows + row) * kD;
         }
 #pragma unroll 1
         for (int q = 0; q < 2; ++q) {
@@ -453,27 +453,13 @@ bwd_dq_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a, const _
   }
 }
 
-// Sum the split partials of each tail unit in CTA order.
+// Sum the partial dQ of the pieces of each tail unit in piece order.
 // Grid: (tail units, row groups of kCombineRows); one thread per head_dim column.
 constexpr int kCombineRows = 8;
-constexpr int kMaxSlots = 1024;
 __global__ void __launch_bounds__(kD) bwd_dq_tc_combine(const LsAttnArgs a, const LsSched sc,
                                                         const LsBwdIn b) {
-  const int u = sc.tail_unit0() + blockIdx.x;
-  const int64_t ipu = sc.items_per_unit();
-  const int64_t i0 = (int64_t)(u - sc.tail_unit0()) * ipu;
-  const int c_lo = sc.tail_cta_of(i0), c_hi = sc.tail_cta_of(i0 + ipu - 1);
-  if (c_lo == c_hi) return;
-  __shared__ int s_slot[kMaxSlots];
-  __shared__ int s_n;
-  if (threadIdx.x == 0) {
-    int n = 0;
-    for (int cc = c_lo; cc <= c_hi && n < kMaxSlots; ++cc)
-      if (sc.tail_nonempty(cc)) s_slot[n++] = sc.slot_of(cc, u);
-    s_n = n;
-  }
-  __syncthreads();
-  const int n = s_n;
+  const int tu = blockIdx.x, T = sc.tail_units, Q = sc.pieces;
+  const int u = sc.tail_unit0() + tu;
   const int nTB = (a.R + kUnitRows - 1) / kUnitRows;
   const int h = u / nTB, t0 = (u % nTB) * kUnitRows;
   const int col = threadIdx.x;
@@ -481,12 +467,11 @@ __global__ void __launch_bounds__(kD) bwd_dq_tc_combine(const LsAttnArgs a, cons
     const int t = t0 + r;
     if (t >= a.R) break;
     float acc = 0.f;
-    for (int i = 0; i < n; ++i) acc += b.part_dq[((int64_t)s_slot[i] * kUnitRows + r) * kD + col];
+    for (int k = 0; k < Q; ++k) acc += b.part_dq[((int64_t)(k * T + tu) * kUnitRows + r) * kD + col];
     float* dst = b.dq + ((int64_t)t * a.hq + h) * kD + col;
     *dst = b.accumulate ? *dst + acc : acc;
   }
 }
-
 }  // namespace
 
 int ls_bwd_unit_rows() { return kUnitRows; }
@@ -524,9 +509,8 @@ cudaError_t ls_launch_bwd_dq(const LsAttnArgs& a, const LsSched& sc, const LsBwd
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   ls_note_launch();
-  const int64_t tail_units = sc.units - (int64_t)sc.waves * sc.ctas;
-  if (tail_units > 0) {
-    bwd_dq_tc_combine<<<dim3((unsigned)tail_units, kUnitRows / kCombineRows), kD, 0, st>>>(a, sc, b);
+  if (sc.has_partials()) {
+    bwd_dq_tc_combine<<<dim3((unsigned)sc.tail_units, kUnitRows / kCombineRows), kD, 0, st>>>(a, sc, b);
     e = cudaGetLastError();
     if (e == cudaSuccess) ls_note_launch();
   }

@@ -448,7 +448,7 @@ replay_fwd_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a, con
           }
           if (valid) out.lse[(int64_t)tq * a.hq + r.h] = lse;
         } else {
-          const int slot = sc.slot_of(blockIdx.x, r.u);
+          const int slot = r.slot;
           float* prow = out.part_o + ((int64_t)slot * kUnitRows + t * kTile + row) * kD;
 #pragma unroll 1
           for (int c0 = 0; c0 < 128; c0 += 32) {
@@ -479,28 +479,14 @@ replay_fwd_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a, con
   }
 }
 
-// Merge the partial (o, lse) of every tail unit split across CTAs (fixed order):
-//   lse = log sum_c exp(lse_c),  o = sum_c exp(lse_c - lse) o_c.
+// Merge the partial (o, lse) of the pieces of every tail unit (fixed piece order):
+//   lse = log sum_k exp(lse_k),  o = sum_k exp(lse_k - lse) o_k.
 // Grid: (tail units, row groups of kCombineRows); one thread per head_dim column.
 constexpr int kCombineRows = 8;
-constexpr int kMaxSlots = 1024;
 __global__ void __launch_bounds__(kD) replay_fwd_tc_combine(const LsAttnArgs a, const LsSched sc,
                                                             const LsFwdOut out) {
-  const int u = sc.tail_unit0() + blockIdx.x;
-  const int64_t ipu = sc.items_per_unit();
-  const int64_t i0 = (int64_t)(u - sc.tail_unit0()) * ipu;
-  const int c_lo = sc.tail_cta_of(i0), c_hi = sc.tail_cta_of(i0 + ipu - 1);
-  if (c_lo == c_hi) return;
-  __shared__ int s_slot[kMaxSlots];
-  __shared__ int s_n;
-  if (threadIdx.x == 0) {
-    int n = 0;
-    for (int cc = c_lo; cc <= c_hi && n < kMaxSlots; ++cc)
-      if (sc.tail_nonempty(cc)) s_slot[n++] = sc.slot_of(cc, u);
-    s_n = n;
-  }
-  __syncthreads();
-  const int n = s_n;
+  const int tu = blockIdx.x, T = sc.tail_units, Q = sc.pieces;
+  const int u = sc.tail_unit0() + tu;
   const int nTB = (a.R + kUnitRows - 1) / kUnitRows;
   const int h = u / nTB, t0 = (u % nTB) * kUnitRows;
   const int col = threadIdx.x;
@@ -508,13 +494,13 @@ __global__ void __launch_bounds__(kD) replay_fwd_tc_combine(const LsAttnArgs a, 
     const int t = t0 + r;
     if (t >= a.R) break;
     float mx = -INFINITY;
-    for (int i = 0; i < n; ++i) mx = fmaxf(mx, out.part_lse[(int64_t)s_slot[i] * kUnitRows + r]);
+    for (int k = 0; k < Q; ++k) mx = fmaxf(mx, out.part_lse[(int64_t)(k * T + tu) * kUnitRows + r]);
     float sum = 0.f;
-    for (int i = 0; i < n; ++i) sum += expf(out.part_lse[(int64_t)s_slot[i] * kUnitRows + r] - mx);
+    for (int k = 0; k < Q; ++k) sum += expf(out.part_lse[(int64_t)(k * T + tu) * kUnitRows + r] - mx);
     const float lse = mx + logf(sum);
     float acc = 0.f;
-    for (int i = 0; i < n; ++i) {
-      const int64_t slot = s_slot[i];
+    for (int k = 0; k < Q; ++k) {
+      const int64_t slot = k * T + tu;
       acc += expf(out.part_lse[slot * kUnitRows + r] - lse) * out.part_o[(slot * kUnitRows + r) * kD + col];
     }
     const int64_t row = (int64_t)t * a.hq + h;
@@ -563,9 +549,8 @@ cudaError_t ls_launch_replay_fwd(const LsAttnArgs& a, const LsSched& sc, const L
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   ls_note_launch();
-  const int64_t tail_units = sc.units - (int64_t)sc.waves * sc.ctas;
-  if (tail_units > 0) {
-    replay_fwd_tc_combine<<<dim3((unsigned)tail_units, kUnitRows / kCombineRows), kD, 0, st>>>(a, sc, out);
+  if (sc.has_partials()) {
+    replay_fwd_tc_combine<<<dim3((unsigned)sc.tail_units, kUnitRows / kCombineRows), kD, 0, st>>>(a, sc, out);
     e = cudaGetLastError();
     if (e == cudaSuccess) ls_note_launch();
   }

@@ -1,7 +1,9 @@
 // Host check of the replay-attention work schedule (ls_sched.h): for many shapes,
-// every (unit, item) is processed exactly once, "complete" is set exactly for units one
-// CTA processes whole, the combine's CTA range for a split unit is exactly the set of
-// CTAs that touched it, and partial-result slots never collide.
+// every (unit, item) is processed exactly once, ranges carry consistent first/last
+// flags, "complete" is set exactly for units one CTA processes whole, every partial
+// slot has exactly one writer and the combine's slots k*T + t of a tail unit are
+// exactly the slots written for it, the waves keep their lockstep assignment, and the
+// tail pieces balance the work to within 2% of the best piece count.
 #include <cstdio>
 #include <cstdlib>
 #include <map>
@@ -18,67 +20,74 @@ static int fail(const char* what, int U, int nt, int sp, int C) {
 static int check(int U, int nt, int sp, int C) {
   LsSched s = ls_make_sched(U, nt, sp, C);
   const int ipu = s.items_per_unit();
+  if (s.tail_units != U - s.waves * s.ctas || s.tail_units < 0 || s.tail_units >= s.ctas)
+    return fail("tail units", U, nt, sp, C);
+  if (s.pieces < 1 || s.pieces > ipu) return fail("piece count", U, nt, sp, C);
   std::vector<int> seen((size_t)U * ipu, 0);
-  std::map<int, std::set<int>> ctas_of_unit;
-  std::map<int, int> complete_of_unit;   // unit -> cta that completed it
-  std::map<int, std::set<int>> slot_writers;  // slot -> units
+  std::map<int, int> complete_of_unit;         // unit -> cta that completed it
+  std::map<int, std::set<int>> slots_of_unit;  // unit -> partial slots written
+  std::map<int, int> writers_of_slot;
   for (int c = 0; c < s.ctas; ++c) {
     LsWalk w(s, c);
-    int u, it, cur = -1;
+    int u, it, slot, cur = -1, cur_slot = -2;
     bool first, last, complete;
     bool expect_first = true;
-    while (w.next(&u, &it, &first, &last, &complete)) {
+    int n = 0;
+    while (w.next(&u, &it, &first, &last, &complete, &slot)) {
+      ++n;
       if (u < 0 || u >= U || it < 0 || it >= ipu) return fail("range", U, nt, sp, C);
       seen[(size_t)u * ipu + it]++;
-      ctas_of_unit[u].insert(c);
       if (first != expect_first) return fail("first flag", U, nt, sp, C);
-      if (!first && u != cur) return fail("unit change without first", U, nt, sp, C);
+      if (!first && (u != cur || slot != cur_slot)) return fail("range change without first", U, nt, sp, C);
       cur = u;
+      cur_slot = slot;
       expect_first = last;
+      if (complete != (slot < 0)) return fail("complete vs slot", U, nt, sp, C);
       if (last) {
         if (complete) {
           if (complete_of_unit.count(u)) return fail("completed twice", U, nt, sp, C);
           complete_of_unit[u] = c;
         } else {
           if (u < s.tail_unit0()) return fail("partial outside tail", U, nt, sp, C);
-          slot_writers[s.slot_of(c, u)].insert(u);
+          if (writers_of_slot[slot]++) return fail("slot written twice", U, nt, sp, C);
+          slots_of_unit[u].insert(slot);
         }
       }
     }
+    if ((n > 0) != s.cta_has_work(c)) return fail("cta_has_work", U, nt, sp, C);
   }
   for (size_t i = 0; i < seen.size(); ++i)
     if (seen[i] != 1) return fail("item not processed exactly once", U, nt, sp, C);
-  for (auto& kv : slot_writers)
-    if (kv.second.size() != 1) return fail("slot collision", U, nt, sp, C);
   for (int u = 0; u < U; ++u) {
-    const std::set<int>& cs = ctas_of_unit[u];
-    if (cs.size() == 1) {
-      if (!complete_of_unit.count(u)) return fail("single-CTA unit not complete", U, nt, sp, C);
+    if (complete_of_unit.count(u)) {
+      if (slots_of_unit.count(u)) return fail("complete unit with partials", U, nt, sp, C);
       continue;
     }
-    if (complete_of_unit.count(u)) return fail("split unit marked complete", U, nt, sp, C);
-    if (u < s.tail_unit0()) return fail("wave unit split", U, nt, sp, C);
-    const long long i0 = (long long)(u - s.tail_unit0()) * ipu;
-    const int lo = s.tail_cta_of(i0), hi = s.tail_cta_of(i0 + ipu - 1);
+    if (!s.has_partials() || u < s.tail_unit0()) return fail("unit neither complete nor split", U, nt, sp, C);
     std::set<int> expect;
-    for (int c = lo; c <= hi; ++c)
-      if (s.tail_nonempty(c)) expect.insert(c);
-    if (expect != cs) return fail("combine CTA range", U, nt, sp, C);
-    for (int c = lo; c <= hi; ++c)
-      if (s.tail_nonempty(c) &&
-          (!slot_writers.count(s.slot_of(c, u)) || !slot_writers[s.slot_of(c, u)].count(u)))
-        return fail("combine slot not written", U, nt, sp, C);
+    for (int k = 0; k < s.pieces; ++k) expect.insert(k * s.tail_units + (u - s.tail_unit0()));
+    if (expect != slots_of_unit[u]) return fail("combine slots", U, nt, sp, C);
   }
   // full waves: wave w gives unit w*C + c to CTA c (lockstep order)
   for (int u = 0; u < s.tail_unit0(); ++u)
     if (complete_of_unit[u] != u % s.ctas) return fail("wave assignment", U, nt, sp, C);
+  // the chosen piece count is within 2% of the best one
+  if (s.tail_units > 0) {
+    double best = 1e30;
+    for (int q = 1; q <= ipu && q <= 32; ++q) {
+      const double cq = ls_tail_cost(s.tail_units, q, s.ctas);
+      if (cq < best) best = cq;
+    }
+    if (ls_tail_cost(s.tail_units, s.pieces, s.ctas) > best * 1.02 + 1e-12)
+      return fail("tail balance", U, nt, sp, C);
+  }
   return 0;
 }
 
 int main() {
   int bad = 0, n = 0;
-  const int Us[] = {1, 2, 3, 7, 8, 96, 151, 152, 153, 304, 384, 1000};
-  const int nts[] = {0, 1, 2, 5, 32, 64, 257};
+  const int Us[] = {1, 2, 3, 7, 8, 96, 151, 152, 153, 304, 384, 768, 1000};
+  const int nts[] = {0, 1, 2, 5, 32, 64, 257, 16384};
   const int sps[] = {1, 2, 3, 4, 32, 256, 1000};
   const int Cs[] = {1, 2, 5, 148, 152, 304};
   for (int U : Us)
@@ -88,6 +97,12 @@ int main() {
           bad += check(U, nt, sp, C);
           ++n;
         }
+  // the two launches of the 2,097,152-position workload: 384 forward and 768 backward
+  // units over 152 CTAs, 256 splits of 64 tiles
+  for (int U : {384, 768}) {
+    LsSched s = ls_make_sched(U, 16384, 256, 152);
+    std::printf("U=%d: %d waves, %d tail units in %d pieces\n", U, s.waves, s.tail_units, s.pieces);
+  }
   std::printf("%d/%d schedules ok\n", n - bad, n);
   return bad ? 1 : 0;
 }
