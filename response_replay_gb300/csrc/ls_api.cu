@@ -89,8 +89,9 @@ ls_status check_replay(const ls_kv_cache* c, int R, int Hq, int num_splits) {
 }
 
 LsSched make_sched(const ls_kv_cache* c, int R, int Hq, int num_splits, int unit_rows, int tile,
-                   int ctas) {
-  const int units = ls_num_units(R, Hq, c->num_kv_heads, unit_rows);
+                   int ctas, bool fwd) {
+  const int units = fwd ? ls_fwd_units(R, Hq, c->num_kv_heads)
+                        : ls_num_units(R, Hq, c->num_kv_heads, unit_rows);
   const int ntiles = (int)((c->num_tokens + tile - 1) / tile);
   return ls_make_sched(units, ntiles, num_splits, ctas);
 }
@@ -137,6 +138,7 @@ LsAttnArgs attn_args(const ls_kv_cache* c, const void* q, const void* kr, const 
   a.hkv = c->num_kv_heads;
   a.hq = Hq;
   a.g = Hq / c->num_kv_heads;
+  a.pack = 1;
   a.R = R;
   a.q = q;
   a.k_resp = kr;
@@ -190,7 +192,7 @@ ls_status ls_replay_attn_fwd_workspace(const ls_kv_cache* cache, int R, int Hq, 
   DevInfo d;
   if ((s = dev_info(&d)) != LS_OK) return s;
   const LsSched sc = make_sched(cache, R, Hq, num_splits, ls_fwd_unit_rows(), ls_fwd_tile(),
-                                d.sms * ls_fwd_ctas_per_sm());
+                                d.sms * ls_fwd_ctas_per_sm(), true);
   *bytes = fwd_ws(sc, ls_fwd_unit_rows()).total;
   return LS_OK;
 }
@@ -209,11 +211,12 @@ ls_status ls_replay_attn_fwd(const ls_kv_cache* cache, const void* q, const void
   DevInfo d;
   if ((s = dev_info(&d)) != LS_OK) return s;
   const LsSched sc = make_sched(cache, R, Hq, num_splits, ls_fwd_unit_rows(), ls_fwd_tile(),
-                                d.sms * ls_fwd_ctas_per_sm());
+                                d.sms * ls_fwd_ctas_per_sm(), true);
   const FwdWs w = fwd_ws(sc, ls_fwd_unit_rows());
   if (w.total > 0 && (!workspace || workspace_bytes < w.total || !aligned16(workspace)))
     return LS_ERR_WORKSPACE;
-  const LsAttnArgs a = attn_args(cache, q, k_resp, v_resp, R, Hq, softmax_scale, d.err);
+  LsAttnArgs a = attn_args(cache, q, k_resp, v_resp, R, Hq, softmax_scale, d.err);
+  a.pack = ls_fwd_pack(R, Hq, cache->num_kv_heads);
   LsFwdOut out;
   out.o = o;
   out.lse = lse;
@@ -230,7 +233,7 @@ ls_status ls_replay_attn_bwd_workspace(const ls_kv_cache* cache, int R, int Hq, 
   DevInfo d;
   if ((s = dev_info(&d)) != LS_OK) return s;
   const LsSched sc = make_sched(cache, R, Hq, num_splits, ls_bwd_unit_rows(), ls_bwd_tile(),
-                                d.sms * ls_bwd_ctas_per_sm());
+                                d.sms * ls_bwd_ctas_per_sm(), false);
   *bytes = bwd_ws(sc, ls_bwd_unit_rows(), R, Hq).total;
   return LS_OK;
 }
@@ -250,7 +253,7 @@ ls_status ls_replay_attn_bwd(const ls_kv_cache* cache, const void* q, const void
   DevInfo d;
   if ((s = dev_info(&d)) != LS_OK) return s;
   const LsSched sc = make_sched(cache, R, Hq, num_splits, ls_bwd_unit_rows(), ls_bwd_tile(),
-                                d.sms * ls_bwd_ctas_per_sm());
+                                d.sms * ls_bwd_ctas_per_sm(), false);
   const BwdWs w = bwd_ws(sc, ls_bwd_unit_rows(), R, Hq);
   if (!workspace || workspace_bytes < w.total || !aligned16(workspace)) return LS_ERR_WORKSPACE;
   const LsAttnArgs a = attn_args(cache, q, k_resp, v_resp, R, Hq, softmax_scale, d.err);

@@ -90,7 +90,7 @@ inline LsSched ls_make_sched(int32_t units, int32_t ntiles, int32_t num_splits, 
   s.tail_units = units - s.waves * c;
   s.pieces = 1;
   if (s.tail_units > 0) {
-    const int32_t qmax = ipu < 32 ? ipu : 32;  // a piece holds at least one item
+    const int32_t qmax = ipu < 64 ? ipu : 64;  // a piece holds at least one item
     double best = ls_tail_cost(s.tail_units, 1, c);
     for (int32_t q = 2; q <= qmax; ++q) {
       const double cq = ls_tail_cost(s.tail_units, q, c);

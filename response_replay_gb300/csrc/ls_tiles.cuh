@@ -1,7 +1,10 @@
 // ls_tiles.cuh -- the sequence of KV tiles one persistent CTA processes, derived from
-// the work walk of ls_sched.h.  A unit is UnitRows consecutive response tokens of one
-// query head; its items are the prompt splits (tile ranges of Tile keys) followed by
-// the response's own keys (tiles 0 .. ceil(last token of the unit / Tile)).
+// the work walk of ls_sched.h.  A unit is UnitRows query rows that share a KV head:
+// with pack = 1, UnitRows consecutive response tokens of one query head; with pack = g
+// (grouped-query packing, for short responses), the rows of consecutive tokens for all
+// g query heads of one KV head, a tile holding floor(Tile / g) whole tokens.  Its items
+// are the prompt splits (tile ranges of Tile keys) followed by the response's own keys
+// (tiles 0 .. ceil(last token of the unit / Tile)).
 #pragma once
 #include <stdint.h>
 
@@ -9,7 +12,7 @@
 
 struct TileRec {
   int32_t u;           // unit
-  int32_t h, kvh, t0;  // query head, kv head, first token of the unit
+  int32_t h, kvh, t0;  // first query head, kv head, first token of the unit
   int32_t key0;        // first key of the tile (prompt position or response index)
   int32_t slot;        // partial-result slot of the tile's range (-1: complete unit)
   bool resp;           // response keys (causal) vs prompt keys
@@ -21,24 +24,27 @@ struct TileCursor {
   LsWalk walk;
   int32_t u, s, t, t_end, slot;
   bool item_first, item_last, item_complete, valid;
-  int32_t R, g, nTB;
+  int32_t R, g, pack, tok_per_unit, nTB;
   int32_t h, kvh, t0;  // derived from u once per item, not per tile
   bool resp;
 
-  __device__ TileCursor(const LsSched& sc, int cta, int32_t R_, int32_t g_)
+  __device__ TileCursor(const LsSched& sc, int cta, int32_t R_, int32_t g_, int32_t pack_ = 1)
       : walk(sc, cta), u(0), s(0), t(0), t_end(0), slot(-1), item_first(false), item_last(false),
-        item_complete(false), valid(false), R(R_), g(g_), h(0), kvh(0), t0(0), resp(false) {
-    nTB = (R + UnitRows - 1) / UnitRows;
+        item_complete(false), valid(false), R(R_), g(g_), pack(pack_), h(0), kvh(0), t0(0),
+        resp(false) {
+    tok_per_unit = (UnitRows / Tile) * (Tile / pack);
+    nTB = (R + tok_per_unit - 1) / tok_per_unit;
   }
 
   __device__ bool open_item() {
     while (walk.next(&u, &s, &item_first, &item_last, &item_complete, &slot)) {
-      h = u / nTB;
-      t0 = (u - h * nTB) * UnitRows;
-      kvh = h / g;
+      const int32_t grp = u / nTB;  // query head (pack 1) or kv head (packed)
+      t0 = (u - grp * nTB) * tok_per_unit;
+      kvh = pack == 1 ? grp / g : grp;
+      h = pack == 1 ? grp : grp * g;
       resp = (s == walk.sc->nsplit);
       if (resp) {
-        const int32_t qe = t0 + UnitRows < R ? t0 + UnitRows : R;
+        const int32_t qe = t0 + tok_per_unit < R ? t0 + tok_per_unit : R;
         t = 0;
         t_end = (qe + Tile - 1) / Tile;
       } else {

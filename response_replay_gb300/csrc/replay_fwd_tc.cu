@@ -113,6 +113,20 @@ replay_fwd_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a, con
     tmem_alloc(smem_u32(const_cast<uint32_t*>(tmem_slot)), 512);
     tmem_relinquish();
   }
+  {
+    // With grouped-query packing a Q tile holds pack * floor(128 / pack) rows; the rest
+    // are never loaded and stay zero (their outputs are never written).
+    const int used = a.pack * (kTile / a.pack);
+    if (used < kTile) {
+      const int per_half = (kTile - used) * 8;  // 16-byte chunks
+      for (int i = tid; i < 4 * per_half; i += kThreads) {
+        const int part = i / per_half, c = i % per_half;  // part = tile * 2 + half
+        *reinterpret_cast<uint4*>(smem + kOffQ + part * kHalfBytes + used * 128 + c * 16) =
+            make_uint4(0, 0, 0, 0);
+      }
+      fence_proxy_async_smem();
+    }
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -133,7 +147,7 @@ replay_fwd_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a, con
       tma_prefetch_desc(&tm.vp);
       tma_prefetch_desc(&tm.kr);
       tma_prefetch_desc(&tm.vr);
-      FwdCursor cur(sc, blockIdx.x, a.R, a.g);
+      FwdCursor cur(sc, blockIdx.x, a.R, a.g, a.pack);
       TileRec r;
       uint32_t ring = 0, units = 0, aux = 0;
       const int32_t ps = 1 << a.ps_log2;
@@ -143,12 +157,14 @@ replay_fwd_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a, con
       while (ok && cur.next(&r)) {
         if (r.first_of_unit) {
           if (units > 0 && !mbar_wait(bar_addr(sbase, B_Q_EMPTY), (units - 1) & 1)) { fail(); break; }
+          // a tile holds tpt tokens x pack heads (pack = 1: 128 tokens of one head)
           const uint32_t qb = bar_addr(sbase, B_Q_FULL);
-          mbar_expect_tx(qb, 2 * kTileBytes);
+          const int32_t tpt = kTile / a.pack;
+          mbar_expect_tx(qb, 2u * 2u * 128u * (uint32_t)(a.pack * tpt));
           for (int tt = 0; tt < 2; ++tt)
             for (int hf = 0; hf < 2; ++hf)
               tma_load_3d(sbase + kOffQ + tt * kTileBytes + hf * kHalfBytes, &tm.q, hf * 64, r.h,
-                          r.t0 + tt * kTile, qb);
+                          r.t0 + tt * tpt, qb);
           ++units;
         }
         for (int kv = 0; kv < 2 && ok; ++kv) {
@@ -241,7 +257,7 @@ replay_fwd_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a, con
                     (accumulate || kk > 0) ? 1u : 0u);
         }
       };
-      FwdCursor cursor(sc, blockIdx.x, a.R, a.g);
+      FwdCursor cursor(sc, blockIdx.x, a.R, a.g, a.pack);
       TileRec cur, nxt;
       uint32_t ring = 0, units = 0, kc = 0;
       bool ok = cursor.next(&cur);
@@ -318,7 +334,11 @@ replay_fwd_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a, con
     const uint32_t s_col = tmem + lane_off + t * kTile;
     const uint32_t o_col = tmem + lane_off + 256 + t * kTile;
     const float c = a.scale_log2;
-    FwdCursor cursor(sc, blockIdx.x, a.R, a.g);
+    // this thread's row within a tile: token row / pack of the tile, head row % pack
+    const int32_t tpt = kTile / a.pack;
+    const int32_t tok_off = t * tpt + row / a.pack, head_off = row % a.pack;
+    const bool row_used = row < a.pack * tpt;
+    FwdCursor cursor(sc, blockIdx.x, a.R, a.g, a.pack);
     TileRec r;
     uint32_t kc = 0, oc = 0;
     float m = -INFINITY, l = 0.f, lcomp = 0.f;
@@ -335,7 +355,7 @@ replay_fwd_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a, con
       reg_fence32(sr + 32);
       reg_fence32(sr + 64);
       reg_fence32(sr + 96);
-      const int32_t tq = r.t0 + t * kTile + row;  // this row's response token
+      const int32_t tq = r.t0 + tok_off;  // this row's response token
       int32_t lim = kTile;                          // keys [key0, key0 + lim) visible
       if (r.resp) {
         const int32_t lr = (tq + 1 < a.R ? tq + 1 : a.R) - r.key0;
@@ -425,9 +445,10 @@ replay_fwd_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a, con
         const float inv = 1.f / lt;
         const float lse = (m + log2f(lt)) * kLn2;
         if (r.complete) {
-          const bool valid = tq < a.R;
+          const bool valid = row_used && tq < a.R;
+          const int32_t hrow = r.h + head_off;
           __nv_bfloat16* orow =
-              static_cast<__nv_bfloat16*>(out.o) + ((int64_t)(valid ? tq : 0) * a.hq + r.h) * kD;
+              static_cast<__nv_bfloat16*>(out.o) + ((int64_t)(valid ? tq : 0) * a.hq + (valid ? hrow : 0)) * kD;
 #pragma unroll 1
           for (int c0 = 0; c0 < 128; c0 += 32) {
             uint32_t ov[32];
@@ -446,7 +467,7 @@ replay_fwd_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a, con
               }
             }
           }
-          if (valid) out.lse[(int64_t)tq * a.hq + r.h] = lse;
+          if (valid) out.lse[(int64_t)tq * a.hq + hrow] = lse;
         } else {
           const int slot = r.slot;
           float* prow = out.part_o + ((int64_t)slot * kUnitRows + t * kTile + row) * kD;
@@ -487,12 +508,16 @@ __global__ void __launch_bounds__(kD) replay_fwd_tc_combine(const LsAttnArgs a, 
                                                             const LsFwdOut out) {
   const int tu = blockIdx.x, T = sc.tail_units, Q = sc.pieces;
   const int u = sc.tail_unit0() + tu;
-  const int nTB = (a.R + kUnitRows - 1) / kUnitRows;
-  const int h = u / nTB, t0 = (u % nTB) * kUnitRows;
+  const int tpt = kTile / a.pack, tok_per_unit = 2 * tpt;
+  const int nTB = (a.R + tok_per_unit - 1) / tok_per_unit;
+  const int grp = u / nTB, t0 = (u % nTB) * tok_per_unit;
+  const int h0 = a.pack == 1 ? grp : grp * a.g;
   const int col = threadIdx.x;
   for (int r = blockIdx.y * kCombineRows; r < (blockIdx.y + 1) * kCombineRows; ++r) {
-    const int t = t0 + r;
-    if (t >= a.R) break;
+    const int l = r % kTile;  // row within its tile
+    if (l >= a.pack * tpt) continue;
+    const int t = t0 + (r / kTile) * tpt + l / a.pack, h = h0 + l % a.pack;
+    if (t >= a.R) continue;
     float mx = -INFINITY;
     for (int k = 0; k < Q; ++k) mx = fmaxf(mx, out.part_lse[(int64_t)(k * T + tu) * kUnitRows + r]);
     float sum = 0.f;
@@ -518,15 +543,30 @@ int ls_num_units(int R, int hq, int hkv, int unit_rows) {
   (void)hkv;
   return hq * ((R + unit_rows - 1) / unit_rows);
 }
+// Responses shorter than a unit would leave most of a one-head unit empty: pack the g
+// query heads of a KV head into the unit's rows instead (each K/V tile then serves g
+// heads at once, and short replays stream the prompt once per KV head).
+int ls_fwd_pack(int R, int hq, int hkv) {
+  const int g = hq / hkv;
+  return (g > 1 && g <= 64 && R < kUnitRows) ? g : 1;
+}
+int ls_fwd_units(int R, int hq, int hkv) {
+  const int pack = ls_fwd_pack(R, hq, hkv);
+  if (pack == 1) return ls_num_units(R, hq, hkv, kUnitRows);
+  const int tok_per_unit = 2 * (kTile / pack);
+  return hkv * ((R + tok_per_unit - 1) / tok_per_unit);
+}
 
 cudaError_t ls_launch_replay_fwd(const LsAttnArgs& a, const LsSched& sc, const LsFwdOut& out,
                                  cudaStream_t st) {
   TmapSet tm;
   const uint32_t box_q[3] = {64, 1, kTile};
   {
+    // Q boxes: 128 tokens of one head, or floor(128 / pack) tokens x pack heads
+    const uint32_t box_qp[3] = {64, (uint32_t)a.pack, (uint32_t)(kTile / a.pack)};
     const uint64_t dims[3] = {(uint64_t)kD, (uint64_t)a.hq, (uint64_t)a.R};
     const uint64_t strides[2] = {(uint64_t)kD * 2, (uint64_t)a.hq * kD * 2};
-    if (!ls_make_tmap_bf16(&tm.q, a.q, 3, dims, strides, box_q)) return cudaErrorInvalidValue;
+    if (!ls_make_tmap_bf16(&tm.q, a.q, 3, dims, strides, box_qp)) return cudaErrorInvalidValue;
   }
   {
     const uint64_t dims[3] = {(uint64_t)kD, (uint64_t)a.hkv, (uint64_t)a.R};

@@ -74,7 +74,7 @@ static int check(int U, int nt, int sp, int C) {
   // the chosen piece count is within 2% of the best one
   if (s.tail_units > 0) {
     double best = 1e30;
-    for (int q = 1; q <= ipu && q <= 32; ++q) {
+    for (int q = 1; q <= ipu && q <= 64; ++q) {
       const double cq = ls_tail_cost(s.tail_units, q, s.ctas);
       if (cq < best) best = cq;
     }
@@ -99,7 +99,7 @@ int main() {
         }
   // the two launches of the 2,097,152-position workload: 384 forward and 768 backward
   // units over 152 CTAs, 256 splits of 64 tiles
-  for (int U : {384, 768}) {
+  for (int U : {4, 384, 768}) {
     LsSched s = ls_make_sched(U, 16384, 256, 152);
     std::printf("U=%d: %d waves, %d tail units in %d pieces\n", U, s.waves, s.tail_units, s.pieces);
   }

@@ -67,6 +67,27 @@ def test_ragged_fwd_bwd(cuda, P, R, hq, hkv, ps, splits):
     check_bwd(case, dq, dk, dv, pb)
 
 
+# Short responses (R < 256): the forward packs the g query heads of a KV head into a
+# unit's rows (floor(128 / g) whole tokens per tile, g not dividing 128 leaves spare
+# rows); g = 1 and R = 1 included, P = 0, more splits than tiles.
+@pytest.mark.parametrize("P,R,hq,hkv,ps,splits", [
+    (3000, 77, 12, 2, 64, 5),
+    (1000, 1, 6, 1, 16, 3),
+    (5000, 200, 8, 2, 128, 7),
+    (777, 255, 24, 3, 32, 4),
+    (0, 50, 4, 1, 64, 2),
+    (2048, 10, 3, 1, 16, 1000),
+    (4096, 130, 5, 5, 64, 4),
+])
+def test_short_response_packed_fwd_bwd(cuda, P, R, hq, hkv, ps, splits):
+    case = Case(P, R, hq, hkv, ps, splits, seed=P * 5 + R + hq, device=cuda, sharp=True)
+    o, lse = case.fwd()
+    pb = check_fwd(case, o, lse)
+    dq, dk, dv = case.bwd(o, lse)
+    check_bwd(case, dq, dk, dv, pb)
+    assert B.ls_last_device_error(0) == B.LS_OK
+
+
 def test_split_count_does_not_change_result(cuda):
     case = Case(4096, 256, 8, 2, 64, 1, seed=5, device=cuda, sharp=True)
     outs = [case.fwd(num_splits=s) for s in (1, 3, 32, 1000)]

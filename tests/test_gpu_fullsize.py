@@ -25,17 +25,19 @@ def rel(x, ref):
     return float(np.abs(x - ref).max() / max(np.abs(ref).max(), 1e-30))
 
 
-@pytest.mark.parametrize("name,nrows,keys,member", [("p128k", 48, 6, 0), ("p1m", 24, 3, 0),
-                                                   ("p2m", 16, 2, 0), ("p4m_reuse", 8, 2, 5)])
-def test_attention_full_size_sampled(cuda, name, nrows, keys, member):
-    """p4m_reuse: P = 4,194,304 with one of its seeded ragged response lengths."""
+@pytest.mark.parametrize("name,nrows,keys,member,R_short", [
+    ("p128k", 48, 6, 0, None), ("p1m", 24, 3, 0, None), ("p2m", 16, 2, 0, None),
+    ("p4m_reuse", 8, 2, 5, None), ("p2m", 16, 2, 0, 48)])
+def test_attention_full_size_sampled(cuda, name, nrows, keys, member, R_short):
+    """p4m_reuse: P = 4,194,304 with one of its seeded ragged response lengths;
+    R_short: the 2,097,152-position prompt replayed by a short response (packed heads)."""
     w = syn.WORKLOADS[name]
     seed = syn.seed_of(name)
     pr = syn.make_prompt(w.P, w.hkv, 128, w.page_size, seed, cuda)
     cache = api.PagedKVCache(pr.num_pages, pr.page_table, w.page_size, w.hkv, w.P, device=cuda)
     cache.capture(pr.k, pr.v)
     del pr
-    R = w.R[member]
+    R = w.R[member] if R_short is None else R_short
     br = syn.make_branch(R, w.hq, w.hkv, 128, seed + 1, cuda)
     scale = 128 ** -0.5
     o, lse = api.replay_fwd(cache, br.q, br.k, br.v, scale, w.num_splits)
