@@ -431,6 +431,76 @@ def cpu_baseline_attention(cache, br, w, scale, budget_s: float):
                       f"{w.P} prompt keys and the causal response keys; {dt:.1f} s"}
 
 
+# ------------------------------------------------------------------ short-response sweep
+
+def run_short_sweep(args, local_rank: int):
+    """Supplementary, labelled sweep (not the headline line): one replay of short
+    responses R over the 2,097,152-position prompt, where the forward streams the prompt
+    K/V once per KV head and HBM bandwidth, not the tensor cores, is the bound.  One JSON
+    line per R: forward and backward times, prompt-KV GB/s of each pass against the
+    measured copy bandwidth, and the FLOP rate."""
+    import torch
+
+    from response_replay_gb300 import synthetic as syn
+    from response_replay_gb300 import torch_api as api
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    w = syn.WORKLOADS[WORKLOAD]
+    seed = syn.seed_of(WORKLOAD)
+    scale = D ** -0.5
+    pr = syn.make_prompt(w.P, w.hkv, D, w.page_size, seed, dev)
+    cache = api.PagedKVCache(pr.num_pages, pr.page_table, w.page_size, w.hkv, w.P, device=dev)
+    cache.capture(pr.k, pr.v)
+    del pr
+    pk, _ = peaks()
+    hbm = pk.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+    kv_bytes = prompt_kv_bytes(w.P, w.hkv)
+    stream = torch.cuda.current_stream()
+    for R in [int(x) for x in args.sweep_short.split(",")]:
+        br = syn.make_branch(R, w.hq, w.hkv, D, seed + 1, dev)
+        o = torch.empty((R, w.hq, D), dtype=torch.bfloat16, device=dev)
+        lse = torch.empty((R, w.hq), dtype=torch.float32, device=dev)
+        dq = torch.empty((R, w.hq, D), dtype=torch.float32, device=dev)
+        dk = torch.empty((R, w.hkv, D), dtype=torch.float32, device=dev)
+        dv = torch.empty((R, w.hkv, D), dtype=torch.float32, device=dev)
+
+        def fwd():
+            api.replay_fwd(cache, br.q, br.k, br.v, scale, w.num_splits, o=o, lse=lse, stream=stream)
+
+        def bwd():
+            api.replay_bwd(cache, br.q, br.k, br.v, o, lse, br.d_o, scale, w.num_splits, dq=dq,
+                           dk=dk, dv=dv, stream=stream)
+
+        def timed(fn):
+            for _ in range(args.warmup):
+                fn()
+            torch.cuda.synchronize()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for _ in range(args.steps):
+                fn()
+            b.record(stream)
+            torch.cuda.synchronize()
+            return a.elapsed_time(b) / args.steps
+
+        f_ms, b_ms = timed(fwd), timed(bwd)
+        f_fl, b_fl = attn_flops(w.P, R, w.hq)
+        print(json.dumps({
+            "sweep": "short responses over the 2,097,152-position prompt (supplementary)",
+            "R": R, "config": {"workload": f"P={w.P:,}, Hq={w.hq}, Hkv={w.hkv}, d=128, "
+                                           f"{w.page_size}-token pages, {w.num_splits} splits"},
+            "fwd_ms": f_ms, "bwd_ms": b_ms,
+            "fwd_kv_gbs": kv_bytes / (f_ms * 1e-3) / 1e9,
+            "bwd_kv_gbs": kv_bytes / (b_ms * 1e-3) / 1e9,
+            "fwd_frac_of_hbm": kv_bytes / (f_ms * 1e-3) / 1e9 / hbm,
+            "bwd_frac_of_hbm": kv_bytes / (b_ms * 1e-3) / 1e9 / hbm,
+            "fwd_tflops": f_fl / (f_ms * 1e-3) / 1e12, "bwd_tflops": b_fl / (b_ms * 1e-3) / 1e12,
+            "hbm_peak_gbs": hbm, "steps": args.steps, "warmup": args.warmup,
+        }), flush=True)
+
+
 # ------------------------------------------------------------------ reference arm
 
 def run_reference(args, rank: int, world: int):
@@ -502,6 +572,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--ref-rows-per-core", type=int, default=2)
+    ap.add_argument("--sweep-short", default=None,
+                    help="comma-separated response lengths: supplementary short-R sweep "
+                         "(one JSON line each) instead of the headline step")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         print("note: fewer than 3 warm-up steps", file=sys.stderr)
@@ -510,6 +583,10 @@ def main():
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     if args.impl == "reference":
         run_reference(args, rank, world)
+        return
+    if args.sweep_short:
+        if rank == 0:
+            run_short_sweep(args, local_rank)
         return
     if world > 1:
         import torch

@@ -90,8 +90,9 @@ ls_status check_replay(const ls_kv_cache* c, int R, int Hq, int num_splits) {
 
 LsSched make_sched(const ls_kv_cache* c, int R, int Hq, int num_splits, int unit_rows, int tile,
                    int ctas, bool fwd) {
+  (void)unit_rows;
   const int units = fwd ? ls_fwd_units(R, Hq, c->num_kv_heads)
-                        : ls_num_units(R, Hq, c->num_kv_heads, unit_rows);
+                        : ls_bwd_units(R, Hq, c->num_kv_heads);
   const int ntiles = (int)((c->num_tokens + tile - 1) / tile);
   return ls_make_sched(units, ntiles, num_splits, ctas);
 }
@@ -139,6 +140,7 @@ LsAttnArgs attn_args(const ls_kv_cache* c, const void* q, const void* kr, const 
   a.hq = Hq;
   a.g = Hq / c->num_kv_heads;
   a.pack = 1;
+  a.tiles = 2;
   a.R = R;
   a.q = q;
   a.k_resp = kr;
@@ -217,6 +219,7 @@ ls_status ls_replay_attn_fwd(const ls_kv_cache* cache, const void* q, const void
     return LS_ERR_WORKSPACE;
   LsAttnArgs a = attn_args(cache, q, k_resp, v_resp, R, Hq, softmax_scale, d.err);
   a.pack = ls_fwd_pack(R, Hq, cache->num_kv_heads);
+  a.tiles = ls_fwd_tiles(R, Hq, cache->num_kv_heads);
   LsFwdOut out;
   out.o = o;
   out.lse = lse;
@@ -256,7 +259,8 @@ ls_status ls_replay_attn_bwd(const ls_kv_cache* cache, const void* q, const void
                                 d.sms * ls_bwd_ctas_per_sm(), false);
   const BwdWs w = bwd_ws(sc, ls_bwd_unit_rows(), R, Hq);
   if (!workspace || workspace_bytes < w.total || !aligned16(workspace)) return LS_ERR_WORKSPACE;
-  const LsAttnArgs a = attn_args(cache, q, k_resp, v_resp, R, Hq, softmax_scale, d.err);
+  LsAttnArgs a = attn_args(cache, q, k_resp, v_resp, R, Hq, softmax_scale, d.err);
+  a.pack = ls_bwd_pack(R, Hq, cache->num_kv_heads);
   LsBwdIn b;
   b.o = o;
   b.lse = lse;

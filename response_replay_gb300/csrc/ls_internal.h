@@ -24,6 +24,8 @@ struct LsAttnArgs {
   int64_t P;                 // valid prompt tokens
   int32_t hkv, hq, g;        // g = hq / hkv
   int32_t pack;              // query rows per token in a tile: g (packed) or 1
+  int32_t tiles;             // forward: query tiles per unit (2, or 1 when a packed unit's
+                             // tokens all fit one tile)
   int32_t R;                 // response tokens
   const void* q;             // bf16 [R][hq][128]
   const void* k_resp;        // bf16 [R][hkv][128]
@@ -63,6 +65,10 @@ int ls_num_units(int R, int hq, int hkv, int unit_rows);
 // Forward: grouped-query packing factor (g for short responses, else 1) and units.
 int ls_fwd_pack(int R, int hq, int hkv);
 int ls_fwd_units(int R, int hq, int hkv);
+int ls_fwd_tiles(int R, int hq, int hkv);
+// Backward: the same packing for its one-tile units.
+int ls_bwd_pack(int R, int hq, int hkv);
+int ls_bwd_units(int R, int hq, int hkv);
 
 cudaError_t ls_launch_capture(const void* k, const void* v, void* k_pool, void* v_pool,
                               const int32_t* page_table, int32_t num_pages, int32_t ps_log2,

@@ -28,11 +28,12 @@ struct TileCursor {
   int32_t h, kvh, t0;  // derived from u once per item, not per tile
   bool resp;
 
-  __device__ TileCursor(const LsSched& sc, int cta, int32_t R_, int32_t g_, int32_t pack_ = 1)
+  __device__ TileCursor(const LsSched& sc, int cta, int32_t R_, int32_t g_, int32_t pack_ = 1,
+                        int32_t tiles_ = UnitRows / Tile)
       : walk(sc, cta), u(0), s(0), t(0), t_end(0), slot(-1), item_first(false), item_last(false),
         item_complete(false), valid(false), R(R_), g(g_), pack(pack_), h(0), kvh(0), t0(0),
         resp(false) {
-    tok_per_unit = (UnitRows / Tile) * (Tile / pack);
+    tok_per_unit = tiles_ * (Tile / pack);
     nTB = (R + tok_per_unit - 1) / tok_per_unit;
   }
 

@@ -123,6 +123,20 @@ bwd_dq_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a, const _
     tmem_alloc(smem_u32(const_cast<uint32_t*>(tmem_slot)), 512);
     tmem_relinquish();
   }
+  {
+    // With grouped-query packing a tile holds pack * floor(128 / pack) rows; the rest of
+    // the Q and dO tiles are never loaded and stay zero (their outputs are never written).
+    const int used = a.pack * (kTile / a.pack);
+    if (used < kTile) {
+      const int per_half = (kTile - used) * 8;  // 16-byte chunks
+      for (int i = tid; i < 4 * per_half; i += kThreads) {
+        const int part = i / per_half, c = i % per_half;  // Q / dO x two halves
+        *reinterpret_cast<uint4*>(smem + kOffQ + part * kHalfBytes + used * 128 + c * 16) =
+            make_uint4(0, 0, 0, 0);
+      }
+      fence_proxy_async_smem();
+    }
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -143,7 +157,7 @@ bwd_dq_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a, const _
       tma_prefetch_desc(&tm.vp);
       tma_prefetch_desc(&tm.kr);
       tma_prefetch_desc(&tm.vr);
-      DqCursor cur(sc, blockIdx.x, a.R, a.g);
+      DqCursor cur(sc, blockIdx.x, a.R, a.g, a.pack);
       TileRec r;
       uint32_t kc = 0, vc = 0, units = 0, aux = 0;
       const int32_t ps = 1 << a.ps_log2;
@@ -153,8 +167,9 @@ bwd_dq_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a, const _
       while (ok && cur.next(&r)) {
         if (r.first_of_unit) {
           if (units > 0 && !mbar_wait(bar_addr(sbase, B_Q_EMPTY), (units - 1) & 1)) { fail(); break; }
+          // the tile holds floor(128 / pack) tokens x pack heads (pack = 1: 128 tokens)
           const uint32_t qb = bar_addr(sbase, B_Q_FULL);
-          mbar_expect_tx(qb, 2 * kTileBytes);
+          mbar_expect_tx(qb, 2u * 2u * 128u * (uint32_t)(a.pack * (kTile / a.pack)));
           for (int hf = 0; hf < 2; ++hf) {
             tma_load_3d(sbase + kOffQ + hf * kHalfBytes, &tm.q, hf * 64, r.h, r.t0, qb);
             tma_load_3d(sbase + kOffDO + hf * kHalfBytes, &tm.d_o, hf * 64, r.h, r.t0, qb);
@@ -231,7 +246,7 @@ bwd_dq_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a, const _
       const uint32_t dk_base = sdesc_lo(sbase + kOffK, 16);
       const uint32_t dv_base = sdesc_lo(sbase + kOffV, 16);
       const uint32_t dkm_base = sdesc_lo(sbase + kOffK, kHalfBytes);
-      DqCursor cursor(sc, blockIdx.x, a.R, a.g);
+      DqCursor cursor(sc, blockIdx.x, a.R, a.g, a.pack);
       // first / last of unit of tiles j (f0, l0) and j+1 (f1, l1)
       bool f0 = false, l0 = false, f1 = false, l1 = false;
       bool have0 = cursor.next_flags(&f0, &l0);
@@ -336,14 +351,18 @@ bwd_dq_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a, const _
     const int row = quad * 32 + lane;
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
     const float c = a.scale_log2;
-    DqCursor cursor(sc, blockIdx.x, a.R, a.g);
+    // this thread's row: token row / pack of the unit, head row % pack
+    const int32_t tok_off = row / a.pack, head_off = row % a.pack;
+    const bool row_used = row < a.pack * (kTile / a.pack);
+    DqCursor cursor(sc, blockIdx.x, a.R, a.g, a.pack);
     TileRec r;
     uint32_t j = 0, uc = 0;
     float lse2 = 0.f, dd = 0.f;
     while (cursor.next(&r)) {
-      const int32_t tq = r.t0 + row;
+      const int32_t tq = r.t0 + tok_off;
+      const int32_t hrow = row_used ? r.h + head_off : r.h;
       if (r.first_of_unit) {
-        const int64_t idx = (int64_t)(tq < a.R ? tq : a.R - 1) * a.hq + r.h;
+        const int64_t idx = (int64_t)(tq < a.R ? tq : a.R - 1) * a.hq + hrow;
         lse2 = b.lse[idx] * kLog2e;
         dd = b.delta[idx];
       }
@@ -410,11 +429,11 @@ bwd_dq_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a, const _
         if (!mbar_wait(bar_addr(sbase, B_DQ_DONE), uc & 1)) { fail(); break; }
         ++uc;
         tc_fence_after();
-        const bool valid = tq < a.R;
+        const bool valid = row_used && tq < a.R;
         float* dst;
         bool acc = false;
         if (r.complete) {
-          dst = b.dq + ((int64_t)(valid ? tq : 0) * a.hq + r.h) * kD;
+          dst = b.dq + ((int64_t)(valid ? tq : 0) * a.hq + hrow) * kD;
           acc = b.accumulate != 0;
         } else {
           dst = b.part_dq + ((int64_t)r.slot * kUnitRows + row) * kD;
@@ -460,12 +479,15 @@ __global__ void __launch_bounds__(kD) bwd_dq_tc_combine(const LsAttnArgs a, cons
                                                         const LsBwdIn b) {
   const int tu = blockIdx.x, T = sc.tail_units, Q = sc.pieces;
   const int u = sc.tail_unit0() + tu;
-  const int nTB = (a.R + kUnitRows - 1) / kUnitRows;
-  const int h = u / nTB, t0 = (u % nTB) * kUnitRows;
+  const int tok_per_unit = kTile / a.pack;
+  const int nTB = (a.R + tok_per_unit - 1) / tok_per_unit;
+  const int grp = u / nTB, t0 = (u % nTB) * tok_per_unit;
+  const int h0 = a.pack == 1 ? grp : grp * a.g;
   const int col = threadIdx.x;
   for (int r = blockIdx.y * kCombineRows; r < (blockIdx.y + 1) * kCombineRows; ++r) {
-    const int t = t0 + r;
-    if (t >= a.R) break;
+    if (r >= a.pack * tok_per_unit) continue;
+    const int t = t0 + r / a.pack, h = h0 + r % a.pack;
+    if (t >= a.R) continue;
     float acc = 0.f;
     for (int k = 0; k < Q; ++k) acc += b.part_dq[((int64_t)(k * T + tu) * kUnitRows + r) * kD + col];
     float* dst = b.dq + ((int64_t)t * a.hq + h) * kD + col;
@@ -475,6 +497,17 @@ __global__ void __launch_bounds__(kD) bwd_dq_tc_combine(const LsAttnArgs a, cons
 }  // namespace
 
 int ls_bwd_unit_rows() { return kUnitRows; }
+// Responses shorter than a unit: pack the g query heads of a KV head into its rows.
+int ls_bwd_pack(int R, int hq, int hkv) {
+  const int g = hq / hkv;
+  return (g > 1 && g <= 64 && R < kUnitRows) ? g : 1;
+}
+int ls_bwd_units(int R, int hq, int hkv) {
+  const int pack = ls_bwd_pack(R, hq, hkv);
+  if (pack == 1) return ls_num_units(R, hq, hkv, kUnitRows);
+  const int tok_per_unit = kTile / pack;
+  return hkv * ((R + tok_per_unit - 1) / tok_per_unit);
+}
 int ls_bwd_tile() { return kTile; }
 int ls_bwd_ctas_per_sm() { return 1; }
 
@@ -482,11 +515,13 @@ cudaError_t ls_launch_bwd_dq(const LsAttnArgs& a, const LsSched& sc, const LsBwd
                              cudaStream_t st) {
   TmapSet tm;
   const uint32_t box_q[3] = {64, 1, kTile};
+  // Q and dO boxes: 128 tokens of one head, or floor(128 / pack) tokens x pack heads
+  const uint32_t box_qp[3] = {64, (uint32_t)a.pack, (uint32_t)(kTile / a.pack)};
   {
     const uint64_t dims[3] = {(uint64_t)kD, (uint64_t)a.hq, (uint64_t)a.R};
     const uint64_t strides[2] = {(uint64_t)kD * 2, (uint64_t)a.hq * kD * 2};
-    if (!ls_make_tmap_bf16(&tm.q, a.q, 3, dims, strides, box_q)) return cudaErrorInvalidValue;
-    if (!ls_make_tmap_bf16(&tm.d_o, b.d_o, 3, dims, strides, box_q)) return cudaErrorInvalidValue;
+    if (!ls_make_tmap_bf16(&tm.q, a.q, 3, dims, strides, box_qp)) return cudaErrorInvalidValue;
+    if (!ls_make_tmap_bf16(&tm.d_o, b.d_o, 3, dims, strides, box_qp)) return cudaErrorInvalidValue;
   }
   {
     const uint64_t dims[3] = {(uint64_t)kD, (uint64_t)a.hkv, (uint64_t)a.R};

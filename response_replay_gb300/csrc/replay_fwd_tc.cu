@@ -93,10 +93,10 @@ replay_fwd_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a, con
   if (tid == 0) {
     for (int i = 0; i < kStages; ++i) {
       mbar_init(bar_addr(sbase, B_KV_FULL + i), 1);
-      mbar_init(bar_addr(sbase, B_KV_EMPTY + i), 2);  // one commit per issuer
+      mbar_init(bar_addr(sbase, B_KV_EMPTY + i), a.tiles);  // one commit per issuer
     }
     mbar_init(bar_addr(sbase, B_Q_FULL), 1);
-    mbar_init(bar_addr(sbase, B_Q_EMPTY), 2);
+    mbar_init(bar_addr(sbase, B_Q_EMPTY), a.tiles);
     mbar_init(bar_addr(sbase, B_AUX), 1);
     for (int t = 0; t < 2; ++t) {
       mbar_init(bar_addr(sbase, B_S_FULL + t), 1);
@@ -147,7 +147,7 @@ replay_fwd_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a, con
       tma_prefetch_desc(&tm.vp);
       tma_prefetch_desc(&tm.kr);
       tma_prefetch_desc(&tm.vr);
-      FwdCursor cur(sc, blockIdx.x, a.R, a.g, a.pack);
+      FwdCursor cur(sc, blockIdx.x, a.R, a.g, a.pack, a.tiles);
       TileRec r;
       uint32_t ring = 0, units = 0, aux = 0;
       const int32_t ps = 1 << a.ps_log2;
@@ -160,8 +160,8 @@ replay_fwd_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a, con
           // a tile holds tpt tokens x pack heads (pack = 1: 128 tokens of one head)
           const uint32_t qb = bar_addr(sbase, B_Q_FULL);
           const int32_t tpt = kTile / a.pack;
-          mbar_expect_tx(qb, 2u * 2u * 128u * (uint32_t)(a.pack * tpt));
-          for (int tt = 0; tt < 2; ++tt)
+          mbar_expect_tx(qb, (uint32_t)a.tiles * 2u * 128u * (uint32_t)(a.pack * tpt));
+          for (int tt = 0; tt < a.tiles; ++tt)
             for (int hf = 0; hf < 2; ++hf)
               tma_load_3d(sbase + kOffQ + tt * kTileBytes + hf * kHalfBytes, &tm.q, hf * 64, r.h,
                           r.t0 + tt * tpt, qb);
@@ -222,7 +222,7 @@ replay_fwd_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a, con
         mbar_wait(bar_addr(sbase, B_KV_FULL + i % kStages), (i / kStages) & 1);
       if (units > 0) mbar_wait(bar_addr(sbase, B_Q_FULL), (units - 1) & 1);
     }
-  } else if (warp == 1 || warp == 2) {
+  } else if (warp == 1 || (warp == 2 && a.tiles == 2)) {
     // ------------------------------------------------------------ MMA issuers
     // One thread per tile: warp 1 drives tile A, warp 2 tile B.  A tcgen05.mma issue
     // stalls the issuing thread while the tensor core's queue is full, so a single
@@ -257,7 +257,7 @@ replay_fwd_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a, con
                     (accumulate || kk > 0) ? 1u : 0u);
         }
       };
-      FwdCursor cursor(sc, blockIdx.x, a.R, a.g, a.pack);
+      FwdCursor cursor(sc, blockIdx.x, a.R, a.g, a.pack, a.tiles);
       TileRec cur, nxt;
       uint32_t ring = 0, units = 0, kc = 0;
       bool ok = cursor.next(&cur);
@@ -295,7 +295,8 @@ replay_fwd_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a, con
         // still running, and each tile's softmax overlaps the other tile's MMAs instead
         // of both softmax warpgroups contending for the exp2 units at the same time.
         if (t == 1 && !mbar_wait(bar_addr(sbase, B_PV_DONE + 0), kc & 1)) { fail(); break; }
-        if (t == 0 && kc > 0 && !mbar_wait(bar_addr(sbase, B_PV_DONE + 1), (kc - 1) & 1)) { fail(); break; }
+        if (t == 0 && kc > 0 && a.tiles == 2 &&
+            !mbar_wait(bar_addr(sbase, B_PV_DONE + 1), (kc - 1) & 1)) { fail(); break; }
         tc_fence_after();
         issue_pv_half(vstage, 0, !cur.first_of_unit);
         if (!mbar_wait(bar_addr(sbase, B_P_FULL + 2 * t + 1), kc & 1)) { fail(); break; }
@@ -328,6 +329,7 @@ replay_fwd_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a, con
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
     // ------------------------------------------------------------ softmax warpgroups
     const int t = (warp - 4) >> 2;         // tile A (0) or B (1)
+    const bool tile_used = t < a.tiles;    // one-tile units leave tile B's warps idle
     const int quad = warp & 3;             // tensor-memory lane quadrant of this warp
     const int row = quad * 32 + lane;      // query row within the tile
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
@@ -338,11 +340,11 @@ replay_fwd_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a, con
     const int32_t tpt = kTile / a.pack;
     const int32_t tok_off = t * tpt + row / a.pack, head_off = row % a.pack;
     const bool row_used = row < a.pack * tpt;
-    FwdCursor cursor(sc, blockIdx.x, a.R, a.g, a.pack);
+    FwdCursor cursor(sc, blockIdx.x, a.R, a.g, a.pack, a.tiles);
     TileRec r;
     uint32_t kc = 0, oc = 0;
     float m = -INFINITY, l = 0.f, lcomp = 0.f;
-    while (cursor.next(&r)) {
+    while (tile_used && cursor.next(&r)) {
       if (!mbar_wait(bar_addr(sbase, B_S_FULL + t), kc & 1)) { fail(); break; }
       tc_fence_after();
       uint32_t sr[128];
@@ -508,14 +510,14 @@ __global__ void __launch_bounds__(kD) replay_fwd_tc_combine(const LsAttnArgs a, 
                                                             const LsFwdOut out) {
   const int tu = blockIdx.x, T = sc.tail_units, Q = sc.pieces;
   const int u = sc.tail_unit0() + tu;
-  const int tpt = kTile / a.pack, tok_per_unit = 2 * tpt;
+  const int tpt = kTile / a.pack, tok_per_unit = a.tiles * tpt;
   const int nTB = (a.R + tok_per_unit - 1) / tok_per_unit;
   const int grp = u / nTB, t0 = (u % nTB) * tok_per_unit;
   const int h0 = a.pack == 1 ? grp : grp * a.g;
   const int col = threadIdx.x;
   for (int r = blockIdx.y * kCombineRows; r < (blockIdx.y + 1) * kCombineRows; ++r) {
     const int l = r % kTile;  // row within its tile
-    if (l >= a.pack * tpt) continue;
+    if (l >= a.pack * tpt || r / kTile >= a.tiles) continue;
     const int t = t0 + (r / kTile) * tpt + l / a.pack, h = h0 + l % a.pack;
     if (t >= a.R) continue;
     float mx = -INFINITY;
@@ -550,10 +552,16 @@ int ls_fwd_pack(int R, int hq, int hkv) {
   const int g = hq / hkv;
   return (g > 1 && g <= 64 && R < kUnitRows) ? g : 1;
 }
+// A packed unit whose tokens all fit one tile runs as a one-tile unit: tile B would be
+// padding, and its S -> softmax -> P V chain would only lengthen each KV step.
+int ls_fwd_tiles(int R, int hq, int hkv) {
+  const int pack = ls_fwd_pack(R, hq, hkv);
+  return (pack > 1 && R <= kTile / pack) ? 1 : 2;
+}
 int ls_fwd_units(int R, int hq, int hkv) {
   const int pack = ls_fwd_pack(R, hq, hkv);
   if (pack == 1) return ls_num_units(R, hq, hkv, kUnitRows);
-  const int tok_per_unit = 2 * (kTile / pack);
+  const int tok_per_unit = ls_fwd_tiles(R, hq, hkv) * (kTile / pack);
   return hkv * ((R + tok_per_unit - 1) / tok_per_unit);
 }
 

@@ -27,7 +27,7 @@ def rel(x, ref):
 
 @pytest.mark.parametrize("name,nrows,keys,member,R_short", [
     ("p128k", 48, 6, 0, None), ("p1m", 24, 3, 0, None), ("p2m", 16, 2, 0, None),
-    ("p4m_reuse", 8, 2, 5, None), ("p2m", 16, 2, 0, 48)])
+    ("p4m_reuse", 8, 2, 5, None), ("p2m", 16, 2, 0, 48), ("p2m", 16, 2, 0, 16)])
 def test_attention_full_size_sampled(cuda, name, nrows, keys, member, R_short):
     """p4m_reuse: P = 4,194,304 with one of its seeded ragged response lengths;
     R_short: the 2,097,152-position prompt replayed by a short response (packed heads)."""
