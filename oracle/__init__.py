@@ -17,6 +17,10 @@ Functions and the definitions they follow (LongStraw pages):
                       (digest, Method, last paragraph).
   grpo             -- clipped surrogate with group-relative advantages (digest,
                       Method, L_policy equation).
+  grpo_logp        -- pre-step scoring: log-softmax gather of the target and the
+                      per-token KL estimate exp(d) - d - 1, d = ref - logp, against a
+                      reference policy (the pages fix no KL form; their 2M-token runs
+                      used beta = 0).
 """
 from __future__ import annotations
 
@@ -49,10 +53,11 @@ def lib():
         l.lso_grpo.argtypes = [P, i32, i64, i32, P, P, P, P, i32, i32, i32, dbl, dbl, i32,
                                P, P, P, P, P, P, P]
         l.lso_grpo_dlogits_row.argtypes = [P, i32, i32, i32, dbl, dbl, P]
+        l.lso_grpo_logp.argtypes = [P, i32, i64, i32, P, P, P, P, P]
         l.lso_num_threads.argtypes = []
         for f in ("lso_capture_kv", "lso_attn_fwd", "lso_attn_fwd_rows", "lso_attn_bwd",
                   "lso_attn_bwd_dq_rows", "lso_attn_bwd_dkdv_keys", "lso_grpo",
-                  "lso_grpo_dlogits_row", "lso_num_threads"):
+                  "lso_grpo_dlogits_row", "lso_grpo_logp", "lso_num_threads"):
             getattr(l, f).restype = C.c_int
         _lib = l
     return _lib
@@ -252,6 +257,26 @@ def grpo(logits: np.ndarray, targets, logp_old, rewards, resp_lens, member_begin
                           float(eps), float(adv_eps), std_ddof, _ptr(loss), _ptr(adv), _ptr(lse),
                           _ptr(logp), _ptr(ratio), _ptr(coef), _ptr(zeroed)), "grpo")
     return GrpoResult(float(loss[0]), adv, lse, logp, ratio, coef, zeroed)
+
+
+def grpo_logp(logits: np.ndarray, targets, ref_logp=None):
+    """Pre-step scoring: (lse, logp, kl) per token row of logits [T][V]; kl is None
+    without reference log-probabilities."""
+    logits = np.ascontiguousarray(logits)
+    T, V = logits.shape
+    targets = np.ascontiguousarray(targets, dtype=np.int32)
+    lse = np.zeros(T, np.float64)
+    logp = np.zeros(T, np.float64)
+    kl = None
+    ref_p = None
+    if ref_logp is not None:
+        ref_logp = np.ascontiguousarray(ref_logp, dtype=np.float64)
+        kl = np.zeros(T, np.float64)
+        ref_p = _ptr(ref_logp)
+    _check(lib().lso_grpo_logp(_ptr(logits), _dtype_code(logits), T, V, _ptr(targets), ref_p,
+                               _ptr(lse), _ptr(logp), _ptr(kl) if kl is not None else None),
+           "grpo_logp")
+    return lse, logp, kl
 
 
 def grpo_dlogits_rows(logits: np.ndarray, rows, targets, lse, coef) -> np.ndarray:

@@ -626,3 +626,29 @@ int lso_grpo_dlogits_row(const void* logits_row, int32_t dtype, int32_t V, int32
   }
   return 0;
 }
+
+/* Pre-step scoring of GRPO (no gradient): per token the log-probability of the target,
+ * logp_t = z_{t,y_t} - logsumexp_v z_{t,v}, and, when reference log-probabilities are
+ * given, the per-token KL estimate of the policy from the reference
+ *   kl_t = exp(ref_t - logp_t) - (ref_t - logp_t) - 1
+ * (non-negative, zero exactly when ref_t = logp_t).  ref_logp and kl may be NULL. */
+int lso_grpo_logp(const void* logits, int32_t dtype, int64_t T, int32_t V,
+                  const int32_t* targets, const double* ref_logp, double* lse, double* logp,
+                  double* kl) {
+  int64_t t;
+  if (T < 0 || V <= 0 || (kl && !ref_logp)) return 1;
+  for (t = 0; t < T; ++t)
+    if (targets[t] < 0 || targets[t] >= V) return 1;
+#pragma omp parallel for schedule(dynamic, 4)
+  for (t = 0; t < T; ++t) {
+    const double l = row_lse(logits, dtype, t, V);
+    const double lp = load_one(logits, t * V + targets[t], dtype) - l;
+    if (lse) lse[t] = l;
+    logp[t] = lp;
+    if (kl) {
+      const double d = ref_logp[t] - lp;
+      kl[t] = exp(d) - d - 1.0;
+    }
+  }
+  return 0;
+}

@@ -119,6 +119,13 @@ int lso_grpo(const void* logits, int32_t dtype, int64_t T, int32_t V,
 int lso_grpo_dlogits_row(const void* logits_row, int32_t dtype, int32_t V, int32_t target,
                          double lse, double coef, double* out);
 
+/* Pre-step scoring (no gradient): lse_t, logp_t = z_{t,y_t} - lse_t and, given
+ * ref_logp, kl_t = exp(ref_t - logp_t) - (ref_t - logp_t) - 1.  lse, ref_logp and kl
+ * may be NULL (kl requires ref_logp). */
+int lso_grpo_logp(const void* logits, int32_t dtype, int64_t T, int32_t V,
+                  const int32_t* targets, const double* ref_logp, double* lse, double* logp,
+                  double* kl);
+
 /* Threads the OpenMP runtime will use (1 when built without OpenMP). */
 int lso_num_threads(void);
 

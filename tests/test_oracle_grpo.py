@@ -152,3 +152,40 @@ def test_invalid_arguments():
         oracle.grpo(logits, t, np.zeros(3), [1.0], [3], 0, 1, 0.2, std_ddof=1)
     with pytest.raises(ValueError):   # target outside the vocabulary
         oracle.grpo(logits, np.array([0, 4, 0], np.int32), np.zeros(3), [0, 1], [1, 2], 0, 2, 0.2)
+
+
+def test_logp_matches_library_log_softmax_and_lse_closed_form():
+    logits, targets, _, _ = rand_case([5, 4], 37, 7)
+    lse, logp, kl = oracle.grpo_logp(logits, targets)
+    assert kl is None
+    np.testing.assert_allclose(logp, lib_logp(logits, targets), atol=1e-13)
+    np.testing.assert_allclose(lse, np.log(np.exp(logits).sum(axis=1)), atol=1e-12)
+    # constant rows: lse = log V + c, logp = -log V
+    c = np.full((3, 50), -2.5)
+    lse_c, logp_c, _ = oracle.grpo_logp(c, np.array([0, 9, 49], np.int32))
+    np.testing.assert_allclose(lse_c, np.log(50) - 2.5, atol=1e-14)
+    np.testing.assert_allclose(logp_c, -np.log(50), atol=1e-14)
+    # the loss oracle computes the same logp
+    r = oracle.grpo(logits, targets, np.zeros(9), [0.0, 1.0], [5, 4], 0, 2, 0.2)
+    np.testing.assert_array_equal(r.logp, logp)
+
+
+def test_kl_estimate_closed_cases():
+    """kl = exp(d) - d - 1 with d = ref - logp: zero when the policies agree, 1 - ln 2 at
+    d = ln 2, e^-1 at d = -1, non-negative, and d^2/2 to third order for small d."""
+    logits, targets, _, rng = rand_case([6, 6], 20, 8)
+    lp = lib_logp(logits, targets)
+    _, logp, kl = oracle.grpo_logp(logits, targets, lp)
+    assert (kl == 0).all()
+    d = np.array([np.log(2.0), -1.0, 0.0, 0.7, -2.3, 1e-3, -1e-3, 3.0, 0.1, -0.1, 2.0, -0.5])
+    _, _, kl = oracle.grpo_logp(logits, targets, logp + d)
+    np.testing.assert_allclose(kl[0], 1 - np.log(2.0), atol=1e-14)
+    np.testing.assert_allclose(kl[1], np.exp(-1.0), atol=1e-14)
+    assert (kl >= 0).all()
+    small = np.abs(d) < 0.2
+    np.testing.assert_allclose(kl[small], d[small] ** 2 / 2, atol=np.abs(d[small]).max() ** 3)
+
+
+def test_logp_rejects_bad_arguments():
+    with pytest.raises(ValueError):
+        oracle.grpo_logp(np.zeros((2, 4)), np.array([0, 4], np.int32))
