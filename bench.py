@@ -368,6 +368,24 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": d2h,
                "ms_per_step": e_ms / K}
 
+    # ---- pre-step scoring (outside the step): log-softmax gather of one member's tokens
+    # with the KL estimate against reference log-probabilities; HBM-bound, V*b read per
+    # token
+    s0, s1 = off[0], off[1]
+    ref_lp = logp_old[s0:s1]
+    api.grpo_logp(gin.logits[s0:s1], gin.targets[s0:s1], ref_lp, stream=stream)
+    torch.cuda.synchronize()
+    ea, eb = ev(), None
+    for _ in range(K):
+        api.grpo_logp(gin.logits[s0:s1], gin.targets[s0:s1], ref_lp, stream=stream)
+    eb = ev()
+    torch.cuda.synchronize()
+    sc_ms = ea.elapsed_time(eb) / K
+    tok_bytes = w.vocab * gin.logits.element_size()
+    comps["grpo_logp_tokens_per_s"] = (s1 - s0) / (sc_ms * 1e-3)
+    comps["grpo_logp_hbm_frac"] = (s1 - s0) * tok_bytes / (sc_ms * 1e-3) / 1e9 / pk.get(
+        "hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+
     # ---- CPU baseline: the oracle on a bounded sample of the same workload
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -198,6 +198,24 @@ ls_status ls_grpo_loss_fwd_bwd_noalloc(const void* logits, ls_dtype dtype, int64
                                        float* loss, void* dlogits, float* logp_out,
                                        float* stats, ls_stream_t stream);
 
+/* ls_grpo_logp: pre-step scoring without a gradient (LongStraw explainer: the replay
+ * is the gradient pass of one member; the log-probabilities a step needs before it,
+ * logp_old and a reference policy's, come from forward-only passes like this one).
+ *   logp_t = logits[t][targets[t]] - logsumexp_v logits[t][v]
+ *   kl_t   = exp(d) - d - 1 with d = ref_logp[t] - logp_t  (when ref_logp is given):
+ *            the per-token KL estimate of the policy from the reference, >= 0 and zero
+ *            exactly where the two agree (the pages fix no KL form; their 2M-token runs
+ *            used beta = 0).
+ * logits: [T][V] dtype (bf16 or fp32), targets: int32 [T], ref_logp: fp32 [T] or NULL;
+ * outputs fp32 [T]: logp_out (required), lse_out (natural-log logsumexp, optional),
+ * kl_out (optional, requires ref_logp).  Each row is read once.  No workspace.
+ * Errors: LS_ERR_INVALID_ARG for a bad dtype, T < 0, V <= 0, a missing or unaligned
+ * required pointer, or kl_out without ref_logp; a target outside [0, V) records
+ * LS_ERR_DEVICE_CHECK (see ls_last_device_error) and yields NaN for that token. */
+ls_status ls_grpo_logp(const void* logits, ls_dtype dtype, int64_t T, int V,
+                       const int32_t* targets, const float* ref_logp, float* logp_out,
+                       float* lse_out, float* kl_out, ls_stream_t stream);
+
 /* ---------------------------------------------------------------- checks
  * ls_validate_page_table: enqueue a check that every entry of the page table covering
  * the cache's num_tokens lies in [0, num_pages) and that no physical page is used

@@ -24,7 +24,7 @@ EXPORTED = (
     "ls_replay_attn_bwd_workspace", "ls_replay_attn_bwd", "ls_grpo_workspace",
     "ls_grpo_loss_fwd_bwd", "ls_validate_page_table", "ls_validate_page_table_workspace",
     "ls_last_device_error", "ls_status_string", "ls_kernel_launches",
-    "ls_grpo_loss_fwd_bwd_noalloc", "ls_selftest_wait_timeout",
+    "ls_grpo_loss_fwd_bwd_noalloc", "ls_selftest_wait_timeout", "ls_grpo_logp",
 )
 
 
@@ -73,6 +73,7 @@ def lib() -> C.CDLL:
             "ls_validate_page_table_workspace": [cache, szp],
             "ls_last_device_error": [P],
             "ls_selftest_wait_timeout": [P],
+            "ls_grpo_logp": [P, i32, i64, i32, P, P, P, P, P, P],
             "ls_status_string": [i32],
         }
         for name, args in sig.items():
@@ -176,6 +177,12 @@ def ls_validate_page_table(cache: ls_kv_cache, workspace: int, workspace_bytes: 
 def ls_kernel_launches() -> int:
     """Kernel launches issued by the library so far in this process."""
     return lib().ls_kernel_launches()
+
+
+def ls_grpo_logp(logits: int, dtype: int, T: int, V: int, targets: int, ref_logp: int | None,
+                 logp_out: int, lse_out: int | None, kl_out: int | None, stream: int = 0) -> None:
+    _ok("ls_grpo_logp", lib().ls_grpo_logp(logits, dtype, T, V, targets, ref_logp, logp_out,
+                                           lse_out, kl_out, stream))
 
 
 def ls_selftest_wait_timeout(stream: int = 0) -> None:

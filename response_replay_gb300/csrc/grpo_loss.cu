@@ -141,6 +141,62 @@ __device__ __forceinline__ void ms_add(MS& a, const float* x2, int n) {
   for (int i = 0; i < n; ++i) a.s += fast_exp2(x2[i] - a.m);
 }
 
+// Pass 1 over one row: the online (max, sum of exp2) of z log2e, reduced over the block;
+// every thread receives the row's pair.  16-byte loads over the aligned body
+// [head, tail0), scalar loads for the unaligned head and tail.  red must not be reused
+// before the next __syncthreads.
+template <typename E>
+__device__ MS row_max_sumexp2(const E* __restrict__ zr, int V, int head, int nvec, int tail0,
+                              MS* red) {
+  using VT = Vec<E>;
+  constexpr int NV = VT::N;
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const uint4* zv = reinterpret_cast<const uint4*>(zr + head);
+  MS ms = {-INFINITY, 0.f};
+  for (int i = tid; i < head; i += kRowThreads) {
+    float x = VT::load1(zr + i) * kLog2e;
+    ms_add(ms, &x, 1);
+  }
+  for (int i = tail0 + tid; i < V; i += kRowThreads) {
+    float x = VT::load1(zr + i) * kLog2e;
+    ms_add(ms, &x, 1);
+  }
+  for (int i = tid; i < nvec; i += 4 * kRowThreads) {
+    uint4 u[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      if (i + k * kRowThreads < nvec) u[k] = zv[i + k * kRowThreads];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      if (i + k * kRowThreads < nvec) {
+        float x[NV];
+        VT::unpack(u[k], x);
+#pragma unroll
+        for (int e = 0; e < NV; ++e) x[e] *= kLog2e;
+        ms_add(ms, x, NV);
+      }
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    MS other = {__shfl_xor_sync(0xffffffffu, ms.m, o), __shfl_xor_sync(0xffffffffu, ms.s, o)};
+    ms = ms_merge(ms, other);
+  }
+  if (lane == 0) red[wid] = ms;
+  __syncthreads();
+  if (wid == 0) {
+    MS a = lane < kRowThreads / 32 ? red[lane] : MS{-INFINITY, 0.f};
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      MS other = {__shfl_xor_sync(0xffffffffu, a.m, o), __shfl_xor_sync(0xffffffffu, a.s, o)};
+      a = ms_merge(a, other);
+    }
+    if (lane == 0) red[kRowThreads / 32] = a;
+  }
+  __syncthreads();
+  return red[kRowThreads / 32];
+}
+
 template <typename E>
 __global__ void __launch_bounds__(kRowThreads) grpo_rows(
     const E* __restrict__ logits, int64_t T, int V, const int32_t* __restrict__ targets,
@@ -157,7 +213,7 @@ __global__ void __launch_bounds__(kRowThreads) grpo_rows(
   float* rho_out = at<float>(ws, w.rho);
   float* zeroed_out = at<float>(ws, w.zeroed);
 
-  __shared__ MS red[kRowThreads / 32];
+  __shared__ MS red[kRowThreads / 32 + 1];
   __shared__ float s_bcast[2];
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int nm = me - mb;
@@ -173,45 +229,8 @@ __global__ void __launch_bounds__(kRowThreads) grpo_rows(
     const uint4* zv = reinterpret_cast<const uint4*>(zr + head);
 
     // ---- pass 1: online max / sum-exp (log2 domain)
-    MS ms = {-INFINITY, 0.f};
-    for (int i = tid; i < head; i += kRowThreads) {
-      float x = VT::load1(zr + i) * kLog2e;
-      ms_add(ms, &x, 1);
-    }
-    for (int i = tail0 + tid; i < V; i += kRowThreads) {
-      float x = VT::load1(zr + i) * kLog2e;
-      ms_add(ms, &x, 1);
-    }
-    for (int i = tid; i < nvec; i += 4 * kRowThreads) {
-      uint4 u[4];
-#pragma unroll
-      for (int k = 0; k < 4; ++k)
-        if (i + k * kRowThreads < nvec) u[k] = zv[i + k * kRowThreads];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        if (i + k * kRowThreads < nvec) {
-          float x[NV];
-          VT::unpack(u[k], x);
-#pragma unroll
-          for (int e = 0; e < NV; ++e) x[e] *= kLog2e;
-          ms_add(ms, x, NV);
-        }
-      }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      MS other = {__shfl_xor_sync(0xffffffffu, ms.m, o), __shfl_xor_sync(0xffffffffu, ms.s, o)};
-      ms = ms_merge(ms, other);
-    }
-    if (lane == 0) red[wid] = ms;
-    __syncthreads();
+    const MS a = row_max_sumexp2<E>(zr, V, head, nvec, tail0, red);
     if (wid == 0) {
-      MS a = lane < kRowThreads / 32 ? red[lane] : MS{-INFINITY, 0.f};
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        MS other = {__shfl_xor_sync(0xffffffffu, a.m, o), __shfl_xor_sync(0xffffffffu, a.s, o)};
-        a = ms_merge(a, other);
-      }
       if (lane == 0) {
         // member of this token (binary search over the range's offsets)
         int lo = 0, hi = nm - 1;
@@ -290,6 +309,45 @@ __global__ void __launch_bounds__(kRowThreads) grpo_rows(
       }
     }
     __syncthreads();  // red / s_bcast reuse in the next row
+  }
+}
+
+// Pre-step scoring: logp_t = z_{t,y} - logsumexp z_t for every token row (one read of
+// the row), and with reference log-probabilities the per-token KL estimate
+// kl_t = exp(d) - d - 1, d = ref_t - logp_t, evaluated as expm1(d) - d (no cancellation
+// for small d).  A target outside [0, V) records LS_DEVERR_CHECK and yields NaN.
+template <typename E>
+__global__ void __launch_bounds__(kRowThreads) grpo_logp_rows(
+    const E* __restrict__ logits, int64_t T, int V, const int32_t* __restrict__ targets,
+    const float* __restrict__ ref_logp, float* __restrict__ logp_out, float* __restrict__ lse_out,
+    float* __restrict__ kl_out, uint32_t* err) {
+  using VT = Vec<E>;
+  constexpr int NV = VT::N;
+  __shared__ MS red[kRowThreads / 32 + 1];
+  for (int64_t row = blockIdx.x; row < T; row += gridDim.x) {
+    const E* zr = logits + row * (int64_t)V;
+    const int h = (int)(((16 - (reinterpret_cast<uintptr_t>(zr) & 15)) & 15) / sizeof(E));
+    const int head = h < V ? h : V;
+    const int nvec = (V - head) / NV;
+    const int tail0 = head + nvec * NV;
+    const MS a = row_max_sumexp2<E>(zr, V, head, nvec, tail0, red);
+    if (threadIdx.x == 0) {
+      const float lse = (a.m + log2f(a.s)) * kLn2;
+      const int32_t y = targets[row];
+      float logp = NAN;
+      if ((uint32_t)y < (uint32_t)V) {
+        logp = VT::load1(zr + y) - lse;
+      } else {
+        ls_report(err, LS_DEVERR_CHECK);
+      }
+      logp_out[row] = logp;
+      if (lse_out) lse_out[row] = lse;
+      if (kl_out) {
+        const float d = ref_logp[row] - logp;
+        kl_out[row] = expm1f(d) - d;
+      }
+    }
+    __syncthreads();  // red reuse in the next row
   }
 }
 
@@ -375,6 +433,26 @@ cudaError_t ls_launch_grpo(const LsGrpoArgs& a, int num_sms, cudaStream_t st) {
   }
   grpo_final<<<1, 1024, 0, st>>>(a.T, a.G, a.member_begin, a.member_end, a.accumulate_loss,
                                  a.loss, a.stats, a.workspace);
+  ls_note_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t ls_launch_grpo_logp(const void* logits, bool is_bf16, int64_t T, int V,
+                                const int32_t* targets, const float* ref_logp, float* logp_out,
+                                float* lse_out, float* kl_out, uint32_t* err, int num_sms,
+                                cudaStream_t st) {
+  if (T <= 0) return cudaSuccess;
+  int64_t grid = (int64_t)num_sms * 2;
+  if (grid > T) grid = T;
+  if (is_bf16) {
+    grpo_logp_rows<__nv_bfloat16><<<(unsigned)grid, kRowThreads, 0, st>>>(
+        static_cast<const __nv_bfloat16*>(logits), T, V, targets, ref_logp, logp_out, lse_out,
+        kl_out, err);
+  } else {
+    grpo_logp_rows<float><<<(unsigned)grid, kRowThreads, 0, st>>>(
+        static_cast<const float*>(logits), T, V, targets, ref_logp, logp_out, lse_out, kl_out,
+        err);
+  }
   ls_note_launch();
   return cudaGetLastError();
 }

@@ -355,6 +355,28 @@ ls_status ls_validate_page_table(const ls_kv_cache* cache, void* workspace, size
                                             (cudaStream_t)stream));
 }
 
+ls_status ls_grpo_logp(const void* logits, ls_dtype dtype, int64_t T, int V,
+                       const int32_t* targets, const float* ref_logp, float* logp_out,
+                       float* lse_out, float* kl_out, ls_stream_t stream) {
+  if (dtype != LS_BF16 && dtype != LS_FP32) return LS_ERR_INVALID_ARG;
+  if (T < 0 || V <= 0 || V > (1 << 30)) return LS_ERR_INVALID_ARG;
+  if (kl_out && !ref_logp) return LS_ERR_INVALID_ARG;
+  if (T > 0) {
+    const void* ptrs[] = {logits, targets, logp_out};
+    for (const void* p : ptrs)
+      if (!p || !aligned16(p)) return LS_ERR_INVALID_ARG;
+    const void* opt[] = {ref_logp, lse_out, kl_out};
+    for (const void* p : opt)
+      if (p && !aligned16(p)) return LS_ERR_INVALID_ARG;
+  }
+  DevInfo d;
+  ls_status s = dev_info(&d);
+  if (s != LS_OK) return s;
+  return from_cuda(ls_launch_grpo_logp(logits, dtype == LS_BF16, T, V, targets, ref_logp,
+                                       logp_out, lse_out, kl_out, d.err, d.sms,
+                                       (cudaStream_t)stream));
+}
+
 ls_status ls_selftest_wait_timeout(ls_stream_t stream) {
   DevInfo d;
   ls_status s = dev_info(&d);

@@ -76,6 +76,10 @@ cudaError_t ls_launch_capture(const void* k, const void* v, void* k_pool, void* 
                               uint32_t* err, cudaStream_t st);
 
 cudaError_t ls_launch_wait_timeout(uint32_t* err, cudaStream_t stream);
+cudaError_t ls_launch_grpo_logp(const void* logits, bool is_bf16, int64_t T, int V,
+                                const int32_t* targets, const float* ref_logp, float* logp_out,
+                                float* lse_out, float* kl_out, uint32_t* err, int num_sms,
+                                cudaStream_t stream);
 cudaError_t ls_launch_validate_pages(const int32_t* page_table, int32_t num_logical,
                                      int32_t num_pages, uint32_t* seen, uint32_t* err,
                                      cudaStream_t st);

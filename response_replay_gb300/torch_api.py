@@ -171,5 +171,31 @@ def grpo_loss_fwd_bwd(logits: torch.Tensor, targets: torch.Tensor, logp_old: tor
     return loss, dlogits, logp_out, stats
 
 
+def grpo_logp(logits: torch.Tensor, targets: torch.Tensor, ref_logp: torch.Tensor | None = None,
+              with_lse: bool = False, stream=None):
+    """Pre-step scoring: returns (logp[T], lse[T] or None, kl[T] or None)."""
+    T, V = logits.shape
+    if logits.dtype == torch.bfloat16:
+        dt = B.LS_BF16
+    elif logits.dtype == torch.float32:
+        dt = B.LS_FP32
+    else:
+        raise ValueError("logits must be bf16 or fp32")
+    _check(logits, "logits", logits.dtype)
+    _check(targets, "targets", torch.int32, (T,))
+    dev = logits.device
+    logp = torch.empty(T, dtype=torch.float32, device=dev)
+    lse = torch.empty(T, dtype=torch.float32, device=dev) if with_lse else None
+    kl = None
+    if ref_logp is not None:
+        _check(ref_logp, "ref_logp", torch.float32, (T,))
+        kl = torch.empty(T, dtype=torch.float32, device=dev)
+    B.ls_grpo_logp(logits.data_ptr(), dt, T, V, targets.data_ptr(),
+                   ref_logp.data_ptr() if ref_logp is not None else None, logp.data_ptr(),
+                   lse.data_ptr() if lse is not None else None,
+                   kl.data_ptr() if kl is not None else None, _stream(stream))
+    return logp, lse, kl
+
+
 def last_device_error(stream=None) -> int:
     return B.ls_last_device_error(_stream(stream))

@@ -121,3 +121,56 @@ def test_length_mismatch_reported(cuda):
     api.grpo_loss_fwd_bwd(inp.logits, inp.targets, lo, inp.rewards, bad, 0, 2, 0.2, loss=loss)
     assert B.ls_last_device_error(0) == B.LS_ERR_DEVICE_CHECK
     assert loss.item() == 7.0   # nothing written
+
+
+# ---- pre-step scoring (log-softmax gather, KL estimate against a reference policy)
+
+def check_logp(logits, targets, ref=None):
+    zl = host_logits(logits)
+    tg = targets.cpu().numpy()
+    ref_t = None if ref is None else torch.from_numpy(ref.astype(np.float32)).to(logits.device)
+    logp, lse, kl = api.grpo_logp(logits, targets, ref_t, with_lse=True)
+    lse_ref, logp_ref, kl_ref = oracle.grpo_logp(zl, tg, None if ref is None else
+                                                 ref.astype(np.float32).astype(np.float64))
+    assert np.abs(logp.cpu().numpy() - logp_ref).max(initial=0.0) <= TOL_LOGP
+    assert np.abs(lse.cpu().numpy() - lse_ref).max(initial=0.0) <= TOL_LOGP
+    if ref is not None:
+        # kl'(d) = e^d - 1, so an error e in logp moves kl by about |e^d - 1| e
+        d = ref.astype(np.float32).astype(np.float64) - logp_ref
+        tol = TOL_LOGP * np.abs(np.expm1(d)) + 1e-6
+        assert (np.abs(kl.cpu().numpy() - kl_ref) <= tol).all()
+        assert (kl.cpu().numpy() >= -1e-7).all()
+    assert B.ls_last_device_error(0) == B.LS_OK
+
+
+@pytest.mark.parametrize("T,V,dtype", [(9, 37, torch.float32), (128, 4096, torch.float32),
+                                       (64, 1001, torch.bfloat16), (48, 151936, torch.bfloat16),
+                                       (0, 64, torch.float32)])
+def test_grpo_logp_parity(cuda, T, V, dtype):
+    g = torch.Generator(device="cpu").manual_seed(T * 131 + V)
+    logits = (torch.randn(T, V, generator=g) * 2.0).to(dtype).to(cuda)
+    targets = torch.randint(0, V, (T,), generator=g, dtype=torch.int32).to(cuda)
+    check_logp(logits, targets)
+    if T > 0:
+        rng = np.random.default_rng(T + V)
+        lp = oracle.grpo_logp(host_logits(logits), targets.cpu().numpy())[1]
+        ref = lp + rng.choice([0.0, 1e-3, -0.4, 0.9, -2.0], size=T)
+        check_logp(logits, targets, ref)
+
+
+def test_grpo_logp_full_member(cuda):
+    """The 2,097,152-position workload's first member: 4,096 tokens x 151,936 bf16 logits."""
+    w = syn.WORKLOADS["p2m"]
+    inp = syn.make_grpo(list(w.R[:1]), w.vocab, w.logits_dtype, w.rewards, syn.seed_of("p2m"),
+                        cuda, shift_frac=w.shift_frac)
+    lp = oracle.grpo_logp(host_logits(inp.logits), inp.targets.cpu().numpy())[1]
+    check_logp(inp.logits, inp.targets, lp + inp.noise.cpu().numpy())
+
+
+def test_grpo_logp_bad_target_reported(cuda):
+    logits = torch.randn(4, 16, device=cuda)
+    targets = torch.tensor([0, 16, 3, -1], dtype=torch.int32, device=cuda)
+    logp, _, _ = api.grpo_logp(logits, targets)
+    assert B.ls_last_device_error(0) == B.LS_ERR_DEVICE_CHECK
+    lp = logp.cpu().numpy()
+    assert np.isnan(lp[1]) and np.isnan(lp[3]) and np.isfinite(lp[[0, 2]]).all()
