@@ -375,6 +375,9 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     ref_lp = logp_old[s0:s1]
     api.grpo_logp(gin.logits[s0:s1], gin.targets[s0:s1], ref_lp, stream=stream)
     torch.cuda.synchronize()
+    # hold the stream for a few ms so that all K calls are queued before the first
+    # starts: the events then time the kernels, not the host's call overhead
+    torch.cuda._sleep(20_000_000)
     ea, eb = ev(), None
     for _ in range(K):
         api.grpo_logp(gin.logits[s0:s1], gin.targets[s0:s1], ref_lp, stream=stream)

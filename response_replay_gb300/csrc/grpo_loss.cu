@@ -10,17 +10,20 @@
 // Three launches:
 //   grpo_prep   1 block : advantages in fp64 (mean/std about the first reward), member
 //                         token offsets, 1/(G R_i); checks that lengths cover T.
-//   grpo_rows   grid    : one CTA per token row at a time.  Pass 1 streams the row once
-//                         (online max / sum-exp, 16-byte loads) and gathers z_target;
-//                         pass 2 re-reads the row (from L2: the row was just read) and
-//                         writes dlogits, or writes zeros without reading when c_t = 0.
-//                         HBM: V*b read + V*b written per token, the algorithmic floor.
+//   row kernel  grid    : pass 1 reduces a token row (online max / sum-exp) and gathers
+//                         z_target; pass 2 writes dlogits, or zeros without reading the
+//                         row when c_t = 0.  HBM: V*b read + V*b written per token, the
+//                         algorithmic floor (pass 2 re-reads the row from L2).  Two forms:
+//     grpo_stream        one CTA per SM, rows streamed through a shared-memory ring by
+//                        bulk copies; used when a row is a whole number of 16-byte units.
+//     grpo_rows          one CTA per row at a time, plain 16-byte loads; any V.
 //   grpo_final  1 block : fixed-order fp64 reduction of the per-token terms -> loss,
 //                         stats.  No floating-point atomics: results are deterministic.
 #include <float.h>
 
 #include "ls_device.cuh"
 #include "ls_internal.h"
+#include "ls_umma.cuh"
 
 namespace {
 
@@ -278,7 +281,9 @@ __global__ void __launch_bounds__(kRowThreads) grpo_rows(
       for (int i = tail0 + tid; i < V; i += kRowThreads) VT::store1(gr + i, 0.f);
     } else {
       uint4* gv = reinterpret_cast<uint4*>(gr + head);
-      for (int i = tid; i < nvec; i += 4 * kRowThreads) {
+      // last-read chunk first: the end of the row is the likeliest to still be in L2
+      constexpr int kChunk = 4 * kRowThreads;
+      for (int i = (nvec - 1) / kChunk * kChunk + tid; i >= 0; i -= kChunk) {
         uint4 u[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k)
@@ -351,6 +356,344 @@ __global__ void __launch_bounds__(kRowThreads) grpo_logp_rows(
   }
 }
 
+// ---------------------------------------------------------------- streamed row kernel
+// Each CTA streams its token rows through shared memory in chunks of two 16-byte vectors
+// per consumer thread: a producer warp issues 1-D bulk copies into a ring of chunks (about 200 KB in flight per SM, so
+// HBM sees deep queues without holding registers), the consumer warps reduce them, and
+// a scalar warp fetches the next row's target, target logit, old (or
+// reference) log-probability and member weights while the consumers work, so the end
+// of a row waits on no global load.
+//   loss form: pass 1 reduces the row to (max, sum exp2), keeping its last chunks (as
+//              many as the ring holds) in shared memory; pass 2 writes dlogits of those
+//              from shared memory and re-loads only the earlier chunks, most recently
+//              read first (the likeliest to still be in L2), with streaming stores.
+//   scoring form: pass 1 only, then logp / lse / KL.
+// Rows must be 16-byte multiples (V * sizeof(E) % 16 == 0) for the bulk copies; other
+// shapes use the one-CTA-per-row kernels above.
+// Two shapes: the scoring form runs two CTAs per SM (16 consumer warps, 6 x 16 KB each);
+// the loss form runs one CTA per SM (30 consumer warps, 6 x 30 KB), which keeps half as
+// many rows live between a row's two passes, so more of pass 2 is served from L2.
+template <bool kLoss>
+struct StreamCfg {
+  static constexpr int kWarps = kLoss ? 30 : 16;  // consumer warps
+  static constexpr int kConsumers = kWarps * 32;
+  static constexpr int kThreads = kConsumers + 64;  // + producer warp + scalar warp
+  static constexpr uint32_t kChunkBytes = kConsumers * 32;  // two 16-byte vectors a thread
+  static constexpr int kStages = kLoss ? 6 : 6;
+  static constexpr int kCtasPerSm = kLoss ? 1 : 2;
+  static_assert(kThreads <= 1024, "one CTA holds at most 1024 threads");
+  static_assert(kStages * kChunkBytes <= 200 * 1024, "ring too large");
+};
+
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t mbar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(dst), "l"(src), "r"(bytes), "r"(mbar)
+      : "memory");
+}
+template <int kCount>
+__device__ __forceinline__ void consumers_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kCount) : "memory");
+}
+
+struct RowScalars {
+  double adv, inv;  // member advantage and 1 / (G R_i) (loss form)
+  float aux;        // old log-probability (loss form) or reference log-probability
+  float zt;         // target logit
+  int32_t y, pad;
+};
+
+struct StreamSmem {
+  uint32_t full, empty, info_full, info_empty, red, bc, info, abort, total;
+};
+__host__ __device__ constexpr StreamSmem stream_smem(int stages, uint32_t chunk_bytes, int warps) {
+  StreamSmem l{};
+  uint32_t p = (uint32_t)stages * chunk_bytes;
+  l.full = p;        p += stages * 8;
+  l.empty = p;       p += stages * 8;
+  l.info_full = p;   p += 2 * 8;
+  l.info_empty = p;  p += 2 * 8;
+  l.red = p;         p += 2 * warps * 8;          // [row parity][warp] (max, sum)
+  l.bc = p;          p += 16;                     // c, lse2, target of the current row
+  l.info = p;        p += 2 * (uint32_t)sizeof(RowScalars);
+  l.abort = p;       p += 16;
+  l.total = p;
+  return l;
+}
+
+struct StreamArgs {
+  const void* logits;
+  int64_t T;
+  int V;
+  const int32_t* targets;
+  const float* aux;  // logp_old (loss form), ref_logp or null (scoring form)
+  // loss form
+  int G, mb, me;
+  float eps;
+  void* dlogits;
+  void* ws;
+  // both: per-row log-probability output (optional in the loss form)
+  float* logp_out;
+  // scoring form
+  float* lse_out;
+  float* kl_out;
+  uint32_t* err;
+};
+
+template <typename E, bool kLoss>
+__global__ void __launch_bounds__(StreamCfg<kLoss>::kThreads, StreamCfg<kLoss>::kCtasPerSm)
+    grpo_stream(const StreamArgs p) {
+  using VT = Vec<E>;
+  using Cfg = StreamCfg<kLoss>;
+  constexpr int NV = VT::N;
+  constexpr int kStages = Cfg::kStages;
+  constexpr int kStreamWarps = Cfg::kWarps;
+  constexpr int kCons = Cfg::kConsumers;
+  constexpr uint32_t kChunkBytes = Cfg::kChunkBytes;
+  constexpr uint32_t kChunkElems = kChunkBytes / sizeof(E);
+  extern __shared__ __align__(1024) uint8_t smem[];
+  constexpr StreamSmem L = stream_smem(kStages, kChunkBytes, kStreamWarps);
+  const int64_t T = p.T;
+  const int V = p.V;
+  double* term_out = nullptr;
+  float* rho_out = nullptr;
+  float* zeroed_out = nullptr;
+  const double* adv_ws = nullptr;
+  const double* inv_ws = nullptr;
+  const int64_t* off = nullptr;
+  if constexpr (kLoss) {
+    const WsLayout w = ws_layout(T, p.G);
+    if (*at<int32_t>(p.ws, w.flag) == 0) return;  // the same for every CTA
+    adv_ws = at<double>(p.ws, w.adv);
+    inv_ws = at<double>(p.ws, w.inv_norm);
+    off = at<int64_t>(p.ws, w.off);
+    term_out = at<double>(p.ws, w.term);
+    rho_out = at<float>(p.ws, w.rho);
+    zeroed_out = at<float>(p.ws, w.zeroed);
+  }
+  const E* logits = static_cast<const E*>(p.logits);
+  const uint32_t row_bytes = (uint32_t)V * sizeof(E);
+  const int nch = (int)((row_bytes + kChunkBytes - 1) / kChunkBytes);
+  constexpr int npass = kLoss ? 2 : 1;
+  // loss form: the last `held` chunks of pass 1 stay in the ring for pass 2
+  const int held = kLoss ? (nch < kStages ? nch : kStages) : 0;
+  const uint32_t full0 = smem_u32(smem + L.full), empty0 = smem_u32(smem + L.empty);
+  const uint32_t ifull0 = smem_u32(smem + L.info_full), iempty0 = smem_u32(smem + L.info_empty);
+  MS* red = reinterpret_cast<MS*>(smem + L.red);
+  float* bc = reinterpret_cast<float*>(smem + L.bc);
+  RowScalars* info = reinterpret_cast<RowScalars*>(smem + L.info);
+  volatile int* abort = reinterpret_cast<volatile int*>(smem + L.abort);
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  // a wait that gives up records the error and stops every later wait of the CTA
+  auto wait = [&](uint32_t bar, uint32_t parity) {
+    if (*abort) return false;
+    if (umma::mbar_wait(bar, parity)) return true;
+    ls_report(p.err, LS_DEVERR_TIMEOUT);
+    *abort = 1;
+    return false;
+  };
+
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      umma::mbar_init(full0 + 8 * s, 1);
+      umma::mbar_init(empty0 + 8 * s, kStreamWarps);
+    }
+    for (int s = 0; s < 2; ++s) {
+      umma::mbar_init(ifull0 + 8 * s, 1);
+      umma::mbar_init(iempty0 + 8 * s, 1);
+    }
+    *abort = 0;
+    umma::fence_barrier_init();
+  }
+  __syncthreads();
+
+  if (wid == kStreamWarps) {
+    // ---- producer: the chunk sequence of every row (pass 1 forward, pass 2 reversed)
+    if (lane == 0) {
+      umma::RingPos<kStages> rp;
+      int issued = 0;
+      for (int64_t row = blockIdx.x; row < T && !*abort; row += gridDim.x) {
+        const uint8_t* src = reinterpret_cast<const uint8_t*>(logits + row * (int64_t)V);
+        for (int ps = 0; ps < npass; ++ps) {
+          // pass 2 re-loads only the chunks that are no longer held in the ring
+          const int n = ps == 0 ? nch : nch - held;
+          for (int k = 0; k < n; ++k) {
+            const int c = ps == 0 ? k : n - 1 - k;
+            const uint32_t off_b = (uint32_t)c * kChunkBytes;
+            const uint32_t bytes = row_bytes - off_b < kChunkBytes ? row_bytes - off_b : kChunkBytes;
+            if (!wait(empty0 + 8 * rp.stage, rp.phase ^ 1u)) break;
+            umma::mbar_expect_tx(full0 + 8 * rp.stage, bytes);
+            bulk_load(smem_u32(smem + rp.stage * kChunkBytes), src + off_b, bytes,
+                      full0 + 8 * rp.stage);
+            ++issued;
+            rp.advance();
+          }
+        }
+      }
+      // no copy may still be landing when the CTA exits: wait for the last fill of each
+      // stage (already complete unless a wait above gave up)
+      for (int s = 0; s < kStages && s < issued; ++s) {
+        rp.stage = rp.stage == 0 ? kStages - 1 : rp.stage - 1;
+        if (rp.stage == kStages - 1) rp.phase ^= 1u;
+        umma::mbar_wait(full0 + 8 * rp.stage, rp.phase);
+      }
+    }
+    return;
+  }
+  if (wid == kStreamWarps + 1) {
+    // ---- scalar warp: per-row scalars one row ahead of the consumers
+    if (lane == 0) {
+      int q = 0;
+      for (int64_t row = blockIdx.x; row < T; row += gridDim.x, ++q) {
+        const int b = q & 1;
+        if (!wait(iempty0 + 8 * b, (((uint32_t)q >> 1) & 1u) ^ 1u)) break;
+        RowScalars r;
+        r.y = p.targets[row];
+        r.zt = (uint32_t)r.y < (uint32_t)V ? VT::load1(logits + row * (int64_t)V + r.y) : 0.f;
+        r.aux = p.aux ? p.aux[row] : 0.f;
+        r.adv = 0.0;
+        r.inv = 0.0;
+        if constexpr (kLoss) {
+          int lo_m = 0, hi_m = p.me - p.mb - 1;  // member of this token
+          while (lo_m < hi_m) {
+            const int mid = (lo_m + hi_m + 1) >> 1;
+            if (off[mid] <= row) lo_m = mid; else hi_m = mid - 1;
+          }
+          r.adv = adv_ws[p.mb + lo_m];
+          r.inv = inv_ws[p.mb + lo_m];
+        }
+        info[b] = r;
+        umma::mbar_arrive(ifull0 + 8 * b);
+      }
+    }
+    return;
+  }
+
+  // ---- consumers
+  umma::RingPos<kStages> rp;
+  int q = 0;
+  for (int64_t row = blockIdx.x; row < T; row += gridDim.x, ++q) {
+    MS ms = {-INFINITY, 0.f};
+    const uint32_t s0 = rp.stage;  // stage of chunk 0; chunk k sits in (s0 + k) % kStages
+    for (int k = 0; k < nch; ++k) {
+      const uint32_t bytes =
+          row_bytes - k * kChunkBytes < kChunkBytes ? row_bytes - k * kChunkBytes : kChunkBytes;
+      const int nvec = (int)(bytes / 16);
+      if (wait(full0 + 8 * rp.stage, rp.phase)) {
+        const uint4* sv = reinterpret_cast<const uint4*>(smem + rp.stage * kChunkBytes);
+        for (int i = tid; i < nvec; i += kCons) {
+          float x[NV];
+          VT::unpack(sv[i], x);
+#pragma unroll
+          for (int e = 0; e < NV; ++e) x[e] *= kLog2e;
+          ms_add(ms, x, NV);
+        }
+      }
+      __syncwarp();
+      if (lane == 0 && k < nch - held) umma::mbar_arrive(empty0 + 8 * rp.stage);
+      rp.advance();
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      MS other = {__shfl_xor_sync(0xffffffffu, ms.m, o), __shfl_xor_sync(0xffffffffu, ms.s, o)};
+      ms = ms_merge(ms, other);
+    }
+    MS* rq = red + (q & 1) * kStreamWarps;
+    if (lane == 0) rq[wid] = ms;
+    consumers_sync<kCons>();
+    if (wid == 0) {
+      MS a = lane < kStreamWarps ? rq[lane] : MS{-INFINITY, 0.f};
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        MS other = {__shfl_xor_sync(0xffffffffu, a.m, o), __shfl_xor_sync(0xffffffffu, a.s, o)};
+        a = ms_merge(a, other);
+      }
+      if (lane == 0) {
+        const int b = q & 1;
+        const float lse2 = a.m + log2f(a.s);
+        wait(ifull0 + 8 * b, ((uint32_t)q >> 1) & 1u);
+        const RowScalars r = info[b];
+        umma::mbar_arrive(iempty0 + 8 * b);
+        const bool valid = (uint32_t)r.y < (uint32_t)V;
+        if (!valid) ls_report(p.err, LS_DEVERR_CHECK);
+        const float logp = valid ? r.zt - lse2 * kLn2 : NAN;
+        if constexpr (kLoss) {
+          float c = 0.f;
+          double term = 0.0;
+          float rho = 0.f, zeroed = 0.f;
+          if (valid) {
+            rho = expf(logp - r.aux);
+            const float A = (float)r.adv;
+            const float clipped = fminf(fmaxf(rho, 1.f - p.eps), 1.f + p.eps);
+            const bool active = rho * A <= clipped * A;  // ties: the unclipped branch
+            term = (double)(active ? rho : clipped) * r.adv;
+            c = active ? (float)(-r.adv * (double)rho * r.inv) : 0.f;
+            zeroed = (!active && A != 0.f) ? 1.f : 0.f;
+          }
+          term_out[row] = term;
+          rho_out[row] = rho;
+          zeroed_out[row] = zeroed;
+          if (p.logp_out) p.logp_out[row] = logp;
+          bc[0] = c;
+          bc[1] = lse2;
+          bc[2] = __int_as_float(r.y);
+        } else {
+          p.logp_out[row] = logp;
+          if (p.lse_out) p.lse_out[row] = lse2 * kLn2;
+          if (p.kl_out) {
+            const float d = r.aux - logp;
+            p.kl_out[row] = expm1f(d) - d;
+          }
+        }
+      }
+    }
+    if constexpr (kLoss) {
+      consumers_sync<kCons>();
+      const float c = bc[0], lse2 = bc[1];
+      const int y = __float_as_int(bc[2]);
+      E* gr = static_cast<E*>(p.dlogits) + row * (int64_t)V;
+      // dlogits of chunk ch from ring stage st (whose fill has landed), then release it
+      auto p2_chunk = [&](uint32_t st, int ch, bool ok) {
+        const uint32_t off_b = (uint32_t)ch * kChunkBytes;
+        const uint32_t bytes = row_bytes - off_b < kChunkBytes ? row_bytes - off_b : kChunkBytes;
+        const int nvec = (int)(bytes / 16);
+        uint4* gv = reinterpret_cast<uint4*>(gr + (size_t)ch * kChunkElems);
+        if (c == 0.f) {
+          const uint4 zero = make_uint4(0, 0, 0, 0);
+          for (int i = tid; i < nvec; i += kCons) __stcs(gv + i, zero);
+        } else if (ok) {
+          const uint4* sv = reinterpret_cast<const uint4*>(smem + st * kChunkBytes);
+          const int ty = y - ch * (int)kChunkElems;
+          for (int i = tid; i < nvec; i += kCons) {
+            float x[NV];
+            VT::unpack(sv[i], x);
+#pragma unroll
+            for (int e = 0; e < NV; ++e) {
+              x[e] = -c * fast_exp2(fmaf(x[e], kLog2e, -lse2));
+              if (i * NV + e == ty) x[e] += c;
+            }
+            __stcs(gv + i, VT::pack(x));
+          }
+        }
+        __syncwarp();
+        if (lane == 0) umma::mbar_arrive(empty0 + 8 * st);
+      };
+      // the held chunks first, oldest first (the producer refills their stages in that
+      // order), then the re-loaded ones, most recently read first (likeliest in L2)
+      for (int j = 0; j < held; ++j) {
+        const int ch = nch - held + j;
+        p2_chunk((s0 + (uint32_t)ch) % kStages, ch, true);
+      }
+      for (int k = 0; k < nch - held; ++k) {
+        const bool ok = wait(full0 + 8 * rp.stage, rp.phase);
+        p2_chunk(rp.stage, nch - held - 1 - k, ok);
+        rp.advance();
+      }
+    }
+  }
+}
+
 __global__ void __launch_bounds__(1024) grpo_final(int64_t T, int G, int mb, int me,
                                                    int accumulate, float* loss, float* stats,
                                                    void* ws) {
@@ -406,13 +749,66 @@ __global__ void __launch_bounds__(1024) grpo_final(int64_t T, int G, int mb, int
 
 size_t ls_grpo_ws_bytes(int64_t T, int G) { return ws_layout(T, G).total; }
 
+namespace {
+// The streamed kernels apply when rows are whole 16-byte multiples (the bulk copies'
+// granularity; the entry points have already checked the buffers' alignment, re-checked
+// here).  Returns false (nothing launched) otherwise; *e is the launch status when it
+// returns true.
+template <bool kLoss>
+bool launch_stream(const StreamArgs& sa, bool is_bf16, int num_sms, cudaStream_t st,
+                   cudaError_t* e) {
+  const int esz = is_bf16 ? 2 : 4;
+  if (((int64_t)sa.V * esz) % 16 != 0 || (reinterpret_cast<uintptr_t>(sa.logits) & 15) ||
+      (kLoss && (reinterpret_cast<uintptr_t>(sa.dlogits) & 15)))
+    return false;
+  using Cfg = StreamCfg<kLoss>;
+  constexpr uint32_t smem = stream_smem(Cfg::kStages, Cfg::kChunkBytes, Cfg::kWarps).total;
+  const void* fn = is_bf16 ? (const void*)grpo_stream<__nv_bfloat16, kLoss>
+                           : (const void*)grpo_stream<float, kLoss>;
+  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+      cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  const int64_t ctas = (int64_t)num_sms * Cfg::kCtasPerSm;
+  const int64_t grid = sa.T < ctas ? sa.T : ctas;
+  if (is_bf16)
+    grpo_stream<__nv_bfloat16, kLoss><<<(unsigned)grid, Cfg::kThreads, smem, st>>>(sa);
+  else
+    grpo_stream<float, kLoss><<<(unsigned)grid, Cfg::kThreads, smem, st>>>(sa);
+  ls_note_launch();
+  *e = cudaGetLastError();
+  return true;
+}
+
+StreamArgs loss_stream_args(const LsGrpoArgs& a) {
+  StreamArgs sa{};
+  sa.logits = a.logits;
+  sa.T = a.T;
+  sa.V = a.V;
+  sa.targets = a.targets;
+  sa.aux = a.logp_old;
+  sa.G = a.G;
+  sa.mb = a.member_begin;
+  sa.me = a.member_end;
+  sa.eps = a.eps;
+  sa.dlogits = a.dlogits;
+  sa.ws = a.workspace;
+  sa.logp_out = a.logp_out;
+  sa.err = a.err;
+  return sa;
+}
+}  // namespace
+
 cudaError_t ls_launch_grpo(const LsGrpoArgs& a, int num_sms, cudaStream_t st) {
   grpo_prep<<<1, 32, 0, st>>>(a.rewards, a.resp_lens, a.G, a.member_begin, a.member_end,
                               a.std_ddof, a.adv_eps, a.T, a.workspace, a.err);
   ls_note_launch();
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  if (a.T > 0) {
+  if (a.T > 0 && launch_stream<true>(loss_stream_args(a), a.is_bf16, num_sms, st, &e)) {
+    if (e != cudaSuccess) return e;
+  } else if (a.T > 0) {
     int64_t grid = (int64_t)num_sms * 2;
     if (grid > a.T) grid = a.T;
     if (a.is_bf16) {
@@ -442,6 +838,18 @@ cudaError_t ls_launch_grpo_logp(const void* logits, bool is_bf16, int64_t T, int
                                 float* lse_out, float* kl_out, uint32_t* err, int num_sms,
                                 cudaStream_t st) {
   if (T <= 0) return cudaSuccess;
+  StreamArgs sa{};
+  sa.logits = logits;
+  sa.T = T;
+  sa.V = V;
+  sa.targets = targets;
+  sa.aux = ref_logp;
+  sa.logp_out = logp_out;
+  sa.lse_out = lse_out;
+  sa.kl_out = kl_out;
+  sa.err = err;
+  cudaError_t e = cudaSuccess;
+  if (launch_stream<false>(sa, is_bf16, num_sms, st, &e)) return e;
   int64_t grid = (int64_t)num_sms * 2;
   if (grid > T) grid = T;
   if (is_bf16) {

@@ -68,12 +68,43 @@ def test_small_workload(cuda):
         check(inp, 0.2, 0, w.G, "fp32")
 
 
-@pytest.mark.parametrize("V,dtype", [(151936, "bf16"), (1001, "bf16"), (1001, "fp32"),
-                                     (7, "fp32"), (33, "bf16")])
+# Rows that are whole 16-byte units take the streamed kernel (bulk copies through a
+# shared-memory ring of 30 KB chunks, the last six chunks of a row held for pass 2):
+# 151,936 bf16 = 10 chunks (4 re-loaded), fp32 = 20 chunks, 92,160 bf16 = exactly the six
+# held chunks, 107,512 bf16 = seven chunks with a ragged last one, 16 / 8 = one short
+# chunk.  Other V (1001, 7, 33) take the one-CTA-per-row kernel.
+@pytest.mark.parametrize("V,dtype", [(151936, "bf16"), (151936, "fp32"), (1001, "bf16"),
+                                     (1001, "fp32"), (7, "fp32"), (33, "bf16"), (16, "bf16"),
+                                     (8, "fp32"), (4104, "bf16"), (92160, "bf16"),
+                                     (107512, "bf16")])
 def test_vocab_sizes_and_alignment(cuda, V, dtype):
     lens = [5, 9, 3]
     inp = syn.make_grpo(lens, V, dtype, "normal", 100 + V, cuda, shift_frac=0.3)
     check(inp, 0.2, 0, 3, dtype)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+def test_unaligned_logits_buffer_rejected(cuda, dtype):
+    """Device pointers must be 16-byte aligned: a logits view at an odd element offset is
+    refused before any launch."""
+    lens = [3, 4]
+    V = 64
+    inp = syn.make_grpo(lens, V, dtype, "normal", 211, cuda)
+    buf = torch.empty(sum(lens) * V + 1, dtype=inp.logits.dtype, device=cuda)
+    buf[1:].copy_(inp.logits.flatten())
+    logits = buf[1:].view(sum(lens), V)
+    assert logits.data_ptr() % 16 != 0
+    lo = torch.zeros(sum(lens), dtype=torch.float32, device=cuda)
+    with pytest.raises(B.LongstrawError):
+        api.grpo_loss_fwd_bwd(logits, inp.targets, lo, inp.rewards, inp.resp_lens, 0, 2, 0.2)
+
+
+def test_many_rows_per_cta(cuda):
+    """T much larger than the number of CTAs: every ring stage is refilled many times and
+    the held chunks of one row give way to the next row's."""
+    lens = [700, 1100, 300, 948]
+    inp = syn.make_grpo(lens, 40960, "bf16", "normal", 223, cuda, shift_frac=0.3)
+    check(inp, 0.2, 0, 4, "bf16")
 
 
 def test_serial_member_calls_accumulate(cuda):
@@ -145,7 +176,8 @@ def check_logp(logits, targets, ref=None):
 
 @pytest.mark.parametrize("T,V,dtype", [(9, 37, torch.float32), (128, 4096, torch.float32),
                                        (64, 1001, torch.bfloat16), (48, 151936, torch.bfloat16),
-                                       (0, 64, torch.float32)])
+                                       (0, 64, torch.float32), (700, 12296, torch.bfloat16),
+                                       (700, 12288, torch.float32)])
 def test_grpo_logp_parity(cuda, T, V, dtype):
     g = torch.Generator(device="cpu").manual_seed(T * 131 + V)
     logits = (torch.randn(T, V, generator=g) * 2.0).to(dtype).to(cuda)
