@@ -397,6 +397,61 @@ __device__ __forceinline__ void consumers_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(kCount) : "memory");
 }
 
+// One thread's online (max, sum exp) over raw logits, for the streamed kernels: the max
+// with three-operand max instructions, the exponent arguments x log2e - m log2e as one
+// packed f32x2 FMA per pair and the sum in two lanes added with packed f32x2 adds.
+struct OnlineMS {
+  float m = -INFINITY;
+  float2 s = {0.f, 0.f};
+  template <int N>
+  __device__ __forceinline__ void add(const float* x) {
+    static_assert(N == 4 || N == 8, "a 16-byte vector of fp32 or bf16");
+    float mx;
+    if constexpr (N == 8)
+      mx = fmax3(fmax3(x[0], x[1], x[2]), fmax3(x[3], x[4], x[5]), fmaxf(x[6], x[7]));
+    else
+      mx = fmaxf(fmax3(x[0], x[1], x[2]), x[3]);
+    if (mx > m) {
+      const float r = fast_exp2((m - mx) * kLog2e);
+      s.x *= r;
+      s.y *= r;
+      m = mx;
+    }
+    if (m == -INFINITY) return;  // only -inf logits so far: they add nothing
+    const float2 l2 = make_float2(kLog2e, kLog2e);
+    const float nm = -m * kLog2e;
+    const float2 b = make_float2(nm, nm);
+#pragma unroll
+    for (int i = 0; i < N; i += 2) {
+      const float2 t = __ffma2_rn(make_float2(x[i], x[i + 1]), l2, b);
+      s = __fadd2_rn(s, make_float2(fast_exp2(t.x), fast_exp2(t.y)));
+    }
+  }
+  // the pair in the log2 domain of MS
+  __device__ __forceinline__ MS log2_pair() const { return {m * kLog2e, s.x + s.y}; }
+};
+
+// dlogits of one 16-byte vector: x <- -c exp2(x log2e - lse2), plus c at lane tl when
+// tl >= 0 (the target), with packed f32x2 FMA / multiply.
+template <int N>
+__device__ __forceinline__ void dlogit_vec(float* x, float c, float lse2, int tl) {
+  const float2 l2 = make_float2(kLog2e, kLog2e);
+  const float2 b = make_float2(-lse2, -lse2);
+  const float2 nc = make_float2(-c, -c);
+#pragma unroll
+  for (int i = 0; i < N; i += 2) {
+    const float2 t = __ffma2_rn(make_float2(x[i], x[i + 1]), l2, b);
+    const float2 g = __fmul2_rn(make_float2(fast_exp2(t.x), fast_exp2(t.y)), nc);
+    x[i] = g.x;
+    x[i + 1] = g.y;
+  }
+  if (tl >= 0) {
+#pragma unroll
+    for (int e = 0; e < N; ++e)
+      if (e == tl) x[e] += c;
+  }
+}
+
 struct RowScalars {
   double adv, inv;  // member advantage and 1 / (G R_i) (loss form)
   float aux;        // old log-probability (loss form) or reference log-probability
@@ -574,7 +629,7 @@ __global__ void __launch_bounds__(StreamCfg<kLoss>::kThreads, StreamCfg<kLoss>::
   umma::RingPos<kStages> rp;
   int q = 0;
   for (int64_t row = blockIdx.x; row < T; row += gridDim.x, ++q) {
-    MS ms = {-INFINITY, 0.f};
+    OnlineMS oms;
     const uint32_t s0 = rp.stage;  // stage of chunk 0; chunk k sits in (s0 + k) % kStages
     for (int k = 0; k < nch; ++k) {
       const uint32_t bytes =
@@ -585,15 +640,14 @@ __global__ void __launch_bounds__(StreamCfg<kLoss>::kThreads, StreamCfg<kLoss>::
         for (int i = tid; i < nvec; i += kCons) {
           float x[NV];
           VT::unpack(sv[i], x);
-#pragma unroll
-          for (int e = 0; e < NV; ++e) x[e] *= kLog2e;
-          ms_add(ms, x, NV);
+          oms.add<NV>(x);
         }
       }
       __syncwarp();
       if (lane == 0 && k < nch - held) umma::mbar_arrive(empty0 + 8 * rp.stage);
       rp.advance();
     }
+    MS ms = oms.log2_pair();
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       MS other = {__shfl_xor_sync(0xffffffffu, ms.m, o), __shfl_xor_sync(0xffffffffu, ms.s, o)};
@@ -664,15 +718,11 @@ __global__ void __launch_bounds__(StreamCfg<kLoss>::kThreads, StreamCfg<kLoss>::
           for (int i = tid; i < nvec; i += kCons) __stcs(gv + i, zero);
         } else if (ok) {
           const uint4* sv = reinterpret_cast<const uint4*>(smem + st * kChunkBytes);
-          const int ty = y - ch * (int)kChunkElems;
+          const int ty = y - ch * (int)kChunkElems;  // target's element within the chunk
           for (int i = tid; i < nvec; i += kCons) {
             float x[NV];
             VT::unpack(sv[i], x);
-#pragma unroll
-            for (int e = 0; e < NV; ++e) {
-              x[e] = -c * fast_exp2(fmaf(x[e], kLog2e, -lse2));
-              if (i * NV + e == ty) x[e] += c;
-            }
+            dlogit_vec<NV>(x, c, lse2, ty >= i * NV && ty < i * NV + NV ? ty - i * NV : -1);
             __stcs(gv + i, VT::pack(x));
           }
         }
