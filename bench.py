@@ -230,27 +230,33 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         e.record(stream)
         return e
 
+    def member(i, m=None, before_loss=None):
+        """One member's replay: forward, GRPO loss (accumulating), backward."""
+        br = branches[i]
+        api.replay_fwd(cache, br.q, br.k, br.v, scale, w.num_splits, o=o, lse=lse, stream=stream)
+        if m is not None:
+            m.append(ev())
+        if before_loss is not None:
+            before_loss()
+        s, e = off[i], off[i + 1]
+        api.grpo_loss_fwd_bwd(gin.logits[s:e], gin.targets[s:e], logp_old[s:e], gin.rewards,
+                              gin.resp_lens, i, i + 1, 0.2, loss=loss, accumulate=i > 0,
+                              dlogits=dlog[: e - s], logp_out=lp_out[s:e], stats=stats,
+                              stream=stream)
+        if m is not None:
+            m.append(ev())
+        api.replay_bwd(cache, br.q, br.k, br.v, o, lse, br.d_o, scale, w.num_splits, dq=dq,
+                       dk=dk, dv=dv, accumulate=i > 0, stream=stream)
+        if m is not None:
+            m.append(ev())
+
     def step(marks=None):
         m = [ev()] if marks is not None else None
         cache.capture(pr.k, pr.v, 0, stream)
         if m is not None:
             m.append(ev())
         for i in range(G):
-            br = branches[i]
-            api.replay_fwd(cache, br.q, br.k, br.v, scale, w.num_splits, o=o, lse=lse, stream=stream)
-            if m is not None:
-                m.append(ev())
-            s, e = off[i], off[i + 1]
-            api.grpo_loss_fwd_bwd(gin.logits[s:e], gin.targets[s:e], logp_old[s:e], gin.rewards,
-                                  gin.resp_lens, i, i + 1, 0.2, loss=loss, accumulate=i > 0,
-                                  dlogits=dlog[: e - s], logp_out=lp_out[s:e], stats=stats,
-                                  stream=stream)
-            if m is not None:
-                m.append(ev())
-            api.replay_bwd(cache, br.q, br.k, br.v, o, lse, br.d_o, scale, w.num_splits, dq=dq,
-                           dk=dk, dv=dv, accumulate=i > 0, stream=stream)
-            if m is not None:
-                m.append(ev())
+            member(i, m)
         return m
 
     # kernel launches of one step, as counted by the library itself
@@ -340,18 +346,67 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                    host["rewards"], host["lens"]] + [x for b in host["br"] for x in b])
         d2h = 4
 
+        # The step's inputs arrive on two copy streams (prompt K on one and V on the other
+        # in page-aligned chunks, then each member's tensors alternating), each piece
+        # marked by an event; the compute stream waits for exactly the pieces its next call
+        # reads, so the prompt is captured chunk by chunk as it lands and a member's
+        # logits arrive while earlier members' attention runs.  A step's copies start only
+        # after the previous step's work is done (no cross-step prefetch).
+        copy_streams = [torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)]
+        n_chunks = 8
+        P = pr.k.shape[0]
+        unit = w.page_size
+        bounds = [(P // unit) * c // n_chunks * unit for c in range(n_chunks)] + [P]
+
+        def mark(st):
+            e = torch.cuda.Event()
+            e.record(st)
+            return e
+
         def e2e_step():
-            pr.k.copy_(host["k"], non_blocking=True)
-            pr.v.copy_(host["v"], non_blocking=True)
-            for b, hb in zip(branches, host["br"]):
-                for dst, src in zip((b.q, b.k, b.v, b.d_o), hb):
-                    dst.copy_(src, non_blocking=True)
-            gin.logits.copy_(host["logits"], non_blocking=True)
-            gin.targets.copy_(host["targets"], non_blocking=True)
-            logp_old.copy_(host["logp_old"], non_blocking=True)
-            gin.rewards.copy_(host["rewards"], non_blocking=True)
-            gin.resp_lens.copy_(host["lens"], non_blocking=True)
-            step()
+            prev = mark(stream)
+            for cs in copy_streams:
+                cs.wait_event(prev)
+            cs0, cs1 = copy_streams
+            with torch.cuda.stream(cs0):
+                gin.rewards.copy_(host["rewards"], non_blocking=True)
+                gin.resp_lens.copy_(host["lens"], non_blocking=True)
+            kv_ev = []
+            for c in range(n_chunks):
+                s, e = bounds[c], bounds[c + 1]
+                with torch.cuda.stream(cs0):
+                    pr.k[s:e].copy_(host["k"][s:e], non_blocking=True)
+                with torch.cuda.stream(cs1):
+                    pr.v[s:e].copy_(host["v"][s:e], non_blocking=True)
+                kv_ev.append((mark(cs0), mark(cs1)))
+            br_ev, lg_ev = [], []
+            for i, (b, hb) in enumerate(zip(branches, host["br"])):
+                with torch.cuda.stream(copy_streams[i % 2]):
+                    for dst, src in zip((b.q, b.k, b.v, b.d_o), hb):
+                        dst.copy_(src, non_blocking=True)
+                br_ev.append(mark(copy_streams[i % 2]))
+                # the member's logits rows, half on each copy stream
+                s, e = off[i], off[i + 1]
+                mid = (s + e) // 2
+                evs = []
+                for cs, (a0, a1) in zip(copy_streams, ((s, mid), (mid, e))):
+                    with torch.cuda.stream(cs):
+                        gin.logits[a0:a1].copy_(host["logits"][a0:a1], non_blocking=True)
+                        gin.targets[a0:a1].copy_(host["targets"][a0:a1], non_blocking=True)
+                        logp_old[a0:a1].copy_(host["logp_old"][a0:a1], non_blocking=True)
+                    evs.append(mark(cs))
+                lg_ev.append(evs)
+            for c in range(n_chunks):
+                stream.wait_event(kv_ev[c][0])
+                stream.wait_event(kv_ev[c][1])
+                s, e = bounds[c], bounds[c + 1]
+                cache.capture(pr.k[s:e], pr.v[s:e], s, stream)
+            for i in range(G):
+                # the forward reads only the member's q / k / v / dO (and the captured
+                # prompt); the loss also waits for its logits rows, whose events follow
+                # the rewards and lengths copied first on copy stream 0
+                stream.wait_event(br_ev[i])
+                member(i, before_loss=lambda i=i: [stream.wait_event(e) for e in lg_ev[i]])
             loss_h.copy_(loss, non_blocking=True)
 
         e2e_step()
