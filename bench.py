@@ -444,6 +444,41 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     comps["grpo_logp_hbm_frac"] = (s1 - s0) * tok_bytes / (sc_ms * 1e-3) / 1e9 / pk.get(
         "hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
 
+    # ---- pre-step scoring, attention half: the forward of G short responses over the
+    # captured prompt, one batched launch (the members' tokens packed into shared tiles)
+    # against G one-member launches.  Short responses are HBM-bound one by one; batched,
+    # each prompt K/V tile serves every member's rows of its KV head at once.
+    for Rs in (2, 16):
+        sbr = [syn.make_branch(Rs, w.hq, w.hkv, D, seed + 101 + i, dev) for i in range(w.G)]
+        sq = torch.stack([b.q for b in sbr]).contiguous()
+        sk = torch.stack([b.k for b in sbr]).contiguous()
+        sv = torch.stack([b.v for b in sbr]).contiguous()
+        so = torch.empty_like(sq)
+        slse = torch.empty(sq.shape[:3], dtype=torch.float32, device=dev)
+
+        def scoring_batched():
+            api.replay_fwd_members(cache, sq, sk, sv, scale, w.num_splits, o=so, lse=slse,
+                                   stream=stream)
+
+        def scoring_serial():
+            for i in range(w.G):
+                api.replay_fwd(cache, sq[i], sk[i], sv[i], scale, w.num_splits, o=so[i],
+                               lse=slse[i], stream=stream)
+
+        for name, fn in (("batched", scoring_batched), ("serial", scoring_serial)):
+            fn()
+            torch.cuda.synchronize()
+            torch.cuda._sleep(20_000_000)  # queue the K calls before the first starts
+            ea = ev()
+            for _ in range(K):
+                fn()
+            eb = ev()
+            torch.cuda.synchronize()
+            comps[f"prestep_fwd_{w.G}x{Rs}_{name}_ms"] = ea.elapsed_time(eb) / K
+        comps[f"prestep_fwd_{w.G}x{Rs}_batched_kv_hbm_frac"] = kv_bytes / (
+            comps[f"prestep_fwd_{w.G}x{Rs}_batched_ms"] * 1e-3) / 1e9 / pk.get(
+            "hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+
     # ---- CPU baseline: the oracle on a bounded sample of the same workload
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -121,6 +121,32 @@ ls_status ls_replay_attn_fwd(const ls_kv_cache* cache, const void* q, const void
                              int num_splits, void* o, float* lse, void* workspace,
                              size_t workspace_bytes, ls_stream_t stream);
 
+/* ls_replay_attn_fwd_members: the same forward for `members` responses of equal length
+ * R over the same captured prompt, in one launch.  Pre-step scoring runs every member
+ * of a group forward-only before the step (explainer, "Serial replay makes G a
+ * schedule": the response branches share the read-only prompt state); batching them
+ * lets the members' rows that share a KV head walk each prompt K/V tile together, so
+ * the prompt streams from HBM about once for all of them instead of once per member.
+ * Member m's rows see the whole prompt and member m's own response keys (j <= t)
+ * only; its result equals ls_replay_attn_fwd on member m's slices (up to rounding).
+ * q: bf16 [members][R][Hq][128]; k_resp, v_resp: bf16 [members][R][num_kv_heads][128];
+ * o: bf16 [members][R][Hq][128]; lse: fp32 [members][R][Hq].  Short responses (the
+ * grouped-query-packed regime) pack the members' tokens into shared 128-row tiles, so
+ * one K/V tile serves members x g x R rows; there a member's rows also meet the other
+ * members' response keys, masked to zero weight, so inputs must be finite (a non-finite
+ * value times a zero weight is not zero; the one-response call has the same property
+ * for the causally masked keys of its own response).  members >= 0 (0 or R == 0 is a
+ * no-op); LS_ERR_UNSUPPORTED when members x R or the work-unit count exceeds 2^30.
+ * Other arguments and errors as ls_replay_attn_fwd; ls_replay_attn_fwd is this call
+ * with members = 1. */
+ls_status ls_replay_attn_fwd_members_workspace(const ls_kv_cache* cache, int R, int members,
+                                               int Hq, int num_splits, size_t* bytes);
+ls_status ls_replay_attn_fwd_members(const ls_kv_cache* cache, const void* q, const void* k_resp,
+                                     const void* v_resp, int R, int members, int Hq,
+                                     float softmax_scale, int num_splits, void* o, float* lse,
+                                     void* workspace, size_t workspace_bytes,
+                                     ls_stream_t stream);
+
 /* ---------------------------------------------------------------- replay backward
  * Gradient of the replayed branch with the prompt state stopgrad: only
  * d(loss)/d(theta) at the captured state is formed and the path through the prompt

@@ -25,6 +25,7 @@ EXPORTED = (
     "ls_grpo_loss_fwd_bwd", "ls_validate_page_table", "ls_validate_page_table_workspace",
     "ls_last_device_error", "ls_status_string", "ls_kernel_launches",
     "ls_grpo_loss_fwd_bwd_noalloc", "ls_selftest_wait_timeout", "ls_grpo_logp",
+    "ls_replay_attn_fwd_members_workspace", "ls_replay_attn_fwd_members",
 )
 
 
@@ -61,6 +62,9 @@ def lib() -> C.CDLL:
             "ls_capture_kv": [cache, P, P, i64, i64, P],
             "ls_replay_attn_fwd_workspace": [cache, i32, i32, i32, szp],
             "ls_replay_attn_fwd": [cache, P, P, P, i32, i32, f32, i32, P, P, P, sz, P],
+            "ls_replay_attn_fwd_members_workspace": [cache, i32, i32, i32, i32, szp],
+            "ls_replay_attn_fwd_members": [cache, P, P, P, i32, i32, i32, f32, i32, P, P, P, sz,
+                                           P],
             "ls_replay_attn_bwd_workspace": [cache, i32, i32, i32, szp],
             "ls_replay_attn_bwd": [cache, P, P, P, P, P, P, i32, i32, f32, i32, i32, P, P, P, P,
                                    sz, P],
@@ -117,6 +121,22 @@ def ls_replay_attn_fwd(cache: ls_kv_cache, q: int, k_resp: int, v_resp: int, R: 
     _ok("ls_replay_attn_fwd",
         lib().ls_replay_attn_fwd(C.byref(cache), q, k_resp, v_resp, R, Hq, softmax_scale,
                                  num_splits, o, lse, workspace, workspace_bytes, stream))
+
+
+def ls_replay_attn_fwd_members_workspace(cache: ls_kv_cache, R: int, members: int, Hq: int,
+                                         num_splits: int) -> int:
+    return _size("ls_replay_attn_fwd_members_workspace", C.byref(cache), R, members, Hq,
+                 num_splits)
+
+
+def ls_replay_attn_fwd_members(cache: ls_kv_cache, q: int, k_resp: int, v_resp: int, R: int,
+                               members: int, Hq: int, softmax_scale: float, num_splits: int,
+                               o: int, lse: int, workspace: int, workspace_bytes: int,
+                               stream: int = 0) -> None:
+    _ok("ls_replay_attn_fwd_members",
+        lib().ls_replay_attn_fwd_members(C.byref(cache), q, k_resp, v_resp, R, members, Hq,
+                                         softmax_scale, num_splits, o, lse, workspace,
+                                         workspace_bytes, stream))
 
 
 def ls_replay_attn_bwd_workspace(cache: ls_kv_cache, R: int, Hq: int, num_splits: int) -> int:

@@ -88,13 +88,47 @@ ls_status check_replay(const ls_kv_cache* c, int R, int Hq, int num_splits) {
   return LS_OK;
 }
 
+LsSched make_sched_units(const ls_kv_cache* c, int units, int num_splits, int tile, int ctas) {
+  const int ntiles = (int)((c->num_tokens + tile - 1) / tile);
+  return ls_make_sched(units, ntiles, num_splits, ctas);
+}
+
 LsSched make_sched(const ls_kv_cache* c, int R, int Hq, int num_splits, int unit_rows, int tile,
                    int ctas, bool fwd) {
   (void)unit_rows;
   const int units = fwd ? ls_fwd_units(R, Hq, c->num_kv_heads)
                         : ls_bwd_units(R, Hq, c->num_kv_heads);
-  const int ntiles = (int)((c->num_tokens + tile - 1) / tile);
-  return ls_make_sched(units, ntiles, num_splits, ctas);
+  return make_sched_units(c, units, num_splits, tile, ctas);
+}
+
+// Forward geometry of `members` responses of R tokens.  Short responses (grouped-query
+// packing) pack the members' tokens into shared tiles as one sequence of members x R
+// tokens; otherwise every member has its own units.
+struct FwdGeom {
+  int pack, tiles, units, upm, rt;
+  bool ok;
+};
+FwdGeom fwd_geom(int R, int members, int Hq, int Hkv) {
+  FwdGeom f;
+  f.pack = ls_fwd_pack(R, Hq, Hkv);
+  f.ok = (int64_t)members * R <= (1 << 30);
+  if (!f.ok) return f;
+  if (members > 1 && f.pack > 1) {
+    const int tpt = ls_fwd_tile() / f.pack;
+    f.rt = members * R;
+    f.tiles = f.rt <= tpt ? 1 : 2;
+    const int tpu = f.tiles * tpt;
+    f.units = (int)((int64_t)Hkv * ((f.rt + tpu - 1) / tpu));
+    f.upm = INT32_MAX;
+  } else {
+    f.rt = R;
+    f.tiles = ls_fwd_tiles(R, Hq, Hkv);
+    const int upm = ls_fwd_units(R, Hq, Hkv);
+    f.ok = (int64_t)members * upm <= (1 << 30);
+    f.units = members * upm;
+    f.upm = members > 1 ? upm : INT32_MAX;
+  }
+  return f;
 }
 
 struct FwdWs {
@@ -142,6 +176,9 @@ LsAttnArgs attn_args(const ls_kv_cache* c, const void* q, const void* kr, const 
   a.pack = 1;
   a.tiles = 2;
   a.R = R;
+  a.members = 1;
+  a.upm = INT32_MAX;
+  a.rt = R;
   a.q = q;
   a.k_resp = kr;
   a.v_resp = vr;
@@ -186,46 +223,67 @@ ls_status ls_capture_kv(const ls_kv_cache* cache, const void* k, const void* v, 
                                      (cudaStream_t)stream));
 }
 
-ls_status ls_replay_attn_fwd_workspace(const ls_kv_cache* cache, int R, int Hq, int num_splits,
-                                       size_t* bytes) {
+ls_status ls_replay_attn_fwd_members_workspace(const ls_kv_cache* cache, int R, int members,
+                                               int Hq, int num_splits, size_t* bytes) {
   ls_status s = check_replay(cache, R, Hq, num_splits);
   if (s != LS_OK) return s;
-  if (!bytes) return LS_ERR_INVALID_ARG;
+  if (!bytes || members < 0) return LS_ERR_INVALID_ARG;
+  const FwdGeom f = fwd_geom(R, members > 0 ? members : 1, Hq, cache->num_kv_heads);
+  if (!f.ok) return LS_ERR_UNSUPPORTED;
   DevInfo d;
   if ((s = dev_info(&d)) != LS_OK) return s;
-  const LsSched sc = make_sched(cache, R, Hq, num_splits, ls_fwd_unit_rows(), ls_fwd_tile(),
-                                d.sms * ls_fwd_ctas_per_sm(), true);
+  const LsSched sc = make_sched_units(cache, f.units, num_splits, ls_fwd_tile(),
+                                      d.sms * ls_fwd_ctas_per_sm());
   *bytes = fwd_ws(sc, ls_fwd_unit_rows()).total;
   return LS_OK;
 }
 
-ls_status ls_replay_attn_fwd(const ls_kv_cache* cache, const void* q, const void* k_resp,
-                             const void* v_resp, int R, int Hq, float softmax_scale, int num_splits,
-                             void* o, float* lse, void* workspace, size_t workspace_bytes,
-                             ls_stream_t stream) {
+ls_status ls_replay_attn_fwd_members(const ls_kv_cache* cache, const void* q, const void* k_resp,
+                                     const void* v_resp, int R, int members, int Hq,
+                                     float softmax_scale, int num_splits, void* o, float* lse,
+                                     void* workspace, size_t workspace_bytes,
+                                     ls_stream_t stream) {
   ls_status s = check_replay(cache, R, Hq, num_splits);
   if (s != LS_OK) return s;
-  if (!isfinite(softmax_scale) || !(softmax_scale > 0.f)) return LS_ERR_INVALID_ARG;
-  if (R == 0) return LS_OK;
+  if (!isfinite(softmax_scale) || !(softmax_scale > 0.f) || members < 0) return LS_ERR_INVALID_ARG;
+  if (R == 0 || members == 0) return LS_OK;
+  const FwdGeom f = fwd_geom(R, members, Hq, cache->num_kv_heads);
+  if (!f.ok) return LS_ERR_UNSUPPORTED;
   const void* ptrs[] = {q, k_resp, v_resp, o, lse};
   for (const void* p : ptrs)
     if (!p || !aligned16(p)) return LS_ERR_INVALID_ARG;
   DevInfo d;
   if ((s = dev_info(&d)) != LS_OK) return s;
-  const LsSched sc = make_sched(cache, R, Hq, num_splits, ls_fwd_unit_rows(), ls_fwd_tile(),
-                                d.sms * ls_fwd_ctas_per_sm(), true);
+  const LsSched sc = make_sched_units(cache, f.units, num_splits, ls_fwd_tile(),
+                                      d.sms * ls_fwd_ctas_per_sm());
   const FwdWs w = fwd_ws(sc, ls_fwd_unit_rows());
   if (w.total > 0 && (!workspace || workspace_bytes < w.total || !aligned16(workspace)))
     return LS_ERR_WORKSPACE;
   LsAttnArgs a = attn_args(cache, q, k_resp, v_resp, R, Hq, softmax_scale, d.err);
-  a.pack = ls_fwd_pack(R, Hq, cache->num_kv_heads);
-  a.tiles = ls_fwd_tiles(R, Hq, cache->num_kv_heads);
+  a.pack = f.pack;
+  a.tiles = f.tiles;
+  a.members = members;
+  a.upm = f.upm;
+  a.rt = f.rt;
   LsFwdOut out;
   out.o = o;
   out.lse = lse;
   out.part_o = reinterpret_cast<float*>(static_cast<char*>(workspace) + w.part_o);
   out.part_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) + w.part_lse);
   return from_cuda(ls_launch_replay_fwd(a, sc, out, (cudaStream_t)stream));
+}
+
+ls_status ls_replay_attn_fwd_workspace(const ls_kv_cache* cache, int R, int Hq, int num_splits,
+                                       size_t* bytes) {
+  return ls_replay_attn_fwd_members_workspace(cache, R, 1, Hq, num_splits, bytes);
+}
+
+ls_status ls_replay_attn_fwd(const ls_kv_cache* cache, const void* q, const void* k_resp,
+                             const void* v_resp, int R, int Hq, float softmax_scale, int num_splits,
+                             void* o, float* lse, void* workspace, size_t workspace_bytes,
+                             ls_stream_t stream) {
+  return ls_replay_attn_fwd_members(cache, q, k_resp, v_resp, R, 1, Hq, softmax_scale, num_splits,
+                                    o, lse, workspace, workspace_bytes, stream);
 }
 
 ls_status ls_replay_attn_bwd_workspace(const ls_kv_cache* cache, int R, int Hq, int num_splits,

@@ -26,9 +26,13 @@ struct LsAttnArgs {
   int32_t pack;              // query rows per token in a tile: g (packed) or 1
   int32_t tiles;             // forward: query tiles per unit (2, or 1 when a packed unit's
                              // tokens all fit one tile)
-  int32_t R;                 // response tokens
-  const void* q;             // bf16 [R][hq][128]
-  const void* k_resp;        // bf16 [R][hkv][128]
+  int32_t R;                 // response tokens (of each member)
+  int32_t members;           // forward: responses of equal length R in one launch
+  int32_t upm;               // units per member (INT32_MAX unless units are per member)
+  int32_t rt;                // tokens the units cover: R, or members x R when the
+                             // members' tokens are packed into shared tiles
+  const void* q;             // bf16 [members][R][hq][128]
+  const void* k_resp;        // bf16 [members][R][hkv][128]
   const void* v_resp;
   float scale_log2;          // softmax_scale * log2(e)
   float scale;               // softmax_scale
@@ -36,8 +40,8 @@ struct LsAttnArgs {
 };
 
 struct LsFwdOut {
-  void* o;                   // bf16 [R][hq][128]
-  float* lse;                // [R][hq]
+  void* o;                   // bf16 [members][R][hq][128]
+  float* lse;                // [members][R][hq]
   float* part_o;             // workspace: [2*ctas][unit_rows][128]
   float* part_lse;           // workspace: [2*ctas][unit_rows]
 };

@@ -5,6 +5,17 @@
 // g query heads of one KV head, a tile holding floor(Tile / g) whole tokens.  Its items
 // are the prompt splits (tile ranges of Tile keys) followed by the response's own keys
 // (tiles 0 .. ceil(last token of the unit / Tile)).
+//
+// A forward launch over several responses of equal length R ("members") runs in one of
+// two layouts (kMode):
+//   1  units of one member each: member m's units follow those of members 0 .. m-1
+//      (upm units per member); used when tiles hold one head's tokens (pack = 1).
+//   2  members packed: the members' tokens are numbered back to back (member m's token t
+//      is number m R + t of RT = members R) and units cover that sequence, so a tile may
+//      hold rows of several members, all sharing each prompt K/V tile.  The response
+//      item of a unit then walks the response keys of every member it holds, member by
+//      member; the softmax masks the rows of the other members.
+// kMode 0 is the one-response walk.
 #pragma once
 #include <stdint.h>
 
@@ -12,42 +23,76 @@
 
 struct TileRec {
   int32_t u;           // unit
-  int32_t h, kvh, t0;  // first query head, kv head, first token of the unit
+  int32_t m;           // member (response) of the unit
+  int32_t h, kvh, t0;  // first query head, kv head, first token of the unit (in its member)
   int32_t key0;        // first key of the tile (prompt position or response index)
   int32_t slot;        // partial-result slot of the tile's range (-1: complete unit)
   bool resp;           // response keys (causal) vs prompt keys
   bool first_of_unit, last_of_unit, complete;
 };
 
-template <int UnitRows, int Tile>
+// kMode 2: the member and key tile of response tile `key0` (as TileCursor reports it:
+// the tile's index in the unit's response walk, times Tile) of the unit whose first
+// member is rm; the members' responses have R < 2 Tile tokens (packing is for short
+// responses), so each has rnt = 1 or 2 key tiles.
+template <int Tile>
+__device__ __forceinline__ void packed_resp_tile(int32_t key0, int32_t rm, int32_t R, int32_t* m,
+                                                 int32_t* key) {
+  const int32_t t = key0 / Tile, rnt = R > Tile ? 2 : 1;
+  const int32_t dm = rnt == 1 ? t : t >> 1;
+  *m = rm + dm;
+  *key = (t - dm * rnt) * Tile;
+}
+
+template <int UnitRows, int Tile, int kMode = 0>
 struct TileCursor {
   LsWalk walk;
   int32_t u, s, t, t_end, slot;
   bool item_first, item_last, item_complete, valid;
-  int32_t R, g, pack, tok_per_unit, nTB;
-  int32_t h, kvh, t0;  // derived from u once per item, not per tile
+  int32_t R, g, pack, tok_per_unit, nTB, upm, RT;
+  int32_t m, h, kvh, t0;  // derived from u once per item, not per tile
   bool resp;
 
+  // RT_: tokens the units cover (R, or members x R in kMode 2; 0 means R).
   __device__ TileCursor(const LsSched& sc, int cta, int32_t R_, int32_t g_, int32_t pack_ = 1,
-                        int32_t tiles_ = UnitRows / Tile)
+                        int32_t tiles_ = UnitRows / Tile, int32_t upm_ = INT32_MAX,
+                        int32_t RT_ = 0)
       : walk(sc, cta), u(0), s(0), t(0), t_end(0), slot(-1), item_first(false), item_last(false),
-        item_complete(false), valid(false), R(R_), g(g_), pack(pack_), h(0), kvh(0), t0(0),
-        resp(false) {
+        item_complete(false), valid(false), R(R_), g(g_), pack(pack_), upm(upm_),
+        RT(RT_ > 0 ? RT_ : R_), m(0), h(0), kvh(0), t0(0), resp(false) {
     tok_per_unit = tiles_ * (Tile / pack);
-    nTB = (R + tok_per_unit - 1) / tok_per_unit;
+    nTB = (RT + tok_per_unit - 1) / tok_per_unit;
   }
+
+
 
   __device__ bool open_item() {
     while (walk.next(&u, &s, &item_first, &item_last, &item_complete, &slot)) {
-      const int32_t grp = u / nTB;  // query head (pack 1) or kv head (packed)
-      t0 = (u - grp * nTB) * tok_per_unit;
+      int32_t ul = u;  // unit within its member
+      if constexpr (kMode == 1) {
+        m = u / upm;
+        ul = u - m * upm;
+      }
+      const int32_t grp = ul / nTB;    // query head (pack 1) or kv head (packed)
+      t0 = (ul - grp * nTB) * tok_per_unit;
       kvh = pack == 1 ? grp / g : grp;
       h = pack == 1 ? grp : grp * g;
       resp = (s == walk.sc->nsplit);
       if (resp) {
-        const int32_t qe = t0 + tok_per_unit < R ? t0 + tok_per_unit : R;
         t = 0;
-        t_end = (qe + Tile - 1) / Tile;
+        if constexpr (kMode == 2) {
+          // Members rm .. ml have rows in the unit.  Each sees keys up to its last row in
+          // the unit: all rnt key tiles of its response, except member ml, whose rows may
+          // stop early.  Tile t (key0 = t Tile) is key tile t % rnt of member
+          // rm + t / rnt (packed_resp_tile).
+          const int32_t ve = t0 + tok_per_unit < RT ? t0 + tok_per_unit : RT;
+          const int32_t rm = t0 / R, ml = (ve - 1) / R;
+          const int32_t rnt = (R + Tile - 1) / Tile;
+          t_end = (ml - rm) * rnt + (ve - ml * R + Tile - 1) / Tile;
+        } else {
+          const int32_t qe = t0 + tok_per_unit < R ? t0 + tok_per_unit : R;
+          t_end = (qe + Tile - 1) / Tile;
+        }
       } else {
         walk.sc->split_tiles(s, &t, &t_end);
       }
@@ -81,6 +126,7 @@ struct TileCursor {
       r->first_of_unit = false;
     }
     r->u = u;
+    r->m = m;
     r->h = h;
     r->t0 = t0;
     r->kvh = kvh;

@@ -75,10 +75,15 @@ struct TmapSet {
   CUtensorMap q, kp, vp, kr, vr;
 };
 
-using FwdCursor = TileCursor<kUnitRows, kTile>;
+template <int kMode>
+using FwdCursor = TileCursor<kUnitRows, kTile, kMode>;
 
 __device__ __forceinline__ uint32_t bar_addr(uint32_t base, int i) { return base + kOffBar + 8 * i; }
 
+// kMode (the unit layouts of ls_tiles.cuh): 0 one response; 1 several responses of
+// equal length, units per member (4-D Q and response maps); 2 several responses packed
+// into shared tiles (Q as one token sequence, 4-D response maps, rows masked by member).
+template <int kMode>
 __global__ void __launch_bounds__(kThreads, 1)
 replay_fwd_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a, const __grid_constant__ LsSched sc,
                      const LsFwdOut out) {
@@ -147,7 +152,7 @@ replay_fwd_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a, con
       tma_prefetch_desc(&tm.vp);
       tma_prefetch_desc(&tm.kr);
       tma_prefetch_desc(&tm.vr);
-      FwdCursor cur(sc, blockIdx.x, a.R, a.g, a.pack, a.tiles);
+      FwdCursor<kMode> cur(sc, blockIdx.x, a.R, a.g, a.pack, a.tiles, a.upm, a.rt);
       TileRec r;
       uint32_t ring = 0, units = 0, aux = 0;
       const int32_t ps = 1 << a.ps_log2;
@@ -163,8 +168,12 @@ replay_fwd_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a, con
           mbar_expect_tx(qb, (uint32_t)a.tiles * 2u * 128u * (uint32_t)(a.pack * tpt));
           for (int tt = 0; tt < a.tiles; ++tt)
             for (int hf = 0; hf < 2; ++hf)
-              tma_load_3d(sbase + kOffQ + tt * kTileBytes + hf * kHalfBytes, &tm.q, hf * 64, r.h,
-                          r.t0 + tt * tpt, qb);
+              if constexpr (kMode == 1)
+                tma_load_4d(sbase + kOffQ + tt * kTileBytes + hf * kHalfBytes, &tm.q, hf * 64,
+                            r.h, r.t0 + tt * tpt, r.m, qb);
+              else
+                tma_load_3d(sbase + kOffQ + tt * kTileBytes + hf * kHalfBytes, &tm.q, hf * 64,
+                            r.h, r.t0 + tt * tpt, qb);
           ++units;
         }
         for (int kv = 0; kv < 2 && ok; ++kv) {
@@ -184,8 +193,14 @@ replay_fwd_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a, con
           mbar_expect_tx(fb, kTileBytes);
           if (r.resp) {
             const void* map = kv == 0 ? (const void*)&tm.kr : (const void*)&tm.vr;
+            int32_t rmem = r.m, key = r.key0;
+            if constexpr (kMode == 2)
+              packed_resp_tile<kTile>(r.key0, r.t0 / a.R, a.R, &rmem, &key);
             for (int hf = 0; hf < 2; ++hf)
-              tma_load_3d(dst + hf * kHalfBytes, map, hf * 64, r.kvh, r.key0, fb);
+              if constexpr (kMode != 0)
+                tma_load_4d(dst + hf * kHalfBytes, map, hf * 64, r.kvh, key, rmem, fb);
+              else
+                tma_load_3d(dst + hf * kHalfBytes, map, hf * 64, r.kvh, key, fb);
           } else {
             const void* map = kv == 0 ? (const void*)&tm.kp : (const void*)&tm.vp;
             for (int b = 0; b < kTile / box_rows; ++b) {
@@ -257,7 +272,7 @@ replay_fwd_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a, con
                     (accumulate || kk > 0) ? 1u : 0u);
         }
       };
-      FwdCursor cursor(sc, blockIdx.x, a.R, a.g, a.pack, a.tiles);
+      FwdCursor<kMode> cursor(sc, blockIdx.x, a.R, a.g, a.pack, a.tiles, a.upm, a.rt);
       TileRec cur, nxt;
       uint32_t ring = 0, units = 0, kc = 0;
       bool ok = cursor.next(&cur);
@@ -340,10 +355,12 @@ replay_fwd_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a, con
     const int32_t tpt = kTile / a.pack;
     const int32_t tok_off = t * tpt + row / a.pack, head_off = row % a.pack;
     const bool row_used = row < a.pack * tpt;
-    FwdCursor cursor(sc, blockIdx.x, a.R, a.g, a.pack, a.tiles);
+    FwdCursor<kMode> cursor(sc, blockIdx.x, a.R, a.g, a.pack, a.tiles, a.upm, a.rt);
     TileRec r;
     uint32_t kc = 0, oc = 0;
     float m = -INFINITY, l = 0.f, lcomp = 0.f;
+    // kMode 2: this row's member and the unit's first member, for the unit at row_t0
+    int32_t row_t0 = -1, row_m = 0, row_um = 0;
     while (tile_used && cursor.next(&r)) {
       if (!mbar_wait(bar_addr(sbase, B_S_FULL + t), kc & 1)) { fail(); break; }
       tc_fence_after();
@@ -357,11 +374,27 @@ replay_fwd_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a, con
       reg_fence32(sr + 32);
       reg_fence32(sr + 64);
       reg_fence32(sr + 96);
-      const int32_t tq = r.t0 + tok_off;  // this row's response token
+      // this row's token: in kMode 2 a number in the members' joint sequence, split
+      // into its member and the token within that member's response
+      const int32_t vt = r.t0 + tok_off;
+      int32_t tq = vt, rmem = 0, unit_m = 0;
+      if constexpr (kMode == 2) {
+        if (r.t0 != row_t0) {  // once per unit, not per tile
+          row_t0 = r.t0;
+          row_m = vt / a.R;
+          row_um = r.t0 / a.R;
+        }
+        rmem = row_m;
+        unit_m = row_um;
+        tq = vt - rmem * a.R;
+      }
       int32_t lim = kTile;                          // keys [key0, key0 + lim) visible
       if (r.resp) {
-        const int32_t lr = (tq + 1 < a.R ? tq + 1 : a.R) - r.key0;
+        int32_t km = 0, key0 = r.key0;              // member and first key of the tile
+        if constexpr (kMode == 2) packed_resp_tile<kTile>(r.key0, unit_m, a.R, &km, &key0);
+        const int32_t lr = (tq + 1 < a.R ? tq + 1 : a.R) - key0;
         lim = lr < kTile ? lr : kTile;
+        if (kMode == 2 && rmem != km) lim = 0;      // another member's keys
       } else if (r.key0 + kTile > a.P) {
         lim = (int32_t)(a.P - r.key0);
       }
@@ -447,10 +480,12 @@ replay_fwd_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a, con
         const float inv = 1.f / lt;
         const float lse = (m + log2f(lt)) * kLn2;
         if (r.complete) {
-          const bool valid = row_used && tq < a.R;
+          const bool valid = row_used && vt < a.rt;
           const int32_t hrow = r.h + head_off;
-          __nv_bfloat16* orow =
-              static_cast<__nv_bfloat16*>(out.o) + ((int64_t)(valid ? tq : 0) * a.hq + (valid ? hrow : 0)) * kD;
+          // output row of token vt (of member r.m when units are per member)
+          const int64_t mrow = kMode == 1 ? (int64_t)r.m * a.R : 0;
+          const int64_t orow_idx = valid ? (mrow + vt) * a.hq + hrow : 0;
+          __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(out.o) + orow_idx * kD;
 #pragma unroll 1
           for (int c0 = 0; c0 < 128; c0 += 32) {
             uint32_t ov[32];
@@ -469,7 +504,7 @@ replay_fwd_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a, con
               }
             }
           }
-          if (valid) out.lse[(int64_t)tq * a.hq + hrow] = lse;
+          if (valid) out.lse[orow_idx] = lse;
         } else {
           const int slot = r.slot;
           float* prow = out.part_o + ((int64_t)slot * kUnitRows + t * kTile + row) * kD;
@@ -511,15 +546,16 @@ __global__ void __launch_bounds__(kD) replay_fwd_tc_combine(const LsAttnArgs a, 
   const int tu = blockIdx.x, T = sc.tail_units, Q = sc.pieces;
   const int u = sc.tail_unit0() + tu;
   const int tpt = kTile / a.pack, tok_per_unit = a.tiles * tpt;
-  const int nTB = (a.R + tok_per_unit - 1) / tok_per_unit;
-  const int grp = u / nTB, t0 = (u % nTB) * tok_per_unit;
+  const int nTB = (a.rt + tok_per_unit - 1) / tok_per_unit;
+  const int m = u / a.upm, ul = u - m * a.upm;  // member, unit within the member
+  const int grp = ul / nTB, t0 = (ul % nTB) * tok_per_unit;
   const int h0 = a.pack == 1 ? grp : grp * a.g;
   const int col = threadIdx.x;
   for (int r = blockIdx.y * kCombineRows; r < (blockIdx.y + 1) * kCombineRows; ++r) {
     const int l = r % kTile;  // row within its tile
     if (l >= a.pack * tpt || r / kTile >= a.tiles) continue;
     const int t = t0 + (r / kTile) * tpt + l / a.pack, h = h0 + l % a.pack;
-    if (t >= a.R) continue;
+    if (t >= a.rt) continue;
     float mx = -INFINITY;
     for (int k = 0; k < Q; ++k) mx = fmaxf(mx, out.part_lse[(int64_t)(k * T + tu) * kUnitRows + r]);
     float sum = 0.f;
@@ -530,7 +566,7 @@ __global__ void __launch_bounds__(kD) replay_fwd_tc_combine(const LsAttnArgs a, 
       const int64_t slot = k * T + tu;
       acc += expf(out.part_lse[slot * kUnitRows + r] - lse) * out.part_o[(slot * kUnitRows + r) * kD + col];
     }
-    const int64_t row = (int64_t)t * a.hq + h;
+    const int64_t row = ((int64_t)m * a.R + t) * a.hq + h;
     static_cast<__nv_bfloat16*>(out.o)[row * kD + col] = __float2bfloat16_rn(acc);
     if (col == 0) out.lse[row] = lse;
   }
@@ -568,19 +604,29 @@ int ls_fwd_units(int R, int hq, int hkv) {
 cudaError_t ls_launch_replay_fwd(const LsAttnArgs& a, const LsSched& sc, const LsFwdOut& out,
                                  cudaStream_t st) {
   TmapSet tm;
-  const uint32_t box_q[3] = {64, 1, kTile};
+  // Q and the response K/V are (dim, head, token) maps, with a fourth dimension for the
+  // member when one launch covers several responses: a box never crosses a member, so
+  // rows past a member's R read as zeros, not as the next member's rows.
+  const uint32_t box_q[4] = {64, 1, kTile, 1};
+  const uint64_t M = (uint64_t)a.members;
+  const int mode = a.members <= 1 ? 0 : (a.rt > a.R ? 2 : 1);
+  const int rank = mode == 0 ? 3 : 4;
   {
-    // Q boxes: 128 tokens of one head, or floor(128 / pack) tokens x pack heads
-    const uint32_t box_qp[3] = {64, (uint32_t)a.pack, (uint32_t)(kTile / a.pack)};
-    const uint64_t dims[3] = {(uint64_t)kD, (uint64_t)a.hq, (uint64_t)a.R};
-    const uint64_t strides[2] = {(uint64_t)kD * 2, (uint64_t)a.hq * kD * 2};
-    if (!ls_make_tmap_bf16(&tm.q, a.q, 3, dims, strides, box_qp)) return cudaErrorInvalidValue;
+    // Q boxes: 128 tokens of one head, or floor(128 / pack) tokens x pack heads; in
+    // kMode 2 the members' tokens are one sequence of rt tokens
+    const uint32_t box_qp[4] = {64, (uint32_t)a.pack, (uint32_t)(kTile / a.pack), 1};
+    const uint64_t dims[4] = {(uint64_t)kD, (uint64_t)a.hq, (uint64_t)(mode == 2 ? a.rt : a.R), M};
+    const uint64_t strides[3] = {(uint64_t)kD * 2, (uint64_t)a.hq * kD * 2,
+                                 (uint64_t)a.R * a.hq * kD * 2};
+    if (!ls_make_tmap_bf16(&tm.q, a.q, mode == 1 ? 4 : 3, dims, strides, box_qp))
+      return cudaErrorInvalidValue;
   }
   {
-    const uint64_t dims[3] = {(uint64_t)kD, (uint64_t)a.hkv, (uint64_t)a.R};
-    const uint64_t strides[2] = {(uint64_t)kD * 2, (uint64_t)a.hkv * kD * 2};
-    if (!ls_make_tmap_bf16(&tm.kr, a.k_resp, 3, dims, strides, box_q)) return cudaErrorInvalidValue;
-    if (!ls_make_tmap_bf16(&tm.vr, a.v_resp, 3, dims, strides, box_q)) return cudaErrorInvalidValue;
+    const uint64_t dims[4] = {(uint64_t)kD, (uint64_t)a.hkv, (uint64_t)a.R, M};
+    const uint64_t strides[3] = {(uint64_t)kD * 2, (uint64_t)a.hkv * kD * 2,
+                                 (uint64_t)a.R * a.hkv * kD * 2};
+    if (!ls_make_tmap_bf16(&tm.kr, a.k_resp, rank, dims, strides, box_q)) return cudaErrorInvalidValue;
+    if (!ls_make_tmap_bf16(&tm.vr, a.v_resp, rank, dims, strides, box_q)) return cudaErrorInvalidValue;
   }
   {
     const int ps = 1 << a.ps_log2;
@@ -590,10 +636,17 @@ cudaError_t ls_launch_replay_fwd(const LsAttnArgs& a, const LsSched& sc, const L
     if (!ls_make_tmap_bf16(&tm.kp, a.k_pool, 2, dims, strides, box)) return cudaErrorInvalidValue;
     if (!ls_make_tmap_bf16(&tm.vp, a.v_pool, 2, dims, strides, box)) return cudaErrorInvalidValue;
   }
-  cudaError_t e = cudaFuncSetAttribute(replay_fwd_tc_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  const void* fn = mode == 0 ? (const void*)replay_fwd_tc_kernel<0>
+                  : mode == 1 ? (const void*)replay_fwd_tc_kernel<1>
+                              : (const void*)replay_fwd_tc_kernel<2>;
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
-  replay_fwd_tc_kernel<<<sc.ctas, kThreads, kSmemBytes, st>>>(tm, a, sc, out);
+  if (mode == 0)
+    replay_fwd_tc_kernel<0><<<sc.ctas, kThreads, kSmemBytes, st>>>(tm, a, sc, out);
+  else if (mode == 1)
+    replay_fwd_tc_kernel<1><<<sc.ctas, kThreads, kSmemBytes, st>>>(tm, a, sc, out);
+  else
+    replay_fwd_tc_kernel<2><<<sc.ctas, kThreads, kSmemBytes, st>>>(tm, a, sc, out);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   ls_note_launch();

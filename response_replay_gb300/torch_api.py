@@ -104,6 +104,32 @@ def replay_fwd(cache: PagedKVCache, q: torch.Tensor, k_resp: torch.Tensor, v_res
     return o, lse
 
 
+def replay_fwd_members(cache: PagedKVCache, q: torch.Tensor, k_resp: torch.Tensor,
+                       v_resp: torch.Tensor, softmax_scale: float, num_splits: int,
+                       o: torch.Tensor | None = None, lse: torch.Tensor | None = None,
+                       stream=None):
+    """Forward of several equal-length responses over the prompt in one launch:
+    q [members][R][Hq][128], k_resp / v_resp [members][R][Hkv][128]."""
+    M, R, hq, _ = q.shape
+    hkv = cache.num_kv_heads
+    _check(q, "q", torch.bfloat16, (M, R, hq, HEAD_DIM))
+    _check(k_resp, "k_resp", torch.bfloat16, (M, R, hkv, HEAD_DIM))
+    _check(v_resp, "v_resp", torch.bfloat16, (M, R, hkv, HEAD_DIM))
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((M, R, hq), dtype=torch.float32, device=q.device)
+    _check(o, "o", torch.bfloat16, q.shape)
+    _check(lse, "lse", torch.float32, (M, R, hq))
+    nbytes = B.ls_replay_attn_fwd_members_workspace(cache.struct, R, M, hq, num_splits)
+    ws = workspace(nbytes, q.device, "fwd")
+    B.ls_replay_attn_fwd_members(cache.struct, q.data_ptr(), k_resp.data_ptr(),
+                                 v_resp.data_ptr(), R, M, hq, softmax_scale, num_splits,
+                                 o.data_ptr(), lse.data_ptr(), ws.data_ptr(), ws.numel(),
+                                 _stream(stream))
+    return o, lse
+
+
 def replay_bwd(cache: PagedKVCache, q, k_resp, v_resp, o, lse, d_o, softmax_scale: float,
                num_splits: int, dq=None, dk=None, dv=None, accumulate: bool = False, stream=None):
     R, hq, _ = q.shape
