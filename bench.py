@@ -230,23 +230,31 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         e.record(stream)
         return e
 
-    def member(i, m=None, before_loss=None):
-        """One member's replay: forward, GRPO loss (accumulating), backward."""
-        br = branches[i]
-        api.replay_fwd(cache, br.q, br.k, br.v, scale, w.num_splits, o=o, lse=lse, stream=stream)
+    def member(i, m=None, before_loss=None, inp=None):
+        """One member's replay: forward, GRPO loss (accumulating), backward.  inp: another
+        set of device input buffers (the e2e double buffer); default the resident one."""
+        if inp is None:
+            br = branches[i]
+            q, kr, vr, d_o = br.q, br.k, br.v, br.d_o
+            logits, targets, lpo = gin.logits, gin.targets, logp_old
+            rewards, lens = gin.rewards, gin.resp_lens
+        else:
+            q, kr, vr, d_o = inp.br[i]
+            logits, targets, lpo, rewards, lens = (inp.logits, inp.targets, inp.logp_old,
+                                                   inp.rewards, inp.lens)
+        api.replay_fwd(cache, q, kr, vr, scale, w.num_splits, o=o, lse=lse, stream=stream)
         if m is not None:
             m.append(ev())
         if before_loss is not None:
             before_loss()
         s, e = off[i], off[i + 1]
-        api.grpo_loss_fwd_bwd(gin.logits[s:e], gin.targets[s:e], logp_old[s:e], gin.rewards,
-                              gin.resp_lens, i, i + 1, 0.2, loss=loss, accumulate=i > 0,
-                              dlogits=dlog[: e - s], logp_out=lp_out[s:e], stats=stats,
-                              stream=stream)
+        api.grpo_loss_fwd_bwd(logits[s:e], targets[s:e], lpo[s:e], rewards, lens, i, i + 1, 0.2,
+                              loss=loss, accumulate=i > 0, dlogits=dlog[: e - s],
+                              logp_out=lp_out[s:e], stats=stats, stream=stream)
         if m is not None:
             m.append(ev())
-        api.replay_bwd(cache, br.q, br.k, br.v, o, lse, br.d_o, scale, w.num_splits, dq=dq,
-                       dk=dk, dv=dv, accumulate=i > 0, stream=stream)
+        api.replay_bwd(cache, q, kr, vr, o, lse, d_o, scale, w.num_splits, dq=dq, dk=dk, dv=dv,
+                       accumulate=i > 0, stream=stream)
         if m is not None:
             m.append(ev())
 
@@ -346,44 +354,59 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                    host["rewards"], host["lens"]] + [x for b in host["br"] for x in b])
         d2h = 4
 
-        # The step's inputs arrive on two copy streams (prompt K on one and V on the other
-        # in page-aligned chunks, then each member's tensors alternating), each piece
-        # marked by an event; the compute stream waits for exactly the pieces its next call
-        # reads, so the prompt is captured chunk by chunk as it lands and a member's
-        # logits arrive while earlier members' attention runs.  A step's copies start only
-        # after the previous step's work is done (no cross-step prefetch).
+        # Inputs go through two sets of device buffers: step s + 1's inputs are copied
+        # into one set while step s computes on the other (a set is refilled only after
+        # the step that read it has finished).  Every step's inputs are copied inside the
+        # timed region; only the first step's copies have no earlier step to hide behind.
+        # Within a set the copies run on two copy streams (prompt K on one and V on the
+        # other in page-aligned chunks, then each member's tensors), each piece marked by
+        # an event; the compute stream waits for exactly the pieces its next call reads.
         copy_streams = [torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)]
         n_chunks = 8
         P = pr.k.shape[0]
         unit = w.page_size
         bounds = [(P // unit) * c // n_chunks * unit for c in range(n_chunks)] + [P]
 
+        class InputSet:
+            def __init__(self, k, v, br, logits, targets, lpo, rewards, lens):
+                self.k, self.v, self.br = k, v, br
+                self.logits, self.targets, self.logp_old = logits, targets, lpo
+                self.rewards, self.lens = rewards, lens
+
+        sets = [InputSet(pr.k, pr.v, [(b.q, b.k, b.v, b.d_o) for b in branches], gin.logits,
+                         gin.targets, logp_old, gin.rewards, gin.resp_lens)]
+        el = torch.empty_like
+        sets.append(InputSet(el(pr.k), el(pr.v), [tuple(el(x) for x in t) for t in sets[0].br],
+                             el(gin.logits), el(gin.targets), el(logp_old), el(gin.rewards),
+                             el(gin.resp_lens)))
+
         def mark(st):
             e = torch.cuda.Event()
             e.record(st)
             return e
 
-        def e2e_step():
-            prev = mark(stream)
+        def issue_copies(dst, after):
+            """Enqueue one step's host->device copies into set dst once `after` has
+            happened; returns the events of its pieces."""
             for cs in copy_streams:
-                cs.wait_event(prev)
+                cs.wait_event(after)
             cs0, cs1 = copy_streams
             with torch.cuda.stream(cs0):
-                gin.rewards.copy_(host["rewards"], non_blocking=True)
-                gin.resp_lens.copy_(host["lens"], non_blocking=True)
+                dst.rewards.copy_(host["rewards"], non_blocking=True)
+                dst.lens.copy_(host["lens"], non_blocking=True)
             kv_ev = []
             for c in range(n_chunks):
                 s, e = bounds[c], bounds[c + 1]
                 with torch.cuda.stream(cs0):
-                    pr.k[s:e].copy_(host["k"][s:e], non_blocking=True)
+                    dst.k[s:e].copy_(host["k"][s:e], non_blocking=True)
                 with torch.cuda.stream(cs1):
-                    pr.v[s:e].copy_(host["v"][s:e], non_blocking=True)
+                    dst.v[s:e].copy_(host["v"][s:e], non_blocking=True)
                 kv_ev.append((mark(cs0), mark(cs1)))
             br_ev, lg_ev = [], []
-            for i, (b, hb) in enumerate(zip(branches, host["br"])):
+            for i, (b, hb) in enumerate(zip(dst.br, host["br"])):
                 with torch.cuda.stream(copy_streams[i % 2]):
-                    for dst, src in zip((b.q, b.k, b.v, b.d_o), hb):
-                        dst.copy_(src, non_blocking=True)
+                    for d_, s_ in zip(b, hb):
+                        d_.copy_(s_, non_blocking=True)
                 br_ev.append(mark(copy_streams[i % 2]))
                 # the member's logits rows, half on each copy stream
                 s, e = off[i], off[i + 1]
@@ -391,31 +414,46 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                 evs = []
                 for cs, (a0, a1) in zip(copy_streams, ((s, mid), (mid, e))):
                     with torch.cuda.stream(cs):
-                        gin.logits[a0:a1].copy_(host["logits"][a0:a1], non_blocking=True)
-                        gin.targets[a0:a1].copy_(host["targets"][a0:a1], non_blocking=True)
-                        logp_old[a0:a1].copy_(host["logp_old"][a0:a1], non_blocking=True)
+                        dst.logits[a0:a1].copy_(host["logits"][a0:a1], non_blocking=True)
+                        dst.targets[a0:a1].copy_(host["targets"][a0:a1], non_blocking=True)
+                        dst.logp_old[a0:a1].copy_(host["logp_old"][a0:a1], non_blocking=True)
                     evs.append(mark(cs))
                 lg_ev.append(evs)
+            return kv_ev, br_ev, lg_ev
+
+        def compute(src, evs):
+            """One step on input set src once its pieces have landed; returns the event
+            after which src may be refilled."""
+            kv_ev, br_ev, lg_ev = evs
             for c in range(n_chunks):
                 stream.wait_event(kv_ev[c][0])
                 stream.wait_event(kv_ev[c][1])
                 s, e = bounds[c], bounds[c + 1]
-                cache.capture(pr.k[s:e], pr.v[s:e], s, stream)
+                cache.capture(src.k[s:e], src.v[s:e], s, stream)
             for i in range(G):
                 # the forward reads only the member's q / k / v / dO (and the captured
                 # prompt); the loss also waits for its logits rows, whose events follow
                 # the rewards and lengths copied first on copy stream 0
                 stream.wait_event(br_ev[i])
-                member(i, before_loss=lambda i=i: [stream.wait_event(e) for e in lg_ev[i]])
+                member(i, before_loss=lambda i=i: [stream.wait_event(e) for e in lg_ev[i]],
+                       inp=src)
             loss_h.copy_(loss, non_blocking=True)
+            return mark(stream)
 
-        e2e_step()
+        def e2e_steps(n):
+            free = [mark(stream), mark(stream)]  # when each set may be refilled
+            evs = issue_copies(sets[0], free[0])
+            for st in range(n):
+                nxt = issue_copies(sets[(st + 1) % 2], free[(st + 1) % 2]) if st + 1 < n else None
+                free[st % 2] = compute(sets[st % 2], evs)
+                evs = nxt
+
+        e2e_steps(1)
         torch.cuda.synchronize()
         if world > 1:
             torch.distributed.barrier()
         a = ev()
-        for _ in range(args.steps):
-            e2e_step()
+        e2e_steps(args.steps)
         b = ev()
         torch.cuda.synchronize()
         e_ms = max_over_ranks(a.elapsed_time(b), world, dev)
