@@ -587,7 +587,8 @@ def run_short_sweep(args, local_rank: int):
     responses R over the 2,097,152-position prompt, where the forward streams the prompt
     K/V once per KV head and HBM bandwidth, not the tensor cores, is the bound.  One JSON
     line per R: forward and backward times, prompt-KV GB/s of each pass against the
-    measured copy bandwidth, and the FLOP rate."""
+    measured copy bandwidth, the FLOP rate, and the batched forward of all G members'
+    responses of R tokens (pre-step scoring) in one launch."""
     import torch
 
     from response_replay_gb300 import synthetic as syn
@@ -634,7 +635,21 @@ def run_short_sweep(args, local_rank: int):
             torch.cuda.synchronize()
             return a.elapsed_time(b) / args.steps
 
+        # pre-step scoring: the forward of all G members' responses of R tokens in one launch
+        G = w.G
+        mq = torch.stack([syn.make_branch(R, w.hq, w.hkv, D, seed + 11 + i, dev).q
+                          for i in range(G)]).contiguous()
+        mk = br.k.unsqueeze(0).repeat(G, 1, 1, 1).contiguous()
+        mv = br.v.unsqueeze(0).repeat(G, 1, 1, 1).contiguous()
+        mo = torch.empty_like(mq)
+        mlse = torch.empty(mq.shape[:3], dtype=torch.float32, device=dev)
+
+        def fwd_members():
+            api.replay_fwd_members(cache, mq, mk, mv, scale, w.num_splits, o=mo, lse=mlse,
+                                   stream=stream)
+
         f_ms, b_ms = timed(fwd), timed(bwd)
+        m_ms = timed(fwd_members)
         f_fl, b_fl = attn_flops(w.P, R, w.hq)
         print(json.dumps({
             "sweep": "short responses over the 2,097,152-position prompt (supplementary)",
@@ -646,6 +661,9 @@ def run_short_sweep(args, local_rank: int):
             "fwd_frac_of_hbm": kv_bytes / (f_ms * 1e-3) / 1e9 / hbm,
             "bwd_frac_of_hbm": kv_bytes / (b_ms * 1e-3) / 1e9 / hbm,
             "fwd_tflops": f_fl / (f_ms * 1e-3) / 1e12, "bwd_tflops": b_fl / (b_ms * 1e-3) / 1e12,
+            "members": G, "members_fwd_ms": m_ms,
+            "members_fwd_frac_of_hbm": kv_bytes / (m_ms * 1e-3) / 1e9 / hbm,
+            "members_fwd_speedup_over_calls": G * f_ms / m_ms,
             "hbm_peak_gbs": hbm, "steps": args.steps, "warmup": args.warmup,
         }), flush=True)
 
