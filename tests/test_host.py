@@ -87,4 +87,27 @@ def test_argument_checks_reject_before_launch(lib):
     assert lib.ls_grpo_workspace(4, 2, C.byref(need)) == 0 and need.value > 0
     assert lib.ls_grpo_loss_fwd_bwd(256, 0, 4, 16, 256, 256, 256, 256, 2, 0, 2, 0.2, 1e-6, 1, 0, 256,
                                     256, None, None, 256, need.value - 1, None) == B.LS_ERR_WORKSPACE
+    # batched forward: negative member count, members x R beyond 2^30, bad scale,
+    # misaligned output; zero members or R = 0 is a no-op (no pointer is touched)
+    assert lib.ls_replay_attn_fwd_members_workspace(C.byref(ok), 16, -1, 8, 4, C.byref(sz)) == \
+        B.LS_ERR_INVALID_ARG
+    assert lib.ls_replay_attn_fwd_members_workspace(C.byref(ok), 1 << 20, 2048, 8, 4,
+                                                    C.byref(sz)) == B.LS_ERR_UNSUPPORTED
+    assert lib.ls_replay_attn_fwd_members(C.byref(ok), 256, 256, 256, 16, -2, 8, 0.1, 4, 256, 256,
+                                          256, 1 << 20, None) == B.LS_ERR_INVALID_ARG
+    assert lib.ls_replay_attn_fwd_members(C.byref(ok), 256, 256, 256, 16, 3, 8, 0.0, 4, 256, 256,
+                                          256, 1 << 20, None) == B.LS_ERR_INVALID_ARG
+    assert lib.ls_replay_attn_fwd_members(C.byref(ok), 256, 256, 256, 16, 3, 8, 0.1, 4, 264, 256,
+                                          256, 1 << 20, None) == B.LS_ERR_INVALID_ARG
+    assert lib.ls_replay_attn_fwd_members(C.byref(ok), None, None, None, 16, 0, 8, 0.1, 4, None,
+                                          None, None, 0, None) == B.LS_OK
+    assert lib.ls_replay_attn_fwd_members(C.byref(ok), None, None, None, 0, 3, 8, 0.1, 4, None,
+                                          None, None, 0, None) == B.LS_OK
+    # pre-step scoring: bad dtype, KL output without reference log-probs, misaligned logits
+    assert lib.ls_grpo_logp(256, 7, 4, 16, 256, None, 256, None, None, None) == \
+        B.LS_ERR_INVALID_ARG
+    assert lib.ls_grpo_logp(256, 0, 4, 16, 256, None, 256, None, 256, None) == \
+        B.LS_ERR_INVALID_ARG
+    assert lib.ls_grpo_logp(258, 0, 4, 16, 256, None, 256, None, None, None) == \
+        B.LS_ERR_INVALID_ARG
     assert B.status_string(B.LS_ERR_TIMEOUT)
