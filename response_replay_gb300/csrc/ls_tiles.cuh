@@ -21,6 +21,13 @@
 
 #include "ls_sched.h"
 
+// Compiled for the device and, by the schedule checker, for the host.
+#ifdef __CUDACC__
+#define LS_TILE_HD __host__ __device__
+#else
+#define LS_TILE_HD
+#endif
+
 struct TileRec {
   int32_t u;           // unit
   int32_t m;           // member (response) of the unit
@@ -36,7 +43,7 @@ struct TileRec {
 // member is rm; the members' responses have R < 2 Tile tokens (packing is for short
 // responses), so each has rnt = 1 or 2 key tiles.
 template <int Tile>
-__device__ __forceinline__ void packed_resp_tile(int32_t key0, int32_t rm, int32_t R, int32_t* m,
+LS_HD void packed_resp_tile(int32_t key0, int32_t rm, int32_t R, int32_t* m,
                                                  int32_t* key) {
   const int32_t t = key0 / Tile, rnt = R > Tile ? 2 : 1;
   const int32_t dm = rnt == 1 ? t : t >> 1;
@@ -54,7 +61,7 @@ struct TileCursor {
   bool resp;
 
   // RT_: tokens the units cover (R, or members x R in kMode 2; 0 means R).
-  __device__ TileCursor(const LsSched& sc, int cta, int32_t R_, int32_t g_, int32_t pack_ = 1,
+  LS_TILE_HD TileCursor(const LsSched& sc, int cta, int32_t R_, int32_t g_, int32_t pack_ = 1,
                         int32_t tiles_ = UnitRows / Tile, int32_t upm_ = INT32_MAX,
                         int32_t RT_ = 0)
       : walk(sc, cta), u(0), s(0), t(0), t_end(0), slot(-1), item_first(false), item_last(false),
@@ -66,7 +73,7 @@ struct TileCursor {
 
 
 
-  __device__ bool open_item() {
+  LS_TILE_HD bool open_item() {
     while (walk.next(&u, &s, &item_first, &item_last, &item_complete, &slot)) {
       int32_t ul = u;  // unit within its member
       if constexpr (kMode == 1) {
@@ -104,7 +111,7 @@ struct TileCursor {
   // The same walk as next(), reporting only whether the tile is the first / last of
   // its unit in this CTA (what an MMA issuer needs), so the common step is a compare
   // and an increment.
-  __device__ bool next_flags(bool* first, bool* last) {
+  LS_TILE_HD bool next_flags(bool* first, bool* last) {
     if (!valid || t >= t_end) {
       valid = open_item();
       if (!valid) return false;
@@ -117,7 +124,7 @@ struct TileCursor {
     return true;
   }
 
-  __device__ bool next(TileRec* r) {
+  LS_TILE_HD bool next(TileRec* r) {
     if (!valid || t >= t_end) {
       valid = open_item();
       if (!valid) return false;

@@ -3,7 +3,10 @@
 // flags, "complete" is set exactly for units one CTA processes whole, every partial
 // slot has exactly one writer and the combine's slots k*T + t of a tail unit are
 // exactly the slots written for it, the waves keep their lockstep assignment, and the
-// tail pieces balance the work to within 2% of the best piece count.
+// tail pieces balance the work to within 2% of the best piece count.  A second check
+// walks the forward's tile cursor (ls_tiles.cuh) in its packed-members layout: every
+// unit visits exactly the response key tiles its members' rows can see (member by
+// member, each once), and the MMA issuer's flag walk sees the same tiles.
 #include <cstdio>
 #include <cstdlib>
 #include <map>
@@ -11,6 +14,7 @@
 #include <vector>
 
 #include "ls_sched.h"
+#include "ls_tiles.cuh"
 
 static int fail(const char* what, int U, int nt, int sp, int C) {
   std::printf("FAIL %s U=%d ntiles=%d splits=%d ctas=%d\n", what, U, nt, sp, C);
@@ -84,6 +88,60 @@ static int check(int U, int nt, int sp, int C) {
   return 0;
 }
 
+// Packed members: `members` responses of R tokens numbered back to back (RT tokens), a
+// tile holding 128 / pack tokens of one KV head, `tiles` tiles per unit.
+static int check_packed(int R, int members, int pack, int hkv, int nt, int sp, int C) {
+  constexpr int kTile = 128, kUnitRows = 256;
+  const int RT = R * members, tpt = kTile / pack;
+  const int tiles = RT <= tpt ? 1 : 2, tpu = tiles * tpt;
+  const int nTB = (RT + tpu - 1) / tpu, U = hkv * nTB;
+  LsSched s = ls_make_sched(U, nt, sp, C);
+  std::map<int, std::multiset<std::pair<int, int>>> got;  // unit -> (member, first key)
+  for (int c = 0; c < s.ctas; ++c) {
+    TileCursor<kUnitRows, kTile, 2> cur(s, c, R, pack, pack, tiles, INT32_MAX, RT);
+    TileCursor<kUnitRows, kTile, 2> flags(s, c, R, pack, pack, tiles, INT32_MAX, RT);
+    TileRec r;
+    bool f0, l0;
+    int n = 0, nf = 0;
+    while (cur.next(&r)) {
+      ++n;
+      if (!flags.next_flags(&f0, &l0) || f0 != r.first_of_unit || l0 != r.last_of_unit) {
+        std::printf("FAIL packed flag walk R=%d members=%d pack=%d\n", R, members, pack);
+        return 1;
+      }
+      ++nf;
+      if (r.t0 != (r.u % nTB) * tpu || r.kvh != r.u / nTB) {
+        std::printf("FAIL packed unit decode R=%d members=%d pack=%d\n", R, members, pack);
+        return 1;
+      }
+      if (r.resp) {
+        int m, key;
+        packed_resp_tile<kTile>(r.key0, r.t0 / R, R, &m, &key);
+        got[r.u].insert({m, key});
+      }
+    }
+    if (flags.next_flags(&f0, &l0)) {
+      std::printf("FAIL packed flag walk longer R=%d members=%d pack=%d\n", R, members, pack);
+      return 1;
+    }
+    (void)nf;
+  }
+  for (int u = 0; u < U; ++u) {
+    std::multiset<std::pair<int, int>> want;
+    const int t0 = (u % nTB) * tpu, ve = t0 + tpu < RT ? t0 + tpu : RT;
+    for (int m = t0 / R; m * R < ve; ++m) {
+      const int e = (ve < (m + 1) * R ? ve : (m + 1) * R) - m * R;  // last row's token + 1
+      for (int k = 0; k * kTile < e; ++k) want.insert({m, k * kTile});
+    }
+    if (got[u] != want) {
+      std::printf("FAIL packed response tiles R=%d members=%d pack=%d hkv=%d unit=%d\n", R,
+                  members, pack, hkv, u);
+      return 1;
+    }
+  }
+  return 0;
+}
+
 int main() {
   int bad = 0, n = 0;
   const int Us[] = {1, 2, 3, 7, 8, 96, 151, 152, 153, 304, 384, 768, 1000};
@@ -103,6 +161,18 @@ int main() {
     LsSched s = ls_make_sched(U, 16384, 256, 152);
     std::printf("U=%d: %d waves, %d tail units in %d pieces\n", U, s.waves, s.tail_units, s.pieces);
   }
-  std::printf("%d/%d schedules ok\n", n - bad, n);
+  int pn = 0, pbad = 0;
+  for (int R : {1, 2, 5, 16, 21, 22, 77, 127, 128, 129, 255})
+    for (int members : {2, 3, 8, 100})
+      for (int pack : {2, 6, 8})
+        for (int hkv : {1, 4})
+          for (int C : {1, 7, 152})
+            for (int nt : {0, 7}) {
+              pbad += check_packed(R, members, pack, hkv, nt, 3, C);
+              ++pn;
+            }
+  bad += pbad;
+  std::printf("%d/%d packed-member walks ok\n", pn - pbad, pn);
+  std::printf("%d/%d schedules ok\n", n - bad + pbad, n);
   return bad ? 1 : 0;
 }
