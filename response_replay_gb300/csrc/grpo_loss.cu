@@ -56,37 +56,63 @@ __device__ __forceinline__ P* at(void* base, size_t off) {
   return reinterpret_cast<P*>(static_cast<char*>(base) + off);
 }
 
+// Sum over the 32 lanes of a warp in a fixed order (the same tree on every call).
+__device__ __forceinline__ double warp_sum(double x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  return x;
+}
+
+// One warp: advantages in fp64 about the first reward (lane-strided sums, fixed-order
+// tree), member token offsets by a warp scan over the member range, 1/(G R_i), the
+// length check, and a zero ticket for the streamed kernel's last-CTA reduction.
 __global__ void grpo_prep(const float* __restrict__ rewards, const int32_t* __restrict__ lens,
                           int G, int mb, int me, int std_ddof, double adv_eps, int64_t T,
                           void* ws, uint32_t* err) {
-  if (threadIdx.x != 0) return;
+  const int lane = threadIdx.x;
+  if (lane >= 32) return;
   const WsLayout w = ws_layout(T, G);
   int32_t* flag = at<int32_t>(ws, w.flag);
   double* adv = at<double>(ws, w.adv);
   double* inv = at<double>(ws, w.inv_norm);
   int64_t* off = at<int64_t>(ws, w.off);
   const double r0 = rewards[0];
-  double mean = 0.0, var = 0.0;
-  for (int i = 0; i < G; ++i) mean += (double)rewards[i] - r0;
-  mean /= G;
-  for (int i = 0; i < G; ++i) {
+  double sum = 0.0;
+  for (int i = lane; i < G; i += 32) sum += (double)rewards[i] - r0;
+  const double mean = warp_sum(sum) / G;
+  double sq = 0.0;
+  for (int i = lane; i < G; i += 32) {
     const double dev = ((double)rewards[i] - r0) - mean;
-    var += dev * dev;
+    sq += dev * dev;
   }
-  var /= (double)(G - std_ddof);
+  const double var = warp_sum(sq) / (double)(G - std_ddof);
   const double sd = sqrt(var);
-  for (int i = 0; i < G; ++i) adv[i] = (((double)rewards[i] - r0) - mean) / (sd + adv_eps);
-  int ok = 1;
-  off[0] = 0;
-  for (int i = mb; i < me; ++i) {
-    const int32_t n = lens[i];
-    if (n < 0) ok = 0;
-    off[i - mb + 1] = off[i - mb] + (n > 0 ? n : 0);
-    inv[i] = n > 0 ? 1.0 / ((double)G * (double)n) : 0.0;
+  for (int i = lane; i < G; i += 32) adv[i] = (((double)rewards[i] - r0) - mean) / (sd + adv_eps);
+  int bad = 0;
+  int64_t carry = 0;  // tokens of the members before this chunk
+  if (lane == 0) off[0] = 0;
+  for (int i0 = mb; i0 < me; i0 += 32) {
+    const int i = i0 + lane;
+    const int32_t n = i < me ? lens[i] : 0;
+    bad |= n < 0;
+    int64_t x = n > 0 ? n : 0;  // inclusive scan over the chunk
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int64_t y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (i < me) {
+      off[i - mb + 1] = carry + x;
+      inv[i] = n > 0 ? 1.0 / ((double)G * (double)n) : 0.0;
+    }
+    carry += __shfl_sync(0xffffffffu, x, 31);
   }
-  if (off[me - mb] != T) ok = 0;
-  if (!ok) ls_report(err, LS_DEVERR_CHECK);
-  *flag = ok;
+  bad = __any_sync(0xffffffffu, bad) || carry != T;
+  if (lane == 0) {
+    if (bad) ls_report(err, LS_DEVERR_CHECK);
+    *flag = !bad;
+    *at<uint32_t>(ws, w.flag + 4) = 0u;  // ticket
+  }
 }
 
 template <typename E>
@@ -356,6 +382,79 @@ __global__ void __launch_bounds__(kRowThreads) grpo_logp_rows(
   }
 }
 
+// Fixed-order reduction of the per-token terms into this call's loss and stats, by
+// kThreads threads (tid): lane-strided partials, a shuffle tree per warp, then warp 0
+// over the warps' results (sh: [kThreads / 32] x 3 doubles, shf: [kThreads / 32] x 2
+// floats of shared memory; sync(): a barrier of the kThreads threads).  The terms may
+// come from other CTAs of the same grid: they are read past L1.
+template <int kThreads, typename Sync>
+__device__ void grpo_reduce(void* ws, int64_t T, int G, int mb, int me, int accumulate,
+                            float* loss, float* stats, int tid, double* sh, float* shf,
+                            Sync sync) {
+  constexpr int kWarps = kThreads / 32;
+  const WsLayout w = ws_layout(T, G);
+  const double* inv = at<double>(ws, w.inv_norm);
+  const int64_t* off = at<int64_t>(ws, w.off);
+  const double* term = at<double>(ws, w.term);
+  const float* rho = at<float>(ws, w.rho);
+  const float* zeroed = at<float>(ws, w.zeroed);
+  const int lane = tid & 31, wid = tid >> 5;
+  double acc = 0.0, zc = 0.0, rs = 0.0;
+  float mn = FLT_MAX, mx = -FLT_MAX;
+  const int nm = me - mb;
+  for (int m = 0; m < nm; ++m) {
+    const double wgt = __ldcg(inv + mb + m) * (double)G;  // 1 / R_i
+    const int64_t e = __ldcg(off + m + 1);
+    for (int64_t t = __ldcg(off + m) + tid; t < e; t += kThreads) acc += __ldcg(term + t) * wgt;
+  }
+  for (int64_t t = tid; t < T; t += kThreads) {
+    const float r = __ldcg(rho + t);
+    zc += __ldcg(zeroed + t);
+    rs += r;
+    mn = fminf(mn, r);
+    mx = fmaxf(mx, r);
+  }
+  acc = warp_sum(acc);
+  zc = warp_sum(zc);
+  rs = warp_sum(rs);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  }
+  if (lane == 0) {
+    sh[wid * 3] = acc;
+    sh[wid * 3 + 1] = zc;
+    sh[wid * 3 + 2] = rs;
+    shf[wid * 2] = mn;
+    shf[wid * 2 + 1] = mx;
+  }
+  sync();
+  if (wid == 0) {
+    const bool h = lane < kWarps;
+    acc = warp_sum(h ? sh[lane * 3] : 0.0);
+    zc = warp_sum(h ? sh[lane * 3 + 1] : 0.0);
+    rs = warp_sum(h ? sh[lane * 3 + 2] : 0.0);
+    mn = h ? shf[lane * 2] : FLT_MAX;
+    mx = h ? shf[lane * 2 + 1] : -FLT_MAX;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    }
+    if (lane == 0) {
+      const float contrib = (float)(-acc / (double)G);
+      loss[0] = accumulate ? loss[0] + contrib : contrib;
+      if (stats) {
+        stats[0] = (float)zc;
+        stats[1] = (float)rs;
+        stats[2] = T > 0 ? mn : 0.f;
+        stats[3] = T > 0 ? mx : 0.f;
+      }
+    }
+  }
+}
+
 // ---------------------------------------------------------------- streamed row kernel
 // Each CTA streams its token rows through shared memory in chunks of two 16-byte vectors
 // per consumer thread: a producer warp issues 1-D bulk copies into a ring of chunks (about 200 KB in flight per SM, so
@@ -460,7 +559,7 @@ struct RowScalars {
 };
 
 struct StreamSmem {
-  uint32_t full, empty, info_full, info_empty, red, bc, info, abort, total;
+  uint32_t full, empty, info_full, info_empty, red, bc, info, abort, fin, total;
 };
 __host__ __device__ constexpr StreamSmem stream_smem(int stages, uint32_t chunk_bytes, int warps) {
   StreamSmem l{};
@@ -472,7 +571,8 @@ __host__ __device__ constexpr StreamSmem stream_smem(int stages, uint32_t chunk_
   l.red = p;         p += 2 * warps * 8;          // [row parity][warp] (max, sum)
   l.bc = p;          p += 16;                     // c, lse2, target of the current row
   l.info = p;        p += 2 * (uint32_t)sizeof(RowScalars);
-  l.abort = p;       p += 16;
+  l.abort = p;       p += 16;                     // abort flag, last-CTA flag
+  l.fin = p;         p += 32 * 3 * 8 + 32 * 2 * 4;  // grpo_reduce scratch
   l.total = p;
   return l;
 }
@@ -494,6 +594,10 @@ struct StreamArgs {
   float* lse_out;
   float* kl_out;
   uint32_t* err;
+  // loss form: the last CTA to finish reduces the terms into loss / stats
+  int accumulate;
+  float* loss;
+  float* stats;
 };
 
 template <typename E, bool kLoss>
@@ -742,57 +846,37 @@ __global__ void __launch_bounds__(StreamCfg<kLoss>::kThreads, StreamCfg<kLoss>::
       }
     }
   }
+  if constexpr (kLoss) {
+    // The last CTA to finish reduces every row's term into the loss (the ticket was
+    // zeroed by the prep launch).  Thread 0 wrote this CTA's terms; the fence orders
+    // them before its ticket.
+    volatile int* last = abort + 1;
+    if (tid == 0) {
+      __threadfence();
+      const uint32_t t = atomicAdd(at<uint32_t>(p.ws, ws_layout(T, p.G).flag + 4), 1u);
+      *last = t == gridDim.x - 1;
+    }
+    consumers_sync<kCons>();
+    if (*last) {
+      __threadfence();
+      grpo_reduce<kCons>(p.ws, T, p.G, p.mb, p.me, p.accumulate, p.loss, p.stats, tid,
+                         reinterpret_cast<double*>(smem + L.fin),
+                         reinterpret_cast<float*>(smem + L.fin + 32 * 3 * 8),
+                         [] { consumers_sync<kCons>(); });
+    }
+  }
 }
 
+// The reduction as its own launch (T = 0, or the one-CTA-per-row kernel).
 __global__ void __launch_bounds__(1024) grpo_final(int64_t T, int G, int mb, int me,
                                                    int accumulate, float* loss, float* stats,
                                                    void* ws) {
   const WsLayout w = ws_layout(T, G);
   if (*at<int32_t>(ws, w.flag) == 0) return;
-  const double* inv = at<double>(ws, w.inv_norm);
-  const int64_t* off = at<int64_t>(ws, w.off);
-  const double* term = at<double>(ws, w.term);
-  const float* rho = at<float>(ws, w.rho);
-  const float* zeroed = at<float>(ws, w.zeroed);
-  __shared__ double s_sum[1024];
-  __shared__ double s_z[1024], s_r[1024];
-  __shared__ float s_mn[1024], s_mx[1024];
-  const int tid = threadIdx.x;
-  double acc = 0.0, zc = 0.0, rs = 0.0;
-  float mn = FLT_MAX, mx = -FLT_MAX;
-  const int nm = me - mb;
-  for (int m = 0; m < nm; ++m) {
-    const double wgt = inv[mb + m] * (double)G;  // 1 / R_i
-    for (int64_t t = off[m] + tid; t < off[m + 1]; t += blockDim.x) acc += term[t] * wgt;
-  }
-  for (int64_t t = tid; t < T; t += blockDim.x) {
-    zc += zeroed[t];
-    rs += rho[t];
-    mn = fminf(mn, rho[t]);
-    mx = fmaxf(mx, rho[t]);
-  }
-  s_sum[tid] = acc; s_z[tid] = zc; s_r[tid] = rs; s_mn[tid] = mn; s_mx[tid] = mx;
-  __syncthreads();
-  for (int s = blockDim.x / 2; s > 0; s >>= 1) {
-    if (tid < s) {
-      s_sum[tid] += s_sum[tid + s];
-      s_z[tid] += s_z[tid + s];
-      s_r[tid] += s_r[tid + s];
-      s_mn[tid] = fminf(s_mn[tid], s_mn[tid + s]);
-      s_mx[tid] = fmaxf(s_mx[tid], s_mx[tid + s]);
-    }
-    __syncthreads();
-  }
-  if (tid == 0) {
-    const float contrib = (float)(-s_sum[0] / (double)G);
-    loss[0] = accumulate ? loss[0] + contrib : contrib;
-    if (stats) {
-      stats[0] = (float)s_z[0];
-      stats[1] = (float)s_r[0];
-      stats[2] = T > 0 ? s_mn[0] : 0.f;
-      stats[3] = T > 0 ? s_mx[0] : 0.f;
-    }
-  }
+  __shared__ double sh[32 * 3];
+  __shared__ float shf[32 * 2];
+  grpo_reduce<1024>(ws, T, G, mb, me, accumulate, loss, stats, threadIdx.x, sh, shf,
+                    [] { __syncthreads(); });
 }
 
 }  // namespace
@@ -846,6 +930,9 @@ StreamArgs loss_stream_args(const LsGrpoArgs& a) {
   sa.ws = a.workspace;
   sa.logp_out = a.logp_out;
   sa.err = a.err;
+  sa.accumulate = a.accumulate_loss;
+  sa.loss = a.loss;
+  sa.stats = a.stats;
   return sa;
 }
 }  // namespace
@@ -857,7 +944,7 @@ cudaError_t ls_launch_grpo(const LsGrpoArgs& a, int num_sms, cudaStream_t st) {
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (a.T > 0 && launch_stream<true>(loss_stream_args(a), a.is_bf16, num_sms, st, &e)) {
-    if (e != cudaSuccess) return e;
+    return e;  // the streamed kernel's last CTA has reduced the loss
   } else if (a.T > 0) {
     int64_t grid = (int64_t)num_sms * 2;
     if (grid > a.T) grid = a.T;
