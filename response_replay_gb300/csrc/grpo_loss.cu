@@ -7,18 +7,24 @@
 // Gradient: dL/dz_v = c_t (1[v == target] - softmax_v), c_t = -A_i rho / (G R_i) when
 // the unclipped term is the active minimum, 0 when the clip holds the term constant.
 //
-// Three launches:
-//   grpo_prep   1 block : advantages in fp64 (mean/std about the first reward), member
-//                         token offsets, 1/(G R_i); checks that lengths cover T.
+// Launches:
+//   grpo_prep   1 warp  : advantages in fp64 (mean/std about the first reward), member
+//                         token offsets, 1/(G R_i); checks that lengths cover T; zeroes
+//                         the row kernel's ticket.
 //   row kernel  grid    : pass 1 reduces a token row (online max / sum-exp) and gathers
 //                         z_target; pass 2 writes dlogits, or zeros without reading the
 //                         row when c_t = 0.  HBM: V*b read + V*b written per token, the
-//                         algorithmic floor (pass 2 re-reads the row from L2).  Two forms:
+//                         algorithmic floor.  Two forms:
 //     grpo_stream        one CTA per SM, rows streamed through a shared-memory ring by
-//                        bulk copies; used when a row is a whole number of 16-byte units.
-//     grpo_rows          one CTA per row at a time, plain 16-byte loads; any V.
-//   grpo_final  1 block : fixed-order fp64 reduction of the per-token terms -> loss,
-//                         stats.  No floating-point atomics: results are deterministic.
+//                        bulk copies, the row's last chunks kept for pass 2; its last
+//                        CTA to finish (ticket) also reduces the loss.  Used when a row
+//                        is a whole number of 16-byte units.
+//     grpo_rows          one CTA per row at a time, plain 16-byte loads, pass 2
+//                        re-reading the row mostly from L2; any V.
+//   grpo_final  1 block : the loss reduction as its own launch, after grpo_rows (or
+//                         when T = 0).
+// The reduction is a fixed-order fp64 sum of the per-token terms (no floating-point
+// atomics), so results are deterministic.
 #include <float.h>
 
 #include "ls_device.cuh"
