@@ -30,6 +30,29 @@
  *
  * Return codes: 0 ok, 1 invalid argument (sizes, a page id outside the pool, a page
  * index beyond the table), 2 out of memory.
+ *
+ * Pins (each function is checked against something other than itself; the pages print
+ * no numeric values for this path, so none comes from them):
+ *   lso_capture_kv          byte-exact scatter, untouched sentinel pages, gather back =
+ *                           input, out-of-table positions rejected
+ *   lso_attn_fwd            brute-force monolithic softmax on tiny inputs for every split
+ *                           count; q = 0 closed form (mean of visible V, lse =
+ *                           log(P + t + 1)); P = 0 equals a library causal attention;
+ *                           R = 1 equals single-query decode; one page with the identity
+ *                           table equals shuffled pages; a hand-worked fixture
+ *   lso_attn_fwd_rows       equals lso_attn_fwd on the sampled rows
+ *   lso_attn_bwd            central finite differences of <dO, O>; P = 0 equals a library
+ *                           autograd of causal attention
+ *   lso_attn_bwd_dq_rows,
+ *   lso_attn_bwd_dkdv_keys  equal lso_attn_bwd on the sampled rows / keys
+ *   lso_grpo                a hand-worked fixture; equal rewards give exactly zero; ratio
+ *                           one gives the closed-form loss and coefficients; the clip
+ *                           on the favourable side zeroes the gradient; constant logits
+ *                           give lse = log V + c; the unclipped limit equals a library
+ *                           log-softmax; per-member calls add up to the whole range
+ *   lso_grpo_dlogits_row    central finite differences of the loss
+ *   lso_grpo_logp           a library log-softmax and the closed-form lse; the KL
+ *                           estimate's closed cases
  */
 #ifndef LONGSTRAW_ORACLE_H
 #define LONGSTRAW_ORACLE_H
