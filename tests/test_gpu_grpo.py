@@ -206,3 +206,21 @@ def test_grpo_logp_bad_target_reported(cuda):
     assert B.ls_last_device_error(0) == B.LS_ERR_DEVICE_CHECK
     lp = logp.cpu().numpy()
     assert np.isnan(lp[1]) and np.isnan(lp[3]) and np.isfinite(lp[[0, 2]]).all()
+
+
+@pytest.mark.parametrize("V,dtype", [(151936, "bf16"), (1001, "fp32")])
+def test_deterministic(cuda, V, dtype):
+    """Whichever CTA finishes last and reduces the loss, the sum runs in one fixed order:
+    repeated calls agree bit for bit (streamed kernel at V = 151,936 bf16, one-CTA-per-row
+    kernel at V = 1001)."""
+    lens = [300, 211, 97]
+    inp = syn.make_grpo(lens, V, dtype, "normal", 333, cuda, shift_frac=0.3)
+    lo = (torch.randn(sum(lens), device=cuda) * 0.05 - 12.0).contiguous()
+    outs = []
+    for _ in range(3):
+        loss, dlog, logp, stats = api.grpo_loss_fwd_bwd(inp.logits, inp.targets, lo, inp.rewards,
+                                                        inp.resp_lens, 0, 3, 0.2)
+        outs.append((loss.clone(), dlog.clone(), logp.clone(), stats.clone()))
+    for other in outs[1:]:
+        for a, b in zip(outs[0], other):
+            assert torch.equal(a, b)
