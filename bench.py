@@ -106,6 +106,25 @@ def whole_job_rate(units_per_rank_step: float, world: int, ms_per_step: float) -
     return units_per_rank_step * world / (ms_per_step * 1e-3)
 
 
+def cpu_model() -> str:
+    """The host CPU's model name (what the oracle baseline ran on), or "unknown"."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
 def rank_seed(base: int, rank: int) -> int:
     """Each rank replays its own independent problem, drawn from its own seed."""
     return base + 1000 * rank
@@ -576,6 +595,7 @@ def cpu_baseline_attention(cache, br, w, scale, budget_s: float):
         fl, dt = run(n2)
         n = n2
     return {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "cpu": cpu_model(),
             "sample": f"{n} random (t, h) rows of one member: fp64 forward + dQ over all "
                       f"{w.P} prompt keys and the causal response keys; {dt:.1f} s"}
 
@@ -720,6 +740,7 @@ def run_reference(args, rank: int, world: int):
         "data": "synthetic", "config": {"workload": "P=2,097,152, Hq=24, Hkv=4, d=128, R=4096 "
                                                     "(sampled rows)"},
         "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "cpu": cpu_model(),
                          "sample": f"{n} random (t, h) rows per step: fp64 forward + dQ over "
                                    f"the full prompt"},
         "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
