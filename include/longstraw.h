@@ -38,6 +38,11 @@
  *     ls_last_device_error() reports and clears it.
  *   - Determinism: no floating-point atomics; the same inputs and launch
  *     configuration give bit-identical outputs.
+ *   - Device reset: the library looks up the device addresses of its own device
+ *     variables (the error word, the no-alloc scratch) once per device and keeps them
+ *     for the life of the process.  cudaDeviceReset() unloads the library's device
+ *     image, so these addresses go stale: do not call the library on a device after
+ *     resetting it in the same process.
  */
 #ifndef LONGSTRAW_H
 #define LONGSTRAW_H

@@ -111,3 +111,11 @@ def test_argument_checks_reject_before_launch(lib):
     assert lib.ls_grpo_logp(258, 0, 4, 16, 256, None, 256, None, None, None) == \
         B.LS_ERR_INVALID_ARG
     assert B.status_string(B.LS_ERR_TIMEOUT)
+
+
+def test_noalloc_scratch_holds_its_largest_call(lib):
+    """The allocation-free GRPO entry point runs on a fixed 4.125 MiB array: the
+    workspace of its largest accepted call (262,144 tokens, 1,024 members) must fit."""
+    need = C.c_size_t(0)
+    assert lib.ls_grpo_workspace(262144, 1024, C.byref(need)) == 0
+    assert need.value <= (4 << 20) + (128 << 10)

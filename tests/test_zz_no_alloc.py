@@ -10,7 +10,8 @@ import numpy as np
 import pytest
 import torch
 
-from parity_util import TOL_DLOGITS, TOL_LOGP, loss_tolerance
+import oracle
+from parity_util import TOL_DLOGITS, TOL_LOGP, loss_tolerance, u16
 from response_replay_gb300 import binding as B
 from response_replay_gb300 import synthetic as syn
 from response_replay_gb300 import torch_api as api
@@ -55,6 +56,20 @@ def test_noalloc_matches_workspace_entry_point_twice(cuda, dtype, V):
         assert ((g - gr).abs().amax(dim=1) / scale).max().item() <= TOL_DLOGITS[dtype]
         assert torch.equal(stats[0], ref_stats[0])
         assert (stats[1:] - ref_stats[1:]).abs().max().item() <= 1e-4 * max(1.0, ref_stats[1].abs().item())
+        # and against the fp64 oracle directly
+        zl = u16(inp.logits) if dtype == "bf16" else inp.logits.cpu().numpy()
+        o = oracle.grpo(zl, inp.targets.cpu().numpy(), logp_old.cpu().numpy().astype(np.float64),
+                        inp.rewards.cpu().numpy(), np.array(lens), 0, 3, 0.2)
+        assert abs(loss.item() - o.loss) <= loss_tolerance(o.loss, o.adv)
+        assert np.abs(logp_n.cpu().numpy() - o.logp).max() <= TOL_LOGP
+        near = np.abs(np.abs(o.ratio - 1.0) - 0.2) < 1e-5
+        rows = [r for r in range(0, sum(lens), 7) if not near[r]]
+        g_ref = oracle.grpo_dlogits_rows(zl, rows, inp.targets.cpu().numpy(), o.lse, o.coef)
+        g_rows = dlog[rows].float().cpu().numpy()
+        for k in range(len(rows)):
+            s = np.abs(g_ref[k]).max()
+            err = np.abs(g_rows[k] - g_ref[k]).max() / s if s > 0 else np.abs(g_rows[k]).max()
+            assert err <= TOL_DLOGITS[dtype], rows[k]
 
 
 def test_noalloc_serial_member_accumulation(cuda):
@@ -79,13 +94,38 @@ def test_noalloc_serial_member_accumulation(cuda):
     assert abs(got.item() - ref.item()) <= loss_tolerance(ref.item(), np.ones(1)) + 1e-7
 
 
+def test_noalloc_largest_group(cuda):
+    """G = 1,024 members (the largest member tables the scratch holds), two tokens of a
+    few members in the call, against the workspace entry point."""
+    G = 1024
+    lens = torch.full((G,), 2, dtype=torch.int32, device=cuda)
+    mb, me = 1000, 1003
+    inp = syn.make_grpo([2] * (me - mb), 64, "fp32", "normal", 5, cuda)
+    rewards = torch.randn(G, generator=syn.gen(cuda, 6), device=cuda)
+    lo = inp.noise.contiguous()
+    ref_loss, ref_dlog, ref_logp, _ = api.grpo_loss_fwd_bwd(inp.logits, inp.targets, lo, rewards,
+                                                            lens, mb, me, 0.2)
+    big = syn.GrpoInputs(inp.logits, inp.targets, rewards, lens, inp.noise)
+    loss = torch.zeros(1, device=cuda)
+    dlog = torch.empty_like(inp.logits)
+    logp = torch.empty(inp.logits.shape[0], device=cuda)
+    stats = torch.empty(4, device=cuda)
+    _noalloc(big, lo, mb, me, 0.2, loss, dlog, logp, stats)
+    torch.cuda.synchronize()
+    assert B.ls_last_device_error(0) == B.LS_OK
+    assert abs(loss.item() - ref_loss.item()) <= loss_tolerance(ref_loss.item(), np.ones(1)) + 1e-9
+    assert torch.equal(logp, ref_logp)
+    assert (dlog - ref_dlog).abs().max().item() <= 1e-6 * ref_dlog.abs().max().item()
+
+
 def test_noalloc_rejects_sizes_beyond_its_scratch(cuda):
-    T = 262145
     logits = torch.empty((1, 8), dtype=torch.float32, device=cuda)  # never read
-    t = torch.zeros(1, dtype=torch.int32, device=cuda)
-    f = torch.zeros(4, device=cuda)
-    with pytest.raises(B.LongstrawError) as ei:
-        B.ls_grpo_loss_fwd_bwd_noalloc(logits.data_ptr(), B.LS_FP32, T, 8, t.data_ptr(),
-                                       f.data_ptr(), f.data_ptr(), t.data_ptr(), 2, 0, 2, 0.2,
-                                       1e-6, 1, 0, f.data_ptr(), logits.data_ptr(), None, None, 0)
-    assert ei.value.status == B.LS_ERR_WORKSPACE
+    t = torch.zeros(2048, dtype=torch.int32, device=cuda)
+    f = torch.zeros(2048, device=cuda)
+    for T, G in ((262145, 2), (2, 1025)):
+        with pytest.raises(B.LongstrawError) as ei:
+            B.ls_grpo_loss_fwd_bwd_noalloc(logits.data_ptr(), B.LS_FP32, T, 8, t.data_ptr(),
+                                           f.data_ptr(), f.data_ptr(), t.data_ptr(), G, 0, 2,
+                                           0.2, 1e-6, 1, 0, f.data_ptr(), logits.data_ptr(), None,
+                                           None, 0)
+        assert ei.value.status == B.LS_ERR_WORKSPACE
