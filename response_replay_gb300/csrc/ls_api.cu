@@ -148,15 +148,22 @@ FwdWs fwd_ws(const LsSched& sc, int unit_rows) {
 }
 
 struct BwdWs {
-  size_t delta, part_dq, total;
+  size_t delta, dt, lse2t, part_dq, part_dkdv, total;
 };
-BwdWs bwd_ws(const LsSched& sc, int unit_rows, int R, int Hq) {
+BwdWs bwd_ws(const LsSched& sc, int unit_rows, int R, int Hq, int Hkv, int sms) {
   BwdWs w;
   size_t p = 0;
+  const size_t rp = (size_t)(R + 127) / 128 * 128;
   w.delta = p;
   p = align256(p + (size_t)R * Hq * 4);
+  w.dt = p;
+  p = align256(p + rp * Hq * 4);
+  w.lse2t = p;
+  p = align256(p + rp * Hq * 4);
   w.part_dq = p;
   p = align256(p + (sc.has_partials() ? (size_t)sc.num_pieces() * unit_rows * kHeadDim * 4 : 0));
+  w.part_dkdv = p;
+  p = align256(p + ls_dkdv_part_bytes(R, Hq, Hkv, sms));
   w.total = p;
   return w;
 }
@@ -295,7 +302,7 @@ ls_status ls_replay_attn_bwd_workspace(const ls_kv_cache* cache, int R, int Hq, 
   if ((s = dev_info(&d)) != LS_OK) return s;
   const LsSched sc = make_sched(cache, R, Hq, num_splits, ls_bwd_unit_rows(), ls_bwd_tile(),
                                 d.sms * ls_bwd_ctas_per_sm(), false);
-  *bytes = bwd_ws(sc, ls_bwd_unit_rows(), R, Hq).total;
+  *bytes = bwd_ws(sc, ls_bwd_unit_rows(), R, Hq, cache->num_kv_heads, d.sms).total;
   return LS_OK;
 }
 
@@ -315,7 +322,7 @@ ls_status ls_replay_attn_bwd(const ls_kv_cache* cache, const void* q, const void
   if ((s = dev_info(&d)) != LS_OK) return s;
   const LsSched sc = make_sched(cache, R, Hq, num_splits, ls_bwd_unit_rows(), ls_bwd_tile(),
                                 d.sms * ls_bwd_ctas_per_sm(), false);
-  const BwdWs w = bwd_ws(sc, ls_bwd_unit_rows(), R, Hq);
+  const BwdWs w = bwd_ws(sc, ls_bwd_unit_rows(), R, Hq, cache->num_kv_heads, d.sms);
   if (!workspace || workspace_bytes < w.total || !aligned16(workspace)) return LS_ERR_WORKSPACE;
   LsAttnArgs a = attn_args(cache, q, k_resp, v_resp, R, Hq, softmax_scale, d.err);
   a.pack = ls_bwd_pack(R, Hq, cache->num_kv_heads);
@@ -324,7 +331,10 @@ ls_status ls_replay_attn_bwd(const ls_kv_cache* cache, const void* q, const void
   b.lse = lse;
   b.d_o = d_o;
   b.delta = reinterpret_cast<float*>(static_cast<char*>(workspace) + w.delta);
+  b.dt = reinterpret_cast<float*>(static_cast<char*>(workspace) + w.dt);
+  b.lse2t = reinterpret_cast<float*>(static_cast<char*>(workspace) + w.lse2t);
   b.part_dq = reinterpret_cast<float*>(static_cast<char*>(workspace) + w.part_dq);
+  b.part_dkdv = reinterpret_cast<float*>(static_cast<char*>(workspace) + w.part_dkdv);
   b.dq = dq;
   b.dk = dk_resp;
   b.dv = dv_resp;

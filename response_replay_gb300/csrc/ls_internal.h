@@ -51,10 +51,13 @@ struct LsBwdIn {
   const float* lse;          // [R][hq]
   const void* d_o;           // bf16 [R][hq][128]
   float* delta;              // workspace [R][hq]: D = <dO, O>
+  float* dt;                 // workspace [hq][rp]: D transposed, rp = R rounded up to 128
+  float* lse2t;              // workspace [hq][rp]: lse log2(e) transposed
   float* dq;                 // [R][hq][128]
   float* dk;                 // [R][hkv][128]
   float* dv;
   float* part_dq;            // workspace: [2*ctas][unit_rows][128]
+  float* part_dkdv;          // workspace: [2*ctas][2][128][128] (response-key kernel)
   int32_t accumulate;
 };
 
@@ -93,6 +96,11 @@ cudaError_t ls_launch_replay_fwd(const LsAttnArgs& a, const LsSched& sc, const L
 
 cudaError_t ls_launch_bwd_dq(const LsAttnArgs& a, const LsSched& sc, const LsBwdIn& b,
                              cudaStream_t st);
+
+// Response-key dK / dV (tcgen05) and the bytes of its partial-sum workspace.
+size_t ls_dkdv_part_bytes(int R, int hq, int hkv, int num_sms);
+cudaError_t ls_launch_bwd_dkdv(const LsAttnArgs& a, const LsBwdIn& b, int num_sms,
+                               cudaStream_t st);
 
 cudaError_t ls_launch_replay_bwd(const LsAttnArgs& a, const LsSched& sc, const LsBwdIn& b,
                                  int num_sms, cudaStream_t st);

@@ -6,13 +6,19 @@
 // tail pieces balance the work to within 2% of the best piece count.  A second check
 // walks the forward's tile cursor (ls_tiles.cuh) in its packed-members layout: every
 // unit visits exactly the response key tiles its members' rows can see (member by
-// member, each once), and the MMA issuer's flag walk sees the same tiles.
+// member, each once), and the MMA issuer's flag walk sees the same tiles.  A third
+// check walks the response-key backward's iteration ranges (ls_dkdv.h): every (KV head,
+// key tile, query head, query tile >= key tile) once, segments flagged first/last at
+// key-tile and range boundaries, "complete" exactly for key tiles one CTA holds whole,
+// every partial slot written once, the combine's slot list of each split key tile equal
+// to the slots written for it, and at most ceil(total / C) iterations per CTA.
 #include <cstdio>
 #include <cstdlib>
 #include <map>
 #include <set>
 #include <vector>
 
+#include "ls_dkdv.h"
 #include "ls_sched.h"
 #include "ls_tiles.cuh"
 
@@ -142,8 +148,81 @@ static int check_packed(int R, int members, int pack, int hkv, int nt, int sp, i
   return 0;
 }
 
+static int check_dkdv(int R, int g, int hkv, int C) {
+  const LsDkdvGeom gm = ls_make_dkdv_geom(R, g, hkv, C);
+  auto bad = [&](const char* what) {
+    std::printf("FAIL dkdv %s R=%d g=%d hkv=%d C=%d\n", what, R, g, hkv, C);
+    return 1;
+  };
+  if (gm.ctas > C || gm.ctas < (gm.total > 0 ? 1 : 0)) return bad("grid");
+  const int nT = gm.nT;
+  std::map<std::vector<int>, int> seen;                // (kvh, kt, h, tt) -> count
+  std::map<std::pair<int, int>, std::vector<int>> written;  // key tile -> slots (cta order)
+  std::map<std::pair<int, int>, int> complete_by;
+  std::set<int> slots;
+  for (int b = 0; b < gm.ctas; ++b) {
+    LsDkdvWalk w(gm, b);
+    LsDkdvIter it;
+    int n = 0;
+    bool open = false;
+    int ckvh = -1, ckt = -1;
+    while (w.next(&it)) {
+      ++n;
+      if (it.tt < it.kt || it.tt >= nT || it.h / g != it.kvh) return bad("iteration");
+      if (++seen[{it.kvh, it.kt, it.h, it.tt}] != 1) return bad("visited twice");
+      const bool new_tile = it.kvh != ckvh || it.kt != ckt;
+      if (it.first != new_tile) return bad("first flag");
+      if (new_tile && open) return bad("segment not closed");
+      open = true;
+      ckvh = it.kvh;
+      ckt = it.kt;
+      if (it.last) {
+        open = false;
+        const auto key = std::make_pair(it.kvh, it.kt);
+        if (it.complete) {
+          if (complete_by.count(key) || written.count(key)) return bad("complete twice");
+          complete_by[key] = b;
+        } else {
+          if (it.slot != 2 * b && it.slot != 2 * b + 1) return bad("slot range");
+          if (!slots.insert(it.slot).second) return bad("slot reused");
+          written[key].push_back(it.slot);
+        }
+      }
+    }
+    if (open) return bad("range ends inside a segment");
+    if (n > gm.per_cta) return bad("balance");
+  }
+  const long long want = (long long)hkv * g * nT * (nT + 1) / 2;
+  if ((long long)seen.size() != want) return bad("coverage");
+  // the combine's view of each split key tile
+  for (int c = 0; c < hkv; ++c)
+    for (int kt = 0; kt < nT; ++kt) {
+      const auto key = std::make_pair(c, kt);
+      const long long s = gm.tile_begin(c, kt), e = s + gm.tile_iters(kt);
+      const int b0 = (int)(s / gm.per_cta), b1 = (int)((e - 1) / gm.per_cta);
+      if (b0 == b1) {
+        if (!complete_by.count(key) || complete_by[key] != b0) return bad("complete owner");
+        continue;
+      }
+      std::vector<int> expect;
+      for (int b = b0; b <= b1; ++b) expect.push_back(gm.slot(b, s));
+      if (written[key] != expect) return bad("combine slots");
+    }
+  return 0;
+}
+
 int main() {
   int bad = 0, n = 0;
+  int dn = 0, dbad = 0;
+  for (int R : {1, 100, 128, 129, 1000, 4096, 8192})
+    for (int g : {1, 6, 8})
+      for (int hkv : {1, 4})
+        for (int C : {1, 3, 148, 152}) {
+          dbad += check_dkdv(R, g, hkv, C);
+          ++dn;
+        }
+  std::printf("%d/%d response-key walks ok\n", dn - dbad, dn);
+  bad += dbad;
   const int Us[] = {1, 2, 3, 7, 8, 96, 151, 152, 153, 304, 384, 768, 1000};
   const int nts[] = {0, 1, 2, 5, 32, 64, 257, 16384};
   const int sps[] = {1, 2, 3, 4, 32, 256, 1000};
@@ -173,6 +252,6 @@ int main() {
             }
   bad += pbad;
   std::printf("%d/%d packed-member walks ok\n", pn - pbad, pn);
-  std::printf("%d/%d schedules ok\n", n - bad + pbad, n);
+  std::printf("%d/%d schedules ok\n", n - bad + pbad + dbad, n);
   return bad ? 1 : 0;
 }
