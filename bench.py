@@ -203,8 +203,8 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     w = syn.WORKLOADS[args.workload]
-    G = w.G if args.members is None else args.members
-    R = w.R[0]
+    C = w.cycles                   # replay cycles over one capture (8 on p4m_reuse)
+    G = w.G if args.members is None else args.members   # members replayed per cycle
     seed = rank_seed(syn.seed_of(args.workload), rank)
     scale = D ** -0.5
     stream = torch.cuda.current_stream()
@@ -212,68 +212,83 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     # ---- resident inputs
     pr = syn.make_prompt(w.P, w.hkv, D, w.page_size, seed, dev)
     cache = api.PagedKVCache(pr.num_pages, pr.page_table, w.page_size, w.hkv, w.P, device=dev)
-    branches = [syn.make_branch(R, w.hq, w.hkv, D, seed + 1 + i, dev) for i in range(G)]
-    lens = list(w.R[:G])
-    gin = syn.make_grpo(lens, w.vocab, w.logits_dtype, w.rewards, seed, dev, shift_frac=w.shift_frac)
-    if G < w.G:
-        # fewer members replayed (profiling): the loss still sees the whole group
-        gin.rewards = torch.from_numpy(
-            syn.draw_rewards(w.rewards, w.G, np.random.default_rng(seed))).to(dev)
-        gin.resp_lens = torch.tensor(list(w.R), dtype=torch.int32, device=dev)
-    T = sum(lens)
-    off = [0]
-    for n in lens:
-        off.append(off[-1] + n)
-    # logp_old = logp + noise: logp from one untimed call of the library itself
-    logp = torch.empty(T, dtype=torch.float32, device=dev)
-    zero = torch.zeros(T, dtype=torch.float32, device=dev)
-    for i in range(G):
-        api.grpo_loss_fwd_bwd(gin.logits[off[i]:off[i + 1]], gin.targets[off[i]:off[i + 1]],
-                              zero[off[i]:off[i + 1]], gin.rewards, gin.resp_lens, i, i + 1, 0.2,
-                              logp_out=logp[off[i]:off[i + 1]],
-                              dlogits=torch.empty_like(gin.logits[off[i]:off[i + 1]]))
-    logp_old = (logp + gin.noise).contiguous()
-    del zero
-    o = torch.empty((R, w.hq, D), dtype=torch.bfloat16, device=dev)
-    lse = torch.empty((R, w.hq), dtype=torch.float32, device=dev)
-    dq = torch.zeros((R, w.hq, D), dtype=torch.float32, device=dev)
-    dk = torch.zeros((R, w.hkv, D), dtype=torch.float32, device=dev)
-    dv = torch.zeros((R, w.hkv, D), dtype=torch.float32, device=dev)
-    dlog = torch.empty((R, w.vocab), dtype=gin.logits.dtype, device=dev)
+    group_lens = [list(w.R[c * w.G:(c + 1) * w.G]) for c in range(C)]  # whole groups
+    replays = [(c, i) for c in range(C) for i in range(G)]
+    Rs = {(c, i): group_lens[c][i] for c, i in replays}
+    Rmax = max(Rs.values())
+    branches = {(c, i): syn.make_branch(Rs[c, i], w.hq, w.hkv, D, seed + 1 + c * w.G + i, dev)
+                for c, i in replays}
+    gins, offs, logp_olds = [], [], []
+    for c in range(C):
+        lens = group_lens[c][:G]
+        gin = syn.make_grpo(lens, w.vocab, w.logits_dtype, w.rewards, seed + 7919 * c, dev,
+                            shift_frac=w.shift_frac)
+        if G < w.G:
+            # fewer members replayed (profiling): the loss still sees the whole group
+            gin.rewards = torch.from_numpy(syn.draw_rewards(
+                w.rewards, w.G, np.random.default_rng(seed + 7919 * c))).to(dev)
+            gin.resp_lens = torch.tensor(group_lens[c], dtype=torch.int32, device=dev)
+        off = [0]
+        for n in lens:
+            off.append(off[-1] + n)
+        # logp_old = logp + noise: logp from one untimed call of the library itself
+        logp = torch.empty(off[-1], dtype=torch.float32, device=dev)
+        zero = torch.zeros(off[-1], dtype=torch.float32, device=dev)
+        for i in range(G):
+            api.grpo_loss_fwd_bwd(gin.logits[off[i]:off[i + 1]], gin.targets[off[i]:off[i + 1]],
+                                  zero[off[i]:off[i + 1]], gin.rewards, gin.resp_lens, i, i + 1,
+                                  0.2, logp_out=logp[off[i]:off[i + 1]],
+                                  dlogits=torch.empty_like(gin.logits[off[i]:off[i + 1]]))
+        logp_olds.append((logp + gin.noise).contiguous())
+        gins.append(gin)
+        offs.append(off)
+        del zero
+    T_step = sum(o_[-1] for o_ in offs)
+    o = torch.empty((Rmax, w.hq, D), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((Rmax, w.hq), dtype=torch.float32, device=dev)
+    dq = torch.zeros((Rmax, w.hq, D), dtype=torch.float32, device=dev)
+    dk = torch.zeros((Rmax, w.hkv, D), dtype=torch.float32, device=dev)
+    dv = torch.zeros((Rmax, w.hkv, D), dtype=torch.float32, device=dev)
+    dlog = torch.empty((Rmax, w.vocab), dtype=gins[0].logits.dtype, device=dev)
     loss = torch.zeros(1, dtype=torch.float32, device=dev)
     stats = torch.empty(4, dtype=torch.float32, device=dev)
-    lp_out = torch.empty(T, dtype=torch.float32, device=dev)
+    lp_out = torch.empty(max(o_[-1] for o_ in offs), dtype=torch.float32, device=dev)
 
     def ev():
         e = torch.cuda.Event(enable_timing=True)
         e.record(stream)
         return e
 
-    def member(i, m=None, before_loss=None, inp=None):
-        """One member's replay: forward, GRPO loss (accumulating), backward.  inp: another
-        set of device input buffers (the e2e double buffer); default the resident one."""
+    def member(c, i, m=None, before_loss=None, inp=None):
+        """One replay (member i of cycle c): forward, GRPO loss (accumulating), backward
+        with gradient accumulation.  inp: another set of device input buffers (the e2e
+        double buffer); default the resident one."""
+        R = Rs[c, i]
         if inp is None:
-            br = branches[i]
+            br = branches[c, i]
             q, kr, vr, d_o = br.q, br.k, br.v, br.d_o
-            logits, targets, lpo = gin.logits, gin.targets, logp_old
+            gin = gins[c]
+            logits, targets, lpo = gin.logits, gin.targets, logp_olds[c]
             rewards, lens = gin.rewards, gin.resp_lens
         else:
             q, kr, vr, d_o = inp.br[i]
             logits, targets, lpo, rewards, lens = (inp.logits, inp.targets, inp.logp_old,
                                                    inp.rewards, inp.lens)
-        api.replay_fwd(cache, q, kr, vr, scale, w.num_splits, o=o, lse=lse, stream=stream)
+        first = c == 0 and i == 0
+        api.replay_fwd(cache, q, kr, vr, scale, w.num_splits, o=o[:R], lse=lse[:R],
+                       stream=stream)
         if m is not None:
             m.append(ev())
         if before_loss is not None:
             before_loss()
-        s, e = off[i], off[i + 1]
+        s, e = offs[c][i], offs[c][i + 1]
         api.grpo_loss_fwd_bwd(logits[s:e], targets[s:e], lpo[s:e], rewards, lens, i, i + 1, 0.2,
-                              loss=loss, accumulate=i > 0, dlogits=dlog[: e - s],
+                              loss=loss, accumulate=not first, dlogits=dlog[: e - s],
                               logp_out=lp_out[s:e], stats=stats, stream=stream)
         if m is not None:
             m.append(ev())
-        api.replay_bwd(cache, q, kr, vr, o, lse, d_o, scale, w.num_splits, dq=dq, dk=dk, dv=dv,
-                       accumulate=i > 0, stream=stream)
+        api.replay_bwd(cache, q, kr, vr, o[:R], lse[:R], d_o, scale, w.num_splits, dq=dq[:R],
+                       dk=dk[:R], dv=dv[:R], accumulate=not first, stream=stream)
         if m is not None:
             m.append(ev())
 
@@ -282,8 +297,8 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         cache.capture(pr.k, pr.v, 0, stream)
         if m is not None:
             m.append(ev())
-        for i in range(G):
-            member(i, m)
+        for c, i in replays:
+            member(c, i, m)
         return m
 
     # kernel launches of one step, as counted by the library itself
@@ -314,47 +329,58 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     assert torch.isfinite(loss).all() and torch.isfinite(dq).all()
 
     cap_ms = fwd_ms = grpo_ms = bwd_ms = 0.0
+    n_rep = len(replays)
     for m in marks_all:
         cap_ms += m[0].elapsed_time(m[1])
-        for i in range(G):
-            a = 1 + 3 * i
+        for r in range(n_rep):
+            a = 1 + 3 * r
             fwd_ms += m[a].elapsed_time(m[a + 1])
             grpo_ms += m[a + 1].elapsed_time(m[a + 2])
             bwd_ms += m[a + 2].elapsed_time(m[a + 3])
     K = args.steps
-    f_fwd, f_bwd = attn_flops(w.P, R, w.hq)
-    step_flops = G * (f_fwd + f_bwd)
+    flops = [attn_flops(w.P, Rs[r], w.hq) for r in replays]
+    f_fwd = sum(f for f, _ in flops)     # per step, all replays
+    f_bwd = sum(b for _, b in flops)
+    step_flops = f_fwd + f_bwd
     ms_per_step = total_ms / K
     value = whole_job_rate(step_flops, world, ms_per_step) / 1e12
     kv_bytes = prompt_kv_bytes(w.P, w.hkv)
     comps = {
-        "attn_fwd_tflops": G * K * f_fwd / (fwd_ms * 1e-3) / 1e12,
-        "attn_bwd_tflops": G * K * f_bwd / (bwd_ms * 1e-3) / 1e12,
-        "prompt_kv_gbs": 2 * G * K * kv_bytes / ((fwd_ms + bwd_ms) * 1e-3) / 1e9,
-        "grpo_tokens_per_s": T * K / (grpo_ms * 1e-3),
+        "attn_fwd_tflops": K * f_fwd / (fwd_ms * 1e-3) / 1e12,
+        "attn_bwd_tflops": K * f_bwd / (bwd_ms * 1e-3) / 1e12,
+        "prompt_kv_gbs": 2 * n_rep * K * kv_bytes / ((fwd_ms + bwd_ms) * 1e-3) / 1e9,
+        "grpo_tokens_per_s": T_step * K / (grpo_ms * 1e-3),
         "capture_gbs": 2 * kv_bytes * K / (cap_ms * 1e-3) / 1e9,
-        "ms_capture": cap_ms / K, "ms_fwd_per_member": fwd_ms / (K * G),
-        "ms_grpo_per_member": grpo_ms / (K * G), "ms_bwd_per_member": bwd_ms / (K * G),
+        "ms_capture": cap_ms / K, "ms_fwd_per_member": fwd_ms / (K * n_rep),
+        "ms_grpo_per_member": grpo_ms / (K * n_rep), "ms_bwd_per_member": bwd_ms / (K * n_rep),
     }
     pk, pk_src = peaks()
     peak = pk.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
-    # dominant launch: the larger of the per-member backward and forward calls
+    # dominant call: the backward or the forward, whichever takes longer over the step;
+    # achieved = its algorithmic FLOPs over all replays / its summed CUDA-event time
     if bwd_ms >= fwd_ms:
-        dom, dom_flops, dom_ms, kfile, kname = "replay_attn_bwd", f_bwd, bwd_ms / (K * G), \
+        dom, dom_flops, dom_ms, kfile, kname = "replay_attn_bwd", f_bwd, bwd_ms / K, \
             "replay_bwd_dq_tc.cu", "bwd_dq_tc_kernel"
     else:
-        dom, dom_flops, dom_ms, kfile, kname = "replay_attn_fwd", f_fwd, fwd_ms / (K * G), \
+        dom, dom_flops, dom_ms, kfile, kname = "replay_attn_fwd", f_fwd, fwd_ms / K, \
             "replay_fwd_tc.cu", "replay_fwd_tc_kernel"
     achieved = dom_flops / (dom_ms * 1e-3) / 1e12
-    roofline = {"bound": "tensor", "kernel": kname, "timed": f"{dom} call (CUDA events)",
+    roofline = {"bound": "tensor", "kernel": kname, "timed": f"{dom} calls (CUDA events)",
                 "achieved": achieved, "peak": peak, "peak_source": f"{pk_src} bf16 sustained",
                 "unit": "TFLOP/s", "frac": achieved / peak,
-                "traffic": traffic_from_profile(kfile, kname)}
+                "traffic": traffic_from_profile(kfile, kname) if args.workload == WORKLOAD
+                else None}
 
     # ---- e2e: the same step through the public API with inputs copied in from pinned
     # host memory every step and the loss read back
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and C > 1:
+        e2e = {"value": None, "unit": "TFLOP/s", "skipped": "multi-cycle workload: its "
+               f"{C} cycles' logits alone are {sum(g_.logits.numel() for g_ in gins) * 2 / 1e9:.0f} "
+               "GB of pinned host memory per input set"}
+    if not args.no_e2e and C == 1:
+        gin, logp_old, off = gins[0], logp_olds[0], offs[0]
+        branch_list = [branches[0, i] for i in range(G)]
         host = {}
 
         def pin(t):
@@ -363,7 +389,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
             return h
 
         host["k"], host["v"] = pin(pr.k), pin(pr.v)
-        host["br"] = [(pin(b.q), pin(b.k), pin(b.v), pin(b.d_o)) for b in branches]
+        host["br"] = [(pin(b.q), pin(b.k), pin(b.v), pin(b.d_o)) for b in branch_list]
         host["logits"] = pin(gin.logits)
         host["targets"], host["logp_old"] = pin(gin.targets), pin(logp_old)
         host["rewards"], host["lens"] = pin(gin.rewards), pin(gin.resp_lens)
@@ -392,7 +418,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                 self.logits, self.targets, self.logp_old = logits, targets, lpo
                 self.rewards, self.lens = rewards, lens
 
-        sets = [InputSet(pr.k, pr.v, [(b.q, b.k, b.v, b.d_o) for b in branches], gin.logits,
+        sets = [InputSet(pr.k, pr.v, [(b.q, b.k, b.v, b.d_o) for b in branch_list], gin.logits,
                          gin.targets, logp_old, gin.rewards, gin.resp_lens)]
         el = torch.empty_like
         sets.append(InputSet(el(pr.k), el(pr.v), [tuple(el(x) for x in t) for t in sets[0].br],
@@ -454,7 +480,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                 # prompt); the loss also waits for its logits rows, whose events follow
                 # the rewards and lengths copied first on copy stream 0
                 stream.wait_event(br_ev[i])
-                member(i, before_loss=lambda i=i: [stream.wait_event(e) for e in lg_ev[i]],
+                member(0, i, before_loss=lambda i=i: [stream.wait_event(e) for e in lg_ev[i]],
                        inp=src)
             loss_h.copy_(loss, non_blocking=True)
             return mark(stream)
@@ -483,8 +509,9 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     # ---- pre-step scoring (outside the step): log-softmax gather of one member's tokens
     # with the KL estimate against reference log-probabilities; HBM-bound, V*b read per
     # token
+    gin, off = gins[0], offs[0]
     s0, s1 = off[0], off[1]
-    ref_lp = logp_old[s0:s1]
+    ref_lp = logp_olds[0][s0:s1]
     api.grpo_logp(gin.logits[s0:s1], gin.targets[s0:s1], ref_lp, stream=stream)
     torch.cuda.synchronize()
     # hold the stream for a few ms so that all K calls are queued before the first
@@ -539,18 +566,25 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     # ---- CPU baseline: the oracle on a bounded sample of the same workload
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline_attention(cache, branches[0], w, scale, budget_s=args.cpu_budget)
+        cpu = cpu_baseline_attention(cache, branches[0, 0], w, scale, budget_s=args.cpu_budget)
 
+    rl = sorted(Rs.values())
+    if C == 1 and rl[0] == rl[-1]:
+        replay_desc = f"G={G} serial replays R={rl[0]}"
+    else:
+        replay_desc = (f"one capture, {C} cycles x G={G} serial replays ({n_rep}), ragged R in "
+                       f"[{rl[0]}, {rl[-1]}] (mean {sum(rl) / len(rl):.0f})")
     out = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic (seeded; shapes of the pages' 2,097,152-position runs)",
+        "data": "synthetic (seeded; shapes of the pages' "
+                + ("4,456,448-position prefix-reuse runs)" if C > 1 else "2,097,152-position runs)"),
         "config": {"workload": f"{args.workload}: P={w.P:,} prompt positions, Hq={w.hq}, "
                                f"Hkv={w.hkv}, d=128, {w.page_size}-token pages shuffled, "
-                               f"{w.num_splits} KV splits; G={G} serial replays R={R}; GRPO "
+                               f"{w.num_splits} KV splits; " + replay_desc + "; GRPO "
                                f"V={w.vocab:,} {w.logits_dtype} logits",
-                   "members": G,
+                   "members": n_rep,
                    "l2": f"inputs larger than L2 (prompt KV {prompt_kv_bytes(w.P, w.hkv)/1e9:.2f} "
                          f"GB per pass)"},
         "components": comps, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
@@ -688,6 +722,66 @@ def run_short_sweep(args, local_rank: int):
         }), flush=True)
 
 
+# ------------------------------------------------------------------ self-attention sweep
+
+def run_self_sweep(args, local_rank: int):
+    """Supplementary, labelled lines (not the headline): replay with no prompt (P = 0),
+    i.e. plain causal attention of a long response, where the response-key part of the
+    backward (dK/dV over the causal triangle) is about half the backward's work.  One
+    JSON line per R with forward and backward time and algorithmic TFLOP/s."""
+    import torch
+
+    from response_replay_gb300 import synthetic as syn
+    from response_replay_gb300 import torch_api as api
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    hq, hkv, ps = 24, 4, 256
+    pr = syn.make_prompt(1, hkv, D, ps, 11, dev)
+    cache = api.PagedKVCache(pr.num_pages, pr.page_table[:0], ps, hkv, 0, device=dev)
+    pk, _ = peaks()
+    stream = torch.cuda.current_stream()
+    scale = D ** -0.5
+    for R in [int(x) for x in args.sweep_self.split(",")]:
+        br = syn.make_branch(R, hq, hkv, D, 12, dev, sharp=True)
+        o = torch.empty((R, hq, D), dtype=torch.bfloat16, device=dev)
+        lse = torch.empty((R, hq), dtype=torch.float32, device=dev)
+        dq = torch.empty((R, hq, D), dtype=torch.float32, device=dev)
+        dk = torch.empty((R, hkv, D), dtype=torch.float32, device=dev)
+        dv = torch.empty((R, hkv, D), dtype=torch.float32, device=dev)
+
+        def fwd():
+            api.replay_fwd(cache, br.q, br.k, br.v, scale, 1, o=o, lse=lse, stream=stream)
+
+        def bwd():
+            api.replay_bwd(cache, br.q, br.k, br.v, o, lse, br.d_o, scale, 1, dq=dq, dk=dk,
+                           dv=dv, stream=stream)
+
+        def timed(fn):
+            for _ in range(args.warmup):
+                fn()
+            torch.cuda.synchronize()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for _ in range(args.steps):
+                fn()
+            b.record(stream)
+            torch.cuda.synchronize()
+            return a.elapsed_time(b) / args.steps
+
+        f_ms, b_ms = timed(fwd), timed(bwd)
+        f_fl, b_fl = attn_flops(0, R, hq)
+        print(json.dumps({
+            "sweep": "causal self-attention of one response, no prompt (supplementary)",
+            "R": R, "config": {"workload": f"P=0, R={R}, Hq={hq}, Hkv={hkv}, d=128"},
+            "fwd_ms": f_ms, "bwd_ms": b_ms,
+            "fwd_tflops": f_fl / (f_ms * 1e-3) / 1e12, "bwd_tflops": b_fl / (b_ms * 1e-3) / 1e12,
+            "bf16_tflops_burst": pk.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]),
+            "steps": args.steps, "warmup": args.warmup,
+        }), flush=True)
+
+
 # ------------------------------------------------------------------ reference arm
 
 def run_reference(args, rank: int, world: int):
@@ -760,6 +854,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--ref-rows-per-core", type=int, default=2)
+    ap.add_argument("--sweep-self", default=None,
+                    help="comma-separated response lengths: supplementary no-prompt (causal "
+                         "self-attention) lines instead of the headline step")
     ap.add_argument("--sweep-short", default=None,
                     help="comma-separated response lengths: supplementary short-R sweep "
                          "(one JSON line each) instead of the headline step")
@@ -775,6 +872,10 @@ def main():
     if args.sweep_short:
         if rank == 0:
             run_short_sweep(args, local_rank)
+        return
+    if args.sweep_self:
+        if rank == 0:
+            run_self_sweep(args, local_rank)
         return
     if world > 1:
         import torch
