@@ -532,8 +532,8 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     # captured prompt, one batched launch (the members' tokens packed into shared tiles)
     # against G one-member launches.  Short responses are HBM-bound one by one; batched,
     # each prompt K/V tile serves every member's rows of its KV head at once.
-    for Rs in (2, 16):
-        sbr = [syn.make_branch(Rs, w.hq, w.hkv, D, seed + 101 + i, dev) for i in range(w.G)]
+    for Rsc in (2, 16):
+        sbr = [syn.make_branch(Rsc, w.hq, w.hkv, D, seed + 101 + i, dev) for i in range(w.G)]
         sq = torch.stack([b.q for b in sbr]).contiguous()
         sk = torch.stack([b.k for b in sbr]).contiguous()
         sv = torch.stack([b.v for b in sbr]).contiguous()
@@ -558,9 +558,9 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                 fn()
             eb = ev()
             torch.cuda.synchronize()
-            comps[f"prestep_fwd_{w.G}x{Rs}_{name}_ms"] = ea.elapsed_time(eb) / K
-        comps[f"prestep_fwd_{w.G}x{Rs}_batched_kv_hbm_frac"] = kv_bytes / (
-            comps[f"prestep_fwd_{w.G}x{Rs}_batched_ms"] * 1e-3) / 1e9 / pk.get(
+            comps[f"prestep_fwd_{w.G}x{Rsc}_{name}_ms"] = ea.elapsed_time(eb) / K
+        comps[f"prestep_fwd_{w.G}x{Rsc}_batched_kv_hbm_frac"] = kv_bytes / (
+            comps[f"prestep_fwd_{w.G}x{Rsc}_batched_ms"] * 1e-3) / 1e9 / pk.get(
             "hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
 
     # ---- CPU baseline: the oracle on a bounded sample of the same workload
