@@ -28,7 +28,10 @@
  *   - Layouts: dense row-major, innermost dimension last, no padding.  bf16 is the
  *     upper half of an IEEE-754 binary32 (1 sign, 8 exponent, 7 fraction bits);
  *     fp32 is binary32.
- *   - Alignment: every device pointer must be 16-byte aligned.
+ *   - Alignment: every device pointer must be 16-byte aligned, except the per-token
+ *     arrays of the loss and scoring calls (targets, logp_old, ref_logp, logp_out,
+ *     lse_out, kl_out), which need 4 bytes, so that a member's slice of a token-major
+ *     buffer can be passed whatever its token offset.
  *   - Errors: arguments are checked on the host first; on failure the call returns
  *     LS_ERR_INVALID_ARG / LS_ERR_UNSUPPORTED / LS_ERR_WORKSPACE and launches
  *     nothing.  A failed launch returns LS_ERR_CUDA.  Conditions only the device can

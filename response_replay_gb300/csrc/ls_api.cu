@@ -50,6 +50,9 @@ ls_status dev_info(DevInfo* out) {
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+// Per-token arrays of the loss and scoring calls are read and written one element at a
+// time, so a member's slice of a token-major buffer (any token offset) is accepted.
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3) == 0; }
 
 int ilog2_exact(int x) {
   if (x <= 0 || (x & (x - 1))) return -1;
@@ -363,10 +366,13 @@ ls_status ls_grpo_loss_fwd_bwd(const void* logits, ls_dtype dtype, int64_t T, in
       !aligned16(loss))
     return LS_ERR_INVALID_ARG;
   if (T > 0) {
-    const void* ptrs[] = {logits, targets, logp_old, dlogits};
-    for (const void* p : ptrs)
+    const void* rows[] = {logits, dlogits};
+    for (const void* p : rows)
       if (!p || !aligned16(p)) return LS_ERR_INVALID_ARG;
-    if (logp_out && !aligned16(logp_out)) return LS_ERR_INVALID_ARG;
+    const void* tok[] = {targets, logp_old};
+    for (const void* p : tok)
+      if (!p || !aligned4(p)) return LS_ERR_INVALID_ARG;
+    if (logp_out && !aligned4(logp_out)) return LS_ERR_INVALID_ARG;
   }
   if (stats && !aligned16(stats)) return LS_ERR_INVALID_ARG;
   const size_t need = ls_grpo_ws_bytes(T, G);
@@ -430,12 +436,13 @@ ls_status ls_grpo_logp(const void* logits, ls_dtype dtype, int64_t T, int V,
   if (T < 0 || V <= 0 || V > (1 << 30)) return LS_ERR_INVALID_ARG;
   if (kl_out && !ref_logp) return LS_ERR_INVALID_ARG;
   if (T > 0) {
-    const void* ptrs[] = {logits, targets, logp_out};
+    if (!logits || !aligned16(logits)) return LS_ERR_INVALID_ARG;
+    const void* ptrs[] = {targets, logp_out};
     for (const void* p : ptrs)
-      if (!p || !aligned16(p)) return LS_ERR_INVALID_ARG;
+      if (!p || !aligned4(p)) return LS_ERR_INVALID_ARG;
     const void* opt[] = {ref_logp, lse_out, kl_out};
     for (const void* p : opt)
-      if (p && !aligned16(p)) return LS_ERR_INVALID_ARG;
+      if (p && !aligned4(p)) return LS_ERR_INVALID_ARG;
   }
   DevInfo d;
   ls_status s = dev_info(&d);

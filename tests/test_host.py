@@ -110,6 +110,12 @@ def test_argument_checks_reject_before_launch(lib):
         B.LS_ERR_INVALID_ARG
     assert lib.ls_grpo_logp(258, 0, 4, 16, 256, None, 256, None, None, None) == \
         B.LS_ERR_INVALID_ARG
+    # per-token arrays need 4-byte alignment (member slices at any token offset), not less
+    assert lib.ls_grpo_logp(256, 0, 4, 16, 258, None, 256, None, None, None) == \
+        B.LS_ERR_INVALID_ARG
+    assert lib.ls_grpo_loss_fwd_bwd(256, 0, 4, 16, 256, 262, 256, 256, 2, 0, 2, 0.2, 1e-6, 1, 0,
+                                    256, 256, None, None, 256, 1 << 20, None) == \
+        B.LS_ERR_INVALID_ARG
     assert B.status_string(B.LS_ERR_TIMEOUT)
 
 
