@@ -28,6 +28,17 @@
 #define LS_TILE_HD
 #endif
 
+// Units are numbered token block major: unit ul (within its member) covers token block
+// tb = ul / ngrp of group grp = ul % ngrp, where a group is a query head (pack = 1,
+// ngrp = Hq) or a KV head (packed, ngrp = Hkv).  A persistent wave then holds units of
+// neighbouring token blocks, whose response items (the causal keys up to the block) are
+// about as long as each other, so short prompts do not leave a wave waiting on its one
+// longest unit; every KV head still appears in every wave.
+LS_TILE_HD inline void unit_coords(int32_t ul, int32_t ngrp, int32_t* grp, int32_t* tb) {
+  *tb = ul / ngrp;
+  *grp = ul - *tb * ngrp;
+}
+
 struct TileRec {
   int32_t u;           // unit
   int32_t m;           // member (response) of the unit
@@ -56,7 +67,7 @@ struct TileCursor {
   LsWalk walk;
   int32_t u, s, t, t_end, slot;
   bool item_first, item_last, item_complete, valid;
-  int32_t R, g, pack, tok_per_unit, nTB, upm, RT;
+  int32_t R, g, pack, tok_per_unit, nTB, upm, RT, ngrp;
   int32_t m, h, kvh, t0;  // derived from u once per item, not per tile
   bool resp;
 
@@ -69,6 +80,8 @@ struct TileCursor {
         RT(RT_ > 0 ? RT_ : R_), m(0), h(0), kvh(0), t0(0), resp(false) {
     tok_per_unit = tiles_ * (Tile / pack);
     nTB = (RT + tok_per_unit - 1) / tok_per_unit;
+    ngrp = (kMode == 1 ? upm : sc.units) / (nTB > 0 ? nTB : 1);
+    if (ngrp < 1) ngrp = 1;
   }
 
 
@@ -80,8 +93,9 @@ struct TileCursor {
         m = u / upm;
         ul = u - m * upm;
       }
-      const int32_t grp = ul / nTB;    // query head (pack 1) or kv head (packed)
-      t0 = (ul - grp * nTB) * tok_per_unit;
+      int32_t grp, tb;                 // query head (pack 1) or kv head (packed)
+      unit_coords(ul, ngrp, &grp, &tb);
+      t0 = tb * tok_per_unit;
       kvh = pack == 1 ? grp / g : grp;
       h = pack == 1 ? grp : grp * g;
       resp = (s == walk.sc->nsplit);

@@ -401,21 +401,33 @@ bwd_dkdv_tc_kernel(const __grid_constant__ TmapSet tm, const DkdvArgs a,
 }
 
 // Key tiles split between CTAs: add the partial sums of their segments in CTA order.
-// Grid: one block per (KV head, key tile); blocks of tiles one CTA held whole exit.
-__global__ void __launch_bounds__(256) bwd_dkdv_tc_combine(const DkdvArgs a, const LsDkdvGeom gm) {
+// Grid: (KV head x key tile, 16 groups of 8 keys); 128 threads, one float4 of dK or dV of
+// one key each per step.  Blocks of key tiles that one CTA held whole exit at once.
+constexpr int kCombineKeys = 8;
+__global__ void __launch_bounds__(128) bwd_dkdv_tc_combine(const DkdvArgs a, const LsDkdvGeom gm) {
   const int kvh = blockIdx.x / gm.nT, kt = blockIdx.x % gm.nT;
   const int64_t s = gm.tile_begin(kvh, kt), e = s + gm.tile_iters(kt);
   const int b0 = (int)(s / gm.per_cta), b1 = (int)((e - 1) / gm.per_cta);
   if (b0 == b1) return;
-  for (int idx = threadIdx.x; idx < 2 * kTile * kD; idx += blockDim.x) {
-    const int which = idx / (kTile * kD), r = (idx / kD) % kTile, col = idx % kD;
+  constexpr int kVec = kD / 4;  // float4 per row
+  for (int idx = threadIdx.x; idx < 2 * kCombineKeys * kVec; idx += blockDim.x) {
+    const int which = idx / (kCombineKeys * kVec);
+    const int r = blockIdx.y * kCombineKeys + (idx / kVec) % kCombineKeys, c4 = idx % kVec;
     const int key = kt * kTile + r;
     if (key >= a.R) continue;
-    float acc = 0.f;
-    for (int b = b0; b <= b1; ++b)
-      acc += a.part[(((int64_t)gm.slot(b, s) * 2 + which) * kTile + r) * kD + col];
-    float* dst = (which == 0 ? a.dk : a.dv) + ((int64_t)key * a.hkv + kvh) * kD + col;
-    *dst = a.accumulate ? *dst + acc : acc;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int b = b0; b <= b1; ++b) {
+      const float4 x = *reinterpret_cast<const float4*>(
+          a.part + (((int64_t)gm.slot(b, s) * 2 + which) * kTile + r) * kD + 4 * c4);
+      acc.x += x.x; acc.y += x.y; acc.z += x.z; acc.w += x.w;
+    }
+    float4* dst = reinterpret_cast<float4*>((which == 0 ? a.dk : a.dv) +
+                                            ((int64_t)key * a.hkv + kvh) * kD + 4 * c4);
+    if (a.accumulate) {
+      const float4 o = *dst;
+      acc.x += o.x; acc.y += o.y; acc.z += o.z; acc.w += o.w;
+    }
+    *dst = acc;
   }
 }
 
@@ -471,7 +483,7 @@ cudaError_t ls_launch_bwd_dkdv(const LsAttnArgs& a, const LsBwdIn& b, int num_sm
       split = s / gm.per_cta != (en - 1) / gm.per_cta;
     }
   if (split) {
-    bwd_dkdv_tc_combine<<<gm.hkv * gm.nT, 256, 0, st>>>(d, gm);
+    bwd_dkdv_tc_combine<<<dim3(gm.hkv * gm.nT, kTile / kCombineKeys), 128, 0, st>>>(d, gm);
     e = cudaGetLastError();
     if (e == cudaSuccess) ls_note_launch();
   }

@@ -546,9 +546,10 @@ __global__ void __launch_bounds__(kD) replay_fwd_tc_combine(const LsAttnArgs a, 
   const int tu = blockIdx.x, T = sc.tail_units, Q = sc.pieces;
   const int u = sc.tail_unit0() + tu;
   const int tpt = kTile / a.pack, tok_per_unit = a.tiles * tpt;
-  const int nTB = (a.rt + tok_per_unit - 1) / tok_per_unit;
   const int m = u / a.upm, ul = u - m * a.upm;  // member, unit within the member
-  const int grp = ul / nTB, t0 = (ul % nTB) * tok_per_unit;
+  int grp, tb;
+  unit_coords(ul, a.pack == 1 ? a.hq : a.hkv, &grp, &tb);
+  const int t0 = tb * tok_per_unit;
   const int h0 = a.pack == 1 ? grp : grp * a.g;
   const int col = threadIdx.x;
   for (int r = blockIdx.y * kCombineRows; r < (blockIdx.y + 1) * kCombineRows; ++r) {

@@ -116,7 +116,7 @@ static int check_packed(int R, int members, int pack, int hkv, int nt, int sp, i
         return 1;
       }
       ++nf;
-      if (r.t0 != (r.u % nTB) * tpu || r.kvh != r.u / nTB) {
+      if (r.t0 != (r.u / hkv) * tpu || r.kvh != r.u % hkv) {
         std::printf("FAIL packed unit decode R=%d members=%d pack=%d\n", R, members, pack);
         return 1;
       }
@@ -134,7 +134,7 @@ static int check_packed(int R, int members, int pack, int hkv, int nt, int sp, i
   }
   for (int u = 0; u < U; ++u) {
     std::multiset<std::pair<int, int>> want;
-    const int t0 = (u % nTB) * tpu, ve = t0 + tpu < RT ? t0 + tpu : RT;
+    const int t0 = (u / hkv) * tpu, ve = t0 + tpu < RT ? t0 + tpu : RT;
     for (int m = t0 / R; m * R < ve; ++m) {
       const int e = (ve < (m + 1) * R ? ve : (m + 1) * R) - m * R;  // last row's token + 1
       for (int k = 0; k * kTile < e; ++k) want.insert({m, k * kTile});
