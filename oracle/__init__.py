@@ -21,6 +21,10 @@ Functions and the definitions they follow (LongStraw pages):
                       per-token KL estimate exp(d) - d - 1, d = ref - logp, against a
                       reference policy (the pages fix no KL form; their 2M-token runs
                       used beta = 0).
+  gdn_fwd/gdn_bwd  -- Gated-DeltaNet replay from a captured recurrent state (digest,
+                      Method step 1 and "Qwen implementation"): the gated delta rule of
+                      Yang, Kautz & Hatamizadeh (ICLR 2025) as a token-by-token loop,
+                      and its reverse-mode gradient (gdn_oracle.c).
 """
 from __future__ import annotations
 
@@ -54,10 +58,13 @@ def lib():
                                P, P, P, P, P, P, P]
         l.lso_grpo_dlogits_row.argtypes = [P, i32, i32, i32, dbl, dbl, P]
         l.lso_grpo_logp.argtypes = [P, i32, i64, i32, P, P, P, P, P]
+        l.lso_gdn_fwd.argtypes = [P, P, P]
+        l.lso_gdn_bwd.argtypes = [P, P, i32, P, P, P, P, P, P]
         l.lso_num_threads.argtypes = []
         for f in ("lso_capture_kv", "lso_attn_fwd", "lso_attn_fwd_rows", "lso_attn_bwd",
                   "lso_attn_bwd_dq_rows", "lso_attn_bwd_dkdv_keys", "lso_grpo",
-                  "lso_grpo_dlogits_row", "lso_grpo_logp", "lso_num_threads"):
+                  "lso_grpo_dlogits_row", "lso_grpo_logp", "lso_gdn_fwd", "lso_gdn_bwd",
+                  "lso_num_threads"):
             getattr(l, f).restype = C.c_int
         _lib = l
     return _lib
@@ -291,3 +298,79 @@ def grpo_dlogits_rows(logits: np.ndarray, rows, targets, lse, coef) -> np.ndarra
                                           int(targets[r]), float(lse[r]), float(coef[r]),
                                           out[i].ctypes.data_as(C.c_void_p)), "grpo_dlogits_row")
     return out
+
+
+class _Gdn(C.Structure):
+    _fields_ = [
+        ("state0", C.c_void_p), ("q", C.c_void_p), ("k", C.c_void_p), ("v", C.c_void_p),
+        ("in_dtype", C.c_int32), ("g", C.c_void_p), ("beta", C.c_void_p), ("R", C.c_int32),
+        ("H", C.c_int32), ("dk", C.c_int32), ("dv", C.c_int32), ("scale", C.c_double),
+    ]
+
+
+@dataclass
+class GdnProblem:
+    """Gated-DeltaNet replay of R response tokens from a captured state (host arrays).
+
+    state0: [H][dv][dk] float64; q, k: [R][H][dk], v: [R][H][dv] (bf16 as uint16 bits,
+    float32 or float64, all the same type); g (log of the decay), beta: [R][H]."""
+    state0: np.ndarray
+    q: np.ndarray
+    k: np.ndarray
+    v: np.ndarray
+    g: np.ndarray
+    beta: np.ndarray
+    scale: float
+
+    def _struct(self):
+        keep = []
+
+        def c(a, dt=None):
+            a = np.ascontiguousarray(a, dtype=dt) if dt is not None else np.ascontiguousarray(a)
+            keep.append(a)
+            return a
+
+        s0 = c(self.state0, np.float64)
+        q, k, v = c(self.q), c(self.k), c(self.v)
+        assert _dtype_code(q) == _dtype_code(k) == _dtype_code(v)
+        g, b = c(self.g, np.float64), c(self.beta, np.float64)
+        R, H, dk = q.shape
+        dv = v.shape[2]
+        assert k.shape == (R, H, dk) and v.shape[:2] == (R, H) and s0.shape == (H, dv, dk)
+        assert g.shape == (R, H) and b.shape == (R, H)
+        st = _Gdn(state0=s0.ctypes.data, q=q.ctypes.data, k=k.ctypes.data, v=v.ctypes.data,
+                  in_dtype=_dtype_code(q), g=g.ctypes.data, beta=b.ctypes.data, R=R, H=H, dk=dk,
+                  dv=dv, scale=float(self.scale))
+        return st, keep
+
+    @property
+    def dims(self):
+        R, H, dk = self.q.shape
+        return R, H, dk, self.v.shape[2]
+
+
+def gdn_fwd(pb: GdnProblem):
+    """o [R][H][dv] and the state after the last token [H][dv][dk], fp64."""
+    R, H, dk, dv = pb.dims
+    st, keep = pb._struct()
+    o = np.zeros((R, H, dv), np.float64)
+    s_out = np.zeros((H, dv, dk), np.float64)
+    _check(lib().lso_gdn_fwd(C.byref(st), _ptr(o), _ptr(s_out)), "gdn_fwd")
+    return o, s_out
+
+
+def gdn_bwd(pb: GdnProblem, d_o: np.ndarray):
+    """dq, dk [R][H][dk], dv [R][H][dv], dg, dbeta [R][H] and the gradient that would
+    reach the captured state [H][dv][dk] (dropped by the replay: stopgrad), fp64."""
+    R, H, dk, dv = pb.dims
+    d_o = np.ascontiguousarray(d_o)
+    st, keep = pb._struct()
+    dq = np.zeros((R, H, dk))
+    dkk = np.zeros((R, H, dk))
+    dvv = np.zeros((R, H, dv))
+    dg = np.zeros((R, H))
+    db = np.zeros((R, H))
+    ds0 = np.zeros((H, dv, dk))
+    _check(lib().lso_gdn_bwd(C.byref(st), _ptr(d_o), _dtype_code(d_o), _ptr(dq), _ptr(dkk),
+                             _ptr(dvv), _ptr(dg), _ptr(db), _ptr(ds0)), "gdn_bwd")
+    return dq, dkk, dvv, dg, db, ds0

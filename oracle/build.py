@@ -11,6 +11,7 @@ import sys
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 SRC = os.path.join(HERE, "longstraw_oracle.c")
+SRCS = [SRC, os.path.join(HERE, "gdn_oracle.c")]
 HDR = os.path.join(HERE, "longstraw_oracle.h")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "liblongstraw_oracle.so")
@@ -20,7 +21,7 @@ def up_to_date() -> bool:
     if not os.path.exists(LIB):
         return False
     t = os.path.getmtime(LIB)
-    return all(os.path.getmtime(p) <= t for p in (SRC, HDR, __file__))
+    return all(os.path.getmtime(p) <= t for p in (*SRCS, HDR, __file__))
 
 
 def build(force: bool = False) -> str:
@@ -29,7 +30,7 @@ def build(force: bool = False) -> str:
     os.makedirs(OUT_DIR, exist_ok=True)
     tmp = LIB + f".tmp{os.getpid()}"
     cmd = ["gcc", "-std=c99", "-O2", "-fopenmp", "-fPIC", "-shared", "-Wall", "-Wextra",
-           "-Wno-unused-parameter", "-o", tmp, SRC, "-lm"]
+           "-Wno-unused-parameter", "-o", tmp, *SRCS, "-lm"]
     subprocess.run(cmd, check=True)
     os.replace(tmp, LIB)
     return LIB

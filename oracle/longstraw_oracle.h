@@ -149,6 +149,36 @@ int lso_grpo_logp(const void* logits, int32_t dtype, int64_t T, int32_t V,
                   const int32_t* targets, const double* ref_logp, double* lse, double* logp,
                   double* kl);
 
+/* Gated-DeltaNet replay from a captured state (gdn_oracle.c): per head h,
+ *   S_t = exp(g_t) S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T,  o_t = S_t (scale q_t),
+ * S_0 = state0[h] (dv x dk, row-major).  q, k: [R][H][dk], v: [R][H][dv] (in_dtype);
+ * g, beta: [R][H] fp64. */
+typedef struct {
+  const double* state0;  /* [H][dv][dk] */
+  const void* q;
+  const void* k;
+  const void* v;
+  int32_t in_dtype;
+  const double* g;
+  const double* beta;
+  int32_t R;
+  int32_t H;
+  int32_t dk;
+  int32_t dv;
+  double scale;
+} lso_gdn;
+
+/* o [R][H][dv] (may be NULL), state_out [H][dv][dk] (may be NULL): the state after
+ * the last token. */
+int lso_gdn_fwd(const lso_gdn* a, double* o, double* state_out);
+
+/* Gradients of <dO, o> (d_o [R][H][dv], element type do_dtype): dq, dk [R][H][dk], dv
+ * [R][H][dv], dg, dbeta [R][H]; dstate0 [H][dv][dk] is the gradient that would reach
+ * the captured state (the replay treats the state as stopgrad).  Any output may be
+ * NULL. */
+int lso_gdn_bwd(const lso_gdn* a, const void* d_o, int32_t do_dtype, double* dq, double* dk,
+                double* dv, double* dg, double* dbeta, double* dstate0);
+
 /* Threads the OpenMP runtime will use (1 when built without OpenMP). */
 int lso_num_threads(void);
 
