@@ -250,6 +250,44 @@ ls_status ls_grpo_logp(const void* logits, ls_dtype dtype, int64_t T, int V,
                        const int32_t* targets, const float* ref_logp, float* logp_out,
                        float* lse_out, float* kl_out, ls_stream_t stream);
 
+/* ---------------------------------------------------------------- Gated-DeltaNet replay
+ * The hybrid model's Gated-DeltaNet layers keep only the compact recurrent state at the
+ * end of the prompt, and each response is replayed from it with that state stopgrad
+ * (digest, "Method" step 1 and "Qwen implementation"; explainer, "Two incompatible
+ * architectures", Qwen bullet).  The pages give no equations for the layer; the
+ * recurrence is the gated delta rule (Yang, Kautz & Hatamizadeh, "Gated Delta Networks:
+ * Improving Mamba2 with Delta Rule", ICLR 2025), per head h and response token t:
+ *   S_t = exp(g_t) S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T,   S_0 = state0[h]
+ *   o_t = S_t (scale q_t)
+ * S is a 128 x 128 fp32 matrix (d_v x d_k, row-major).  Heads are independent; for
+ * grouped key heads the caller passes each value head's q and k.
+ *   state0     fp32 [H][128][128]: the captured state (read only)
+ *   q, k, v    bf16 [R][H][128]; k is used as given (the layer normalises it)
+ *   g, beta    fp32 [R][H]: log of the decay (g <= 0 in the layer) and the write strength
+ *   o          bf16 [R][H][128]
+ *   state_out  fp32 [H][128][128] or NULL: the state after the last token (running the
+ *              prompt from a zero state with state_out set is the capture)
+ * Work is done in 64-token chunks; the result does not depend on R's split into chunks
+ * beyond rounding.  R == 0 copies state0 to state_out.  workspace: the *_workspace
+ * query's bytes (about 0.33 MB (forward) / 0.6 MB (backward) per head and 64 tokens).
+ * Errors as for the attention calls; LS_ERR_UNSUPPORTED when ceil(R / 64) * H > 65535. */
+ls_status ls_gdn_replay_fwd_workspace(int R, int H, size_t* bytes);
+ls_status ls_gdn_replay_fwd(const float* state0, const void* q, const void* k, const void* v,
+                            const float* g, const float* beta, int R, int H, float scale, void* o,
+                            float* state_out, void* workspace, size_t workspace_bytes,
+                            ls_stream_t stream);
+
+/* ls_gdn_replay_bwd: gradients of the replayed response with the captured state
+ * stopgrad (the gradient that would reach state0 is dropped).  d_o: bf16 [R][H][128];
+ * dq, dk, dv: fp32 [R][H][128]; dg, dbeta: fp32 [R][H]; accumulate != 0 adds into them.
+ * The forward's chunk quantities are recomputed; inputs as for the forward. */
+ls_status ls_gdn_replay_bwd_workspace(int R, int H, size_t* bytes);
+ls_status ls_gdn_replay_bwd(const float* state0, const void* q, const void* k, const void* v,
+                            const float* g, const float* beta, const void* d_o, int R, int H,
+                            float scale, int accumulate, float* dq, float* dk, float* dv, float* dg,
+                            float* dbeta, void* workspace, size_t workspace_bytes,
+                            ls_stream_t stream);
+
 /* ---------------------------------------------------------------- checks
  * ls_validate_page_table: enqueue a check that every entry of the page table covering
  * the cache's num_tokens lies in [0, num_pages) and that no physical page is used

@@ -26,6 +26,8 @@ EXPORTED = (
     "ls_last_device_error", "ls_status_string", "ls_kernel_launches",
     "ls_grpo_loss_fwd_bwd_noalloc", "ls_selftest_wait_timeout", "ls_grpo_logp",
     "ls_replay_attn_fwd_members_workspace", "ls_replay_attn_fwd_members",
+    "ls_gdn_replay_fwd_workspace", "ls_gdn_replay_fwd", "ls_gdn_replay_bwd_workspace",
+    "ls_gdn_replay_bwd",
 )
 
 
@@ -79,6 +81,11 @@ def lib() -> C.CDLL:
             "ls_selftest_wait_timeout": [P],
             "ls_grpo_logp": [P, i32, i64, i32, P, P, P, P, P, P],
             "ls_status_string": [i32],
+            "ls_gdn_replay_fwd_workspace": [i32, i32, szp],
+            "ls_gdn_replay_bwd_workspace": [i32, i32, szp],
+            "ls_gdn_replay_fwd": [P, P, P, P, P, P, i32, i32, f32, P, P, P, sz, P],
+            "ls_gdn_replay_bwd": [P, P, P, P, P, P, P, i32, i32, f32, i32, P, P, P, P, P, P, sz,
+                                  P],
         }
         for name, args in sig.items():
             f = getattr(l, name)
@@ -213,3 +220,27 @@ def ls_selftest_wait_timeout(stream: int = 0) -> None:
 def ls_last_device_error(stream: int = 0) -> int:
     """Synchronise `stream`; return the recorded device-side status (LS_OK if none)."""
     return lib().ls_last_device_error(stream)
+
+
+def ls_gdn_replay_fwd_workspace(R: int, H: int) -> int:
+    return _size("ls_gdn_replay_fwd_workspace", R, H)
+
+
+def ls_gdn_replay_bwd_workspace(R: int, H: int) -> int:
+    return _size("ls_gdn_replay_bwd_workspace", R, H)
+
+
+def ls_gdn_replay_fwd(state0: int, q: int, k: int, v: int, g: int, beta: int, R: int, H: int,
+                      scale: float, o: int, state_out: int | None, workspace: int,
+                      workspace_bytes: int, stream: int = 0) -> None:
+    _ok("ls_gdn_replay_fwd",
+        lib().ls_gdn_replay_fwd(state0, q, k, v, g, beta, R, H, scale, o, state_out, workspace,
+                                workspace_bytes, stream))
+
+
+def ls_gdn_replay_bwd(state0: int, q: int, k: int, v: int, g: int, beta: int, d_o: int, R: int,
+                      H: int, scale: float, accumulate: int, dq: int, dk: int, dv: int, dg: int,
+                      dbeta: int, workspace: int, workspace_bytes: int, stream: int = 0) -> None:
+    _ok("ls_gdn_replay_bwd",
+        lib().ls_gdn_replay_bwd(state0, q, k, v, g, beta, d_o, R, H, scale, accumulate, dq, dk,
+                                dv, dg, dbeta, workspace, workspace_bytes, stream))

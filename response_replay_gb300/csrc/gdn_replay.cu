@@ -1,0 +1,742 @@
+// gdn_replay.cu -- Gated-DeltaNet replay from a captured recurrent state.
+//
+// For the hybrid model's Gated-DeltaNet layers LongStraw keeps only the compact
+// recurrent state at the end of the prompt (digest, "Method" step 1 and "Qwen
+// implementation"; explainer, "Two incompatible architectures", Qwen bullet) and replays
+// each response from it with that state stopgrad.  The layer is the gated delta rule
+// (Yang, Kautz & Hatamizadeh, "Gated Delta Networks", ICLR 2025), per head:
+//   S_t = exp(g_t) S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T,   o_t = S_t (scale q_t)
+// with S a 128 x 128 (d_v x d_k) fp32 matrix and S_0 the captured state.
+//
+// Chunked form (64-token chunks; within a chunk G_t is the running sum of g, gamma_t =
+// exp(G_t), Gam[t][i] = exp(G_t - G_i) for i <= t, lam_i = gamma_C / gamma_i):
+//   Ms = (K K^T) * Gam strictly lower,  T = (I + diag(beta) Ms)^-1
+//   W  = T diag(beta gamma) K,  U0 = T diag(beta) V,  U = U0 - W S0^T
+//   O  = diag(gamma) Q' S0^T + ((Q' K^T) * Gam, lower incl.) U,   Q' = scale Q
+//   S_C = gamma_C S0 + U^T diag(lam) K
+// Every step that does not depend on the state runs for all (head, chunk) pairs at once
+// as batched matrix products; only the state hand-off between chunks is sequential, and
+// it splits by rows of S (row i of S_{c+1} needs only row i of S_c), so it runs as one
+// warp per (head, row).  The backward is the adjoint of the same steps: the gradient of
+// the state is carried from chunk to chunk in reverse (again row by row), the rest is
+// batched per chunk.  The gradient reaching S_0 is dropped: the captured state is
+// stopgrad.
+//
+// Arithmetic is fp32 on the CUDA cores (the chunk matrices are 64 x 64 to 128 x 128 and
+// the triangular solve is sequential within a column); inputs q, k, v, dO are bf16.
+#include <math.h>
+
+#include "ls_device.cuh"
+#include "ls_internal.h"
+
+namespace {
+
+constexpr int kD = 128;   // head dims (d_k = d_v)
+constexpr int kC = 64;    // chunk length
+constexpr float kLog2e = 1.4426950408889634f;
+
+// ---------------------------------------------------------------- workspace layout
+// Per (head, chunk) pair b = h * nC + c, fp32 blocks of the sizes below.
+struct GdnLayout {
+  int nC, nb;
+  size_t qf, kf, vf, dof;            // [nb][64][128]
+  size_t x1, x2, x3, x4, x5, x6;     // [nb][64][128] scratch
+  size_t w, u;                       // [nb][64][128]
+  size_t ms, tm, p, m1, m2;          // [nb][64][64]
+  size_t sc, dsc;                    // [nb][128][128]
+  size_t gcum, gam, lam, beta;       // [nb][64]
+  size_t total;
+};
+
+size_t al256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+GdnLayout gdn_layout(int R, int H, bool bwd) {
+  GdnLayout L;
+  L.nC = (R + kC - 1) / kC;
+  L.nb = L.nC * H;
+  const size_t cd = (size_t)L.nb * kC * kD * 4, cc = (size_t)L.nb * kC * kC * 4;
+  const size_t dd = (size_t)L.nb * kD * kD * 4, c1 = (size_t)L.nb * kC * 4;
+  size_t p = 0;
+  auto take = [&](size_t n) { const size_t o = p; p = al256(p + n); return o; };
+  L.qf = take(cd); L.kf = take(cd); L.vf = take(cd);
+  L.dof = bwd ? take(cd) : 0;
+  L.x1 = take(cd); L.x2 = take(cd);
+  L.x3 = bwd ? take(cd) : 0; L.x4 = bwd ? take(cd) : 0;
+  L.x5 = bwd ? take(cd) : 0; L.x6 = bwd ? take(cd) : 0;
+  L.w = take(cd); L.u = take(cd);
+  L.ms = take(cc); L.tm = take(cc); L.p = take(cc);
+  L.m1 = bwd ? take(cc) : 0; L.m2 = bwd ? take(cc) : 0;
+  L.sc = take(dd);
+  L.dsc = bwd ? take(dd) : 0;
+  L.gcum = take(c1); L.gam = take(c1); L.lam = take(c1); L.beta = take(c1);
+  L.total = p;
+  return L;
+}
+
+template <typename T>
+T* at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
+}
+
+__device__ __forceinline__ float bf2f(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+// ---------------------------------------------------------------- chunk inputs
+// Grid (nC, H), 128 threads (one per head dim).  Chunk c of head h: qf = scale q, kf, vf
+// (and dof when d_o is given) as fp32 [64][128], zeros past R; per token the running log
+// decay G, gamma = exp(G), lam = gamma_C / gamma and beta (g = beta = 0 past R, so padding
+// neither decays nor writes the state).
+__global__ void __launch_bounds__(128) gdn_load(const __nv_bfloat16* __restrict__ q,
+                                                const __nv_bfloat16* __restrict__ k,
+                                                const __nv_bfloat16* __restrict__ v,
+                                                const __nv_bfloat16* __restrict__ d_o,
+                                                const float* __restrict__ g,
+                                                const float* __restrict__ beta, int R, int H,
+                                                float scale, float* qf, float* kf, float* vf,
+                                                float* dof, float* gcum, float* gam, float* lam,
+                                                float* bet) {
+  const int c = blockIdx.x, h = blockIdx.y, nC = gridDim.x, j = threadIdx.x;
+  const int64_t b = (int64_t)h * nC + c;
+  for (int t = 0; t < kC; ++t) {
+    const int tok = c * kC + t;
+    const bool ok = tok < R;
+    const int64_t src = ((int64_t)tok * H + h) * kD + j;
+    const int64_t dst = (b * kC + t) * kD + j;
+    qf[dst] = ok ? scale * bf2f(q[src]) : 0.f;
+    kf[dst] = ok ? bf2f(k[src]) : 0.f;
+    vf[dst] = ok ? bf2f(v[src]) : 0.f;
+    if (dof) dof[dst] = ok ? bf2f(d_o[src]) : 0.f;
+  }
+  __shared__ float gs[kC];
+  if (j < kC) {
+    const int tok = c * kC + j;
+    gs[j] = tok < R ? g[(int64_t)tok * H + h] : 0.f;
+    bet[b * kC + j] = tok < R ? beta[(int64_t)tok * H + h] : 0.f;
+  }
+  __syncthreads();
+  if (j == 0) {  // running sum in token order
+    float s = 0.f;
+    for (int t = 0; t < kC; ++t) {
+      s += gs[t];
+      gs[t] = s;
+    }
+  }
+  __syncthreads();
+  if (j < kC) {
+    const float G = gs[j], GC = gs[kC - 1];
+    gcum[b * kC + j] = G;
+    gam[b * kC + j] = exp2f(G * kLog2e);
+    lam[b * kC + j] = exp2f((GC - G) * kLog2e);
+  }
+}
+
+// ---------------------------------------------------------------- batched products
+// C[b] = alpha diag(rs[b]) op(A[b]) op(B[b]) (+ C[b]), op(X) = X or X^T, masked to the
+// lower triangle (mask 1: row >= col, 2: row > col; 0: none).  Row-major, leading
+// dimensions lda / ldb / ldc, batch strides sA / sB / sC (elements); rs may be NULL.
+// 64 x 64 output tiles, 256 threads, 16 x 4 x 4 accumulation (M, N multiples of 64, K of
+// 16: the chunk shapes 64 and 128).
+template <bool TA, bool TB>
+__global__ void __launch_bounds__(256) gdn_gemm(const float* __restrict__ A, int lda, int64_t sA,
+                                                const float* __restrict__ B, int ldb, int64_t sB,
+                                                float* C, int ldc, int64_t sC, int K, float alpha,
+                                                const float* __restrict__ rs, int64_t srs,
+                                                int accumulate, int mask) {
+  __shared__ float As[16][64 + 4];
+  __shared__ float Bs[16][64 + 4];
+  const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
+  const int m0 = blockIdx.y * 64, n0 = blockIdx.x * 64;
+  const int64_t bz = blockIdx.z;
+  A += bz * sA;
+  B += bz * sB;
+  C += bz * sC;
+  if (mask && n0 > m0 + 63) {  // tile entirely above the diagonal
+    if (!accumulate)
+      for (int e = tid; e < 64 * 64; e += 256) C[(int64_t)(m0 + e / 64) * ldc + n0 + e % 64] = 0.f;
+    return;
+  }
+  float acc[4][4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+  for (int k0 = 0; k0 < K; k0 += 16) {
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int e = tid + 256 * r;  // 1024 elements of each 64 x 16 / 16 x 64 tile
+      if (TA) {  // op(A)[m][k] = A[k][m]: read along m
+        const int kk = e / 64, mm = e % 64;
+        As[kk][mm] = A[(int64_t)(k0 + kk) * lda + m0 + mm];
+      } else {
+        const int mm = e / 16, kk = e % 16;
+        As[kk][mm] = A[(int64_t)(m0 + mm) * lda + k0 + kk];
+      }
+      if (TB) {  // op(B)[k][n] = B[n][k]
+        const int nn = e / 16, kk = e % 16;
+        Bs[kk][nn] = B[(int64_t)(n0 + nn) * ldb + k0 + kk];
+      } else {
+        const int kk = e / 64, nn = e % 64;
+        Bs[kk][nn] = B[(int64_t)(k0 + kk) * ldb + n0 + nn];
+      }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int kk = 0; kk < 16; ++kk) {
+      float a[4], bb[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) a[i] = As[kk][ty + 16 * i];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) bb[j] = Bs[kk][tx + 16 * j];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], bb[j], acc[i][j]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int m = m0 + ty + 16 * i;
+    const float sc = alpha * (rs ? rs[bz * srs + m] : 1.f);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int n = n0 + tx + 16 * j;
+      float x = sc * acc[i][j];
+      if ((mask == 1 && n > m) || (mask == 2 && n >= m)) x = 0.f;
+      float* p = C + (int64_t)m * ldc + n;
+      *p = accumulate ? *p + x : x;
+    }
+  }
+}
+
+// ---------------------------------------------------------------- elementwise steps
+// X[b][t][i] *= exp(G_t - G_i) (and beta_t when rowb), on the lower triangle (strict when
+// strict), zero above.  Grid nb, 256 threads.
+__global__ void __launch_bounds__(256) gdn_decay(float* X, const float* __restrict__ gcum,
+                                                 const float* __restrict__ rowb, int strict,
+                                                 float* copy_to) {
+  const int64_t b = blockIdx.x;
+  const float* G = gcum + b * kC;
+  for (int e = threadIdx.x; e < kC * kC; e += blockDim.x) {
+    const int t = e / kC, i = e % kC;
+    float* x = X + b * kC * kC + e;
+    float y = 0.f;
+    if (i < t || (!strict && i == t)) y = *x * exp2f((G[t] - G[i]) * kLog2e);
+    if (copy_to) copy_to[b * kC * kC + e] = y;
+    if (rowb) y *= rowb[b * kC + t];
+    *x = y;
+  }
+}
+
+// Y[b][t][:] = a * s1[b][t] * X1[b][t][:] + c * X2[b][t][:]  (X2 may be NULL); grid nb x 64
+// rows, 128 threads.
+__global__ void __launch_bounds__(128) gdn_rows(float* Y, const float* X1, const float* s1,
+                                                const float* s2, float a, const float* X2,
+                                                float c) {
+  const int64_t b = blockIdx.x;
+  const int t = blockIdx.y, j = threadIdx.x;
+  const int64_t e = (b * kC + t) * kD + j;
+  float sc = a * (s1 ? s1[b * kC + t] : 1.f) * (s2 ? s2[b * kC + t] : 1.f);
+  float y = sc * X1[e];
+  if (X2) y += c * X2[e];
+  Y[e] = y;
+}
+
+// T = (I + A)^-1 for the unit lower-triangular I + A of each chunk (A strictly lower):
+// column j of T is the forward substitution T[t][j] = [t == j] - sum_{j <= i < t} A[t][i]
+// T[i][j], independent of the other columns.  Grid nb, 64 threads (one per column).
+__global__ void __launch_bounds__(64) gdn_tri_inv(const float* __restrict__ A, float* Tm) {
+  __shared__ float As[kC][kC + 1];
+  const int64_t b = blockIdx.x;
+  const int j = threadIdx.x;
+  for (int e = j; e < kC * kC; e += kC) As[e / kC][e % kC] = A[b * kC * kC + e];
+  __syncthreads();
+  float col[kC];
+#pragma unroll
+  for (int t = 0; t < kC; ++t) {
+    float s = t == j ? 1.f : 0.f;
+#pragma unroll
+    for (int i = 0; i < t; ++i) s = fmaf(-As[t][i], col[i], s);
+    col[t] = t >= j ? s : 0.f;
+  }
+#pragma unroll
+  for (int t = 0; t < kC; ++t) Tm[b * kC * kC + t * kC + j] = col[t];
+}
+
+// p[0..63] per lane -> lane l holds the warp sums of entries 2l and 2l + 1 in p[0], p[1].
+__device__ __forceinline__ void warp_reduce64(float* p, int lane) {
+#pragma unroll
+  for (int off = 16, n = 64; off >= 1; off >>= 1, n >>= 1) {
+    const bool up = (lane & off) != 0;
+#pragma unroll
+    for (int j = 0; j < n / 2; ++j) {
+      const float send = up ? p[j] : p[j + n / 2];
+      const float keep = up ? p[j + n / 2] : p[j];
+      p[j] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+    }
+  }
+}
+
+// ---------------------------------------------------------------- state hand-off
+// Forward: row i of the state, chunk by chunk (grid (H, 8), 16 warps, one row each):
+//   Sc[b][i][:] = S[i][:]   (state entering chunk c)
+//   u_t = U0[t][i] - W[t] . S[i]                 (written over U0)
+//   S[i] <- gamma_C S[i] + sum_t lam_t u_t K[t]
+constexpr int kScanRows = 16;
+__global__ void __launch_bounds__(32 * kScanRows) gdn_scan_fwd(const float* __restrict__ state0,
+                                                               int nC, const float* __restrict__ W,
+                                                               const float* __restrict__ kf,
+                                                               float* U, const float* __restrict__ gam,
+                                                               const float* __restrict__ lam,
+                                                               float* Sc, float* state_out) {
+  extern __shared__ float sm[];
+  float* Ws = sm;                // [64][128]
+  float* Ks = sm + kC * kD;      // [64][128]
+  const int h = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int i = blockIdx.y * kScanRows + warp;
+  float S[4];
+#pragma unroll
+  for (int m = 0; m < 4; ++m) S[m] = state0[((int64_t)h * kD + i) * kD + lane + 32 * m];
+  for (int c = 0; c < nC; ++c) {
+    const int64_t b = (int64_t)h * nC + c;
+    __syncthreads();
+    for (int e = threadIdx.x; e < kC * kD; e += blockDim.x) {
+      Ws[e] = W[b * kC * kD + e];
+      Ks[e] = kf[b * kC * kD + e];
+    }
+    __syncthreads();
+#pragma unroll
+    for (int m = 0; m < 4; ++m) Sc[(b * kD + i) * kD + lane + 32 * m] = S[m];
+    float p[kC];
+#pragma unroll
+    for (int t = 0; t < kC; ++t) {
+      float s = 0.f;
+#pragma unroll
+      for (int m = 0; m < 4; ++m) s = fmaf(Ws[t * kD + lane + 32 * m], S[m], s);
+      p[t] = s;
+    }
+    warp_reduce64(p, lane);
+    float vl[2];
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const int t = 2 * lane + r;
+      float* up = U + (b * kC + t) * kD + i;
+      const float u = *up - p[r];
+      *up = u;
+      vl[r] = lam[b * kC + t] * u;
+    }
+    const float gC = gam[b * kC + kC - 1];
+#pragma unroll
+    for (int m = 0; m < 4; ++m) S[m] *= gC;
+#pragma unroll 8
+    for (int t = 0; t < kC; ++t) {
+      const float vt = __shfl_sync(0xffffffffu, vl[t & 1], t >> 1);
+#pragma unroll
+      for (int m = 0; m < 4; ++m) S[m] = fmaf(vt, Ks[t * kD + lane + 32 * m], S[m]);
+    }
+  }
+  if (state_out)
+#pragma unroll
+    for (int m = 0; m < 4; ++m) state_out[((int64_t)h * kD + i) * kD + lane + 32 * m] = S[m];
+}
+
+// Backward: row i of dS (the gradient of the state leaving the chunk), chunks in reverse:
+//   dSC[b][i][:] = dS[i]
+//   a_t = K[t] . dS[i];  dZ_t = dZ0[t][i] + sum_{s >= t} T[s][t] lam_s a_s;  dY_t = beta_t dZ_t
+//   dS[i] <- gamma_C dS[i] + sum_t gamma_t (dO[t][i] Q'[t] - dY_t K[t])
+__global__ void __launch_bounds__(32 * kScanRows) gdn_scan_bwd(int nC, const float* __restrict__ kf,
+                                                               const float* __restrict__ qf,
+                                                               const float* __restrict__ dof,
+                                                               const float* __restrict__ Tm,
+                                                               const float* __restrict__ dZ0,
+                                                               const float* __restrict__ gam,
+                                                               const float* __restrict__ lam,
+                                                               const float* __restrict__ bet,
+                                                               float* dSC) {
+  extern __shared__ float sm[];
+  float* Ks = sm;                 // [64][128]
+  float* Qs = sm + kC * kD;       // [64][128]
+  float* Ts = sm + 2 * kC * kD;   // [64][64]
+  const int h = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int i = blockIdx.y * kScanRows + warp;
+  float dS[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int c = nC - 1; c >= 0; --c) {
+    const int64_t b = (int64_t)h * nC + c;
+    __syncthreads();
+    for (int e = threadIdx.x; e < kC * kD; e += blockDim.x) {
+      Ks[e] = kf[b * kC * kD + e];
+      Qs[e] = qf[b * kC * kD + e];
+    }
+    for (int e = threadIdx.x; e < kC * kC; e += blockDim.x) Ts[e] = Tm[b * kC * kC + e];
+    __syncthreads();
+#pragma unroll
+    for (int m = 0; m < 4; ++m) dSC[(b * kD + i) * kD + lane + 32 * m] = dS[m];
+    float p[kC];
+#pragma unroll
+    for (int t = 0; t < kC; ++t) {
+      float s = 0.f;
+#pragma unroll
+      for (int m = 0; m < 4; ++m) s = fmaf(Ks[t * kD + lane + 32 * m], dS[m], s);
+      p[t] = s;
+    }
+    warp_reduce64(p, lane);
+    float bv[2];
+#pragma unroll
+    for (int r = 0; r < 2; ++r) bv[r] = lam[b * kC + 2 * lane + r] * p[r];
+    float z0 = 0.f, z1 = 0.f;
+#pragma unroll 8
+    for (int s = 0; s < kC; ++s) {
+      const float bs = __shfl_sync(0xffffffffu, bv[s & 1], s >> 1);
+      const float2 tt = *reinterpret_cast<const float2*>(Ts + s * kC + 2 * lane);
+      z0 = fmaf(tt.x, bs, z0);  // T[s][t] is zero for s < t
+      z1 = fmaf(tt.y, bs, z1);
+    }
+    float cq[2], ck[2];
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const int t = 2 * lane + r;
+      const float dz = dZ0[(b * kC + t) * kD + i] + (r == 0 ? z0 : z1);
+      const float gm = gam[b * kC + t];
+      cq[r] = gm * dof[(b * kC + t) * kD + i];
+      ck[r] = gm * bet[b * kC + t] * dz;
+    }
+    const float gC = gam[b * kC + kC - 1];
+#pragma unroll
+    for (int m = 0; m < 4; ++m) dS[m] *= gC;
+#pragma unroll 8
+    for (int t = 0; t < kC; ++t) {
+      const float a = __shfl_sync(0xffffffffu, cq[t & 1], t >> 1);
+      const float e = __shfl_sync(0xffffffffu, ck[t & 1], t >> 1);
+#pragma unroll
+      for (int m = 0; m < 4; ++m)
+        dS[m] = fmaf(a, Qs[t * kD + lane + 32 * m], fmaf(-e, Ks[t * kD + lane + 32 * m], dS[m]));
+    }
+  }
+}
+
+// ---------------------------------------------------------------- outputs
+// o (bf16 [R][H][128]) from the chunk-major fp32 result.  Grid (nC, H), 128 threads.
+__global__ void __launch_bounds__(128) gdn_store_o(const float* __restrict__ X, int R, int H,
+                                                   __nv_bfloat16* o) {
+  const int c = blockIdx.x, h = blockIdx.y, nC = gridDim.x, j = threadIdx.x;
+  const int64_t b = (int64_t)h * nC + c;
+  for (int t = 0; t < kC; ++t) {
+    const int tok = c * kC + t;
+    if (tok < R) o[((int64_t)tok * H + h) * kD + j] = __float2bfloat16_rn(X[(b * kC + t) * kD + j]);
+  }
+}
+
+// dq, dk, dv (fp32 [R][H][128]) from chunk-major results (accumulate adds).
+__global__ void __launch_bounds__(128) gdn_store_grads(const float* __restrict__ dQ,
+                                                       const float* __restrict__ dK,
+                                                       const float* __restrict__ dV, int R, int H,
+                                                       float qscale, int accumulate, float* dq,
+                                                       float* dk, float* dv) {
+  const int c = blockIdx.x, h = blockIdx.y, nC = gridDim.x, j = threadIdx.x;
+  const int64_t b = (int64_t)h * nC + c;
+  for (int t = 0; t < kC; ++t) {
+    const int tok = c * kC + t;
+    if (tok >= R) break;
+    const int64_t src = (b * kC + t) * kD + j, dst = ((int64_t)tok * H + h) * kD + j;
+    const float x = qscale * dQ[src], y = dK[src], z = dV[src];
+    dq[dst] = accumulate ? dq[dst] + x : x;
+    dk[dst] = accumulate ? dk[dst] + y : y;
+    dv[dst] = accumulate ? dv[dst] + z : z;
+  }
+}
+
+// Per chunk: dbeta and dg.  With dlam_t = U_t . (dSC k_t), the row dots of the chunk and
+// the row/column sums of dP * P and dMs * Ms:
+//   dG_t = gamma_t dO_t . (S0 q'_t) - gamma_t dY_t . (S0 k_t) + rowsum_t(dP P) -
+//          colsum_t(dP P) + rowsum_t(dMs Ms) - colsum_t(dMs Ms) - lam_t dlam_t
+//          + [t = C-1] (gamma_C <dSC, S0> + sum_i lam_i dlam_i)
+//   dg_j = sum_{t >= j} dG_t;   dbeta_t = dZ_t . Y_t + sum_i dA[t][i] Ms[t][i]
+// Grid (nC, H), 256 threads.
+struct GdnScalarIn {
+  const float *u, *kds, *dof, *qs, *dy, *ks, *dz, *y;  // [nb][64][128]
+  const float *dp, *p, *dms, *ms, *da;                 // [nb][64][64]
+  const float *sc, *dsc;                               // [nb][128][128]
+  const float *gam, *lam;                              // [nb][64]
+};
+__global__ void __launch_bounds__(256) gdn_scalar_grads(const GdnScalarIn in, int R, int H,
+                                                        int accumulate, float* dg, float* dbeta) {
+  const int c = blockIdx.x, h = blockIdx.y, nC = gridDim.x;
+  const int64_t b = (int64_t)h * nC + c;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  __shared__ float dG[kC], dl[kC], zb[kC], red[8];
+  // row dots, one warp per row
+  for (int t = warp; t < kC; t += 8) {
+    const int64_t r = (b * kC + t) * kD;
+    float s_l = 0.f, s_o = 0.f, s_y = 0.f, s_z = 0.f;
+    for (int a = lane; a < kD; a += 32) {
+      s_l += in.u[r + a] * in.kds[r + a];
+      s_o += in.dof[r + a] * in.qs[r + a];
+      s_y += in.dy[r + a] * in.ks[r + a];
+      s_z += in.dz[r + a] * in.y[r + a];
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      s_l += __shfl_xor_sync(0xffffffffu, s_l, off);
+      s_o += __shfl_xor_sync(0xffffffffu, s_o, off);
+      s_y += __shfl_xor_sync(0xffffffffu, s_y, off);
+      s_z += __shfl_xor_sync(0xffffffffu, s_z, off);
+    }
+    if (lane == 0) {
+      const float gm = in.gam[b * kC + t];
+      dl[t] = s_l;
+      dG[t] = gm * s_o - gm * s_y - in.lam[b * kC + t] * s_l;
+      zb[t] = s_z;
+    }
+  }
+  // <dSC, S0>
+  float sd = 0.f;
+  for (int e = tid; e < kD * kD; e += blockDim.x) sd += in.dsc[b * kD * kD + e] * in.sc[b * kD * kD + e];
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) sd += __shfl_xor_sync(0xffffffffu, sd, off);
+  if (lane == 0) red[warp] = sd;
+  __syncthreads();
+  if (tid < kC) {
+    const int t = tid;
+    const float* dp = in.dp + b * kC * kC;
+    const float* pp = in.p + b * kC * kC;
+    const float* dm = in.dms + b * kC * kC;
+    const float* mm = in.ms + b * kC * kC;
+    const float* da = in.da + b * kC * kC;
+    float r1 = 0.f, c1 = 0.f, r2 = 0.f, c2 = 0.f, rb = 0.f;
+    for (int i = 0; i < kC; ++i) {
+      r1 += dp[t * kC + i] * pp[t * kC + i];
+      c1 += dp[i * kC + t] * pp[i * kC + t];
+      r2 += dm[t * kC + i] * mm[t * kC + i];
+      c2 += dm[i * kC + t] * mm[i * kC + t];
+      rb += da[t * kC + i] * mm[t * kC + i];
+    }
+    dG[t] += r1 - c1 + r2 - c2;
+    zb[t] += rb;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    float sdot = 0.f, sl = 0.f;
+    for (int w = 0; w < 8; ++w) sdot += red[w];
+    for (int i = 0; i < kC; ++i) sl += in.lam[b * kC + i] * dl[i];
+    dG[kC - 1] += in.gam[b * kC + kC - 1] * sdot + sl;
+    float run = 0.f;  // dg_j = sum_{t >= j} dG_t
+    for (int t = kC - 1; t >= 0; --t) {
+      run += dG[t];
+      dG[t] = run;
+    }
+  }
+  __syncthreads();
+  if (tid < kC) {
+    const int tok = c * kC + tid;
+    if (tok < R) {
+      const int64_t o = (int64_t)tok * H + h;
+      dg[o] = accumulate ? dg[o] + dG[tid] : dG[tid];
+      dbeta[o] = accumulate ? dbeta[o] + zb[tid] : zb[tid];
+    }
+  }
+}
+
+// ---------------------------------------------------------------- launch helpers
+struct Launcher {
+  cudaStream_t st;
+  cudaError_t err = cudaSuccess;
+  void check() {
+    if (err == cudaSuccess) err = cudaGetLastError();
+    if (err == cudaSuccess) ls_note_launch();
+  }
+};
+
+// C = alpha diag(rs) op(A) op(B) (+C), all nb batches; M x N output, contraction K.
+void gemm(Launcher& L, int nb, bool ta, bool tb, int M, int N, int K, const float* A, int lda,
+          int64_t sA, const float* B, int ldb, int64_t sB, float* C, int ldc, int64_t sC,
+          float alpha, const float* rs = nullptr, int64_t srs = kC, int accumulate = 0,
+          int mask = 0) {
+  if (L.err != cudaSuccess) return;
+  const dim3 grid(N / 64, M / 64, nb);
+  if (!ta && !tb)
+    gdn_gemm<false, false><<<grid, 256, 0, L.st>>>(A, lda, sA, B, ldb, sB, C, ldc, sC, K, alpha, rs, srs, accumulate, mask);
+  else if (!ta && tb)
+    gdn_gemm<false, true><<<grid, 256, 0, L.st>>>(A, lda, sA, B, ldb, sB, C, ldc, sC, K, alpha, rs, srs, accumulate, mask);
+  else if (ta && !tb)
+    gdn_gemm<true, false><<<grid, 256, 0, L.st>>>(A, lda, sA, B, ldb, sB, C, ldc, sC, K, alpha, rs, srs, accumulate, mask);
+  else
+    gdn_gemm<true, true><<<grid, 256, 0, L.st>>>(A, lda, sA, B, ldb, sB, C, ldc, sC, K, alpha, rs, srs, accumulate, mask);
+  L.check();
+}
+
+constexpr int64_t kCD = kC * kD, kCC = kC * kC, kDD = kD * kD;
+
+// The state-independent chunk algebra and the forward state hand-off, shared by the
+// forward and the backward (which recomputes it): T, W, U (= U0 - W S0^T after the scan),
+// Sc, and P = (Q' K^T) * Gam (lower incl.).
+void gdn_common(Launcher& L, const LsGdnArgs& a, const GdnLayout& W_, void* ws,
+                const void* d_o, float* state_out) {
+  const int nb = W_.nb, nC = W_.nC;
+  float* qf = at<float>(ws, W_.qf);
+  float* kf = at<float>(ws, W_.kf);
+  float* vf = at<float>(ws, W_.vf);
+  float* dof = d_o ? at<float>(ws, W_.dof) : nullptr;
+  float* gcum = at<float>(ws, W_.gcum);
+  float* gam = at<float>(ws, W_.gam);
+  float* lam = at<float>(ws, W_.lam);
+  float* bet = at<float>(ws, W_.beta);
+  gdn_load<<<dim3(nC, a.H), 128, 0, L.st>>>(
+      static_cast<const __nv_bfloat16*>(a.q), static_cast<const __nv_bfloat16*>(a.k),
+      static_cast<const __nv_bfloat16*>(a.v), static_cast<const __nv_bfloat16*>(d_o), a.g, a.beta,
+      a.R, a.H, a.scale, qf, kf, vf, dof, gcum, gam, lam, bet);
+  L.check();
+  float* ms = at<float>(ws, W_.ms);
+  float* tm = at<float>(ws, W_.tm);
+  float* pm = at<float>(ws, W_.p);
+  float* x1 = at<float>(ws, W_.x1);
+  float* x2 = at<float>(ws, W_.x2);
+  float* w = at<float>(ws, W_.w);
+  float* u = at<float>(ws, W_.u);
+  // A = diag(beta) (K K^T * Gam) strictly lower (in tm for now), Ms kept
+  gemm(L, nb, false, true, kC, kC, kD, kf, kD, kCD, kf, kD, kCD, tm, kC, kCC, 1.f);
+  if (L.err != cudaSuccess) return;
+  gdn_decay<<<nb, 256, 0, L.st>>>(tm, gcum, bet, 1, ms);
+  L.check();
+  // T = (I + A)^-1, in place of A (read into shared memory first)
+  if (L.err != cudaSuccess) return;
+  gdn_tri_inv<<<nb, kC, 0, L.st>>>(tm, tm);
+  L.check();
+  // W = T diag(beta gamma) K,  U0 = T diag(beta) V
+  if (L.err != cudaSuccess) return;
+  gdn_rows<<<dim3(nb, kC), kD, 0, L.st>>>(x1, kf, bet, gam, 1.f, nullptr, 0.f);
+  L.check();
+  if (L.err != cudaSuccess) return;
+  gdn_rows<<<dim3(nb, kC), kD, 0, L.st>>>(x2, vf, bet, nullptr, 1.f, nullptr, 0.f);
+  L.check();
+  gemm(L, nb, false, false, kC, kD, kC, tm, kC, kCC, x1, kD, kCD, w, kD, kCD, 1.f);
+  gemm(L, nb, false, false, kC, kD, kC, tm, kC, kCC, x2, kD, kCD, u, kD, kCD, 1.f);
+  if (L.err != cudaSuccess) return;
+  const size_t smem = 2 * kCD * sizeof(float);
+  L.err = cudaFuncSetAttribute(gdn_scan_fwd, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (L.err != cudaSuccess) return;
+  gdn_scan_fwd<<<dim3(a.H, kD / kScanRows), 32 * kScanRows, smem, L.st>>>(
+      a.state0, nC, w, kf, u, gam, lam, at<float>(ws, W_.sc), state_out);
+  L.check();
+  // P = (Q' K^T) * Gam, lower incl.
+  gemm(L, nb, false, true, kC, kC, kD, qf, kD, kCD, kf, kD, kCD, pm, kC, kCC, 1.f);
+  if (L.err != cudaSuccess) return;
+  gdn_decay<<<nb, 256, 0, L.st>>>(pm, gcum, nullptr, 0, nullptr);
+  L.check();
+}
+
+}  // namespace
+
+size_t ls_gdn_ws_bytes(int R, int H, bool bwd) { return gdn_layout(R, H, bwd).total; }
+
+cudaError_t ls_launch_gdn_fwd(const LsGdnArgs& a, void* o, float* state_out, void* ws,
+                              cudaStream_t st) {
+  const GdnLayout W_ = gdn_layout(a.R, a.H, false);
+  Launcher L{st};
+  gdn_common(L, a, W_, ws, nullptr, state_out);
+  const int nb = W_.nb;
+  float* x1 = at<float>(ws, W_.x1);
+  // O = diag(gamma) Q' S0^T + P U
+  gemm(L, nb, false, true, kC, kD, kD, at<float>(ws, W_.qf), kD, kCD, at<float>(ws, W_.sc), kD,
+       kDD, x1, kD, kCD, 1.f, at<float>(ws, W_.gam));
+  gemm(L, nb, false, false, kC, kD, kC, at<float>(ws, W_.p), kC, kCC, at<float>(ws, W_.u), kD,
+       kCD, x1, kD, kCD, 1.f, nullptr, kC, 1);
+  if (L.err != cudaSuccess) return L.err;
+  gdn_store_o<<<dim3(W_.nC, a.H), kD, 0, st>>>(x1, a.R, a.H, static_cast<__nv_bfloat16*>(o));
+  L.check();
+  return L.err;
+}
+
+cudaError_t ls_launch_gdn_bwd(const LsGdnArgs& a, const void* d_o, int accumulate, float* dq,
+                              float* dk, float* dv, float* dg, float* dbeta, void* ws,
+                              cudaStream_t st) {
+  const GdnLayout W_ = gdn_layout(a.R, a.H, true);
+  Launcher L{st};
+  gdn_common(L, a, W_, ws, d_o, nullptr);
+  const int nb = W_.nb, nC = W_.nC;
+  float* qf = at<float>(ws, W_.qf);
+  float* kf = at<float>(ws, W_.kf);
+  float* vf = at<float>(ws, W_.vf);
+  float* dof = at<float>(ws, W_.dof);
+  float* gam = at<float>(ws, W_.gam);
+  float* lam = at<float>(ws, W_.lam);
+  float* bet = at<float>(ws, W_.beta);
+  float* gcum = at<float>(ws, W_.gcum);
+  float* ms = at<float>(ws, W_.ms);
+  float* tm = at<float>(ws, W_.tm);
+  float* pm = at<float>(ws, W_.p);
+  float* u = at<float>(ws, W_.u);
+  float* sc = at<float>(ws, W_.sc);
+  float* dsc = at<float>(ws, W_.dsc);
+  float* x1 = at<float>(ws, W_.x1);
+  float* x2 = at<float>(ws, W_.x2);
+  float* x3 = at<float>(ws, W_.x3);
+  float* x4 = at<float>(ws, W_.x4);
+  float* x5 = at<float>(ws, W_.x5);
+  float* x6 = at<float>(ws, W_.x6);
+  float* m1 = at<float>(ws, W_.m1);
+  float* m2 = at<float>(ws, W_.m2);
+  float* w = at<float>(ws, W_.w);
+  // x3 = P^T dO;  dZ0 = T^T x3 (in w, free after the forward scan)
+  gemm(L, nb, true, false, kC, kD, kC, pm, kC, kCC, dof, kD, kCD, x3, kD, kCD, 1.f);
+  gemm(L, nb, true, false, kC, kD, kC, tm, kC, kCC, x3, kD, kCD, w, kD, kCD, 1.f);
+  if (L.err != cudaSuccess) return L.err;
+  {
+    const size_t smem = (2 * kCD + kCC) * sizeof(float);
+    L.err = cudaFuncSetAttribute(gdn_scan_bwd, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (L.err != cudaSuccess) return L.err;
+    gdn_scan_bwd<<<dim3(a.H, kD / kScanRows), 32 * kScanRows, smem, st>>>(nC, kf, qf, dof, tm, w,
+                                                                         gam, lam, bet, dsc);
+    L.check();
+  }
+  // x1 = K S0^T (the state's read-out at k_t);  x2 = Y = V - diag(gamma) x1
+  gemm(L, nb, false, true, kC, kD, kD, kf, kD, kCD, sc, kD, kDD, x1, kD, kCD, 1.f);
+  if (L.err != cudaSuccess) return L.err;
+  gdn_rows<<<dim3(nb, kC), kD, 0, st>>>(x2, x1, gam, nullptr, -1.f, vf, 1.f);
+  L.check();
+  // x4 = K dSC^T;  dU = x3 + diag(lam) x4 (into x3)
+  gemm(L, nb, false, true, kC, kD, kD, kf, kD, kCD, dsc, kD, kDD, x4, kD, kCD, 1.f);
+  if (L.err != cudaSuccess) return L.err;
+  gdn_rows<<<dim3(nb, kC), kD, 0, st>>>(x3, x4, lam, nullptr, 1.f, x3, 1.f);
+  L.check();
+  // x5 = dZ = T^T dU;  x6 = dY = diag(beta) dZ (= dV)
+  gemm(L, nb, true, false, kC, kD, kC, tm, kC, kCC, x3, kD, kCD, x5, kD, kCD, 1.f);
+  if (L.err != cudaSuccess) return L.err;
+  gdn_rows<<<dim3(nb, kC), kD, 0, st>>>(x6, x5, bet, nullptr, 1.f, nullptr, 0.f);
+  L.check();
+  // m1 = dA = -(dZ U^T) strictly lower;  tm <- dMs = diag(beta) dA (T is no longer needed)
+  gemm(L, nb, false, true, kC, kC, kD, x5, kD, kCD, u, kD, kCD, m1, kC, kCC, -1.f, nullptr, kC, 0, 2);
+  gemm(L, nb, false, true, kC, kC, kD, x5, kD, kCD, u, kD, kCD, tm, kC, kCC, -1.f, bet, kC, 0, 2);
+  // m2 = dP = dO U^T lower incl.
+  gemm(L, nb, false, true, kC, kC, kD, dof, kD, kCD, u, kD, kCD, m2, kC, kCC, 1.f, nullptr, kC, 0, 1);
+  // x3 <- Q' S0^T (for dg; dU is no longer needed)
+  gemm(L, nb, false, true, kC, kD, kD, qf, kD, kCD, sc, kD, kDD, x3, kD, kCD, 1.f);
+  if (L.err != cudaSuccess) return L.err;
+  {
+    GdnScalarIn in;
+    in.u = u; in.kds = x4; in.dof = dof; in.qs = x3; in.dy = x6; in.ks = x1; in.dz = x5;
+    in.y = x2; in.dp = m2; in.p = pm; in.dms = tm; in.ms = ms; in.da = m1; in.sc = sc;
+    in.dsc = dsc; in.gam = gam; in.lam = lam;
+    gdn_scalar_grads<<<dim3(nC, a.H), 256, 0, st>>>(in, a.R, a.H, accumulate, dg, dbeta);
+    L.check();
+  }
+  if (L.err != cudaSuccess) return L.err;
+  // dP * Gam (m2) and dKK = dMs * Gam (tm), lower / strictly lower
+  gdn_decay<<<nb, 256, 0, st>>>(m2, gcum, nullptr, 0, nullptr);
+  L.check();
+  if (L.err != cudaSuccess) return L.err;
+  gdn_decay<<<nb, 256, 0, st>>>(tm, gcum, nullptr, 1, nullptr);
+  L.check();
+  // dQ' = diag(gamma) dO S0 + (dP Gam) K   -> x1 (K S0^T no longer needed)
+  gemm(L, nb, false, false, kC, kD, kD, dof, kD, kCD, sc, kD, kDD, x1, kD, kCD, 1.f, gam);
+  gemm(L, nb, false, false, kC, kD, kC, m2, kC, kCC, kf, kD, kCD, x1, kD, kCD, 1.f, nullptr, kC, 1);
+  // dK = diag(lam) U dSC + (dP Gam)^T Q' - diag(gamma) dY S0 + (dKK + dKK^T) K  -> x4
+  gemm(L, nb, false, false, kC, kD, kD, u, kD, kCD, dsc, kD, kDD, x4, kD, kCD, 1.f, lam);
+  gemm(L, nb, true, false, kC, kD, kC, m2, kC, kCC, qf, kD, kCD, x4, kD, kCD, 1.f, nullptr, kC, 1);
+  gemm(L, nb, false, false, kC, kD, kD, x6, kD, kCD, sc, kD, kDD, x4, kD, kCD, -1.f, gam, kC, 1);
+  gemm(L, nb, false, false, kC, kD, kC, tm, kC, kCC, kf, kD, kCD, x4, kD, kCD, 1.f, nullptr, kC, 1);
+  gemm(L, nb, true, false, kC, kD, kC, tm, kC, kCC, kf, kD, kCD, x4, kD, kCD, 1.f, nullptr, kC, 1);
+  if (L.err != cudaSuccess) return L.err;
+  gdn_store_grads<<<dim3(nC, a.H), kD, 0, st>>>(x1, x4, x6, a.R, a.H, a.scale, accumulate, dq, dk,
+                                                dv);
+  L.check();
+  return L.err;
+}

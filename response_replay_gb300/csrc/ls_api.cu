@@ -91,9 +91,15 @@ ls_status check_replay(const ls_kv_cache* c, int R, int Hq, int num_splits) {
   return LS_OK;
 }
 
-LsSched make_sched_units(const ls_kv_cache* c, int units, int num_splits, int tile, int ctas) {
+// resp_tokens: the response tokens a unit's causal item can reach (R, or members x R
+// for packed members).  Token-block-major units when the prompt is short next to them.
+LsSched make_sched_units(const ls_kv_cache* c, int units, int num_splits, int tile, int ctas,
+                         int64_t resp_tokens) {
   const int ntiles = (int)((c->num_tokens + tile - 1) / tile);
-  return ls_make_sched(units, ntiles, num_splits, ctas);
+  LsSched s = ls_make_sched(units, ntiles, num_splits, ctas);
+  const int64_t resp_tiles = (resp_tokens + tile - 1) / tile;
+  s.tb_major = (int64_t)ntiles < 8 * resp_tiles ? 1 : 0;
+  return s;
 }
 
 LsSched make_sched(const ls_kv_cache* c, int R, int Hq, int num_splits, int unit_rows, int tile,
@@ -101,7 +107,7 @@ LsSched make_sched(const ls_kv_cache* c, int R, int Hq, int num_splits, int unit
   (void)unit_rows;
   const int units = fwd ? ls_fwd_units(R, Hq, c->num_kv_heads)
                         : ls_bwd_units(R, Hq, c->num_kv_heads);
-  return make_sched_units(c, units, num_splits, tile, ctas);
+  return make_sched_units(c, units, num_splits, tile, ctas, R);
 }
 
 // Forward geometry of `members` responses of R tokens.  Short responses (grouped-query
@@ -243,7 +249,7 @@ ls_status ls_replay_attn_fwd_members_workspace(const ls_kv_cache* cache, int R, 
   DevInfo d;
   if ((s = dev_info(&d)) != LS_OK) return s;
   const LsSched sc = make_sched_units(cache, f.units, num_splits, ls_fwd_tile(),
-                                      d.sms * ls_fwd_ctas_per_sm());
+                                      d.sms * ls_fwd_ctas_per_sm(), f.rt);
   *bytes = fwd_ws(sc, ls_fwd_unit_rows()).total;
   return LS_OK;
 }
@@ -265,7 +271,7 @@ ls_status ls_replay_attn_fwd_members(const ls_kv_cache* cache, const void* q, co
   DevInfo d;
   if ((s = dev_info(&d)) != LS_OK) return s;
   const LsSched sc = make_sched_units(cache, f.units, num_splits, ls_fwd_tile(),
-                                      d.sms * ls_fwd_ctas_per_sm());
+                                      d.sms * ls_fwd_ctas_per_sm(), f.rt);
   const FwdWs w = fwd_ws(sc, ls_fwd_unit_rows());
   if (w.total > 0 && (!workspace || workspace_bytes < w.total || !aligned16(workspace)))
     return LS_ERR_WORKSPACE;
@@ -450,6 +456,66 @@ ls_status ls_grpo_logp(const void* logits, ls_dtype dtype, int64_t T, int V,
   return from_cuda(ls_launch_grpo_logp(logits, dtype == LS_BF16, T, V, targets, ref_logp,
                                        logp_out, lse_out, kl_out, d.err, d.sms,
                                        (cudaStream_t)stream));
+}
+
+ls_status ls_gdn_replay_fwd_workspace(int R, int H, size_t* bytes) {
+  if (R < 0 || H <= 0 || !bytes) return LS_ERR_INVALID_ARG;
+  if ((int64_t)R * H >= (1ll << 31) || (R + 63) / 64 * (int64_t)H > 65535) return LS_ERR_UNSUPPORTED;
+  *bytes = ls_gdn_ws_bytes(R, H, false);
+  return LS_OK;
+}
+
+ls_status ls_gdn_replay_bwd_workspace(int R, int H, size_t* bytes) {
+  if (R < 0 || H <= 0 || !bytes) return LS_ERR_INVALID_ARG;
+  if ((int64_t)R * H >= (1ll << 31) || (R + 63) / 64 * (int64_t)H > 65535) return LS_ERR_UNSUPPORTED;
+  *bytes = ls_gdn_ws_bytes(R, H, true);
+  return LS_OK;
+}
+
+ls_status ls_gdn_replay_fwd(const float* state0, const void* q, const void* k, const void* v,
+                            const float* g, const float* beta, int R, int H, float scale, void* o,
+                            float* state_out, void* workspace, size_t workspace_bytes,
+                            ls_stream_t stream) {
+  size_t need = 0;
+  ls_status s = ls_gdn_replay_fwd_workspace(R, H, &need);
+  if (s != LS_OK) return s;
+  if (!isfinite(scale)) return LS_ERR_INVALID_ARG;
+  if (!state0 || !aligned16(state0) || (state_out && !aligned16(state_out))) return LS_ERR_INVALID_ARG;
+  if (R == 0) {  // no tokens: the state passes through unchanged
+    if (state_out && state_out != state0)
+      return from_cuda(cudaMemcpyAsync(state_out, state0, (size_t)H * 128 * 128 * 4,
+                                       cudaMemcpyDeviceToDevice, (cudaStream_t)stream));
+    return LS_OK;
+  }
+  const void* ptrs[] = {q, k, v, g, beta, o};
+  for (const void* p : ptrs)
+    if (!p || !aligned16(p)) return LS_ERR_INVALID_ARG;
+  if (!workspace || workspace_bytes < need || !aligned16(workspace)) return LS_ERR_WORKSPACE;
+  DevInfo d;
+  if ((s = dev_info(&d)) != LS_OK) return s;
+  LsGdnArgs a{state0, q, k, v, g, beta, R, H, scale};
+  return from_cuda(ls_launch_gdn_fwd(a, o, state_out, workspace, (cudaStream_t)stream));
+}
+
+ls_status ls_gdn_replay_bwd(const float* state0, const void* q, const void* k, const void* v,
+                            const float* g, const float* beta, const void* d_o, int R, int H,
+                            float scale, int accumulate, float* dq, float* dk, float* dv, float* dg,
+                            float* dbeta, void* workspace, size_t workspace_bytes,
+                            ls_stream_t stream) {
+  size_t need = 0;
+  ls_status s = ls_gdn_replay_bwd_workspace(R, H, &need);
+  if (s != LS_OK) return s;
+  if (!isfinite(scale)) return LS_ERR_INVALID_ARG;
+  if (R == 0) return LS_OK;
+  const void* ptrs[] = {state0, q, k, v, g, beta, d_o, dq, dk, dv, dg, dbeta};
+  for (const void* p : ptrs)
+    if (!p || !aligned16(p)) return LS_ERR_INVALID_ARG;
+  if (!workspace || workspace_bytes < need || !aligned16(workspace)) return LS_ERR_WORKSPACE;
+  DevInfo d;
+  if ((s = dev_info(&d)) != LS_OK) return s;
+  LsGdnArgs a{state0, q, k, v, g, beta, R, H, scale};
+  return from_cuda(ls_launch_gdn_bwd(a, d_o, accumulate != 0, dq, dk, dv, dg, dbeta, workspace,
+                                     (cudaStream_t)stream));
 }
 
 ls_status ls_selftest_wait_timeout(ls_stream_t stream) {

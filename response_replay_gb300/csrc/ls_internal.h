@@ -128,3 +128,21 @@ struct LsGrpoArgs {
 };
 size_t ls_grpo_ws_bytes(int64_t T, int G);
 cudaError_t ls_launch_grpo(const LsGrpoArgs& a, int num_sms, cudaStream_t st);
+
+// Gated-DeltaNet replay (gdn_replay.cu): head dims 128 (d_k = d_v), 64-token chunks.
+struct LsGdnArgs {
+  const float* state0;  // [H][128][128] (d_v x d_k): the captured state
+  const void* q;        // bf16 [R][H][128]
+  const void* k;
+  const void* v;
+  const float* g;       // [R][H] log decay
+  const float* beta;    // [R][H]
+  int32_t R, H;
+  float scale;
+};
+size_t ls_gdn_ws_bytes(int R, int H, bool bwd);
+cudaError_t ls_launch_gdn_fwd(const LsGdnArgs& a, void* o, float* state_out, void* ws,
+                              cudaStream_t st);
+cudaError_t ls_launch_gdn_bwd(const LsGdnArgs& a, const void* d_o, int accumulate, float* dq,
+                              float* dk, float* dv, float* dg, float* dbeta, void* ws,
+                              cudaStream_t st);

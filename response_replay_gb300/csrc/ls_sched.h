@@ -40,6 +40,8 @@ struct LsSched {
   int32_t nsplit;      // non-empty prompt splits S (0 when P == 0)
   int32_t tail_units;  // T = U - W*C
   int32_t pieces;      // Q pieces per tail unit (1: tail units are processed whole)
+  int32_t tb_major;    // unit numbering (ls_tiles.cuh, unit_coords): token block major when
+                       // the response's causal keys are a large share of a unit's work
 
   LS_HD int32_t items_per_unit() const { return nsplit + 1; }
   LS_HD int32_t tail_unit0() const { return waves * ctas; }
@@ -89,6 +91,7 @@ inline LsSched ls_make_sched(int32_t units, int32_t ntiles, int32_t num_splits, 
   s.waves = units / c;
   s.tail_units = units - s.waves * c;
   s.pieces = 1;
+  s.tb_major = 0;
   if (s.tail_units > 0) {
     const int32_t qmax = ipu < 64 ? ipu : 64;  // a piece holds at least one item
     double best = ls_tail_cost(s.tail_units, 1, c);

@@ -28,15 +28,23 @@
 #define LS_TILE_HD
 #endif
 
-// Units are numbered token block major: unit ul (within its member) covers token block
-// tb = ul / ngrp of group grp = ul % ngrp, where a group is a query head (pack = 1,
-// ngrp = Hq) or a KV head (packed, ngrp = Hkv).  A persistent wave then holds units of
-// neighbouring token blocks, whose response items (the causal keys up to the block) are
-// about as long as each other, so short prompts do not leave a wave waiting on its one
-// longest unit; every KV head still appears in every wave.
-LS_TILE_HD inline void unit_coords(int32_t ul, int32_t ngrp, int32_t* grp, int32_t* tb) {
-  *tb = ul / ngrp;
-  *grp = ul - *tb * ngrp;
+// Unit numbering.  Group grp is a query head (pack = 1, ngrp = Hq groups) or a KV head
+// (packed, ngrp = Hkv), tb the unit's token block (nTB blocks).  Group major (unit = grp
+// nTB + tb) puts the units of one head next to each other, so a persistent wave holds
+// few KV heads and each prompt K/V tile serves many CTAs from L2.  Token block major
+// (unit = tb ngrp + grp) puts units of neighbouring token blocks in a wave, whose
+// response items (causal keys up to the block) are about as long as each other: used
+// when those items are a large share of the work (short prompts), where group major
+// would leave every wave waiting on its one longest unit.
+LS_TILE_HD inline void unit_coords(int32_t ul, int32_t ngrp, int32_t nTB, bool tb_major,
+                                   int32_t* grp, int32_t* tb) {
+  if (tb_major) {
+    *tb = ul / ngrp;
+    *grp = ul - *tb * ngrp;
+  } else {
+    *grp = ul / nTB;
+    *tb = ul - *grp * nTB;
+  }
 }
 
 struct TileRec {
@@ -94,7 +102,7 @@ struct TileCursor {
         ul = u - m * upm;
       }
       int32_t grp, tb;                 // query head (pack 1) or kv head (packed)
-      unit_coords(ul, ngrp, &grp, &tb);
+      unit_coords(ul, ngrp, nTB, walk.sc->tb_major != 0, &grp, &tb);
       t0 = tb * tok_per_unit;
       kvh = pack == 1 ? grp / g : grp;
       h = pack == 1 ? grp : grp * g;

@@ -480,8 +480,9 @@ __global__ void __launch_bounds__(kD) bwd_dq_tc_combine(const LsAttnArgs a, cons
   const int tu = blockIdx.x, T = sc.tail_units, Q = sc.pieces;
   const int u = sc.tail_unit0() + tu;
   const int tok_per_unit = kTile / a.pack;
+  const int nTB = (a.R + tok_per_unit - 1) / tok_per_unit;
   int grp, tb;
-  unit_coords(u, a.pack == 1 ? a.hq : a.hkv, &grp, &tb);
+  unit_coords(u, a.pack == 1 ? a.hq : a.hkv, nTB, sc.tb_major != 0, &grp, &tb);
   const int t0 = tb * tok_per_unit;
   const int h0 = a.pack == 1 ? grp : grp * a.g;
   const int col = threadIdx.x;

@@ -547,8 +547,9 @@ __global__ void __launch_bounds__(kD) replay_fwd_tc_combine(const LsAttnArgs a, 
   const int u = sc.tail_unit0() + tu;
   const int tpt = kTile / a.pack, tok_per_unit = a.tiles * tpt;
   const int m = u / a.upm, ul = u - m * a.upm;  // member, unit within the member
+  const int nTB = (a.rt + tok_per_unit - 1) / tok_per_unit;
   int grp, tb;
-  unit_coords(ul, a.pack == 1 ? a.hq : a.hkv, &grp, &tb);
+  unit_coords(ul, a.pack == 1 ? a.hq : a.hkv, nTB, sc.tb_major != 0, &grp, &tb);
   const int t0 = tb * tok_per_unit;
   const int h0 = a.pack == 1 ? grp : grp * a.g;
   const int col = threadIdx.x;

@@ -177,3 +177,34 @@ def make_grpo(resp_lens, vocab: int, logits_dtype: str, rewards: str, seed: int,
     return GrpoInputs(logits, torch.from_numpy(targets).to(device),
                       torch.from_numpy(r).to(device), torch.from_numpy(lens).to(device),
                       torch.from_numpy(noise.astype(np.float32)).to(device))
+
+
+@dataclass
+class GdnInputs:
+    """Inputs of a Gated-DeltaNet replay (one layer): the captured state and the response
+    tokens' projections."""
+    state0: torch.Tensor   # [H][128][128] fp32 (d_v x d_k)
+    q: torch.Tensor        # [R][H][128] bf16, unit rows
+    k: torch.Tensor        # [R][H][128] bf16, unit rows
+    v: torch.Tensor        # [R][H][128] bf16
+    g: torch.Tensor        # [R][H] fp32, log decay
+    beta: torch.Tensor     # [R][H] fp32 in (0, 1)
+    d_o: torch.Tensor      # [R][H][128] bf16
+
+
+def make_gdn(R: int, H: int, seed: int, device="cpu", d: int = HEAD_DIM,
+             decay=(0.9, 1.0), state_std: float = 0.1) -> GdnInputs:
+    """q, k: N(0,1) rows normalised to unit length (the layer normalises them); v, dO:
+    N(0,1); decay exp(g) ~ U(decay); beta = sigmoid(N(0,1)); state0 ~ N(0, state_std)."""
+    gg = gen(device, seed)
+    q = torch.randn(R, H, d, generator=gg, device=device)
+    k = torch.randn(R, H, d, generator=gg, device=device)
+    q = (q / q.norm(dim=2, keepdim=True).clamp_min(1e-6)).to(torch.bfloat16)
+    k = (k / k.norm(dim=2, keepdim=True).clamp_min(1e-6)).to(torch.bfloat16)
+    v = torch.randn(R, H, d, generator=gg, device=device).to(torch.bfloat16)
+    d_o = torch.randn(R, H, d, generator=gg, device=device).to(torch.bfloat16)
+    u = torch.rand(R, H, generator=gg, device=device)
+    g = torch.log(decay[0] + (decay[1] - decay[0]) * u).float().contiguous()
+    beta = torch.sigmoid(torch.randn(R, H, generator=gg, device=device)).float().contiguous()
+    state0 = (torch.randn(H, d, d, generator=gg, device=device) * state_std).float()
+    return GdnInputs(state0, q, k, v, g, beta, d_o)

@@ -223,5 +223,51 @@ def grpo_logp(logits: torch.Tensor, targets: torch.Tensor, ref_logp: torch.Tenso
     return logp, lse, kl
 
 
+def gdn_replay_fwd(state0: torch.Tensor, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                   g: torch.Tensor, beta: torch.Tensor, scale: float, o: torch.Tensor | None = None,
+                   state_out: torch.Tensor | None = None, with_state: bool = False, stream=None):
+    """Gated-DeltaNet replay of R tokens from a captured state: state0 fp32 [H][128][128],
+    q/k/v bf16 [R][H][128], g/beta fp32 [R][H].  Returns (o, state_out or None)."""
+    R, H, _ = q.shape
+    _check(state0, "state0", torch.float32, (H, HEAD_DIM, HEAD_DIM))
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _check(t, n, torch.bfloat16, (R, H, HEAD_DIM))
+    _check(g, "g", torch.float32, (R, H))
+    _check(beta, "beta", torch.float32, (R, H))
+    if o is None:
+        o = torch.empty_like(q)
+    if state_out is None and with_state:
+        state_out = torch.empty_like(state0)
+    nbytes = B.ls_gdn_replay_fwd_workspace(R, H)
+    ws = workspace(nbytes, q.device, "gdn")
+    B.ls_gdn_replay_fwd(state0.data_ptr(), q.data_ptr(), k.data_ptr(), v.data_ptr(), g.data_ptr(),
+                        beta.data_ptr(), R, H, scale, o.data_ptr(),
+                        state_out.data_ptr() if state_out is not None else None, ws.data_ptr(),
+                        ws.numel(), _stream(stream))
+    return o, state_out
+
+
+def gdn_replay_bwd(state0, q, k, v, g, beta, d_o, scale: float, grads=None,
+                   accumulate: bool = False, stream=None):
+    """Gradients (dq, dk, dv, dg, dbeta) of the replay with the captured state stopgrad."""
+    R, H, _ = q.shape
+    _check(d_o, "d_o", torch.bfloat16, (R, H, HEAD_DIM))
+    if grads is None:
+        dev = q.device
+        grads = (torch.empty((R, H, HEAD_DIM), dtype=torch.float32, device=dev),
+                 torch.empty((R, H, HEAD_DIM), dtype=torch.float32, device=dev),
+                 torch.empty((R, H, HEAD_DIM), dtype=torch.float32, device=dev),
+                 torch.empty((R, H), dtype=torch.float32, device=dev),
+                 torch.empty((R, H), dtype=torch.float32, device=dev))
+    dq, dk, dv, dg, db = grads
+    nbytes = B.ls_gdn_replay_bwd_workspace(R, H)
+    ws = workspace(nbytes, q.device, "gdn")
+    B.ls_gdn_replay_bwd(state0.data_ptr(), q.data_ptr(), k.data_ptr(), v.data_ptr(), g.data_ptr(),
+                        beta.data_ptr(), d_o.data_ptr(), R, H, scale, int(accumulate),
+                        dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), dg.data_ptr(), db.data_ptr(),
+                        ws.data_ptr(), ws.numel(), _stream(stream))
+    return dq, dk, dv, dg, db
+
+
 def last_device_error(stream=None) -> int:
     return B.ls_last_device_error(_stream(stream))

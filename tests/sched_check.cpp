@@ -96,12 +96,17 @@ static int check(int U, int nt, int sp, int C) {
 
 // Packed members: `members` responses of R tokens numbered back to back (RT tokens), a
 // tile holding 128 / pack tokens of one KV head, `tiles` tiles per unit.
-static int check_packed(int R, int members, int pack, int hkv, int nt, int sp, int C) {
+static int check_packed(int R, int members, int pack, int hkv, int nt, int sp, int C,
+                        int tb_major) {
   constexpr int kTile = 128, kUnitRows = 256;
   const int RT = R * members, tpt = kTile / pack;
   const int tiles = RT <= tpt ? 1 : 2, tpu = tiles * tpt;
   const int nTB = (RT + tpu - 1) / tpu, U = hkv * nTB;
   LsSched s = ls_make_sched(U, nt, sp, C);
+  s.tb_major = tb_major;
+  // the unit's KV head and first token under either numbering
+  auto kvh_of = [&](int u) { return tb_major ? u % hkv : u / nTB; };
+  auto t0_of = [&](int u) { return (tb_major ? u / hkv : u % nTB) * tpu; };
   std::map<int, std::multiset<std::pair<int, int>>> got;  // unit -> (member, first key)
   for (int c = 0; c < s.ctas; ++c) {
     TileCursor<kUnitRows, kTile, 2> cur(s, c, R, pack, pack, tiles, INT32_MAX, RT);
@@ -116,7 +121,7 @@ static int check_packed(int R, int members, int pack, int hkv, int nt, int sp, i
         return 1;
       }
       ++nf;
-      if (r.t0 != (r.u / hkv) * tpu || r.kvh != r.u % hkv) {
+      if (r.t0 != t0_of(r.u) || r.kvh != kvh_of(r.u)) {
         std::printf("FAIL packed unit decode R=%d members=%d pack=%d\n", R, members, pack);
         return 1;
       }
@@ -134,7 +139,7 @@ static int check_packed(int R, int members, int pack, int hkv, int nt, int sp, i
   }
   for (int u = 0; u < U; ++u) {
     std::multiset<std::pair<int, int>> want;
-    const int t0 = (u / hkv) * tpu, ve = t0 + tpu < RT ? t0 + tpu : RT;
+    const int t0 = t0_of(u), ve = t0 + tpu < RT ? t0 + tpu : RT;
     for (int m = t0 / R; m * R < ve; ++m) {
       const int e = (ve < (m + 1) * R ? ve : (m + 1) * R) - m * R;  // last row's token + 1
       for (int k = 0; k * kTile < e; ++k) want.insert({m, k * kTile});
@@ -247,8 +252,10 @@ int main() {
         for (int hkv : {1, 4})
           for (int C : {1, 7, 152})
             for (int nt : {0, 7}) {
-              pbad += check_packed(R, members, pack, hkv, nt, 3, C);
-              ++pn;
+              for (int tbm = 0; tbm < 2; ++tbm) {
+                pbad += check_packed(R, members, pack, hkv, nt, 3, C, tbm);
+                ++pn;
+              }
             }
   bad += pbad;
   std::printf("%d/%d packed-member walks ok\n", pn - pbad, pn);
