@@ -782,6 +782,89 @@ def run_self_sweep(args, local_rank: int):
         }), flush=True)
 
 
+# ------------------------------------------------------------------ Gated-DeltaNet replay
+
+GDN_HEADS = 32
+
+
+def gdn_flops(R: int, H: int) -> tuple[float, float]:
+    """fp32 FLOPs the chunked Gated-DeltaNet replay executes per layer (64-token chunks,
+    128 x 128 state): per chunk and head the forward does K K^T, the triangular inverse,
+    W and U0, the state hand-off, Q K^T, Q S^T and P U; the backward recomputes the
+    forward's chunk algebra and runs the adjoint products and its own hand-off."""
+    C, d = 64, 128
+    nc = -(-R // C) * H
+    fwd = 2.0 * (C * C * d + C ** 3 / 6 + 2 * C * C * d + 2 * C * d * d + C * C * d + C * d * d
+                 + C * C * d)
+    bwd_extra = 2.0 * (2 * C * C * d + 2 * C * d * d + C * C * d + 2 * C * d * d + C * C * d
+                       + 2 * C * C * d + C * C * d + C * d * d + (C * d * d + C * C * d)
+                       + (2 * C * d * d + 3 * C * C * d))
+    rec = fwd - 2.0 * (C * C * d + C * d * d + C * C * d)   # the forward minus its output
+    return nc * fwd, nc * (rec + bwd_extra)
+
+
+def alu_peak_tflops(sm_mhz: float = 2070.0, sms: int = 152) -> float:
+    """fp32 FMA peak of the CUDA cores: 128 FMA lanes per SM per clock, 2 FLOPs each."""
+    return sms * 128 * 2 * sm_mhz * 1e6 / 1e12
+
+
+def run_gdn_sweep(args, local_rank: int):
+    """Supplementary, labelled lines: one Gated-DeltaNet layer replayed from a captured
+    state (32 heads, 128 x 128 state), forward and backward times per response length,
+    against the CUDA cores' fp32 peak (the chunk algebra runs in fp32 on them)."""
+    import torch
+
+    from response_replay_gb300 import synthetic as syn
+    from response_replay_gb300 import torch_api as api
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    for R in [int(x) for x in args.sweep_gdn.split(",")]:
+        inp = syn.make_gdn(R, GDN_HEADS, 21, dev)
+        scale = D ** -0.5
+        o = torch.empty_like(inp.q)
+        grads = api.gdn_replay_bwd(inp.state0, inp.q, inp.k, inp.v, inp.g, inp.beta, inp.d_o,
+                                   scale)
+
+        def fwd():
+            api.gdn_replay_fwd(inp.state0, inp.q, inp.k, inp.v, inp.g, inp.beta, scale, o=o,
+                               stream=stream)
+
+        def bwd():
+            api.gdn_replay_bwd(inp.state0, inp.q, inp.k, inp.v, inp.g, inp.beta, inp.d_o, scale,
+                               grads=grads, stream=stream)
+
+        def timed(fn):
+            for _ in range(args.warmup):
+                fn()
+            torch.cuda.synchronize()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for _ in range(args.steps):
+                fn()
+            b.record(stream)
+            torch.cuda.synchronize()
+            return a.elapsed_time(b) / args.steps
+
+        f_ms, b_ms = timed(fwd), timed(bwd)
+        f_fl, b_fl = gdn_flops(R, GDN_HEADS)
+        peak = alu_peak_tflops()
+        print(json.dumps({
+            "sweep": "Gated-DeltaNet replay from a captured state, one layer (supplementary)",
+            "R": R, "config": {"workload": f"R={R} response tokens, H={GDN_HEADS} heads, "
+                                           "128 x 128 fp32 state, 64-token chunks"},
+            "fwd_ms": f_ms, "bwd_ms": b_ms,
+            "fwd_tflops": f_fl / (f_ms * 1e-3) / 1e12, "bwd_tflops": b_fl / (b_ms * 1e-3) / 1e12,
+            "roofline": {"bound": "alu", "peak": peak, "unit": "TFLOP/s",
+                         "peak_source": "152 SMs x 128 fp32 FMA lanes x 2 x 2.07 GHz",
+                         "fwd_frac": f_fl / (f_ms * 1e-3) / 1e12 / peak,
+                         "bwd_frac": b_fl / (b_ms * 1e-3) / 1e12 / peak},
+            "steps": args.steps, "warmup": args.warmup,
+        }), flush=True)
+
+
 # ------------------------------------------------------------------ reference arm
 
 def run_reference(args, rank: int, world: int):
@@ -857,6 +940,9 @@ def main():
     ap.add_argument("--sweep-self", default=None,
                     help="comma-separated response lengths: supplementary no-prompt (causal "
                          "self-attention) lines instead of the headline step")
+    ap.add_argument("--sweep-gdn", default=None,
+                    help="comma-separated response lengths: supplementary Gated-DeltaNet "
+                         "replay lines instead of the headline step")
     ap.add_argument("--sweep-short", default=None,
                     help="comma-separated response lengths: supplementary short-R sweep "
                          "(one JSON line each) instead of the headline step")
@@ -876,6 +962,10 @@ def main():
     if args.sweep_self:
         if rank == 0:
             run_self_sweep(args, local_rank)
+        return
+    if args.sweep_gdn:
+        if rank == 0:
+            run_gdn_sweep(args, local_rank)
         return
     if world > 1:
         import torch
