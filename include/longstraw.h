@@ -179,6 +179,39 @@ ls_status ls_replay_attn_bwd(const ls_kv_cache* cache, const void* q, const void
                              float* dv_resp, void* workspace, size_t workspace_bytes,
                              ls_stream_t stream);
 
+/* ---------------------------------------------------------------- ragged members
+ * ls_replay_attn_fwd_ragged / ls_replay_attn_bwd_ragged: the replay of `members`
+ * responses of different lengths lens[0 .. members) (a HOST array) over the same captured
+ * prompt, in one forward and one backward launch.  The members' tokens lie back to back
+ * (member m's token t is row off_m + t, off_m = lens[0] + ... + lens[m-1], T = the sum):
+ *   q, o, d_o: bf16 [T][Hq][128]; k_resp, v_resp: bf16 [T][num_kv_heads][128];
+ *   lse: fp32 [T][Hq]; dq: fp32 [T][Hq][128]; dk_resp, dv_resp: fp32 [T][num_kv_heads][128].
+ * Each member sees the whole prompt and its own response keys j <= t only (a
+ * block-diagonal causal mask over the concatenation), so member m's results equal the
+ * one-response calls on its slices, up to rounding; the work of all members shares one
+ * schedule over the GPU (the pages replay members one by one; on one GPU with room for
+ * a whole group this fills the SMs better for short and mixed lengths).  As for the
+ * batched forward, inputs must be finite: a member's rows meet other members' keys with
+ * zero weight, and a non-finite value times zero is not zero.
+ * 1 <= members <= 64, lens[m] >= 0 (empty members allowed); T <= 2^30, and for the
+ * backward of more than one member T <= 131,072 (LS_ERR_UNSUPPORTED otherwise).  Other
+ * arguments, workspace and errors as ls_replay_attn_fwd / ls_replay_attn_bwd, which are
+ * these calls with one member. */
+ls_status ls_replay_attn_fwd_ragged_workspace(const ls_kv_cache* cache, const int32_t* lens,
+                                              int members, int Hq, int num_splits, size_t* bytes);
+ls_status ls_replay_attn_fwd_ragged(const ls_kv_cache* cache, const void* q, const void* k_resp,
+                                    const void* v_resp, const int32_t* lens, int members, int Hq,
+                                    float softmax_scale, int num_splits, void* o, float* lse,
+                                    void* workspace, size_t workspace_bytes, ls_stream_t stream);
+ls_status ls_replay_attn_bwd_ragged_workspace(const ls_kv_cache* cache, const int32_t* lens,
+                                              int members, int Hq, int num_splits, size_t* bytes);
+ls_status ls_replay_attn_bwd_ragged(const ls_kv_cache* cache, const void* q, const void* k_resp,
+                                    const void* v_resp, const void* o, const float* lse,
+                                    const void* d_o, const int32_t* lens, int members, int Hq,
+                                    float softmax_scale, int num_splits, int accumulate, float* dq,
+                                    float* dk_resp, float* dv_resp, void* workspace,
+                                    size_t workspace_bytes, ls_stream_t stream);
+
 /* ---------------------------------------------------------------- GRPO loss
  * The clipped surrogate of the digest's Method section,
  *   L = -(1/G) sum_i (1/R_i) sum_t min(rho_{i,t} A_i, clip(rho_{i,t}, 1-eps, 1+eps) A_i),

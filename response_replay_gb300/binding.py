@@ -27,7 +27,8 @@ EXPORTED = (
     "ls_grpo_loss_fwd_bwd_noalloc", "ls_selftest_wait_timeout", "ls_grpo_logp",
     "ls_replay_attn_fwd_members_workspace", "ls_replay_attn_fwd_members",
     "ls_gdn_replay_fwd_workspace", "ls_gdn_replay_fwd", "ls_gdn_replay_bwd_workspace",
-    "ls_gdn_replay_bwd",
+    "ls_gdn_replay_bwd", "ls_replay_attn_fwd_ragged_workspace", "ls_replay_attn_fwd_ragged",
+    "ls_replay_attn_bwd_ragged_workspace", "ls_replay_attn_bwd_ragged",
 )
 
 
@@ -81,6 +82,11 @@ def lib() -> C.CDLL:
             "ls_selftest_wait_timeout": [P],
             "ls_grpo_logp": [P, i32, i64, i32, P, P, P, P, P, P],
             "ls_status_string": [i32],
+            "ls_replay_attn_fwd_ragged_workspace": [cache, P, i32, i32, i32, szp],
+            "ls_replay_attn_fwd_ragged": [cache, P, P, P, P, i32, i32, f32, i32, P, P, P, sz, P],
+            "ls_replay_attn_bwd_ragged_workspace": [cache, P, i32, i32, i32, szp],
+            "ls_replay_attn_bwd_ragged": [cache, P, P, P, P, P, P, P, i32, i32, f32, i32, i32, P,
+                                          P, P, P, sz, P],
             "ls_gdn_replay_fwd_workspace": [i32, i32, szp],
             "ls_gdn_replay_bwd_workspace": [i32, i32, szp],
             "ls_gdn_replay_fwd": [P, P, P, P, P, P, i32, i32, f32, P, P, P, sz, P],
@@ -244,3 +250,40 @@ def ls_gdn_replay_bwd(state0: int, q: int, k: int, v: int, g: int, beta: int, d_
     _ok("ls_gdn_replay_bwd",
         lib().ls_gdn_replay_bwd(state0, q, k, v, g, beta, d_o, R, H, scale, accumulate, dq, dk,
                                 dv, dg, dbeta, workspace, workspace_bytes, stream))
+
+
+def _lens(lens) -> tuple:
+    arr = (C.c_int32 * len(lens))(*[int(x) for x in lens])
+    return arr, len(lens)
+
+
+def ls_replay_attn_fwd_ragged_workspace(cache: ls_kv_cache, lens, Hq: int, num_splits: int) -> int:
+    arr, n = _lens(lens)
+    return _size("ls_replay_attn_fwd_ragged_workspace", C.byref(cache), arr, n, Hq, num_splits)
+
+
+def ls_replay_attn_fwd_ragged(cache: ls_kv_cache, q: int, k_resp: int, v_resp: int, lens, Hq: int,
+                              softmax_scale: float, num_splits: int, o: int, lse: int,
+                              workspace: int, workspace_bytes: int, stream: int = 0) -> None:
+    """lens: the members' response lengths (host)."""
+    arr, n = _lens(lens)
+    _ok("ls_replay_attn_fwd_ragged",
+        lib().ls_replay_attn_fwd_ragged(C.byref(cache), q, k_resp, v_resp, arr, n, Hq,
+                                        softmax_scale, num_splits, o, lse, workspace,
+                                        workspace_bytes, stream))
+
+
+def ls_replay_attn_bwd_ragged_workspace(cache: ls_kv_cache, lens, Hq: int, num_splits: int) -> int:
+    arr, n = _lens(lens)
+    return _size("ls_replay_attn_bwd_ragged_workspace", C.byref(cache), arr, n, Hq, num_splits)
+
+
+def ls_replay_attn_bwd_ragged(cache: ls_kv_cache, q: int, k_resp: int, v_resp: int, o: int, lse: int,
+                              d_o: int, lens, Hq: int, softmax_scale: float, num_splits: int,
+                              accumulate: int, dq: int, dk_resp: int, dv_resp: int, workspace: int,
+                              workspace_bytes: int, stream: int = 0) -> None:
+    arr, n = _lens(lens)
+    _ok("ls_replay_attn_bwd_ragged",
+        lib().ls_replay_attn_bwd_ragged(C.byref(cache), q, k_resp, v_resp, o, lse, d_o, arr, n,
+                                        Hq, softmax_scale, num_splits, accumulate, dq, dk_resp,
+                                        dv_resp, workspace, workspace_bytes, stream))

@@ -5,6 +5,7 @@
 #include <mutex>
 
 #include "../../include/longstraw.h"
+#include "ls_dkdv.h"
 #include "ls_internal.h"
 
 // One error word per device (module globals are instantiated per device).  Kernels
@@ -93,12 +94,20 @@ ls_status check_replay(const ls_kv_cache* c, int R, int Hq, int num_splits) {
 
 // resp_tokens: the response tokens a unit's causal item can reach (R, or members x R
 // for packed members).  Token-block-major units when the prompt is short next to them.
+// seg: the response's segments (NULL: one response of resp_tokens).
 LsSched make_sched_units(const ls_kv_cache* c, int units, int num_splits, int tile, int ctas,
-                         int64_t resp_tokens) {
+                         int64_t resp_tokens, const LsSegs* seg = nullptr) {
   const int ntiles = (int)((c->num_tokens + tile - 1) / tile);
   LsSched s = ls_make_sched(units, ntiles, num_splits, ctas);
   const int64_t resp_tiles = (resp_tokens + tile - 1) / tile;
   s.tb_major = (int64_t)ntiles < 8 * resp_tiles ? 1 : 0;
+  if (seg) {
+    s.seg = *seg;
+  } else {
+    s.seg.n = 1;
+    s.seg.off[0] = 0;
+    s.seg.off[1] = (int32_t)resp_tokens;
+  }
   return s;
 }
 
@@ -159,7 +168,8 @@ FwdWs fwd_ws(const LsSched& sc, int unit_rows) {
 struct BwdWs {
   size_t delta, dt, lse2t, part_dq, part_dkdv, total;
 };
-BwdWs bwd_ws(const LsSched& sc, int unit_rows, int R, int Hq, int Hkv, int sms) {
+BwdWs bwd_ws(const LsSched& sc, int unit_rows, int R, int Hq, int Hkv, int sms,
+             const LsSegs* segs = nullptr) {
   BwdWs w;
   size_t p = 0;
   const size_t rp = (size_t)(R + 127) / 128 * 128;
@@ -172,7 +182,7 @@ BwdWs bwd_ws(const LsSched& sc, int unit_rows, int R, int Hq, int Hkv, int sms) 
   w.part_dq = p;
   p = align256(p + (sc.has_partials() ? (size_t)sc.num_pieces() * unit_rows * kHeadDim * 4 : 0));
   w.part_dkdv = p;
-  p = align256(p + ls_dkdv_part_bytes(R, Hq, Hkv, sms));
+  p = align256(p + ls_dkdv_part_bytes(R, Hq, Hkv, sms, segs));
   w.total = p;
   return w;
 }
@@ -202,6 +212,26 @@ LsAttnArgs attn_args(const ls_kv_cache* c, const void* q, const void* kr, const 
   a.scale_log2 = scale * 1.4426950408889634f;
   a.err = err;
   return a;
+}
+
+// Segments of ragged members laid out back to back (host lens); the total in *T and the
+// longest member in *rmax.
+ls_status make_segs(const int32_t* lens, int members, LsSegs* seg, int* T, int* rmax) {
+  if (!lens || members < 1 || members > kLsMaxSegs) return LS_ERR_INVALID_ARG;
+  int64_t t = 0;
+  int m = 0;
+  seg->n = members;
+  seg->off[0] = 0;
+  for (int i = 0; i < members; ++i) {
+    if (lens[i] < 0) return LS_ERR_INVALID_ARG;
+    t += lens[i];
+    if (t > (1 << 30)) return LS_ERR_UNSUPPORTED;
+    seg->off[i + 1] = (int32_t)t;
+    if (lens[i] > m) m = lens[i];
+  }
+  *T = (int)t;
+  *rmax = m;
+  return LS_OK;
 }
 
 }  // namespace
@@ -302,36 +332,45 @@ ls_status ls_replay_attn_fwd(const ls_kv_cache* cache, const void* q, const void
                                     o, lse, workspace, workspace_bytes, stream);
 }
 
-ls_status ls_replay_attn_bwd_workspace(const ls_kv_cache* cache, int R, int Hq, int num_splits,
-                                       size_t* bytes) {
+}  // extern "C"
+
+namespace {
+
+// Backward of one response of R tokens cut into the segments `seg` (one segment: a
+// single response; several: ragged members back to back, each seeing the prompt and its
+// own keys).  resp_max: the longest segment.
+ls_status bwd_workspace_impl(const ls_kv_cache* cache, int R, const LsSegs& seg, int resp_max,
+                             int Hq, int num_splits, size_t* bytes) {
   ls_status s = check_replay(cache, R, Hq, num_splits);
   if (s != LS_OK) return s;
   if (!bytes) return LS_ERR_INVALID_ARG;
+  if (seg.n > 1 && (R + 127) / 128 > kLsMaxDkTiles) return LS_ERR_UNSUPPORTED;
   DevInfo d;
   if ((s = dev_info(&d)) != LS_OK) return s;
-  const LsSched sc = make_sched(cache, R, Hq, num_splits, ls_bwd_unit_rows(), ls_bwd_tile(),
-                                d.sms * ls_bwd_ctas_per_sm(), false);
-  *bytes = bwd_ws(sc, ls_bwd_unit_rows(), R, Hq, cache->num_kv_heads, d.sms).total;
+  const LsSched sc = make_sched_units(cache, ls_bwd_units(R, Hq, cache->num_kv_heads), num_splits,
+                                      ls_bwd_tile(), d.sms * ls_bwd_ctas_per_sm(), resp_max, &seg);
+  *bytes = bwd_ws(sc, ls_bwd_unit_rows(), R, Hq, cache->num_kv_heads, d.sms, &seg).total;
   return LS_OK;
 }
 
-ls_status ls_replay_attn_bwd(const ls_kv_cache* cache, const void* q, const void* k_resp,
-                             const void* v_resp, const void* o, const float* lse, const void* d_o,
-                             int R, int Hq, float softmax_scale, int num_splits, int accumulate,
-                             float* dq, float* dk_resp, float* dv_resp, void* workspace,
-                             size_t workspace_bytes, ls_stream_t stream) {
+ls_status bwd_impl(const ls_kv_cache* cache, const void* q, const void* k_resp, const void* v_resp,
+                   const void* o, const float* lse, const void* d_o, int R, const LsSegs& seg,
+                   int resp_max, int Hq, float softmax_scale, int num_splits, int accumulate,
+                   float* dq, float* dk_resp, float* dv_resp, void* workspace,
+                   size_t workspace_bytes, ls_stream_t stream) {
   ls_status s = check_replay(cache, R, Hq, num_splits);
   if (s != LS_OK) return s;
   if (!isfinite(softmax_scale) || !(softmax_scale > 0.f)) return LS_ERR_INVALID_ARG;
   if (R == 0) return LS_OK;
+  if (seg.n > 1 && (R + 127) / 128 > kLsMaxDkTiles) return LS_ERR_UNSUPPORTED;
   const void* ptrs[] = {q, k_resp, v_resp, o, lse, d_o, dq, dk_resp, dv_resp};
   for (const void* p : ptrs)
     if (!p || !aligned16(p)) return LS_ERR_INVALID_ARG;
   DevInfo d;
   if ((s = dev_info(&d)) != LS_OK) return s;
-  const LsSched sc = make_sched(cache, R, Hq, num_splits, ls_bwd_unit_rows(), ls_bwd_tile(),
-                                d.sms * ls_bwd_ctas_per_sm(), false);
-  const BwdWs w = bwd_ws(sc, ls_bwd_unit_rows(), R, Hq, cache->num_kv_heads, d.sms);
+  const LsSched sc = make_sched_units(cache, ls_bwd_units(R, Hq, cache->num_kv_heads), num_splits,
+                                      ls_bwd_tile(), d.sms * ls_bwd_ctas_per_sm(), resp_max, &seg);
+  const BwdWs w = bwd_ws(sc, ls_bwd_unit_rows(), R, Hq, cache->num_kv_heads, d.sms, &seg);
   if (!workspace || workspace_bytes < w.total || !aligned16(workspace)) return LS_ERR_WORKSPACE;
   LsAttnArgs a = attn_args(cache, q, k_resp, v_resp, R, Hq, softmax_scale, d.err);
   a.pack = ls_bwd_pack(R, Hq, cache->num_kv_heads);
@@ -349,6 +388,112 @@ ls_status ls_replay_attn_bwd(const ls_kv_cache* cache, const void* q, const void
   b.dv = dv_resp;
   b.accumulate = accumulate != 0;
   return from_cuda(ls_launch_replay_bwd(a, sc, b, d.sms, (cudaStream_t)stream));
+}
+
+LsSegs single_seg(int R) {
+  LsSegs s;
+  s.n = 1;
+  s.off[0] = 0;
+  s.off[1] = R;
+  return s;
+}
+
+}  // namespace
+
+extern "C" {
+
+ls_status ls_replay_attn_bwd_workspace(const ls_kv_cache* cache, int R, int Hq, int num_splits,
+                                       size_t* bytes) {
+  return bwd_workspace_impl(cache, R, single_seg(R), R, Hq, num_splits, bytes);
+}
+
+ls_status ls_replay_attn_bwd(const ls_kv_cache* cache, const void* q, const void* k_resp,
+                             const void* v_resp, const void* o, const float* lse, const void* d_o,
+                             int R, int Hq, float softmax_scale, int num_splits, int accumulate,
+                             float* dq, float* dk_resp, float* dv_resp, void* workspace,
+                             size_t workspace_bytes, ls_stream_t stream) {
+  return bwd_impl(cache, q, k_resp, v_resp, o, lse, d_o, R, single_seg(R), R, Hq, softmax_scale,
+                  num_splits, accumulate, dq, dk_resp, dv_resp, workspace, workspace_bytes, stream);
+}
+
+ls_status ls_replay_attn_bwd_ragged_workspace(const ls_kv_cache* cache, const int32_t* lens,
+                                              int members, int Hq, int num_splits, size_t* bytes) {
+  LsSegs seg;
+  int T = 0, rmax = 0;
+  ls_status s = make_segs(lens, members, &seg, &T, &rmax);
+  if (s != LS_OK) return s;
+  return bwd_workspace_impl(cache, T, seg, rmax, Hq, num_splits, bytes);
+}
+
+ls_status ls_replay_attn_bwd_ragged(const ls_kv_cache* cache, const void* q, const void* k_resp,
+                                    const void* v_resp, const void* o, const float* lse,
+                                    const void* d_o, const int32_t* lens, int members, int Hq,
+                                    float softmax_scale, int num_splits, int accumulate, float* dq,
+                                    float* dk_resp, float* dv_resp, void* workspace,
+                                    size_t workspace_bytes, ls_stream_t stream) {
+  LsSegs seg;
+  int T = 0, rmax = 0;
+  ls_status s = make_segs(lens, members, &seg, &T, &rmax);
+  if (s != LS_OK) return s;
+  return bwd_impl(cache, q, k_resp, v_resp, o, lse, d_o, T, seg, rmax, Hq, softmax_scale,
+                  num_splits, accumulate, dq, dk_resp, dv_resp, workspace, workspace_bytes, stream);
+}
+
+ls_status ls_replay_attn_fwd_ragged_workspace(const ls_kv_cache* cache, const int32_t* lens,
+                                              int members, int Hq, int num_splits, size_t* bytes) {
+  LsSegs seg;
+  int T = 0, rmax = 0;
+  ls_status s = make_segs(lens, members, &seg, &T, &rmax);
+  if (s != LS_OK) return s;
+  s = check_replay(cache, T, Hq, num_splits);
+  if (s != LS_OK) return s;
+  if (!bytes) return LS_ERR_INVALID_ARG;
+  const FwdGeom f = fwd_geom(T, 1, Hq, cache->num_kv_heads);
+  if (!f.ok) return LS_ERR_UNSUPPORTED;
+  DevInfo d;
+  if ((s = dev_info(&d)) != LS_OK) return s;
+  const LsSched sc = make_sched_units(cache, f.units, num_splits, ls_fwd_tile(),
+                                      d.sms * ls_fwd_ctas_per_sm(), rmax, &seg);
+  *bytes = fwd_ws(sc, ls_fwd_unit_rows()).total;
+  return LS_OK;
+}
+
+ls_status ls_replay_attn_fwd_ragged(const ls_kv_cache* cache, const void* q, const void* k_resp,
+                                    const void* v_resp, const int32_t* lens, int members, int Hq,
+                                    float softmax_scale, int num_splits, void* o, float* lse,
+                                    void* workspace, size_t workspace_bytes, ls_stream_t stream) {
+  LsSegs seg;
+  int T = 0, rmax = 0;
+  ls_status s = make_segs(lens, members, &seg, &T, &rmax);
+  if (s != LS_OK) return s;
+  s = check_replay(cache, T, Hq, num_splits);
+  if (s != LS_OK) return s;
+  if (!isfinite(softmax_scale) || !(softmax_scale > 0.f)) return LS_ERR_INVALID_ARG;
+  if (T == 0) return LS_OK;
+  const FwdGeom f = fwd_geom(T, 1, Hq, cache->num_kv_heads);
+  if (!f.ok) return LS_ERR_UNSUPPORTED;
+  const void* ptrs[] = {q, k_resp, v_resp, o, lse};
+  for (const void* p : ptrs)
+    if (!p || !aligned16(p)) return LS_ERR_INVALID_ARG;
+  DevInfo d;
+  if ((s = dev_info(&d)) != LS_OK) return s;
+  const LsSched sc = make_sched_units(cache, f.units, num_splits, ls_fwd_tile(),
+                                      d.sms * ls_fwd_ctas_per_sm(), rmax, &seg);
+  const FwdWs w = fwd_ws(sc, ls_fwd_unit_rows());
+  if (w.total > 0 && (!workspace || workspace_bytes < w.total || !aligned16(workspace)))
+    return LS_ERR_WORKSPACE;
+  LsAttnArgs a = attn_args(cache, q, k_resp, v_resp, T, Hq, softmax_scale, d.err);
+  a.pack = f.pack;
+  a.tiles = f.tiles;
+  a.members = 1;
+  a.upm = f.upm;
+  a.rt = f.rt;
+  LsFwdOut out;
+  out.o = o;
+  out.lse = lse;
+  out.part_o = reinterpret_cast<float*>(static_cast<char*>(workspace) + w.part_o);
+  out.part_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) + w.part_lse);
+  return from_cuda(ls_launch_replay_fwd(a, sc, out, (cudaStream_t)stream));
 }
 
 ls_status ls_grpo_workspace(int64_t T, int G, size_t* bytes) {

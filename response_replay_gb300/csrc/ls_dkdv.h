@@ -16,9 +16,15 @@
 // deterministic).  A CTA range has at most one segment of each kind, so the slots are
 // unique.
 //
+// Ragged members replayed in one launch form one response of several segments
+// (ls_sched.h, LsSegs); a key then meets only the query tiles up to the end of its own
+// segment, so key tile kt's span of query tiles comes from a table instead of nT - kt.
+//
 // Included by host and device code.
 #pragma once
 #include <stdint.h>
+
+#include "ls_sched.h"
 
 #ifdef __CUDACC__
 #define LS_DK_HD __host__ __device__ __forceinline__
@@ -26,32 +32,55 @@
 #define LS_DK_HD inline
 #endif
 
+constexpr int kLsMaxDkTiles = 1024;  // key tiles of a segmented response (131,072 tokens)
+
 struct LsDkdvGeom {
   int32_t nT;       // key (and query) tiles of 128 tokens: ceil(R / 128)
   int32_t g;        // query heads per KV head
   int32_t hkv;      // KV heads
-  int64_t ikv;      // iterations per KV head: g nT (nT + 1) / 2
+  int64_t ikv;      // iterations per KV head: g nT (nT + 1) / 2 (one segment)
   int64_t total;    // hkv * ikv
   int64_t per_cta;  // c
   int32_t ctas;     // ceil(total / c)
+  int32_t ragged;   // spans from pre[] (several segments)
+  int32_t pre[kLsMaxDkTiles + 1];  // ragged: query tiles met by key tiles 0 .. kt-1
 
-  // First iteration of key tile kt of KV head c, and its iteration count.
+  // Query tiles key tile kt meets, the first iteration of key tile kt of KV head c, and
+  // its iteration count.
+  LS_DK_HD int32_t span(int32_t kt) const { return ragged ? pre[kt + 1] - pre[kt] : nT - kt; }
   LS_DK_HD int64_t tile_begin(int32_t c, int32_t kt) const {
-    return (int64_t)c * ikv + (int64_t)g * ((int64_t)kt * nT - (int64_t)kt * (kt - 1) / 2);
+    const int64_t before = ragged ? (int64_t)pre[kt]
+                                  : (int64_t)kt * nT - (int64_t)kt * (kt - 1) / 2;
+    return (int64_t)c * ikv + (int64_t)g * before;
   }
-  LS_DK_HD int64_t tile_iters(int32_t kt) const { return (int64_t)g * (nT - kt); }
+  LS_DK_HD int64_t tile_iters(int32_t kt) const { return (int64_t)g * span(kt); }
   // Partial-sum slot of CTA b's segment of a key tile that starts at iteration s.
   LS_DK_HD int32_t slot(int32_t b, int64_t s) const {
     return s <= (int64_t)b * per_cta ? 2 * b : 2 * b + 1;
   }
 };
 
-inline LsDkdvGeom ls_make_dkdv_geom(int32_t R, int32_t g, int32_t hkv, int32_t max_ctas) {
+// segs: the response's segments (NULL or one segment: a single response); with several
+// segments nT must not exceed kLsMaxDkTiles (the caller checks).
+inline LsDkdvGeom ls_make_dkdv_geom(int32_t R, int32_t g, int32_t hkv, int32_t max_ctas,
+                                    const LsSegs* segs = nullptr) {
   LsDkdvGeom d;
   d.nT = (R + 127) / 128;
   d.g = g;
   d.hkv = hkv;
-  d.ikv = (int64_t)g * d.nT * (d.nT + 1) / 2;
+  d.ragged = segs && segs->n > 1 && d.nT <= kLsMaxDkTiles ? 1 : 0;
+  d.pre[0] = 0;
+  if (d.ragged) {
+    for (int32_t kt = 0; kt < d.nT; ++kt) {
+      const int32_t last = (kt + 1) * 128 < R ? (kt + 1) * 128 - 1 : R - 1;
+      int32_t lo, hi;
+      ls_seg_bounds(*segs, last, &lo, &hi);  // the last key's segment ends latest
+      d.pre[kt + 1] = d.pre[kt] + ((hi + 127) / 128 - kt);
+    }
+    d.ikv = (int64_t)g * d.pre[d.nT];
+  } else {
+    d.ikv = (int64_t)g * d.nT * (d.nT + 1) / 2;
+  }
   d.total = d.ikv * hkv;
   const int32_t C = max_ctas > 0 ? max_ctas : 1;
   d.per_cta = d.total > 0 ? (d.total + C - 1) / C : 1;
@@ -89,7 +118,7 @@ struct LsDkdvWalk {
         r -= gm->tile_iters(kt);
         ++kt;
       }
-      const int32_t span = gm->nT - kt;
+      const int32_t span = gm->span(kt);
       hh = (int32_t)(r / span);
       tt = kt + (int32_t)(r - (int64_t)hh * span);
       ts = gm->tile_begin(kvh, kt);
@@ -109,7 +138,7 @@ struct LsDkdvWalk {
     it->complete = ts >= r0 && te <= r1;
     it->slot = it->complete ? -1 : gm->slot(b, ts);
     ++i;
-    if (++tt == gm->nT) {  // next query head, or next key tile
+    if (++tt == kt + gm->span(kt)) {  // next query head, or next key tile
       if (++hh == gm->g) {
         hh = 0;
         if (++kt == gm->nT) {

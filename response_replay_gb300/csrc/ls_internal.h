@@ -98,9 +98,9 @@ cudaError_t ls_launch_bwd_dq(const LsAttnArgs& a, const LsSched& sc, const LsBwd
                              cudaStream_t st);
 
 // Response-key dK / dV (tcgen05) and the bytes of its partial-sum workspace.
-size_t ls_dkdv_part_bytes(int R, int hq, int hkv, int num_sms);
-cudaError_t ls_launch_bwd_dkdv(const LsAttnArgs& a, const LsBwdIn& b, int num_sms,
-                               cudaStream_t st);
+size_t ls_dkdv_part_bytes(int R, int hq, int hkv, int num_sms, const LsSegs* segs);
+cudaError_t ls_launch_bwd_dkdv(const LsAttnArgs& a, const LsSegs& seg, const LsBwdIn& b,
+                               int num_sms, cudaStream_t st);
 
 cudaError_t ls_launch_replay_bwd(const LsAttnArgs& a, const LsSched& sc, const LsBwdIn& b,
                                  int num_sms, cudaStream_t st);

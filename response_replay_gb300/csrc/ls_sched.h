@@ -31,6 +31,27 @@
 #define LS_HD inline
 #endif
 
+// Segments of a concatenated response (ragged members replayed in one launch):
+// segment s holds tokens [off[s], off[s + 1]).  Every token sees the whole prompt and
+// the response keys of its own segment up to itself, so members never see each other.
+// A single response is one segment [0, R).
+constexpr int kLsMaxSegs = 64;
+struct LsSegs {
+  int32_t n;
+  int32_t off[kLsMaxSegs + 1];
+};
+
+// Bounds [lo, hi) of the segment holding token t (t past the end: the last segment).
+LS_HD void ls_seg_bounds(const LsSegs& s, int32_t t, int32_t* lo, int32_t* hi) {
+  int32_t a = 0, b = s.n;  // off[a] <= t < off[b]
+  while (b - a > 1) {
+    const int32_t m = (a + b) >> 1;
+    if (s.off[m] <= t) a = m; else b = m;
+  }
+  *lo = s.off[a];
+  *hi = s.off[a + 1];
+}
+
 struct LsSched {
   int32_t units;       // U
   int32_t ctas;        // C (grid size)
@@ -42,6 +63,7 @@ struct LsSched {
   int32_t pieces;      // Q pieces per tail unit (1: tail units are processed whole)
   int32_t tb_major;    // unit numbering (ls_tiles.cuh, unit_coords): token block major when
                        // the response's causal keys are a large share of a unit's work
+  LsSegs seg;          // segments of the response tokens (one: a single response)
 
   LS_HD int32_t items_per_unit() const { return nsplit + 1; }
   LS_HD int32_t tail_unit0() const { return waves * ctas; }
@@ -92,6 +114,9 @@ inline LsSched ls_make_sched(int32_t units, int32_t ntiles, int32_t num_splits, 
   s.tail_units = units - s.waves * c;
   s.pieces = 1;
   s.tb_major = 0;
+  s.seg.n = 1;
+  s.seg.off[0] = 0;
+  s.seg.off[1] = 0;
   if (s.tail_units > 0) {
     const int32_t qmax = ipu < 64 ? ipu : 64;  // a piece holds at least one item
     double best = ls_tail_cost(s.tail_units, 1, c);

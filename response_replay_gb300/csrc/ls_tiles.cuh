@@ -121,6 +121,11 @@ struct TileCursor {
         } else {
           const int32_t qe = t0 + tok_per_unit < R ? t0 + tok_per_unit : R;
           t_end = (qe + Tile - 1) / Tile;
+          if (walk.sc->seg.n > 1) {  // keys before the first token's segment: unseen
+            int32_t lo, hi;
+            ls_seg_bounds(walk.sc->seg, t0, &lo, &hi);
+            t = lo / Tile;
+          }
         }
       } else {
         walk.sc->split_tiles(s, &t, &t_end);

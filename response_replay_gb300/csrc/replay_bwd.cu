@@ -80,5 +80,5 @@ cudaError_t ls_launch_replay_bwd(const LsAttnArgs& a, const LsSched& sc, const L
   if (e != cudaSuccess) return e;
   e = ls_launch_bwd_dq(a, sc, b, st);
   if (e != cudaSuccess) return e;
-  return ls_launch_bwd_dkdv(a, b, num_sms, st);
+  return ls_launch_bwd_dkdv(a, sc.seg, b, num_sms, st);
 }

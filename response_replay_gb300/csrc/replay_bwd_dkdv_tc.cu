@@ -93,12 +93,13 @@ struct DkdvArgs {
   float* part;              // [2 ctas][2][128][128]: dK, dV partial sums
   int32_t accumulate;
   uint32_t* err;
+  LsSegs seg;               // segments of the response (one: a single response)
 };
 
 __device__ __forceinline__ uint32_t bar_addr(uint32_t base, int i) { return base + kOffBar + 8 * i; }
 
 __global__ void __launch_bounds__(kThreads, 1)
-bwd_dkdv_tc_kernel(const __grid_constant__ TmapSet tm, const DkdvArgs a,
+bwd_dkdv_tc_kernel(const __grid_constant__ TmapSet tm, const __grid_constant__ DkdvArgs a,
                    const __grid_constant__ LsDkdvGeom gm) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -285,8 +286,14 @@ bwd_dkdv_tc_kernel(const __grid_constant__ TmapSet tm, const DkdvArgs a,
     LsDkdvWalk w(gm, blockIdx.x);
     LsDkdvIter it;
     uint32_t n = 0, sg = 0;
+    int32_t key_hi = a.R, key_kt = -1;  // end of this row's key's segment (its last query + 1)
     while (w.next(&it)) {
       const uint32_t st = n & 1;
+      if (a.seg.n > 1 && it.kt != key_kt) {
+        key_kt = it.kt;
+        int32_t lo;
+        ls_seg_bounds(a.seg, it.kt * kTile + row, &lo, &key_hi);
+      }
       const float* lse2 = reinterpret_cast<const float*>(smem + kOffStat + st * kStatBytes) + 64 * cgrp;
       const float* dd = lse2 + kTile;
       if (!mbar_wait(bar_addr(sbase, B_S_FULL), n & 1)) { fail(); break; }
@@ -313,6 +320,12 @@ bwd_dkdv_tc_kernel(const __grid_constant__ TmapSet tm, const DkdvArgs a,
 #pragma unroll
         for (int k = 0; k < 64; ++k)
           if (64 * cgrp + k < row) p[k] = 0.f;
+      }
+      if ((it.tt + 1) * kTile > key_hi) {  // queries of later segments do not see this key
+        const int32_t q0 = it.tt * kTile + 64 * cgrp;
+#pragma unroll
+        for (int k = 0; k < 64; ++k)
+          if (q0 + k >= key_hi) p[k] = 0.f;
       }
       {
         uint32_t pk[32];
@@ -404,7 +417,8 @@ bwd_dkdv_tc_kernel(const __grid_constant__ TmapSet tm, const DkdvArgs a,
 // Grid: (KV head x key tile, 16 groups of 8 keys); 128 threads, one float4 of dK or dV of
 // one key each per step.  Blocks of key tiles that one CTA held whole exit at once.
 constexpr int kCombineKeys = 8;
-__global__ void __launch_bounds__(128) bwd_dkdv_tc_combine(const DkdvArgs a, const LsDkdvGeom gm) {
+__global__ void __launch_bounds__(128) bwd_dkdv_tc_combine(const __grid_constant__ DkdvArgs a,
+                                                           const __grid_constant__ LsDkdvGeom gm) {
   const int kvh = blockIdx.x / gm.nT, kt = blockIdx.x % gm.nT;
   const int64_t s = gm.tile_begin(kvh, kt), e = s + gm.tile_iters(kt);
   const int b0 = (int)(s / gm.per_cta), b1 = (int)((e - 1) / gm.per_cta);
@@ -433,15 +447,16 @@ __global__ void __launch_bounds__(128) bwd_dkdv_tc_combine(const DkdvArgs a, con
 
 }  // namespace
 
-size_t ls_dkdv_part_bytes(int R, int hq, int hkv, int num_sms) {
-  const LsDkdvGeom gm = ls_make_dkdv_geom(R, hq / hkv, hkv, num_sms);
+size_t ls_dkdv_part_bytes(int R, int hq, int hkv, int num_sms, const LsSegs* segs) {
+  const LsDkdvGeom gm = ls_make_dkdv_geom(R, hq / hkv, hkv, num_sms, segs);
   return (size_t)2 * gm.ctas * 2 * kTile * kD * sizeof(float);
 }
 
-cudaError_t ls_launch_bwd_dkdv(const LsAttnArgs& a, const LsBwdIn& b, int num_sms,
-                               cudaStream_t st) {
-  const LsDkdvGeom gm = ls_make_dkdv_geom(a.R, a.g, a.hkv, num_sms);
+cudaError_t ls_launch_bwd_dkdv(const LsAttnArgs& a, const LsSegs& seg, const LsBwdIn& b,
+                               int num_sms, cudaStream_t st) {
+  const LsDkdvGeom gm = ls_make_dkdv_geom(a.R, a.g, a.hkv, num_sms, &seg);
   if (gm.total == 0) return cudaSuccess;
+  if (seg.n > 1 && !gm.ragged) return cudaErrorInvalidValue;  // checked by the entry point
   TmapSet tm;
   const uint32_t box[3] = {64, 1, kTile};
   {
@@ -469,6 +484,7 @@ cudaError_t ls_launch_bwd_dkdv(const LsAttnArgs& a, const LsBwdIn& b, int num_sm
   d.part = b.part_dkdv;
   d.accumulate = b.accumulate;
   d.err = a.err;
+  d.seg = seg;
   cudaError_t e =
       cudaFuncSetAttribute(bwd_dkdv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;

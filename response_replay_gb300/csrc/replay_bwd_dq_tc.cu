@@ -86,8 +86,8 @@ using DqCursor = TileCursor<kUnitRows, kTile>;
 __device__ __forceinline__ uint32_t bar_addr(uint32_t base, int i) { return base + kOffBar + 8 * i; }
 
 __global__ void __launch_bounds__(kThreads, 1)
-bwd_dq_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a, const __grid_constant__ LsSched sc,
-                 const LsBwdIn b) {
+bwd_dq_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a,
+                 const __grid_constant__ LsSched sc, const LsBwdIn b) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -358,6 +358,7 @@ bwd_dq_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a, const _
     TileRec r;
     uint32_t j = 0, uc = 0;
     float lse2 = 0.f, dd = 0.f;
+    int32_t row_lo = 0;  // first response key this row's token may see (segments)
     while (cursor.next(&r)) {
       const int32_t tq = r.t0 + tok_off;
       const int32_t hrow = row_used ? r.h + head_off : r.h;
@@ -365,15 +366,20 @@ bwd_dq_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a, const _
         const int64_t idx = (int64_t)(tq < a.R ? tq : a.R - 1) * a.hq + hrow;
         lse2 = b.lse[idx] * kLog2e;
         dd = b.delta[idx];
+        if (sc.seg.n > 1) {
+          int32_t hi;
+          ls_seg_bounds(sc.seg, tq, &row_lo, &hi);
+        }
       }
       const uint32_t db = j & 1;  // dP buffer of tile j; dS(j) is written over it
       if (!mbar_wait(bar_addr(sbase, B_S_FULL), j & 1)) { fail(); break; }
       if (!mbar_wait(bar_addr(sbase, B_DP_FULL + db), (j >> 1) & 1)) { fail(); break; }
       tc_fence_after();
-      int32_t lim = kTile;
+      int32_t lim = kTile, lo = 0;  // keys [key0 + lo, key0 + lim) visible
       if (r.resp) {
         const int32_t lr = (tq + 1 < a.R ? tq + 1 : a.R) - r.key0;
         lim = lr < kTile ? lr : kTile;
+        lo = row_lo - r.key0;
       } else if (r.key0 + kTile > a.P) {
         lim = (int32_t)(a.P - r.key0);
       }
@@ -409,10 +415,10 @@ bwd_dq_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a, const _
           d2[i] = ds2.x;
           d2[i + 1] = ds2.y;
         }
-        if (col0 + 32 > lim) {  // only the ragged prompt tail and the diagonal need a mask
+        if (col0 + 32 > lim || col0 < lo) {  // ragged prompt tail, diagonal, segment start
 #pragma unroll
           for (int i = 0; i < 32; ++i)
-            if (col0 + i >= lim) d2[i] = 0.f;
+            if (col0 + i >= lim || col0 + i < lo) d2[i] = 0.f;
         }
         uint32_t ds[16];
 #pragma unroll

@@ -85,8 +85,8 @@ __device__ __forceinline__ uint32_t bar_addr(uint32_t base, int i) { return base
 // into shared tiles (Q as one token sequence, 4-D response maps, rows masked by member).
 template <int kMode>
 __global__ void __launch_bounds__(kThreads, 1)
-replay_fwd_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a, const __grid_constant__ LsSched sc,
-                     const LsFwdOut out) {
+replay_fwd_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a,
+                     const __grid_constant__ LsSched sc, const LsFwdOut out) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -388,20 +388,26 @@ replay_fwd_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a, con
         unit_m = row_um;
         tq = vt - rmem * a.R;
       }
-      int32_t lim = kTile;                          // keys [key0, key0 + lim) visible
+      int32_t lim = kTile, lo = 0;                  // keys [key0 + lo, key0 + lim) visible
       if (r.resp) {
         int32_t km = 0, key0 = r.key0;              // member and first key of the tile
         if constexpr (kMode == 2) packed_resp_tile<kTile>(r.key0, unit_m, a.R, &km, &key0);
         const int32_t lr = (tq + 1 < a.R ? tq + 1 : a.R) - key0;
         lim = lr < kTile ? lr : kTile;
         if (kMode == 2 && rmem != km) lim = 0;      // another member's keys
+        if (kMode == 0 && sc.seg.n > 1) {           // keys of earlier segments (ragged
+          int32_t s0, s1;                           // members: response tiles only)
+          ls_seg_bounds(sc.seg, vt, &s0, &s1);
+          lo = s0 - key0;
+        }
       } else if (r.key0 + kTile > a.P) {
         lim = (int32_t)(a.P - r.key0);
       }
-      if (lim < kTile) {  // only the ragged prompt tail and the diagonal need a mask
+      if (lim < kTile || lo > 0) {  // the ragged prompt tail, the diagonal, segment starts
+        const int32_t l0 = lo > 0 ? lo : 0, l1 = lim > l0 ? lim : l0;  // visible [l0, l1)
 #pragma unroll
         for (int j = 0; j < 128; ++j)
-          if (j >= lim) sr[j] = __float_as_uint(-INFINITY);
+          if ((uint32_t)(j - l0) >= (uint32_t)(l1 - l0)) sr[j] = __float_as_uint(-INFINITY);
       }
       // row max: 8 independent chains of three-operand max
       float mx8[8];

@@ -223,6 +223,59 @@ def grpo_logp(logits: torch.Tensor, targets: torch.Tensor, ref_logp: torch.Tenso
     return logp, lse, kl
 
 
+def replay_fwd_ragged(cache: PagedKVCache, q: torch.Tensor, k_resp: torch.Tensor,
+                      v_resp: torch.Tensor, lens, softmax_scale: float, num_splits: int,
+                      o: torch.Tensor | None = None, lse: torch.Tensor | None = None, stream=None):
+    """Forward of ragged members laid out back to back: q [T][Hq][128], k_resp / v_resp
+    [T][Hkv][128], lens the members' lengths (summing to T)."""
+    T, hq, _ = q.shape
+    lens = [int(x) for x in lens]
+    if sum(lens) != T:
+        raise ValueError("member lengths must add up to the token count")
+    _check(q, "q", torch.bfloat16, (T, hq, HEAD_DIM))
+    _check(k_resp, "k_resp", torch.bfloat16, (T, cache.num_kv_heads, HEAD_DIM))
+    _check(v_resp, "v_resp", torch.bfloat16, (T, cache.num_kv_heads, HEAD_DIM))
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((T, hq), dtype=torch.float32, device=q.device)
+    nbytes = B.ls_replay_attn_fwd_ragged_workspace(cache.struct, lens, hq, num_splits)
+    ws = workspace(nbytes, q.device, "fwd")
+    B.ls_replay_attn_fwd_ragged(cache.struct, q.data_ptr(), k_resp.data_ptr(), v_resp.data_ptr(),
+                                lens, hq, softmax_scale, num_splits, o.data_ptr(), lse.data_ptr(),
+                                ws.data_ptr(), ws.numel(), _stream(stream))
+    return o, lse
+
+
+def replay_bwd_ragged(cache: PagedKVCache, q, k_resp, v_resp, o, lse, d_o, lens,
+                      softmax_scale: float, num_splits: int, dq=None, dk=None, dv=None,
+                      accumulate: bool = False, stream=None):
+    """Backward of ragged members laid out back to back (see replay_fwd_ragged)."""
+    T, hq, _ = q.shape
+    hkv = cache.num_kv_heads
+    lens = [int(x) for x in lens]
+    if sum(lens) != T:
+        raise ValueError("member lengths must add up to the token count")
+    for t, n in ((q, "q"), (o, "o"), (d_o, "d_o")):
+        _check(t, n, torch.bfloat16, (T, hq, HEAD_DIM))
+    _check(lse, "lse", torch.float32, (T, hq))
+    dev = q.device
+    if dq is None:
+        dq = torch.empty((T, hq, HEAD_DIM), dtype=torch.float32, device=dev)
+    if dk is None:
+        dk = torch.empty((T, hkv, HEAD_DIM), dtype=torch.float32, device=dev)
+    if dv is None:
+        dv = torch.empty((T, hkv, HEAD_DIM), dtype=torch.float32, device=dev)
+    nbytes = B.ls_replay_attn_bwd_ragged_workspace(cache.struct, lens, hq, num_splits)
+    ws = workspace(nbytes, dev, "bwd")
+    B.ls_replay_attn_bwd_ragged(cache.struct, q.data_ptr(), k_resp.data_ptr(), v_resp.data_ptr(),
+                                o.data_ptr(), lse.data_ptr(), d_o.data_ptr(), lens, hq,
+                                softmax_scale, num_splits, int(accumulate), dq.data_ptr(),
+                                dk.data_ptr(), dv.data_ptr(), ws.data_ptr(), ws.numel(),
+                                _stream(stream))
+    return dq, dk, dv
+
+
 def gdn_replay_fwd(state0: torch.Tensor, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
                    g: torch.Tensor, beta: torch.Tensor, scale: float, o: torch.Tensor | None = None,
                    state_out: torch.Tensor | None = None, with_state: bool = False, stream=None):

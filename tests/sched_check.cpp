@@ -153,11 +153,31 @@ static int check_packed(int R, int members, int pack, int hkv, int nt, int sp, i
   return 0;
 }
 
-static int check_dkdv(int R, int g, int hkv, int C) {
-  const LsDkdvGeom gm = ls_make_dkdv_geom(R, g, hkv, C);
+// lens: ragged members (segments of one response), empty for a single response
+static int check_dkdv(int R, int g, int hkv, int C, const std::vector<int>& lens = {}) {
+  LsSegs seg;
+  seg.n = 1;
+  seg.off[0] = 0;
+  seg.off[1] = R;
+  if (!lens.empty()) {
+    seg.n = (int)lens.size();
+    R = 0;
+    for (int i = 0; i < seg.n; ++i) {
+      R += lens[i];
+      seg.off[i + 1] = R;
+    }
+  }
+  const LsDkdvGeom gm = ls_make_dkdv_geom(R, g, hkv, C, &seg);
   auto bad = [&](const char* what) {
-    std::printf("FAIL dkdv %s R=%d g=%d hkv=%d C=%d\n", what, R, g, hkv, C);
+    std::printf("FAIL dkdv %s R=%d g=%d hkv=%d C=%d segments=%d\n", what, R, g, hkv, C, seg.n);
     return 1;
+  };
+  // the query tiles key tile kt must meet: up to the end of its last key's segment
+  auto want_span = [&](int kt) {
+    const int last = (kt + 1) * 128 < R ? (kt + 1) * 128 - 1 : R - 1;
+    int k = 0;
+    while (seg.off[k + 1] <= last) ++k;
+    return (seg.off[k + 1] + 127) / 128 - kt;
   };
   if (gm.ctas > C || gm.ctas < (gm.total > 0 ? 1 : 0)) return bad("grid");
   const int nT = gm.nT;
@@ -173,7 +193,8 @@ static int check_dkdv(int R, int g, int hkv, int C) {
     int ckvh = -1, ckt = -1;
     while (w.next(&it)) {
       ++n;
-      if (it.tt < it.kt || it.tt >= nT || it.h / g != it.kvh) return bad("iteration");
+      if (it.tt < it.kt || it.tt >= it.kt + want_span(it.kt) || it.h / g != it.kvh)
+        return bad("iteration");
       if (++seen[{it.kvh, it.kt, it.h, it.tt}] != 1) return bad("visited twice");
       const bool new_tile = it.kvh != ckvh || it.kt != ckt;
       if (it.first != new_tile) return bad("first flag");
@@ -197,7 +218,8 @@ static int check_dkdv(int R, int g, int hkv, int C) {
     if (open) return bad("range ends inside a segment");
     if (n > gm.per_cta) return bad("balance");
   }
-  const long long want = (long long)hkv * g * nT * (nT + 1) / 2;
+  long long want = 0;
+  for (int kt = 0; kt < nT; ++kt) want += (long long)hkv * g * want_span(kt);
   if ((long long)seen.size() != want) return bad("coverage");
   // the combine's view of each split key tile
   for (int c = 0; c < hkv; ++c)
@@ -226,6 +248,17 @@ int main() {
           dbad += check_dkdv(R, g, hkv, C);
           ++dn;
         }
+  // ragged members: a cycle of the 4,194,304-position workload's lengths, short and
+  // empty members, members ending inside and on tile boundaries
+  const std::vector<std::vector<int>> raggeds = {
+      {6012, 5295, 2370, 5318, 2053, 7773, 3591, 959}, {1, 0, 5, 300, 0, 128, 127, 129},
+      {128, 128, 256}, {7, 1000, 3}, {4096, 1}};
+  for (const auto& l : raggeds)
+    for (int g : {1, 6})
+      for (int C : {1, 7, 152}) {
+        dbad += check_dkdv(0, g, 4, C, l);
+        ++dn;
+      }
   std::printf("%d/%d response-key walks ok\n", dn - dbad, dn);
   bad += dbad;
   const int Us[] = {1, 2, 3, 7, 8, 96, 151, 152, 153, 304, 384, 768, 1000};
