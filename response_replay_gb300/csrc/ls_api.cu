@@ -278,8 +278,9 @@ ls_status ls_replay_attn_fwd_members_workspace(const ls_kv_cache* cache, int R, 
   if (!f.ok) return LS_ERR_UNSUPPORTED;
   DevInfo d;
   if ((s = dev_info(&d)) != LS_OK) return s;
-  const LsSched sc = make_sched_units(cache, f.units, num_splits, ls_fwd_tile(),
-                                      d.sms * ls_fwd_ctas_per_sm(), f.rt);
+  LsSched sc = make_sched_units(cache, f.units, num_splits, ls_fwd_tile(),
+                                d.sms * ls_fwd_ctas_per_sm(), f.rt);
+  if (members > 1) sc.tb_major = 0;  // the members' layouts walk their units group major
   *bytes = fwd_ws(sc, ls_fwd_unit_rows()).total;
   return LS_OK;
 }
@@ -300,8 +301,9 @@ ls_status ls_replay_attn_fwd_members(const ls_kv_cache* cache, const void* q, co
     if (!p || !aligned16(p)) return LS_ERR_INVALID_ARG;
   DevInfo d;
   if ((s = dev_info(&d)) != LS_OK) return s;
-  const LsSched sc = make_sched_units(cache, f.units, num_splits, ls_fwd_tile(),
-                                      d.sms * ls_fwd_ctas_per_sm(), f.rt);
+  LsSched sc = make_sched_units(cache, f.units, num_splits, ls_fwd_tile(),
+                                d.sms * ls_fwd_ctas_per_sm(), f.rt);
+  if (members > 1) sc.tb_major = 0;  // the members' layouts walk their units group major
   const FwdWs w = fwd_ws(sc, ls_fwd_unit_rows());
   if (w.total > 0 && (!workspace || workspace_bytes < w.total || !aligned16(workspace)))
     return LS_ERR_WORKSPACE;

@@ -15,7 +15,9 @@
 //      hold rows of several members, all sharing each prompt K/V tile.  The response
 //      item of a unit then walks the response keys of every member it holds, member by
 //      member; the softmax masks the rows of the other members.
-// kMode 0 is the one-response walk.
+// kMode 0 is the one-response walk; kMode 3 the same for one response cut into segments
+// (ragged members back to back, ls_sched.h LsSegs): a unit's response walk starts at the
+// key tile of its first token's segment.
 #pragma once
 #include <stdint.h>
 
@@ -70,12 +72,14 @@ LS_HD void packed_resp_tile(int32_t key0, int32_t rm, int32_t R, int32_t* m,
   *key = (t - dm * rnt) * Tile;
 }
 
-template <int UnitRows, int Tile, int kMode = 0>
+// kTbMajor: units numbered token block major (unit_coords); a template parameter so the
+// group-major walk of long prompts compiles to the plain decode.
+template <int UnitRows, int Tile, int kMode = 0, bool kTbMajor = false>
 struct TileCursor {
   LsWalk walk;
   int32_t u, s, t, t_end, slot;
   bool item_first, item_last, item_complete, valid;
-  int32_t R, g, pack, tok_per_unit, nTB, upm, RT, ngrp;
+  int32_t R, g, pack, tok_per_unit, nTB, upm, RT;
   int32_t m, h, kvh, t0;  // derived from u once per item, not per tile
   bool resp;
 
@@ -88,8 +92,7 @@ struct TileCursor {
         RT(RT_ > 0 ? RT_ : R_), m(0), h(0), kvh(0), t0(0), resp(false) {
     tok_per_unit = tiles_ * (Tile / pack);
     nTB = (RT + tok_per_unit - 1) / tok_per_unit;
-    ngrp = (kMode == 1 ? upm : sc.units) / (nTB > 0 ? nTB : 1);
-    if (ngrp < 1) ngrp = 1;
+
   }
 
 
@@ -101,9 +104,15 @@ struct TileCursor {
         m = u / upm;
         ul = u - m * upm;
       }
-      int32_t grp, tb;                 // query head (pack 1) or kv head (packed)
-      unit_coords(ul, ngrp, nTB, walk.sc->tb_major != 0, &grp, &tb);
-      t0 = tb * tok_per_unit;
+      int32_t grp;                     // query head (pack 1) or kv head (packed)
+      if constexpr (kTbMajor) {
+        int32_t ngrp = (kMode == 1 ? upm : walk.sc->units) / nTB, tb;
+        unit_coords(ul, ngrp, nTB, true, &grp, &tb);
+        t0 = tb * tok_per_unit;
+      } else {
+        grp = ul / nTB;
+        t0 = (ul - grp * nTB) * tok_per_unit;
+      }
       kvh = pack == 1 ? grp / g : grp;
       h = pack == 1 ? grp : grp * g;
       resp = (s == walk.sc->nsplit);
@@ -121,7 +130,7 @@ struct TileCursor {
         } else {
           const int32_t qe = t0 + tok_per_unit < R ? t0 + tok_per_unit : R;
           t_end = (qe + Tile - 1) / Tile;
-          if (walk.sc->seg.n > 1) {  // keys before the first token's segment: unseen
+          if constexpr (kMode == 3) {  // keys before the first token's segment: unseen
             int32_t lo, hi;
             ls_seg_bounds(walk.sc->seg, t0, &lo, &hi);
             t = lo / Tile;

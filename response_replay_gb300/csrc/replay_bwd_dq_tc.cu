@@ -81,10 +81,14 @@ struct TmapSet {
   CUtensorMap q, d_o, kp, vp, kr, vr;
 };
 
-using DqCursor = TileCursor<kUnitRows, kTile>;
+// kSeg: one response cut into segments (ragged members back to back); kTb: units
+// numbered token block major (short prompts)
+template <bool kSeg, bool kTb>
+using DqCursor = TileCursor<kUnitRows, kTile, kSeg ? 3 : 0, kTb>;
 
 __device__ __forceinline__ uint32_t bar_addr(uint32_t base, int i) { return base + kOffBar + 8 * i; }
 
+template <bool kSeg, bool kTb>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_dq_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a,
                  const __grid_constant__ LsSched sc, const LsBwdIn b) {
@@ -157,7 +161,7 @@ bwd_dq_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a,
       tma_prefetch_desc(&tm.vp);
       tma_prefetch_desc(&tm.kr);
       tma_prefetch_desc(&tm.vr);
-      DqCursor cur(sc, blockIdx.x, a.R, a.g, a.pack);
+      DqCursor<kSeg, kTb> cur(sc, blockIdx.x, a.R, a.g, a.pack);
       TileRec r;
       uint32_t kc = 0, vc = 0, units = 0, aux = 0;
       const int32_t ps = 1 << a.ps_log2;
@@ -246,7 +250,7 @@ bwd_dq_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a,
       const uint32_t dk_base = sdesc_lo(sbase + kOffK, 16);
       const uint32_t dv_base = sdesc_lo(sbase + kOffV, 16);
       const uint32_t dkm_base = sdesc_lo(sbase + kOffK, kHalfBytes);
-      DqCursor cursor(sc, blockIdx.x, a.R, a.g, a.pack);
+      DqCursor<kSeg, kTb> cursor(sc, blockIdx.x, a.R, a.g, a.pack);
       // first / last of unit of tiles j (f0, l0) and j+1 (f1, l1)
       bool f0 = false, l0 = false, f1 = false, l1 = false;
       bool have0 = cursor.next_flags(&f0, &l0);
@@ -354,7 +358,7 @@ bwd_dq_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a,
     // this thread's row: token row / pack of the unit, head row % pack
     const int32_t tok_off = row / a.pack, head_off = row % a.pack;
     const bool row_used = row < a.pack * (kTile / a.pack);
-    DqCursor cursor(sc, blockIdx.x, a.R, a.g, a.pack);
+    DqCursor<kSeg, kTb> cursor(sc, blockIdx.x, a.R, a.g, a.pack);
     TileRec r;
     uint32_t j = 0, uc = 0;
     float lse2 = 0.f, dd = 0.f;
@@ -366,7 +370,7 @@ bwd_dq_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a,
         const int64_t idx = (int64_t)(tq < a.R ? tq : a.R - 1) * a.hq + hrow;
         lse2 = b.lse[idx] * kLog2e;
         dd = b.delta[idx];
-        if (sc.seg.n > 1) {
+        if constexpr (kSeg) {
           int32_t hi;
           ls_seg_bounds(sc.seg, tq, &row_lo, &hi);
         }
@@ -379,7 +383,7 @@ bwd_dq_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a,
       if (r.resp) {
         const int32_t lr = (tq + 1 < a.R ? tq + 1 : a.R) - r.key0;
         lim = lr < kTile ? lr : kTile;
-        lo = row_lo - r.key0;
+        if constexpr (kSeg) lo = row_lo - r.key0;
       } else if (r.key0 + kTile > a.P) {
         lim = (int32_t)(a.P - r.key0);
       }
@@ -545,10 +549,16 @@ cudaError_t ls_launch_bwd_dq(const LsAttnArgs& a, const LsSched& sc, const LsBwd
     if (!ls_make_tmap_bf16(&tm.kp, a.k_pool, 2, dims, strides, box)) return cudaErrorInvalidValue;
     if (!ls_make_tmap_bf16(&tm.vp, a.v_pool, 2, dims, strides, box)) return cudaErrorInvalidValue;
   }
-  cudaError_t e =
-      cudaFuncSetAttribute(bwd_dq_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  const bool seg = sc.seg.n > 1, tb = sc.tb_major != 0;
+  const void* fn = seg ? (tb ? (const void*)bwd_dq_tc_kernel<true, true>
+                             : (const void*)bwd_dq_tc_kernel<true, false>)
+                       : (tb ? (const void*)bwd_dq_tc_kernel<false, true>
+                             : (const void*)bwd_dq_tc_kernel<false, false>);
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
-  bwd_dq_tc_kernel<<<sc.ctas, kThreads, kSmemBytes, st>>>(tm, a, sc, b);
+  void* args[] = {(void*)&tm, (void*)&a, (void*)&sc, (void*)&b};
+  e = cudaLaunchKernel(fn, dim3(sc.ctas), dim3(kThreads), args, kSmemBytes, st);
+  if (e != cudaSuccess) return e;
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   ls_note_launch();

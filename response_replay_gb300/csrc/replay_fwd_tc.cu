@@ -75,15 +75,17 @@ struct TmapSet {
   CUtensorMap q, kp, vp, kr, vr;
 };
 
-template <int kMode>
-using FwdCursor = TileCursor<kUnitRows, kTile, kMode>;
+template <int kMode, bool kTb>
+using FwdCursor = TileCursor<kUnitRows, kTile, kMode, kTb>;
 
 __device__ __forceinline__ uint32_t bar_addr(uint32_t base, int i) { return base + kOffBar + 8 * i; }
 
 // kMode (the unit layouts of ls_tiles.cuh): 0 one response; 1 several responses of
 // equal length, units per member (4-D Q and response maps); 2 several responses packed
-// into shared tiles (Q as one token sequence, 4-D response maps, rows masked by member).
-template <int kMode>
+// into shared tiles (Q as one token sequence, 4-D response maps, rows masked by member);
+// 3 one response cut into segments (ragged members back to back, rows masked by segment).
+// kTb: units numbered token block major (short prompts; ls_tiles.cuh unit_coords).
+template <int kMode, bool kTb>
 __global__ void __launch_bounds__(kThreads, 1)
 replay_fwd_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a,
                      const __grid_constant__ LsSched sc, const LsFwdOut out) {
@@ -152,7 +154,7 @@ replay_fwd_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a,
       tma_prefetch_desc(&tm.vp);
       tma_prefetch_desc(&tm.kr);
       tma_prefetch_desc(&tm.vr);
-      FwdCursor<kMode> cur(sc, blockIdx.x, a.R, a.g, a.pack, a.tiles, a.upm, a.rt);
+      FwdCursor<kMode, kTb> cur(sc, blockIdx.x, a.R, a.g, a.pack, a.tiles, a.upm, a.rt);
       TileRec r;
       uint32_t ring = 0, units = 0, aux = 0;
       const int32_t ps = 1 << a.ps_log2;
@@ -197,7 +199,7 @@ replay_fwd_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a,
             if constexpr (kMode == 2)
               packed_resp_tile<kTile>(r.key0, r.t0 / a.R, a.R, &rmem, &key);
             for (int hf = 0; hf < 2; ++hf)
-              if constexpr (kMode != 0)
+              if constexpr (kMode == 1 || kMode == 2)
                 tma_load_4d(dst + hf * kHalfBytes, map, hf * 64, r.kvh, key, rmem, fb);
               else
                 tma_load_3d(dst + hf * kHalfBytes, map, hf * 64, r.kvh, key, fb);
@@ -272,7 +274,7 @@ replay_fwd_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a,
                     (accumulate || kk > 0) ? 1u : 0u);
         }
       };
-      FwdCursor<kMode> cursor(sc, blockIdx.x, a.R, a.g, a.pack, a.tiles, a.upm, a.rt);
+      FwdCursor<kMode, kTb> cursor(sc, blockIdx.x, a.R, a.g, a.pack, a.tiles, a.upm, a.rt);
       TileRec cur, nxt;
       uint32_t ring = 0, units = 0, kc = 0;
       bool ok = cursor.next(&cur);
@@ -355,7 +357,7 @@ replay_fwd_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a,
     const int32_t tpt = kTile / a.pack;
     const int32_t tok_off = t * tpt + row / a.pack, head_off = row % a.pack;
     const bool row_used = row < a.pack * tpt;
-    FwdCursor<kMode> cursor(sc, blockIdx.x, a.R, a.g, a.pack, a.tiles, a.upm, a.rt);
+    FwdCursor<kMode, kTb> cursor(sc, blockIdx.x, a.R, a.g, a.pack, a.tiles, a.upm, a.rt);
     TileRec r;
     uint32_t kc = 0, oc = 0;
     float m = -INFINITY, l = 0.f, lcomp = 0.f;
@@ -395,7 +397,7 @@ replay_fwd_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a,
         const int32_t lr = (tq + 1 < a.R ? tq + 1 : a.R) - key0;
         lim = lr < kTile ? lr : kTile;
         if (kMode == 2 && rmem != km) lim = 0;      // another member's keys
-        if (kMode == 0 && sc.seg.n > 1) {           // keys of earlier segments (ragged
+        if constexpr (kMode == 3) {                 // keys of earlier segments (ragged
           int32_t s0, s1;                           // members: response tiles only)
           ls_seg_bounds(sc.seg, vt, &s0, &s1);
           lo = s0 - key0;
@@ -617,8 +619,8 @@ cudaError_t ls_launch_replay_fwd(const LsAttnArgs& a, const LsSched& sc, const L
   // rows past a member's R read as zeros, not as the next member's rows.
   const uint32_t box_q[4] = {64, 1, kTile, 1};
   const uint64_t M = (uint64_t)a.members;
-  const int mode = a.members <= 1 ? 0 : (a.rt > a.R ? 2 : 1);
-  const int rank = mode == 0 ? 3 : 4;
+  const int mode = a.members <= 1 ? (sc.seg.n > 1 ? 3 : 0) : (a.rt > a.R ? 2 : 1);
+  const int rank = (mode == 0 || mode == 3) ? 3 : 4;
   {
     // Q boxes: 128 tokens of one head, or floor(128 / pack) tokens x pack heads; in
     // kMode 2 the members' tokens are one sequence of rt tokens
@@ -644,17 +646,21 @@ cudaError_t ls_launch_replay_fwd(const LsAttnArgs& a, const LsSched& sc, const L
     if (!ls_make_tmap_bf16(&tm.kp, a.k_pool, 2, dims, strides, box)) return cudaErrorInvalidValue;
     if (!ls_make_tmap_bf16(&tm.vp, a.v_pool, 2, dims, strides, box)) return cudaErrorInvalidValue;
   }
-  const void* fn = mode == 0 ? (const void*)replay_fwd_tc_kernel<0>
-                  : mode == 1 ? (const void*)replay_fwd_tc_kernel<1>
-                              : (const void*)replay_fwd_tc_kernel<2>;
+  // token-block-major instances for the one-response layouts (the only ones whose
+  // schedule can ask for it: members' launches take long responses or packed tokens)
+  const bool tb = sc.tb_major != 0 && (mode == 0 || mode == 3);
+  const void* fn = mode == 0 ? (tb ? (const void*)replay_fwd_tc_kernel<0, true>
+                                   : (const void*)replay_fwd_tc_kernel<0, false>)
+                  : mode == 1 ? (const void*)replay_fwd_tc_kernel<1, false>
+                  : mode == 2 ? (const void*)replay_fwd_tc_kernel<2, false>
+                  : (tb ? (const void*)replay_fwd_tc_kernel<3, true>
+                        : (const void*)replay_fwd_tc_kernel<3, false>);
+  if ((mode == 1 || mode == 2) && sc.tb_major) return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
-  if (mode == 0)
-    replay_fwd_tc_kernel<0><<<sc.ctas, kThreads, kSmemBytes, st>>>(tm, a, sc, out);
-  else if (mode == 1)
-    replay_fwd_tc_kernel<1><<<sc.ctas, kThreads, kSmemBytes, st>>>(tm, a, sc, out);
-  else
-    replay_fwd_tc_kernel<2><<<sc.ctas, kThreads, kSmemBytes, st>>>(tm, a, sc, out);
+  void* args[] = {(void*)&tm, (void*)&a, (void*)&sc, (void*)&out};
+  e = cudaLaunchKernel(fn, dim3(sc.ctas), dim3(kThreads), args, kSmemBytes, st);
+  if (e != cudaSuccess) return e;
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   ls_note_launch();

@@ -96,8 +96,9 @@ static int check(int U, int nt, int sp, int C) {
 
 // Packed members: `members` responses of R tokens numbered back to back (RT tokens), a
 // tile holding 128 / pack tokens of one KV head, `tiles` tiles per unit.
-static int check_packed(int R, int members, int pack, int hkv, int nt, int sp, int C,
-                        int tb_major) {
+template <bool kTb>
+static int check_packed(int R, int members, int pack, int hkv, int nt, int sp, int C) {
+  const int tb_major = kTb ? 1 : 0;
   constexpr int kTile = 128, kUnitRows = 256;
   const int RT = R * members, tpt = kTile / pack;
   const int tiles = RT <= tpt ? 1 : 2, tpu = tiles * tpt;
@@ -109,8 +110,8 @@ static int check_packed(int R, int members, int pack, int hkv, int nt, int sp, i
   auto t0_of = [&](int u) { return (tb_major ? u / hkv : u % nTB) * tpu; };
   std::map<int, std::multiset<std::pair<int, int>>> got;  // unit -> (member, first key)
   for (int c = 0; c < s.ctas; ++c) {
-    TileCursor<kUnitRows, kTile, 2> cur(s, c, R, pack, pack, tiles, INT32_MAX, RT);
-    TileCursor<kUnitRows, kTile, 2> flags(s, c, R, pack, pack, tiles, INT32_MAX, RT);
+    TileCursor<kUnitRows, kTile, 2, kTb> cur(s, c, R, pack, pack, tiles, INT32_MAX, RT);
+    TileCursor<kUnitRows, kTile, 2, kTb> flags(s, c, R, pack, pack, tiles, INT32_MAX, RT);
     TileRec r;
     bool f0, l0;
     int n = 0, nf = 0;
@@ -285,10 +286,9 @@ int main() {
         for (int hkv : {1, 4})
           for (int C : {1, 7, 152})
             for (int nt : {0, 7}) {
-              for (int tbm = 0; tbm < 2; ++tbm) {
-                pbad += check_packed(R, members, pack, hkv, nt, 3, C, tbm);
-                ++pn;
-              }
+              pbad += check_packed<false>(R, members, pack, hkv, nt, 3, C);
+              pbad += check_packed<true>(R, members, pack, hkv, nt, 3, C);
+              pn += 2;
             }
   bad += pbad;
   std::printf("%d/%d packed-member walks ok\n", pn - pbad, pn);
