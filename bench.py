@@ -292,13 +292,56 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         if m is not None:
             m.append(ev())
 
+    # --batched: each cycle's members replay in one ragged forward and one ragged backward
+    # launch (their tokens back to back) and one loss call over the cycle's members
+    if args.batched:
+        cyc = {}
+        for c in range(C):
+            bs = [branches[c, i] for i in range(G)]
+            cyc[c] = tuple(torch.cat([getattr(b, f) for b in bs]).contiguous()
+                           for f in ("q", "k", "v", "d_o"))
+        Tc = max(o_[-1] for o_ in offs)
+        o_c = torch.empty((Tc, w.hq, D), dtype=torch.bfloat16, device=dev)
+        lse_c = torch.empty((Tc, w.hq), dtype=torch.float32, device=dev)
+        dq_c = torch.zeros((Tc, w.hq, D), dtype=torch.float32, device=dev)
+        dk_c = torch.zeros((Tc, w.hkv, D), dtype=torch.float32, device=dev)
+        dv_c = torch.zeros((Tc, w.hkv, D), dtype=torch.float32, device=dev)
+        dlog_c = torch.empty((Tc, w.vocab), dtype=gins[0].logits.dtype, device=dev)
+
+    def cycle(c, m=None):
+        """Cycle c's members in one ragged launch per pass (see --batched)."""
+        T = offs[c][-1]
+        lens = group_lens[c][:G]
+        q, kr, vr, d_o = cyc[c]
+        gin = gins[c]
+        first = c == 0
+        api.replay_fwd_ragged(cache, q, kr, vr, lens, scale, w.num_splits, o=o_c[:T],
+                              lse=lse_c[:T], stream=stream)
+        if m is not None:
+            m.append(ev())
+        api.grpo_loss_fwd_bwd(gin.logits, gin.targets, logp_olds[c], gin.rewards, gin.resp_lens,
+                              0, G, 0.2, loss=loss, accumulate=not first, dlogits=dlog_c[:T],
+                              logp_out=lp_out[:T], stats=stats, stream=stream)
+        if m is not None:
+            m.append(ev())
+        api.replay_bwd_ragged(cache, q, kr, vr, o_c[:T], lse_c[:T], d_o, lens, scale,
+                              w.num_splits, dq=dq_c[:T], dk=dk_c[:T], dv=dv_c[:T],
+                              accumulate=not first, stream=stream)
+        if m is not None:
+            m.append(ev())
+
+    groups = list(range(C)) if args.batched else replays
+
     def step(marks=None):
         m = [ev()] if marks is not None else None
         cache.capture(pr.k, pr.v, 0, stream)
         if m is not None:
             m.append(ev())
-        for c, i in replays:
-            member(c, i, m)
+        for gr in groups:
+            if args.batched:
+                cycle(gr, m)
+            else:
+                member(*gr, m)
         return m
 
     # kernel launches of one step, as counted by the library itself
@@ -326,13 +369,13 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         torch.cuda.synchronize()
     total_ms = max_over_ranks(t0.elapsed_time(t1), world, dev)
     assert B.ls_last_device_error(0) == B.LS_OK
-    assert torch.isfinite(loss).all() and torch.isfinite(dq).all()
+    assert torch.isfinite(loss).all() and torch.isfinite(dq_c if args.batched else dq).all()
 
     cap_ms = fwd_ms = grpo_ms = bwd_ms = 0.0
     n_rep = len(replays)
     for m in marks_all:
         cap_ms += m[0].elapsed_time(m[1])
-        for r in range(n_rep):
+        for r in range(len(groups)):
             a = 1 + 3 * r
             fwd_ms += m[a].elapsed_time(m[a + 1])
             grpo_ms += m[a + 1].elapsed_time(m[a + 2])
@@ -378,7 +421,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         e2e = {"value": None, "unit": "TFLOP/s", "skipped": "multi-cycle workload: its "
                f"{C} cycles' logits alone are {sum(g_.logits.numel() for g_ in gins) * 2 / 1e9:.0f} "
                "GB of pinned host memory per input set"}
-    if not args.no_e2e and C == 1:
+    if not args.no_e2e and C == 1 and not args.batched:
         gin, logp_old, off = gins[0], logp_olds[0], offs[0]
         branch_list = [branches[0, i] for i in range(G)]
         host = {}
@@ -572,8 +615,10 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     if C == 1 and rl[0] == rl[-1]:
         replay_desc = f"G={G} serial replays R={rl[0]}"
     else:
-        replay_desc = (f"one capture, {C} cycles x G={G} serial replays ({n_rep}), ragged R in "
-                       f"[{rl[0]}, {rl[-1]}] (mean {sum(rl) / len(rl):.0f})")
+        how = ("each cycle's members in one ragged forward, one loss and one ragged backward "
+               "call" if args.batched else "serial replays")
+        replay_desc = (f"one capture, {C} cycles x G={G} ({n_rep} replays), {how}, ragged R "
+                       f"in [{rl[0]}, {rl[-1]}] (mean {sum(rl) / len(rl):.0f})")
     out = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
@@ -931,6 +976,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--members", type=int, default=None, help="replay fewer members (debug)")
+    ap.add_argument("--batched", action="store_true",
+                    help="replay each cycle's members in one ragged launch per pass")
     ap.add_argument("--workload", default=WORKLOAD,
                     help="p2m (default, the metric's configuration); smaller ones for profiling")
     ap.add_argument("--no-e2e", action="store_true")
