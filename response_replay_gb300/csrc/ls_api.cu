@@ -136,7 +136,7 @@ FwdGeom fwd_geom(int R, int members, int Hq, int Hkv) {
     f.rt = members * R;
     f.tiles = f.rt <= tpt ? 1 : 2;
     const int tpu = f.tiles * tpt;
-    f.units = (int)((int64_t)Hkv * ((f.rt + tpu - 1) / tpu));
+    f.units = (int)((int64_t)(Hq / f.pack) * ((f.rt + tpu - 1) / tpu));
     f.upm = INT32_MAX;
   } else {
     f.rt = R;

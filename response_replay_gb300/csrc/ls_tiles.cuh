@@ -1,8 +1,9 @@
 // ls_tiles.cuh -- the sequence of KV tiles one persistent CTA processes, derived from
 // the work walk of ls_sched.h.  A unit is UnitRows query rows that share a KV head:
-// with pack = 1, UnitRows consecutive response tokens of one query head; with pack = g
-// (grouped-query packing, for short responses), the rows of consecutive tokens for all
-// g query heads of one KV head, a tile holding floor(Tile / g) whole tokens.  Its items
+// with pack = 1, UnitRows consecutive response tokens of one query head; with pack > 1
+// (grouped-query packing, for short responses; pack divides g), the rows of consecutive
+// tokens for a group of pack query heads of one KV head, a tile holding floor(Tile /
+// pack) whole tokens.  Unit groups are numbered grp = h / pack.  Its items
 // are the prompt splits (tile ranges of Tile keys) followed by the response's own keys
 // (tiles 0 .. ceil(last token of the unit / Tile)).
 //
@@ -113,8 +114,8 @@ struct TileCursor {
         grp = ul / nTB;
         t0 = (ul - grp * nTB) * tok_per_unit;
       }
-      kvh = pack == 1 ? grp / g : grp;
-      h = pack == 1 ? grp : grp * g;
+      h = grp * pack;                  // first query head of the unit's group
+      kvh = h / g;
       resp = (s == walk.sc->nsplit);
       if (resp) {
         t = 0;

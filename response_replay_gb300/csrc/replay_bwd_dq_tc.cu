@@ -492,9 +492,9 @@ __global__ void __launch_bounds__(kD) bwd_dq_tc_combine(const LsAttnArgs a, cons
   const int tok_per_unit = kTile / a.pack;
   const int nTB = (a.R + tok_per_unit - 1) / tok_per_unit;
   int grp, tb;
-  unit_coords(u, a.pack == 1 ? a.hq : a.hkv, nTB, sc.tb_major != 0, &grp, &tb);
+  unit_coords(u, a.hq / a.pack, nTB, sc.tb_major != 0, &grp, &tb);
   const int t0 = tb * tok_per_unit;
-  const int h0 = a.pack == 1 ? grp : grp * a.g;
+  const int h0 = grp * a.pack;
   const int col = threadIdx.x;
   for (int r = blockIdx.y * kCombineRows; r < (blockIdx.y + 1) * kCombineRows; ++r) {
     if (r >= a.pack * tok_per_unit) continue;
@@ -509,16 +509,33 @@ __global__ void __launch_bounds__(kD) bwd_dq_tc_combine(const LsAttnArgs a, cons
 }  // namespace
 
 int ls_bwd_unit_rows() { return kUnitRows; }
-// Responses shorter than a unit: pack the g query heads of a KV head into its rows.
+// Responses shorter than a unit: a tile holds `pack` query heads of one KV head (pack
+// dividing g) for floor(128 / pack) tokens; the pack with the fewest tiles, ties to the
+// larger pack except that one head per tile wins any tie.
+namespace {
+int64_t bwd_tiles_for(int R, int hq, int pack) {
+  const int tpt = kTile / pack;
+  return (int64_t)(hq / pack) * ((R + tpt - 1) / tpt);
+}
+}  // namespace
 int ls_bwd_pack(int R, int hq, int hkv) {
   const int g = hq / hkv;
-  return (g > 1 && g <= 64 && R < kUnitRows) ? g : 1;
+  int best = 1;
+  int64_t bt = INT64_MAX;
+  for (int p = g < 64 ? g : 64; p >= 2; --p) {
+    if (g % p) continue;
+    const int64_t t = bwd_tiles_for(R, hq, p);
+    if (t < bt) {
+      best = p;
+      bt = t;
+    }
+  }
+  return bwd_tiles_for(R, hq, 1) <= bt ? 1 : best;
 }
 int ls_bwd_units(int R, int hq, int hkv) {
   const int pack = ls_bwd_pack(R, hq, hkv);
-  if (pack == 1) return ls_num_units(R, hq, hkv, kUnitRows);
   const int tok_per_unit = kTile / pack;
-  return hkv * ((R + tok_per_unit - 1) / tok_per_unit);
+  return (hq / pack) * ((R + tok_per_unit - 1) / tok_per_unit);
 }
 int ls_bwd_tile() { return kTile; }
 int ls_bwd_ctas_per_sm() { return 1; }

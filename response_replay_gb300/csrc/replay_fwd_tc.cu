@@ -557,9 +557,9 @@ __global__ void __launch_bounds__(kD) replay_fwd_tc_combine(const LsAttnArgs a, 
   const int m = u / a.upm, ul = u - m * a.upm;  // member, unit within the member
   const int nTB = (a.rt + tok_per_unit - 1) / tok_per_unit;
   int grp, tb;
-  unit_coords(ul, a.pack == 1 ? a.hq : a.hkv, nTB, sc.tb_major != 0, &grp, &tb);
+  unit_coords(ul, a.hq / a.pack, nTB, sc.tb_major != 0, &grp, &tb);
   const int t0 = tb * tok_per_unit;
-  const int h0 = a.pack == 1 ? grp : grp * a.g;
+  const int h0 = grp * a.pack;
   const int col = threadIdx.x;
   for (int r = blockIdx.y * kCombineRows; r < (blockIdx.y + 1) * kCombineRows; ++r) {
     const int l = r % kTile;  // row within its tile
@@ -591,24 +591,42 @@ int ls_num_units(int R, int hq, int hkv, int unit_rows) {
   (void)hkv;
   return hq * ((R + unit_rows - 1) / unit_rows);
 }
-// Responses shorter than a unit would leave most of a one-head unit empty: pack the g
-// query heads of a KV head into the unit's rows instead (each K/V tile then serves g
-// heads at once, and short replays stream the prompt once per KV head).
+// Grouped-query packing.  A one-head unit of 256 tokens leaves most of its rows empty
+// for short responses, so a tile may instead hold `pack` query heads of one KV head
+// (pack dividing g) for floor(128 / pack) tokens: each K/V tile then serves pack heads
+// at once.  Units then cover (KV head, group of pack heads, token block); a packed unit
+// whose tokens all fit one tile runs as a one-tile unit (tile B would be padding).
+// The pack is the one with the fewest tiles to compute; on a tie the larger pack (fewer
+// units streaming the prompt), except that one head per tile wins any tie.
+namespace {
+int64_t fwd_tiles_for(int R, int hq, int pack) {
+  const int tpt = kTile / pack;
+  const int tiles = (pack > 1 && R <= tpt) ? 1 : 2;
+  return (int64_t)(hq / pack) * tiles * ((R + tiles * tpt - 1) / (tiles * tpt));
+}
+}  // namespace
 int ls_fwd_pack(int R, int hq, int hkv) {
   const int g = hq / hkv;
-  return (g > 1 && g <= 64 && R < kUnitRows) ? g : 1;
+  int best = 1;
+  int64_t bt = INT64_MAX;
+  for (int p = g < 64 ? g : 64; p >= 2; --p) {
+    if (g % p) continue;
+    const int64_t t = fwd_tiles_for(R, hq, p);
+    if (t < bt) {
+      best = p;
+      bt = t;
+    }
+  }
+  return fwd_tiles_for(R, hq, 1) <= bt ? 1 : best;
 }
-// A packed unit whose tokens all fit one tile runs as a one-tile unit: tile B would be
-// padding, and its S -> softmax -> P V chain would only lengthen each KV step.
 int ls_fwd_tiles(int R, int hq, int hkv) {
   const int pack = ls_fwd_pack(R, hq, hkv);
   return (pack > 1 && R <= kTile / pack) ? 1 : 2;
 }
 int ls_fwd_units(int R, int hq, int hkv) {
   const int pack = ls_fwd_pack(R, hq, hkv);
-  if (pack == 1) return ls_num_units(R, hq, hkv, kUnitRows);
   const int tok_per_unit = ls_fwd_tiles(R, hq, hkv) * (kTile / pack);
-  return hkv * ((R + tok_per_unit - 1) / tok_per_unit);
+  return (hq / pack) * ((R + tok_per_unit - 1) / tok_per_unit);
 }
 
 cudaError_t ls_launch_replay_fwd(const LsAttnArgs& a, const LsSched& sc, const LsFwdOut& out,

@@ -78,6 +78,13 @@ def test_ragged_fwd_bwd(cuda, P, R, hq, hkv, ps, splits):
     (0, 50, 4, 1, 64, 2),
     (2048, 10, 3, 1, 16, 1000),
     (4096, 130, 5, 5, 64, 4),
+    # a tile holds a divisor of g heads: g = 6 packs 2 heads x 64 tokens at R = 48 / 64
+    # (forward) and 64 / 128 (both passes); 127 tokens take one head per tile backward
+    (3000, 64, 12, 2, 64, 5),
+    (2000, 48, 24, 4, 128, 3),
+    (1500, 128, 6, 1, 64, 4),
+    (1000, 127, 12, 2, 32, 7),
+    (2500, 96, 8, 2, 64, 3),
 ])
 def test_short_response_packed_fwd_bwd(cuda, P, R, hq, hkv, ps, splits):
     case = Case(P, R, hq, hkv, ps, splits, seed=P * 5 + R + hq, device=cuda, sharp=True)
