@@ -131,6 +131,9 @@ FwdGeom fwd_geom(int R, int members, int Hq, int Hkv) {
   f.pack = ls_fwd_pack(R, Hq, Hkv);
   f.ok = (int64_t)members * R <= (1 << 30);
   if (!f.ok) return f;
+  // the packed-members walk holds at most two key tiles per member (short responses);
+  // longer members take per-member units of one head
+  if (members > 1 && R >= 2 * ls_fwd_tile()) f.pack = 1;
   if (members > 1 && f.pack > 1) {
     const int tpt = ls_fwd_tile() / f.pack;
     f.rt = members * R;
@@ -140,8 +143,9 @@ FwdGeom fwd_geom(int R, int members, int Hq, int Hkv) {
     f.upm = INT32_MAX;
   } else {
     f.rt = R;
-    f.tiles = ls_fwd_tiles(R, Hq, Hkv);
-    const int upm = ls_fwd_units(R, Hq, Hkv);
+    f.tiles = f.pack == 1 ? 2 : ls_fwd_tiles(R, Hq, Hkv);
+    const int upm = f.pack == 1 ? ls_num_units(R, Hq, Hkv, ls_fwd_unit_rows())
+                                : ls_fwd_units(R, Hq, Hkv);
     f.ok = (int64_t)members * upm <= (1 << 30);
     f.units = members * upm;
     f.upm = members > 1 ? upm : INT32_MAX;
