@@ -114,8 +114,10 @@ struct TileCursor {
         grp = ul / nTB;
         t0 = (ul - grp * nTB) * tok_per_unit;
       }
-      h = grp * pack;                  // first query head of the unit's group
-      kvh = h / g;
+      // first query head of the unit's group, and its KV head (the one-head and all-g
+      // cases written as before: the decode sits in every role's inner loop)
+      h = pack == 1 ? grp : grp * pack;
+      kvh = pack == 1 ? grp / g : (pack == g ? grp : h / g);
       resp = (s == walk.sc->nsplit);
       if (resp) {
         t = 0;

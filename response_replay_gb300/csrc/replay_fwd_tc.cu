@@ -596,13 +596,17 @@ int ls_num_units(int R, int hq, int hkv, int unit_rows) {
 // (pack dividing g) for floor(128 / pack) tokens: each K/V tile then serves pack heads
 // at once.  Units then cover (KV head, group of pack heads, token block); a packed unit
 // whose tokens all fit one tile runs as a one-tile unit (tile B would be padding).
-// The pack is the one with the fewest tiles to compute; on a tie the larger pack (fewer
-// units streaming the prompt), except that one head per tile wins any tie.
+// The pack is the one with the least work, counted in tiles with a one-tile unit
+// costing 1.6 tiles (measured at P = 2,097,152, g = 6: a one-tile unit has no second tile
+// to run while its softmax works, 0.17 ms against 0.11 ms per tile of two-tile units);
+// on a tie the larger pack (fewer units streaming the prompt), except that one head per
+// tile wins any tie.
 namespace {
-int64_t fwd_tiles_for(int R, int hq, int pack) {
+int64_t fwd_tiles_for(int R, int hq, int pack) {  // in tenths of a two-tile unit's tile
   const int tpt = kTile / pack;
   const int tiles = (pack > 1 && R <= tpt) ? 1 : 2;
-  return (int64_t)(hq / pack) * tiles * ((R + tiles * tpt - 1) / (tiles * tpt));
+  const int64_t units = (int64_t)(hq / pack) * ((R + tiles * tpt - 1) / (tiles * tpt));
+  return units * (tiles == 1 ? 16 : 20);
 }
 }  // namespace
 int ls_fwd_pack(int R, int hq, int hkv) {
