@@ -73,9 +73,11 @@ LS_HD void packed_resp_tile(int32_t key0, int32_t rm, int32_t R, int32_t* m,
   *key = (t - dm * rnt) * Tile;
 }
 
-// kTbMajor: units numbered token block major (unit_coords); a template parameter so the
-// group-major walk of long prompts compiles to the plain decode.
-template <int UnitRows, int Tile, int kMode = 0, bool kTbMajor = false>
+// kTbMajor: units numbered token block major (unit_coords); kPacked: tiles hold pack > 1
+// heads (grouped-query packing).  Template parameters, so that the one-head, group-major
+// walk of long responses compiles to the plainest decode (it sits in every role's inner
+// loop, and measured slower by 1% with the general forms compiled in).
+template <int UnitRows, int Tile, int kMode = 0, bool kTbMajor = false, bool kPacked = true>
 struct TileCursor {
   LsWalk walk;
   int32_t u, s, t, t_end, slot;
@@ -114,10 +116,13 @@ struct TileCursor {
         grp = ul / nTB;
         t0 = (ul - grp * nTB) * tok_per_unit;
       }
-      // first query head of the unit's group, and its KV head (the one-head and all-g
-      // cases written as before: the decode sits in every role's inner loop)
-      h = pack == 1 ? grp : grp * pack;
-      kvh = pack == 1 ? grp / g : (pack == g ? grp : h / g);
+      if constexpr (kPacked) {         // first query head of the unit's group, KV head
+        h = grp * pack;
+        kvh = h / g;
+      } else {
+        h = grp;
+        kvh = grp / g;
+      }
       resp = (s == walk.sc->nsplit);
       if (resp) {
         t = 0;

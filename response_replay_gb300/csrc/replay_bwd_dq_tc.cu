@@ -83,12 +83,12 @@ struct TmapSet {
 
 // kSeg: one response cut into segments (ragged members back to back); kTb: units
 // numbered token block major (short prompts)
-template <bool kSeg, bool kTb>
-using DqCursor = TileCursor<kUnitRows, kTile, kSeg ? 3 : 0, kTb>;
+template <bool kSeg, bool kTb, bool kPk>
+using DqCursor = TileCursor<kUnitRows, kTile, kSeg ? 3 : 0, kTb, kPk>;
 
 __device__ __forceinline__ uint32_t bar_addr(uint32_t base, int i) { return base + kOffBar + 8 * i; }
 
-template <bool kSeg, bool kTb>
+template <bool kSeg, bool kTb, bool kPk>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_dq_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a,
                  const __grid_constant__ LsSched sc, const LsBwdIn b) {
@@ -161,7 +161,7 @@ bwd_dq_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a,
       tma_prefetch_desc(&tm.vp);
       tma_prefetch_desc(&tm.kr);
       tma_prefetch_desc(&tm.vr);
-      DqCursor<kSeg, kTb> cur(sc, blockIdx.x, a.R, a.g, a.pack);
+      DqCursor<kSeg, kTb, kPk> cur(sc, blockIdx.x, a.R, a.g, a.pack);
       TileRec r;
       uint32_t kc = 0, vc = 0, units = 0, aux = 0;
       const int32_t ps = 1 << a.ps_log2;
@@ -250,7 +250,7 @@ bwd_dq_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a,
       const uint32_t dk_base = sdesc_lo(sbase + kOffK, 16);
       const uint32_t dv_base = sdesc_lo(sbase + kOffV, 16);
       const uint32_t dkm_base = sdesc_lo(sbase + kOffK, kHalfBytes);
-      DqCursor<kSeg, kTb> cursor(sc, blockIdx.x, a.R, a.g, a.pack);
+      DqCursor<kSeg, kTb, kPk> cursor(sc, blockIdx.x, a.R, a.g, a.pack);
       // first / last of unit of tiles j (f0, l0) and j+1 (f1, l1)
       bool f0 = false, l0 = false, f1 = false, l1 = false;
       bool have0 = cursor.next_flags(&f0, &l0);
@@ -358,7 +358,7 @@ bwd_dq_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a,
     // this thread's row: token row / pack of the unit, head row % pack
     const int32_t tok_off = row / a.pack, head_off = row % a.pack;
     const bool row_used = row < a.pack * (kTile / a.pack);
-    DqCursor<kSeg, kTb> cursor(sc, blockIdx.x, a.R, a.g, a.pack);
+    DqCursor<kSeg, kTb, kPk> cursor(sc, blockIdx.x, a.R, a.g, a.pack);
     TileRec r;
     uint32_t j = 0, uc = 0;
     float lse2 = 0.f, dd = 0.f;
@@ -566,11 +566,17 @@ cudaError_t ls_launch_bwd_dq(const LsAttnArgs& a, const LsSched& sc, const LsBwd
     if (!ls_make_tmap_bf16(&tm.kp, a.k_pool, 2, dims, strides, box)) return cudaErrorInvalidValue;
     if (!ls_make_tmap_bf16(&tm.vp, a.v_pool, 2, dims, strides, box)) return cudaErrorInvalidValue;
   }
-  const bool seg = sc.seg.n > 1, tb = sc.tb_major != 0;
-  const void* fn = seg ? (tb ? (const void*)bwd_dq_tc_kernel<true, true>
-                             : (const void*)bwd_dq_tc_kernel<true, false>)
-                       : (tb ? (const void*)bwd_dq_tc_kernel<false, true>
-                             : (const void*)bwd_dq_tc_kernel<false, false>);
+  const bool seg = sc.seg.n > 1, tb = sc.tb_major != 0, pk = a.pack > 1;
+  const void* const fns[8] = {
+      (const void*)bwd_dq_tc_kernel<false, false, false>,
+      (const void*)bwd_dq_tc_kernel<false, false, true>,
+      (const void*)bwd_dq_tc_kernel<false, true, false>,
+      (const void*)bwd_dq_tc_kernel<false, true, true>,
+      (const void*)bwd_dq_tc_kernel<true, false, false>,
+      (const void*)bwd_dq_tc_kernel<true, false, true>,
+      (const void*)bwd_dq_tc_kernel<true, true, false>,
+      (const void*)bwd_dq_tc_kernel<true, true, true>};
+  const void* fn = fns[(seg ? 4 : 0) + (tb ? 2 : 0) + (pk ? 1 : 0)];
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
   void* args[] = {(void*)&tm, (void*)&a, (void*)&sc, (void*)&b};

@@ -75,8 +75,8 @@ struct TmapSet {
   CUtensorMap q, kp, vp, kr, vr;
 };
 
-template <int kMode, bool kTb>
-using FwdCursor = TileCursor<kUnitRows, kTile, kMode, kTb>;
+template <int kMode, bool kTb, bool kPk>
+using FwdCursor = TileCursor<kUnitRows, kTile, kMode, kTb, kPk>;
 
 __device__ __forceinline__ uint32_t bar_addr(uint32_t base, int i) { return base + kOffBar + 8 * i; }
 
@@ -84,8 +84,9 @@ __device__ __forceinline__ uint32_t bar_addr(uint32_t base, int i) { return base
 // equal length, units per member (4-D Q and response maps); 2 several responses packed
 // into shared tiles (Q as one token sequence, 4-D response maps, rows masked by member);
 // 3 one response cut into segments (ragged members back to back, rows masked by segment).
-// kTb: units numbered token block major (short prompts; ls_tiles.cuh unit_coords).
-template <int kMode, bool kTb>
+// kTb: units numbered token block major (short prompts; ls_tiles.cuh unit_coords);
+// kPk: tiles hold a.pack > 1 heads (grouped-query packing).
+template <int kMode, bool kTb, bool kPk>
 __global__ void __launch_bounds__(kThreads, 1)
 replay_fwd_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a,
                      const __grid_constant__ LsSched sc, const LsFwdOut out) {
@@ -154,7 +155,7 @@ replay_fwd_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a,
       tma_prefetch_desc(&tm.vp);
       tma_prefetch_desc(&tm.kr);
       tma_prefetch_desc(&tm.vr);
-      FwdCursor<kMode, kTb> cur(sc, blockIdx.x, a.R, a.g, a.pack, a.tiles, a.upm, a.rt);
+      FwdCursor<kMode, kTb, kPk> cur(sc, blockIdx.x, a.R, a.g, a.pack, a.tiles, a.upm, a.rt);
       TileRec r;
       uint32_t ring = 0, units = 0, aux = 0;
       const int32_t ps = 1 << a.ps_log2;
@@ -274,7 +275,7 @@ replay_fwd_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a,
                     (accumulate || kk > 0) ? 1u : 0u);
         }
       };
-      FwdCursor<kMode, kTb> cursor(sc, blockIdx.x, a.R, a.g, a.pack, a.tiles, a.upm, a.rt);
+      FwdCursor<kMode, kTb, kPk> cursor(sc, blockIdx.x, a.R, a.g, a.pack, a.tiles, a.upm, a.rt);
       TileRec cur, nxt;
       uint32_t ring = 0, units = 0, kc = 0;
       bool ok = cursor.next(&cur);
@@ -357,7 +358,7 @@ replay_fwd_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a,
     const int32_t tpt = kTile / a.pack;
     const int32_t tok_off = t * tpt + row / a.pack, head_off = row % a.pack;
     const bool row_used = row < a.pack * tpt;
-    FwdCursor<kMode, kTb> cursor(sc, blockIdx.x, a.R, a.g, a.pack, a.tiles, a.upm, a.rt);
+    FwdCursor<kMode, kTb, kPk> cursor(sc, blockIdx.x, a.R, a.g, a.pack, a.tiles, a.upm, a.rt);
     TileRec r;
     uint32_t kc = 0, oc = 0;
     float m = -INFINITY, l = 0.f, lcomp = 0.f;
@@ -670,13 +671,24 @@ cudaError_t ls_launch_replay_fwd(const LsAttnArgs& a, const LsSched& sc, const L
   }
   // token-block-major instances for the one-response layouts (the only ones whose
   // schedule can ask for it: members' launches take long responses or packed tokens)
-  const bool tb = sc.tb_major != 0 && (mode == 0 || mode == 3);
-  const void* fn = mode == 0 ? (tb ? (const void*)replay_fwd_tc_kernel<0, true>
-                                   : (const void*)replay_fwd_tc_kernel<0, false>)
-                  : mode == 1 ? (const void*)replay_fwd_tc_kernel<1, false>
-                  : mode == 2 ? (const void*)replay_fwd_tc_kernel<2, false>
-                  : (tb ? (const void*)replay_fwd_tc_kernel<3, true>
-                        : (const void*)replay_fwd_tc_kernel<3, false>);
+  const bool tb = sc.tb_major != 0 && (mode == 0 || mode == 3), pk = a.pack > 1;
+  const void* fn;
+  if (mode == 1) {
+    fn = (const void*)replay_fwd_tc_kernel<1, false, false>;
+  } else if (mode == 2) {
+    fn = (const void*)replay_fwd_tc_kernel<2, false, true>;
+  } else if (mode == 0) {
+    fn = tb ? (pk ? (const void*)replay_fwd_tc_kernel<0, true, true>
+                  : (const void*)replay_fwd_tc_kernel<0, true, false>)
+            : (pk ? (const void*)replay_fwd_tc_kernel<0, false, true>
+                  : (const void*)replay_fwd_tc_kernel<0, false, false>);
+  } else {
+    fn = tb ? (pk ? (const void*)replay_fwd_tc_kernel<3, true, true>
+                  : (const void*)replay_fwd_tc_kernel<3, true, false>)
+            : (pk ? (const void*)replay_fwd_tc_kernel<3, false, true>
+                  : (const void*)replay_fwd_tc_kernel<3, false, false>);
+  }
+  if ((mode == 1 && pk) || (mode == 2 && !pk)) return cudaErrorInvalidValue;
   if ((mode == 1 || mode == 2) && sc.tb_major) return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;

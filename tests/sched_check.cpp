@@ -110,8 +110,8 @@ static int check_packed(int R, int members, int pack, int hkv, int nt, int sp, i
   auto t0_of = [&](int u) { return (tb_major ? u / hkv : u % nTB) * tpu; };
   std::map<int, std::multiset<std::pair<int, int>>> got;  // unit -> (member, first key)
   for (int c = 0; c < s.ctas; ++c) {
-    TileCursor<kUnitRows, kTile, 2, kTb> cur(s, c, R, pack, pack, tiles, INT32_MAX, RT);
-    TileCursor<kUnitRows, kTile, 2, kTb> flags(s, c, R, pack, pack, tiles, INT32_MAX, RT);
+    TileCursor<kUnitRows, kTile, 2, kTb, true> cur(s, c, R, pack, pack, tiles, INT32_MAX, RT);
+    TileCursor<kUnitRows, kTile, 2, kTb, true> flags(s, c, R, pack, pack, tiles, INT32_MAX, RT);
     TileRec r;
     bool f0, l0;
     int n = 0, nf = 0;
