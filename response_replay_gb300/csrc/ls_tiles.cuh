@@ -119,9 +119,9 @@ struct TileCursor {
       if constexpr (kPacked) {         // first query head of the unit's group, KV head
         h = grp * pack;
         kvh = h / g;
-      } else {
-        h = grp;
-        kvh = grp / g;
+      } else {                         // pack is 1 here; this form measured fastest
+        kvh = pack == 1 ? grp / g : grp;
+        h = pack == 1 ? grp : grp * g;
       }
       resp = (s == walk.sc->nsplit);
       if (resp) {
