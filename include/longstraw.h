@@ -169,7 +169,11 @@ ls_status ls_replay_attn_fwd_members(const ls_kv_cache* cache, const void* q, co
  * o, lse: the forward's outputs for the same inputs; d_o: bf16 [R][Hq][128].
  * dq: fp32 [R][Hq][128]; dk_resp, dv_resp: fp32 [R][num_kv_heads][128].
  * accumulate != 0 adds into dq/dk_resp/dv_resp instead of overwriting them (serial
- * replay accumulates gradients member by member: digest, Method step 3). */
+ * replay accumulates gradients member by member: digest, Method step 3).
+ * The environment variable LS_BWD_PAIR=1, read once per process, runs dQ on pairs of
+ * SMs (cluster CTA pairs); the default one-CTA kernel measured faster on every shape
+ * tried.  Both give the same results up to summation order; the workspace query and
+ * the call must see the same setting. */
 ls_status ls_replay_attn_bwd_workspace(const ls_kv_cache* cache, int R, int Hq,
                                        int num_splits, size_t* bytes);
 ls_status ls_replay_attn_bwd(const ls_kv_cache* cache, const void* q, const void* k_resp,

@@ -1,6 +1,7 @@
 // ls_api.cu -- the extern "C" entry points of include/longstraw.h: argument checks,
 // workspace layout, the per-device error word and the kernel launches.
 #include <math.h>
+#include <stdlib.h>
 #include <atomic>
 #include <mutex>
 
@@ -25,6 +26,7 @@ constexpr int kHeadDim = 128;
 
 struct DevInfo {
   int sms = 0;
+  int pairs = 0;  // CTA pairs resident at once for the pair dQ kernel (0: none)
   uint32_t* err = nullptr;
 };
 DevInfo g_dev[kMaxDevices];
@@ -44,6 +46,12 @@ ls_status dev_info(DevInfo* out) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_ls_device_error) != cudaSuccess) return LS_ERR_CUDA;
     d.err = static_cast<uint32_t*>(p);
+    int pairs = 0;
+    if (ls_bwd_pair_workers(&pairs) != cudaSuccess) {
+      pairs = 0;
+      (void)cudaGetLastError();  // not fatal: the one-CTA dQ kernel runs instead
+    }
+    d.pairs = pairs;
     d.sms = sms;
   }
   *out = d;
@@ -111,12 +119,31 @@ LsSched make_sched_units(const ls_kv_cache* c, int units, int num_splits, int ti
   return s;
 }
 
-LsSched make_sched(const ls_kv_cache* c, int R, int Hq, int num_splits, int unit_rows, int tile,
-                   int ctas, bool fwd) {
-  (void)unit_rows;
-  const int units = fwd ? ls_fwd_units(R, Hq, c->num_kv_heads)
-                        : ls_bwd_units(R, Hq, c->num_kv_heads);
-  return make_sched_units(c, units, num_splits, tile, ctas, R);
+// Backward dQ geometry: CTA pairs (two-tile units over pairs of SMs) when the device
+// fits them, else one CTA per unit of one tile.  LS_BWD_PAIR=0 / 1 in the environment
+// selects the one-CTA / pair kernel.
+struct BwdGeom {
+  int pair, pack, units, unit_rows, workers;
+};
+BwdGeom bwd_geom(int R, int Hq, int Hkv, const DevInfo& d) {
+  static const int env = [] {
+    const char* e = getenv("LS_BWD_PAIR");
+    return e ? atoi(e) : -1;
+  }();
+  BwdGeom g;
+  g.pair = (env == 1 && d.pairs > 0) ? 1 : 0;
+  if (g.pair) {
+    g.pack = ls_bwd_pair_pack(R, Hq, Hkv);
+    g.units = ls_bwd_pair_units(R, Hq, Hkv);
+    g.unit_rows = ls_bwd_pair_unit_rows();
+    g.workers = d.pairs;
+  } else {
+    g.pack = ls_bwd_pack(R, Hq, Hkv);
+    g.units = ls_bwd_units(R, Hq, Hkv);
+    g.unit_rows = ls_bwd_unit_rows();
+    g.workers = d.sms * ls_bwd_ctas_per_sm();
+  }
+  return g;
 }
 
 // Forward geometry of `members` responses of R tokens.  Short responses (grouped-query
@@ -353,9 +380,10 @@ ls_status bwd_workspace_impl(const ls_kv_cache* cache, int R, const LsSegs& seg,
   if (seg.n > 1 && (R + 127) / 128 > kLsMaxDkTiles) return LS_ERR_UNSUPPORTED;
   DevInfo d;
   if ((s = dev_info(&d)) != LS_OK) return s;
-  const LsSched sc = make_sched_units(cache, ls_bwd_units(R, Hq, cache->num_kv_heads), num_splits,
-                                      ls_bwd_tile(), d.sms * ls_bwd_ctas_per_sm(), resp_max, &seg);
-  *bytes = bwd_ws(sc, ls_bwd_unit_rows(), R, Hq, cache->num_kv_heads, d.sms, &seg).total;
+  const BwdGeom g = bwd_geom(R, Hq, cache->num_kv_heads, d);
+  const LsSched sc = make_sched_units(cache, g.units, num_splits, ls_bwd_tile(), g.workers,
+                                      resp_max, &seg);
+  *bytes = bwd_ws(sc, g.unit_rows, R, Hq, cache->num_kv_heads, d.sms, &seg).total;
   return LS_OK;
 }
 
@@ -374,12 +402,13 @@ ls_status bwd_impl(const ls_kv_cache* cache, const void* q, const void* k_resp, 
     if (!p || !aligned16(p)) return LS_ERR_INVALID_ARG;
   DevInfo d;
   if ((s = dev_info(&d)) != LS_OK) return s;
-  const LsSched sc = make_sched_units(cache, ls_bwd_units(R, Hq, cache->num_kv_heads), num_splits,
-                                      ls_bwd_tile(), d.sms * ls_bwd_ctas_per_sm(), resp_max, &seg);
-  const BwdWs w = bwd_ws(sc, ls_bwd_unit_rows(), R, Hq, cache->num_kv_heads, d.sms, &seg);
+  const BwdGeom g = bwd_geom(R, Hq, cache->num_kv_heads, d);
+  const LsSched sc = make_sched_units(cache, g.units, num_splits, ls_bwd_tile(), g.workers,
+                                      resp_max, &seg);
+  const BwdWs w = bwd_ws(sc, g.unit_rows, R, Hq, cache->num_kv_heads, d.sms, &seg);
   if (!workspace || workspace_bytes < w.total || !aligned16(workspace)) return LS_ERR_WORKSPACE;
   LsAttnArgs a = attn_args(cache, q, k_resp, v_resp, R, Hq, softmax_scale, d.err);
-  a.pack = ls_bwd_pack(R, Hq, cache->num_kv_heads);
+  a.pack = g.pack;
   LsBwdIn b;
   b.o = o;
   b.lse = lse;
@@ -393,6 +422,7 @@ ls_status bwd_impl(const ls_kv_cache* cache, const void* q, const void* k_resp, 
   b.dk = dk_resp;
   b.dv = dv_resp;
   b.accumulate = accumulate != 0;
+  b.pair = g.pair;
   return from_cuda(ls_launch_replay_bwd(a, sc, b, d.sms, (cudaStream_t)stream));
 }
 

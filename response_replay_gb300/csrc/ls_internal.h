@@ -56,9 +56,10 @@ struct LsBwdIn {
   float* dq;                 // [R][hq][128]
   float* dk;                 // [R][hkv][128]
   float* dv;
-  float* part_dq;            // workspace: [2*ctas][unit_rows][128]
+  float* part_dq;            // workspace: [pieces][unit_rows][128]
   float* part_dkdv;          // workspace: [2*ctas][2][128][128] (response-key kernel)
   int32_t accumulate;
+  int32_t pair;              // dQ on CTA pairs (replay_bwd_dq_pair.cu) instead of one CTA
 };
 
 // Geometry of the replay kernels (fixed at build time).
@@ -76,6 +77,12 @@ int ls_fwd_tiles(int R, int hq, int hkv);
 // Backward: the same packing for its one-tile units.
 int ls_bwd_pack(int R, int hq, int hkv);
 int ls_bwd_units(int R, int hq, int hkv);
+// Backward dQ on CTA pairs: units of two tiles (one per CTA), their packing, and the
+// number of pairs resident at once (the persistent grid).
+int ls_bwd_pair_unit_rows();
+int ls_bwd_pair_pack(int R, int hq, int hkv);
+int ls_bwd_pair_units(int R, int hq, int hkv);
+cudaError_t ls_bwd_pair_workers(int* pairs);
 
 cudaError_t ls_launch_capture(const void* k, const void* v, void* k_pool, void* v_pool,
                               const int32_t* page_table, int32_t num_pages, int32_t ps_log2,
@@ -96,6 +103,9 @@ cudaError_t ls_launch_replay_fwd(const LsAttnArgs& a, const LsSched& sc, const L
 
 cudaError_t ls_launch_bwd_dq(const LsAttnArgs& a, const LsSched& sc, const LsBwdIn& b,
                              cudaStream_t st);
+// sc.ctas counts pairs here.
+cudaError_t ls_launch_bwd_dq_pair(const LsAttnArgs& a, const LsSched& sc, const LsBwdIn& b,
+                                  cudaStream_t st);
 
 // Response-key dK / dV (tcgen05) and the bytes of its partial-sum workspace.
 size_t ls_dkdv_part_bytes(int R, int hq, int hkv, int num_sms, const LsSegs* segs);

@@ -12,8 +12,9 @@
 //   bwd_delta     D = rowsum(dO * O) per (t, h), one warp per row; also writes D and
 //                 lse log2(e) transposed ([head][token], padded to whole 128-token tiles
 //                 with 0 / +inf) for the response-key kernel.
-//   dQ            replay_bwd_dq_tc.cu: q-stationary tcgen05 kernel over prompt and
-//                 response keys, same schedule as the forward, plus its split combine.
+//   dQ            replay_bwd_dq_pair.cu (CTA pairs) or replay_bwd_dq_tc.cu (one CTA):
+//                 q-stationary tcgen05 kernel over prompt and response keys, the
+//                 forward's kind of schedule, plus its split combine.
 //   dK, dV        replay_bwd_dkdv_tc.cu: key-stationary tcgen05 kernel over the causal
 //                 R x R triangle of the response's own keys, plus its split combine.
 // Deterministic: no atomics.
@@ -78,7 +79,7 @@ cudaError_t ls_launch_replay_bwd(const LsAttnArgs& a, const LsSched& sc, const L
   ls_note_launch();
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  e = ls_launch_bwd_dq(a, sc, b, st);
+  e = b.pair ? ls_launch_bwd_dq_pair(a, sc, b, st) : ls_launch_bwd_dq(a, sc, b, st);
   if (e != cudaSuccess) return e;
   return ls_launch_bwd_dkdv(a, sc.seg, b, num_sms, st);
 }
