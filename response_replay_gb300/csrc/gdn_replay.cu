@@ -28,6 +28,7 @@
 
 #include "ls_device.cuh"
 #include "ls_internal.h"
+#include "ls_umma.cuh"
 
 namespace {
 
@@ -277,68 +278,162 @@ __device__ __forceinline__ void warp_reduce64(float* p, int lane) {
 }
 
 // ---------------------------------------------------------------- state hand-off
-// Forward: row i of the state, chunk by chunk (grid (H, 8), 16 warps, one row each):
-//   Sc[b][i][:] = S[i][:]   (state entering chunk c)
-//   u_t = U0[t][i] - W[t] . S[i]                 (written over U0)
+// Forward: rows of the state, chunk by chunk.  A CTA owns 32 rows of one head's state
+// (grid (H, 4), 4 warps of 8 rows; lane l holds columns 4l .. 4l+3 of each row):
+//   Sc[b][i][:] = S[i][:]                        (state entering chunk c)
+//   u_t = U0[t][i] - W[t] . S[i]                 (written over U0; lane l: t = 2l, 2l+1)
 //   S[i] <- gamma_C S[i] + sum_t lam_t u_t K[t]
-constexpr int kScanRows = 16;
-__global__ void __launch_bounds__(32 * kScanRows) gdn_scan_fwd(const float* __restrict__ state0,
-                                                               int nC, const float* __restrict__ W,
-                                                               const float* __restrict__ kf,
-                                                               float* U, const float* __restrict__ gam,
-                                                               const float* __restrict__ lam,
-                                                               float* Sc, float* state_out) {
-  extern __shared__ float sm[];
-  float* Ws = sm;                // [64][128]
-  float* Ks = sm + kC * kD;      // [64][128]
+// Each chunk's W^T and K (32 KB each) arrive by bulk copy into a two-stage ring, one
+// chunk ahead, and every value read from shared memory serves the warp's 8 rows: with
+// one row per warp the shared-memory pipe was saturated (1.05 ms at R = 4,096, H = 32).
+constexpr int kScanCtaRows = 32, kScanWarpRows = 8, kScanWarps = 4;
+constexpr int kScanVStride = kScanCtaRows + 4;          // v rows: spread the lanes' stores
+constexpr uint32_t kScanChunkBytes = kC * kD * 4;       // one of W^T, K
+constexpr size_t kScanFwdSmem = 4 * (size_t)kScanChunkBytes +
+                                (size_t)(kScanCtaRows * kD + kC * kScanVStride) * 4 + 64;
+__global__ void __launch_bounds__(32 * kScanWarps) gdn_scan_fwd(const float* __restrict__ state0,
+                                                                int nC, const float* __restrict__ Wtg,
+                                                                const float* __restrict__ kf,
+                                                                float* U, const float* __restrict__ gam,
+                                                                const float* __restrict__ lam,
+                                                                float* Sc, float* state_out,
+                                                                uint32_t* err) {
+  extern __shared__ __align__(128) uint8_t smraw[];
+  float* ring = reinterpret_cast<float*>(smraw);         // stage s: W^T [128][64], K [64][128]
+  float* Ssm = ring + 4 * kC * kD;                       // [32][128]: rows entering the chunk
+  float* Vsm = Ssm + kScanCtaRows * kD;                  // [64][kScanVStride]: lam_t u_t
+  const uint32_t full0 = smem_u32(Vsm + kC * kScanVStride), empty0 = full0 + 16;
   const int h = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int i = blockIdx.y * kScanRows + warp;
-  float S[4];
+  const int wr = warp * kScanWarpRows;                   // the warp's rows: i0 + wr + r
+  const int i0 = blockIdx.y * kScanCtaRows;
+  if (threadIdx.x == 0) {
+    for (int st = 0; st < 2; ++st) {
+      umma::mbar_init(full0 + 8 * st, 1);
+      umma::mbar_init(empty0 + 8 * st, kScanWarps);
+    }
+    umma::fence_barrier_init();
+  }
+  __syncthreads();
+  auto issue = [&](int c) {  // chunk c into stage c & 1 (one thread)
+    const int st = c & 1;
+    const int64_t b = (int64_t)h * nC + c;
+    umma::mbar_expect_tx(full0 + 8 * st, 2 * kScanChunkBytes);
+    umma::bulk_load(smem_u32(ring + st * 2 * kC * kD), Wtg + b * kC * kD, kScanChunkBytes, full0 + 8 * st);
+    umma::bulk_load(smem_u32(ring + st * 2 * kC * kD + kC * kD), kf + b * kC * kD, kScanChunkBytes,
+                    full0 + 8 * st);
+  };
+  int issued = 0;
+  if (threadIdx.x == 0 && nC > 0) {
+    issue(0);
+    issued = 1;
+  }
+  float S[kScanWarpRows][4];
 #pragma unroll
-  for (int m = 0; m < 4; ++m) S[m] = state0[((int64_t)h * kD + i) * kD + lane + 32 * m];
+  for (int r = 0; r < kScanWarpRows; ++r) {
+    const float4 v = *reinterpret_cast<const float4*>(state0 + ((int64_t)h * kD + i0 + wr + r) * kD + 4 * lane);
+    S[r][0] = v.x; S[r][1] = v.y; S[r][2] = v.z; S[r][3] = v.w;
+  }
+  bool ok = true;
   for (int c = 0; c < nC; ++c) {
     const int64_t b = (int64_t)h * nC + c;
-    __syncthreads();
-    for (int e = threadIdx.x; e < kC * kD; e += blockDim.x) {
-      Ws[e] = W[b * kC * kD + e];
-      Ks[e] = kf[b * kC * kD + e];
+    const int st = c & 1;
+    // the next chunk's copies (warp 0; its stage was last read in chunk c - 1)
+    if (warp == 0 && c + 1 < nC) {
+      ok = c == 0 || umma::mbar_wait(empty0 + 8 * ((c + 1) & 1), ((c - 1) >> 1) & 1);
+      if (ok && lane == 0) {
+        issue(c + 1);
+        issued = c + 2;
+      }
     }
-    __syncthreads();
+    // this chunk's U0 and lam, independent of the state: in flight before the waits
+    float u0[kScanWarpRows][2], lm[2];
 #pragma unroll
-    for (int m = 0; m < 4; ++m) Sc[(b * kD + i) * kD + lane + 32 * m] = S[m];
-    float p[kC];
+    for (int q = 0; q < 2; ++q) {
+      const int t = 2 * lane + q;
+      lm[q] = lam[b * kC + t];
 #pragma unroll
-    for (int t = 0; t < kC; ++t) {
-      float s = 0.f;
-#pragma unroll
-      for (int m = 0; m < 4; ++m) s = fmaf(Ws[t * kD + lane + 32 * m], S[m], s);
-      p[t] = s;
-    }
-    warp_reduce64(p, lane);
-    float vl[2];
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      const int t = 2 * lane + r;
-      float* up = U + (b * kC + t) * kD + i;
-      const float u = *up - p[r];
-      *up = u;
-      vl[r] = lam[b * kC + t] * u;
+      for (int r = 0; r < kScanWarpRows; ++r) u0[r][q] = U[(b * kC + t) * kD + i0 + wr + r];
     }
     const float gC = gam[b * kC + kC - 1];
+    // the state entering the chunk: to Sc, and this warp's rows to shared memory
 #pragma unroll
-    for (int m = 0; m < 4; ++m) S[m] *= gC;
-#pragma unroll 8
-    for (int t = 0; t < kC; ++t) {
-      const float vt = __shfl_sync(0xffffffffu, vl[t & 1], t >> 1);
-#pragma unroll
-      for (int m = 0; m < 4; ++m) S[m] = fmaf(vt, Ks[t * kD + lane + 32 * m], S[m]);
+    for (int r = 0; r < kScanWarpRows; ++r) {
+      const float4 v = make_float4(S[r][0], S[r][1], S[r][2], S[r][3]);
+      *reinterpret_cast<float4*>(Sc + (b * kD + i0 + wr + r) * kD + 4 * lane) = v;
+      *reinterpret_cast<float4*>(Ssm + (wr + r) * kD + 4 * lane) = v;
     }
-  }
-  if (state_out)
+    __syncwarp();
+    if (!ok || !umma::mbar_wait(full0 + 8 * st, (c >> 1) & 1)) {
+      ls_report(err, LS_DEVERR_TIMEOUT);
+      ok = false;
+      break;
+    }
+    const float* Wt = ring + st * 2 * kC * kD;
+    const float* Ks = Wt + kC * kD;
+    // W[t] . S[i] for t = 2 lane, 2 lane + 1
+    float acc[kScanWarpRows][2];
 #pragma unroll
-    for (int m = 0; m < 4; ++m) state_out[((int64_t)h * kD + i) * kD + lane + 32 * m] = S[m];
+    for (int r = 0; r < kScanWarpRows; ++r) acc[r][0] = acc[r][1] = 0.f;
+#pragma unroll 2
+    for (int k = 0; k < kD; k += 4) {
+      float2 w[4];
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) w[kk] = *reinterpret_cast<const float2*>(Wt + (k + kk) * kC + 2 * lane);
+#pragma unroll
+      for (int r = 0; r < kScanWarpRows; ++r) {
+        const float4 sv = *reinterpret_cast<const float4*>(Ssm + (wr + r) * kD + k);
+        acc[r][0] = fmaf(w[0].x, sv.x, fmaf(w[1].x, sv.y, fmaf(w[2].x, sv.z, fmaf(w[3].x, sv.w, acc[r][0]))));
+        acc[r][1] = fmaf(w[0].y, sv.x, fmaf(w[1].y, sv.y, fmaf(w[2].y, sv.z, fmaf(w[3].y, sv.w, acc[r][1]))));
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const int t = 2 * lane + q;
+      float vr[kScanWarpRows];
+#pragma unroll
+      for (int r = 0; r < kScanWarpRows; ++r) {
+        const float u = u0[r][q] - acc[r][q];
+        U[(b * kC + t) * kD + i0 + wr + r] = u;
+        vr[r] = lm[q] * u;
+      }
+      *reinterpret_cast<float4*>(Vsm + t * kScanVStride + wr) = make_float4(vr[0], vr[1], vr[2], vr[3]);
+      *reinterpret_cast<float4*>(Vsm + t * kScanVStride + wr + 4) = make_float4(vr[4], vr[5], vr[6], vr[7]);
+    }
+    __syncwarp();
+    // S[i] <- gamma_C S[i] + sum_t v_t K[t]
+#pragma unroll
+    for (int r = 0; r < kScanWarpRows; ++r)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) S[r][q] *= gC;
+#pragma unroll 4
+    for (int t = 0; t < kC; ++t) {
+      const float4 kv = *reinterpret_cast<const float4*>(Ks + t * kD + 4 * lane);
+      const float4 va = *reinterpret_cast<const float4*>(Vsm + t * kScanVStride + wr);
+      const float4 vb = *reinterpret_cast<const float4*>(Vsm + t * kScanVStride + wr + 4);
+      const float vv[kScanWarpRows] = {va.x, va.y, va.z, va.w, vb.x, vb.y, vb.z, vb.w};
+#pragma unroll
+      for (int r = 0; r < kScanWarpRows; ++r) {
+        S[r][0] = fmaf(vv[r], kv.x, S[r][0]);
+        S[r][1] = fmaf(vv[r], kv.y, S[r][1]);
+        S[r][2] = fmaf(vv[r], kv.z, S[r][2]);
+        S[r][3] = fmaf(vv[r], kv.w, S[r][3]);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) umma::mbar_arrive(empty0 + 8 * st);  // this warp is done with the stage
+  }
+  if (ok && state_out)
+#pragma unroll
+    for (int r = 0; r < kScanWarpRows; ++r)
+      *reinterpret_cast<float4*>(state_out + ((int64_t)h * kD + i0 + wr + r) * kD + 4 * lane) =
+          make_float4(S[r][0], S[r][1], S[r][2], S[r][3]);
+  // do not leave while a copy into this CTA's shared memory may be in flight
+  if (threadIdx.x == 0)
+    for (int c = issued - 2 > 0 ? issued - 2 : 0; c < issued; ++c)
+      umma::mbar_wait(full0 + 8 * (c & 1), (c >> 1) & 1);
 }
 
+constexpr int kScanRows = 16;  // backward hand-off: rows of dS per CTA, one per warp
 // Backward: row i of dS (the gradient of the state leaving the chunk), chunks in reverse:
 //   dSC[b][i][:] = dS[i]
 //   a_t = K[t] . dS[i];  dZ_t = dZ0[t][i] + sum_{s >= t} T[s][t] lam_s a_s;  dY_t = beta_t dZ_t
@@ -362,11 +457,28 @@ __global__ void __launch_bounds__(32 * kScanRows) gdn_scan_bwd(int nC, const flo
   for (int c = nC - 1; c >= 0; --c) {
     const int64_t b = (int64_t)h * nC + c;
     __syncthreads();
-    for (int e = threadIdx.x; e < kC * kD; e += blockDim.x) {
-      Ks[e] = kf[b * kC * kD + e];
-      Qs[e] = qf[b * kC * kD + e];
+    {
+      // all loads of the chunk in flight at once
+      constexpr int kPer = kC * kD / 4 / (32 * kScanRows), kPerT = kC * kC / 4 / (32 * kScanRows);
+      const float4* K4 = reinterpret_cast<const float4*>(kf + b * kC * kD);
+      const float4* Q4 = reinterpret_cast<const float4*>(qf + b * kC * kD);
+      const float4* T4 = reinterpret_cast<const float4*>(Tm + b * kC * kC);
+      float4 kv[kPer], qv[kPer], tv[kPerT];
+#pragma unroll
+      for (int q = 0; q < kPer; ++q) {
+        kv[q] = K4[threadIdx.x + q * 32 * kScanRows];
+        qv[q] = Q4[threadIdx.x + q * 32 * kScanRows];
+      }
+#pragma unroll
+      for (int q = 0; q < kPerT; ++q) tv[q] = T4[threadIdx.x + q * 32 * kScanRows];
+#pragma unroll
+      for (int q = 0; q < kPer; ++q) {
+        reinterpret_cast<float4*>(Ks)[threadIdx.x + q * 32 * kScanRows] = kv[q];
+        reinterpret_cast<float4*>(Qs)[threadIdx.x + q * 32 * kScanRows] = qv[q];
+      }
+#pragma unroll
+      for (int q = 0; q < kPerT; ++q) reinterpret_cast<float4*>(Ts)[threadIdx.x + q * 32 * kScanRows] = tv[q];
     }
-    for (int e = threadIdx.x; e < kC * kC; e += blockDim.x) Ts[e] = Tm[b * kC * kC + e];
     __syncthreads();
 #pragma unroll
     for (int m = 0; m < 4; ++m) dSC[(b * kD + i) * kD + lane + 32 * m] = dS[m];
@@ -607,14 +719,15 @@ void gdn_common(Launcher& L, const LsGdnArgs& a, const GdnLayout& W_, void* ws,
   if (L.err != cudaSuccess) return;
   gdn_rows<<<dim3(nb, kC), kD, 0, L.st>>>(x2, vf, bet, nullptr, 1.f, nullptr, 0.f);
   L.check();
-  gemm(L, nb, false, false, kC, kD, kC, tm, kC, kCC, x1, kD, kCD, w, kD, kCD, 1.f);
+  // W^T [128][64] per chunk (the state hand-off reads W by columns)
+  gemm(L, nb, true, true, kD, kC, kC, x1, kD, kCD, tm, kC, kCC, w, kC, kCD, 1.f);
   gemm(L, nb, false, false, kC, kD, kC, tm, kC, kCC, x2, kD, kCD, u, kD, kCD, 1.f);
   if (L.err != cudaSuccess) return;
-  const size_t smem = 2 * kCD * sizeof(float);
-  L.err = cudaFuncSetAttribute(gdn_scan_fwd, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  L.err = cudaFuncSetAttribute(gdn_scan_fwd, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)kScanFwdSmem);
   if (L.err != cudaSuccess) return;
-  gdn_scan_fwd<<<dim3(a.H, kD / kScanRows), 32 * kScanRows, smem, L.st>>>(
-      a.state0, nC, w, kf, u, gam, lam, at<float>(ws, W_.sc), state_out);
+  gdn_scan_fwd<<<dim3(a.H, kD / kScanCtaRows), 32 * kScanWarps, kScanFwdSmem, L.st>>>(
+      a.state0, nC, w, kf, u, gam, lam, at<float>(ws, W_.sc), state_out, a.err);
   L.check();
   // P = (Q' K^T) * Gam, lower incl.
   gemm(L, nb, false, true, kC, kC, kD, qf, kD, kCD, kf, kD, kCD, pm, kC, kCC, 1.f);

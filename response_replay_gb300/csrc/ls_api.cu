@@ -674,7 +674,7 @@ ls_status ls_gdn_replay_fwd(const float* state0, const void* q, const void* k, c
   if (!workspace || workspace_bytes < need || !aligned16(workspace)) return LS_ERR_WORKSPACE;
   DevInfo d;
   if ((s = dev_info(&d)) != LS_OK) return s;
-  LsGdnArgs a{state0, q, k, v, g, beta, R, H, scale};
+  LsGdnArgs a{state0, q, k, v, g, beta, R, H, scale, d.err};
   return from_cuda(ls_launch_gdn_fwd(a, o, state_out, workspace, (cudaStream_t)stream));
 }
 
@@ -694,7 +694,7 @@ ls_status ls_gdn_replay_bwd(const float* state0, const void* q, const void* k, c
   if (!workspace || workspace_bytes < need || !aligned16(workspace)) return LS_ERR_WORKSPACE;
   DevInfo d;
   if ((s = dev_info(&d)) != LS_OK) return s;
-  LsGdnArgs a{state0, q, k, v, g, beta, R, H, scale};
+  LsGdnArgs a{state0, q, k, v, g, beta, R, H, scale, d.err};
   return from_cuda(ls_launch_gdn_bwd(a, d_o, accumulate != 0, dq, dk, dv, dg, dbeta, workspace,
                                      (cudaStream_t)stream));
 }

@@ -149,6 +149,7 @@ struct LsGdnArgs {
   const float* beta;    // [R][H]
   int32_t R, H;
   float scale;
+  uint32_t* err;        // device error word (bounded pipeline waits report here)
 };
 size_t ls_gdn_ws_bytes(int R, int H, bool bwd);
 cudaError_t ls_launch_gdn_fwd(const LsGdnArgs& a, void* o, float* state_out, void* ws,
