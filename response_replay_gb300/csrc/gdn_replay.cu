@@ -433,96 +433,164 @@ __global__ void __launch_bounds__(32 * kScanWarps) gdn_scan_fwd(const float* __r
       umma::mbar_wait(full0 + 8 * (c & 1), (c >> 1) & 1);
 }
 
-constexpr int kScanRows = 16;  // backward hand-off: rows of dS per CTA, one per warp
-// Backward: row i of dS (the gradient of the state leaving the chunk), chunks in reverse:
+// Backward: rows of dS (the gradient of the state leaving the chunk), chunks in reverse:
 //   dSC[b][i][:] = dS[i]
 //   a_t = K[t] . dS[i];  dZ_t = dZ0[t][i] + sum_{s >= t} T[s][t] lam_s a_s;  dY_t = beta_t dZ_t
 //   dS[i] <- gamma_C dS[i] + sum_t gamma_t (dO[t][i] Q'[t] - dY_t K[t])
-__global__ void __launch_bounds__(32 * kScanRows) gdn_scan_bwd(int nC, const float* __restrict__ kf,
-                                                               const float* __restrict__ qf,
-                                                               const float* __restrict__ dof,
-                                                               const float* __restrict__ Tm,
-                                                               const float* __restrict__ dZ0,
-                                                               const float* __restrict__ gam,
-                                                               const float* __restrict__ lam,
-                                                               const float* __restrict__ bet,
-                                                               float* dSC) {
-  extern __shared__ float sm[];
-  float* Ks = sm;                 // [64][128]
-  float* Qs = sm + kC * kD;       // [64][128]
-  float* Ts = sm + 2 * kC * kD;   // [64][64]
+// A CTA owns 32 rows of one head's dS (grid (H, 4), 4 warps).  The row update runs with
+// 8 rows per warp and 4 columns per lane; the dot products and the triangular product
+// run with one row per lane and one 16-token block per warp, reading the rows from
+// shared memory (padded: conflict-free) and K and T as broadcasts.  Each chunk's K, Q'
+// and T arrive by bulk copy into a two-stage ring one chunk ahead.
+constexpr int kBsRowStride = kD + 4;   // dS rows in shared memory
+constexpr int kBsAStride = kScanCtaRows + 1;
+constexpr uint32_t kBsStageBytes = (2 * kC * kD + kC * kC) * 4;  // K, Q', T of a chunk
+constexpr size_t kScanBwdSmem = 2 * (size_t)kBsStageBytes +
+                                (size_t)(kScanCtaRows * kBsRowStride + kC * kBsAStride +
+                                         2 * kC * kScanVStride) * 4 + 64;
+__global__ void __launch_bounds__(32 * kScanWarps) gdn_scan_bwd(int nC, const float* __restrict__ kf,
+                                                                const float* __restrict__ qf,
+                                                                const float* __restrict__ dof,
+                                                                const float* __restrict__ Tm,
+                                                                const float* __restrict__ dZ0,
+                                                                const float* __restrict__ gam,
+                                                                const float* __restrict__ lam,
+                                                                const float* __restrict__ bet,
+                                                                float* dSC, uint32_t* err) {
+  extern __shared__ __align__(128) uint8_t smraw[];
+  float* ring = reinterpret_cast<float*>(smraw);              // stage: K, Q' [64][128], T [64][64]
+  float* Ssm = ring + 2 * (2 * kC * kD + kC * kC);            // [32][kBsRowStride]
+  float* Asm = Ssm + kScanCtaRows * kBsRowStride;             // [64][kBsAStride]: lam_s a_s
+  float* Cq = Asm + kC * kBsAStride;                           // [64][kScanVStride]
+  float* Ck = Cq + kC * kScanVStride;                         // [64][kScanVStride]
+  const uint32_t full0 = smem_u32(Ck + kC * kScanVStride);
   const int h = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int i = blockIdx.y * kScanRows + warp;
-  float dS[4] = {0.f, 0.f, 0.f, 0.f};
-  for (int c = nC - 1; c >= 0; --c) {
+  const int wr = warp * kScanWarpRows;   // update layout: rows wr .. wr+7, columns 4 lane ..
+  const int t0 = 16 * warp;              // dot layout: row lane, tokens t0 .. t0+15
+  const int i0 = blockIdx.y * kScanCtaRows;
+  if (threadIdx.x == 0) {
+    umma::mbar_init(full0, 1);
+    umma::mbar_init(full0 + 8, 1);
+    umma::fence_barrier_init();
+  }
+  __syncthreads();
+  auto issue = [&](int n) {  // the n-th chunk in reverse order into stage n & 1 (one thread)
+    const int st = n & 1;
+    const int64_t b = (int64_t)h * nC + (nC - 1 - n);
+    float* dst = ring + st * (2 * kC * kD + kC * kC);
+    umma::mbar_expect_tx(full0 + 8 * st, kBsStageBytes);
+    umma::bulk_load(smem_u32(dst), kf + b * kC * kD, kC * kD * 4, full0 + 8 * st);
+    umma::bulk_load(smem_u32(dst + kC * kD), qf + b * kC * kD, kC * kD * 4, full0 + 8 * st);
+    umma::bulk_load(smem_u32(dst + 2 * kC * kD), Tm + b * kC * kC, kC * kC * 4, full0 + 8 * st);
+  };
+  int issued = 0;
+  if (threadIdx.x == 0 && nC > 0) {
+    issue(0);
+    issued = 1;
+  }
+  float dS[kScanWarpRows][4];
+#pragma unroll
+  for (int r = 0; r < kScanWarpRows; ++r)
+#pragma unroll
+    for (int q = 0; q < 4; ++q) dS[r][q] = 0.f;
+  for (int n = 0; n < nC; ++n) {
+    const int c = nC - 1 - n, st = n & 1;
     const int64_t b = (int64_t)h * nC + c;
-    __syncthreads();
-    {
-      // all loads of the chunk in flight at once
-      constexpr int kPer = kC * kD / 4 / (32 * kScanRows), kPerT = kC * kC / 4 / (32 * kScanRows);
-      const float4* K4 = reinterpret_cast<const float4*>(kf + b * kC * kD);
-      const float4* Q4 = reinterpret_cast<const float4*>(qf + b * kC * kD);
-      const float4* T4 = reinterpret_cast<const float4*>(Tm + b * kC * kC);
-      float4 kv[kPer], qv[kPer], tv[kPerT];
+    // this chunk's dZ0, dO (this lane's row, the warp's tokens) and per-token scalars
+    float dz0[16], dov[16];
 #pragma unroll
-      for (int q = 0; q < kPer; ++q) {
-        kv[q] = K4[threadIdx.x + q * 32 * kScanRows];
-        qv[q] = Q4[threadIdx.x + q * 32 * kScanRows];
-      }
-#pragma unroll
-      for (int q = 0; q < kPerT; ++q) tv[q] = T4[threadIdx.x + q * 32 * kScanRows];
-#pragma unroll
-      for (int q = 0; q < kPer; ++q) {
-        reinterpret_cast<float4*>(Ks)[threadIdx.x + q * 32 * kScanRows] = kv[q];
-        reinterpret_cast<float4*>(Qs)[threadIdx.x + q * 32 * kScanRows] = qv[q];
-      }
-#pragma unroll
-      for (int q = 0; q < kPerT; ++q) reinterpret_cast<float4*>(Ts)[threadIdx.x + q * 32 * kScanRows] = tv[q];
-    }
-    __syncthreads();
-#pragma unroll
-    for (int m = 0; m < 4; ++m) dSC[(b * kD + i) * kD + lane + 32 * m] = dS[m];
-    float p[kC];
-#pragma unroll
-    for (int t = 0; t < kC; ++t) {
-      float s = 0.f;
-#pragma unroll
-      for (int m = 0; m < 4; ++m) s = fmaf(Ks[t * kD + lane + 32 * m], dS[m], s);
-      p[t] = s;
-    }
-    warp_reduce64(p, lane);
-    float bv[2];
-#pragma unroll
-    for (int r = 0; r < 2; ++r) bv[r] = lam[b * kC + 2 * lane + r] * p[r];
-    float z0 = 0.f, z1 = 0.f;
-#pragma unroll 8
-    for (int s = 0; s < kC; ++s) {
-      const float bs = __shfl_sync(0xffffffffu, bv[s & 1], s >> 1);
-      const float2 tt = *reinterpret_cast<const float2*>(Ts + s * kC + 2 * lane);
-      z0 = fmaf(tt.x, bs, z0);  // T[s][t] is zero for s < t
-      z1 = fmaf(tt.y, bs, z1);
-    }
-    float cq[2], ck[2];
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      const int t = 2 * lane + r;
-      const float dz = dZ0[(b * kC + t) * kD + i] + (r == 0 ? z0 : z1);
-      const float gm = gam[b * kC + t];
-      cq[r] = gm * dof[(b * kC + t) * kD + i];
-      ck[r] = gm * bet[b * kC + t] * dz;
+    for (int tt = 0; tt < 16; ++tt) {
+      dz0[tt] = dZ0[(b * kC + t0 + tt) * kD + i0 + lane];
+      dov[tt] = dof[(b * kC + t0 + tt) * kD + i0 + lane];
     }
     const float gC = gam[b * kC + kC - 1];
+    // dS entering this step: to dSC and to shared memory
 #pragma unroll
-    for (int m = 0; m < 4; ++m) dS[m] *= gC;
-#pragma unroll 8
+    for (int r = 0; r < kScanWarpRows; ++r) {
+      const float4 v = make_float4(dS[r][0], dS[r][1], dS[r][2], dS[r][3]);
+      *reinterpret_cast<float4*>(dSC + (b * kD + i0 + wr + r) * kD + 4 * lane) = v;
+      *reinterpret_cast<float4*>(Ssm + (wr + r) * kBsRowStride + 4 * lane) = v;
+    }
+    __syncthreads();  // rows in shared memory; the other stage's last readers are done
+    if (threadIdx.x == 0 && n + 1 < nC) {
+      issue(n + 1);
+      issued = n + 2;
+    }
+    const bool got = umma::mbar_wait(full0 + 8 * st, (n >> 1) & 1);
+    if (!__syncthreads_and(got)) {
+      if (threadIdx.x == 0) ls_report(err, LS_DEVERR_TIMEOUT);
+      break;
+    }
+    const float* Ks = ring + st * (2 * kC * kD + kC * kC);
+    const float* Qs = Ks + kC * kD;
+    const float* Ts = Qs + kC * kD;
+    // a_t = K[t] . dS[row lane] for the warp's 16 tokens
+    float av[16];
+#pragma unroll
+    for (int tt = 0; tt < 16; ++tt) av[tt] = 0.f;
+#pragma unroll 2
+    for (int k = 0; k < kD; k += 4) {
+      const float4 sv = *reinterpret_cast<const float4*>(Ssm + lane * kBsRowStride + k);
+#pragma unroll
+      for (int tt = 0; tt < 16; ++tt) {
+        const float4 kv = *reinterpret_cast<const float4*>(Ks + (t0 + tt) * kD + k);
+        av[tt] = fmaf(kv.x, sv.x, fmaf(kv.y, sv.y, fmaf(kv.z, sv.z, fmaf(kv.w, sv.w, av[tt]))));
+      }
+    }
+#pragma unroll
+    for (int tt = 0; tt < 16; ++tt) Asm[(t0 + tt) * kBsAStride + lane] = __ldg(lam + b * kC + t0 + tt) * av[tt];
+    __syncthreads();
+    // z_t = sum_{s >= t} T[s][t] lam_s a_s  (T[s][t] = 0 for s < t)
+    float z[16];
+#pragma unroll
+    for (int tt = 0; tt < 16; ++tt) z[tt] = 0.f;
+    for (int s2 = t0; s2 < kC; ++s2) {
+      const float bs = Asm[s2 * kBsAStride + lane];
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        const float4 tv = *reinterpret_cast<const float4*>(Ts + s2 * kC + t0 + 4 * q4);
+        z[4 * q4 + 0] = fmaf(tv.x, bs, z[4 * q4 + 0]);
+        z[4 * q4 + 1] = fmaf(tv.y, bs, z[4 * q4 + 1]);
+        z[4 * q4 + 2] = fmaf(tv.z, bs, z[4 * q4 + 2]);
+        z[4 * q4 + 3] = fmaf(tv.w, bs, z[4 * q4 + 3]);
+      }
+    }
+#pragma unroll
+    for (int tt = 0; tt < 16; ++tt) {
+      const int t = t0 + tt;
+      const float gm = __ldg(gam + b * kC + t);
+      Cq[t * kScanVStride + lane] = gm * dov[tt];
+      Ck[t * kScanVStride + lane] = gm * __ldg(bet + b * kC + t) * (dz0[tt] + z[tt]);
+    }
+    __syncthreads();
+    // dS[i] <- gamma_C dS[i] + sum_t (cq_t Q'[t] - ck_t K[t])
+#pragma unroll
+    for (int r = 0; r < kScanWarpRows; ++r)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) dS[r][q] *= gC;
+#pragma unroll 2
     for (int t = 0; t < kC; ++t) {
-      const float a = __shfl_sync(0xffffffffu, cq[t & 1], t >> 1);
-      const float e = __shfl_sync(0xffffffffu, ck[t & 1], t >> 1);
+      const float4 kv = *reinterpret_cast<const float4*>(Ks + t * kD + 4 * lane);
+      const float4 qv = *reinterpret_cast<const float4*>(Qs + t * kD + 4 * lane);
+      const float4 qa = *reinterpret_cast<const float4*>(Cq + t * kScanVStride + wr);
+      const float4 qb = *reinterpret_cast<const float4*>(Cq + t * kScanVStride + wr + 4);
+      const float4 ka = *reinterpret_cast<const float4*>(Ck + t * kScanVStride + wr);
+      const float4 kb = *reinterpret_cast<const float4*>(Ck + t * kScanVStride + wr + 4);
+      const float cq[kScanWarpRows] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
+      const float ck[kScanWarpRows] = {ka.x, ka.y, ka.z, ka.w, kb.x, kb.y, kb.z, kb.w};
 #pragma unroll
-      for (int m = 0; m < 4; ++m)
-        dS[m] = fmaf(a, Qs[t * kD + lane + 32 * m], fmaf(-e, Ks[t * kD + lane + 32 * m], dS[m]));
+      for (int r = 0; r < kScanWarpRows; ++r) {
+        dS[r][0] = fmaf(cq[r], qv.x, fmaf(-ck[r], kv.x, dS[r][0]));
+        dS[r][1] = fmaf(cq[r], qv.y, fmaf(-ck[r], kv.y, dS[r][1]));
+        dS[r][2] = fmaf(cq[r], qv.z, fmaf(-ck[r], kv.z, dS[r][2]));
+        dS[r][3] = fmaf(cq[r], qv.w, fmaf(-ck[r], kv.w, dS[r][3]));
+      }
     }
   }
+  // do not leave while a copy into this CTA's shared memory may be in flight
+  if (threadIdx.x == 0)
+    for (int n = issued - 2 > 0 ? issued - 2 : 0; n < issued; ++n)
+      umma::mbar_wait(full0 + 8 * (n & 1), (n >> 1) & 1);
 }
 
 // ---------------------------------------------------------------- outputs
@@ -793,11 +861,11 @@ cudaError_t ls_launch_gdn_bwd(const LsGdnArgs& a, const void* d_o, int accumulat
   gemm(L, nb, true, false, kC, kD, kC, tm, kC, kCC, x3, kD, kCD, w, kD, kCD, 1.f);
   if (L.err != cudaSuccess) return L.err;
   {
-    const size_t smem = (2 * kCD + kCC) * sizeof(float);
-    L.err = cudaFuncSetAttribute(gdn_scan_bwd, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    L.err = cudaFuncSetAttribute(gdn_scan_bwd, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kScanBwdSmem);
     if (L.err != cudaSuccess) return L.err;
-    gdn_scan_bwd<<<dim3(a.H, kD / kScanRows), 32 * kScanRows, smem, st>>>(nC, kf, qf, dof, tm, w,
-                                                                         gam, lam, bet, dsc);
+    gdn_scan_bwd<<<dim3(a.H, kD / kScanCtaRows), 32 * kScanWarps, kScanBwdSmem, st>>>(
+        nC, kf, qf, dof, tm, w, gam, lam, bet, dsc, a.err);
     L.check();
   }
   // x1 = K S0^T (the state's read-out at k_t);  x2 = Y = V - diag(gamma) x1
