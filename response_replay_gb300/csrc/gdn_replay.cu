@@ -134,17 +134,18 @@ __global__ void __launch_bounds__(128) gdn_load(const __nv_bfloat16* __restrict_
 // C[b] = alpha diag(rs[b]) op(A[b]) op(B[b]) (+ C[b]), op(X) = X or X^T, masked to the
 // lower triangle (mask 1: row >= col, 2: row > col; 0: none).  Row-major, leading
 // dimensions lda / ldb / ldc, batch strides sA / sB / sC (elements); rs may be NULL.
-// 64 x 64 output tiles, 256 threads, 16 x 4 x 4 accumulation (M, N multiples of 64, K of
-// 16: the chunk shapes 64 and 128).
+// 64 x 64 output tiles, 64 threads with 8 x 8 outputs each (rows 8 ty .., columns 8 tx ..),
+// K in slabs of 16 (M, N multiples of 64, K of 16: the chunk shapes 64 and 128); four
+// 16-byte shared-memory loads feed 64 FMAs.
 template <bool TA, bool TB>
-__global__ void __launch_bounds__(256) gdn_gemm(const float* __restrict__ A, int lda, int64_t sA,
-                                                const float* __restrict__ B, int ldb, int64_t sB,
-                                                float* C, int ldc, int64_t sC, int K, float alpha,
-                                                const float* __restrict__ rs, int64_t srs,
-                                                int accumulate, int mask) {
-  __shared__ float As[16][64 + 4];
-  __shared__ float Bs[16][64 + 4];
-  const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
+__global__ void __launch_bounds__(64) gdn_gemm(const float* __restrict__ A, int lda, int64_t sA,
+                                               const float* __restrict__ B, int ldb, int64_t sB,
+                                               float* C, int ldc, int64_t sC, int K, float alpha,
+                                               const float* __restrict__ rs, int64_t srs,
+                                               int accumulate, int mask) {
+  __shared__ __align__(16) float As[16][64 + 4];
+  __shared__ __align__(16) float Bs[16][64 + 4];
+  const int tid = threadIdx.x, tx = tid & 7, ty = tid >> 3;
   const int m0 = blockIdx.y * 64, n0 = blockIdx.x * 64;
   const int64_t bz = blockIdx.z;
   A += bz * sA;
@@ -152,59 +153,72 @@ __global__ void __launch_bounds__(256) gdn_gemm(const float* __restrict__ A, int
   C += bz * sC;
   if (mask && n0 > m0 + 63) {  // tile entirely above the diagonal
     if (!accumulate)
-      for (int e = tid; e < 64 * 64; e += 256) C[(int64_t)(m0 + e / 64) * ldc + n0 + e % 64] = 0.f;
+      for (int e = tid; e < 64 * 64; e += 64) C[(int64_t)(m0 + e / 64) * ldc + n0 + e % 64] = 0.f;
     return;
   }
-  float acc[4][4];
+  float acc[8][8];
 #pragma unroll
-  for (int i = 0; i < 4; ++i)
+  for (int i = 0; i < 8; ++i)
 #pragma unroll
-    for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+    for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
   for (int k0 = 0; k0 < K; k0 += 16) {
+    float av[16], bv[16];  // the slab's loads all in flight before the stores
 #pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      const int e = tid + 256 * r;  // 1024 elements of each 64 x 16 / 16 x 64 tile
+    for (int r = 0; r < 16; ++r) {
+      const int e = tid + 64 * r;  // 1024 elements of each 64 x 16 / 16 x 64 tile
       if (TA) {  // op(A)[m][k] = A[k][m]: read along m
-        const int kk = e / 64, mm = e % 64;
-        As[kk][mm] = A[(int64_t)(k0 + kk) * lda + m0 + mm];
+        av[r] = A[(int64_t)(k0 + e / 64) * lda + m0 + e % 64];
       } else {
-        const int mm = e / 16, kk = e % 16;
-        As[kk][mm] = A[(int64_t)(m0 + mm) * lda + k0 + kk];
+        av[r] = A[(int64_t)(m0 + e / 16) * lda + k0 + e % 16];
       }
       if (TB) {  // op(B)[k][n] = B[n][k]
-        const int nn = e / 16, kk = e % 16;
-        Bs[kk][nn] = B[(int64_t)(n0 + nn) * ldb + k0 + kk];
+        bv[r] = B[(int64_t)(n0 + e / 16) * ldb + k0 + e % 16];
       } else {
-        const int kk = e / 64, nn = e % 64;
-        Bs[kk][nn] = B[(int64_t)(k0 + kk) * ldb + n0 + nn];
+        bv[r] = B[(int64_t)(k0 + e / 64) * ldb + n0 + e % 64];
       }
+    }
+#pragma unroll
+    for (int r = 0; r < 16; ++r) {
+      const int e = tid + 64 * r;
+      if (TA) As[e / 64][e % 64] = av[r]; else As[e % 16][e / 16] = av[r];
+      if (TB) Bs[e % 16][e / 16] = bv[r]; else Bs[e / 64][e % 64] = bv[r];
     }
     __syncthreads();
 #pragma unroll
     for (int kk = 0; kk < 16; ++kk) {
-      float a[4], bb[4];
+      const float4 a0 = *reinterpret_cast<const float4*>(&As[kk][8 * ty]);
+      const float4 a1 = *reinterpret_cast<const float4*>(&As[kk][8 * ty + 4]);
+      const float4 b0 = *reinterpret_cast<const float4*>(&Bs[kk][8 * tx]);
+      const float4 b1 = *reinterpret_cast<const float4*>(&Bs[kk][8 * tx + 4]);
+      const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+      const float bb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
 #pragma unroll
-      for (int i = 0; i < 4; ++i) a[i] = As[kk][ty + 16 * i];
+      for (int i = 0; i < 8; ++i)
 #pragma unroll
-      for (int j = 0; j < 4; ++j) bb[j] = Bs[kk][tx + 16 * j];
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], bb[j], acc[i][j]);
+        for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(a[i], bb[j], acc[i][j]);
     }
     __syncthreads();
   }
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int m = m0 + ty + 16 * i;
+  for (int i = 0; i < 8; ++i) {
+    const int m = m0 + 8 * ty + i;
     const float sc = alpha * (rs ? rs[bz * srs + m] : 1.f);
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int n = n0 + tx + 16 * j;
-      float x = sc * acc[i][j];
-      if ((mask == 1 && n > m) || (mask == 2 && n >= m)) x = 0.f;
-      float* p = C + (int64_t)m * ldc + n;
-      *p = accumulate ? *p + x : x;
+    for (int j4 = 0; j4 < 2; ++j4) {
+      const int n = n0 + 8 * tx + 4 * j4;
+      float x[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        x[j] = sc * acc[i][4 * j4 + j];
+        if ((mask == 1 && n + j > m) || (mask == 2 && n + j >= m)) x[j] = 0.f;
+      }
+      float4* p = reinterpret_cast<float4*>(C + (int64_t)m * ldc + n);
+      float4 v = make_float4(x[0], x[1], x[2], x[3]);
+      if (accumulate) {
+        const float4 o = *p;
+        v.x += o.x; v.y += o.y; v.z += o.z; v.w += o.w;
+      }
+      *p = v;
     }
   }
 }
@@ -228,18 +242,25 @@ __global__ void __launch_bounds__(256) gdn_decay(float* X, const float* __restri
   }
 }
 
-// Y[b][t][:] = a * s1[b][t] * X1[b][t][:] + c * X2[b][t][:]  (X2 may be NULL); grid nb x 64
-// rows, 128 threads.
-__global__ void __launch_bounds__(128) gdn_rows(float* Y, const float* X1, const float* s1,
+// Y[b][t][:] = a * s1[b][t] * X1[b][t][:] + c * X2[b][t][:]  (X2 may be NULL); grid nb
+// (a chunk per CTA), 256 threads.
+__global__ void __launch_bounds__(256) gdn_rows(float* Y, const float* X1, const float* s1,
                                                 const float* s2, float a, const float* X2,
                                                 float c) {
   const int64_t b = blockIdx.x;
-  const int t = blockIdx.y, j = threadIdx.x;
-  const int64_t e = (b * kC + t) * kD + j;
-  float sc = a * (s1 ? s1[b * kC + t] : 1.f) * (s2 ? s2[b * kC + t] : 1.f);
-  float y = sc * X1[e];
-  if (X2) y += c * X2[e];
-  Y[e] = y;
+#pragma unroll
+  for (int q = 0; q < kC * kD / 4 / 256; ++q) {  // the chunk's 64 rows as float4
+    const int e4 = threadIdx.x + 256 * q, t = e4 / (kD / 4);
+    const float sc = a * (s1 ? s1[b * kC + t] : 1.f) * (s2 ? s2[b * kC + t] : 1.f);
+    const int64_t e = b * kC * kD / 4 + e4;
+    float4 y = reinterpret_cast<const float4*>(X1)[e];
+    y.x *= sc; y.y *= sc; y.z *= sc; y.w *= sc;
+    if (X2) {
+      const float4 x2 = reinterpret_cast<const float4*>(X2)[e];
+      y.x += c * x2.x; y.y += c * x2.y; y.z += c * x2.z; y.w += c * x2.w;
+    }
+    reinterpret_cast<float4*>(Y)[e] = y;
+  }
 }
 
 // T = (I + A)^-1 for the unit lower-triangular I + A of each chunk (A strictly lower):
@@ -674,23 +695,44 @@ __global__ void __launch_bounds__(256) gdn_scalar_grads(const GdnScalarIn in, in
   for (int off = 16; off > 0; off >>= 1) sd += __shfl_xor_sync(0xffffffffu, sd, off);
   if (lane == 0) red[warp] = sd;
   __syncthreads();
-  if (tid < kC) {
-    const int t = tid;
+  {
     const float* dp = in.dp + b * kC * kC;
     const float* pp = in.p + b * kC * kC;
     const float* dm = in.dms + b * kC * kC;
     const float* mm = in.ms + b * kC * kC;
     const float* da = in.da + b * kC * kC;
-    float r1 = 0.f, c1 = 0.f, r2 = 0.f, c2 = 0.f, rb = 0.f;
-    for (int i = 0; i < kC; ++i) {
-      r1 += dp[t * kC + i] * pp[t * kC + i];
-      c1 += dp[i * kC + t] * pp[i * kC + t];
-      r2 += dm[t * kC + i] * mm[t * kC + i];
-      c2 += dm[i * kC + t] * mm[i * kC + t];
-      rb += da[t * kC + i] * mm[t * kC + i];
+    // row sums: one warp per row (coalesced), reduced by shuffles
+    for (int t = warp; t < kC; t += 8) {
+      float r1 = 0.f, r2 = 0.f, rb = 0.f;
+#pragma unroll
+      for (int i = lane; i < kC; i += 32) {
+        const float m = mm[t * kC + i];
+        r1 += dp[t * kC + i] * pp[t * kC + i];
+        r2 += dm[t * kC + i] * m;
+        rb += da[t * kC + i] * m;
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        r1 += __shfl_xor_sync(0xffffffffu, r1, off);
+        r2 += __shfl_xor_sync(0xffffffffu, r2, off);
+        rb += __shfl_xor_sync(0xffffffffu, rb, off);
+      }
+      if (lane == 0) {
+        dG[t] += r1 + r2;
+        zb[t] += rb;
+      }
     }
-    dG[t] += r1 - c1 + r2 - c2;
-    zb[t] += rb;
+    __syncthreads();
+    // column sums: one thread per column (coalesced across the columns)
+    if (tid < kC) {
+      const int t = tid;
+      float c1 = 0.f, c2 = 0.f;
+      for (int i = 0; i < kC; ++i) {
+        c1 += dp[i * kC + t] * pp[i * kC + t];
+        c2 += dm[i * kC + t] * mm[i * kC + t];
+      }
+      dG[t] -= c1 + c2;
+    }
   }
   __syncthreads();
   if (tid == 0) {
@@ -733,13 +775,13 @@ void gemm(Launcher& L, int nb, bool ta, bool tb, int M, int N, int K, const floa
   if (L.err != cudaSuccess) return;
   const dim3 grid(N / 64, M / 64, nb);
   if (!ta && !tb)
-    gdn_gemm<false, false><<<grid, 256, 0, L.st>>>(A, lda, sA, B, ldb, sB, C, ldc, sC, K, alpha, rs, srs, accumulate, mask);
+    gdn_gemm<false, false><<<grid, 64, 0, L.st>>>(A, lda, sA, B, ldb, sB, C, ldc, sC, K, alpha, rs, srs, accumulate, mask);
   else if (!ta && tb)
-    gdn_gemm<false, true><<<grid, 256, 0, L.st>>>(A, lda, sA, B, ldb, sB, C, ldc, sC, K, alpha, rs, srs, accumulate, mask);
+    gdn_gemm<false, true><<<grid, 64, 0, L.st>>>(A, lda, sA, B, ldb, sB, C, ldc, sC, K, alpha, rs, srs, accumulate, mask);
   else if (ta && !tb)
-    gdn_gemm<true, false><<<grid, 256, 0, L.st>>>(A, lda, sA, B, ldb, sB, C, ldc, sC, K, alpha, rs, srs, accumulate, mask);
+    gdn_gemm<true, false><<<grid, 64, 0, L.st>>>(A, lda, sA, B, ldb, sB, C, ldc, sC, K, alpha, rs, srs, accumulate, mask);
   else
-    gdn_gemm<true, true><<<grid, 256, 0, L.st>>>(A, lda, sA, B, ldb, sB, C, ldc, sC, K, alpha, rs, srs, accumulate, mask);
+    gdn_gemm<true, true><<<grid, 64, 0, L.st>>>(A, lda, sA, B, ldb, sB, C, ldc, sC, K, alpha, rs, srs, accumulate, mask);
   L.check();
 }
 
@@ -782,10 +824,10 @@ void gdn_common(Launcher& L, const LsGdnArgs& a, const GdnLayout& W_, void* ws,
   L.check();
   // W = T diag(beta gamma) K,  U0 = T diag(beta) V
   if (L.err != cudaSuccess) return;
-  gdn_rows<<<dim3(nb, kC), kD, 0, L.st>>>(x1, kf, bet, gam, 1.f, nullptr, 0.f);
+  gdn_rows<<<nb, 256, 0, L.st>>>(x1, kf, bet, gam, 1.f, nullptr, 0.f);
   L.check();
   if (L.err != cudaSuccess) return;
-  gdn_rows<<<dim3(nb, kC), kD, 0, L.st>>>(x2, vf, bet, nullptr, 1.f, nullptr, 0.f);
+  gdn_rows<<<nb, 256, 0, L.st>>>(x2, vf, bet, nullptr, 1.f, nullptr, 0.f);
   L.check();
   // W^T [128][64] per chunk (the state hand-off reads W by columns)
   gemm(L, nb, true, true, kD, kC, kC, x1, kD, kCD, tm, kC, kCC, w, kC, kCD, 1.f);
@@ -871,17 +913,17 @@ cudaError_t ls_launch_gdn_bwd(const LsGdnArgs& a, const void* d_o, int accumulat
   // x1 = K S0^T (the state's read-out at k_t);  x2 = Y = V - diag(gamma) x1
   gemm(L, nb, false, true, kC, kD, kD, kf, kD, kCD, sc, kD, kDD, x1, kD, kCD, 1.f);
   if (L.err != cudaSuccess) return L.err;
-  gdn_rows<<<dim3(nb, kC), kD, 0, st>>>(x2, x1, gam, nullptr, -1.f, vf, 1.f);
+  gdn_rows<<<nb, 256, 0, st>>>(x2, x1, gam, nullptr, -1.f, vf, 1.f);
   L.check();
   // x4 = K dSC^T;  dU = x3 + diag(lam) x4 (into x3)
   gemm(L, nb, false, true, kC, kD, kD, kf, kD, kCD, dsc, kD, kDD, x4, kD, kCD, 1.f);
   if (L.err != cudaSuccess) return L.err;
-  gdn_rows<<<dim3(nb, kC), kD, 0, st>>>(x3, x4, lam, nullptr, 1.f, x3, 1.f);
+  gdn_rows<<<nb, 256, 0, st>>>(x3, x4, lam, nullptr, 1.f, x3, 1.f);
   L.check();
   // x5 = dZ = T^T dU;  x6 = dY = diag(beta) dZ (= dV)
   gemm(L, nb, true, false, kC, kD, kC, tm, kC, kCC, x3, kD, kCD, x5, kD, kCD, 1.f);
   if (L.err != cudaSuccess) return L.err;
-  gdn_rows<<<dim3(nb, kC), kD, 0, st>>>(x6, x5, bet, nullptr, 1.f, nullptr, 0.f);
+  gdn_rows<<<nb, 256, 0, st>>>(x6, x5, bet, nullptr, 1.f, nullptr, 0.f);
   L.check();
   // m1 = dA = -(dZ U^T) strictly lower;  tm <- dMs = diag(beta) dA (T is no longer needed)
   gemm(L, nb, false, true, kC, kC, kD, x5, kD, kCD, u, kD, kCD, m1, kC, kCC, -1.f, nullptr, kC, 0, 2);
