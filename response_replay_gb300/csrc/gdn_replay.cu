@@ -161,8 +161,9 @@ __global__ void __launch_bounds__(64) gdn_gemm(const float* __restrict__ A, int 
   for (int i = 0; i < 8; ++i)
 #pragma unroll
     for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
-  for (int k0 = 0; k0 < K; k0 += 16) {
-    float av[16], bv[16];  // the slab's loads all in flight before the stores
+  // The next slab is loaded into registers while the current one is multiplied.
+  float av[16], bv[16];
+  auto load_slab = [&](int k0) {
 #pragma unroll
     for (int r = 0; r < 16; ++r) {
       const int e = tid + 64 * r;  // 1024 elements of each 64 x 16 / 16 x 64 tile
@@ -177,6 +178,9 @@ __global__ void __launch_bounds__(64) gdn_gemm(const float* __restrict__ A, int 
         bv[r] = B[(int64_t)(k0 + e / 64) * ldb + n0 + e % 64];
       }
     }
+  };
+  load_slab(0);
+  for (int k0 = 0; k0 < K; k0 += 16) {
 #pragma unroll
     for (int r = 0; r < 16; ++r) {
       const int e = tid + 64 * r;
@@ -184,6 +188,7 @@ __global__ void __launch_bounds__(64) gdn_gemm(const float* __restrict__ A, int 
       if (TB) Bs[e % 16][e / 16] = bv[r]; else Bs[e / 64][e % 64] = bv[r];
     }
     __syncthreads();
+    if (k0 + 16 < K) load_slab(k0 + 16);
 #pragma unroll
     for (int kk = 0; kk < 16; ++kk) {
       const float4 a0 = *reinterpret_cast<const float4*>(&As[kk][8 * ty]);
