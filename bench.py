@@ -767,6 +767,88 @@ def run_short_sweep(args, local_rank: int):
         }), flush=True)
 
 
+# ------------------------------------------------------------------ host-resident pages
+
+def run_host_sweep(args, local_rank: int):
+    """Supplementary, labelled lines (not the headline): the 2,097,152-position prompt's
+    pages held in pinned host memory (Grace memory, read over NVLink-C2C by the kernels
+    themselves) against the same pages in HBM.  One JSON line per R with forward and
+    backward times in both placements, the prompt-KV GB/s of each pass, and the measured
+    host-to-device copy bandwidth (a 4 GiB copy from pinned memory) for comparison."""
+    import torch
+
+    from response_replay_gb300 import synthetic as syn
+    from response_replay_gb300 import torch_api as api
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    w = syn.WORKLOADS[WORKLOAD]
+    seed = syn.seed_of(WORKLOAD)
+    scale = D ** -0.5
+    pr = syn.make_prompt(w.P, w.hkv, D, w.page_size, seed, dev)
+    dcache = api.PagedKVCache(pr.num_pages, pr.page_table, w.page_size, w.hkv, w.P, device=dev)
+    dcache.capture(pr.k, pr.v)
+    hcache = api.PagedKVCache(pr.num_pages, pr.page_table, w.page_size, w.hkv, w.P,
+                              host_pools=True)
+    hcache.capture(pr.k, pr.v)  # written over the link by the capture kernel
+    del pr
+    stream = torch.cuda.current_stream()
+
+    def timed(fn, steps):
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(steps):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / steps
+
+    # copy-engine bandwidth from pinned host memory, for scale
+    src = torch.empty(1 << 31, dtype=torch.int16, pin_memory=True)
+    dst = torch.empty(1 << 31, dtype=torch.int16, device=dev)
+    copy_ms = timed(lambda: dst.copy_(src, non_blocking=True), max(args.steps, 3))
+    h2d_gbs = src.numel() * 2 / (copy_ms * 1e-3) / 1e9
+    del src, dst
+    kv_bytes = prompt_kv_bytes(w.P, w.hkv)
+    for R in [int(x) for x in args.sweep_host.split(",")]:
+        br = syn.make_branch(R, w.hq, w.hkv, D, seed + 1, dev)
+        o = torch.empty((R, w.hq, D), dtype=torch.bfloat16, device=dev)
+        lse = torch.empty((R, w.hq), dtype=torch.float32, device=dev)
+        dq = torch.empty((R, w.hq, D), dtype=torch.float32, device=dev)
+        dk = torch.empty((R, w.hkv, D), dtype=torch.float32, device=dev)
+        dv = torch.empty((R, w.hkv, D), dtype=torch.float32, device=dev)
+        res = {}
+        for name, cache in (("hbm", dcache), ("host", hcache)):
+            def fwd():
+                api.replay_fwd(cache, br.q, br.k, br.v, scale, w.num_splits, o=o, lse=lse,
+                               stream=stream)
+
+            def bwd():
+                api.replay_bwd(cache, br.q, br.k, br.v, o, lse, br.d_o, scale, w.num_splits,
+                               dq=dq, dk=dk, dv=dv, stream=stream)
+
+            steps = args.steps if R < 1024 else max(1, args.steps // 5)
+            res[name] = (timed(fwd, steps), timed(bwd, steps))
+        f_fl, b_fl = attn_flops(w.P, R, w.hq)
+        (fh, bh), (fd, bd) = res["host"], res["hbm"]
+        print(json.dumps({
+            "sweep": "prompt pages in host (Grace) memory vs HBM, 2,097,152 positions "
+                     "(supplementary)",
+            "R": R, "config": {"workload": f"P={w.P:,}, Hq={w.hq}, Hkv={w.hkv}, d=128, "
+                                           f"{w.page_size}-token pages, {w.num_splits} splits"},
+            "host_fwd_ms": fh, "host_bwd_ms": bh, "hbm_fwd_ms": fd, "hbm_bwd_ms": bd,
+            "host_fwd_kv_gbs": kv_bytes / (fh * 1e-3) / 1e9,
+            "host_bwd_kv_gbs": kv_bytes / (bh * 1e-3) / 1e9,
+            "host_fwd_tflops": f_fl / (fh * 1e-3) / 1e12,
+            "host_bwd_tflops": b_fl / (bh * 1e-3) / 1e12,
+            "h2d_copy_gbs": h2d_gbs, "steps": args.steps, "warmup": args.warmup,
+        }), flush=True)
+
+
 # ------------------------------------------------------------------ self-attention sweep
 
 def run_self_sweep(args, local_rank: int):
@@ -990,6 +1072,9 @@ def main():
     ap.add_argument("--sweep-gdn", default=None,
                     help="comma-separated response lengths: supplementary Gated-DeltaNet "
                          "replay lines instead of the headline step")
+    ap.add_argument("--sweep-host", default=None,
+                    help="comma-separated response lengths: supplementary lines with the "
+                         "prompt pages in pinned host memory against HBM")
     ap.add_argument("--sweep-short", default=None,
                     help="comma-separated response lengths: supplementary short-R sweep "
                          "(one JSON line each) instead of the headline step")
@@ -1009,6 +1094,10 @@ def main():
     if args.sweep_self:
         if rank == 0:
             run_self_sweep(args, local_rank)
+        return
+    if args.sweep_host:
+        if rank == 0:
+            run_host_sweep(args, local_rank)
         return
     if args.sweep_gdn:
         if rank == 0:

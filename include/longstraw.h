@@ -82,7 +82,12 @@ typedef enum { LS_BF16 = 0, LS_FP32 = 1 } ls_dtype;
  *   num_tokens      P, the valid prompt positions; P <= num_logical_pages * page_size.
  *                   Positions >= P on the last page are never read by attention.
  * Supported: head_dim == 128; page_size a power of two in [16, 4096]; num_pages *
- * num_kv_heads * page_size < 2^31. */
+ * num_kv_heads * page_size < 2^31.
+ * The pools may live in host memory that the GPU reads directly (pinned, mapped
+ * allocations; on a Grace-Blackwell node the Grace memory behind NVLink-C2C): the
+ * capture writes and every replay reads them there, with no staging copy.  This is the
+ * GB300 counterpart of holding the prompt's pages in CPU memory (explainer, "Two
+ * incompatible architectures", GLM bullet).  page_table stays in GPU memory. */
 typedef struct {
   void* k_pool;
   void* v_pool;

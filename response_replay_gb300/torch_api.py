@@ -44,22 +44,42 @@ def workspace(nbytes: int, device: torch.device, key: str = "default") -> torch.
     return ws
 
 
+def _check_pool(t: torch.Tensor, name: str, shape):
+    """A page pool: GPU memory, or pinned host memory the GPU reads directly."""
+    if not t.is_cuda and not (t.device.type == "cpu" and t.is_pinned()):
+        raise ValueError(f"{name} must be a CUDA tensor or a pinned host tensor")
+    if t.dtype != torch.bfloat16:
+        raise ValueError(f"{name}: expected torch.bfloat16, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: expected shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
 class PagedKVCache:
-    """K/V page pools plus page table of one attention layer (ls_kv_cache)."""
+    """K/V page pools plus page table of one attention layer (ls_kv_cache).
+
+    host_pools=True places the pools in pinned host memory (on a Grace-Blackwell node,
+    Grace memory read over NVLink-C2C); the kernels read and write them there."""
 
     def __init__(self, num_pages: int, page_table: torch.Tensor, page_size: int, num_kv_heads: int,
                  num_tokens: int, device=None, fill: float | None = None,
-                 k_pool: torch.Tensor | None = None, v_pool: torch.Tensor | None = None):
+                 k_pool: torch.Tensor | None = None, v_pool: torch.Tensor | None = None,
+                 host_pools: bool = False):
         device = torch.device(device) if device is not None else page_table.device
         shape = (num_pages, num_kv_heads, page_size, HEAD_DIM)
         if k_pool is None:
-            k_pool = torch.empty(shape, dtype=torch.bfloat16, device=device)
-            v_pool = torch.empty(shape, dtype=torch.bfloat16, device=device)
+            if host_pools:
+                k_pool = torch.empty(shape, dtype=torch.bfloat16, pin_memory=True)
+                v_pool = torch.empty(shape, dtype=torch.bfloat16, pin_memory=True)
+            else:
+                k_pool = torch.empty(shape, dtype=torch.bfloat16, device=device)
+                v_pool = torch.empty(shape, dtype=torch.bfloat16, device=device)
             if fill is not None:
                 k_pool.fill_(fill)
                 v_pool.fill_(fill)
-        _check(k_pool, "k_pool", torch.bfloat16, shape)
-        _check(v_pool, "v_pool", torch.bfloat16, shape)
+        _check_pool(k_pool, "k_pool", shape)
+        _check_pool(v_pool, "v_pool", shape)
         _check(page_table, "page_table", torch.int32)
         self.k_pool, self.v_pool, self.page_table = k_pool, v_pool, page_table
         self.page_size, self.num_kv_heads, self.num_tokens = page_size, num_kv_heads, num_tokens
@@ -69,7 +89,7 @@ class PagedKVCache:
 
     @property
     def device(self):
-        return self.k_pool.device
+        return self.page_table.device
 
     def capture(self, k: torch.Tensor, v: torch.Tensor, start_pos: int = 0, stream=None) -> None:
         n = k.shape[0]
