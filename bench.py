@@ -849,6 +849,91 @@ def run_host_sweep(args, local_rank: int):
         }), flush=True)
 
 
+# ------------------------------------------------------------------ streamed layers
+
+def run_layers_sweep(args, local_rank: int):
+    """Supplementary, labelled line (not the headline): one response of R = 4,096 tokens
+    replayed through L layers over the 2,097,152-position prompt, forward in layer order
+    and backward last layer first, with the layers' prompt pages (a) all in GPU memory and
+    (b) in pinned host memory, streamed into a two-slot GPU page cache one layer ahead of
+    use (each layer's copy overlapping the previous layer's replay)."""
+    import torch
+
+    from response_replay_gb300 import layers as L
+    from response_replay_gb300 import synthetic as syn
+    from response_replay_gb300 import torch_api as api
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    w = syn.WORKLOADS[WORKLOAD]
+    seed = syn.seed_of(WORKLOAD)
+    scale = D ** -0.5
+    nl = int(args.sweep_layers)
+    R = w.R[0]
+    pr = syn.make_prompt(w.P, w.hkv, D, w.page_size, seed, dev)
+    res = L.LayeredKVCache(nl, pr.num_pages, pr.page_table, w.page_size, w.hkv, w.P, device=dev)
+    st = L.StreamedLayers(nl, pr.num_pages, pr.page_table, w.page_size, w.hkv, w.P, device=dev)
+    for l in range(nl):  # the same prompt K/V in every layer (the values do not matter here)
+        res.capture(l, pr.k, pr.v)
+        st.capture(l, pr.k, pr.v)
+    del pr
+    br = syn.make_branch(R, w.hq, w.hkv, D, seed + 1, dev)
+    o = [torch.empty((R, w.hq, D), dtype=torch.bfloat16, device=dev) for _ in range(nl)]
+    lse = [torch.empty((R, w.hq), dtype=torch.float32, device=dev) for _ in range(nl)]
+    dq = torch.empty((R, w.hq, D), dtype=torch.float32, device=dev)
+    dk = torch.empty((R, w.hkv, D), dtype=torch.float32, device=dev)
+    dv = torch.empty((R, w.hkv, D), dtype=torch.float32, device=dev)
+
+    def step(get, pre, rel):
+        for l in range(nl):
+            c = get(l)
+            if l + 1 < nl:
+                pre(l + 1)
+            api.replay_fwd(c, br.q, br.k, br.v, scale, w.num_splits, o=o[l], lse=lse[l])
+            rel(l)
+        pre(nl - 1)
+        for l in reversed(range(nl)):
+            c = get(l)
+            if l > 0:
+                pre(l - 1)
+            api.replay_bwd(c, br.q, br.k, br.v, o[l], lse[l], br.d_o, scale, w.num_splits,
+                           dq=dq, dk=dk, dv=dv)
+            rel(l)
+
+    none = lambda l: None  # noqa: E731
+    runs = {"hbm": lambda: step(lambda l: res[l], none, none),
+            "streamed": lambda: step(st.cache, st.prefetch, st.release)}
+    out = {}
+    for name, fn in runs.items():
+        for _ in range(max(args.warmup, 1)):
+            fn()
+        torch.cuda.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(args.steps):
+            fn()
+        b.record()
+        torch.cuda.synchronize()
+        out[name] = a.elapsed_time(b) / args.steps
+    f_fl, b_fl = attn_flops(w.P, R, w.hq)
+    print(json.dumps({
+        "sweep": "layers' prompt pages streamed from host (Grace) memory vs held in HBM "
+                 "(supplementary)",
+        "layers": nl, "R": R,
+        "config": {"workload": f"P={w.P:,}, Hq={w.hq}, Hkv={w.hkv}, d=128, {w.page_size}-token "
+                               f"pages, {w.num_splits} splits; forward over the layers, then "
+                               f"backward last layer first"},
+        "hbm_ms": out["hbm"], "streamed_ms": out["streamed"],
+        "streamed_over_hbm": out["streamed"] / out["hbm"],
+        "streamed_tflops": nl * (f_fl + b_fl) / (out["streamed"] * 1e-3) / 1e12,
+        "hbm_tflops": nl * (f_fl + b_fl) / (out["hbm"] * 1e-3) / 1e12,
+        "copy_bytes_per_layer": st.bytes_per_layer,
+        "host_pinned_bytes": nl * st.bytes_per_layer,
+        "steps": args.steps, "warmup": args.warmup,
+    }), flush=True)
+
+
 # ------------------------------------------------------------------ self-attention sweep
 
 def run_self_sweep(args, local_rank: int):
@@ -1072,6 +1157,9 @@ def main():
     ap.add_argument("--sweep-gdn", default=None,
                     help="comma-separated response lengths: supplementary Gated-DeltaNet "
                          "replay lines instead of the headline step")
+    ap.add_argument("--sweep-layers", default=None,
+                    help="number of layers: supplementary line with the layers' prompt pages "
+                         "streamed from pinned host memory against held in HBM")
     ap.add_argument("--sweep-host", default=None,
                     help="comma-separated response lengths: supplementary lines with the "
                          "prompt pages in pinned host memory against HBM")
@@ -1098,6 +1186,10 @@ def main():
     if args.sweep_host:
         if rank == 0:
             run_host_sweep(args, local_rank)
+        return
+    if args.sweep_layers:
+        if rank == 0:
+            run_layers_sweep(args, local_rank)
         return
     if args.sweep_gdn:
         if rank == 0:

@@ -19,6 +19,10 @@ takes its dQ / dK / dV.  This module holds the part that needs no weights:
 - ``reverse_replay_bwd``: the backward of one response through all layers, last layer
   first.  A layer's dK / dV are allocated at that layer's backward and dropped once the
   caller's consumer returns, so one layer's K/V gradients are alive at a time.
+- ``StreamedLayers``: the L layers' prompt pages in pinned host memory (Grace memory on a
+  GB300 node), streamed into a two-slot page cache in GPU memory one layer ahead of the
+  replay that reads them (explainer, same section, GLM bullet: the prompt's pages held in
+  CPU memory).
 
 Every step of the computation is a call of the replay backward in the CUDA library.
 """
@@ -121,3 +125,84 @@ def reverse_replay_bwd(layers: LayeredKVCache, saved: Sequence[tuple],
                             num_splits, stream=stream)
         dk, dv = grads.release()
         consume(l, dq, dk, dv)
+
+
+class StreamedLayers:
+    """The captured prompt pages of L layers held in pinned host memory (on a
+    Grace-Blackwell node, Grace memory: room for every layer of a long prompt, which HBM
+    would not hold), streamed into a two-slot page cache in GPU memory one layer ahead of
+    the replay that reads them.
+
+    The kernels could read the host pages directly, but every unit of a long replay
+    re-reads the prompt and those reads are not kept in L2, so a long replay from host
+    pages is bound by the host link many times over.  Copied once into GPU memory, a
+    layer's pages serve every unit at HBM speed, and the copy of the next layer runs on
+    its own stream while the current layer is replayed.
+
+    Use: ``prefetch(l)`` starts layer l's copy (it waits until the slot's previous layer
+    is released); ``cache(l)`` returns the layer's ``PagedKVCache`` in GPU memory and makes
+    the current stream wait for its copy; ``release(l)`` marks the point on the current
+    stream after which the slot may be overwritten.  Capture writes the host pages
+    directly (``capture``)."""
+
+    def __init__(self, num_layers: int, num_pages: int, page_table: torch.Tensor,
+                 page_size: int, num_kv_heads: int, num_tokens: int, device=None):
+        if num_layers < 1:
+            raise ValueError("num_layers must be at least 1")
+        device = torch.device(device) if device is not None else page_table.device
+        self.device = device
+        shape = (num_pages, num_kv_heads, page_size, api.HEAD_DIM)
+        self.host = [api.PagedKVCache(num_pages, page_table, page_size, num_kv_heads, num_tokens,
+                                      host_pools=True) for _ in range(num_layers)]
+        self.slots = [api.PagedKVCache(num_pages, page_table, page_size, num_kv_heads, num_tokens,
+                                       device=device) for _ in range(2)]
+        self.copy_stream = torch.cuda.Stream(device)
+        self.ready = [torch.cuda.Event() for _ in range(2)]
+        self.free = [torch.cuda.Event() for _ in range(2)]
+        self.freed = [True, True]        # no release owed before the first copy
+        self.layer_in = [None, None]     # layer held (or being copied) by each slot
+        self.bytes_per_layer = 2 * int(torch.Size(shape).numel()) * 2
+
+    def __len__(self) -> int:
+        return len(self.host)
+
+    def capture(self, layer: int, k: torch.Tensor, v: torch.Tensor, start_pos: int = 0,
+                stream=None) -> None:
+        self.host[layer].capture(k, v, start_pos, stream)
+        for s in range(2):              # a slot holding this layer is now stale
+            if self.layer_in[s] == layer:
+                self.layer_in[s] = None
+
+    def _slot(self, layer: int) -> int:
+        for s in range(2):
+            if self.layer_in[s] == layer:
+                return s
+        return layer % 2
+
+    def prefetch(self, layer: int) -> None:
+        s = self._slot(layer)
+        if self.layer_in[s] == layer:
+            return
+        cs = self.copy_stream
+        # the capture that wrote the host pages, and the slot's last reader, come first
+        cs.wait_stream(torch.cuda.current_stream(self.device))
+        if not self.freed[s]:
+            cs.wait_event(self.free[s])
+        with torch.cuda.stream(cs):
+            self.slots[s].k_pool.copy_(self.host[layer].k_pool, non_blocking=True)
+            self.slots[s].v_pool.copy_(self.host[layer].v_pool, non_blocking=True)
+            self.ready[s].record(cs)
+        self.layer_in[s] = layer
+        self.freed[s] = False
+
+    def cache(self, layer: int) -> api.PagedKVCache:
+        self.prefetch(layer)
+        s = self._slot(layer)
+        torch.cuda.current_stream(self.device).wait_event(self.ready[s])
+        return self.slots[s]
+
+    def release(self, layer: int) -> None:
+        s = self._slot(layer)
+        if self.layer_in[s] == layer:
+            self.free[s].record(torch.cuda.current_stream(self.device))
+            self.freed[s] = True

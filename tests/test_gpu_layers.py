@@ -72,3 +72,55 @@ def test_three_layers_reverse_replay(cuda):
     assert g.touches == 2
     assert rel_err(g.dk.cpu().numpy(), dk1 + dk2) <= TOL_GRAD
     assert rel_err(g.dv.cpu().numpy(), dv1 + dv2) <= TOL_GRAD
+
+
+def test_streamed_layers_match_resident_layers(cuda):
+    """Three layers' prompt pages captured into pinned host memory and streamed through
+    the two-slot GPU page cache one layer ahead: forward (layers in order) and backward
+    (last layer first) bit-identical to the same layers held in GPU memory, one layer
+    against the oracle."""
+    P, R, hq, hkv, ps, splits, nl = 3000, 200, 8, 2, 64, 5, 3
+    scale = 128 ** -0.5
+    pr0 = syn.make_prompt(P, hkv, 128, ps, 700, cuda, extra_pages=2, sharp=True)
+    res = L.LayeredKVCache(nl, pr0.num_pages, pr0.page_table, ps, hkv, P, device=cuda)
+    st = L.StreamedLayers(nl, pr0.num_pages, pr0.page_table, ps, hkv, P, device=cuda)
+    brs = []
+    for l in range(nl):
+        pr = syn.make_prompt(P, hkv, 128, ps, 700 + 3 * l, cuda, sharp=True)
+        res.capture(l, pr.k[:P].contiguous(), pr.v[:P].contiguous())
+        st.capture(l, pr.k[:P].contiguous(), pr.v[:P].contiguous())
+        brs.append(syn.make_branch(R, hq, hkv, 128, 720 + l, cuda, sharp=True))
+    outs_r, outs_s = [], []
+    st.prefetch(0)
+    for l in range(nl):
+        c = st.cache(l)
+        if l + 1 < nl:
+            st.prefetch(l + 1)
+        br = brs[l]
+        outs_s.append(api.replay_fwd(c, br.q, br.k, br.v, scale, splits))
+        st.release(l)
+        outs_r.append(api.replay_fwd(res[l], br.q, br.k, br.v, scale, splits))
+    st.prefetch(nl - 1)
+    for l in reversed(range(nl)):
+        c = st.cache(l)
+        if l > 0:
+            st.prefetch(l - 1)
+        br = brs[l]
+        o, lse = outs_s[l]
+        g_s = api.replay_bwd(c, br.q, br.k, br.v, o, lse, br.d_o, scale, splits)
+        st.release(l)
+        g_r = api.replay_bwd(res[l], br.q, br.k, br.v, o, lse, br.d_o, scale, splits)
+        torch.cuda.synchronize()
+        for a, b in zip(g_s, g_r):
+            assert torch.equal(a, b), l
+    torch.cuda.synchronize()
+    assert B.ls_last_device_error(0) == B.LS_OK
+    for (o_s, l_s), (o_r, l_r) in zip(outs_s, outs_r):
+        assert torch.equal(o_s, o_r) and torch.equal(l_s, l_r)
+    assert not st.host[1].k_pool.is_cuda and st.host[1].k_pool.is_pinned()
+    pt = pr0.page_table.cpu().numpy()
+    pb = oracle.AttnProblem(u16(st.host[1].k_pool), u16(st.host[1].v_pool), pt, P,
+                            u16(brs[1].q), u16(brs[1].k), u16(brs[1].v), scale, splits)
+    o_ref, lse_ref = oracle.attn_fwd(pb)
+    assert rel_err(outs_s[1][0].float().cpu().numpy(), o_ref) <= TOL_O
+    assert float(np.abs(outs_s[1][1].cpu().numpy() - lse_ref).max()) <= TOL_LSE
