@@ -15,14 +15,15 @@
 //               only by dP, early in a tile, so one stage refills in time; K lives from
 //               S(j) to dQ(j) and its load lead decides whether S waits (measured: 4 K /
 //               1 V stages 1% faster than 3 / 2, 2 / 3 30% slower).
-//   warp 1      MMA issuer (one thread): S = Q K^T (SS), dP = dO V^T (SS, into one of two
+//   warp 1      MMA issuer (one thread; with warp 2 for token-block-major launches, see
+//               issue_two): S = Q K^T (SS), dP = dO V^T (SS, into one of two
 //               dP buffers), dQ += dS K (TS: dS from tensor memory, K as an MN-major
 //               operand).  Per tile j: dP(j+1) once V(j+1) has landed; S(j+1) once the
 //               dS warps hold S(j) and dP(j) in registers (both run while dS(j) is
 //               computed); dQ(j) once dS(j) is in tensor memory.  Every wait sits behind
 //               a group that is still running.  A K tile lives from S(j) to dQ(j), so the
 //               4-stage ring gives each K load about three tiles of lead.
-//   warps 2-3   idle (complete warpgroup 0)
+//   warps 2-3   idle (complete warpgroup 0; warp 2 issues S in token-block-major launches)
 //   warps 4-7 / 8-11  two warpgroups split the 128 key columns of each query row (64
 //               each): p = exp2(s scale log2e - lse log2e), ds = p (dp - D), packed as
 //               bf16 pairs over their own dP columns; at the end of a unit they read dQ,
@@ -91,6 +92,118 @@ using DqCursor = TileCursor<kUnitRows, kTile, kSeg ? 3 : 0, kTb, kPk>;
 
 __device__ __forceinline__ uint32_t bar_addr(uint32_t base, int i) { return base + kOffBar + 8 * i; }
 
+// The MMA issue of token-block-major launches on two threads (lane 0 of warps 1 and 2):
+//   warp 2  S(j) = Q K^T, once the dS warps hold S(j-1) in registers;
+//   warp 1  dP(j+1) = dO V^T, then dQ(j) += dS(j) K once dS(j) is in tensor memory.
+// The threads' MMAs use disjoint tensor memory (S vs the dP buffers and dQ), so the only
+// order between them is the one the dS warps' barriers give.  The unit's Q / dO are free
+// once both its last S and its last dP are done (two arrivals), and both threads commit
+// to B_DONE before tensor memory is released.
+template <bool kSeg, bool kPk, typename Fail>
+__device__ __forceinline__ void issue_two(int warp, uint32_t sbase, uint32_t tmem,
+                                          const LsSched& sc, const LsAttnArgs& a, Fail fail) {
+  const uint32_t idQK = idesc_bf16_f32(kTile, kTile, false);
+  const uint32_t idDQ = idesc_bf16_f32(kTile, kD, true);
+  DqCursor<kSeg, true, kPk> cursor(sc, blockIdx.x, a.R, a.g, a.pack);
+  uint32_t qunits = 0;
+  auto wait_q = [&]() -> bool {
+    const bool w = mbar_wait(bar_addr(sbase, B_Q_FULL), qunits & 1);
+    ++qunits;
+    return w;
+  };
+  if (warp == 2) {
+    const uint32_t dq_base = sdesc_lo(sbase + kOffQ, 16);
+    const uint32_t dk_base = sdesc_lo(sbase + kOffK, 16);
+    RingPos<kKStages> ks;
+    bool f = false, l = false;
+    uint32_t j = 0;
+    while (cursor.next_flags(&f, &l)) {
+      if (f && !wait_q()) { fail(); break; }
+      if (!mbar_wait(bar_addr(sbase, B_K_FULL + ks.stage), ks.phase)) { fail(); break; }
+      // S has one buffer: S(j) overwrites S(j-1) once the dS warps hold it
+      if (j > 0 && !mbar_wait(bar_addr(sbase, B_SDP_FREE), (j - 1) & 1)) { fail(); break; }
+      tc_fence_after();
+      const uint32_t b0 = dk_base + ((ks.stage * kTileBytes) >> 4);
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        const uint32_t off = ((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4;
+        mma_ss_lo(tmem + kColS, dq_base + off, b0 + off, idQK, kk > 0);
+      }
+      mma_commit(bar_addr(sbase, B_S_FULL));
+      if (l) mma_commit(bar_addr(sbase, B_Q_EMPTY));  // the unit's Q is free
+      ks.advance();
+      ++j;
+    }
+  } else {
+    const uint32_t ddo_base = sdesc_lo(sbase + kOffDO, 16);
+    const uint32_t dv_base = sdesc_lo(sbase + kOffV, 16);
+    const uint32_t dkm_base = sdesc_lo(sbase + kOffK, kHalfBytes);
+    bool f0 = false, l0 = false, f1 = false, l1 = false;
+    bool have0 = cursor.next_flags(&f0, &l0);
+    bool have1 = have0 && cursor.next_flags(&f1, &l1);
+    RingPos<kKStages> kq;
+    RingPos<kVStages> vs;
+    uint32_t j = 0;
+    bool ok = true;
+    // dP into buffer db from V stage st; the unit's dO is free after its last dP
+    auto mma_dp = [&](uint32_t st, uint32_t db, bool last_of_unit) {
+      const uint32_t b0 = dv_base + ((st * kTileBytes) >> 4);
+      const uint32_t d = tmem + kColDp + db * kTile;
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        const uint32_t off = ((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4;
+        mma_ss_lo(d, ddo_base + off, b0 + off, idQK, kk > 0);
+      }
+      mma_commit(bar_addr(sbase, B_DP_FULL + db));
+      mma_commit(bar_addr(sbase, B_V_EMPTY + st));
+      if (last_of_unit) mma_commit(bar_addr(sbase, B_Q_EMPTY));
+    };
+    if (have0) {
+      ok = wait_q() && mbar_wait(bar_addr(sbase, B_V_FULL + vs.stage), vs.phase);
+      if (ok) {
+        tc_fence_after();
+        mma_dp(vs.stage, 0, l0);
+        vs.advance();
+      } else {
+        fail();
+      }
+    }
+    while (ok && have0) {
+      // dP(j+1) needs V(j+1) (its buffer's previous dS(j-1) went to dQ(j-1), issued before
+      // it by this thread); dQ(j) needs dS(j) (K(j) landed before S(j) ran)
+      if (have1) {
+        if (f1 && !wait_q()) { fail(); break; }
+        if (!mbar_wait(bar_addr(sbase, B_V_FULL + vs.stage), vs.phase)) { fail(); break; }
+        tc_fence_after();
+        mma_dp(vs.stage, (j + 1) & 1, l1);
+        vs.advance();
+      }
+      if (!mbar_wait(bar_addr(sbase, B_DS_FULL + (j & 1)), (j >> 1) & 1)) { fail(); break; }
+      if (!mbar_wait(bar_addr(sbase, B_K_FULL + kq.stage), kq.phase)) { fail(); break; }
+      tc_fence_after();
+      const uint32_t bq = dkm_base + ((kq.stage * kTileBytes) >> 4);
+      const uint32_t aq = tmem + kColDp + (j & 1) * kTile;  // dS(j)
+      mma_ts_lo(tmem + kColDq, aq, bq, idDQ, f0 ? 0u : 1u);
+#pragma unroll
+      for (int kk = 1; kk < 8; ++kk) {
+        const uint32_t acol = kk < 4 ? kk * 8 : 64 + (kk - 4) * 8;
+        mma_ts_lo(tmem + kColDq, aq + acol, bq + ((kk * 2048) >> 4), idDQ, 1u);
+      }
+      mma_commit(bar_addr(sbase, B_K_EMPTY + kq.stage));
+      if (l0) mma_commit(bar_addr(sbase, B_DQ_DONE));
+      kq.advance();
+      f0 = f1;
+      l0 = l1;
+      have0 = have1;
+      have1 = have1 && cursor.next_flags(&f1, &l1);
+      ++j;
+    }
+  }
+  // every MMA this thread issued has finished before tensor memory is released
+  mma_commit(bar_addr(sbase, B_DONE));
+  mbar_wait(bar_addr(sbase, B_DONE), 0);
+}
+
 template <bool kSeg, bool kTb, bool kPk>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_dq_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a,
@@ -113,7 +226,7 @@ bwd_dq_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a,
       mbar_init(bar_addr(sbase, B_V_EMPTY + i), 1);
     }
     mbar_init(bar_addr(sbase, B_Q_FULL), 1);
-    mbar_init(bar_addr(sbase, B_Q_EMPTY), 1);
+    mbar_init(bar_addr(sbase, B_Q_EMPTY), kTb ? 2 : 1);  // the unit's last S (and last dP)
     mbar_init(bar_addr(sbase, B_S_FULL), 1);
     mbar_init(bar_addr(sbase, B_DP_FULL + 0), 1);
     mbar_init(bar_addr(sbase, B_DP_FULL + 1), 1);
@@ -121,7 +234,7 @@ bwd_dq_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a,
     mbar_init(bar_addr(sbase, B_DS_FULL + 0), 256);
     mbar_init(bar_addr(sbase, B_DS_FULL + 1), 256);
     mbar_init(bar_addr(sbase, B_DQ_DONE), 1);
-    mbar_init(bar_addr(sbase, B_DONE), 1);
+    mbar_init(bar_addr(sbase, B_DONE), kTb ? 2 : 1);     // one commit per MMA issuer
     mbar_init(bar_addr(sbase, B_AUX), 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -238,116 +351,126 @@ bwd_dq_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a,
         mbar_wait(bar_addr(sbase, B_V_FULL + i % kVStages), (i / kVStages) & 1);
       if (units > 0) mbar_wait(bar_addr(sbase, B_Q_FULL), (units - 1) & 1);
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    // One thread.  Issuing a tcgen05.mma holds the thread until the tensor core has
-    // nearly taken the instruction, so nothing but MMAs may sit between groups.  Per
-    // tile j: settle the loads of tile j+1, then as soon as the dS warps hold S(j) and
-    // dP(j) in registers issue S(j+1) and dP(j+1) (they run while dS(j) is computed),
-    // then once dS(j) is in tensor memory issue dQ(j).
-    if (lane == 0) {
-      const uint32_t idQK = idesc_bf16_f32(kTile, kTile, false);
-      const uint32_t idDQ = idesc_bf16_f32(kTile, kD, true);
-      const uint32_t dq_base = sdesc_lo(sbase + kOffQ, 16);
-      const uint32_t ddo_base = sdesc_lo(sbase + kOffDO, 16);
-      const uint32_t dk_base = sdesc_lo(sbase + kOffK, 16);
-      const uint32_t dv_base = sdesc_lo(sbase + kOffV, 16);
-      const uint32_t dkm_base = sdesc_lo(sbase + kOffK, kHalfBytes);
-      DqCursor<kSeg, kTb, kPk> cursor(sc, blockIdx.x, a.R, a.g, a.pack);
-      // first / last of unit of tiles j (f0, l0) and j+1 (f1, l1)
-      bool f0 = false, l0 = false, f1 = false, l1 = false;
-      bool have0 = cursor.next_flags(&f0, &l0);
-      bool have1 = have0 && cursor.next_flags(&f1, &l1);
-      RingPos<kKStages> ks, kq;  // K ring: next S, next dQ
-      RingPos<kVStages> vs;      // V ring: next dP
-      uint32_t qunits = 0, j = 0;
-      bool ok = true;
-      auto wait_q = [&]() -> bool {
-        const bool w = mbar_wait(bar_addr(sbase, B_Q_FULL), qunits & 1);
-        ++qunits;
-        return w;
-      };
-      // S = Q K^T from K stage st
-      auto mma_s = [&](uint32_t st, bool last_of_unit) {
-        const uint32_t b0 = dk_base + ((st * kTileBytes) >> 4);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t off = ((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4;
-          mma_ss_lo(tmem + kColS, dq_base + off, b0 + off, idQK, kk > 0);
+  } else if (warp == 1 || (kTb && warp == 2)) {
+    // ------------------------------------------------------------ MMA issuers
+    // Issuing a tcgen05.mma holds the thread until the tensor core has nearly taken the
+    // instruction (it runs about one MMA ahead of its issuer), so nothing but MMAs may sit
+    // between groups of one issuing thread.
+    //  * Token-block-major launches (short prompts, long causal items): two threads issue,
+    //    warp 2 the S groups and warp 1 dP and dQ, so each one's waits and commits are
+    //    covered by the other's MMAs (P = 0, R = 8,192: 1.27 -> 1.17 ms).
+    //  * Otherwise one thread, per tile j: settle the loads of tile j+1, then as soon as
+    //    the dS warps hold S(j) and dP(j) in registers issue S(j+1) and dP(j+1) (they run
+    //    while dS(j) is computed), then once dS(j) is in tensor memory issue dQ(j).  Two
+    //    threads measured 8% slower here: S then interleaves with dQ and delays the
+    //    chain S -> dS -> dQ.
+    if constexpr (kTb) {
+      if (lane == 0) issue_two<kSeg, kPk>(warp, sbase, tmem, sc, a, [&]() { fail(); });
+    } else {
+      if (lane == 0) {
+        const uint32_t idQK = idesc_bf16_f32(kTile, kTile, false);
+        const uint32_t idDQ = idesc_bf16_f32(kTile, kD, true);
+        const uint32_t dq_base = sdesc_lo(sbase + kOffQ, 16);
+        const uint32_t ddo_base = sdesc_lo(sbase + kOffDO, 16);
+        const uint32_t dk_base = sdesc_lo(sbase + kOffK, 16);
+        const uint32_t dv_base = sdesc_lo(sbase + kOffV, 16);
+        const uint32_t dkm_base = sdesc_lo(sbase + kOffK, kHalfBytes);
+        DqCursor<kSeg, kTb, kPk> cursor(sc, blockIdx.x, a.R, a.g, a.pack);
+        // first / last of unit of tiles j (f0, l0) and j+1 (f1, l1)
+        bool f0 = false, l0 = false, f1 = false, l1 = false;
+        bool have0 = cursor.next_flags(&f0, &l0);
+        bool have1 = have0 && cursor.next_flags(&f1, &l1);
+        RingPos<kKStages> ks, kq;  // K ring: next S, next dQ
+        RingPos<kVStages> vs;      // V ring: next dP
+        uint32_t qunits = 0, j = 0;
+        bool ok = true;
+        auto wait_q = [&]() -> bool {
+          const bool w = mbar_wait(bar_addr(sbase, B_Q_FULL), qunits & 1);
+          ++qunits;
+          return w;
+        };
+        // S = Q K^T from K stage st
+        auto mma_s = [&](uint32_t st, bool last_of_unit) {
+          const uint32_t b0 = dk_base + ((st * kTileBytes) >> 4);
+  #pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t off = ((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4;
+            mma_ss_lo(tmem + kColS, dq_base + off, b0 + off, idQK, kk > 0);
+          }
+          mma_commit(bar_addr(sbase, B_S_FULL));
+          // the unit's Q and dO are free once its last S (issued after its last dP) is done
+          if (last_of_unit) mma_commit(bar_addr(sbase, B_Q_EMPTY));
+        };
+        // dP = dO V^T into dP buffer db from V stage st
+        auto mma_dp = [&](uint32_t st, uint32_t db) {
+          const uint32_t b0 = dv_base + ((st * kTileBytes) >> 4);
+          const uint32_t d = tmem + kColDp + db * kTile;
+  #pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t off = ((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4;
+            mma_ss_lo(d, ddo_base + off, b0 + off, idQK, kk > 0);
+          }
+          mma_commit(bar_addr(sbase, B_DP_FULL + db));
+          mma_commit(bar_addr(sbase, B_V_EMPTY + st));
+        };
+        // prologue: S(0), dP(0)
+        if (have0) {
+          ok = wait_q() && mbar_wait(bar_addr(sbase, B_K_FULL + ks.stage), ks.phase) &&
+               mbar_wait(bar_addr(sbase, B_V_FULL + vs.stage), vs.phase);
+          if (ok) {
+            tc_fence_after();
+            mma_dp(vs.stage, 0);
+            mma_s(ks.stage, l0);
+            ks.advance();
+            vs.advance();
+          } else {
+            fail();
+          }
         }
-        mma_commit(bar_addr(sbase, B_S_FULL));
-        // the unit's Q and dO are free once its last S (issued after its last dP) is done
-        if (last_of_unit) mma_commit(bar_addr(sbase, B_Q_EMPTY));
-      };
-      // dP = dO V^T into dP buffer db from V stage st
-      auto mma_dp = [&](uint32_t st, uint32_t db) {
-        const uint32_t b0 = dv_base + ((st * kTileBytes) >> 4);
-        const uint32_t d = tmem + kColDp + db * kTile;
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t off = ((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4;
-          mma_ss_lo(d, ddo_base + off, b0 + off, idQK, kk > 0);
-        }
-        mma_commit(bar_addr(sbase, B_DP_FULL + db));
-        mma_commit(bar_addr(sbase, B_V_EMPTY + st));
-      };
-      // prologue: S(0), dP(0)
-      if (have0) {
-        ok = wait_q() && mbar_wait(bar_addr(sbase, B_K_FULL + ks.stage), ks.phase) &&
-             mbar_wait(bar_addr(sbase, B_V_FULL + vs.stage), vs.phase);
-        if (ok) {
+        while (ok && have0) {
+          // Groups of tile j+1 and j, each wait placed so that the group before it is
+          // still running on the tensor core:
+          //   dP(j+1) needs V(j+1) (its buffer's previous dS(j-1) went to dQ(j-1), issued
+          //     earlier by this thread); a new unit's dO also needs that unit's Q/dO load,
+          //     which follows the old unit's last S;
+          //   S(j+1) needs K(j+1) and the dS warps to hold S(j) in registers;
+          //   dQ(j) needs dS(j).
+          const uint32_t bq = dkm_base + ((kq.stage * kTileBytes) >> 4);
+          const uint32_t aq = tmem + kColDp + (j & 1) * kTile;  // dS(j)
+          if (have1) {
+            if (f1 && !wait_q()) { fail(); break; }
+            if (!mbar_wait(bar_addr(sbase, B_V_FULL + vs.stage), vs.phase)) { fail(); break; }
+            tc_fence_after();
+            mma_dp(vs.stage, (j + 1) & 1);
+            vs.advance();
+            if (!mbar_wait(bar_addr(sbase, B_K_FULL + ks.stage), ks.phase)) { fail(); break; }
+          }
+          if (!mbar_wait(bar_addr(sbase, B_SDP_FREE), j & 1)) { fail(); break; }
           tc_fence_after();
-          mma_dp(vs.stage, 0);
-          mma_s(ks.stage, l0);
-          ks.advance();
-          vs.advance();
-        } else {
-          fail();
-        }
-      }
-      while (ok && have0) {
-        // Groups of tile j+1 and j, each wait placed so that the group before it is
-        // still running on the tensor core:
-        //   dP(j+1) needs V(j+1) (its buffer's previous dS(j-1) went to dQ(j-1), issued
-        //     earlier by this thread); a new unit's dO also needs that unit's Q/dO load,
-        //     which follows the old unit's last S;
-        //   S(j+1) needs K(j+1) and the dS warps to hold S(j) in registers;
-        //   dQ(j) needs dS(j).
-        const uint32_t bq = dkm_base + ((kq.stage * kTileBytes) >> 4);
-        const uint32_t aq = tmem + kColDp + (j & 1) * kTile;  // dS(j)
-        if (have1) {
-          if (f1 && !wait_q()) { fail(); break; }
-          if (!mbar_wait(bar_addr(sbase, B_V_FULL + vs.stage), vs.phase)) { fail(); break; }
+          if (have1) {
+            mma_s(ks.stage, l1);
+            ks.advance();
+          }
+          if (!mbar_wait(bar_addr(sbase, B_DS_FULL + (j & 1)), (j >> 1) & 1)) { fail(); break; }
           tc_fence_after();
-          mma_dp(vs.stage, (j + 1) & 1);
-          vs.advance();
-          if (!mbar_wait(bar_addr(sbase, B_K_FULL + ks.stage), ks.phase)) { fail(); break; }
+          mma_ts_lo(tmem + kColDq, aq, bq, idDQ, f0 ? 0u : 1u);
+  #pragma unroll
+          for (int kk = 1; kk < 8; ++kk) {
+            const uint32_t acol = kk < 4 ? kk * 8 : 64 + (kk - 4) * 8;
+            mma_ts_lo(tmem + kColDq, aq + acol, bq + ((kk * 2048) >> 4), idDQ, 1u);
+          }
+          mma_commit(bar_addr(sbase, B_K_EMPTY + kq.stage));
+          if (l0) mma_commit(bar_addr(sbase, B_DQ_DONE));
+          kq.advance();
+          f0 = f1;
+          l0 = l1;
+          have0 = have1;
+          have1 = have1 && cursor.next_flags(&f1, &l1);
+          ++j;
         }
-        if (!mbar_wait(bar_addr(sbase, B_SDP_FREE), j & 1)) { fail(); break; }
-        tc_fence_after();
-        if (have1) {
-          mma_s(ks.stage, l1);
-          ks.advance();
-        }
-        if (!mbar_wait(bar_addr(sbase, B_DS_FULL + (j & 1)), (j >> 1) & 1)) { fail(); break; }
-        tc_fence_after();
-        mma_ts_lo(tmem + kColDq, aq, bq, idDQ, f0 ? 0u : 1u);
-#pragma unroll
-        for (int kk = 1; kk < 8; ++kk) {
-          const uint32_t acol = kk < 4 ? kk * 8 : 64 + (kk - 4) * 8;
-          mma_ts_lo(tmem + kColDq, aq + acol, bq + ((kk * 2048) >> 4), idDQ, 1u);
-        }
-        mma_commit(bar_addr(sbase, B_K_EMPTY + kq.stage));
-        if (l0) mma_commit(bar_addr(sbase, B_DQ_DONE));
-        kq.advance();
-        f0 = f1;
-        l0 = l1;
-        have0 = have1;
-        have1 = have1 && cursor.next_flags(&f1, &l1);
-        ++j;
+        mma_commit(bar_addr(sbase, B_DONE));
+        mbar_wait(bar_addr(sbase, B_DONE), 0);
       }
-      mma_commit(bar_addr(sbase, B_DONE));
-      mbar_wait(bar_addr(sbase, B_DONE), 0);
     }
   }
   } else {
