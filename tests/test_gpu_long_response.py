@@ -6,7 +6,8 @@ Two checks cover it:
   * the fp64 oracle on every key of a 2,048-token response over a 2,048-position prompt
     with sharp inputs (scores of unit spread);
   * the all-zero-key closed forms (tests/closed_forms.py, pinned against the oracle) at
-    R = 4,096 and 8,192 with and without a prompt, where the oracle would need hours:
+    R = 4,096 and 8,192 with and without a prompt, and R = 4,096 over the full
+    2,097,152-position prompt, where the oracle would need hours:
     keys 0, 1, R/2 and R - 1 of every KV head, plus O and LSE of every row.
 """
 import numpy as np
@@ -40,7 +41,8 @@ def test_whole_response_every_key_sharp(cuda):
         assert rel_err(x[:4].cpu().numpy(), ref[:4]) <= TOL_GRAD
 
 
-@pytest.mark.parametrize("P,R", [(0, 4096), (4096, 4096), (0, 8192), (4096, 8192)])
+@pytest.mark.parametrize("P,R", [(0, 4096), (4096, 4096), (0, 8192), (4096, 8192),
+                                 (2097152, 4096)])
 def test_long_response_first_keys_closed_form(cuda, P, R):
     hq, hkv, ps, splits, d = 24, 4, 256, 4, 128
     scale = d ** -0.5
@@ -57,7 +59,7 @@ def test_long_response_first_keys_closed_form(cuda, P, R):
     dq, dk, dv = api.replay_bwd(cache, br.q, k0, br.v, o, lse, br.d_o, scale, splits)
     torch.cuda.synchronize()
     assert B.ls_last_device_error(0) == B.LS_OK
-    vp = pr.v.double().sum(0).cpu().numpy() if P > 0 else np.zeros((hkv, d))
+    vp = pr.v[:P].sum(0, dtype=torch.float64).cpu().numpy() if P > 0 else np.zeros((hkv, d))
     vr = br.v.double().cpu().numpy()
     lse_ref, o_ref = uniform_attention(P, vp, vr)
     g = hq // hkv
