@@ -60,11 +60,13 @@ def lib():
         l.lso_grpo_logp.argtypes = [P, i32, i64, i32, P, P, P, P, P]
         l.lso_gdn_fwd.argtypes = [P, P, P]
         l.lso_gdn_bwd.argtypes = [P, P, i32, P, P, P, P, P, P]
+        l.lso_mla_fwd.argtypes = [P, P, P]
+        l.lso_mla_fwd_rows.argtypes = [P, i32, P, P, P, P]
         l.lso_num_threads.argtypes = []
         for f in ("lso_capture_kv", "lso_attn_fwd", "lso_attn_fwd_rows", "lso_attn_bwd",
                   "lso_attn_bwd_dq_rows", "lso_attn_bwd_dkdv_keys", "lso_grpo",
                   "lso_grpo_dlogits_row", "lso_grpo_logp", "lso_gdn_fwd", "lso_gdn_bwd",
-                  "lso_num_threads"):
+                  "lso_mla_fwd", "lso_mla_fwd_rows", "lso_num_threads"):
             getattr(l, f).restype = C.c_int
         _lib = l
     return _lib
@@ -374,3 +376,68 @@ def gdn_bwd(pb: GdnProblem, d_o: np.ndarray):
     _check(lib().lso_gdn_bwd(C.byref(st), _ptr(d_o), _dtype_code(d_o), _ptr(dq), _ptr(dkk),
                              _ptr(dvv), _ptr(dg), _ptr(db), _ptr(ds0)), "gdn_bwd")
     return dq, dkk, dvv, dg, db, ds0
+
+
+class _Mla(C.Structure):
+    _fields_ = [
+        ("lat_pool", C.c_void_p), ("page_size", C.c_int32), ("page_table", C.c_void_p),
+        ("num_pages", C.c_int64), ("num_logical_pages", C.c_int64), ("P", C.c_int64),
+        ("q", C.c_void_p), ("lat_resp", C.c_void_p), ("R", C.c_int32), ("H", C.c_int32),
+        ("d_c", C.c_int32), ("d_r", C.c_int32), ("scale", C.c_double),
+    ]
+
+
+@dataclass
+class MlaProblem:
+    """One response branch over latent (MLA-style) pages (host arrays, bf16 as uint16).
+
+    lat_pool: [num_pages][page_size][d_c + d_r]; page_table: [num_logical_pages] int32;
+    q: [R][H][d_c + d_r]; lat_resp: [R][d_c + d_r]."""
+    lat_pool: np.ndarray
+    page_table: np.ndarray
+    P: int
+    q: np.ndarray
+    lat_resp: np.ndarray
+    scale: float
+    d_c: int = 512
+
+    def _struct(self):
+        keep = []
+
+        def c(a, dt):
+            a = np.ascontiguousarray(a, dtype=dt)
+            keep.append(a)
+            return a
+
+        lp, q, lr = c(self.lat_pool, np.uint16), c(self.q, np.uint16), c(self.lat_resp, np.uint16)
+        pt = c(self.page_table, np.int32)
+        num_pages, ps, D = lp.shape
+        R, H, D2 = q.shape
+        assert D2 == D and lr.shape == (R, D) and 0 < self.d_c <= D
+        st = _Mla(lat_pool=lp.ctypes.data, page_size=ps, page_table=pt.ctypes.data,
+                  num_pages=num_pages, num_logical_pages=pt.shape[0], P=self.P,
+                  q=q.ctypes.data, lat_resp=lr.ctypes.data, R=R, H=H, d_c=self.d_c,
+                  d_r=D - self.d_c, scale=float(self.scale))
+        return st, keep
+
+
+def mla_fwd(pb: MlaProblem):
+    """O [R][H][d_c] and LSE [R][H] (natural log), fp64."""
+    R, H, _ = pb.q.shape
+    st, keep = pb._struct()
+    o = np.zeros((R, H, pb.d_c), np.float64)
+    lse = np.zeros((R, H), np.float64)
+    _check(lib().lso_mla_fwd(C.byref(st), _ptr(o), _ptr(lse)), "mla_fwd")
+    return o, lse
+
+
+def mla_fwd_rows(pb: MlaProblem, ts, hs):
+    """O [n][d_c], LSE [n] for the rows (ts[i], hs[i])."""
+    ts = np.ascontiguousarray(ts, dtype=np.int32)
+    hs = np.ascontiguousarray(hs, dtype=np.int32)
+    st, keep = pb._struct()
+    o = np.zeros((len(ts), pb.d_c), np.float64)
+    lse = np.zeros((len(ts),), np.float64)
+    _check(lib().lso_mla_fwd_rows(C.byref(st), len(ts), _ptr(ts), _ptr(hs), _ptr(o),
+                                  _ptr(lse)), "mla_fwd_rows")
+    return o, lse

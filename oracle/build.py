@@ -11,7 +11,7 @@ import sys
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 SRC = os.path.join(HERE, "longstraw_oracle.c")
-SRCS = [SRC, os.path.join(HERE, "gdn_oracle.c")]
+SRCS = [SRC, os.path.join(HERE, "gdn_oracle.c"), os.path.join(HERE, "mla_oracle.c")]
 HDR = os.path.join(HERE, "longstraw_oracle.h")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "liblongstraw_oracle.so")

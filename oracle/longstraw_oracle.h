@@ -53,6 +53,12 @@
  *   lso_grpo_dlogits_row    central finite differences of the loss
  *   lso_grpo_logp           a library log-softmax and the closed-form lse; the KL
  *                           estimate's closed cases
+ *   lso_mla_fwd             brute-force softmax over the gathered rows on tiny inputs;
+ *                           q = 0 closed form (mean of the visible latents, lse =
+ *                           log(P + t + 1)); equals lso_attn_fwd with one KV head, K the
+ *                           whole row and V the row with its rotary part zeroed; one page
+ *                           with the identity table equals shuffled pages
+ *   lso_mla_fwd_rows        equals lso_mla_fwd on the sampled rows
  */
 #ifndef LONGSTRAW_ORACLE_H
 #define LONGSTRAW_ORACLE_H
@@ -181,6 +187,35 @@ int lso_gdn_bwd(const lso_gdn* a, const void* d_o, int32_t do_dtype, double* dq,
 
 /* Threads the OpenMP runtime will use (1 when built without OpenMP). */
 int lso_num_threads(void);
+
+/* Latent (MLA-style) pages plus one response branch (mla_oracle.c).
+ * lat_pool: bf16 [num_pages][page_size][d_c + d_r], each row a position's latent c
+ * (d_c values) then its rotary key (d_r values); page_table [num_logical_pages];
+ * P valid prompt positions; q: bf16 [R][H][d_c + d_r] absorbed queries; lat_resp:
+ * bf16 [R][d_c + d_r] the response's own rows.  All heads share every row. */
+typedef struct {
+  const uint16_t* lat_pool;
+  int32_t page_size;
+  const int32_t* page_table;
+  int64_t num_pages;
+  int64_t num_logical_pages;
+  int64_t P;
+  const uint16_t* q;
+  const uint16_t* lat_resp;
+  int32_t R;
+  int32_t H;
+  int32_t d_c;
+  int32_t d_r;
+  double scale;
+} lso_mla;
+
+/* o [R][H][d_c] = softmax over keys (P prompt rows, response rows j <= t) of
+ * scale <q, row> applied to the rows' first d_c values; lse [R][H] (natural log). */
+int lso_mla_fwd(const lso_mla* a, double* o, double* lse);
+
+/* The same for the listed (t, h) rows only: o [n][d_c], lse [n]. */
+int lso_mla_fwd_rows(const lso_mla* a, int32_t n, const int32_t* ts, const int32_t* hs,
+                     double* o, double* lse);
 
 #ifdef __cplusplus
 }

@@ -1,0 +1,125 @@
+"""Pins of the fp64 latent-attention (MLA-style) oracle against things other than itself:
+a brute-force softmax over the gathered rows, the q = 0 closed form, the attention
+oracle (itself pinned) in the equivalent one-KV-head problem, and page-table
+invariance.  A wrong page lookup, a dropped rotary term, the rotary part leaking into
+the output, a wrong causal bound or a wrong scale fails at least one."""
+import numpy as np
+import pytest
+
+import oracle
+
+
+def bf16_bits(x: np.ndarray) -> np.ndarray:
+    """Round-to-nearest-even bf16 bit patterns of x."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    return ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)
+
+
+def bf16_value(b: np.ndarray) -> np.ndarray:
+    return (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def latent_problem(P, R, H, d_c, d_r, ps, seed, extra_pages=2, scale=0.1, zero_q=False):
+    """Random latent pages (shuffled, stale rows NaN) and a branch; also the prompt rows
+    in logical order as fp64 for brute force."""
+    rng = np.random.default_rng(seed)
+    D = d_c + d_r
+    logical = (P + ps - 1) // ps
+    num_pages = logical + extra_pages
+    pt = rng.permutation(num_pages)[:logical].astype(np.int32)
+    pool = np.full((num_pages, ps, D), 0x7FC0, np.uint16)   # bf16 NaN in unused slots
+    rows = bf16_bits(rng.standard_normal((P, D)))
+    for p in range(P):
+        pool[pt[p // ps], p % ps] = rows[p]
+    q = bf16_bits(np.zeros((R, H, D)) if zero_q else rng.standard_normal((R, H, D)))
+    resp = bf16_bits(rng.standard_normal((R, D)))
+    pb = oracle.MlaProblem(pool, pt if P > 0 else np.zeros(1, np.int32), P, q, resp, scale,
+                           d_c=d_c)
+    return pb, bf16_value(rows)
+
+
+def brute_force(pb, rows):
+    """Textbook softmax over the full key matrix [prompt rows; response rows]."""
+    R, H, D = pb.q.shape
+    keys = np.concatenate([rows, bf16_value(pb.lat_resp)], 0)      # [P + R, D]
+    q = bf16_value(pb.q)
+    o = np.zeros((R, H, pb.d_c))
+    lse = np.zeros((R, H))
+    for t in range(R):
+        vis = keys[:pb.P + t + 1]
+        s = pb.scale * q[t] @ vis.T                                 # [H, P + t + 1]
+        m = s.max(1, keepdims=True)
+        w = np.exp(s - m)
+        lse[t] = m[:, 0] + np.log(w.sum(1))
+        o[t] = (w / w.sum(1, keepdims=True)) @ vis[:, :pb.d_c]
+    return o, lse
+
+
+@pytest.mark.parametrize("P,R,H,d_c,d_r,ps", [
+    (37, 5, 3, 16, 8, 8), (0, 6, 2, 12, 4, 4), (64, 1, 4, 8, 0, 16), (100, 9, 2, 20, 6, 32),
+])
+def test_matches_brute_force(P, R, H, d_c, d_r, ps):
+    pb, rows = latent_problem(P, R, H, d_c, d_r, ps, seed=P + 10 * R + H)
+    o, lse = oracle.mla_fwd(pb)
+    o_bf, lse_bf = brute_force(pb, rows)
+    np.testing.assert_allclose(o, o_bf, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, lse_bf, rtol=0, atol=1e-12)
+
+
+def test_zero_query_is_mean_of_visible_latents():
+    P, R, H, d_c, d_r = 50, 7, 3, 10, 6
+    pb, rows = latent_problem(P, R, H, d_c, d_r, 16, seed=3, zero_q=True)
+    o, lse = oracle.mla_fwd(pb)
+    lat = np.concatenate([rows, bf16_value(pb.lat_resp)], 0)[:, :d_c]
+    for t in range(R):
+        np.testing.assert_allclose(o[t], np.broadcast_to(lat[:P + t + 1].mean(0), (H, d_c)),
+                                   rtol=0, atol=1e-12)
+        np.testing.assert_allclose(lse[t], np.log(P + t + 1.0), rtol=0, atol=1e-12)
+
+
+def test_equals_one_kv_head_attention():
+    """Latent attention is attention with one KV head whose key is the whole row and whose
+    value is the row with its rotary part zeroed (output columns past d_c are then 0)."""
+    P, R, H, d_c, d_r, ps = 70, 6, 4, 12, 4, 16
+    pb, rows = latent_problem(P, R, H, d_c, d_r, ps, seed=11)
+    o, lse = oracle.mla_fwd(pb)
+    kp = bf16_value(pb.lat_pool)[:, None]                        # [pages][1][ps][D]
+    vp = kp.copy()
+    vp[..., d_c:] = 0.0
+    kr = bf16_value(pb.lat_resp)[:, None]
+    vr = kr.copy()
+    vr[..., d_c:] = 0.0
+    ap = oracle.AttnProblem(np.nan_to_num(kp), np.nan_to_num(vp), pb.page_table, P,
+                            bf16_value(pb.q), kr, vr, pb.scale, 3)
+    o_a, lse_a = oracle.attn_fwd(ap)
+    np.testing.assert_allclose(o, o_a[..., :d_c], rtol=0, atol=1e-12)
+    assert np.abs(o_a[..., d_c:]).max() == 0.0
+    np.testing.assert_allclose(lse, lse_a, rtol=0, atol=1e-12)
+
+
+def test_page_table_invariance():
+    """The same prompt rows on one identity-mapped page give the same result."""
+    P, R, H, d_c, d_r, ps = 45, 4, 2, 8, 8, 8
+    pb, rows = latent_problem(P, R, H, d_c, d_r, ps, seed=21)
+    one = np.zeros((1, P, d_c + d_r), np.uint16)
+    one[0] = bf16_bits(rows)
+    pb1 = oracle.MlaProblem(one, np.zeros(1, np.int32), P, pb.q, pb.lat_resp, pb.scale, d_c=d_c)
+    o, lse = oracle.mla_fwd(pb)
+    o1, lse1 = oracle.mla_fwd(pb1)
+    np.testing.assert_array_equal(o, o1)
+    np.testing.assert_array_equal(lse, lse1)
+
+
+def test_rows_sampler_and_bad_page():
+    P, R, H, d_c, d_r, ps = 33, 5, 3, 8, 4, 8
+    pb, rows = latent_problem(P, R, H, d_c, d_r, ps, seed=5)
+    o, lse = oracle.mla_fwd(pb)
+    ts, hs = np.array([0, 4, 2, 4]), np.array([2, 0, 1, 2])
+    o_r, lse_r = oracle.mla_fwd_rows(pb, ts, hs)
+    np.testing.assert_array_equal(o_r, o[ts, hs])
+    np.testing.assert_array_equal(lse_r, lse[ts, hs])
+    bad = pb.page_table.copy()
+    bad[1] = pb.lat_pool.shape[0]
+    with pytest.raises(ValueError):
+        oracle.mla_fwd(oracle.MlaProblem(pb.lat_pool, bad, P, pb.q, pb.lat_resp, pb.scale,
+                                         d_c=d_c))
