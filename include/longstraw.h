@@ -17,6 +17,8 @@
  *                          response's own keys only (the prompt state is stopgrad)
  *   ls_grpo_loss_fwd_bwd   token-level clipped surrogate with group-relative
  *                          advantages and its logits gradient
+ *   ls_mla_replay_fwd      the forward over latent (MLA-style) pages, which may be
+ *                          held in host memory
  *
  * Conventions shared by every call
  *   - Memory: every pointer argument is DEVICE memory on the current CUDA device unless
@@ -328,6 +330,58 @@ ls_status ls_gdn_replay_bwd(const float* state0, const void* q, const void* k, c
                             const float* g, const float* beta, const void* d_o, int R, int H,
                             float scale, int accumulate, float* dq, float* dk, float* dv, float* dg,
                             float* dbeta, void* workspace, size_t workspace_bytes,
+                            ls_stream_t stream);
+
+/* ---------------------------------------------------------------- latent (MLA) replay
+ * The GLM path keeps its multi-head latent attention state as latent pages held in CPU
+ * memory and replays each response over them (explainer, "Two incompatible
+ * architectures, same transaction", GLM bullet).  The pages give no equations for the
+ * layer; it is multi-head latent attention (DeepSeek-V2, 2024) with the key
+ * up-projection absorbed into the query.  Every position j keeps one row shared by all
+ * heads, its latent c_j (512 values) followed by its rotary key r_j (64 values); the
+ * caller passes each head's absorbed query (576 values), and
+ *   s_{t,h,j} = softmax_scale * <q_{t,h}, [c_j ; r_j]>,  j over all P prompt rows and
+ *               the response rows j <= t
+ *   lse_{t,h} = log sum_j exp(s_{t,h,j})        (natural log)
+ *   o_{t,h}   = sum_j exp(s_{t,h,j} - lse_{t,h}) c_j   (512 values)
+ * The value up-projection and the output projection are weights (the caller's).
+ *
+ * ls_latent_cache: the captured prompt rows of one latent-attention layer.
+ *   pool        bf16 [num_pages][page_size][576]; may be pinned host memory that the
+ *               GPU reads directly (on a Grace-Blackwell node, Grace memory behind
+ *               NVLink-C2C): capture writes it there and the replay reads it there.
+ *   page_table  int32 [num_logical_pages] in GPU memory: logical page -> physical page.
+ *   num_tokens  P <= num_logical_pages * page_size.
+ * Supported: page_size a power of two in [32, 4096]; num_pages * page_size < 2^31.
+ *
+ * ls_capture_latent: pool[pt[p / ps]][p % ps][:] = lat[p - start_pos][:] for p in
+ * [start_pos, start_pos + n); lat bf16 [n][576].  Bit copy; a page id outside the pool
+ * skips the row and sets LS_ERR_DEVICE_CHECK.
+ *
+ * ls_mla_replay_fwd: the forward of one response of R tokens with H heads.
+ * q: bf16 [R][H][576]; lat_resp: bf16 [R][576] (the response's own rows); o: bf16
+ * [R][H][512]; lse: fp32 [R][H].  num_splits (>= 1) cuts the prompt into that many
+ * ranges of 32-row tiles, merged by log-sum-exp; the result does not depend on it
+ * beyond rounding.  softmax_scale finite and > 0.  R == 0 is a no-op; P == 0 is causal
+ * attention over the response rows.  Inputs must be finite (a row past a query's
+ * causal bound has weight zero, and zero times a non-finite value is not zero).
+ * LS_ERR_UNSUPPORTED when R x H >= 2^31.  No backward is provided. */
+typedef struct {
+  void* pool;
+  const int32_t* page_table;
+  int32_t num_pages;
+  int32_t num_logical_pages;
+  int32_t page_size;
+  int64_t num_tokens;
+} ls_latent_cache;
+
+ls_status ls_capture_latent(const ls_latent_cache* cache, const void* lat, int64_t start_pos,
+                            int64_t n, ls_stream_t stream);
+ls_status ls_mla_replay_fwd_workspace(const ls_latent_cache* cache, int R, int H, int num_splits,
+                                      size_t* bytes);
+ls_status ls_mla_replay_fwd(const ls_latent_cache* cache, const void* q, const void* lat_resp,
+                            int R, int H, float softmax_scale, int num_splits, void* o,
+                            float* lse, void* workspace, size_t workspace_bytes,
                             ls_stream_t stream);
 
 /* ---------------------------------------------------------------- checks

@@ -29,6 +29,7 @@ EXPORTED = (
     "ls_gdn_replay_fwd_workspace", "ls_gdn_replay_fwd", "ls_gdn_replay_bwd_workspace",
     "ls_gdn_replay_bwd", "ls_replay_attn_fwd_ragged_workspace", "ls_replay_attn_fwd_ragged",
     "ls_replay_attn_bwd_ragged_workspace", "ls_replay_attn_bwd_ragged",
+    "ls_capture_latent", "ls_mla_replay_fwd_workspace", "ls_mla_replay_fwd",
 )
 
 
@@ -37,6 +38,13 @@ class ls_kv_cache(C.Structure):
         ("k_pool", C.c_void_p), ("v_pool", C.c_void_p), ("page_table", C.c_void_p),
         ("num_pages", C.c_int32), ("num_logical_pages", C.c_int32), ("page_size", C.c_int32),
         ("num_kv_heads", C.c_int32), ("head_dim", C.c_int32), ("num_tokens", C.c_int64),
+    ]
+
+
+class ls_latent_cache(C.Structure):
+    _fields_ = [
+        ("pool", C.c_void_p), ("page_table", C.c_void_p), ("num_pages", C.c_int32),
+        ("num_logical_pages", C.c_int32), ("page_size", C.c_int32), ("num_tokens", C.c_int64),
     ]
 
 
@@ -60,8 +68,12 @@ def lib() -> C.CDLL:
         l = C.CDLL(LIB_PATH)
         P, i32, i64, sz, f32 = C.c_void_p, C.c_int, C.c_int64, C.c_size_t, C.c_float
         cache = C.POINTER(ls_kv_cache)
+        lcache = C.POINTER(ls_latent_cache)
         szp = C.POINTER(C.c_size_t)
         sig = {
+            "ls_capture_latent": [lcache, P, i64, i64, P],
+            "ls_mla_replay_fwd_workspace": [lcache, i32, i32, i32, szp],
+            "ls_mla_replay_fwd": [lcache, P, P, i32, i32, f32, i32, P, P, P, sz, P],
             "ls_capture_kv": [cache, P, P, i64, i64, P],
             "ls_replay_attn_fwd_workspace": [cache, i32, i32, i32, szp],
             "ls_replay_attn_fwd": [cache, P, P, P, i32, i32, f32, i32, P, P, P, sz, P],
@@ -250,6 +262,23 @@ def ls_gdn_replay_bwd(state0: int, q: int, k: int, v: int, g: int, beta: int, d_
     _ok("ls_gdn_replay_bwd",
         lib().ls_gdn_replay_bwd(state0, q, k, v, g, beta, d_o, R, H, scale, accumulate, dq, dk,
                                 dv, dg, dbeta, workspace, workspace_bytes, stream))
+
+
+def ls_capture_latent(cache: ls_latent_cache, lat: int, start_pos: int, n: int,
+                      stream: int = 0) -> None:
+    _ok("ls_capture_latent", lib().ls_capture_latent(C.byref(cache), lat, start_pos, n, stream))
+
+
+def ls_mla_replay_fwd_workspace(cache: ls_latent_cache, R: int, H: int, num_splits: int) -> int:
+    return _size("ls_mla_replay_fwd_workspace", C.byref(cache), R, H, num_splits)
+
+
+def ls_mla_replay_fwd(cache: ls_latent_cache, q: int, lat_resp: int, R: int, H: int,
+                      softmax_scale: float, num_splits: int, o: int, lse: int, workspace: int,
+                      workspace_bytes: int, stream: int = 0) -> None:
+    _ok("ls_mla_replay_fwd",
+        lib().ls_mla_replay_fwd(C.byref(cache), q, lat_resp, R, H, softmax_scale, num_splits, o,
+                                lse, workspace, workspace_bytes, stream))
 
 
 def _lens(lens) -> tuple:

@@ -699,6 +699,109 @@ ls_status ls_gdn_replay_bwd(const float* state0, const void* q, const void* k, c
                                      (cudaStream_t)stream));
 }
 
+// ---- latent (MLA-style) replay
+
+}  // extern "C"
+
+namespace {
+
+ls_status check_latent(const ls_latent_cache* c) {
+  if (!c) return LS_ERR_INVALID_ARG;
+  const int l = ilog2_exact(c->page_size);
+  if (l < 5 || l > 12) return LS_ERR_UNSUPPORTED;
+  if (c->num_pages <= 0 || c->num_logical_pages < 0 || c->num_tokens < 0) return LS_ERR_INVALID_ARG;
+  if ((int64_t)c->num_pages * c->page_size >= (1ll << 31)) return LS_ERR_UNSUPPORTED;
+  if (c->num_tokens > (int64_t)c->num_logical_pages * c->page_size) return LS_ERR_INVALID_ARG;
+  if (!c->pool || !aligned16(c->pool)) return LS_ERR_INVALID_ARG;
+  if (c->num_logical_pages > 0 && !c->page_table) return LS_ERR_INVALID_ARG;
+  return LS_OK;
+}
+
+// Units: (row tile of 128 token-major (t, h) rows) x (half of the output columns).
+ls_status mla_sched(const ls_latent_cache* c, int R, int H, int num_splits, LsSched* sc,
+                    size_t* part_o, size_t* part_lse, size_t* total) {
+  if (R < 0 || H <= 0 || num_splits < 1) return LS_ERR_INVALID_ARG;
+  const int64_t rows = (int64_t)R * H;
+  const int64_t units = 2 * ((rows + ls_mla_unit_rows() - 1) / ls_mla_unit_rows());
+  if (rows >= (1ll << 31) || units >= (1ll << 30)) return LS_ERR_UNSUPPORTED;
+  DevInfo d;
+  const ls_status s = dev_info(&d);
+  if (s != LS_OK) return s;
+  const int tile = ls_mla_tile();
+  *sc = ls_make_sched((int)units, (int)((c->num_tokens + tile - 1) / tile), num_splits, d.sms);
+  const size_t pieces = sc->has_partials() ? (size_t)sc->num_pieces() : 0;
+  *part_o = 0;
+  *part_lse = align256(pieces * ls_mla_unit_rows() * ls_mla_half() * sizeof(float));
+  *total = *part_lse + align256(pieces * ls_mla_unit_rows() * sizeof(float));
+  return LS_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+ls_status ls_capture_latent(const ls_latent_cache* cache, const void* lat, int64_t start_pos,
+                            int64_t n, ls_stream_t stream) {
+  ls_status s = check_latent(cache);
+  if (s != LS_OK) return s;
+  if (start_pos < 0 || n < 0) return LS_ERR_INVALID_ARG;
+  if (start_pos + n > (int64_t)cache->num_logical_pages * cache->page_size) return LS_ERR_INVALID_ARG;
+  if (n == 0) return LS_OK;
+  if (!lat || !aligned16(lat)) return LS_ERR_INVALID_ARG;
+  DevInfo d;
+  if ((s = dev_info(&d)) != LS_OK) return s;
+  return from_cuda(ls_launch_capture_latent(lat, cache->pool, cache->page_table, cache->num_pages,
+                                            ilog2_exact(cache->page_size), start_pos, n, d.sms,
+                                            d.err, (cudaStream_t)stream));
+}
+
+ls_status ls_mla_replay_fwd_workspace(const ls_latent_cache* cache, int R, int H, int num_splits,
+                                      size_t* bytes) {
+  ls_status s = check_latent(cache);
+  if (s != LS_OK) return s;
+  if (!bytes) return LS_ERR_INVALID_ARG;
+  LsSched sc;
+  size_t po, pl;
+  return mla_sched(cache, R, H, num_splits, &sc, &po, &pl, bytes);
+}
+
+ls_status ls_mla_replay_fwd(const ls_latent_cache* cache, const void* q, const void* lat_resp,
+                            int R, int H, float softmax_scale, int num_splits, void* o,
+                            float* lse, void* workspace, size_t workspace_bytes,
+                            ls_stream_t stream) {
+  ls_status s = check_latent(cache);
+  if (s != LS_OK) return s;
+  if (!isfinite(softmax_scale) || !(softmax_scale > 0.f)) return LS_ERR_INVALID_ARG;
+  LsSched sc;
+  size_t po, pl, total;
+  if ((s = mla_sched(cache, R, H, num_splits, &sc, &po, &pl, &total)) != LS_OK) return s;
+  if (R == 0) return LS_OK;
+  const void* ptrs[] = {q, lat_resp, o, lse};
+  for (const void* p : ptrs)
+    if (!p || !aligned16(p)) return LS_ERR_INVALID_ARG;
+  if (total > 0 && (!workspace || workspace_bytes < total || !aligned16(workspace)))
+    return LS_ERR_WORKSPACE;
+  DevInfo d;
+  if ((s = dev_info(&d)) != LS_OK) return s;
+  LsMlaArgs a;
+  a.pool = cache->pool;
+  a.page_table = cache->page_table;
+  a.num_pages = cache->num_pages;
+  a.ps_log2 = ilog2_exact(cache->page_size);
+  a.P = cache->num_tokens;
+  a.q = q;
+  a.lat_resp = lat_resp;
+  a.R = R;
+  a.H = H;
+  a.scale_log2 = softmax_scale * 1.4426950408889634f;
+  a.o = o;
+  a.lse = lse;
+  a.part_o = reinterpret_cast<float*>(static_cast<char*>(workspace) + po);
+  a.part_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) + pl);
+  a.err = d.err;
+  return from_cuda(ls_launch_mla_fwd(a, sc, (cudaStream_t)stream));
+}
+
 ls_status ls_selftest_wait_timeout(ls_stream_t stream) {
   DevInfo d;
   ls_status s = dev_info(&d);

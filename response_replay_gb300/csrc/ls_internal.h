@@ -157,3 +157,29 @@ cudaError_t ls_launch_gdn_fwd(const LsGdnArgs& a, void* o, float* state_out, voi
 cudaError_t ls_launch_gdn_bwd(const LsGdnArgs& a, const void* d_o, int accumulate, float* dq,
                               float* dk, float* dv, float* dg, float* dbeta, void* ws,
                               cudaStream_t st);
+
+// Latent (MLA-style) replay forward (mla_replay.cu): rows of 576 bf16 values (512 latent
+// + 64 rotary), outputs of 512; units = (128 token-major (t, h) rows) x (half of the
+// output columns), unit u covering row tile u >> 1 and half u & 1.
+struct LsMlaArgs {
+  const void* pool;           // bf16 [num_pages][page_size][576]
+  const int32_t* page_table;  // [ceil(P / page_size)]
+  int32_t num_pages, ps_log2;
+  int64_t P;
+  const void* q;              // bf16 [R][H][576]
+  const void* lat_resp;       // bf16 [R][576]
+  int32_t R, H;
+  float scale_log2;           // softmax scale x log2(e)
+  void* o;                    // bf16 [R][H][512]
+  float* lse;                 // [R][H]
+  float* part_o;              // [pieces][128][256] partials of tail-unit pieces
+  float* part_lse;            // [pieces][128]
+  uint32_t* err;
+};
+int ls_mla_tile();
+int ls_mla_unit_rows();
+int ls_mla_half();
+cudaError_t ls_launch_mla_fwd(const LsMlaArgs& a, const LsSched& sc, cudaStream_t st);
+cudaError_t ls_launch_capture_latent(const void* src, void* pool, const int32_t* page_table,
+                                     int32_t num_pages, int32_t ps_log2, int64_t start,
+                                     int64_t n, int sms, uint32_t* err, cudaStream_t st);

@@ -208,3 +208,44 @@ def make_gdn(R: int, H: int, seed: int, device="cpu", d: int = HEAD_DIM,
     beta = torch.sigmoid(torch.randn(R, H, generator=gg, device=device)).float().contiguous()
     state0 = (torch.randn(H, d, d, generator=gg, device=device) * state_std).float()
     return GdnInputs(state0, q, k, v, g, beta, d_o)
+
+
+LATENT_ROW = 576   # latent (512) + rotary key (64) values per position
+
+
+@dataclass
+class LatentPrompt:
+    """Prompt rows of a latent-attention layer to capture, and the page placement."""
+    lat: torch.Tensor          # [P][576] bf16, logical order
+    page_table: torch.Tensor   # [ceil(P / page_size)] int32
+    num_pages: int
+    page_size: int
+
+
+@dataclass
+class LatentBranch:
+    """One response branch of a latent-attention layer."""
+    q: torch.Tensor            # [R][H][576] bf16 absorbed queries
+    lat: torch.Tensor          # [R][576] bf16 the response's own rows
+
+
+def make_latent_prompt(P: int, page_size: int, seed: int, device="cpu",
+                       extra_pages: int = 0) -> LatentPrompt:
+    """Rows ~ N(0,1); page table a seeded random choice of distinct physical pages."""
+    g = gen(device, seed)
+    lat = torch.randn(P, LATENT_ROW, generator=g, device=device).to(torch.bfloat16)
+    logical = (P + page_size - 1) // page_size
+    num_pages = logical + extra_pages
+    rng = np.random.default_rng(seed)
+    pt = rng.permutation(num_pages)[:logical].astype(np.int32)
+    return LatentPrompt(lat, torch.from_numpy(pt).to(device), num_pages, page_size)
+
+
+def make_latent_branch(R: int, H: int, seed: int, device="cpu", sharp: bool = False) -> LatentBranch:
+    """Rows ~ N(0,1); queries N(0,1) (sharp: scores of spread ~1.7 at scale 1/sqrt(192))
+    or N(0,1)/sqrt(576) (near-uniform)."""
+    g = gen(device, seed)
+    qs = 1.0 if sharp else LATENT_ROW ** -0.5
+    q = (torch.randn(R, H, LATENT_ROW, generator=g, device=device) * qs).to(torch.bfloat16)
+    lat = torch.randn(R, LATENT_ROW, generator=g, device=device).to(torch.bfloat16)
+    return LatentBranch(q, lat)

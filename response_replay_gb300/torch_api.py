@@ -344,3 +344,63 @@ def gdn_replay_bwd(state0, q, k, v, g, beta, d_o, scale: float, grads=None,
 
 def last_device_error(stream=None) -> int:
     return B.ls_last_device_error(_stream(stream))
+
+
+# ---------------------------------------------------------------- latent (MLA) replay
+
+LATENT_DIM = 512           # c_j: the values attention averages
+LATENT_ROW = 576           # c_j followed by the 64-value rotary key
+
+
+class LatentCache:
+    """Latent (MLA-style) pages of one layer plus page table (ls_latent_cache): rows of
+    LATENT_ROW bf16 values shared by all heads.  host_pool=True places the pool in pinned
+    host memory (Grace memory on a Grace-Blackwell node), read there by the kernels."""
+
+    def __init__(self, num_pages: int, page_table: torch.Tensor, page_size: int, num_tokens: int,
+                 device=None, fill: float | None = None, pool: torch.Tensor | None = None,
+                 host_pool: bool = False):
+        device = torch.device(device) if device is not None else page_table.device
+        shape = (num_pages, page_size, LATENT_ROW)
+        if pool is None:
+            pool = (torch.empty(shape, dtype=torch.bfloat16, pin_memory=True) if host_pool
+                    else torch.empty(shape, dtype=torch.bfloat16, device=device))
+            if fill is not None:
+                pool.fill_(fill)
+        _check_pool(pool, "pool", shape)
+        _check(page_table, "page_table", torch.int32)
+        self.pool, self.page_table = pool, page_table
+        self.page_size, self.num_tokens = page_size, num_tokens
+        self.struct = B.ls_latent_cache(pool.data_ptr(), page_table.data_ptr(), num_pages,
+                                        page_table.numel(), page_size, num_tokens)
+
+    @property
+    def device(self):
+        return self.page_table.device
+
+    def capture(self, lat: torch.Tensor, start_pos: int = 0, stream=None) -> None:
+        n = lat.shape[0]
+        _check(lat, "lat", torch.bfloat16, (n, LATENT_ROW))
+        B.ls_capture_latent(self.struct, lat.data_ptr(), start_pos, n, _stream(stream))
+
+
+def mla_replay_fwd(cache: LatentCache, q: torch.Tensor, lat_resp: torch.Tensor,
+                   softmax_scale: float, num_splits: int, o: torch.Tensor | None = None,
+                   lse: torch.Tensor | None = None, stream=None):
+    """q [R][H][576] absorbed queries, lat_resp [R][576] the response's own rows ->
+    o [R][H][512] (bf16), lse [R][H] (fp32)."""
+    R, H, _ = q.shape
+    _check(q, "q", torch.bfloat16, (R, H, LATENT_ROW))
+    _check(lat_resp, "lat_resp", torch.bfloat16, (R, LATENT_ROW))
+    if o is None:
+        o = torch.empty((R, H, LATENT_DIM), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((R, H), dtype=torch.float32, device=q.device)
+    _check(o, "o", torch.bfloat16, (R, H, LATENT_DIM))
+    _check(lse, "lse", torch.float32, (R, H))
+    nbytes = B.ls_mla_replay_fwd_workspace(cache.struct, R, H, num_splits)
+    ws = workspace(nbytes, q.device, "mla_fwd")
+    B.ls_mla_replay_fwd(cache.struct, q.data_ptr(), lat_resp.data_ptr(), R, H, softmax_scale,
+                        num_splits, o.data_ptr(), lse.data_ptr(), ws.data_ptr(), ws.numel(),
+                        _stream(stream))
+    return o, lse
