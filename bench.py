@@ -849,6 +849,91 @@ def run_host_sweep(args, local_rank: int):
         }), flush=True)
 
 
+# ------------------------------------------------------------------ latent (MLA) replay
+
+MLA_ROW, MLA_DC = 576, 512
+
+
+def mla_flops(P: int, R: int, H: int) -> tuple[float, float]:
+    """(algorithmic, executed) FLOPs of one latent replay forward: per (query row, visible
+    key) 2 x 576 for the score and 2 x 512 for the output; the kernel computes every
+    score twice (once per half of the output columns)."""
+    pairs = R * H * (P + (R + 1) / 2)
+    return pairs * 2 * (MLA_ROW + MLA_DC), pairs * 2 * (2 * MLA_ROW + MLA_DC)
+
+
+def run_mla_sweep(args, local_rank: int):
+    """Supplementary, labelled lines (not the headline): the latent (MLA-style) replay
+    forward over a prompt of P (default 2,097,152) 576-value latent rows (256-row pages,
+    256 splits), H query heads, with the pool in HBM and (for short responses) in pinned host
+    memory read over the host link; one JSON line per R."""
+    import torch
+
+    from response_replay_gb300 import synthetic as syn
+    from response_replay_gb300 import torch_api as api
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    P, ps, splits, H = args.mla_p, 256, 256, args.mla_heads
+    scale = 192 ** -0.5
+    pr = syn.make_latent_prompt(P, ps, 4242, dev)
+    dcache = api.LatentCache(pr.num_pages, pr.page_table, ps, P, device=dev)
+    dcache.capture(pr.lat)
+    hcache = None
+    if args.mla_host_max_r > 0:
+        hcache = api.LatentCache(pr.num_pages, pr.page_table, ps, P, host_pool=True)
+        hcache.capture(pr.lat)  # written over the link by the capture kernel
+    del pr
+    stream = torch.cuda.current_stream()
+
+    def timed(fn, steps):
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(steps):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / steps
+
+    h2d_gbs = None
+    Rs = [int(x) for x in args.sweep_mla.split(",")]
+    if any(R <= args.mla_host_max_r for R in Rs):  # copy-engine rate from pinned memory
+        src = torch.empty(1 << 31, dtype=torch.int16, pin_memory=True)
+        dst = torch.empty(1 << 31, dtype=torch.int16, device=dev)
+        copy_ms = timed(lambda: dst.copy_(src, non_blocking=True), max(args.steps, 3))
+        h2d_gbs = src.numel() * 2 / (copy_ms * 1e-3) / 1e9
+        del src, dst
+    pk, pk_src = peaks()
+    peak = pk.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+    lat_bytes = P * MLA_ROW * 2
+    for R in Rs:
+        br = syn.make_latent_branch(R, H, 4243, dev, sharp=True)
+        o = torch.empty((R, H, MLA_DC), dtype=torch.bfloat16, device=dev)
+        lse = torch.empty((R, H), dtype=torch.float32, device=dev)
+        line = {"sweep": f"latent (MLA-style) replay forward, {P:,} positions (supplementary)",
+                "R": R, "config": {"workload": f"P={P:,} latent rows of {MLA_ROW} bf16 "
+                                               f"({MLA_DC} latent + 64 rotary), H={H}, "
+                                               f"{ps}-row pages, {splits} splits"}}
+        for name, cache in (("hbm", dcache), ("host", hcache)):
+            if name == "host" and R > args.mla_host_max_r:
+                continue
+            ms = timed(lambda: api.mla_replay_fwd(cache, br.q, br.lat, scale, splits, o=o,
+                                                  lse=lse, stream=stream), args.steps)
+            alg, exe = mla_flops(P, R, H)
+            line.update({f"{name}_fwd_ms": ms,
+                         f"{name}_tflops": alg / (ms * 1e-3) / 1e12,
+                         f"{name}_executed_tflops": exe / (ms * 1e-3) / 1e12,
+                         f"{name}_latent_gbs": lat_bytes / (ms * 1e-3) / 1e9})
+        line.update({"executed_frac_of_bf16_burst": line["hbm_executed_tflops"] / peak,
+                     "peak": f"{pk_src} bf16 burst {peak}", "h2d_copy_gbs": h2d_gbs,
+                     "steps": args.steps, "warmup": args.warmup})
+        print(json.dumps(line), flush=True)
+
+
 # ------------------------------------------------------------------ streamed layers
 
 def run_layers_sweep(args, local_rank: int):
@@ -1163,6 +1248,12 @@ def main():
     ap.add_argument("--sweep-host", default=None,
                     help="comma-separated response lengths: supplementary lines with the "
                          "prompt pages in pinned host memory against HBM")
+    ap.add_argument("--sweep-mla", default=None,
+                    help="comma-separated response lengths: supplementary latent (MLA-style) "
+                         "replay lines instead of the headline step")
+    ap.add_argument("--mla-heads", type=int, default=64)
+    ap.add_argument("--mla-p", type=int, default=2097152)
+    ap.add_argument("--mla-host-max-r", type=int, default=16)
     ap.add_argument("--sweep-short", default=None,
                     help="comma-separated response lengths: supplementary short-R sweep "
                          "(one JSON line each) instead of the headline step")
@@ -1190,6 +1281,10 @@ def main():
     if args.sweep_layers:
         if rank == 0:
             run_layers_sweep(args, local_rank)
+        return
+    if args.sweep_mla:
+        if rank == 0:
+            run_mla_sweep(args, local_rank)
         return
     if args.sweep_gdn:
         if rank == 0:

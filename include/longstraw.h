@@ -361,7 +361,7 @@ ls_status ls_gdn_replay_bwd(const float* state0, const void* q, const void* k, c
  * ls_mla_replay_fwd: the forward of one response of R tokens with H heads.
  * q: bf16 [R][H][576]; lat_resp: bf16 [R][576] (the response's own rows); o: bf16
  * [R][H][512]; lse: fp32 [R][H].  num_splits (>= 1) cuts the prompt into that many
- * ranges of 32-row tiles, merged by log-sum-exp; the result does not depend on it
+ * ranges of 64-row tiles, merged by log-sum-exp; the result does not depend on it
  * beyond rounding.  softmax_scale finite and > 0.  R == 0 is a no-op; P == 0 is causal
  * attention over the response rows.  Inputs must be finite (a row past a query's
  * causal bound has weight zero, and zero times a non-finite value is not zero).

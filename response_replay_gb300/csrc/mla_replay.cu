@@ -17,27 +17,37 @@
 // and leave none for the scores, so a unit is 128 query rows (token-major (t, h) rows)
 // times one half of the output columns; the two halves of a row tile are separate
 // units, each computing the full 576-wide scores (the price of the split: the score
-// products run twice).  The 128 x 576 Q tile (144 KB) stays in shared memory for the
-// unit; latent tiles of 32 rows (36 KB) stream through a two-stage ring.  Prompt tiles
-// are gathered page by page through the page table, and the pages may be pinned host
-// memory read over the host link.
+// products run twice).  Latent tiles are 64 rows (72 KB) in a two-stage ring: the score
+// MMA then has N = 64, and a tile's fixed costs (waits, commits, the softmax round trip)
+// are paid once per 64 rows (measured: 32-row tiles ran the tensor pipe 26% busy).  The
+// unit's Q tile is split between the 128 tensor-memory columns the output and the two
+// score buffers leave free (values 0-255, the A operand of the first 16 score MMAs) and
+// shared memory (values 256-575, 80 KB).  Prompt tiles are gathered page by page through
+// the page table, and the pages may be pinned host memory read over the host link.
 //
 // CTA (one per SM, persistent, 8 warps) over the same split-KV schedule as the other
 // replay kernels (ls_sched.h: whole units in waves, tail units cut into pieces whose
 // partial (o, lse) mla_fwd_combine merges):
-//   warp 0      TMA producer: the unit's Q (9 boxes of 64 values x 128 rows), then the
-//               latent tiles (9 boxes of 64 values x 32 rows); rows of a ragged last
-//               prompt tile are zeroed before the tile is handed over.
-//   warp 1      MMA issuer (one thread): S(g) = Q L^T into one of two score buffers (36
-//               SS MMAs, M=128 N=32 K=16), then O += P(g-1) L[:, half] for the tile
-//               before (two TS MMAs, M=128 N=256, P from tensor memory, the latent tile
-//               as an MN-major operand).  S(g) runs while the softmax works on g-1.
-//   warps 4-7   softmax, one query row per thread: scores of the tile, masks, running
+//   warp 0      TMA producer: the shared-memory part of the unit's Q (5 boxes of 64
+//               values x 128 rows), then the latent tiles (9 boxes of 64 values x 64
+//               rows, two of 32 rows on 32-row pages); rows of a ragged last prompt tile
+//               are zeroed before the hand-over.
+//   warp 1      MMA issuer (one thread): S(g) = Q L^T into one of two score buffers (16
+//               TS MMAs with Q from tensor memory, then 20 SS MMAs; M=128 N=64 K=16),
+//               then O += P(g-1) L[:, half] for the tile before (four TS MMAs, M=128
+//               N=256, P from tensor memory, the latent tile as an MN-major operand).
+//               S(g) runs while the softmax works on g-1; at a range boundary the old
+//               range's last P L goes first, so its output can be read and the next Q
+//               written into tensor memory.
+//   warps 4-7   at the start of a range, the tensor-memory part of Q (each thread its
+//               row's first 256 values, once the old range's score MMAs are done);
+//               softmax, one query row per thread: scores of the tile, masks, running
 //               max in the log2 domain (O rescaled only when the max grows by more than
 //               2^8, after the previous tile's P L has finished), compensated row sum, P
 //               as bf16 pairs over the score buffer; at the end of a range normalises O
 //               and writes o / lse, or a partial for the combine.
-// Tensor memory (512 columns): O [0,256), S0 [256,288), S1 [288,320).
+// Tensor memory (512 columns): O [0,256), S0 [256,320), S1 [320,384), Q values 0-255 as
+// bf16 pairs [384,512).
 #include <math.h>
 
 #include "ls_device.cuh"
@@ -53,20 +63,23 @@ constexpr int kDc = 512;                  // latent values (output columns)
 constexpr int kD = 576;                   // latent + rotary values (score length)
 constexpr int kAtoms = kD / 64;           // 128-byte swizzle atoms per row
 constexpr int kRows = 128;                // query rows per unit
-constexpr int kKeys = 32;                 // latent rows per tile
+constexpr int kKeys = 64;                 // latent rows per tile
 constexpr int kHalf = kDc / 2;            // output columns per unit
 constexpr int kStages = 2;
+constexpr int kQtAtoms = 4;               // Q atoms held in tensor memory (values 0-255)
 constexpr int kThreads = 256;
 constexpr uint32_t kQAtomBytes = kRows * 128;           // 16 KB
-constexpr uint32_t kLAtomBytes = kKeys * 128;           // 4 KB
-constexpr uint32_t kQBytes = kAtoms * kQAtomBytes;      // 144 KB
-constexpr uint32_t kStageBytes = kAtoms * kLAtomBytes;  // 36 KB
+constexpr uint32_t kLAtomBytes = kKeys * 128;           // 8 KB
+constexpr uint32_t kQBytes = (kAtoms - kQtAtoms) * kQAtomBytes;  // 80 KB in shared memory
+constexpr uint32_t kStageBytes = kAtoms * kLAtomBytes;  // 72 KB
 constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffRing = kQBytes;
 constexpr uint32_t kOffBar = kOffRing + kStages * kStageBytes;
 constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;  // + barriers + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
-constexpr uint32_t kColO = 0, kColS = kHalf;
+constexpr uint32_t kColO = 0, kColS = kHalf, kColQ = kHalf + 2 * kKeys;
+static_assert(kColQ + kQtAtoms * 32 == 512, "tensor memory columns");
+constexpr int kPCols = kKeys / 2;         // P(g) as bf16 pairs over its score buffer
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleLog2 = 8.0f;
 
@@ -75,6 +88,7 @@ enum {
   B_KV_EMPTY = B_KV_FULL + kStages,
   B_Q_FULL = B_KV_EMPTY + kStages,
   B_Q_EMPTY,
+  B_QT_FULL,                 // the softmax warps wrote the range's Q values 0-383
   B_S_FULL,                  // 2: scores of tile g in buffer g & 1
   B_P_FULL = B_S_FULL + 2,   // 2: P of tile g written over buffer g & 1
   B_PV_DONE = B_P_FULL + 2,  // P L of a tile finished (one phase per tile)
@@ -98,7 +112,7 @@ struct MlaTile {
 };
 
 // The tiles of one CTA in schedule order: each (unit, item) of LsWalk expanded into its
-// 32-row tiles (a prompt split's tile range, or the response rows up to the row tile's
+// 64-row tiles (a prompt split's tile range, or the response rows up to the row tile's
 // last token).  Every item has at least one tile (non-empty splits; R >= 1), so the
 // first / last flags of a range always land on a tile.
 struct MlaCursor {
@@ -165,6 +179,7 @@ mla_fwd_kernel(const __grid_constant__ MlaTmaps tm, const LsMlaArgs a,
     }
     mbar_init(bar(sbase, B_Q_FULL), 1);
     mbar_init(bar(sbase, B_Q_EMPTY), 1);
+    mbar_init(bar(sbase, B_QT_FULL), kRows);
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(sbase, B_S_FULL + i), 1);
       mbar_init(bar(sbase, B_P_FULL + i), kRows);
@@ -200,14 +215,16 @@ mla_fwd_kernel(const __grid_constant__ MlaTmaps tm, const LsMlaArgs a,
       MlaTile r;
       uint32_t ring = 0, ranges = 0, aux = 0;
       const int32_t ps = 1 << a.ps_log2;
+      const int32_t box_rows = ps < kKeys ? ps : kKeys;
       const int32_t pool_rows = a.num_pages * ps;
       while (cur.next(&r)) {
         if (r.first) {
           if (ranges > 0 && !mbar_wait(bar(sbase, B_Q_EMPTY), (ranges - 1) & 1)) { fail(); break; }
           const uint32_t qb = bar(sbase, B_Q_FULL);
           mbar_expect_tx(qb, kQBytes);
-          for (int at = 0; at < kAtoms; ++at)
-            tma_load_2d(sbase + kOffQ + at * kQAtomBytes, &tm.q, at * 64, (r.u >> 1) * kRows, qb);
+          for (int at = kQtAtoms; at < kAtoms; ++at)
+            tma_load_2d(sbase + kOffQ + (at - kQtAtoms) * kQAtomBytes, &tm.q, at * 64,
+                        (r.u >> 1) * kRows, qb);
           ++ranges;
         }
         const uint32_t st = ring % kStages;
@@ -219,18 +236,24 @@ mla_fwd_kernel(const __grid_constant__ MlaTmaps tm, const LsMlaArgs a,
         const uint32_t fb = bar(sbase, ragged ? (int)B_AUX : B_KV_FULL + (int)st);
         const uint32_t dst = sbase + kOffRing + st * kStageBytes;
         mbar_expect_tx(fb, kStageBytes);
-        const void* map = &tm.lr;
-        int32_t y = r.key0;
-        if (!r.resp) {
-          map = &tm.lp;
-          y = pool_rows;  // a bad page id reads as zeros (out of the map)
-          const int32_t phys = __ldg(a.page_table + (r.key0 >> a.ps_log2));
-          if ((uint32_t)phys < (uint32_t)a.num_pages)
-            y = phys * ps + (r.key0 & (ps - 1));
-          else
-            ls_report(a.err, LS_DEVERR_CHECK);
+        if (r.resp) {
+          for (int at = 0; at < kAtoms; ++at)
+            tma_load_2d(dst + at * kLAtomBytes, &tm.lr, at * 64, r.key0, fb);
+        } else {
+          for (int bb = 0; bb < kKeys / box_rows; ++bb) {
+            const int32_t pos = r.key0 + bb * box_rows;
+            int32_t y = pool_rows;  // past P or a bad page id: reads as zeros
+            if (pos < a.P) {
+              const int32_t phys = __ldg(a.page_table + (pos >> a.ps_log2));
+              if ((uint32_t)phys < (uint32_t)a.num_pages)
+                y = phys * ps + (pos & (ps - 1));
+              else
+                ls_report(a.err, LS_DEVERR_CHECK);
+            }
+            for (int at = 0; at < kAtoms; ++at)
+              tma_load_2d(dst + at * kLAtomBytes + bb * box_rows * 128, &tm.lp, at * 64, y, fb);
+          }
         }
-        for (int at = 0; at < kAtoms; ++at) tma_load_2d(dst + at * kLAtomBytes, map, at * 64, y, fb);
         if (ragged) {
           if (!mbar_wait(fb, aux & 1)) { fail(); break; }
           ++aux;
@@ -269,8 +292,10 @@ mla_fwd_kernel(const __grid_constant__ MlaTmaps tm, const LsMlaArgs a,
             sbase + kOffRing + pstage * kStageBytes + (uint32_t)(p.u & 1) * 4u * kLAtomBytes,
             kLAtomBytes);
         const uint32_t a0 = tmem + kColS + (pg & 1) * kKeys;
-        mma_ts_lo(tmem + kColO, a0, b0, idPV, p.first ? 0u : 1u);
-        mma_ts_lo(tmem + kColO, a0 + 8, b0 + (2048u >> 4), idPV, 1u);
+#pragma unroll
+        for (int kk = 0; kk < kKeys / 16; ++kk)  // 16 latent rows per MMA
+          mma_ts_lo(tmem + kColO, a0 + kk * 8, b0 + ((kk * 2048u) >> 4), idPV,
+                    (kk > 0 || !p.first) ? 1u : 0u);
         mma_commit(bar(sbase, B_KV_EMPTY + pstage));
         mma_commit(bar(sbase, B_PV_DONE));
         if (p.last) mma_commit(bar(sbase, B_O_DONE));
@@ -278,7 +303,12 @@ mla_fwd_kernel(const __grid_constant__ MlaTmaps tm, const LsMlaArgs a,
       };
       while (cur.next(&r)) {
         if (r.first) {
+          // the old range's last P L first: the softmax warps read its output and only
+          // then write this range's Q into tensor memory
+          if (have_prev && !issue_pv(prev, prev_stage, g - 1)) { ok = false; break; }
+          have_prev = false;
           if (!mbar_wait(bar(sbase, B_Q_FULL), ranges & 1)) { ok = false; break; }
+          if (!mbar_wait(bar(sbase, B_QT_FULL), ranges & 1)) { ok = false; break; }
           ++ranges;
         }
         if (!mbar_wait(bar(sbase, B_KV_FULL + ks.stage), ks.phase)) { ok = false; break; }
@@ -287,10 +317,15 @@ mla_fwd_kernel(const __grid_constant__ MlaTmaps tm, const LsMlaArgs a,
         const uint32_t b0 = sdesc_lo(sbase + kOffRing + ks.stage * kStageBytes, 16);
         const uint32_t d = tmem + kColS + (g & 1) * kKeys;
 #pragma unroll
-        for (int kk = 0; kk < 4 * kAtoms; ++kk) {
-          const uint32_t oa = ((kk >> 2) * kQAtomBytes + (kk & 3) * 32) >> 4;
+        for (int kk = 0; kk < 4 * kQtAtoms; ++kk) {  // Q values 0-255 from tensor memory
           const uint32_t ob = ((kk >> 2) * kLAtomBytes + (kk & 3) * 32) >> 4;
-          mma_ss_lo(d, q_lo + oa, b0 + ob, idS, kk > 0);
+          mma_ts_lo(d, tmem + kColQ + kk * 8, b0 + ob, idS, kk > 0);
+        }
+#pragma unroll
+        for (int kk = 4 * kQtAtoms; kk < 4 * kAtoms; ++kk) {  // values 256-575 from shared
+          const uint32_t oa = (((kk >> 2) - kQtAtoms) * kQAtomBytes + (kk & 3) * 32) >> 4;
+          const uint32_t ob = ((kk >> 2) * kLAtomBytes + (kk & 3) * 32) >> 4;
+          mma_ss_lo(d, q_lo + oa, b0 + ob, idS, 1u);
         }
         mma_commit(bar(sbase, B_S_FULL + (g & 1)));
         if (r.last) mma_commit(bar(sbase, B_Q_EMPTY));  // the range's Q is read by S only
@@ -315,16 +350,44 @@ mla_fwd_kernel(const __grid_constant__ MlaTmaps tm, const LsMlaArgs a,
     const int64_t nrows = (int64_t)a.R * a.H;
     MlaCursor cur(sc, blockIdx.x, a.R, a.H);
     MlaTile r;
-    uint32_t g = 0, oc = 0;
+    uint32_t g = 0, oc = 0, ranges = 0;
     float m = -INFINITY, l = 0.f, lcomp = 0.f;
     while (cur.next(&r)) {
+      if (r.first) {
+        // Q values 0-255 of this thread's row into tensor memory (bf16 pairs), once the
+        // old range's score MMAs have read theirs; rows past R x H are zeros
+        if (ranges > 0 && !mbar_wait(bar(sbase, B_Q_EMPTY), (ranges - 1) & 1)) { fail(); break; }
+        tc_fence_after();
+        const int64_t qrow = (int64_t)(r.u >> 1) * kRows + row;
+        const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.q) +
+                                                         (qrow < nrows ? qrow : 0) * kD);
+#pragma unroll 1
+        for (int c0 = 0; c0 < kQtAtoms * 32; c0 += 32) {
+          uint32_t qv[32];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const uint4 v = qrow < nrows ? __ldg(src + c0 / 4 + i) : make_uint4(0, 0, 0, 0);
+            qv[4 * i] = v.x;
+            qv[4 * i + 1] = v.y;
+            qv[4 * i + 2] = v.z;
+            qv[4 * i + 3] = v.w;
+          }
+          tmem_st32(lane_base + kColQ + c0, qv);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(bar(sbase, B_QT_FULL));
+        ++ranges;
+      }
       if (!mbar_wait(bar(sbase, B_S_FULL + (g & 1)), (g >> 1) & 1)) { fail(); break; }
       tc_fence_after();
       const uint32_t s_col = lane_base + kColS + (g & 1) * kKeys;
-      uint32_t sr[32];
+      uint32_t sr[kKeys];
       tmem_ld32(s_col, sr);
+      tmem_ld32(s_col + 32, sr + 32);
       tmem_wait_ld();
       reg_fence32(sr);
+      reg_fence32(sr + 32);
       const int64_t grow = (int64_t)(r.u >> 1) * kRows + row;  // (t, h) row, token-major
       const int32_t tq = (int32_t)(grow / a.H);
       int32_t lim = kKeys;  // visible keys [0, lim) of the tile
@@ -339,15 +402,16 @@ mla_fwd_kernel(const __grid_constant__ MlaTmaps tm, const LsMlaArgs a,
         for (int j = 0; j < kKeys; ++j)
           if (j >= lim) sr[j] = __float_as_uint(-INFINITY);
       }
-      float mx4[4];
+      float mx8[8];
 #pragma unroll
-      for (int k = 0; k < 4; ++k) mx4[k] = fmaxf(__uint_as_float(sr[k]), __uint_as_float(sr[k + 4]));
+      for (int k = 0; k < 8; ++k) mx8[k] = fmaxf(__uint_as_float(sr[k]), __uint_as_float(sr[k + 8]));
 #pragma unroll
-      for (int j = 8; j < kKeys; j += 8)
+      for (int j = 16; j < kKeys; j += 16)
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
-          mx4[k] = fmax3(mx4[k], __uint_as_float(sr[j + k]), __uint_as_float(sr[j + 4 + k]));
-      const float mt = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * c;
+        for (int k = 0; k < 8; ++k)
+          mx8[k] = fmax3(mx8[k], __uint_as_float(sr[j + k]), __uint_as_float(sr[j + 8 + k]));
+      const float mt = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
+                             fmaxf(mx8[6], mx8[7])) * c;
       bool rescale = false;
       float alpha = 1.f;
       if (r.first) {
@@ -378,9 +442,9 @@ mla_fwd_kernel(const __grid_constant__ MlaTmaps tm, const LsMlaArgs a,
       const float msub = (m == -INFINITY) ? 0.f : m;
       const float2 c2 = make_float2(c, c), nm2 = make_float2(-msub, -msub);
       float2 ls2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-      uint32_t pk[16];
+      uint32_t pk[kPCols];
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
+      for (int j = 0; j < kPCols; ++j) {
         float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[2 * j]), __uint_as_float(sr[2 * j + 1])),
                               c2, nm2);
         x.x = fast_exp2(x.x);
@@ -388,7 +452,7 @@ mla_fwd_kernel(const __grid_constant__ MlaTmaps tm, const LsMlaArgs a,
         ls2[j & 1] = __fadd2_rn(ls2[j & 1], x);
         pk[j] = pack_bf16(x.x, x.y);
       }
-      tmem_st16(s_col, pk);
+      tmem_st32(s_col, pk);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar(sbase, B_P_FULL + (g & 1)));
@@ -532,8 +596,10 @@ cudaError_t ls_launch_mla_fwd(const LsMlaArgs& a, const LsSched& sc, cudaStream_
     const uint64_t strides[1] = {(uint64_t)kD * 2};
     const uint32_t box[2] = {64, (uint32_t)kKeys};
     if (!ls_make_tmap_bf16(&tm.lr, a.lat_resp, 2, dims, strides, box)) return cudaErrorInvalidValue;
+    // prompt boxes never cross a page: 64 rows, or one 32-row page
     const uint64_t pdims[2] = {(uint64_t)kD, (uint64_t)a.num_pages << a.ps_log2};
-    if (!ls_make_tmap_bf16(&tm.lp, a.pool, 2, pdims, strides, box)) return cudaErrorInvalidValue;
+    const uint32_t pbox[2] = {64, (uint32_t)((1 << a.ps_log2) < kKeys ? (1 << a.ps_log2) : kKeys)};
+    if (!ls_make_tmap_bf16(&tm.lp, a.pool, 2, pdims, strides, pbox)) return cudaErrorInvalidValue;
   }
   cudaError_t e = cudaFuncSetAttribute(mla_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        kSmemBytes);
