@@ -22,16 +22,20 @@
 // are paid once per 64 rows (measured: 32-row tiles ran the tensor pipe 26% busy).  The
 // unit's Q tile is split between the 128 tensor-memory columns the output and the two
 // score buffers leave free (values 0-255, the A operand of the first 16 score MMAs) and
-// shared memory (values 256-575, 80 KB).  Prompt tiles are gathered page by page through
-// the page table, and the pages may be pinned host memory read over the host link.
+// shared memory (values 256-575, 80 KB).  A stage can be refilled only once P L of its
+// tile is done, and the next score MMAs need it right after, so the producer also
+// prefetches prompt tiles into L2 four tiles ahead (the refills then hit L2).  Prompt
+// tiles are gathered page by page through the page table, and the pages may be pinned
+// host memory read over the host link.
 //
 // CTA (one per SM, persistent, 8 warps) over the same split-KV schedule as the other
 // replay kernels (ls_sched.h: whole units in waves, tail units cut into pieces whose
 // partial (o, lse) mla_fwd_combine merges):
 //   warp 0      TMA producer: the shared-memory part of the unit's Q (5 boxes of 64
 //               values x 128 rows), then the latent tiles (9 boxes of 64 values x 64
-//               rows, two of 32 rows on 32-row pages); rows of a ragged last prompt tile
-//               are zeroed before the hand-over.
+//               rows, two of 32 rows on 32-row pages), and L2 prefetches of the prompt
+//               tiles four ahead; rows of a ragged last prompt tile are zeroed before the
+//               hand-over.
 //   warp 1      MMA issuer (one thread): S(g) = Q L^T into one of two score buffers (16
 //               TS MMAs with Q from tensor memory, then 20 SS MMAs; M=128 N=64 K=16),
 //               then O += P(g-1) L[:, half] for the tile before (four TS MMAs, M=128
@@ -66,6 +70,7 @@ constexpr int kRows = 128;                // query rows per unit
 constexpr int kKeys = 64;                 // latent rows per tile
 constexpr int kHalf = kDc / 2;            // output columns per unit
 constexpr int kStages = 2;
+constexpr int kPrefetch = 4;              // prompt tiles prefetched into L2 ahead of the loads
 constexpr int kQtAtoms = 4;               // Q atoms held in tensor memory (values 0-255)
 constexpr int kThreads = 256;
 constexpr uint32_t kQAtomBytes = kRows * 128;           // 16 KB
@@ -104,6 +109,14 @@ struct MlaTmaps {
 };
 
 __device__ __forceinline__ uint32_t bar(uint32_t sbase, int i) { return sbase + kOffBar + 8u * i; }
+
+// Prefetch a tensor-map box into L2 (no shared memory, no barrier).
+__device__ __forceinline__ void tma_prefetch_l2_2d(const void* tmap, int32_t x, int32_t y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                   reinterpret_cast<uint64_t>(tmap)),
+               "r"(x), "r"(y)
+               : "memory");
+}
 
 // One latent tile of the walk.
 struct MlaTile {
@@ -217,7 +230,26 @@ mla_fwd_kernel(const __grid_constant__ MlaTmaps tm, const LsMlaArgs a,
       const int32_t ps = 1 << a.ps_log2;
       const int32_t box_rows = ps < kKeys ? ps : kKeys;
       const int32_t pool_rows = a.num_pages * ps;
+      // a second walk kPrefetch tiles ahead: its prompt tiles are prefetched into L2, so
+      // the stage loads (which may start only when a stage is released) hit L2
+      MlaCursor ahead(sc, blockIdx.x, a.R, a.H);
+      MlaTile ra;
+      bool more = true;
+      auto prefetch = [&]() {
+        more = more && ahead.next(&ra);
+        if (!more || ra.resp) return;
+        for (int bb = 0; bb < kKeys / box_rows; ++bb) {
+          const int32_t pos = ra.key0 + bb * box_rows;
+          if (pos >= a.P) break;
+          const int32_t phys = __ldg(a.page_table + (pos >> a.ps_log2));
+          if ((uint32_t)phys >= (uint32_t)a.num_pages) continue;
+          const int32_t y = phys * ps + (pos & (ps - 1));
+          for (int at = 0; at < kAtoms; ++at) tma_prefetch_l2_2d(&tm.lp, at * 64, y);
+        }
+      };
+      for (int i = 0; i < kPrefetch; ++i) prefetch();
       while (cur.next(&r)) {
+        prefetch();
         if (r.first) {
           if (ranges > 0 && !mbar_wait(bar(sbase, B_Q_EMPTY), (ranges - 1) & 1)) { fail(); break; }
           const uint32_t qb = bar(sbase, B_Q_FULL);
