@@ -1,9 +1,10 @@
 """Seeded random shapes for replay attention, forward and backward, against the fp64
 oracle: prompt lengths from 0 up, response lengths from 1 token to a few tiles, every
 grouped-query ratio up to 8, page sizes 16-256, split counts from 1 to more than the
-prompt has tiles, scores of unit spread or near-uniform, and ragged member lists with
-empty members.  The shapes are drawn once from a fixed seed, so every run checks the
-same cases; each is small enough for the oracle to finish in about a second."""
+prompt has tiles, scores of unit spread or near-uniform, ragged member lists with
+empty members, and latent (MLA-style) replays with 1-128 heads and 32-4096-row pages.
+The shapes are drawn once from a fixed seed, so every run checks the same cases; each is
+small enough for the oracle to finish in about a second."""
 import numpy as np
 import pytest
 import torch
@@ -98,3 +99,34 @@ def test_random_ragged_members(cuda, P, lens, hq, hkv, ps, splits):
         for name, x, ref in (("dq", dq, dq_ref), ("dk", dk, dk_ref), ("dv", dv, dv_ref)):
             err = rel_err(x[s:e].cpu().numpy(), ref)
             assert err <= TOL_GRAD, (m, name, err)
+
+
+def _draw_latent(n, seed):
+    rng = np.random.default_rng(seed)
+    cases = []
+    while len(cases) < n:
+        H = int(rng.choice([1, 3, 16, 20, 64, 128]))
+        P = 0 if rng.random() < 0.15 else int(rng.integers(1, 6000))
+        R = int(np.exp(rng.uniform(0, np.log(200))))
+        ps = int(rng.choice([32, 64, 256, 4096]))
+        splits = int(rng.choice([1, 2, 5, 64, 1000]))
+        sharp = bool(rng.random() < 0.7)
+        if R * (P + R) * H > 3_000_000:
+            continue
+        cases.append((P, R, H, ps, splits, sharp))
+    return cases
+
+
+LATENT = _draw_latent(10, 20261205)
+
+
+@pytest.mark.parametrize("P,R,H,ps,splits,sharp", LATENT)
+def test_random_latent_replay(cuda, P, R, H, ps, splits, sharp):
+    from test_gpu_mla import SCALE, make, problem
+    cache, br = make(P, R, H, ps, 40 + P + R + H, cuda, sharp=sharp, extra_pages=1)
+    o, lse = api.mla_replay_fwd(cache, br.q, br.lat, SCALE, splits)
+    torch.cuda.synchronize()
+    assert B.ls_last_device_error(0) == B.LS_OK
+    o_ref, lse_ref = oracle.mla_fwd(problem(cache, br, P))
+    assert rel_err(o.float().cpu().numpy(), o_ref) <= TOL_O
+    assert float(np.abs(lse.cpu().numpy() - lse_ref).max()) <= TOL_LSE
