@@ -934,6 +934,84 @@ def run_mla_sweep(args, local_rank: int):
         print(json.dumps(line), flush=True)
 
 
+def run_mla_layers_sweep(args, local_rank: int):
+    """Supplementary, labelled line (not the headline): one response of R tokens replayed
+    (forward) through L latent-attention layers over a 2,097,152-row latent prompt, with
+    every layer's pages (a) in GPU memory and (b) in pinned host memory, streamed into a
+    two-slot GPU page cache one layer ahead (each layer's copy overlapping the previous
+    layer's replay)."""
+    import torch
+
+    from response_replay_gb300 import layers as Lm
+    from response_replay_gb300 import synthetic as syn
+    from response_replay_gb300 import torch_api as api
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    P, ps, splits, H, nl, R = args.mla_p, 256, 256, args.mla_heads, args.sweep_mla_layers, \
+        args.mla_layers_r
+    scale = 192 ** -0.5
+    pr0 = syn.make_latent_prompt(P, ps, 5100, dev)
+    st = Lm.StreamedLatentLayers(nl, pr0.num_pages, pr0.page_table, ps, P, device=dev)
+    res, brs = [], []
+    for l in range(nl):
+        lat = syn.make_latent_prompt(P, ps, 5100 + l, dev).lat
+        c = api.LatentCache(pr0.num_pages, pr0.page_table, ps, P, device=dev)
+        c.capture(lat)
+        st.capture(l, lat)
+        res.append(c)
+        del lat
+        brs.append(syn.make_latent_branch(R, H, 5200 + l, dev, sharp=True))
+    stream = torch.cuda.current_stream()
+    o = torch.empty((R, H, MLA_DC), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((R, H), dtype=torch.float32, device=dev)
+
+    def resident():
+        for l in range(nl):
+            api.mla_replay_fwd(res[l], brs[l].q, brs[l].lat, scale, splits, o=o, lse=lse,
+                               stream=stream)
+
+    def streamed():
+        st.prefetch(0)
+        for l in range(nl):
+            c = st.cache(l)
+            if l + 1 < nl:
+                st.prefetch(l + 1)
+            api.mla_replay_fwd(c, brs[l].q, brs[l].lat, scale, splits, o=o, lse=lse,
+                               stream=stream)
+            st.release(l)
+
+    def timed(fn):
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(args.steps):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / args.steps
+
+    ms_res, ms_str = timed(resident), timed(streamed)
+    # the copy alone, from pinned host memory into a slot
+    cp = timed(lambda: st.slots[0].pool.copy_(st.host[0].pool, non_blocking=True))
+    alg, _ = mla_flops(P, R, H)
+    print(json.dumps({
+        "sweep": f"latent replay through {nl} layers, pages streamed from host memory vs held "
+                 "in HBM (supplementary)",
+        "config": {"workload": f"P={P:,} latent rows of {MLA_ROW} bf16, H={H}, R={R}, "
+                               f"{ps}-row pages, {splits} splits, {nl} layers"},
+        "hbm_ms": ms_res, "streamed_ms": ms_str, "slowdown": ms_str / ms_res,
+        "hbm_tflops": nl * alg / (ms_res * 1e-3) / 1e12,
+        "streamed_tflops": nl * alg / (ms_str * 1e-3) / 1e12,
+        "layer_copy_ms": cp, "layer_bytes": st.bytes_per_layer,
+        "layer_copy_gbs": st.bytes_per_layer / (cp * 1e-3) / 1e9,
+        "steps": args.steps, "warmup": args.warmup,
+    }), flush=True)
+
+
 # ------------------------------------------------------------------ streamed layers
 
 def run_layers_sweep(args, local_rank: int):
@@ -1251,6 +1329,10 @@ def main():
     ap.add_argument("--sweep-mla", default=None,
                     help="comma-separated response lengths: supplementary latent (MLA-style) "
                          "replay lines instead of the headline step")
+    ap.add_argument("--sweep-mla-layers", type=int, default=0,
+                    help="number of latent-attention layers: supplementary line with their "
+                         "pages streamed from pinned host memory against held in HBM")
+    ap.add_argument("--mla-layers-r", type=int, default=256)
     ap.add_argument("--mla-heads", type=int, default=64)
     ap.add_argument("--mla-p", type=int, default=2097152)
     ap.add_argument("--mla-host-max-r", type=int, default=16)
@@ -1285,6 +1367,10 @@ def main():
     if args.sweep_mla:
         if rank == 0:
             run_mla_sweep(args, local_rank)
+        return
+    if args.sweep_mla_layers:
+        if rank == 0:
+            run_mla_layers_sweep(args, local_rank)
         return
     if args.sweep_gdn:
         if rank == 0:

@@ -22,7 +22,7 @@ takes its dQ / dK / dV.  This module holds the part that needs no weights:
 - ``StreamedLayers``: the L layers' prompt pages in pinned host memory (Grace memory on a
   GB300 node), streamed into a two-slot page cache in GPU memory one layer ahead of the
   replay that reads them (explainer, same section, GLM bullet: the prompt's pages held in
-  CPU memory).
+  CPU memory); ``StreamedLatentLayers`` does the same for latent (MLA-style) pages.
 
 Every step of the computation is a call of the replay backward in the CUDA library.
 """
@@ -127,11 +127,11 @@ def reverse_replay_bwd(layers: LayeredKVCache, saved: Sequence[tuple],
         consume(l, dq, dk, dv)
 
 
-class StreamedLayers:
-    """The captured prompt pages of L layers held in pinned host memory (on a
-    Grace-Blackwell node, Grace memory: room for every layer of a long prompt, which HBM
-    would not hold), streamed into a two-slot page cache in GPU memory one layer ahead of
-    the replay that reads them.
+class _TwoSlotLayers:
+    """Every layer's captured pages in pinned host memory (on a Grace-Blackwell node,
+    Grace memory: room for every layer of a long prompt, which HBM would not hold),
+    streamed into a two-slot page cache in GPU memory one layer ahead of the replay that
+    reads them.
 
     The kernels could read the host pages directly, but every unit of a long replay
     re-reads the prompt and those reads are not kept in L2, so a long replay from host
@@ -140,35 +140,30 @@ class StreamedLayers:
     its own stream while the current layer is replayed.
 
     Use: ``prefetch(l)`` starts layer l's copy (it waits until the slot's previous layer
-    is released); ``cache(l)`` returns the layer's ``PagedKVCache`` in GPU memory and makes
-    the current stream wait for its copy; ``release(l)`` marks the point on the current
+    is released); ``cache(l)`` returns the layer's cache in GPU memory and makes the
+    current stream wait for its copy; ``release(l)`` marks the point on the current
     stream after which the slot may be overwritten.  Capture writes the host pages
-    directly (``capture``)."""
+    directly (``capture``).  Subclasses name the caches and their page pools."""
 
-    def __init__(self, num_layers: int, num_pages: int, page_table: torch.Tensor,
-                 page_size: int, num_kv_heads: int, num_tokens: int, device=None):
-        if num_layers < 1:
-            raise ValueError("num_layers must be at least 1")
-        device = torch.device(device) if device is not None else page_table.device
+    def __init__(self, host: list, slots: list, device, bytes_per_layer: int):
         self.device = device
-        shape = (num_pages, num_kv_heads, page_size, api.HEAD_DIM)
-        self.host = [api.PagedKVCache(num_pages, page_table, page_size, num_kv_heads, num_tokens,
-                                      host_pools=True) for _ in range(num_layers)]
-        self.slots = [api.PagedKVCache(num_pages, page_table, page_size, num_kv_heads, num_tokens,
-                                       device=device) for _ in range(2)]
+        self.host = host
+        self.slots = slots
         self.copy_stream = torch.cuda.Stream(device)
         self.ready = [torch.cuda.Event() for _ in range(2)]
         self.free = [torch.cuda.Event() for _ in range(2)]
         self.freed = [True, True]        # no release owed before the first copy
         self.layer_in = [None, None]     # layer held (or being copied) by each slot
-        self.bytes_per_layer = 2 * int(torch.Size(shape).numel()) * 2
+        self.bytes_per_layer = bytes_per_layer
+
+    @staticmethod
+    def _pools(cache) -> tuple:
+        raise NotImplementedError
 
     def __len__(self) -> int:
         return len(self.host)
 
-    def capture(self, layer: int, k: torch.Tensor, v: torch.Tensor, start_pos: int = 0,
-                stream=None) -> None:
-        self.host[layer].capture(k, v, start_pos, stream)
+    def _stale(self, layer: int) -> None:
         for s in range(2):              # a slot holding this layer is now stale
             if self.layer_in[s] == layer:
                 self.layer_in[s] = None
@@ -189,13 +184,13 @@ class StreamedLayers:
         if not self.freed[s]:
             cs.wait_event(self.free[s])
         with torch.cuda.stream(cs):
-            self.slots[s].k_pool.copy_(self.host[layer].k_pool, non_blocking=True)
-            self.slots[s].v_pool.copy_(self.host[layer].v_pool, non_blocking=True)
+            for dst, src in zip(self._pools(self.slots[s]), self._pools(self.host[layer])):
+                dst.copy_(src, non_blocking=True)
             self.ready[s].record(cs)
         self.layer_in[s] = layer
         self.freed[s] = False
 
-    def cache(self, layer: int) -> api.PagedKVCache:
+    def cache(self, layer: int):
         self.prefetch(layer)
         s = self._slot(layer)
         torch.cuda.current_stream(self.device).wait_event(self.ready[s])
@@ -206,3 +201,54 @@ class StreamedLayers:
         if self.layer_in[s] == layer:
             self.free[s].record(torch.cuda.current_stream(self.device))
             self.freed[s] = True
+
+
+class StreamedLayers(_TwoSlotLayers):
+    """The captured prompt K/V pages of L attention layers in pinned host memory,
+    streamed through a two-slot GPU page cache (see _TwoSlotLayers)."""
+
+    def __init__(self, num_layers: int, num_pages: int, page_table: torch.Tensor,
+                 page_size: int, num_kv_heads: int, num_tokens: int, device=None):
+        if num_layers < 1:
+            raise ValueError("num_layers must be at least 1")
+        device = torch.device(device) if device is not None else page_table.device
+        shape = (num_pages, num_kv_heads, page_size, api.HEAD_DIM)
+        host = [api.PagedKVCache(num_pages, page_table, page_size, num_kv_heads, num_tokens,
+                                 host_pools=True) for _ in range(num_layers)]
+        slots = [api.PagedKVCache(num_pages, page_table, page_size, num_kv_heads, num_tokens,
+                                  device=device) for _ in range(2)]
+        super().__init__(host, slots, device, 2 * int(torch.Size(shape).numel()) * 2)
+
+    @staticmethod
+    def _pools(cache) -> tuple:
+        return cache.k_pool, cache.v_pool
+
+    def capture(self, layer: int, k: torch.Tensor, v: torch.Tensor, start_pos: int = 0,
+                stream=None) -> None:
+        self.host[layer].capture(k, v, start_pos, stream)
+        self._stale(layer)
+
+
+class StreamedLatentLayers(_TwoSlotLayers):
+    """The captured latent (MLA-style) pages of L latent-attention layers in pinned host
+    memory (the GLM layers' CPU-resident latent pages of the explainer, GLM bullet),
+    streamed through a two-slot GPU page cache (see _TwoSlotLayers)."""
+
+    def __init__(self, num_layers: int, num_pages: int, page_table: torch.Tensor,
+                 page_size: int, num_tokens: int, device=None):
+        if num_layers < 1:
+            raise ValueError("num_layers must be at least 1")
+        device = torch.device(device) if device is not None else page_table.device
+        host = [api.LatentCache(num_pages, page_table, page_size, num_tokens, host_pool=True)
+                for _ in range(num_layers)]
+        slots = [api.LatentCache(num_pages, page_table, page_size, num_tokens, device=device)
+                 for _ in range(2)]
+        super().__init__(host, slots, device, num_pages * page_size * api.LATENT_ROW * 2)
+
+    @staticmethod
+    def _pools(cache) -> tuple:
+        return (cache.pool,)
+
+    def capture(self, layer: int, lat: torch.Tensor, start_pos: int = 0, stream=None) -> None:
+        self.host[layer].capture(lat, start_pos, stream)
+        self._stale(layer)

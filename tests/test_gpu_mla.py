@@ -1,8 +1,9 @@
 """GPU parity of the latent (MLA-style) replay forward against the fp64 oracle, through
 the C ABI: element by element at small sizes (several row tiles and split pieces,
 ragged prompt tails, P = 0, one token per tile at 128 heads), latent pages in pinned
-host memory (bit-identical to the same pages in GPU memory), the capture, a bad page
-id, and sampled rows over a 2,097,152-position prompt."""
+host memory (bit-identical to the same pages in GPU memory), layers streamed from host
+memory through the two-slot GPU page cache, the capture, a bad page id, and sampled rows
+over a 2,097,152-position prompt."""
 import numpy as np
 import pytest
 import torch
@@ -135,3 +136,38 @@ def test_mla_full_prompt_sampled_rows(cuda):
     assert float(np.abs(lse.cpu().numpy()[ts, hs] - lse_ref).max()) <= TOL_LSE
     # the rows are sharp: the LSE sits well above log(P + t + 1)
     assert np.abs(lse_ref - np.log(P + ts + 1.0)).max() > 0.1
+
+
+def test_streamed_latent_layers_match_resident(cuda):
+    """Three layers' latent pages captured into pinned host memory and streamed through the
+    two-slot GPU page cache one layer ahead: every layer's forward bit-identical to the
+    same pages held in GPU memory, one layer against the oracle."""
+    from response_replay_gb300 import layers as L
+    P, R, H, ps, splits, nl = 3000, 40, 16, 64, 5, 3
+    pr0 = syn.make_latent_prompt(P, ps, 900, cuda, extra_pages=2)
+    st = L.StreamedLatentLayers(nl, pr0.num_pages, pr0.page_table, ps, P, device=cuda)
+    res, brs = [], []
+    for l in range(nl):
+        lat = syn.make_latent_prompt(P, ps, 900 + 3 * l, cuda).lat[:P].contiguous()
+        c = api.LatentCache(pr0.num_pages, pr0.page_table, ps, P, device=cuda)
+        c.capture(lat)
+        res.append(c)
+        st.capture(l, lat)
+        brs.append(syn.make_latent_branch(R, H, 920 + l, cuda, sharp=True))
+    st.prefetch(0)
+    outs = []
+    for l in range(nl):
+        c = st.cache(l)
+        if l + 1 < nl:
+            st.prefetch(l + 1)
+        outs.append(api.mla_replay_fwd(c, brs[l].q, brs[l].lat, SCALE, splits))
+        st.release(l)
+    torch.cuda.synchronize()
+    assert B.ls_last_device_error(0) == B.LS_OK
+    for l in range(nl):
+        o_r, l_r = api.mla_replay_fwd(res[l], brs[l].q, brs[l].lat, SCALE, splits)
+        assert torch.equal(outs[l][0], o_r) and torch.equal(outs[l][1], l_r), l
+    assert not st.host[1].pool.is_cuda and st.host[1].pool.is_pinned()
+    o_ref, lse_ref = oracle.mla_fwd(problem(st.host[1], brs[1], P))
+    assert rel_err(outs[1][0].float().cpu().numpy(), o_ref) <= TOL_O
+    assert float(np.abs(outs[1][1].cpu().numpy() - lse_ref).max()) <= TOL_LSE
