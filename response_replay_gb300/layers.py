@@ -139,11 +139,13 @@ class _TwoSlotLayers:
     layer's pages serve every unit at HBM speed, and the copy of the next layer runs on
     its own stream while the current layer is replayed.
 
-    Use: ``prefetch(l)`` starts layer l's copy (it waits until the slot's previous layer
-    is released); ``cache(l)`` returns the layer's cache in GPU memory and makes the
-    current stream wait for its copy; ``release(l)`` marks the point on the current
-    stream after which the slot may be overwritten.  Capture writes the host pages
-    directly (``capture``).  Subclasses name the caches and their page pools."""
+    Use: ``prefetch(l)`` starts layer l's copy into slot l % 2 (the copy waits for the
+    work already queued on the current stream and for the release of the slot's previous
+    layer; a slot whose layer was never released is not overwritten: ValueError);
+    ``cache(l)`` returns the layer's cache in GPU memory and makes the current stream wait
+    for its copy; ``release(l)`` marks the point on the current stream after which the
+    slot may be overwritten.  Capture writes the host pages directly (``capture``).
+    Subclasses name the caches and their page pools."""
 
     def __init__(self, host: list, slots: list, device, bytes_per_layer: int):
         self.device = device
@@ -152,7 +154,8 @@ class _TwoSlotLayers:
         self.copy_stream = torch.cuda.Stream(device)
         self.ready = [torch.cuda.Event() for _ in range(2)]
         self.free = [torch.cuda.Event() for _ in range(2)]
-        self.freed = [True, True]        # no release owed before the first copy
+        self.held = [False, False]       # a layer was copied into the slot
+        self.released = [False, False]   # ... and released since (free[s] marks when)
         self.layer_in = [None, None]     # layer held (or being copied) by each slot
         self.bytes_per_layer = bytes_per_layer
 
@@ -178,17 +181,22 @@ class _TwoSlotLayers:
         s = self._slot(layer)
         if self.layer_in[s] == layer:
             return
+        if self.held[s] and not self.released[s]:
+            raise ValueError(f"slot {s} still holds layer {self.layer_in[s]}: release it "
+                             f"before prefetching layer {layer}")
         cs = self.copy_stream
-        # the capture that wrote the host pages, and the slot's last reader, come first
+        # the capture that wrote the host pages and the work queued so far come first, and
+        # the slot's previous layer's last reader (marked by its release)
         cs.wait_stream(torch.cuda.current_stream(self.device))
-        if not self.freed[s]:
+        if self.held[s]:
             cs.wait_event(self.free[s])
         with torch.cuda.stream(cs):
             for dst, src in zip(self._pools(self.slots[s]), self._pools(self.host[layer])):
                 dst.copy_(src, non_blocking=True)
             self.ready[s].record(cs)
         self.layer_in[s] = layer
-        self.freed[s] = False
+        self.held[s] = True
+        self.released[s] = False
 
     def cache(self, layer: int):
         self.prefetch(layer)
@@ -200,7 +208,7 @@ class _TwoSlotLayers:
         s = self._slot(layer)
         if self.layer_in[s] == layer:
             self.free[s].record(torch.cuda.current_stream(self.device))
-            self.freed[s] = True
+            self.released[s] = True
 
 
 class StreamedLayers(_TwoSlotLayers):

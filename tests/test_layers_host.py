@@ -76,3 +76,119 @@ def test_saved_must_match_layers(monkeypatch):
     except ValueError:
         return
     raise AssertionError("mismatched saved list accepted")
+
+
+class _Log:
+    """Records stream / event operations of the two-slot layer cache."""
+
+    def __init__(self):
+        self.ops = []
+
+
+def _fake_cuda(monkeypatch, log):
+    class Event:
+        n = 0
+
+        def __init__(self):
+            Event.n += 1
+            self.name = f"e{Event.n}"
+
+        def record(self, stream=None):
+            log.ops.append(("record", self.name, getattr(stream, "name", "cur")))
+
+    class Stream:
+        def __init__(self, device=None, name="copy"):
+            self.name = name
+
+        def wait_stream(self, other):
+            log.ops.append(("wait_stream", self.name, other.name))
+
+        def wait_event(self, ev):
+            log.ops.append(("wait_event", self.name, ev.name))
+
+    class Ctx:
+        def __init__(self, s):
+            self.s = s
+
+        def __enter__(self):
+            return self.s
+
+        def __exit__(self, *a):
+            return False
+
+    current = Stream(name="cur")
+    monkeypatch.setattr(torch.cuda, "Stream", Stream)
+    monkeypatch.setattr(torch.cuda, "Event", Event)
+    monkeypatch.setattr(torch.cuda, "current_stream", lambda device=None: current)
+    monkeypatch.setattr(torch.cuda, "stream", lambda s: Ctx(s))
+
+
+class _Pool:
+    def __init__(self, log, name):
+        self.log, self.name = log, name
+
+    def copy_(self, src, non_blocking=False):
+        self.log.ops.append(("copy", self.name, src.name))
+
+
+class _Cache:
+    def __init__(self, log, name):
+        self.pool = _Pool(log, name)
+        self.captured = 0
+
+    def capture(self, lat, start_pos=0, stream=None):
+        self.captured += 1
+
+
+def test_two_slot_layers_order_their_copies(monkeypatch):
+    """Layer l goes to slot l % 2; a slot's copy waits for the current stream (the capture
+    and the slot's last reader) and, once the slot has held a layer, for that layer's
+    release; a resident layer is not copied again; a new capture makes its slot stale."""
+    log = _Log()
+    _fake_cuda(monkeypatch, log)
+    host = [_Cache(log, f"host{l}") for l in range(3)]
+    slots = [_Cache(log, f"slot{s}") for s in range(2)]
+
+    class Layers(L._TwoSlotLayers):
+        @staticmethod
+        def _pools(cache):
+            return (cache.pool,)
+
+    st = Layers(host, slots, "cpu", 123)
+    assert len(st) == 3 and st.bytes_per_layer == 123
+    st.prefetch(0)
+    assert ("copy", "slot0", "host0") in log.ops
+    assert ("wait_stream", "copy", "cur") in log.ops
+    assert not any(op[0] == "wait_event" and op[1] == "copy" for op in log.ops)
+    n = len(log.ops)
+    assert st.cache(0) is slots[0]                      # no second copy, a wait for it
+    assert [op for op in log.ops[n:] if op[0] == "copy"] == []
+    assert log.ops[-1][0] == "wait_event" and log.ops[-1][1] == "cur"
+    st.prefetch(1)
+    assert log.ops[-2] == ("copy", "slot1", "host1")
+    st.release(0)
+    release_ev = log.ops[-1][1]
+    assert log.ops[-1][0] == "record" and log.ops[-1][2] == "cur"
+    n = len(log.ops)
+    st.prefetch(2)                                      # reuses slot 0 after its release
+    new = log.ops[n:]
+    assert ("wait_event", "copy", release_ev) in new
+    assert ("copy", "slot0", "host2") in new
+    assert new.index(("wait_event", "copy", release_ev)) < new.index(("copy", "slot0", "host2"))
+    assert st.layer_in == [2, 1]
+    n = len(log.ops)
+    st.prefetch(1)                                      # resident: nothing to do
+    assert log.ops[n:] == []
+    # layer 1 was never released: its slot is not overwritten
+    st._stale(1)                                        # as a new capture into layer 1 does
+    assert st.layer_in == [2, None]
+    try:
+        st.prefetch(1)
+        raise AssertionError("prefetch over an unreleased slot")
+    except ValueError:
+        pass
+    st.layer_in[1] = 1
+    st.release(1)
+    st._stale(1)
+    st.prefetch(1)                                      # stale after a capture: copied again
+    assert log.ops[-2] == ("copy", "slot1", "host1")
