@@ -24,9 +24,11 @@
 // score buffers leave free (values 0-255, the A operand of the first 16 score MMAs) and
 // shared memory (values 256-575, 80 KB).  A stage can be refilled only once P L of its
 // tile is done, and the next score MMAs need it right after, so the producer also
-// prefetches prompt tiles into L2 four tiles ahead (the refills then hit L2).  Prompt
-// tiles are gathered page by page through the page table, and the pages may be pinned
-// host memory read over the host link.
+// prefetches prompt tiles into L2 four tiles ahead (the refills then hit L2).  In a stage
+// the unit's output half (atoms 4h .. 4h+3) sits in the last four 8 KB slots and the
+// other five atoms in the first five, loaded in slot order (measured 3% faster than the
+// atoms in their own order).  Prompt tiles are gathered page by page through the page
+// table, and the pages may be pinned host memory read over the host link.
 //
 // CTA (one per SM, persistent, 8 warps) over the same split-KV schedule as the other
 // replay kernels (ls_sched.h: whole units in waves, tail units cut into pieces whose
@@ -116,6 +118,17 @@ __device__ __forceinline__ void tma_prefetch_l2_2d(const void* tmap, int32_t x, 
                    reinterpret_cast<uint64_t>(tmap)),
                "r"(x), "r"(y)
                : "memory");
+}
+
+// Stage slot of latent atom `at` (values 64 at .. 64 at + 63) for output half h: the half's
+// four atoms in slots 5-8, the others in slots 0-4; atom_in_slot is the inverse.
+__device__ __forceinline__ int slot_of(int h, int at) {
+  if (h == 0) return at >= 4 ? at - 4 : at + 5;
+  return at < 4 ? at : (at == 8 ? 4 : at + 1);
+}
+__device__ __forceinline__ int atom_in_slot(int h, int sl) {
+  if (h == 0) return sl < 5 ? 4 + sl : sl - 5;
+  return sl < 4 ? sl : (sl == 4 ? 8 : sl - 1);
 }
 
 // One latent tile of the walk.
@@ -269,8 +282,9 @@ mla_fwd_kernel(const __grid_constant__ MlaTmaps tm, const LsMlaArgs a,
         const uint32_t dst = sbase + kOffRing + st * kStageBytes;
         mbar_expect_tx(fb, kStageBytes);
         if (r.resp) {
-          for (int at = 0; at < kAtoms; ++at)
-            tma_load_2d(dst + at * kLAtomBytes, &tm.lr, at * 64, r.key0, fb);
+          for (int sl = 0; sl < kAtoms; ++sl)
+            tma_load_2d(dst + sl * kLAtomBytes, &tm.lr, atom_in_slot(r.u & 1, sl) * 64, r.key0,
+                        fb);
         } else {
           for (int bb = 0; bb < kKeys / box_rows; ++bb) {
             const int32_t pos = r.key0 + bb * box_rows;
@@ -282,8 +296,9 @@ mla_fwd_kernel(const __grid_constant__ MlaTmaps tm, const LsMlaArgs a,
               else
                 ls_report(a.err, LS_DEVERR_CHECK);
             }
-            for (int at = 0; at < kAtoms; ++at)
-              tma_load_2d(dst + at * kLAtomBytes + bb * box_rows * 128, &tm.lp, at * 64, y, fb);
+            for (int sl = 0; sl < kAtoms; ++sl)
+              tma_load_2d(dst + sl * kLAtomBytes + bb * box_rows * 128, &tm.lp,
+                          atom_in_slot(r.u & 1, sl) * 64, y, fb);
           }
         }
         if (ragged) {
@@ -320,9 +335,8 @@ mla_fwd_kernel(const __grid_constant__ MlaTmaps tm, const LsMlaArgs a,
       auto issue_pv = [&](const MlaTile& p, uint32_t pstage, uint32_t pg) -> bool {
         if (!mbar_wait(bar(sbase, B_P_FULL + (pg & 1)), (pg >> 1) & 1)) return false;
         tc_fence_after();
-        const uint32_t b0 = sdesc_lo(
-            sbase + kOffRing + pstage * kStageBytes + (uint32_t)(p.u & 1) * 4u * kLAtomBytes,
-            kLAtomBytes);
+        const uint32_t b0 = sdesc_lo(sbase + kOffRing + pstage * kStageBytes + 5u * kLAtomBytes,
+                                     kLAtomBytes);  // slots 5-8: the output half
         const uint32_t a0 = tmem + kColS + (pg & 1) * kKeys;
 #pragma unroll
         for (int kk = 0; kk < kKeys / 16; ++kk)  // 16 latent rows per MMA
@@ -348,15 +362,16 @@ mla_fwd_kernel(const __grid_constant__ MlaTmaps tm, const LsMlaArgs a,
         // S(g): its buffer last held P(g - 2), whose P L was issued before this
         const uint32_t b0 = sdesc_lo(sbase + kOffRing + ks.stage * kStageBytes, 16);
         const uint32_t d = tmem + kColS + (g & 1) * kKeys;
+        const int h = r.u & 1;
 #pragma unroll
         for (int kk = 0; kk < 4 * kQtAtoms; ++kk) {  // Q values 0-255 from tensor memory
-          const uint32_t ob = ((kk >> 2) * kLAtomBytes + (kk & 3) * 32) >> 4;
+          const uint32_t ob = (slot_of(h, kk >> 2) * kLAtomBytes + (kk & 3) * 32) >> 4;
           mma_ts_lo(d, tmem + kColQ + kk * 8, b0 + ob, idS, kk > 0);
         }
 #pragma unroll
         for (int kk = 4 * kQtAtoms; kk < 4 * kAtoms; ++kk) {  // values 256-575 from shared
           const uint32_t oa = (((kk >> 2) - kQtAtoms) * kQAtomBytes + (kk & 3) * 32) >> 4;
-          const uint32_t ob = ((kk >> 2) * kLAtomBytes + (kk & 3) * 32) >> 4;
+          const uint32_t ob = (slot_of(h, kk >> 2) * kLAtomBytes + (kk & 3) * 32) >> 4;
           mma_ss_lo(d, q_lo + oa, b0 + ob, idS, 1u);
         }
         mma_commit(bar(sbase, B_S_FULL + (g & 1)));
