@@ -46,6 +46,11 @@ constexpr int kThreads = 384;
 // 128-column S row per thread) rise to 192: 128 x 112 + 256 x 192 = 63488 <= 64512.
 constexpr int kRegsLaunch = 168, kRegsControl = 112, kRegsSoftmax = 192;
 static_assert(128 * kRegsControl + 256 * kRegsSoftmax <= kThreads * kRegsLaunch, "register split");
+// The packed-members layout (member masks in the softmax) spills at 192; it takes 200 and
+// leaves 96 to the control warps: 128 x 96 + 256 x 200 = 63488.
+template <int kMode> constexpr int regs_control() { return kMode == 2 ? 96 : kRegsControl; }
+template <int kMode> constexpr int regs_softmax() { return kMode == 2 ? 200 : kRegsSoftmax; }
+static_assert(128 * 96 + 256 * 200 <= kThreads * kRegsLaunch, "register split (members)");
 constexpr uint32_t kTileBytes = kTile * kD * 2;  // 32 KB
 constexpr uint32_t kHalfBytes = kTileBytes / 2;  // 16 KB: 128 rows x 64 dims
 constexpr uint32_t kOffQ = 0;                    // Q_A, Q_B
@@ -146,7 +151,7 @@ replay_fwd_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a,
   };
 
   if (warp < 4) {
-  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsControl));
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(regs_control<kMode>()));
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
@@ -344,7 +349,7 @@ replay_fwd_tc_kernel(const __grid_constant__ TmapSet tm, const LsAttnArgs a,
     }
   }
   } else {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(regs_softmax<kMode>()));
     // ------------------------------------------------------------ softmax warpgroups
     const int t = (warp - 4) >> 2;         // tile A (0) or B (1)
     const bool tile_used = t < a.tiles;    // one-tile units leave tile B's warps idle
