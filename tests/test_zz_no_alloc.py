@@ -129,3 +129,31 @@ def test_noalloc_rejects_sizes_beyond_its_scratch(cuda):
                                            0.2, 1e-6, 1, 0, f.data_ptr(), logits.data_ptr(), None,
                                            None, 0)
         assert ei.value.status == B.LS_ERR_WORKSPACE
+
+
+def test_noalloc_call_captured_in_a_cuda_graph(cuda):
+    """After one eager call (which looks up the scratch array on this device), the call
+    can be captured in a CUDA graph; replaying the graph gives bit-identical outputs to an
+    eager call on the same inputs."""
+    lens = [40, 25, 63]
+    inp = syn.make_grpo(lens, 2048, "bf16", "normal", 4242, cuda, shift_frac=0.3)
+    logp_old = inp.noise.contiguous()
+    T = sum(lens)
+    outs = [(torch.zeros(1, device=cuda), torch.empty_like(inp.logits),
+             torch.empty(T, device=cuda), torch.empty(4, device=cuda)) for _ in range(2)]
+    _noalloc(inp, logp_old, 0, 3, 0.2, *outs[0])          # eager (first call on the device)
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(graph, stream=s):
+            _noalloc(inp, logp_old, 0, 3, 0.2, *outs[1])
+    torch.cuda.current_stream().wait_stream(s)
+    for t in outs[1]:
+        t.fill_(float("nan"))                              # every output is written anew
+    graph.replay()
+    torch.cuda.synchronize()
+    assert B.ls_last_device_error(0) == B.LS_OK
+    for a, b in zip(outs[0], outs[1]):
+        assert torch.equal(a, b)
