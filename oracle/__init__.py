@@ -62,11 +62,15 @@ def lib():
         l.lso_gdn_bwd.argtypes = [P, P, i32, P, P, P, P, P, P]
         l.lso_mla_fwd.argtypes = [P, P, P]
         l.lso_mla_fwd_rows.argtypes = [P, i32, P, P, P, P]
+        l.lso_mla_bwd.argtypes = [P, P, P, P]
+        l.lso_mla_bwd_dq_rows.argtypes = [P, P, i32, P, P, P]
+        l.lso_mla_bwd_dlat_keys.argtypes = [P, P, i32, P, P]
         l.lso_num_threads.argtypes = []
         for f in ("lso_capture_kv", "lso_attn_fwd", "lso_attn_fwd_rows", "lso_attn_bwd",
                   "lso_attn_bwd_dq_rows", "lso_attn_bwd_dkdv_keys", "lso_grpo",
                   "lso_grpo_dlogits_row", "lso_grpo_logp", "lso_gdn_fwd", "lso_gdn_bwd",
-                  "lso_mla_fwd", "lso_mla_fwd_rows", "lso_num_threads"):
+                  "lso_mla_fwd", "lso_mla_fwd_rows", "lso_mla_bwd", "lso_mla_bwd_dq_rows",
+                  "lso_mla_bwd_dlat_keys", "lso_num_threads"):
             getattr(l, f).restype = C.c_int
         _lib = l
     return _lib
@@ -441,3 +445,39 @@ def mla_fwd_rows(pb: MlaProblem, ts, hs):
     _check(lib().lso_mla_fwd_rows(C.byref(st), len(ts), _ptr(ts), _ptr(hs), _ptr(o),
                                   _ptr(lse)), "mla_fwd_rows")
     return o, lse
+
+
+def mla_bwd(pb: MlaProblem, d_o):
+    """dq [R][H][D] and d lat [R][D] (the response's own rows; prompt rows stopgrad), fp64.
+    d_o: bf16 bits (uint16) [R][H][d_c]."""
+    R, H, D = pb.q.shape
+    d_o = np.ascontiguousarray(d_o, dtype=np.uint16)
+    assert d_o.shape == (R, H, pb.d_c)
+    st, keep = pb._struct()
+    dq = np.zeros((R, H, D), np.float64)
+    dlat = np.zeros((R, D), np.float64)
+    _check(lib().lso_mla_bwd(C.byref(st), _ptr(d_o), _ptr(dq), _ptr(dlat)), "mla_bwd")
+    return dq, dlat
+
+
+def mla_bwd_dq_rows(pb: MlaProblem, d_o, ts, hs):
+    """dq [n][D] for the rows (ts[i], hs[i])."""
+    ts = np.ascontiguousarray(ts, dtype=np.int32)
+    hs = np.ascontiguousarray(hs, dtype=np.int32)
+    d_o = np.ascontiguousarray(d_o, dtype=np.uint16)
+    st, keep = pb._struct()
+    dq = np.zeros((len(ts), pb.q.shape[2]), np.float64)
+    _check(lib().lso_mla_bwd_dq_rows(C.byref(st), _ptr(d_o), len(ts), _ptr(ts), _ptr(hs),
+                                     _ptr(dq)), "mla_bwd_dq_rows")
+    return dq
+
+
+def mla_bwd_dlat_keys(pb: MlaProblem, d_o, js):
+    """d lat [n][D] for the response rows js[i]."""
+    js = np.ascontiguousarray(js, dtype=np.int32)
+    d_o = np.ascontiguousarray(d_o, dtype=np.uint16)
+    st, keep = pb._struct()
+    dl = np.zeros((len(js), pb.q.shape[2]), np.float64)
+    _check(lib().lso_mla_bwd_dlat_keys(C.byref(st), _ptr(d_o), len(js), _ptr(js), _ptr(dl)),
+           "mla_bwd_dlat_keys")
+    return dl

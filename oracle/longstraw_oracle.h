@@ -59,6 +59,11 @@
  *                           whole row and V the row with its rotary part zeroed; one page
  *                           with the identity table equals shuffled pages
  *   lso_mla_fwd_rows        equals lso_mla_fwd on the sampled rows
+ *   lso_mla_bwd             central finite differences of <dO, O> through lso_mla_fwd
+ *                           (steps exact in bf16); one key: dq = 0 and d lat = [dO ; 0]
+ *                           summed over the heads
+ *   lso_mla_bwd_dq_rows,
+ *   lso_mla_bwd_dlat_keys   equal lso_mla_bwd on the sampled rows / keys
  */
 #ifndef LONGSTRAW_ORACLE_H
 #define LONGSTRAW_ORACLE_H
@@ -216,6 +221,18 @@ int lso_mla_fwd(const lso_mla* a, double* o, double* lse);
 /* The same for the listed (t, h) rows only: o [n][d_c], lse [n]. */
 int lso_mla_fwd_rows(const lso_mla* a, int32_t n, const int32_t* ts, const int32_t* hs,
                      double* o, double* lse);
+
+/* Backward with the prompt rows stopgrad; d_o: bf16 [R][H][d_c].  dq [R][H][d_c + d_r];
+ * dlat [R][d_c + d_r], the gradient of the response's own rows. */
+int lso_mla_bwd(const lso_mla* a, const uint16_t* d_o, double* dq, double* dlat);
+
+/* dq of the listed (t, h) rows only: dq [n][d_c + d_r]. */
+int lso_mla_bwd_dq_rows(const lso_mla* a, const uint16_t* d_o, int32_t n, const int32_t* ts,
+                        const int32_t* hs, double* dq);
+
+/* d lat of the listed response rows only: dlat [n][d_c + d_r]. */
+int lso_mla_bwd_dlat_keys(const lso_mla* a, const uint16_t* d_o, int32_t n, const int32_t* js,
+                          double* dlat);
 
 #ifdef __cplusplus
 }

@@ -123,3 +123,78 @@ def test_rows_sampler_and_bad_page():
     with pytest.raises(ValueError):
         oracle.mla_fwd(oracle.MlaProblem(pb.lat_pool, bad, P, pb.q, pb.lat_resp, pb.scale,
                                          d_c=d_c))
+
+
+# ----------------------------------------------------------------------------- backward
+# Pins of lso_mla_bwd: central finite differences of L = <dO, O> through the forward
+# oracle (pinned above), with steps that are exact in bf16 so the perturbed inputs are
+# what the forward reads; and the one-key closed form.  A dropped D term, a missing
+# scale, the value term of d lat missing or leaking into the rotary part, a wrong causal
+# bound on d lat, or a gradient given to the prompt rows fails at least one of them.
+
+def _loss(pb, g):
+    o, _ = oracle.mla_fwd(pb)
+    return float((o * bf16_value(g)).sum())
+
+
+def _fd(pb, g, arr, idx):
+    """Richardson-extrapolated central difference of L in arr[idx], taken at the value 1.0
+    (set beforehand), with steps 1/64 and 1/128 (1 +- h exact in bf16)."""
+    def central(h):
+        arr[idx] = bf16_bits(np.array([1.0 + h]))[0]
+        lp = _loss(pb, g)
+        arr[idx] = bf16_bits(np.array([1.0 - h]))[0]
+        lm = _loss(pb, g)
+        arr[idx] = bf16_bits(np.array([1.0]))[0]
+        return (lp - lm) / (2 * h)
+    d1, d2 = central(1 / 64), central(1 / 128)
+    return (4 * d2 - d1) / 3
+
+
+@pytest.mark.parametrize("P,R,H,d_c,d_r,ps", [(23, 4, 2, 8, 4, 8), (0, 5, 3, 6, 2, 4)])
+def test_bwd_matches_finite_differences(P, R, H, d_c, d_r, ps):
+    pb, _ = latent_problem(P, R, H, d_c, d_r, ps, seed=77 + P + R, scale=0.3)
+    rng = np.random.default_rng(5 + P)
+    g = bf16_bits(rng.standard_normal((R, H, d_c)))
+    D = d_c + d_r
+    probes_q = [(R - 1, H - 1, D - 1), (0, 0, 0), (R // 2, 1 % H, d_c), (R - 1, 0, d_c - 1)]
+    probes_l = [(0, 0), (0, D - 1), (R - 1, 1), (R // 2, d_c), (R - 2, d_c - 1)]
+    for (t, h, d) in probes_q:
+        pb.q[t, h, d] = bf16_bits(np.array([1.0]))[0]
+    for (j, d) in probes_l:
+        pb.lat_resp[j, d] = bf16_bits(np.array([1.0]))[0]
+    dq, dlat = oracle.mla_bwd(pb, g)
+    scale_q = np.abs(dq).max()
+    scale_l = np.abs(dlat).max()
+    for (t, h, d) in probes_q:
+        fd = _fd(pb, g, pb.q, (t, h, d))
+        assert abs(fd - dq[t, h, d]) <= 1e-6 * scale_q + 1e-5 * abs(fd), ((t, h, d), fd, dq[t, h, d])
+    for (j, d) in probes_l:
+        fd = _fd(pb, g, pb.lat_resp, (j, d))
+        assert abs(fd - dlat[j, d]) <= 1e-6 * scale_l + 1e-5 * abs(fd), ((j, d), fd, dlat[j, d])
+
+
+def test_bwd_one_key_closed_form():
+    """A one-token response over an empty prompt attends only to its own row: P = 1, so
+    dS = 0, dq = 0, and the row's gradient is the heads' dO summed (value role only)."""
+    H, d_c, d_r = 4, 10, 6
+    pb, _ = latent_problem(0, 1, H, d_c, d_r, 8, seed=11)
+    g = bf16_bits(np.random.default_rng(2).standard_normal((1, H, d_c)))
+    dq, dlat = oracle.mla_bwd(pb, g)
+    np.testing.assert_allclose(dq, 0.0, rtol=0, atol=1e-12)
+    want = np.concatenate([bf16_value(g)[0].sum(0), np.zeros(d_r)])
+    np.testing.assert_allclose(dlat[0], want, rtol=0, atol=1e-12)
+
+
+def test_bwd_rows_and_keys_match_full():
+    P, R, H, d_c, d_r, ps = 41, 7, 3, 12, 4, 16
+    pb, _ = latent_problem(P, R, H, d_c, d_r, ps, seed=19)
+    g = bf16_bits(np.random.default_rng(3).standard_normal((R, H, d_c)))
+    dq, dlat = oracle.mla_bwd(pb, g)
+    ts = np.array([0, R - 1, 3, 3], np.int32)
+    hs = np.array([0, H - 1, 1, 2], np.int32)
+    np.testing.assert_allclose(oracle.mla_bwd_dq_rows(pb, g, ts, hs), dq[ts, hs], rtol=0,
+                               atol=1e-13)
+    js = np.array([R - 1, 0, 4], np.int32)
+    np.testing.assert_allclose(oracle.mla_bwd_dlat_keys(pb, g, js), dlat[js], rtol=0,
+                               atol=1e-12)
