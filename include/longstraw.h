@@ -19,6 +19,8 @@
  *                          advantages and its logits gradient
  *   ls_mla_replay_fwd      the forward over latent (MLA-style) pages, which may be
  *                          held in host memory
+ *   ls_mla_replay_bwd      its backward: dq, and the gradient of the response's own
+ *                          latent rows (the prompt rows are stopgrad)
  *
  * Conventions shared by every call
  *   - Memory: every pointer argument is DEVICE memory on the current CUDA device unless
@@ -365,7 +367,22 @@ ls_status ls_gdn_replay_bwd(const float* state0, const void* q, const void* k, c
  * beyond rounding.  softmax_scale finite and > 0.  R == 0 is a no-op; P == 0 is causal
  * attention over the response rows.  Inputs must be finite (a row past a query's
  * causal bound has weight zero, and zero times a non-finite value is not zero).
- * LS_ERR_UNSUPPORTED when R x H >= 2^31.  No backward is provided. */
+ * LS_ERR_UNSUPPORTED when R x H >= 2^31.
+ *
+ * ls_mla_replay_bwd: the backward of ls_mla_replay_fwd with the prompt rows stopgrad
+ * (LongStraw paper digest, Method, last paragraph: the captured state takes no
+ * gradient).  With P = exp(s - lse), D_{t,h} = <dO_{t,h}, o_{t,h}>, dP_j = <dO, c_j> and
+ * dS = P (dP - D):
+ *   dq_{t,h} = softmax_scale sum_j dS_{t,h,j} [c_j ; r_j]     (all visible rows j)
+ *   dlat_j   = sum_{t >= j} sum_h ( P_{t,h,j} [dO_{t,h} ; 0] + softmax_scale dS_{t,h,j} q_{t,h} )
+ * for the response's own rows j (the latent is both key and value; its rotary part is a
+ * key only).  q, lat_resp, R, H, softmax_scale and the cache as for the forward; o
+ * (bf16 [R][H][512]) and lse (fp32 [R][H]) are the forward's outputs, d_o bf16
+ * [R][H][512].  dq: fp32 [R][H][576]; dlat: fp32 [R][576]; both overwritten.
+ * num_splits (>= 1) cuts the prompt into ranges of 32-row tiles whose partial dq are
+ * added in a fixed order (the result does not depend on it beyond rounding; a given
+ * split count gives the same bits every call).  Workspace from
+ * ls_mla_replay_bwd_workspace (never zero for R > 0).  R == 0 is a no-op. */
 typedef struct {
   void* pool;
   const int32_t* page_table;
@@ -383,6 +400,12 @@ ls_status ls_mla_replay_fwd(const ls_latent_cache* cache, const void* q, const v
                             int R, int H, float softmax_scale, int num_splits, void* o,
                             float* lse, void* workspace, size_t workspace_bytes,
                             ls_stream_t stream);
+ls_status ls_mla_replay_bwd_workspace(const ls_latent_cache* cache, int R, int H, int num_splits,
+                                      size_t* bytes);
+ls_status ls_mla_replay_bwd(const ls_latent_cache* cache, const void* q, const void* lat_resp,
+                            const void* o, const float* lse, const void* d_o, int R, int H,
+                            float softmax_scale, int num_splits, float* dq, float* dlat,
+                            void* workspace, size_t workspace_bytes, ls_stream_t stream);
 
 /* ---------------------------------------------------------------- checks
  * ls_validate_page_table: enqueue a check that every entry of the page table covering

@@ -30,6 +30,7 @@ EXPORTED = (
     "ls_gdn_replay_bwd", "ls_replay_attn_fwd_ragged_workspace", "ls_replay_attn_fwd_ragged",
     "ls_replay_attn_bwd_ragged_workspace", "ls_replay_attn_bwd_ragged",
     "ls_capture_latent", "ls_mla_replay_fwd_workspace", "ls_mla_replay_fwd",
+    "ls_mla_replay_bwd_workspace", "ls_mla_replay_bwd",
 )
 
 
@@ -74,6 +75,8 @@ def lib() -> C.CDLL:
             "ls_capture_latent": [lcache, P, i64, i64, P],
             "ls_mla_replay_fwd_workspace": [lcache, i32, i32, i32, szp],
             "ls_mla_replay_fwd": [lcache, P, P, i32, i32, f32, i32, P, P, P, sz, P],
+            "ls_mla_replay_bwd_workspace": [lcache, i32, i32, i32, szp],
+            "ls_mla_replay_bwd": [lcache, P, P, P, P, P, i32, i32, f32, i32, P, P, P, sz, P],
             "ls_capture_kv": [cache, P, P, i64, i64, P],
             "ls_replay_attn_fwd_workspace": [cache, i32, i32, i32, szp],
             "ls_replay_attn_fwd": [cache, P, P, P, i32, i32, f32, i32, P, P, P, sz, P],
@@ -279,6 +282,18 @@ def ls_mla_replay_fwd(cache: ls_latent_cache, q: int, lat_resp: int, R: int, H: 
     _ok("ls_mla_replay_fwd",
         lib().ls_mla_replay_fwd(C.byref(cache), q, lat_resp, R, H, softmax_scale, num_splits, o,
                                 lse, workspace, workspace_bytes, stream))
+
+
+def ls_mla_replay_bwd_workspace(cache: ls_latent_cache, R: int, H: int, num_splits: int) -> int:
+    return _size("ls_mla_replay_bwd_workspace", C.byref(cache), R, H, num_splits)
+
+
+def ls_mla_replay_bwd(cache: ls_latent_cache, q: int, lat_resp: int, o: int, lse: int, d_o: int,
+                      R: int, H: int, softmax_scale: float, num_splits: int, dq: int, dlat: int,
+                      workspace: int, workspace_bytes: int, stream: int = 0) -> None:
+    _ok("ls_mla_replay_bwd",
+        lib().ls_mla_replay_bwd(C.byref(cache), q, lat_resp, o, lse, d_o, R, H, softmax_scale,
+                                num_splits, dq, dlat, workspace, workspace_bytes, stream))
 
 
 def _lens(lens) -> tuple:

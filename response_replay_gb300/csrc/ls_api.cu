@@ -736,6 +736,29 @@ ls_status mla_sched(const ls_latent_cache* c, int R, int H, int num_splits, LsSc
   return LS_OK;
 }
 
+// Backward units: (row tile of 64 (t, h) rows) x (part of the 576 dq columns).  Workspace:
+// D per row, partial dq of tail-unit pieces, partial d lat of units cut between CTAs.
+ls_status mla_bwd_sched(const ls_latent_cache* c, int R, int H, int num_splits, LsSched* sc,
+                        size_t* off_pdq, size_t* off_pdl, size_t* total, int* sms) {
+  if (R < 0 || H <= 0 || num_splits < 1) return LS_ERR_INVALID_ARG;
+  const int64_t rows = (int64_t)R * H;
+  const int64_t units = 2 * ((rows + ls_mla_bwd_unit_rows() - 1) / ls_mla_bwd_unit_rows());
+  if (rows >= (1ll << 31) || units >= (1ll << 30)) return LS_ERR_UNSUPPORTED;
+  DevInfo d;
+  const ls_status s = dev_info(&d);
+  if (s != LS_OK) return s;
+  const int tile = ls_mla_bwd_tile();
+  *sc = ls_make_sched((int)units, (int)((c->num_tokens + tile - 1) / tile), num_splits, d.sms);
+  const size_t pieces = sc->has_partials() ? (size_t)sc->num_pieces() : 0;
+  const size_t pc = (size_t)ls_mla_bwd_part_cols();
+  *off_pdq = align256((size_t)rows * sizeof(float));
+  *off_pdl = *off_pdq + align256(pieces * ls_mla_bwd_unit_rows() * pc * sizeof(float));
+  *total = *off_pdl +
+           align256((size_t)2 * ls_mla_bwd_dlat_ctas(R, H, d.sms) * 128 * pc * sizeof(float));
+  *sms = d.sms;
+  return LS_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -800,6 +823,61 @@ ls_status ls_mla_replay_fwd(const ls_latent_cache* cache, const void* q, const v
   a.part_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) + pl);
   a.err = d.err;
   return from_cuda(ls_launch_mla_fwd(a, sc, (cudaStream_t)stream));
+}
+
+ls_status ls_mla_replay_bwd_workspace(const ls_latent_cache* cache, int R, int H, int num_splits,
+                                      size_t* bytes) {
+  ls_status s = check_latent(cache);
+  if (s != LS_OK) return s;
+  if (!bytes) return LS_ERR_INVALID_ARG;
+  LsSched sc;
+  size_t a, b;
+  int sms;
+  return mla_bwd_sched(cache, R, H, num_splits, &sc, &a, &b, bytes, &sms);
+}
+
+ls_status ls_mla_replay_bwd(const ls_latent_cache* cache, const void* q, const void* lat_resp,
+                            const void* o, const float* lse, const void* d_o, int R, int H,
+                            float softmax_scale, int num_splits, float* dq, float* dlat,
+                            void* workspace, size_t workspace_bytes, ls_stream_t stream) {
+  ls_status s = check_latent(cache);
+  if (s != LS_OK) return s;
+  if (!isfinite(softmax_scale) || !(softmax_scale > 0.f)) return LS_ERR_INVALID_ARG;
+  LsSched sc;
+  size_t off_pdq, off_pdl, total;
+  int sms;
+  if ((s = mla_bwd_sched(cache, R, H, num_splits, &sc, &off_pdq, &off_pdl, &total, &sms)) != LS_OK)
+    return s;
+  if (R == 0) return LS_OK;
+  const void* ptrs[] = {q, lat_resp, o, lse, d_o, dq, dlat};
+  for (const void* p : ptrs)
+    if (!p || !aligned16(p)) return LS_ERR_INVALID_ARG;
+  if (!workspace || workspace_bytes < total || !aligned16(workspace)) return LS_ERR_WORKSPACE;
+  DevInfo d;
+  if ((s = dev_info(&d)) != LS_OK) return s;
+  LsMlaBwdArgs a;
+  a.pool = cache->pool;
+  a.page_table = cache->page_table;
+  a.num_pages = cache->num_pages;
+  a.ps_log2 = ilog2_exact(cache->page_size);
+  a.P = cache->num_tokens;
+  a.q = q;
+  a.lat_resp = lat_resp;
+  a.o = o;
+  a.lse = lse;
+  a.d_o = d_o;
+  a.R = R;
+  a.H = H;
+  a.scale = softmax_scale;
+  a.scale_log2 = softmax_scale * 1.4426950408889634f;
+  char* ws = static_cast<char*>(workspace);
+  a.delta = reinterpret_cast<float*>(ws);
+  a.dq = dq;
+  a.dlat = dlat;
+  a.part_dq = reinterpret_cast<float*>(ws + off_pdq);
+  a.part_dlat = reinterpret_cast<float*>(ws + off_pdl);
+  a.err = d.err;
+  return from_cuda(ls_launch_mla_bwd(a, sc, sms, (cudaStream_t)stream));
 }
 
 ls_status ls_selftest_wait_timeout(ls_stream_t stream) {

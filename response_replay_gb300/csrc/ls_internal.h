@@ -183,3 +183,29 @@ cudaError_t ls_launch_mla_fwd(const LsMlaArgs& a, const LsSched& sc, cudaStream_
 cudaError_t ls_launch_capture_latent(const void* src, void* pool, const int32_t* page_table,
                                      int32_t num_pages, int32_t ps_log2, int64_t start,
                                      int64_t n, int sms, uint32_t* err, cudaStream_t st);
+
+// Latent replay backward (mla_replay_bwd.cu).
+struct LsMlaBwdArgs {
+  const void* pool;           // bf16 [num_pages][page_size][576]
+  const int32_t* page_table;  // [ceil(P / page_size)]
+  int32_t num_pages, ps_log2;
+  int64_t P;
+  const void* q;              // bf16 [R][H][576]
+  const void* lat_resp;       // bf16 [R][576]
+  const void* o;              // bf16 [R][H][512], the forward's output
+  const float* lse;           // [R][H]
+  const void* d_o;            // bf16 [R][H][512]
+  int32_t R, H;
+  float scale, scale_log2;
+  float* delta;               // [R][H]: <dO, o>
+  float* dq;                  // [R][H][576]
+  float* dlat;                // [R][576]
+  float* part_dq;             // [pieces][64][320] partials of tail-unit pieces
+  float* part_dlat;           // [2 x d lat CTAs][128][320]
+  uint32_t* err;
+};
+int ls_mla_bwd_tile();
+int ls_mla_bwd_unit_rows();
+int ls_mla_bwd_part_cols();
+int ls_mla_bwd_dlat_ctas(int32_t R, int32_t H, int sms);
+cudaError_t ls_launch_mla_bwd(const LsMlaBwdArgs& a, const LsSched& sc, int sms, cudaStream_t st);

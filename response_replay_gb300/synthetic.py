@@ -211,6 +211,7 @@ def make_gdn(R: int, H: int, seed: int, device="cpu", d: int = HEAD_DIM,
 
 
 LATENT_ROW = 576   # latent (512) + rotary key (64) values per position
+LATENT_DIM = 512   # latent values (the output width)
 
 
 @dataclass
@@ -227,6 +228,7 @@ class LatentBranch:
     """One response branch of a latent-attention layer."""
     q: torch.Tensor            # [R][H][576] bf16 absorbed queries
     lat: torch.Tensor          # [R][576] bf16 the response's own rows
+    d_o: torch.Tensor          # [R][H][512] bf16 output gradient
 
 
 def make_latent_prompt(P: int, page_size: int, seed: int, device="cpu",
@@ -243,9 +245,10 @@ def make_latent_prompt(P: int, page_size: int, seed: int, device="cpu",
 
 def make_latent_branch(R: int, H: int, seed: int, device="cpu", sharp: bool = False) -> LatentBranch:
     """Rows ~ N(0,1); queries N(0,1) (sharp: scores of spread ~1.7 at scale 1/sqrt(192))
-    or N(0,1)/sqrt(576) (near-uniform)."""
+    or N(0,1)/sqrt(576) (near-uniform); output gradient N(0,1), drawn last."""
     g = gen(device, seed)
     qs = 1.0 if sharp else LATENT_ROW ** -0.5
     q = (torch.randn(R, H, LATENT_ROW, generator=g, device=device) * qs).to(torch.bfloat16)
     lat = torch.randn(R, LATENT_ROW, generator=g, device=device).to(torch.bfloat16)
-    return LatentBranch(q, lat)
+    d_o = torch.randn(R, H, LATENT_DIM, generator=g, device=device).to(torch.bfloat16)
+    return LatentBranch(q, lat, d_o)

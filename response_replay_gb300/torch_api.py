@@ -404,3 +404,30 @@ def mla_replay_fwd(cache: LatentCache, q: torch.Tensor, lat_resp: torch.Tensor,
                         num_splits, o.data_ptr(), lse.data_ptr(), ws.data_ptr(), ws.numel(),
                         _stream(stream))
     return o, lse
+
+
+def mla_replay_bwd(cache: LatentCache, q: torch.Tensor, lat_resp: torch.Tensor, o: torch.Tensor,
+                   lse: torch.Tensor, d_o: torch.Tensor, softmax_scale: float, num_splits: int,
+                   dq: torch.Tensor | None = None, dlat: torch.Tensor | None = None, stream=None):
+    """Backward of mla_replay_fwd with the prompt rows stopgrad: o, lse from the forward,
+    d_o [R][H][512] bf16 -> dq [R][H][576] and dlat [R][576] (fp32, the gradient of the
+    response's own rows)."""
+    R, H, _ = q.shape
+    _check(q, "q", torch.bfloat16, (R, H, LATENT_ROW))
+    _check(lat_resp, "lat_resp", torch.bfloat16, (R, LATENT_ROW))
+    _check(o, "o", torch.bfloat16, (R, H, LATENT_DIM))
+    _check(lse, "lse", torch.float32, (R, H))
+    _check(d_o, "d_o", torch.bfloat16, (R, H, LATENT_DIM))
+    if dq is None:
+        dq = torch.empty((R, H, LATENT_ROW), dtype=torch.float32, device=q.device)
+    if dlat is None:
+        dlat = torch.empty((R, LATENT_ROW), dtype=torch.float32, device=q.device)
+    _check(dq, "dq", torch.float32, (R, H, LATENT_ROW))
+    _check(dlat, "dlat", torch.float32, (R, LATENT_ROW))
+    nbytes = B.ls_mla_replay_bwd_workspace(cache.struct, R, H, num_splits)
+    ws = workspace(nbytes, q.device, "mla_bwd")
+    B.ls_mla_replay_bwd(cache.struct, q.data_ptr(), lat_resp.data_ptr(), o.data_ptr(),
+                        lse.data_ptr(), d_o.data_ptr(), R, H, softmax_scale, num_splits,
+                        dq.data_ptr(), dlat.data_ptr(), ws.data_ptr(), ws.numel(),
+                        _stream(stream))
+    return dq, dlat
