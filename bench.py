@@ -862,6 +862,23 @@ def mla_flops(P: int, R: int, H: int) -> tuple[float, float]:
     return pairs * 2 * (MLA_ROW + MLA_DC), pairs * 2 * (2 * MLA_ROW + MLA_DC)
 
 
+def mla_bwd_flops(P: int, R: int, H: int) -> tuple[float, float]:
+    """(algorithmic, executed) FLOPs of one latent replay backward.  Algorithmic: per
+    (query row, visible key) 2 x (576 score + 512 dP + 576 dq); per (query row, response
+    key j <= t) 2 x (512 + 576) for the response row's gradient.  Executed on the tensor
+    pipe: the dq kernel's stacked 128-lane products cost 2 x (2 x 576 + 320 + 256) per
+    (row, key) and run once per dq part for S|dP; the response-row kernel walks 128-key
+    tiles over 16-row blocks from each tile's first token, 2 x (2 x 2 x 576 + 576 + 512)
+    per walked (row, key)."""
+    pairs = R * H * (P + (R + 1) / 2)
+    resp_pairs = R * H * (R + 1) / 2
+    alg = pairs * 2 * (2 * MLA_ROW + MLA_DC) + resp_pairs * 2 * (MLA_ROW + MLA_DC)
+    rb_hi = -(-R * H // 16)
+    walked = sum(128 * 16 * (rb_hi - 8 * kt * H) for kt in range(-(-R // 128)))
+    exe = pairs * 2 * 2 * (2 * MLA_ROW + 320 + 256) + walked * 2 * (4 * MLA_ROW + MLA_ROW + MLA_DC)
+    return alg, exe
+
+
 def run_mla_sweep(args, local_rank: int):
     """Supplementary, labelled lines (not the headline): the latent (MLA-style) replay
     forward over a prompt of P (default 2,097,152) 576-value latent rows (256-row pages,
@@ -928,6 +945,18 @@ def run_mla_sweep(args, local_rank: int):
                          f"{name}_tflops": alg / (ms * 1e-3) / 1e12,
                          f"{name}_executed_tflops": exe / (ms * 1e-3) / 1e12,
                          f"{name}_latent_gbs": lat_bytes / (ms * 1e-3) / 1e9})
+        if args.mla_bwd:
+            d_o = br.d_o
+            dq = torch.empty((R, H, MLA_ROW), dtype=torch.float32, device=dev)
+            dl = torch.empty((R, MLA_ROW), dtype=torch.float32, device=dev)
+            api.mla_replay_fwd(dcache, br.q, br.lat, scale, splits, o=o, lse=lse, stream=stream)
+            ms = timed(lambda: api.mla_replay_bwd(dcache, br.q, br.lat, o, lse, d_o, scale,
+                                                  splits, dq=dq, dlat=dl, stream=stream),
+                       args.steps)
+            alg, exe = mla_bwd_flops(P, R, H)
+            line.update({"hbm_bwd_ms": ms, "hbm_bwd_tflops": alg / (ms * 1e-3) / 1e12,
+                         "hbm_bwd_executed_tflops": exe / (ms * 1e-3) / 1e12,
+                         "bwd_executed_frac_of_bf16_burst": exe / (ms * 1e-3) / 1e12 / peak})
         line.update({"executed_frac_of_bf16_burst": line["hbm_executed_tflops"] / peak,
                      "peak": f"{pk_src} bf16 burst {peak}", "h2d_copy_gbs": h2d_gbs,
                      "steps": args.steps, "warmup": args.warmup})
@@ -1329,6 +1358,8 @@ def main():
     ap.add_argument("--sweep-mla", default=None,
                     help="comma-separated response lengths: supplementary latent (MLA-style) "
                          "replay lines instead of the headline step")
+    ap.add_argument("--mla-bwd", action="store_true",
+                    help="with --sweep-mla: also time the latent replay backward (HBM pool)")
     ap.add_argument("--sweep-mla-layers", type=int, default=0,
                     help="number of latent-attention layers: supplementary line with their "
                          "pages streamed from pinned host memory against held in HBM")

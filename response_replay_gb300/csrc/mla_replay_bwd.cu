@@ -572,6 +572,7 @@ constexpr int kKT = 128;                  // response latent rows per unit (M)
 constexpr int kNB = 16;                   // query rows per iteration
 constexpr int kN2 = 2 * kNB;              // stacked: Q rows 0-15, dO rows 16-31
 constexpr int kRStages = 2;
+constexpr int kMinIters = 16;             // fewest iterations a CTA of the walk takes
 constexpr uint32_t kLTAtomBytes = kKT * 128;                     // 16 KB
 constexpr uint32_t kLTBytes = kAtoms * kLTAtomBytes;             // 144 KB
 constexpr uint32_t kRAtomBytes = kN2 * 128;                      // 4 KB
@@ -629,8 +630,10 @@ DlatGeom make_dlat_geom(int32_t R, int32_t H, int sms) {
   g.ctas = 1;
   g.total = 0;
   g.total = g.unit_begin(2 * g.nkt);
+  // at least kMinIters iterations per CTA: a thinner slice costs more in its latent tile
+  // load and in the partial sums it leaves than it saves
   int64_t c = sms;
-  if (c > g.total) c = g.total;
+  if (c > g.total / kMinIters) c = g.total / kMinIters;
   g.ctas = c < 1 ? 1 : (int32_t)c;
   return g;
 }
@@ -903,7 +906,7 @@ mla_bwd_dlat_kernel(const __grid_constant__ DlatTmaps tm, const LsMlaBwdArgs a,
 }
 
 // Units cut by a chunk boundary: their partial sums added in CTA order.  Grid: (units,
-// key groups of 8); one thread per accumulator column of the part.  Whole units were
+// key groups of 2); one thread per accumulator column of the part.  Whole units were
 // written by the kernel itself.
 __global__ void __launch_bounds__(kPartCols) mla_bwd_dlat_combine(const LsMlaBwdArgs a,
                                                                   const DlatGeom gm) {
@@ -919,7 +922,7 @@ __global__ void __launch_bounds__(kPartCols) mla_bwd_dlat_combine(const LsMlaBwd
     }
   }
   if (c0 < 0 || (c0 == c1 && gm.chunk_begin(c0) <= ub && gm.chunk_begin(c0 + 1) >= ue)) return;
-  for (int kk = blockIdx.y * 8; kk < blockIdx.y * 8 + 8; ++kk) {
+  for (int kk = blockIdx.y * 2; kk < blockIdx.y * 2 + 2; ++kk) {
     const int32_t j = (u >> 1) * kKT + kk;
     if (j >= a.R) break;
     float acc = 0.f;
@@ -986,7 +989,7 @@ cudaError_t ls_launch_mla_bwd(const LsMlaBwdArgs& a, const LsSched& sc, int sms,
   mla_bwd_dlat_kernel<<<gm.ctas, kThreads, kSmemBytes2, st>>>(tl, a, gm);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   ls_note_launch();
-  mla_bwd_dlat_combine<<<dim3((unsigned)(2 * gm.nkt), kKT / 8), kPartCols, 0, st>>>(a, gm);
+  mla_bwd_dlat_combine<<<dim3((unsigned)(2 * gm.nkt), kKT / 2), kPartCols, 0, st>>>(a, gm);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   ls_note_launch();
   return cudaSuccess;

@@ -2,7 +2,8 @@
 oracle: prompt lengths from 0 up, response lengths from 1 token to a few tiles, every
 grouped-query ratio up to 8, page sizes 16-256, split counts from 1 to more than the
 prompt has tiles, scores of unit spread or near-uniform, ragged member lists with
-empty members, and latent (MLA-style) replays with 1-128 heads and 32-4096-row pages.
+empty members, and latent (MLA-style) replays, forward and backward, with 1-128 heads
+and 32-4096-row pages.
 The shapes are drawn once from a fixed seed, so every run checks the same cases; each is
 small enough for the oracle to finish in about a second."""
 import numpy as np
@@ -127,6 +128,13 @@ def test_random_latent_replay(cuda, P, R, H, ps, splits, sharp):
     o, lse = api.mla_replay_fwd(cache, br.q, br.lat, SCALE, splits)
     torch.cuda.synchronize()
     assert B.ls_last_device_error(0) == B.LS_OK
-    o_ref, lse_ref = oracle.mla_fwd(problem(cache, br, P))
+    pb = problem(cache, br, P)
+    o_ref, lse_ref = oracle.mla_fwd(pb)
     assert rel_err(o.float().cpu().numpy(), o_ref) <= TOL_O
     assert float(np.abs(lse.cpu().numpy() - lse_ref).max()) <= TOL_LSE
+    dq, dlat = api.mla_replay_bwd(cache, br.q, br.lat, o, lse, br.d_o, SCALE, splits)
+    torch.cuda.synchronize()
+    assert B.ls_last_device_error(0) == B.LS_OK
+    dq_ref, dlat_ref = oracle.mla_bwd(pb, u16(br.d_o))
+    assert rel_err(dq.cpu().numpy(), dq_ref) <= TOL_GRAD
+    assert rel_err(dlat.cpu().numpy(), dlat_ref) <= TOL_GRAD

@@ -80,6 +80,17 @@ def test_mla_bwd_host_pool_matches_device_pool(cuda):
     assert rel_err(dl_h.cpu().numpy(), dl_ref) <= TOL_GRAD
 
 
+def test_mla_bwd_bad_page_is_reported(cuda):
+    cache, br = make(500, 4, 8, 32, 3, cuda)
+    o, lse = api.mla_replay_fwd(cache, br.q, br.lat, SCALE, 2)
+    torch.cuda.synchronize()
+    assert B.ls_last_device_error(0) == B.LS_OK
+    cache.page_table[2] = cache.pool.shape[0] + 5
+    api.mla_replay_bwd(cache, br.q, br.lat, o, lse, br.d_o, SCALE, 2)
+    assert B.ls_last_device_error(0) == B.LS_ERR_DEVICE_CHECK
+    assert B.ls_last_device_error(0) == B.LS_OK
+
+
 def test_mla_bwd_argument_checks(cuda):
     cache, br = make(300, 4, 8, 32, 3, cuda)
     o, lse = api.mla_replay_fwd(cache, br.q, br.lat, SCALE, 1)
