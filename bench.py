@@ -950,13 +950,18 @@ def run_mla_sweep(args, local_rank: int):
             dq = torch.empty((R, H, MLA_ROW), dtype=torch.float32, device=dev)
             dl = torch.empty((R, MLA_ROW), dtype=torch.float32, device=dev)
             api.mla_replay_fwd(dcache, br.q, br.lat, scale, splits, o=o, lse=lse, stream=stream)
-            ms = timed(lambda: api.mla_replay_bwd(dcache, br.q, br.lat, o, lse, d_o, scale,
-                                                  splits, dq=dq, dlat=dl, stream=stream),
-                       args.steps)
             alg, exe = mla_bwd_flops(P, R, H)
-            line.update({"hbm_bwd_ms": ms, "hbm_bwd_tflops": alg / (ms * 1e-3) / 1e12,
-                         "hbm_bwd_executed_tflops": exe / (ms * 1e-3) / 1e12,
-                         "bwd_executed_frac_of_bf16_burst": exe / (ms * 1e-3) / 1e12 / peak})
+            for name, cache in (("hbm", dcache), ("host", hcache)):
+                if name == "host" and R > args.mla_host_max_r:
+                    continue
+                ms = timed(lambda: api.mla_replay_bwd(cache, br.q, br.lat, o, lse, d_o, scale,
+                                                      splits, dq=dq, dlat=dl, stream=stream),
+                           args.steps)
+                line.update({f"{name}_bwd_ms": ms,
+                             f"{name}_bwd_tflops": alg / (ms * 1e-3) / 1e12,
+                             f"{name}_bwd_executed_tflops": exe / (ms * 1e-3) / 1e12,
+                             f"{name}_bwd_latent_gbs": lat_bytes / (ms * 1e-3) / 1e9})
+            line["bwd_executed_frac_of_bf16_burst"] = line["hbm_bwd_executed_tflops"] / peak
         line.update({"executed_frac_of_bf16_burst": line["hbm_executed_tflops"] / peak,
                      "peak": f"{pk_src} bf16 burst {peak}", "h2d_copy_gbs": h2d_gbs,
                      "steps": args.steps, "warmup": args.warmup})
@@ -965,7 +970,8 @@ def run_mla_sweep(args, local_rank: int):
 
 def run_mla_layers_sweep(args, local_rank: int):
     """Supplementary, labelled line (not the headline): one response of R tokens replayed
-    (forward) through L latent-attention layers over a 2,097,152-row latent prompt, with
+    (forward, and with --mla-bwd the backward in reverse layer order) through L
+    latent-attention layers over a 2,097,152-row latent prompt, with
     every layer's pages (a) in GPU memory and (b) in pinned host memory, streamed into a
     two-slot GPU page cache one layer ahead (each layer's copy overlapping the previous
     layer's replay)."""
@@ -992,13 +998,22 @@ def run_mla_layers_sweep(args, local_rank: int):
         del lat
         brs.append(syn.make_latent_branch(R, H, 5200 + l, dev, sharp=True))
     stream = torch.cuda.current_stream()
-    o = torch.empty((R, H, MLA_DC), dtype=torch.bfloat16, device=dev)
-    lse = torch.empty((R, H), dtype=torch.float32, device=dev)
+    os_ = [torch.empty((R, H, MLA_DC), dtype=torch.bfloat16, device=dev) for _ in range(nl)]
+    lses = [torch.empty((R, H), dtype=torch.float32, device=dev) for _ in range(nl)]
+    dq = torch.empty((R, H, MLA_ROW), dtype=torch.float32, device=dev)
+    dl = torch.empty((R, MLA_ROW), dtype=torch.float32, device=dev)
+
+    def bwd(c, l):
+        api.mla_replay_bwd(c, brs[l].q, brs[l].lat, os_[l], lses[l], brs[l].d_o, scale, splits,
+                           dq=dq, dlat=dl, stream=stream)
 
     def resident():
         for l in range(nl):
-            api.mla_replay_fwd(res[l], brs[l].q, brs[l].lat, scale, splits, o=o, lse=lse,
-                               stream=stream)
+            api.mla_replay_fwd(res[l], brs[l].q, brs[l].lat, scale, splits, o=os_[l],
+                               lse=lses[l], stream=stream)
+        if args.mla_bwd:
+            for l in reversed(range(nl)):
+                bwd(res[l], l)
 
     def streamed():
         st.prefetch(0)
@@ -1006,9 +1021,17 @@ def run_mla_layers_sweep(args, local_rank: int):
             c = st.cache(l)
             if l + 1 < nl:
                 st.prefetch(l + 1)
-            api.mla_replay_fwd(c, brs[l].q, brs[l].lat, scale, splits, o=o, lse=lse,
+            api.mla_replay_fwd(c, brs[l].q, brs[l].lat, scale, splits, o=os_[l], lse=lses[l],
                                stream=stream)
             st.release(l)
+        if args.mla_bwd:  # backward in reverse layer order through the same two slots
+            st.prefetch(nl - 1)
+            for l in reversed(range(nl)):
+                c = st.cache(l)
+                if l > 0:
+                    st.prefetch(l - 1)
+                bwd(c, l)
+                st.release(l)
 
     def timed(fn):
         for _ in range(args.warmup):
@@ -1027,9 +1050,11 @@ def run_mla_layers_sweep(args, local_rank: int):
     # the copy alone, from pinned host memory into a slot
     cp = timed(lambda: st.slots[0].pool.copy_(st.host[0].pool, non_blocking=True))
     alg, _ = mla_flops(P, R, H)
+    if args.mla_bwd:
+        alg += mla_bwd_flops(P, R, H)[0]
     print(json.dumps({
-        "sweep": f"latent replay through {nl} layers, pages streamed from host memory vs held "
-                 "in HBM (supplementary)",
+        "sweep": f"latent replay through {nl} layers ({'forward, then backward in reverse' if args.mla_bwd else 'forward'}), "
+                 "pages streamed from host memory vs held in HBM (supplementary)",
         "config": {"workload": f"P={P:,} latent rows of {MLA_ROW} bf16, H={H}, R={R}, "
                                f"{ps}-row pages, {splits} splits, {nl} layers"},
         "hbm_ms": ms_res, "streamed_ms": ms_str, "slowdown": ms_str / ms_res,
@@ -1359,7 +1384,8 @@ def main():
                     help="comma-separated response lengths: supplementary latent (MLA-style) "
                          "replay lines instead of the headline step")
     ap.add_argument("--mla-bwd", action="store_true",
-                    help="with --sweep-mla: also time the latent replay backward (HBM pool)")
+                    help="with --sweep-mla / --sweep-mla-layers: also time the latent replay "
+                         "backward")
     ap.add_argument("--sweep-mla-layers", type=int, default=0,
                     help="number of latent-attention layers: supplementary line with their "
                          "pages streamed from pinned host memory against held in HBM")

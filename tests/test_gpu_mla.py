@@ -140,8 +140,9 @@ def test_mla_full_prompt_sampled_rows(cuda):
 
 def test_streamed_latent_layers_match_resident(cuda):
     """Three layers' latent pages captured into pinned host memory and streamed through the
-    two-slot GPU page cache one layer ahead: every layer's forward bit-identical to the
-    same pages held in GPU memory, one layer against the oracle."""
+    two-slot GPU page cache one layer ahead (forward in layer order, backward in reverse):
+    every layer's forward and backward bit-identical to the same pages held in GPU
+    memory, one layer's forward against the oracle."""
     from response_replay_gb300 import layers as L
     P, R, H, ps, splits, nl = 3000, 40, 16, 64, 5, 3
     pr0 = syn.make_latent_prompt(P, ps, 900, cuda, extra_pages=2)
@@ -162,11 +163,24 @@ def test_streamed_latent_layers_match_resident(cuda):
             st.prefetch(l + 1)
         outs.append(api.mla_replay_fwd(c, brs[l].q, brs[l].lat, SCALE, splits))
         st.release(l)
+    # the backward in reverse layer order through the same two slots
+    st.prefetch(nl - 1)
+    grads = [None] * nl
+    for l in reversed(range(nl)):
+        c = st.cache(l)
+        if l > 0:
+            st.prefetch(l - 1)
+        grads[l] = api.mla_replay_bwd(c, brs[l].q, brs[l].lat, outs[l][0], outs[l][1],
+                                      brs[l].d_o, SCALE, splits)
+        st.release(l)
     torch.cuda.synchronize()
     assert B.ls_last_device_error(0) == B.LS_OK
     for l in range(nl):
         o_r, l_r = api.mla_replay_fwd(res[l], brs[l].q, brs[l].lat, SCALE, splits)
         assert torch.equal(outs[l][0], o_r) and torch.equal(outs[l][1], l_r), l
+        dq_r, dl_r = api.mla_replay_bwd(res[l], brs[l].q, brs[l].lat, o_r, l_r, brs[l].d_o,
+                                        SCALE, splits)
+        assert torch.equal(grads[l][0], dq_r) and torch.equal(grads[l][1], dl_r), l
     assert not st.host[1].pool.is_cuda and st.host[1].pool.is_pinned()
     o_ref, lse_ref = oracle.mla_fwd(problem(st.host[1], brs[1], P))
     assert rel_err(outs[1][0].float().cpu().numpy(), o_ref) <= TOL_O
