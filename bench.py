@@ -866,16 +866,16 @@ def mla_bwd_flops(P: int, R: int, H: int) -> tuple[float, float]:
     """(algorithmic, executed) FLOPs of one latent replay backward.  Algorithmic: per
     (query row, visible key) 2 x (576 score + 512 dP + 576 dq); per (query row, response
     key j <= t) 2 x (512 + 576) for the response row's gradient.  Executed on the tensor
-    pipe: the dq kernel's stacked 128-lane products cost 2 x (2 x 576 + 320 + 256) per
-    (row, key) and run once per dq part for S|dP; the response-row kernel walks 128-key
-    tiles over 16-row blocks from each tile's first token, 2 x (2 x 2 x 576 + 576 + 512)
-    per walked (row, key)."""
+    pipe: the dq kernel's 128-lane products hold 64 query rows, so per (row, key) they cost
+    2 x 2 x (576 + 320 + 256) (S|dP, and the dq products on all 128 lanes); the
+    response-row kernel walks 128-key tiles over 16-row blocks from each tile's first
+    token, 2 x (2 x 2 x 576 + 576 + 512) per walked (row, key)."""
     pairs = R * H * (P + (R + 1) / 2)
     resp_pairs = R * H * (R + 1) / 2
     alg = pairs * 2 * (2 * MLA_ROW + MLA_DC) + resp_pairs * 2 * (MLA_ROW + MLA_DC)
     rb_hi = -(-R * H // 16)
     walked = sum(128 * 16 * (rb_hi - 8 * kt * H) for kt in range(-(-R // 128)))
-    exe = pairs * 2 * 2 * (2 * MLA_ROW + 320 + 256) + walked * 2 * (4 * MLA_ROW + MLA_ROW + MLA_DC)
+    exe = pairs * 2 * 2 * (MLA_ROW + 320 + 256) + walked * 2 * (4 * MLA_ROW + MLA_ROW + MLA_DC)
     return alg, exe
 
 

@@ -736,13 +736,13 @@ ls_status mla_sched(const ls_latent_cache* c, int R, int H, int num_splits, LsSc
   return LS_OK;
 }
 
-// Backward units: (row tile of 64 (t, h) rows) x (part of the 576 dq columns).  Workspace:
+// Backward units: row tiles of 64 (t, h) rows (all 576 dq columns each).  Workspace:
 // D per row, partial dq of tail-unit pieces, partial d lat of units cut between CTAs.
 ls_status mla_bwd_sched(const ls_latent_cache* c, int R, int H, int num_splits, LsSched* sc,
                         size_t* off_pdq, size_t* off_pdl, size_t* total, int* sms) {
   if (R < 0 || H <= 0 || num_splits < 1) return LS_ERR_INVALID_ARG;
   const int64_t rows = (int64_t)R * H;
-  const int64_t units = 2 * ((rows + ls_mla_bwd_unit_rows() - 1) / ls_mla_bwd_unit_rows());
+  const int64_t units = (rows + ls_mla_bwd_unit_rows() - 1) / ls_mla_bwd_unit_rows();
   if (rows >= (1ll << 31) || units >= (1ll << 30)) return LS_ERR_UNSUPPORTED;
   DevInfo d;
   const ls_status s = dev_info(&d);
@@ -752,7 +752,7 @@ ls_status mla_bwd_sched(const ls_latent_cache* c, int R, int H, int num_splits, 
   const size_t pieces = sc->has_partials() ? (size_t)sc->num_pieces() : 0;
   const size_t pc = (size_t)ls_mla_bwd_part_cols();
   *off_pdq = align256((size_t)rows * sizeof(float));
-  *off_pdl = *off_pdq + align256(pieces * ls_mla_bwd_unit_rows() * pc * sizeof(float));
+  *off_pdl = *off_pdq + align256(pieces * ls_mla_bwd_unit_rows() * 576 * sizeof(float));
   *total = *off_pdl +
            align256((size_t)2 * ls_mla_bwd_dlat_ctas(R, H, d.sms) * 128 * pc * sizeof(float));
   *sms = d.sms;

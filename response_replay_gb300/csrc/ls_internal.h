@@ -200,7 +200,7 @@ struct LsMlaBwdArgs {
   float* delta;               // [R][H]: <dO, o>
   float* dq;                  // [R][H][576]
   float* dlat;                // [R][576]
-  float* part_dq;             // [pieces][64][320] partials of tail-unit pieces
+  float* part_dq;             // [pieces][64][576] partials of tail-unit pieces
   float* part_dlat;           // [2 x d lat CTAs][128][320]
   uint32_t* err;
 };

@@ -17,13 +17,19 @@
 // columns.  So the dq kernel stacks 64 query rows over the same 64 rows' dO on the 128
 // lanes of one MMA: Q rows on lanes 0-63, dO rows on lanes 64-127 (their rotary 64
 // values zero), times the latent tile, gives S on lanes 0-63 and dP on lanes 64-127 in
-// one product (M = 128, N = 32 keys, K = 576).  dS lands on lanes 64-127 and
-// dq += dS L runs on all 128 lanes (lanes 0-63 carry nothing of use), split in two
-// units per row tile: values {0-255, 512-575} (320 columns) and {256-511} (256).  Each
-// unit recomputes S and dP.
+// one product (M = 128, N = 32 keys, K = 576).  dq then lives on both lane halves of
+// the same 320 columns: values {0-255, 512-575} on lanes 64-127 and values 256-511 on
+// lanes 0-63.  Each lane half is written by a product whose A operand (dS as bf16 in
+// tensor memory) is dS on that half and zero on the other, so each product adds exactly
+// zero to the other half's columns:
+//   [0 ; dS] L[:, 0-255] and [0 ; dS] L[:, 512-575] -> lanes 64-127
+//   [dS ; 0] L[:, 256-511]                          -> lanes 0-63
+// The two zero-padded copies of dS fill the tile's 32-column S|dP buffer once S and dP
+// have been read out, so the whole dq of a row tile takes no more tensor memory than the
+// scores and one unit computes it with no recompute of S and dP.
 //
-// mla_bwd_dq_kernel (one CTA per SM, persistent, 8 warps; units = (64-row tile, dq part)
-// over the split-KV schedule of ls_sched.h; pieces of tail units leave partial dq that
+// mla_bwd_dq_kernel (one CTA per SM, persistent, 8 warps; units = 64-row tiles over the
+// split-KV schedule of ls_sched.h; pieces of tail units leave partial dq that
 // mla_bwd_dq_combine adds in piece order):
 //   warp 0      TMA producer: the shared-memory part of the stacked operand (values
 //               256-575: Q rows 0-63, dO rows 64-127), then the latent tiles (9 boxes of
@@ -32,12 +38,14 @@
 //               tile are zeroed before the hand-over.
 //   warp 1      MMA issuer (one thread): S|dP(g) into one of two 32-column buffers (16 TS
 //               MMAs with values 0-255 from tensor memory, 20 SS), then dq += dS(g-1) L
-//               (TS, dS from tensor memory, the latent tile as an MN-major operand: N = 256
-//               and 64 for part 0, N = 256 for part 1).
+//               (three TS MMAs per 16 keys as above, the latent tile as an MN-major
+//               operand).
 //   warps 4-5   lanes 0-63: P = exp2(s scale log2 e - lse log2 e) with the causal and
-//               ragged masks, handed to warps 6-7 through shared memory.
-//   warps 6-7   lanes 64-127: dS = P (dP - D) as bf16 pairs over their dP columns; at the
-//               end of a range they read dq, scale it and write dq (or a partial).
+//               ragged masks; warps 6-7, lanes 64-127: dP.  Each pair hands its values to
+//               the other through shared memory, both form dS = P (dP - D) (the same
+//               bits on both sides) and write their zero-padded copy over the buffer.  At
+//               the end of a range each half reads its dq columns, scales them and
+//               writes dq (or a partial).
 //   At the start of a range all four write the tensor-memory part of the stacked operand
 //   (each thread its row's values 0-255 of Q or dO).
 // Tensor memory (512 columns): stacked values 0-255 as bf16 pairs [0,128), S|dP buffers
@@ -88,11 +96,11 @@ constexpr uint32_t kLAtomBytes = kKeys * 128;                    // 4 KB
 constexpr uint32_t kABytes = (kAtoms - kTAtoms) * kAAtomBytes;   // 80 KB
 constexpr uint32_t kAFill = (kAtoms - kTAtoms) * kRows * 128 + (8 - kTAtoms) * kRows * 128;
 constexpr uint32_t kStageBytes = kAtoms * kLAtomBytes;           // 36 KB
-constexpr uint32_t kPexBytes = kRows * kKeys * 4;                // 8 KB
+constexpr uint32_t kXBytes = kRows * kKeys * 4;                  // 8 KB: one side's values
 constexpr uint32_t kOffA = 0;
 constexpr uint32_t kOffRing = kABytes;
-constexpr uint32_t kOffPex = kOffRing + kStages * kStageBytes;
-constexpr uint32_t kOffBar = kOffPex + 2 * kPexBytes;
+constexpr uint32_t kOffX = kOffRing + kStages * kStageBytes;     // [tile & 1][P, dP]
+constexpr uint32_t kOffBar = kOffX + 4 * kXBytes;
 constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 constexpr uint32_t kColA = 0, kColS = kTAtoms * 32, kColDq = kColS + 2 * kKeys;
@@ -105,9 +113,9 @@ enum {
   B_Q_EMPTY,
   B_QT_FULL,                  // the four softmax warps wrote values 0-255 of the range
   B_S_FULL,                   // 2: S|dP of tile g in buffer g & 1
-  B_PX_FULL = B_S_FULL + 2,   // 2: P of tile g in exchange buffer g & 1
-  B_PX_EMPTY = B_PX_FULL + 2, // 2: exchange buffer read
-  B_DS_FULL = B_PX_EMPTY + 2, // 2: dS of tile g over buffer g & 1
+  B_X_FULL = B_S_FULL + 2,    // 2: P and dP of tile g in exchange buffer g & 1
+  B_X_EMPTY = B_X_FULL + 2,   // 2: exchange buffer read by both sides
+  B_DS_FULL = B_X_EMPTY + 2,  // 2: dS of tile g over buffer g & 1
   B_DQ_DONE = B_DS_FULL + 2,  // the range's last dq MMA finished
   B_AUX,                      // producer: ragged prompt tile landed
   B_DONE,
@@ -151,7 +159,7 @@ struct DqCursor {
       resp = s == walk.sc->nsplit;
       if (resp) {
         const int64_t rows = (int64_t)R * H;
-        const int64_t end = (int64_t)(u >> 1) * kRows + kRows;
+        const int64_t end = (int64_t)u * kRows + kRows;
         const int32_t t_hi = (int32_t)(((end < rows ? end : rows) - 1) / H);
         t = 0;
         t_end = t_hi / kKeys + 1;
@@ -211,9 +219,9 @@ mla_bwd_dq_kernel(const __grid_constant__ DqTmaps tm, const LsMlaBwdArgs a,
     mbar_init(bar(sbase, B_QT_FULL), kM);
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(sbase, B_S_FULL + i), 1);
-      mbar_init(bar(sbase, B_PX_FULL + i), kRows);
-      mbar_init(bar(sbase, B_PX_EMPTY + i), kRows);
-      mbar_init(bar(sbase, B_DS_FULL + i), kRows);
+      mbar_init(bar(sbase, B_X_FULL + i), kM);
+      mbar_init(bar(sbase, B_X_EMPTY + i), kM);
+      mbar_init(bar(sbase, B_DS_FULL + i), kM);
     }
     mbar_init(bar(sbase, B_DQ_DONE), 1);
     mbar_init(bar(sbase, B_AUX), 1);
@@ -264,7 +272,7 @@ mla_bwd_dq_kernel(const __grid_constant__ DqTmaps tm, const LsMlaBwdArgs a,
         if (r.first) {
           if (ranges > 0 && !mbar_wait(bar(sbase, B_Q_EMPTY), (ranges - 1) & 1)) { fail(); break; }
           const uint32_t qb = bar(sbase, B_Q_FULL);
-          const int32_t row0 = (r.u >> 1) * kRows;
+          const int32_t row0 = r.u * kRows;
           mbar_expect_tx(qb, kAFill);
           for (int at = kTAtoms; at < kAtoms; ++at)
             tma_load_2d(sbase + kOffA + (at - kTAtoms) * kAAtomBytes, &tm.q, at * 64, row0, qb);
@@ -332,16 +340,20 @@ mla_bwd_dq_kernel(const __grid_constant__ DqTmaps tm, const LsMlaBwdArgs a,
         if (!mbar_wait(bar(sbase, B_DS_FULL + (pg & 1)), (pg >> 1) & 1)) return false;
         tc_fence_after();
         const uint32_t sb = sbase + kOffRing + pstage * kStageBytes;
-        const uint32_t a0 = tmem + kColS + (pg & 1) * kKeys;
-        const bool part0 = (p.u & 1) == 0;
-        const uint32_t b256 = sdesc_lo(sb + (part0 ? 0u : 4u * kLAtomBytes), kLAtomBytes);
-        const uint32_t b64 = sdesc_lo(sb + 8u * kLAtomBytes, kLAtomBytes);
+        // [0 ; dS] in the buffer's first 16 columns, [dS ; 0] in the next 16
+        const uint32_t a_hi = tmem + kColS + (pg & 1) * kKeys, a_lo = a_hi + kKeys / 2;
+        const uint32_t b_lat = sdesc_lo(sb, kLAtomBytes);                    // values 0-255
+        const uint32_t b_mid = sdesc_lo(sb + 4u * kLAtomBytes, kLAtomBytes);  // 256-511
+        const uint32_t b_rot = sdesc_lo(sb + 8u * kLAtomBytes, kLAtomBytes);  // 512-575
 #pragma unroll
         for (int kk = 0; kk < kKeys / 16; ++kk) {  // 16 latent rows per MMA
           const uint32_t acc = (kk > 0 || !p.first) ? 1u : 0u;
           const uint32_t ob = (kk * 2048u) >> 4;
-          mma_ts_lo(tmem + kColDq, a0 + kk * 8, b256 + ob, id256, acc);
-          if (part0) mma_ts_lo(tmem + kColDq + 256, a0 + kk * 8, b64 + ob, id64, acc);
+          // the first product of a range sets all 128 lanes (zero on lanes 0-63), so the
+          // lanes 0-63 product accumulates from the start
+          mma_ts_lo(tmem + kColDq, a_hi + kk * 8, b_lat + ob, id256, acc);
+          mma_ts_lo(tmem + kColDq + 256, a_hi + kk * 8, b_rot + ob, id64, acc);
+          mma_ts_lo(tmem + kColDq, a_lo + kk * 8, b_mid + ob, id256, 1u);
         }
         mma_commit(bar(sbase, B_KV_EMPTY + pstage));
         if (p.last) mma_commit(bar(sbase, B_DQ_DONE));
@@ -389,9 +401,9 @@ mla_bwd_dq_kernel(const __grid_constant__ DqTmaps tm, const LsMlaBwdArgs a,
       mbar_wait(bar(sbase, B_DONE), 0);
     }
   } else if (warp >= 4) {
-    // ------------------------------------------------------------ P / dS warps
+    // ------------------------------------------------------------ P / dP / dS warps
     const int row = (warp - 4) * 32 + lane;  // tensor-memory lane
-    const bool is_s = row < kRows;           // lanes 0-63: S and P; 64-127: dP and dS
+    const bool is_s = row < kRows;           // lanes 0-63: S and P; 64-127: dP
     const int rr = row & (kRows - 1);
     const uint32_t lane_base = tmem + ((uint32_t)((warp - 4) * 32) << 16);
     const float c = a.scale_log2;
@@ -399,9 +411,9 @@ mla_bwd_dq_kernel(const __grid_constant__ DqTmaps tm, const LsMlaBwdArgs a,
     DqCursor cur(sc, blockIdx.x, a.R, a.H);
     DqTile r;
     uint32_t g = 0, oc = 0, ranges = 0;
-    float stat = 0.f;  // lse log2(e) of the row (lanes 0-63) or its D (lanes 64-127)
+    float lse2 = 0.f, dd = 0.f;  // the row's lse log2(e) (lanes 0-63) and D
     while (cur.next(&r)) {
-      const int64_t grow = (int64_t)(r.u >> 1) * kRows + rr;  // (t, h) row, token-major
+      const int64_t grow = (int64_t)r.u * kRows + rr;  // (t, h) row, token-major
       const bool valid = grow < nrows;
       if (r.first) {
         // values 0-255 of this thread's row (Q on lanes 0-63, dO on 64-127) into tensor
@@ -426,7 +438,8 @@ mla_bwd_dq_kernel(const __grid_constant__ DqTmaps tm, const LsMlaBwdArgs a,
           }
           tmem_st32(lane_base + kColA + c0, v);
         }
-        stat = valid ? (is_s ? __ldg(a.lse + grow) * kLog2e : __ldg(a.delta + grow)) : 0.f;
+        lse2 = valid && is_s ? __ldg(a.lse + grow) * kLog2e : 0.f;
+        dd = valid ? __ldg(a.delta + grow) : 0.f;
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(bar(sbase, B_QT_FULL));
@@ -439,7 +452,8 @@ mla_bwd_dq_kernel(const __grid_constant__ DqTmaps tm, const LsMlaBwdArgs a,
       tmem_ld32(s_col, x);
       tmem_wait_ld();
       reg_fence32(x);
-      float4* px = reinterpret_cast<float4*>(smem + kOffPex + (g & 1) * kPexBytes + rr * kKeys * 4);
+      // lanes 0-63 turn S into P; lanes 64-127 keep dP as it is
+      float mine[kKeys];
       if (is_s) {
         const int32_t tq = (int32_t)(grow / a.H);
         int32_t lim = kKeys;  // visible keys [0, lim) of the tile
@@ -450,64 +464,80 @@ mla_bwd_dq_kernel(const __grid_constant__ DqTmaps tm, const LsMlaBwdArgs a,
           lim = (int32_t)(a.P - r.key0);
         }
         if (!valid) lim = 0;
-        float p[kKeys];
 #pragma unroll
         for (int j = 0; j < kKeys; ++j)
-          p[j] = j < lim ? fast_exp2(__uint_as_float(x[j]) * c - stat) : 0.f;
-        tc_fence_before();
-        if (!mbar_wait(bar(sbase, B_PX_EMPTY + (g & 1)), ((g >> 1) & 1) ^ 1)) { fail(); break; }
-        // 16-byte chunk k of the row at position k ^ (row & 7): a warp's stores and the
-        // reading warp's loads touch every bank once per quarter-warp
-#pragma unroll
-        for (int k = 0; k < kKeys / 4; ++k)
-          px[k ^ (rr & 7)] = make_float4(p[4 * k], p[4 * k + 1], p[4 * k + 2], p[4 * k + 3]);
-        mbar_arrive(bar(sbase, B_PX_FULL + (g & 1)));
+          mine[j] = j < lim ? fast_exp2(__uint_as_float(x[j]) * c - lse2) : 0.f;
       } else {
-        if (!mbar_wait(bar(sbase, B_PX_FULL + (g & 1)), (g >> 1) & 1)) { fail(); break; }
-        float p[kKeys];
 #pragma unroll
-        for (int k = 0; k < kKeys / 4; ++k) {
-          const float4 w = px[k ^ (rr & 7)];
-          p[4 * k] = w.x;
-          p[4 * k + 1] = w.y;
-          p[4 * k + 2] = w.z;
-          p[4 * k + 3] = w.w;
-        }
-        mbar_arrive(bar(sbase, B_PX_EMPTY + (g & 1)));
-        uint32_t pk[kKeys / 2];
+        for (int j = 0; j < kKeys; ++j) mine[j] = __uint_as_float(x[j]);
+      }
+      tc_fence_before();
+      // Exchange: P rows at side 0, dP rows at side 1 of buffer g & 1; 16-byte chunk k
+      // of a row at position k ^ (row & 7), so a quarter-warp's accesses touch every bank
+      // once.
+      uint8_t* xb = smem + kOffX + (g & 1) * 2 * kXBytes;
+      float4* own = reinterpret_cast<float4*>(xb + (is_s ? 0 : kXBytes) + rr * kKeys * 4);
+      const float4* other =
+          reinterpret_cast<const float4*>(xb + (is_s ? kXBytes : 0) + rr * kKeys * 4);
+      if (!mbar_wait(bar(sbase, B_X_EMPTY + (g & 1)), ((g >> 1) & 1) ^ 1)) { fail(); break; }
 #pragma unroll
-        for (int j = 0; j < kKeys / 2; ++j)
-          pk[j] = pack_bf16(p[2 * j] * (__uint_as_float(x[2 * j]) - stat),
-                            p[2 * j + 1] * (__uint_as_float(x[2 * j + 1]) - stat));
-        tmem_st16(s_col, pk);
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(bar(sbase, B_DS_FULL + (g & 1)));
-        if (r.last) {
-          if (!mbar_wait(bar(sbase, B_DQ_DONE), oc & 1)) { fail(); break; }
-          ++oc;
-          tc_fence_after();
-          const int h = r.u & 1;
-          const int nc = part_cols(h);
-          float* drow = r.complete ? a.dq + (valid ? grow : 0) * kD
-                                   : a.part_dq + ((int64_t)r.slot * kRows + rr) * kPartCols;
+      for (int k = 0; k < kKeys / 4; ++k)
+        own[k ^ (rr & 7)] = make_float4(mine[4 * k], mine[4 * k + 1], mine[4 * k + 2], mine[4 * k + 3]);
+      mbar_arrive(bar(sbase, B_X_FULL + (g & 1)));
+      if (!mbar_wait(bar(sbase, B_X_FULL + (g & 1)), (g >> 1) & 1)) { fail(); break; }
+      float theirs[kKeys];
+#pragma unroll
+      for (int k = 0; k < kKeys / 4; ++k) {
+        const float4 w = other[k ^ (rr & 7)];
+        theirs[4 * k] = w.x;
+        theirs[4 * k + 1] = w.y;
+        theirs[4 * k + 2] = w.z;
+        theirs[4 * k + 3] = w.w;
+      }
+      mbar_arrive(bar(sbase, B_X_EMPTY + (g & 1)));
+      // dS = P (dP - D), the same operands and operations on both sides; lanes 64-127
+      // write [dS, 0] and lanes 0-63 [0, dS] over the buffer's 32 columns
+      uint32_t pk[kKeys];
+#pragma unroll
+      for (int j = 0; j < kKeys / 2; ++j) {
+        const float p0 = is_s ? mine[2 * j] : theirs[2 * j];
+        const float p1 = is_s ? mine[2 * j + 1] : theirs[2 * j + 1];
+        const float q0 = is_s ? theirs[2 * j] : mine[2 * j];
+        const float q1 = is_s ? theirs[2 * j + 1] : mine[2 * j + 1];
+        const uint32_t w = pack_bf16(p0 * (q0 - dd), p1 * (q1 - dd));
+        pk[j] = is_s ? 0u : w;
+        pk[kKeys / 2 + j] = is_s ? w : 0u;
+      }
+      tmem_st32(s_col, pk);
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar(sbase, B_DS_FULL + (g & 1)));
+      if (r.last) {
+        if (!mbar_wait(bar(sbase, B_DQ_DONE), oc & 1)) { fail(); break; }
+        ++oc;
+        tc_fence_after();
+        // lanes 64-127: values 0-255 and 512-575 (320 columns); lanes 0-63: 256-511 (256)
+        const int h = is_s ? 1 : 0;
+        const int nc = part_cols(h);
+        float* drow = r.complete ? a.dq + (valid ? grow : 0) * kD
+                                 : a.part_dq + ((int64_t)r.slot * kRows + rr) * kD;
 #pragma unroll 1
-          for (int c0 = 0; c0 < nc; c0 += 32) {
-            uint32_t v[32];
-            tmem_ld32(lane_base + kColDq + c0, v);
-            tmem_wait_ld();
-            reg_fence32(v);
-            if (valid || !r.complete) {
-              float* dst = drow + (r.complete ? part_value(h, c0) : c0);
+        for (int c0 = 0; c0 < kPartCols; c0 += 32) {
+          if (c0 >= nc) break;
+          uint32_t v[32];
+          tmem_ld32(lane_base + kColDq + c0, v);
+          tmem_wait_ld();
+          reg_fence32(v);
+          if (valid || !r.complete) {
+            float* dst = drow + part_value(h, c0);
 #pragma unroll
-              for (int i = 0; i < 32; i += 4)
-                *reinterpret_cast<float4*>(dst + i) =
-                    make_float4(__uint_as_float(v[i]) * a.scale, __uint_as_float(v[i + 1]) * a.scale,
-                                __uint_as_float(v[i + 2]) * a.scale, __uint_as_float(v[i + 3]) * a.scale);
-            }
+            for (int i = 0; i < 32; i += 4)
+              *reinterpret_cast<float4*>(dst + i) =
+                  make_float4(__uint_as_float(v[i]) * a.scale, __uint_as_float(v[i + 1]) * a.scale,
+                              __uint_as_float(v[i + 2]) * a.scale, __uint_as_float(v[i + 3]) * a.scale);
           }
-          tc_fence_before();
         }
+        tc_fence_before();
       }
       ++g;
       if (*abort_flag) break;
@@ -522,22 +552,19 @@ mla_bwd_dq_kernel(const __grid_constant__ DqTmaps tm, const LsMlaBwdArgs a,
 }
 
 // Partial dq of the pieces of every tail unit, added in fixed piece order.
-// Grid: (tail units, row groups of 8); one thread per accumulator column of the part.
+// Grid: (tail units, row groups of 8); one thread per dq value.
 constexpr int kCombineRows = 8;
-__global__ void __launch_bounds__(kPartCols) mla_bwd_dq_combine(const LsMlaBwdArgs a,
-                                                                const LsSched sc) {
+__global__ void __launch_bounds__(kD) mla_bwd_dq_combine(const LsMlaBwdArgs a, const LsSched sc) {
   const int tu = blockIdx.x, T = sc.tail_units, Q = sc.pieces;
   const int u = sc.tail_unit0() + tu;
-  const int h = u & 1, col = threadIdx.x;
-  if (col >= part_cols(h)) return;
+  const int col = threadIdx.x;
   const int64_t nrows = (int64_t)a.R * a.H;
   for (int r = blockIdx.y * kCombineRows; r < (blockIdx.y + 1) * kCombineRows; ++r) {
-    const int64_t grow = (int64_t)(u >> 1) * kRows + r;
+    const int64_t grow = (int64_t)u * kRows + r;
     if (grow >= nrows) break;
     float acc = 0.f;
-    for (int k = 0; k < Q; ++k)
-      acc += a.part_dq[((int64_t)(k * T + tu) * kRows + r) * kPartCols + col];
-    a.dq[grow * kD + part_value(h, col)] = acc;
+    for (int k = 0; k < Q; ++k) acc += a.part_dq[((int64_t)(k * T + tu) * kRows + r) * kD + col];
+    a.dq[grow * kD + col] = acc;
   }
 }
 
@@ -978,7 +1005,7 @@ cudaError_t ls_launch_mla_bwd(const LsMlaBwdArgs& a, const LsSched& sc, int sms,
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   ls_note_launch();
   if (sc.has_partials()) {
-    mla_bwd_dq_combine<<<dim3((unsigned)sc.tail_units, kRows / kCombineRows), kPartCols, 0, st>>>(a, sc);
+    mla_bwd_dq_combine<<<dim3((unsigned)sc.tail_units, kRows / kCombineRows), kD, 0, st>>>(a, sc);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     ls_note_launch();
   }
