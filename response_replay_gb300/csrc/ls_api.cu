@@ -728,7 +728,9 @@ ls_status mla_sched(const ls_latent_cache* c, int R, int H, int num_splits, LsSc
   const ls_status s = dev_info(&d);
   if (s != LS_OK) return s;
   const int tile = ls_mla_tile();
-  *sc = ls_make_sched((int)units, (int)((c->num_tokens + tile - 1) / tile), num_splits, d.sms);
+  // a 1-token response of 64 heads is two units: let them spread over every SM
+  *sc = ls_make_sched((int)units, (int)((c->num_tokens + tile - 1) / tile), num_splits, d.sms,
+                      256);
   const size_t pieces = sc->has_partials() ? (size_t)sc->num_pieces() : 0;
   *part_o = 0;
   *part_lse = align256(pieces * ls_mla_unit_rows() * ls_mla_half() * sizeof(float));
@@ -748,7 +750,9 @@ ls_status mla_bwd_sched(const ls_latent_cache* c, int R, int H, int num_splits, 
   const ls_status s = dev_info(&d);
   if (s != LS_OK) return s;
   const int tile = ls_mla_bwd_tile();
-  *sc = ls_make_sched((int)units, (int)((c->num_tokens + tile - 1) / tile), num_splits, d.sms);
+  // one 64-row unit holds a 1-token response of 64 heads: let it spread over every SM
+  *sc = ls_make_sched((int)units, (int)((c->num_tokens + tile - 1) / tile), num_splits, d.sms,
+                      256);
   const size_t pieces = sc->has_partials() ? (size_t)sc->num_pieces() : 0;
   const size_t pc = (size_t)ls_mla_bwd_part_cols();
   *off_pdq = align256((size_t)rows * sizeof(float));

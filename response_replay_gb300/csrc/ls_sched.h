@@ -90,8 +90,10 @@ inline double ls_tail_cost(int32_t T, int32_t q, int32_t C) {
 }
 
 // Host: build the schedule for U units, a prompt of `ntiles` tiles, the caller's split
-// request and a grid of at most `max_ctas` CTAs.
-inline LsSched ls_make_sched(int32_t units, int32_t ntiles, int32_t num_splits, int32_t max_ctas) {
+// request and a grid of at most `max_ctas` CTAs; a tail unit is cut into at most
+// `max_pieces` pieces.
+inline LsSched ls_make_sched(int32_t units, int32_t ntiles, int32_t num_splits, int32_t max_ctas,
+                             int32_t max_pieces = 64) {
   LsSched s;
   s.units = units;
   s.ntiles = ntiles;
@@ -118,7 +120,7 @@ inline LsSched ls_make_sched(int32_t units, int32_t ntiles, int32_t num_splits, 
   s.seg.off[0] = 0;
   s.seg.off[1] = 0;
   if (s.tail_units > 0) {
-    const int32_t qmax = ipu < 64 ? ipu : 64;  // a piece holds at least one item
+    const int32_t qmax = ipu < max_pieces ? ipu : max_pieces;  // a piece holds at least one item
     double best = ls_tail_cost(s.tail_units, 1, c);
     for (int32_t q = 2; q <= qmax; ++q) {
       const double cq = ls_tail_cost(s.tail_units, q, c);

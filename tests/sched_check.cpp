@@ -27,12 +27,12 @@ static int fail(const char* what, int U, int nt, int sp, int C) {
   return 1;
 }
 
-static int check(int U, int nt, int sp, int C) {
-  LsSched s = ls_make_sched(U, nt, sp, C);
+static int check(int U, int nt, int sp, int C, int max_pieces = 64) {
+  LsSched s = ls_make_sched(U, nt, sp, C, max_pieces);
   const int ipu = s.items_per_unit();
   if (s.tail_units != U - s.waves * s.ctas || s.tail_units < 0 || s.tail_units >= s.ctas)
     return fail("tail units", U, nt, sp, C);
-  if (s.pieces < 1 || s.pieces > ipu) return fail("piece count", U, nt, sp, C);
+  if (s.pieces < 1 || s.pieces > ipu || s.pieces > max_pieces) return fail("piece count", U, nt, sp, C);
   std::vector<int> seen((size_t)U * ipu, 0);
   std::map<int, int> complete_of_unit;         // unit -> cta that completed it
   std::map<int, std::set<int>> slots_of_unit;  // unit -> partial slots written
@@ -271,6 +271,14 @@ int main() {
       for (int sp : sps)
         for (int C : Cs) {
           bad += check(U, nt, sp, C);
+          ++n;
+        }
+  // the latent backward's cap of 256 pieces (a lone unit spread over every CTA)
+  for (int U : {1, 2, 3, 152, 153})
+    for (int nt : {0, 5, 257, 65536})
+      for (int sp : {1, 256, 1000})
+        for (int C : {1, 152, 304}) {
+          bad += check(U, nt, sp, C, 256);
           ++n;
         }
   // the two launches of the 2,097,152-position workload: 384 forward and 768 backward
