@@ -893,12 +893,14 @@ def run_mla_sweep(args, local_rank: int):
     torch.cuda.set_device(dev)
     P, ps, splits, H = args.mla_p, 256, 256, args.mla_heads
     scale = 192 ** -0.5
-    pr = syn.make_latent_prompt(P, ps, 4242, dev)
-    dcache = api.LatentCache(pr.num_pages, pr.page_table, ps, P, device=dev)
-    dcache.capture(pr.lat)
+    pr = syn.make_latent_prompt(max(P, 1), ps, 4242, dev)  # P = 0: causal response only
+    pt = pr.page_table if P > 0 else pr.page_table[:0]
+    dcache = api.LatentCache(pr.num_pages, pt, ps, P, device=dev)
+    if P > 0:
+        dcache.capture(pr.lat)
     hcache = None
-    if args.mla_host_max_r > 0:
-        hcache = api.LatentCache(pr.num_pages, pr.page_table, ps, P, host_pool=True)
+    if args.mla_host_max_r > 0 and P > 0:
+        hcache = api.LatentCache(pr.num_pages, pt, ps, P, host_pool=True)
         hcache.capture(pr.lat)  # written over the link by the capture kernel
     del pr
     stream = torch.cuda.current_stream()
@@ -936,7 +938,7 @@ def run_mla_sweep(args, local_rank: int):
                                                f"({MLA_DC} latent + 64 rotary), H={H}, "
                                                f"{ps}-row pages, {splits} splits"}}
         for name, cache in (("hbm", dcache), ("host", hcache)):
-            if name == "host" and R > args.mla_host_max_r:
+            if name == "host" and (cache is None or R > args.mla_host_max_r):
                 continue
             ms = timed(lambda: api.mla_replay_fwd(cache, br.q, br.lat, scale, splits, o=o,
                                                   lse=lse, stream=stream), args.steps)
@@ -952,7 +954,7 @@ def run_mla_sweep(args, local_rank: int):
             api.mla_replay_fwd(dcache, br.q, br.lat, scale, splits, o=o, lse=lse, stream=stream)
             alg, exe = mla_bwd_flops(P, R, H)
             for name, cache in (("hbm", dcache), ("host", hcache)):
-                if name == "host" and R > args.mla_host_max_r:
+                if name == "host" and (cache is None or R > args.mla_host_max_r):
                     continue
                 ms = timed(lambda: api.mla_replay_bwd(cache, br.q, br.lat, o, lse, d_o, scale,
                                                       splits, dq=dq, dlat=dl, stream=stream),
