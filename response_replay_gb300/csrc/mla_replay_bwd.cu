@@ -53,7 +53,8 @@
 //
 // mla_bwd_dlat_kernel: the response rows' gradient, key-stationary.  A unit is one
 // 128-row tile of the response's latent rows (M = 128, resident in shared memory) and
-// one part of the 576 output columns (as above); it walks the query rows that see the
+// one part of the 576 output columns ({0-255, 512-575} or {256-511}, each unit computing
+// S^T and dP^T for itself); it walks the query rows that see the
 // tile (tokens t >= the tile's first row) 16 at a time:
 //   S^T|dP^T = L [Q rows ; dO rows]^T   (SS, M = 128 keys, N = 32: 16 Q rows, 16 dO rows)
 //   P^T, dS^T scale as bf16 (one key per thread)
@@ -76,9 +77,10 @@ constexpr int kD = 576;                   // latent + rotary values
 constexpr int kAtoms = kD / 64;           // 128-byte swizzle atoms per row
 constexpr int kThreads = 256;
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr int kPartCols = 320;            // columns of dq / d lat part 0 (part 1: 256)
+constexpr int kPartCols = 320;            // columns of part 0 (part 1: 256)
 
-// Columns of part h of a 576-value gradient row: accumulator column c -> value.
+// Parts of a 576-value gradient row: part 0 = values {0-255, 512-575} (dq: lanes 64-127;
+// d lat: even units), part 1 = values 256-511; accumulator column c of part h -> value.
 __device__ __forceinline__ int part_value(int h, int c) {
   return h == 0 ? (c < 256 ? c : c + 256) : c + 256;
 }
