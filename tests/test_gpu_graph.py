@@ -90,3 +90,54 @@ def test_replay_step_in_a_cuda_graph(cuda):
     for a, b in zip(replayed, outs):
         assert torch.equal(a, b)
     assert not torch.equal(replayed[0], eager[0])
+
+
+def test_latent_replay_in_a_cuda_graph(cuda):
+    """The latent capture, forward and backward captured once: replays bit-identical to
+    eager calls, and they follow the inputs when these change in place."""
+    P, R, H, ps, splits, scale = 3000, 70, 16, 64, 5, 192 ** -0.5
+    pr = syn.make_latent_prompt(P, ps, 401, cuda, extra_pages=1)
+    lat = pr.lat[:P].contiguous()
+    cache = api.LatentCache(pr.num_pages, pr.page_table, ps, P, device=cuda)
+    br = syn.make_latent_branch(R, H, 402, cuda, sharp=True)
+    o = torch.empty((R, H, 512), dtype=torch.bfloat16, device=cuda)
+    lse = torch.empty((R, H), dtype=torch.float32, device=cuda)
+    dq = torch.empty((R, H, 576), dtype=torch.float32, device=cuda)
+    dl = torch.empty((R, 576), dtype=torch.float32, device=cuda)
+
+    def step():
+        cache.capture(lat)
+        api.mla_replay_fwd(cache, br.q, br.lat, scale, splits, o=o, lse=lse)
+        api.mla_replay_bwd(cache, br.q, br.lat, o, lse, br.d_o, scale, splits, dq=dq, dlat=dl)
+
+    outs = (o, lse, dq, dl)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):  # eager warm-up: every workspace exists before capture
+        step()
+        step()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    eager = [t.clone() for t in outs]
+
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    for t in outs:
+        t.fill_(float("nan"))
+    graph.replay()
+    torch.cuda.synchronize()
+    assert B.ls_last_device_error(0) == B.LS_OK
+    for a, b in zip(outs, eager):
+        assert torch.equal(a, b)
+
+    br.q.mul_(0.5)
+    br.d_o.mul_(-1.0)
+    graph.replay()
+    torch.cuda.synchronize()
+    replayed = [t.clone() for t in outs]
+    step()
+    torch.cuda.synchronize()
+    for a, b in zip(replayed, outs):
+        assert torch.equal(a, b)
+    assert not torch.equal(replayed[2], eager[2])
