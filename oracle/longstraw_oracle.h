@@ -61,7 +61,8 @@
  *   lso_mla_fwd_rows        equals lso_mla_fwd on the sampled rows
  *   lso_mla_bwd             central finite differences of <dO, O> through lso_mla_fwd
  *                           (steps exact in bf16); one key: dq = 0 and d lat = [dO ; 0]
- *                           summed over the heads
+ *                           summed over the heads; equals lso_attn_bwd with one KV head
+ *                           (dq = dQ, d lat = dK + dV)
  *   lso_mla_bwd_dq_rows,
  *   lso_mla_bwd_dlat_keys   equal lso_mla_bwd on the sampled rows / keys
  */

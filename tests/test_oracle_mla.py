@@ -198,3 +198,27 @@ def test_bwd_rows_and_keys_match_full():
     js = np.array([R - 1, 0, 4], np.int32)
     np.testing.assert_allclose(oracle.mla_bwd_dlat_keys(pb, g, js), dlat[js], rtol=0,
                                atol=1e-12)
+
+
+def test_bwd_equals_one_kv_head_attention():
+    """The same one-KV-head problem as above, backward: dq equals the attention oracle's
+    dQ (itself pinned), and the response rows' gradient equals its dK + dV (the latent is
+    both the key and the value; dO padded with zeros past d_c leaves dV's rotary part 0)."""
+    P, R, H, d_c, d_r, ps = 70, 6, 4, 12, 4, 16
+    pb, rows = latent_problem(P, R, H, d_c, d_r, ps, seed=13)
+    g = bf16_bits(np.random.default_rng(4).standard_normal((R, H, d_c)))
+    dq, dlat = oracle.mla_bwd(pb, g)
+    kp = bf16_value(pb.lat_pool)[:, None]
+    vp = kp.copy()
+    vp[..., d_c:] = 0.0
+    kr = bf16_value(pb.lat_resp)[:, None]
+    vr = kr.copy()
+    vr[..., d_c:] = 0.0
+    ap = oracle.AttnProblem(np.nan_to_num(kp), np.nan_to_num(vp), pb.page_table, P,
+                            bf16_value(pb.q), kr, vr, pb.scale, 3)
+    g_pad = np.zeros((R, H, d_c + d_r), np.uint16)
+    g_pad[..., :d_c] = g
+    dq_a, dk_a, dv_a = oracle.attn_bwd(ap, g_pad)
+    np.testing.assert_allclose(dq, dq_a, rtol=0, atol=1e-12)
+    assert np.abs(dv_a[..., d_c:]).max() == 0.0
+    np.testing.assert_allclose(dlat, (dk_a + dv_a)[:, 0], rtol=0, atol=1e-12)
