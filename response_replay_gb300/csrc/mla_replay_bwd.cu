@@ -829,6 +829,11 @@ mla_bwd_dlat_kernel(const __grid_constant__ DlatTmaps tm, const LsMlaBwdArgs a,
           have_prev = false;
           if (!mbar_wait(bar2(sbase, C_L_FULL), units & 1)) { ok = false; break; }
           ++units;
+        } else if (have_prev) {
+          // the product of the iteration before goes first: it frees the row stage that
+          // iteration g + 1 is loaded into, so that load lands while S^T(g) computes
+          if (!issue_dlat(prev, prev_stage, g - 1)) { ok = false; break; }
+          have_prev = false;
         }
         if (!mbar_wait(bar2(sbase, C_R_FULL + ks.stage), ks.phase)) { ok = false; break; }
         tc_fence_after();
@@ -842,7 +847,6 @@ mla_bwd_dlat_kernel(const __grid_constant__ DlatTmaps tm, const LsMlaBwdArgs a,
         }
         mma_commit(bar2(sbase, C_S_FULL + (g & 1)));
         if (it.last) mma_commit(bar2(sbase, C_L_EMPTY));  // the latent tile is read by S only
-        if (have_prev && !issue_dlat(prev, prev_stage, g - 1)) { ok = false; break; }
         prev = it;
         prev_stage = ks.stage;
         have_prev = true;
