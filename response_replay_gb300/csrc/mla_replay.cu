@@ -116,6 +116,12 @@ struct MlaTmaps {
 
 __device__ __forceinline__ uint32_t bar(uint32_t sbase, int i) { return sbase + kOffBar + 8u * i; }
 
+// A phase that has already completed returns on a plain test; otherwise the bounded,
+// sleeping wait.
+__device__ __forceinline__ bool wait_fast(uint32_t b, uint32_t parity) {
+  return mbar_try_wait(b, parity) || mbar_wait(b, parity);
+}
+
 // Prefetch a tensor-map box into L2 (no shared memory, no barrier).
 __device__ __forceinline__ void tma_prefetch_l2_2d(const void* tmap, int32_t x, int32_t y) {
   asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
@@ -337,7 +343,7 @@ mla_fwd_kernel(const __grid_constant__ MlaTmaps tm, const LsMlaArgs a,
       bool have_prev = false, ok = true;
       // O += P(pg) L[:, half] for the tile before; its latent stage is free afterwards.
       auto issue_pv = [&](const MlaTile& p, uint32_t pstage, uint32_t pg) -> bool {
-        if (!mbar_wait(bar(sbase, B_P_FULL + (pg & 1)), (pg >> 1) & 1)) return false;
+        if (!wait_fast(bar(sbase, B_P_FULL + (pg & 1)), (pg >> 1) & 1)) return false;
         tc_fence_after();
         const uint32_t b0 = sdesc_lo(sbase + kOffRing + pstage * kStageBytes + 5u * kLAtomBytes,
                                      kLAtomBytes);  // slots 5-8: the output half
@@ -366,7 +372,7 @@ mla_fwd_kernel(const __grid_constant__ MlaTmaps tm, const LsMlaArgs a,
           if (!issue_pv(prev, prev_stage, g - 1)) { ok = false; break; }
           have_prev = false;
         }
-        if (!mbar_wait(bar(sbase, B_KV_FULL + ks.stage), ks.phase)) { ok = false; break; }
+        if (!wait_fast(bar(sbase, B_KV_FULL + ks.stage), ks.phase)) { ok = false; break; }
         tc_fence_after();
         // S(g): its buffer last held P(g - 2), whose P L was issued before this
         const uint32_t b0 = sdesc_lo(sbase + kOffRing + ks.stage * kStageBytes, 16);
@@ -390,7 +396,7 @@ mla_fwd_kernel(const __grid_constant__ MlaTmaps tm, const LsMlaArgs a,
         have_prev = true;
         ks.advance();
         ++g;
-        if (*abort_flag) { ok = false; break; }
+        if ((g & 15) == 0 && *abort_flag) { ok = false; break; }
       }
       if (ok && have_prev && !issue_pv(prev, prev_stage, g - 1)) ok = false;
       if (!ok) fail();

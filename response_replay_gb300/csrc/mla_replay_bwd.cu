@@ -131,6 +131,12 @@ struct DqTmaps {
 
 __device__ __forceinline__ uint32_t bar(uint32_t sbase, int i) { return sbase + kOffBar + 8u * i; }
 
+// A phase that has already completed returns on a plain test; otherwise the bounded,
+// sleeping wait.
+__device__ __forceinline__ bool wait_fast(uint32_t b, uint32_t parity) {
+  return mbar_try_wait(b, parity) || mbar_wait(b, parity);
+}
+
 __device__ __forceinline__ void tma_prefetch_l2_2d(const void* tmap, int32_t x, int32_t y) {
   asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
                    reinterpret_cast<uint64_t>(tmap)),
@@ -339,7 +345,7 @@ mla_bwd_dq_kernel(const __grid_constant__ DqTmaps tm, const LsMlaBwdArgs a,
       bool have_prev = false, ok = true;
       // dq += dS(pg) L for the tile before; its latent stage is free afterwards.
       auto issue_dq = [&](const DqTile& p, uint32_t pstage, uint32_t pg) -> bool {
-        if (!mbar_wait(bar(sbase, B_DS_FULL + (pg & 1)), (pg >> 1) & 1)) return false;
+        if (!wait_fast(bar(sbase, B_DS_FULL + (pg & 1)), (pg >> 1) & 1)) return false;
         tc_fence_after();
         const uint32_t sb = sbase + kOffRing + pstage * kStageBytes;
         // [0 ; dS] in the buffer's first 16 columns, [dS ; 0] in the next 16
@@ -371,7 +377,7 @@ mla_bwd_dq_kernel(const __grid_constant__ DqTmaps tm, const LsMlaBwdArgs a,
           if (!mbar_wait(bar(sbase, B_QT_FULL), ranges & 1)) { ok = false; break; }
           ++ranges;
         }
-        if (!mbar_wait(bar(sbase, B_KV_FULL + ks.stage), ks.phase)) { ok = false; break; }
+        if (!wait_fast(bar(sbase, B_KV_FULL + ks.stage), ks.phase)) { ok = false; break; }
         tc_fence_after();
         // S|dP(g): its buffer last held dS(g - 2), whose dq MMA was issued before this
         const uint32_t b0 = sdesc_lo(sbase + kOffRing + ks.stage * kStageBytes, 16);
@@ -395,7 +401,7 @@ mla_bwd_dq_kernel(const __grid_constant__ DqTmaps tm, const LsMlaBwdArgs a,
         have_prev = true;
         ks.advance();
         ++g;
-        if (*abort_flag) { ok = false; break; }
+        if ((g & 15) == 0 && *abort_flag) { ok = false; break; }
       }
       if (ok && have_prev && !issue_dq(prev, prev_stage, g - 1)) ok = false;
       if (!ok) fail();
@@ -806,7 +812,7 @@ mla_bwd_dlat_kernel(const __grid_constant__ DlatTmaps tm, const LsMlaBwdArgs a,
       bool have_prev = false, ok = true;
       // d lat += P^T dO + dS^T Q of the iteration before; its row stage is free afterwards.
       auto issue_dlat = [&](const DlatIt& p, uint32_t pstage, uint32_t pg) -> bool {
-        if (!mbar_wait(bar2(sbase, C_PD_FULL + (pg & 1)), (pg >> 1) & 1)) return false;
+        if (!wait_fast(bar2(sbase, C_PD_FULL + (pg & 1)), (pg >> 1) & 1)) return false;
         tc_fence_after();
         const uint32_t sb = sbase + kOffR + pstage * kRStageBytes;
         const uint32_t aP = tmem + kColB + (pg & 1) * kN2;  // P^T: 16 rows as 8 columns
@@ -835,7 +841,7 @@ mla_bwd_dlat_kernel(const __grid_constant__ DlatTmaps tm, const LsMlaBwdArgs a,
           if (!issue_dlat(prev, prev_stage, g - 1)) { ok = false; break; }
           have_prev = false;
         }
-        if (!mbar_wait(bar2(sbase, C_R_FULL + ks.stage), ks.phase)) { ok = false; break; }
+        if (!wait_fast(bar2(sbase, C_R_FULL + ks.stage), ks.phase)) { ok = false; break; }
         tc_fence_after();
         const uint32_t b0 = sdesc_lo(sbase + kOffR + ks.stage * kRStageBytes, 16);
         const uint32_t d = tmem + kColB + (g & 1) * kN2;
@@ -852,7 +858,7 @@ mla_bwd_dlat_kernel(const __grid_constant__ DlatTmaps tm, const LsMlaBwdArgs a,
         have_prev = true;
         ks.advance();
         ++g;
-        if (*abort_flag) { ok = false; break; }
+        if ((g & 15) == 0 && *abort_flag) { ok = false; break; }
       }
       if (ok && have_prev && !issue_dlat(prev, prev_stage, g - 1)) ok = false;
       if (!ok) fail();
