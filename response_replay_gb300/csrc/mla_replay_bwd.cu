@@ -52,7 +52,8 @@
 // [128,160) and [160,192), dq [192,512).
 //
 // mla_bwd_dlat_kernel: the response rows' gradient, key-stationary.  A unit is one
-// 128-row tile of the response's latent rows (M = 128, resident in shared memory) and
+// 128-row tile of the response's latent rows (M = 128, resident: values 0-255 in tensor
+// memory, written by the key-lane warps, 256-575 in shared memory) and
 // one part of the 576 output columns ({0-255, 512-575} or {256-511}, each unit computing
 // S^T and dP^T for itself); it walks the query rows that see the
 // tile (tokens t >= the tile's first row) 16 at a time:
@@ -606,10 +607,11 @@ __global__ void __launch_bounds__(256) mla_bwd_delta(const LsMlaBwdArgs a) {
 constexpr int kKT = 128;                  // response latent rows per unit (M)
 constexpr int kNB = 16;                   // query rows per iteration
 constexpr int kN2 = 2 * kNB;              // stacked: Q rows 0-15, dO rows 16-31
-constexpr int kRStages = 2;
+constexpr int kRStages = 4;
+constexpr int kLtAtoms = 4;               // latent values 0-255 of the tile in tensor memory
 constexpr int kMinIters = 16;             // fewest iterations a CTA of the walk takes
 constexpr uint32_t kLTAtomBytes = kKT * 128;                     // 16 KB
-constexpr uint32_t kLTBytes = kAtoms * kLTAtomBytes;             // 144 KB
+constexpr uint32_t kLTBytes = (kAtoms - kLtAtoms) * kLTAtomBytes;  // 80 KB: values 256-575
 constexpr uint32_t kRAtomBytes = kN2 * 128;                      // 4 KB
 constexpr uint32_t kRStageBytes = kAtoms * kRAtomBytes;          // 36 KB
 constexpr uint32_t kRFill = kAtoms * kNB * 128 + 8 * kNB * 128;  // Q 9 atoms, dO 8 atoms
@@ -618,11 +620,14 @@ constexpr uint32_t kOffR = kLTBytes;
 constexpr uint32_t kOffBar2 = kOffR + kRStages * kRStageBytes;
 constexpr uint32_t kSmemBytes2 = kOffBar2 + 256 + 1024;
 static_assert(kSmemBytes2 <= 232448, "shared memory per CTA");
-constexpr uint32_t kColB = 0, kColAcc = 2 * kN2;  // S^T|dP^T buffers [0,64), d lat [64,384)
+// S^T|dP^T buffers [0,64), d lat [64,384), latent values 0-255 as bf16 pairs [384,512)
+constexpr uint32_t kColB = 0, kColAcc = 2 * kN2, kColL = kColAcc + kPartCols;
+static_assert(kColL + kLtAtoms * 32 == 512, "tensor memory columns");
 
 enum {
   C_L_FULL = 0,
   C_L_EMPTY,
+  C_LT_FULL,                    // the key-lane warps wrote the tile's values 0-255
   C_R_FULL,                     // 2 row stages
   C_R_EMPTY = C_R_FULL + kRStages,
   C_S_FULL = C_R_EMPTY + kRStages,  // 2: S^T|dP^T of iteration g in buffer g & 1
@@ -737,6 +742,7 @@ mla_bwd_dlat_kernel(const __grid_constant__ DlatTmaps tm, const LsMlaBwdArgs a,
   if (tid == 0) {
     mbar_init(bar2(sbase, C_L_FULL), 1);
     mbar_init(bar2(sbase, C_L_EMPTY), 1);
+    mbar_init(bar2(sbase, C_LT_FULL), kKT);
     for (int i = 0; i < kRStages; ++i) {
       mbar_init(bar2(sbase, C_R_FULL + i), 1);
       mbar_init(bar2(sbase, C_R_EMPTY + i), 1);
@@ -778,8 +784,9 @@ mla_bwd_dlat_kernel(const __grid_constant__ DlatTmaps tm, const LsMlaBwdArgs a,
           if (units > 0 && !mbar_wait(bar2(sbase, C_L_EMPTY), (units - 1) & 1)) { fail(); break; }
           const uint32_t lb = bar2(sbase, C_L_FULL);
           mbar_expect_tx(lb, kLTBytes);
-          for (int at = 0; at < kAtoms; ++at)
-            tma_load_2d(sbase + kOffL + at * kLTAtomBytes, &tm.lr, at * 64, (it.u >> 1) * kKT, lb);
+          for (int at = kLtAtoms; at < kAtoms; ++at)
+            tma_load_2d(sbase + kOffL + (at - kLtAtoms) * kLTAtomBytes, &tm.lr, at * 64,
+                        (it.u >> 1) * kKT, lb);
           ++units;
         }
         const uint32_t st = ring % kRStages;
@@ -834,6 +841,7 @@ mla_bwd_dlat_kernel(const __grid_constant__ DlatTmaps tm, const LsMlaBwdArgs a,
           if (have_prev && !issue_dlat(prev, prev_stage, g - 1)) { ok = false; break; }
           have_prev = false;
           if (!mbar_wait(bar2(sbase, C_L_FULL), units & 1)) { ok = false; break; }
+          if (!mbar_wait(bar2(sbase, C_LT_FULL), units & 1)) { ok = false; break; }
           ++units;
         } else if (have_prev) {
           // the product of the iteration before goes first: it frees the row stage that
@@ -846,10 +854,15 @@ mla_bwd_dlat_kernel(const __grid_constant__ DlatTmaps tm, const LsMlaBwdArgs a,
         const uint32_t b0 = sdesc_lo(sbase + kOffR + ks.stage * kRStageBytes, 16);
         const uint32_t d = tmem + kColB + (g & 1) * kN2;
 #pragma unroll
-        for (int kk = 0; kk < 4 * kAtoms; ++kk) {
-          const uint32_t oa = ((kk >> 2) * kLTAtomBytes + (kk & 3) * 32) >> 4;
+        for (int kk = 0; kk < 4 * kLtAtoms; ++kk) {  // values 0-255 from tensor memory
           const uint32_t ob = ((kk >> 2) * kRAtomBytes + (kk & 3) * 32) >> 4;
-          mma_ss_lo(d, l_lo + oa, b0 + ob, idS, kk > 0);
+          mma_ts_lo(d, tmem + kColL + kk * 8, b0 + ob, idS, kk > 0);
+        }
+#pragma unroll
+        for (int kk = 4 * kLtAtoms; kk < 4 * kAtoms; ++kk) {  // values 256-575 from shared
+          const uint32_t oa = (((kk >> 2) - kLtAtoms) * kLTAtomBytes + (kk & 3) * 32) >> 4;
+          const uint32_t ob = ((kk >> 2) * kRAtomBytes + (kk & 3) * 32) >> 4;
+          mma_ss_lo(d, l_lo + oa, b0 + ob, idS, 1u);
         }
         mma_commit(bar2(sbase, C_S_FULL + (g & 1)));
         if (it.last) mma_commit(bar2(sbase, C_L_EMPTY));  // the latent tile is read by S only
@@ -873,9 +886,35 @@ mla_bwd_dlat_kernel(const __grid_constant__ DlatTmaps tm, const LsMlaBwdArgs a,
     const int64_t nrows = (int64_t)a.R * a.H;
     DlatCursor cur(gm, blockIdx.x);
     DlatIt it;
-    uint32_t g = 0, oc = 0;
+    uint32_t g = 0, oc = 0, units = 0;
     while (cur.next(&it)) {
       const int32_t j = (it.u >> 1) * kKT + k;  // response row
+      if (it.first) {
+        // values 0-255 of this lane's latent row into tensor memory, once the old unit's
+        // score MMAs have read theirs; rows past R are zeros
+        if (units > 0 && !mbar_wait(bar2(sbase, C_L_EMPTY), (units - 1) & 1)) { fail(); break; }
+        tc_fence_after();
+        const bool in = j < a.R;
+        const uint4* src = reinterpret_cast<const uint4*>(
+            static_cast<const __nv_bfloat16*>(a.lat_resp) + (int64_t)(in ? j : 0) * kD);
+#pragma unroll 1
+        for (int c0 = 0; c0 < kLtAtoms * 32; c0 += 32) {
+          uint32_t v[32];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const uint4 w = in ? __ldg(src + c0 / 4 + i) : make_uint4(0, 0, 0, 0);
+            v[4 * i] = w.x;
+            v[4 * i + 1] = w.y;
+            v[4 * i + 2] = w.z;
+            v[4 * i + 3] = w.w;
+          }
+          tmem_st32(lane_base + kColL + c0, v);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(bar2(sbase, C_LT_FULL));
+        ++units;
+      }
       if (!mbar_wait(bar2(sbase, C_S_FULL + (g & 1)), (g >> 1) & 1)) { fail(); break; }
       tc_fence_after();
       const uint32_t b_col = lane_base + kColB + (g & 1) * kN2;
