@@ -915,6 +915,16 @@ mla_bwd_dlat_kernel(const __grid_constant__ DlatTmaps tm, const LsMlaBwdArgs a,
         mbar_arrive(bar2(sbase, C_LT_FULL));
         ++units;
       }
+      // the block's 16 lse and D values (the same for every thread), loaded before the
+      // wait so their latency hides behind it
+      float lse2[kNB], dd[kNB];
+#pragma unroll
+      for (int n = 0; n < kNB; ++n) {
+        const int64_t row = (int64_t)it.rb * kNB + n;
+        const bool in = row < nrows;
+        lse2[n] = in ? __ldg(a.lse + row) * kLog2e : 0.f;
+        dd[n] = in ? __ldg(a.delta + row) : 0.f;
+      }
       if (!mbar_wait(bar2(sbase, C_S_FULL + (g & 1)), (g >> 1) & 1)) { fail(); break; }
       tc_fence_after();
       const uint32_t b_col = lane_base + kColB + (g & 1) * kN2;
@@ -932,8 +942,8 @@ mla_bwd_dlat_kernel(const __grid_constant__ DlatTmaps tm, const LsMlaBwdArgs a,
           const bool vis = row < nrows && j < a.R && (int64_t)j * a.H <= row;  // j <= t
           float p = 0.f, ds = 0.f;
           if (vis) {
-            p = fast_exp2(__uint_as_float(x[n + e]) * c - __ldg(a.lse + row) * kLog2e);
-            ds = p * (__uint_as_float(x[kNB + n + e]) - __ldg(a.delta + row)) * a.scale;
+            p = fast_exp2(__uint_as_float(x[n + e]) * c - lse2[n + e]);
+            ds = p * (__uint_as_float(x[kNB + n + e]) - dd[n + e]) * a.scale;
           }
           pv[e] = p;
           dv[e] = ds;
