@@ -440,6 +440,17 @@ mla_fwd_kernel(const __grid_constant__ MlaTmaps tm, const LsMlaArgs a,
         mbar_arrive(bar(sbase, B_QT_FULL));
         ++ranges;
       }
+      // the row's token and the tile's visible keys [0, lim), worked out before the wait
+      // for the scores (the wait is on the tile's critical path)
+      const int64_t grow = (int64_t)(r.u >> 1) * kRows + row;  // (t, h) row, token-major
+      const int32_t tq = (int32_t)(grow / a.H);
+      int32_t lim = kKeys;
+      if (r.resp) {
+        const int32_t lr = tq + 1 - r.key0;
+        lim = lr < kKeys ? lr : kKeys;
+      } else if (r.key0 + kKeys > a.P) {
+        lim = (int32_t)(a.P - r.key0);
+      }
       if (!mbar_wait(bar(sbase, B_S_FULL + (g & 1)), (g >> 1) & 1)) { fail(); break; }
       tc_fence_after();
       const uint32_t s_col = lane_base + kColS + (g & 1) * kKeys;
@@ -449,15 +460,6 @@ mla_fwd_kernel(const __grid_constant__ MlaTmaps tm, const LsMlaArgs a,
       tmem_wait_ld();
       reg_fence32(sr);
       reg_fence32(sr + 32);
-      const int64_t grow = (int64_t)(r.u >> 1) * kRows + row;  // (t, h) row, token-major
-      const int32_t tq = (int32_t)(grow / a.H);
-      int32_t lim = kKeys;  // visible keys [0, lim) of the tile
-      if (r.resp) {
-        const int32_t lr = tq + 1 - r.key0;
-        lim = lr < kKeys ? lr : kKeys;
-      } else if (r.key0 + kKeys > a.P) {
-        lim = (int32_t)(a.P - r.key0);
-      }
       if (lim < kKeys) {
 #pragma unroll
         for (int j = 0; j < kKeys; ++j)
