@@ -454,6 +454,18 @@ mla_bwd_dq_kernel(const __grid_constant__ DqTmaps tm, const LsMlaBwdArgs a,
         mbar_arrive(bar(sbase, B_QT_FULL));
         ++ranges;
       }
+      // the tile's visible keys [0, lim) for this row, worked out before the wait
+      int32_t lim = kKeys;
+      if (is_s) {
+        const int32_t tq = (int32_t)(grow / a.H);
+        if (r.resp) {
+          const int32_t lr = tq + 1 - r.key0;
+          lim = lr < kKeys ? lr : kKeys;
+        } else if (r.key0 + kKeys > a.P) {
+          lim = (int32_t)(a.P - r.key0);
+        }
+        if (!valid) lim = 0;
+      }
       if (!mbar_wait(bar(sbase, B_S_FULL + (g & 1)), (g >> 1) & 1)) { fail(); break; }
       tc_fence_after();
       const uint32_t s_col = lane_base + kColS + (g & 1) * kKeys;
@@ -464,15 +476,6 @@ mla_bwd_dq_kernel(const __grid_constant__ DqTmaps tm, const LsMlaBwdArgs a,
       // lanes 0-63 turn S into P; lanes 64-127 keep dP as it is
       float mine[kKeys];
       if (is_s) {
-        const int32_t tq = (int32_t)(grow / a.H);
-        int32_t lim = kKeys;  // visible keys [0, lim) of the tile
-        if (r.resp) {
-          const int32_t lr = tq + 1 - r.key0;
-          lim = lr < kKeys ? lr : kKeys;
-        } else if (r.key0 + kKeys > a.P) {
-          lim = (int32_t)(a.P - r.key0);
-        }
-        if (!valid) lim = 0;
 #pragma unroll
         for (int j = 0; j < kKeys; ++j)
           mine[j] = j < lim ? fast_exp2(__uint_as_float(x[j]) * c - lse2) : 0.f;
