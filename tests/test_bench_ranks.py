@@ -79,3 +79,20 @@ def test_reference_arm_prints_the_contract_line():
     assert d["cpu_baseline"]["value"] == d["value"]
     assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}
+
+
+def test_latent_flop_counts_match_a_pair_count():
+    """The latent sweep's algorithmic FLOPs are the visible (query row, key) pairs times
+    the per-pair products: 576 + 512 MACs forward; 576 + 512 + 576 backward plus
+    512 + 576 for each pair with a response key (the response rows' gradient)."""
+    sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    import bench
+    for P, R, H in [(0, 1, 1), (37, 5, 3), (1000, 64, 64)]:
+        pairs = sum((P + t + 1) * H for t in range(R))
+        resp = sum((t + 1) * H for t in range(R))
+        fwd, fwd_exe = bench.mla_flops(P, R, H)
+        bwd, bwd_exe = bench.mla_bwd_flops(P, R, H)
+        assert fwd == pytest.approx(pairs * 2 * (576 + 512), rel=1e-12)
+        assert bwd == pytest.approx(pairs * 2 * (576 + 512 + 576) + resp * 2 * (512 + 576),
+                                    rel=1e-12)
+        assert fwd_exe >= fwd and bwd_exe >= bwd
